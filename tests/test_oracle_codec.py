@@ -1,0 +1,310 @@
+"""Pins of the oracle's codec (key/value records, page layout, dequant, decode).
+
+What fixes each expected value:
+* key MSE: the Lloyd-Max distortion of N(0,1) at b bits (J. Max 1960, Table I),
+  since rotated unit-vector coordinates scaled by sqrt(d) are ~N(0,1)
+  (brightcoding blog, "What is TurboQuant-GPU?": rotation makes coordinates
+  approximately Gaussian, where Lloyd-Max is optimal);
+* QJL: the 1-bit sign sketch of the residual gives an unbiased inner-product
+  estimate (0xsero/turboquant, "Operational Constraints": near-unbiased
+  approximate inner products) -- checked by Monte Carlo over independent S;
+* values: per-group min/max affine quantisation (0xsero/turboquant "Value
+  Compression"; tiny-turboquant "Measured quality": one scale/zero pair per
+  group) -- numpy's own float16 rounding and exact rational arithmetic;
+* compression ratios: the figures printed on the brightcoding blog, rebuilt
+  from the oracle's record sizes (tests/golden/compression_ratios.json);
+* decode: dense softmax attention over the dequantised cache (numpy), the
+  rotated-space identity <Pi q, Pi k> = <q, k>, and closed-form special cases.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+MAX_MSE = {2: 0.1175, 3: 0.03454, 4: 0.009497}
+
+
+def _bf16(x):
+    """float64 array -> bf16 bit patterns (round to nearest even via float32 of exact bf16 grid)."""
+    return O.bf16_from_double(np.asarray(x, dtype=np.float64))
+
+
+# --------------------------------------------------------------------------- #
+# Keys                                                                           #
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_key_codebook_distortion_matches_lloyd_max(bits):
+    d = 128
+    ora = O.Oracle(d, bits, 4, 32, seed=1)
+    rng = np.random.default_rng(bits)
+    k = _bf16(rng.standard_normal((4000, d)))
+    rec = ora.compress_rows(k=k)
+    c = ora.params()["centroids"]
+    codes = np.stack([O.unpack(r, d, bits) for r in rec["k_code"]])
+    mse = np.mean((rec["z"] - c[codes]) ** 2)
+    assert abs(mse - MAX_MSE[bits]) < 0.05 * MAX_MSE[bits]
+    # the stored norm is the bf16 rounding of ||k||
+    kd = O.bf16_to_double(k)
+    assert np.array_equal(rec["k_norm"], _bf16(np.linalg.norm(kd, axis=1)))
+
+
+def test_key_zero_vector_gives_zero_record():
+    ora = O.Oracle(128, 3, 4, 32, seed=0)
+    rec = ora.compress_rows(k=np.zeros((2, 128), np.uint16))
+    for f in ("k_code", "k_sign", "k_norm", "k_gamma"):
+        assert not rec[f].any()
+
+
+def test_qjl_gamma_is_residual_norm():
+    d = 128
+    ora = O.Oracle(d, 2, 4, 32, seed=2)
+    rng = np.random.default_rng(5)
+    k = _bf16(rng.standard_normal((64, d)))
+    rec = ora.compress_rows(k=k)
+    c = ora.params()["centroids"]
+    codes = np.stack([O.unpack(r, d, 2) for r in rec["k_code"]])
+    r = (rec["z"] - c[codes]) / math.sqrt(d)
+    assert np.allclose(rec["gamma"], np.linalg.norm(r, axis=1), rtol=1e-12)
+    assert np.array_equal(rec["k_gamma"], _bf16(rec["gamma"]))
+
+
+@pytest.mark.parametrize("bits", [2, 3])
+def test_qjl_estimator_unbiased_monte_carlo(bits):
+    """Fixed Pi, q, k; independent S: mean of <q, K~> is <q, k> (bias <= 2^-8 rel)."""
+    d, P, n_mc = 32, 16, 4000
+    rng = np.random.default_rng(100 + bits)
+    k_d = O.bf16_to_double(_bf16(rng.standard_normal(d)))
+    q = k_d + 0.5 * rng.standard_normal(d)  # aligned with k so the residual term matters
+    truth = float(q @ k_d)
+    kk = _bf16(k_d).reshape(1, 1, d)
+    vv = np.zeros((1, 1, d), np.uint16)
+    slot = np.array([0], np.int64)
+    est = np.empty(n_mc)
+    mse_only = None
+    for s in range(n_mc):
+        ora = O.Oracle(d, bits, 4, 32, seed=0, qjl_seed=1000 + s)
+        kc, vc = ora.compress_kv(kk, vv, slot, P, 1)
+        kt, _ = ora.dequant_slots(kc, vc, P, 1, slot)
+        est[s] = q @ kt[0, 0]
+        if mse_only is None:  # codebook-only reconstruction n16 * Pi^T c[code]/sqrt(d)
+            prm = ora.params()
+            rec = ora.compress_rows(k=kk[0])
+            codes = O.unpack(rec["k_code"][0], d, bits)
+            n16 = O.bf16_to_double(rec["k_norm"][0])
+            mse_only = float(q @ (n16 * prm["Pi"].T @ (prm["centroids"][codes] / math.sqrt(d))))
+    se = est.std(ddof=1) / math.sqrt(n_mc)
+    assert abs(est.mean() - truth) < 4 * se + 2.0 ** -8 * abs(truth)
+    # the residual correction is what removes the bias: without it the estimate is off
+    assert abs(mse_only - truth) > 10 * se
+
+
+# --------------------------------------------------------------------------- #
+# Values                                                                         #
+# --------------------------------------------------------------------------- #
+
+def _groups(rng, n, g):
+    x = rng.standard_normal((n, g)) * np.exp(rng.standard_normal((n, 1)))
+    x[0] = 1.25                     # constant group
+    x[1] = 0.0                      # all zeros
+    x[2, : g // 2] = -3.0           # two-valued group
+    x[2, g // 2:] = 5.5
+    return _bf16(x)
+
+
+@pytest.mark.parametrize("vbits", [2, 3, 4])
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_value_group_quantisation_exact(vbits, g):
+    d = 128
+    ora = O.Oracle(d, 4, vbits, g, seed=0)
+    rng = np.random.default_rng(vbits * 1000 + g)
+    v = _groups(rng, 3 * (d // g) * 20, g).reshape(-1, d)
+    rec = ora.compress_rows(v=v)
+    L = (1 << vbits) - 1
+    xs = O.bf16_to_double(v).reshape(len(v), d // g, g)
+    codes = np.stack([O.unpack(r, d, vbits) for r in rec["v_code"]]).reshape(len(v), d // g, g)
+    meta = rec["v_meta"].reshape(len(v), d // g, 2)
+    mn, mx = xs.min(axis=2), xs.max(axis=2)
+    # scale / zero: fp16 round-to-nearest-even of (max-min)/L and of min (numpy's rounding)
+    assert np.array_equal(meta[..., 0], ((mx - mn) / L).astype(np.float16).view(np.uint16))
+    assert np.array_equal(meta[..., 1], mn.astype(np.float16).view(np.uint16))
+    s = meta[..., 0].view(np.float16).astype(np.float64)
+    z = meta[..., 1].view(np.float16).astype(np.float64)
+    assert codes.max() <= L
+    # exact round-half-up of (x - z)/s, checked in rational arithmetic on a sample
+    for i in range(0, xs.shape[0], 7):
+        for gi in range(xs.shape[1]):
+            S, Z = Fraction(s[i, gi]), Fraction(z[i, gi])
+            for j in range(0, g, 5):
+                X = Fraction(xs[i, gi, j])
+                want = 0 if S == 0 else min(max(math.floor((X - Z) / S + Fraction(1, 2)), 0), L)
+                assert codes[i, gi, j] == want
+    # reconstruction within half a step inside the representable range
+    rec_x = codes * s[..., None] + z[..., None]
+    inside = (xs >= z[..., None] - s[..., None] / 2) & (xs <= z[..., None] + (L + 0.5) * s[..., None])
+    assert np.all(np.abs(rec_x - xs)[inside] <= s[..., None].repeat(g, 2)[inside] / 2 + 1e-12)
+    # a constant group reconstructs exactly
+    const = (mx == mn)
+    assert np.all(np.abs(rec_x - xs)[np.repeat(const[..., None], g, 2)] == 0)
+
+
+# --------------------------------------------------------------------------- #
+# Page layout                                                                    #
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("kb,vb,g,d,P", [(3, 4, 32, 128, 16), (4, 4, 64, 256, 32), (2, 2, 32, 128, 16)])
+def test_page_layout_offsets(kb, vb, g, d, P):
+    ora = O.Oracle(d, kb, vb, g, seed=3)
+    geo = ora.geometry(P)
+    qjl = kb <= 3
+    assert geo["k_page"] == P * (d * kb // 8 + (d // 8 + 2 if qjl else 0) + 2)
+    assert geo["v_page"] == P * (d * vb // 8 + 4 * d // g)
+    for f in ("k_code", "k_sign", "v_code", "v_meta"):
+        assert (P * geo[f]) % 16 == 0  # every sub-array stays 16-byte aligned
+    Hkv, nb, T = 2, 3, 5
+    rng = np.random.default_rng(9)
+    k = _bf16(rng.standard_normal((T, Hkv, d)))
+    v = _bf16(rng.standard_normal((T, Hkv, d)))
+    slots = np.array([P + 3, 2 * P + P - 1, -1, 0, 5], np.int64)
+    kc, vc = ora.compress_kv(k, v, slots, P, nb)
+    rec = ora.compress_rows(k=k.reshape(-1, d), v=v.reshape(-1, d))
+    kc2 = np.zeros_like(kc)
+    vc2 = np.zeros_like(vc)
+    for t, s in enumerate(slots):
+        if s < 0:
+            continue
+        blk, off = divmod(int(s), P)
+        for h in range(Hkv):
+            i = t * Hkv + h
+            kr = (blk * Hkv + h) * geo["k_page"]
+            vr = (blk * Hkv + h) * geo["v_page"]
+            kc2[kr + off * geo["k_code"]: kr + (off + 1) * geo["k_code"]] = rec["k_code"][i]
+            base = kr + P * geo["k_code"]
+            if qjl:
+                kc2[base + off * geo["k_sign"]: base + (off + 1) * geo["k_sign"]] = rec["k_sign"][i]
+            base += P * geo["k_sign"]
+            kc2[base + 2 * off: base + 2 * off + 2] = np.array([rec["k_norm"][i]], np.uint16).view(np.uint8)
+            if qjl:
+                base += 2 * P
+                kc2[base + 2 * off: base + 2 * off + 2] = np.array([rec["k_gamma"][i]], np.uint16).view(np.uint8)
+            vc2[vr + off * geo["v_code"]: vr + (off + 1) * geo["v_code"]] = rec["v_code"][i]
+            base = vr + P * geo["v_code"]
+            vc2[base + off * geo["v_meta"]: base + (off + 1) * geo["v_meta"]] = rec["v_meta"][i].view(np.uint8)
+    assert np.array_equal(kc, kc2)
+    assert np.array_equal(vc, vc2)
+
+
+def test_compression_ratios_from_record_sizes():
+    gold = json.load(open(os.path.join(GOLDEN, "compression_ratios.json")))
+    d = 128
+    fp16_bytes = 2 * 2 * d  # one fp16 key plus one fp16 value
+    # 2-bit key codebook + QJL: key record bytes from the oracle's geometry
+    k_rec = O.Oracle(d, 2, 3, 32, seed=0).geometry(16)["k_page"] // 16
+    assert k_rec == 32 + 16 + 2 + 2
+    # 3-bit MSE value: 3-bit codes (oracle geometry) plus one 16-bit norm
+    v_rec = O.Oracle(d, 4, 3, 128, seed=0).geometry(16)["v_code"] + 2
+    ratio = fp16_bytes / (k_rec + v_rec)
+    assert round(ratio, 2) == gold["turboquant_2bit_k_qjl_3bit_v_vs_fp16"]["value"]
+    assert round(16 / (4 + 8 / 32), 2) == gold["mxfp4_vs_fp16"]["value"]
+    assert round(16 / (4 + 8 / 16), 2) == gold["nvfp4_vs_fp16"]["value"]
+
+
+# --------------------------------------------------------------------------- #
+# Decode                                                                         #
+# --------------------------------------------------------------------------- #
+
+def _tiny_case(d=128, kb=3, vb=4, g=32, P=16, B=3, Hkv=2, G=2, lens=(37, 16, 1), seed=4):
+    ora = O.Oracle(d, kb, vb, g, seed=seed)
+    rng = np.random.default_rng(seed)
+    lens = np.array(lens, np.int32)
+    npg = (lens + P - 1) // P
+    nb = int(npg.sum()) + 2
+    perm = rng.permutation(nb).astype(np.int32)
+    maxb = int(npg.max())
+    bt = np.full((B, maxb), -1, np.int32)
+    st = 0
+    for b in range(B):
+        bt[b, : npg[b]] = perm[st: st + npg[b]]
+        st += npg[b]
+    T = int(lens.sum())
+    k = _bf16(rng.standard_normal((T, Hkv, d)) * 1.5)
+    v = _bf16(rng.standard_normal((T, Hkv, d)))
+    slots = np.concatenate([bt[b, np.arange(lens[b]) // P].astype(np.int64) * P + np.arange(lens[b]) % P
+                            for b in range(B)])
+    kc, vc = ora.compress_kv(k, v, slots, P, nb)
+    q = _bf16(rng.standard_normal((B, Hkv * G, d)))
+    return ora, dict(q=q, kc=kc, vc=vc, bt=bt, lens=lens, P=P, Hkv=Hkv, slots=slots, d=d)
+
+
+def _numpy_attention(ora, c, sm_scale):
+    """Dense softmax attention over the oracle's dequantised K~, V~ (numpy)."""
+    q = O.bf16_to_double(c["q"])
+    B, Hq, d = q.shape
+    G = Hq // c["Hkv"]
+    out = np.zeros((B, Hq, d))
+    for b in range(B):
+        L = int(c["lens"][b])
+        if L == 0:
+            continue
+        pos = np.arange(L)
+        slots = c["bt"][b, pos // c["P"]].astype(np.int64) * c["P"] + pos % c["P"]
+        K, V = ora.dequant_slots(c["kc"], c["vc"], c["P"], c["Hkv"], slots)
+        for h in range(Hq):
+            s = sm_scale * K[:, h // G] @ q[b, h]
+            p = np.exp(s - s.max())
+            out[b, h] = (p / p.sum()) @ V[:, h // G]
+    return out
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(d=256, kb=4, vb=4, g=64, P=32, lens=(70, 33, 2)),
+                                dict(kb=2, vb=2, g=32, G=4, lens=(5, 64, 17))])
+def test_decode_matches_dense_attention(kw):
+    ora, c = _tiny_case(**kw)
+    sm = c["d"] ** -0.5
+    ref = _numpy_attention(ora, c, sm)
+    for mode in (0, 1):
+        out = ora.decode(c["q"], c["kc"], c["vc"], c["bt"], c["lens"], c["Hkv"], c["P"], sm, mode=mode)
+        assert np.abs(out - ref).max() < 1e-10 * max(1.0, np.abs(ref).max())
+
+
+def test_decode_special_cases():
+    ora, c = _tiny_case(lens=(1, 0, 16))
+    sm = c["d"] ** -0.5
+    out = ora.decode(c["q"], c["kc"], c["vc"], c["bt"], c["lens"], c["Hkv"], c["P"], sm)
+    # seq_len 1: the output is the single dequantised value
+    _, V = ora.dequant_slots(c["kc"], c["vc"], c["P"], c["Hkv"], [int(c["bt"][0, 0]) * c["P"]])
+    for h in range(4):
+        assert np.array_equal(out[0, h], V[0, h // 2])
+    # seq_len 0: zeros
+    assert not out[1].any()
+    # zero query: uniform weights, the mean of the dequantised values
+    q0 = c["q"].copy()
+    q0[2] = 0
+    out0 = ora.decode(q0, c["kc"], c["vc"], c["bt"], c["lens"], c["Hkv"], c["P"], sm)
+    slots = c["bt"][2, 0].astype(np.int64) * c["P"] + np.arange(16)
+    _, V = ora.dequant_slots(c["kc"], c["vc"], c["P"], c["Hkv"], slots)
+    for h in range(4):
+        assert np.allclose(out0[2, h], V[:, h // 2].mean(axis=0), atol=1e-12)
+
+
+def test_decode_identical_keys_average_values():
+    d, P, Hkv = 128, 16, 1
+    ora = O.Oracle(d, 3, 4, 32, seed=8)
+    rng = np.random.default_rng(8)
+    key = _bf16(rng.standard_normal(d))
+    k = np.tile(key, (20, 1)).reshape(20, 1, d)
+    v = _bf16(rng.standard_normal((20, 1, d)))
+    bt = np.array([[1, 0]], np.int32)
+    slots = np.concatenate([np.arange(16) + 16, np.arange(4)]).astype(np.int64)
+    kc, vc = ora.compress_kv(k, v, slots, P, 2)
+    q = _bf16(rng.standard_normal((1, 2, d)) * 3)
+    out = ora.decode(q, kc, vc, bt, np.array([20], np.int32), Hkv, P, d ** -0.5)
+    _, V = ora.dequant_slots(kc, vc, P, Hkv, slots)
+    assert np.allclose(out[0, 0], V[:, 0].mean(axis=0), atol=1e-12)
+    assert np.allclose(out[0, 1], V[:, 0].mean(axis=0), atol=1e-12)
