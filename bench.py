@@ -1,0 +1,478 @@
+#!/usr/bin/env python3
+"""Benchmark: compress the full context, then decode one token, for every layer of
+the long-context mixed-bit workload (8 layers; per-layer (k_bits, v_bits) drawn
+from {(4,4),(4,3),(3,3),(3,2),(2,2)}; batch 4, 64 query / 8 KV heads, d=128,
+131,072 tokens per sequence, page size 16, V group 32) on synthetic data.
+
+One step = every hot-path call over one batch: for each layer, tq_compress_kv of
+all 524,288 tokens x 8 KV heads, then tq_decode_attention of one query token per
+sequence (3 launches).  Inputs (17 GB of bf16 K/V) exceed L2, and the order is
+compress all layers then decode all layers, so each decode reads pages last
+touched several GB of traffic earlier.
+
+The printed value is whole-step algorithmic throughput in GB/s: bytes that must
+move (K/V read, slots read, records written; records, queries, block tables
+read and outputs written for decode) over the device time of a step.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
+For N > 1 launch with torch.distributed.run; every rank runs its own copy of the
+workload (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rotated_codebook_kv_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode attn compressed-KV GB/s & % HBM roofline; compress Mtoken-heads/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------- #
+# Algorithmic bytes                                                             #
+# --------------------------------------------------------------------------- #
+
+def record_bytes(d, kb, vb, g):
+    qjl = kb <= 3
+    k = d * kb // 8 + (d // 8 + 2 if qjl else 0) + 2
+    v = d * vb // 8 + 4 * (d // g)
+    return k, v
+
+
+def compress_bytes(w, T):
+    """Read K and V rows and the slot, write both records, per token-head."""
+    k, v = record_bytes(w.head_dim, w.k_bits, w.v_bits, w.group)
+    rows = T * w.num_kv_heads
+    return rows * (4 * w.head_dim + k + v) + T * 8
+
+
+def decode_bytes(w, seq_lens, max_blocks):
+    k, v = record_bytes(w.head_dim, w.k_bits, w.v_bits, w.group)
+    toks = int(sum(seq_lens))
+    pages = sum((int(s) + w.page_size - 1) // w.page_size for s in seq_lens)
+    qo = 2 * w.batch * w.num_q_heads * w.head_dim * 2
+    return toks * w.num_kv_heads * (k + v) + qo + pages * 4 + w.batch * 4
+
+
+# --------------------------------------------------------------------------- #
+# Environment helpers                                                           #
+# --------------------------------------------------------------------------- #
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        for key in ("hbm_gbs", "hbm_gbs_burst", "hbm_copy_gbs"):
+            if key in peaks and isinstance(peaks[key], (int, float)):
+                return float(peaks[key]), "measured"
+            if key in peaks and isinstance(peaks[key], dict) and "value" in peaks[key]:
+                return float(peaks[key]["value"]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def committed_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            data = json.load(f)
+        ent = data[kernel]
+        src = open(os.path.join(ROOT, ent["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest() != ent["source_sha256"]:
+            return None
+        return ent
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks / throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- #
+# GPU arm                                                                        #
+# --------------------------------------------------------------------------- #
+
+class Layer:
+    def __init__(self, w, layer, device, pinned_host=False):
+        from rotated_codebook_kv_gb300 import Codec
+        self.w = lw = w.for_layer(layer)
+        self.codec = Codec(lw.head_dim, lw.k_bits, lw.v_bits, lw.group, lw.codec_seed(layer))
+        b = W.generate(lw, layer=layer, device=device)
+        self.b = b
+        self.kc, self.vc = self.codec.alloc_cache(b.num_blocks, lw.num_kv_heads, lw.page_size, device=device)
+        self.maxb = b.block_table.shape[1]
+        self.splits = self.codec.decode_splits(lw.batch, lw.num_kv_heads, self.maxb, lw.page_size)
+        self.ws = self.codec.workspace(lw.batch, lw.num_q_heads, self.splits, device=device)
+        self.out = torch.empty_like(b.q)
+        self.T = b.num_tokens
+        self.seq_lens = b.seq_lens.cpu().tolist()
+        self.c_bytes = compress_bytes(lw, self.T)
+        self.d_bytes = decode_bytes(lw, self.seq_lens, self.maxb)
+        self.host = None
+        if pinned_host:
+            self.host = {n: getattr(b, n).cpu().pin_memory() for n in
+                         ("k", "v", "slot_mapping", "q", "block_table", "seq_lens")}
+            self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+
+    def compress(self, stream):
+        lw, b = self.w, self.b
+        self.codec.compress_kv(b.k, b.v, b.slot_mapping, self.kc, self.vc, lw.page_size, b.num_blocks, stream=stream)
+
+    def decode(self, stream):
+        lw, b = self.w, self.b
+        self.codec.decode_attention(b.q, self.kc, self.vc, b.block_table, b.seq_lens, lw.num_kv_heads, lw.page_size,
+                                    b.num_blocks, b.sm_scale, splits=self.splits, workspace=self.ws, out=self.out,
+                                    stream=stream)
+
+    def h2d(self, stream):
+        with torch.cuda.stream(stream):
+            for n, t in self.host.items():
+                getattr(self.b, n).copy_(t, non_blocking=True)
+        return sum(t.numel() * t.element_size() for t in self.host.values())
+
+    def d2h(self, stream):
+        with torch.cuda.stream(stream):
+            self.out_host.copy_(self.out, non_blocking=True)
+        return self.out.numel() * self.out.element_size()
+
+
+def run_gpu(args, rank, world, local_rank):
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = W.long_context_mixed(seed=rank)
+    layers = [Layer(w, l, dev, pinned_host=not args.no_e2e) for l in range(w.layers)]
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def events(n):
+        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+
+    c_ev = [events(len(layers)) for _ in range(args.steps)]
+    d_ev = [events(len(layers)) for _ in range(args.steps)]
+
+    def step(s=None):
+        for i, L in enumerate(layers):
+            if s is not None:
+                c_ev[s][i][0].record(stream)
+            L.compress(stream)
+            if s is not None:
+                c_ev[s][i][1].record(stream)
+        for i, L in enumerate(layers):
+            if s is not None:
+                d_ev[s][i][0].record(stream)
+            L.decode(stream)
+            if s is not None:
+                d_ev[s][i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for L in layers:
+        if L.codec.get_status(stream) != 0:
+            raise RuntimeError("device status bits set during warm-up")
+
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for s_ in range(args.steps):
+            step(s_)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    c_ms = [sum(c_ev[s_][i][0].elapsed_time(c_ev[s_][i][1]) for s_ in range(args.steps)) for i in range(len(layers))]
+    d_ms = [sum(d_ev[s_][i][0].elapsed_time(d_ev[s_][i][1]) for s_ in range(args.steps)) for i in range(len(layers))]
+    elapsed = t0.elapsed_time(t1) / args.steps
+    elapsed = max_over_ranks(elapsed, world)
+    clk = clocks.summary()
+
+    step_bytes = sum(L.c_bytes + L.d_bytes for L in layers)
+    value = world * step_bytes / (elapsed * 1e-3) / 1e9
+    c_bytes = sum(L.c_bytes for L in layers)
+    d_bytes = sum(L.d_bytes for L in layers)
+    c_time = sum(c_ms) / args.steps * 1e-3
+    d_time = sum(d_ms) / args.steps * 1e-3
+    rows = sum(L.T * L.w.num_kv_heads for L in layers)
+    peak, peak_kind = measured_peak()
+    c_gbs = c_bytes / c_time / 1e9
+    d_gbs = d_bytes / d_time / 1e9
+    traffic = committed_traffic("compress_kernel")
+    launches = args.steps * len(layers) * 4
+
+    # ---- end to end: host buffers, copies inside the timed region ------------
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(1):
+            for L in layers:
+                L.h2d(stream)
+                L.compress(stream)
+            for L in layers:
+                L.decode(stream)
+                L.d2h(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h2d = d2h = 0
+        e0.record(stream)
+        for _ in range(args.steps):
+            h2d = d2h = 0
+            for L in layers:
+                h2d += L.h2d(stream)
+                L.compress(stream)
+            for L in layers:
+                L.decode(stream)
+                d2h += L.d2h(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+        e2e = {"value": round(world * step_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    for L in layers:
+        if L.codec.get_status(stream) != 0:
+            raise RuntimeError("device status bits set during the timed region")
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in, fp32 compute, packed u8 cache",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/q; random page placement)",
+        "config": {
+            "workload": "long_context_mixed",
+            "layers": w.layers,
+            "layer_bits": [list(p) for p in w.layer_bits],
+            "batch": w.batch, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "seq_len": w.seq_len, "page_size": w.page_size, "v_group": w.group,
+            "decode_splits": [L.splits for L in layers],
+            "l2": "inputs larger than L2 (17 GB K/V per step); no flush",
+        },
+        "compress_mtoken_heads_per_s": round(world * rows / c_time / 1e6, 1),
+        "compress_gbs": round(c_gbs, 1),
+        "compress_frac": round(c_gbs / peak, 4),
+        "decode_gbs": round(d_gbs, 1),
+        "decode_frac": round(d_gbs / peak, 4),
+        "decode_kv_tokens_per_s": round(world * sum(sum(L.seq_lens) * L.w.num_kv_heads for L in layers) / d_time, 1),
+        "decode_query_tokens_per_s": round(world * w.batch * w.layers / d_time, 1),
+        "roofline": {
+            "bound": "hbm", "kernel": "compress_kernel (tq_compress_kv)",
+            "achieved": round(c_gbs, 1), "peak": peak, "peak_kind": f"of {peak_kind}",
+            "unit": "GB/s", "frac": round(c_gbs / peak, 4),
+            "traffic": None if traffic is None else traffic.get("bytes_per_launch"),
+            "algorithmic_bytes_per_launch": round(c_bytes / len(layers)),
+        },
+        "roofline_decode": {
+            "bound": "hbm", "kernel": "qrot + decode_kernel + combine (tq_decode_attention)",
+            "achieved": round(d_gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(d_gbs / peak, 4),
+            "algorithmic_bytes_per_call": round(d_bytes / len(layers)),
+        },
+        "clocks": clk,
+        "gpu_launches": launches,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    return line
+
+
+# --------------------------------------------------------------------------- #
+# CPU oracle (baseline / reference arm)                                         #
+# --------------------------------------------------------------------------- #
+
+class OracleSample:
+    """A bounded sample of the same workload: per layer, the first `tok` tokens of
+    `nseq` sequences on the first `nkv` KV heads, compressed then decoded (one
+    query token per sequence, G query heads per KV head) by the CPU oracle."""
+
+    def __init__(self, w, tok=1024, nseq=4, nkv=4):
+        import oracle as O
+        self.O = O
+        self.items = []
+        self.bytes = 0
+        self.rows = 0
+        for layer in range(w.layers):
+            lw = W.scaled(w.for_layer(layer), batch=nseq, seq_len=tok, num_kv_heads=nkv,
+                          num_q_heads=nkv * (w.num_q_heads // w.num_kv_heads))
+            b = W.generate(lw, layer=layer, device="cpu")
+            ora = O.Oracle(lw.head_dim, lw.k_bits, lw.v_bits, lw.group, w.codec_seed(layer))
+            self.items.append((lw, b, ora, W.as_u16(b.k), W.as_u16(b.v), W.as_u16(b.q),
+                               b.slot_mapping.numpy(), b.block_table.numpy(), b.seq_lens.numpy()))
+            self.bytes += compress_bytes(lw, b.num_tokens) + decode_bytes(lw, b.seq_lens.tolist(),
+                                                                           b.block_table.shape[1])
+            self.rows += b.num_tokens * nkv
+        self.desc = (f"per layer x{w.layers}: {tok} tokens x {nseq} sequences x {nkv} KV heads compressed, "
+                     f"then decoded with {w.num_q_heads // w.num_kv_heads} query heads per KV head")
+
+    def run(self, nthreads=0):
+        for lw, b, ora, k, v, q, sm, bt, sl in self.items:
+            kc, vc = ora.compress_kv(k, v, sm, lw.page_size, b.num_blocks, nthreads=nthreads)
+            ora.decode(q, kc, vc, bt, sl, lw.num_kv_heads, lw.page_size, b.sm_scale, mode=1, nthreads=nthreads)
+
+
+def cpu_baseline(w, budget_s=12.0):
+    s = OracleSample(w)
+    cores = os.cpu_count() or 1
+    t = time.perf_counter()
+    s.run()
+    one = time.perf_counter() - t
+    reps = max(1, min(int(budget_s / max(one, 1e-3)), 50))
+    t = time.perf_counter()
+    for _ in range(reps):
+        s.run()
+    el = time.perf_counter() - t
+    return {"value": round(s.bytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{s.desc}; {reps} repetitions, {el:.1f} s", "seconds": round(el, 2)}
+
+
+def run_reference(args):
+    w = W.long_context_mixed(seed=0)
+    s = OracleSample(w)
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        s.run()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        s.run()
+    el = (time.perf_counter() - t) / args.steps
+    value = s.bytes / el / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "long_context_mixed", "layers": w.layers,
+                   "layer_bits": [list(p) for p in w.layer_bits], "sample": s.desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": s.desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# --------------------------------------------------------------------------- #
+# Distributed plumbing                                                           #
+# --------------------------------------------------------------------------- #
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)))
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -74,6 +74,7 @@ def _load():
                                                    ctypes.c_int64, i64p, u8p, u8p, ctypes.c_int, ctypes.c_int64,
                                                    ctypes.c_int]),
             "tq_or_dequant_slots": (None, [vp, u8p, u8p, ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int64, dp, dp]),
+            "tq_or_key_qjl_given_codes": (None, [vp, u16p, u8p, ctypes.c_int64, u8p, u16p, dp, dp]),
             "tq_or_decode": (None, [vp, u16p, u8p, u8p, i32p, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, i32p,
                                     ctypes.c_int64, dp, ctypes.c_int]),
@@ -257,6 +258,18 @@ class Oracle:
                                     Hkv * d, Hkv * d, _ptr(sm, ctypes.c_int64), _ptr(k_cache, ctypes.c_uint8),
                                     _ptr(v_cache, ctypes.c_uint8), page_size, num_blocks, nthreads)
         return k_cache, v_cache
+
+    def key_qjl_given_codes(self, k, codes):
+        """QJL signs / gamma of key rows ([n, d] bf16 bits) for given codes ([n, d] uint8)."""
+        k = np.ascontiguousarray(k, dtype=np.uint16)
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        n = k.shape[0]
+        out = {"k_sign": np.zeros((n, self.d // 8), np.uint8), "k_gamma": np.zeros(n, np.uint16),
+               "pg": np.zeros((n, self.d)), "gamma": np.zeros(n)}
+        self._lib.tq_or_key_qjl_given_codes(self._h, _ptr(k, ctypes.c_uint16), _ptr(codes, ctypes.c_uint8), n,
+                                            _ptr(out["k_sign"], ctypes.c_uint8), _ptr(out["k_gamma"], ctypes.c_uint16),
+                                            _ptr(out["pg"], ctypes.c_double), _ptr(out["gamma"], ctypes.c_double))
+        return out
 
     def dequant_slots(self, k_cache, v_cache, page_size: int, Hkv: int, slots):
         """K~ (original space) and V~ as doubles, [n_slots, Hkv, d]."""

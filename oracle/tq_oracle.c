@@ -449,6 +449,48 @@ static void or_compress_value(const or_ctx *c, const uint16_t *vin, uint8_t *vco
     tq_or_pack(code, d, c->vb, vcode);
 }
 
+/*
+ * The QJL half of a key record for given codes (O4 steps 4-5): r = y - c/sqrt(d),
+ * gamma = ||r||, sigma_i = [(S r)_i >= 0].  Used where two correct encoders may
+ * take different codes for a coordinate that sits on a threshold: the signs
+ * are then defined by the codes actually stored.
+ */
+void tq_or_key_qjl_given_codes(const or_ctx *c, const uint16_t *k, const uint8_t *codes, int64_t n,
+                               uint8_t *ksign, uint16_t *kgamma, double *pg, double *gamma_out)
+{
+    int d = c->d;
+    double sd = sqrt((double)d);
+    for (int64_t row = 0; row < n; ++row) {
+        const uint16_t *kin = k + row * d;
+        const uint8_t *cd = codes + row * d;
+        double kk[256], r[256];
+        uint8_t sig[256];
+        double nsq = 0.0;
+        for (int j = 0; j < d; ++j) {
+            kk[j] = tq_or_bf16_to_double(kin[j]);
+            nsq += kk[j] * kk[j];
+        }
+        double nn = sqrt(nsq);
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < d; ++j) acc += c->Pi[i * d + j] * kk[j];
+            r[i] = (nn > 0.0 ? acc / nn : 0.0) - c->cent[cd[i]] / sd;
+        }
+        double gsq = 0.0;
+        for (int i = 0; i < d; ++i) gsq += r[i] * r[i];
+        double g = sqrt(gsq);
+        kgamma[row] = tq_or_bf16_from_double(g);
+        if (gamma_out) gamma_out[row] = g;
+        for (int i = 0; i < d; ++i) {
+            double p = 0.0;
+            for (int j = 0; j < d; ++j) p += c->S[i * d + j] * r[j];
+            sig[i] = (p >= 0.0);
+            if (pg) pg[row * d + i] = g > 0.0 ? p / g : 0.0;
+        }
+        tq_or_pack(sig, d, 1, ksign + row * (d / 8));
+    }
+}
+
 /* ------------------------------------------------------------------------- */
 /* Threading helper                                                           */
 /* ------------------------------------------------------------------------- */

@@ -1,0 +1,292 @@
+// tq_api.cu -- the C ABI declared in include/tq.h: argument validation, table
+// upload, workspace carve-up and kernel launches.  No call on the hot path
+// synchronises or allocates.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "tq.h"
+#include "tq_internal.h"
+
+struct tq_ctx {
+    tq::Codec codec;
+    void *dev_tables;  // Pi, PiT, S, ST (fp32) then the status word
+    int device;
+    int num_sms;
+    uint64_t seed;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+tq_status fail(tq_status s, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+tq_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(TQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_bits(int b) { return b >= 2 && b <= 4; }
+
+}  // namespace
+
+extern "C" {
+
+const char *tq_last_error(void) { return g_last_error.c_str(); }
+
+tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed, tq_handle *out)
+{
+    if (!out) return fail(TQ_ERR_INVALID_ARG, "tq_init: out is NULL");
+    *out = nullptr;
+    if (head_dim != 128 && head_dim != 256)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_init: head_dim %d not in {128, 256}", head_dim);
+    if (!supported_bits(k_bits) || !supported_bits(v_bits))
+        return fail(TQ_ERR_UNSUPPORTED, "tq_init: k_bits %d / v_bits %d not in {2, 3, 4}", k_bits, v_bits);
+    if ((group != 32 && group != 64 && group != 128) || head_dim % group)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_init: group %d not in {32, 64, 128} or does not divide %d", group,
+                    head_dim);
+    tq::HostTables ht;
+    if (!tq::build_tables(head_dim, k_bits, seed, &ht))
+        return fail(TQ_ERR_CUDA, "tq_init: Lloyd-Max iteration did not converge");
+
+    const int d = head_dim;
+    const size_t dd = static_cast<size_t>(d) * d;
+    std::vector<float> host(4 * dd);
+    for (int i = 0; i < d; ++i)
+        for (int j = 0; j < d; ++j) {
+            const size_t a = static_cast<size_t>(i) * d + j, t = static_cast<size_t>(j) * d + i;
+            host[a] = static_cast<float>(ht.Pi[a]);
+            host[dd + t] = static_cast<float>(ht.Pi[a]);
+            host[2 * dd + a] = static_cast<float>(ht.S[a]);
+            host[3 * dd + t] = static_cast<float>(ht.S[a]);
+        }
+    tq_ctx *c = new tq_ctx();
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e != cudaSuccess) {
+        delete c;
+        return cuda_fail(e, "tq_init: device query");
+    }
+    e = cudaMalloc(&c->dev_tables, 4 * dd * sizeof(float) + 256);
+    if (e != cudaSuccess) {
+        delete c;
+        return fail(TQ_ERR_OOM, "tq_init: cudaMalloc: %s", cudaGetErrorString(e));
+    }
+    float *base = static_cast<float *>(c->dev_tables);
+    e = cudaMemcpy(base, host.data(), 4 * dd * sizeof(float), cudaMemcpyHostToDevice);
+    unsigned *status = reinterpret_cast<unsigned *>(base + 4 * dd);
+    if (e == cudaSuccess) e = cudaMemset(status, 0, 256);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaFree(c->dev_tables);
+        delete c;
+        return cuda_fail(e, "tq_init: upload");
+    }
+    tq::Codec &k = c->codec;
+    std::memset(&k, 0, sizeof k);
+    k.d = d;
+    k.k_bits = k_bits;
+    k.v_bits = v_bits;
+    k.group = group;
+    k.qjl = (k_bits <= 3);
+    k.k_code_bytes = d * k_bits / 8;
+    k.k_sign_bytes = k.qjl ? d / 8 : 0;
+    k.v_code_bytes = d * v_bits / 8;
+    k.v_meta_bytes = (d / group) * 4;
+    for (int i = 0; i < (1 << k_bits); ++i) k.centroids[i] = static_cast<float>(ht.centroids[i]);
+    for (int i = 0; i + 1 < (1 << k_bits); ++i) k.thresholds[i] = static_cast<float>(ht.thresholds[i]);
+    k.Pi = base;
+    k.PiT = base + dd;
+    k.S = base + 2 * dd;
+    k.ST = base + 3 * dd;
+    k.status = status;
+    c->seed = seed;
+    *out = c;
+    return TQ_OK;
+}
+
+tq_status tq_destroy(tq_handle h)
+{
+    if (!h) return TQ_OK;
+    cudaError_t e = cudaFree(h->dev_tables);
+    delete h;
+    if (e != cudaSuccess) return cuda_fail(e, "tq_destroy");
+    return TQ_OK;
+}
+
+tq_status tq_cache_layout(tq_handle h, int page_size, size_t *k_page_bytes, size_t *v_page_bytes)
+{
+    if (!h || !k_page_bytes || !v_page_bytes) return fail(TQ_ERR_INVALID_ARG, "tq_cache_layout: NULL argument");
+    if (page_size != 16 && page_size != 32)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_cache_layout: page_size %d not in {16, 32}", page_size);
+    const tq::PageGeom g = tq::page_geom(h->codec, page_size);
+    *k_page_bytes = static_cast<size_t>(g.k_page);
+    *v_page_bytes = static_cast<size_t>(g.v_page);
+    return TQ_OK;
+}
+
+tq_status tq_compress_kv(tq_handle h, const uint16_t *k, const uint16_t *v, int64_t T, int num_kv_heads,
+                         int64_t k_stride_tok, int64_t v_stride_tok, const int64_t *slot_mapping, uint8_t *k_cache,
+                         uint8_t *v_cache, int page_size, int64_t num_blocks, void *stream)
+{
+    if (!h) return fail(TQ_ERR_INVALID_ARG, "tq_compress_kv: NULL handle");
+    if (page_size != 16 && page_size != 32)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_compress_kv: page_size %d not in {16, 32}", page_size);
+    if (T < 0 || num_kv_heads < 1 || num_blocks < 1)
+        return fail(TQ_ERR_INVALID_ARG, "tq_compress_kv: T=%lld num_kv_heads=%d num_blocks=%lld",
+                    static_cast<long long>(T), num_kv_heads, static_cast<long long>(num_blocks));
+    if (T == 0) return TQ_OK;
+    const int d = h->codec.d;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+        return fail(TQ_ERR_INVALID_ARG, "tq_compress_kv: NULL pointer");
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return fail(TQ_ERR_INVALID_ARG, "tq_compress_kv: k, v and the caches must be 16-byte aligned");
+    if (k_stride_tok < static_cast<int64_t>(num_kv_heads) * d || v_stride_tok < static_cast<int64_t>(num_kv_heads) * d ||
+        k_stride_tok % 8 || v_stride_tok % 8)
+        return fail(TQ_ERR_INVALID_ARG,
+                    "tq_compress_kv: token strides must be >= num_kv_heads*head_dim and multiples of 8 elements");
+    if (T * num_kv_heads / 32 >= (int64_t(1) << 31))
+        return fail(TQ_ERR_UNSUPPORTED, "tq_compress_kv: too many token-heads in one call");
+    const tq::PageGeom g = tq::page_geom(h->codec, page_size);
+    cudaError_t e = tq::launch_compress(h->codec, g, k, v, T, num_kv_heads, k_stride_tok, v_stride_tok, slot_mapping,
+                                        k_cache, v_cache, num_blocks, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tq_compress_kv: launch");
+    return TQ_OK;
+}
+
+tq_status tq_dequant_kv(tq_handle h, const uint8_t *k_cache, const uint8_t *v_cache, int page_size,
+                        int64_t num_blocks, int num_kv_heads, const int64_t *slots, int64_t T, uint16_t *k_out,
+                        uint16_t *v_out, void *stream)
+{
+    if (!h) return fail(TQ_ERR_INVALID_ARG, "tq_dequant_kv: NULL handle");
+    if (page_size != 16 && page_size != 32)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_dequant_kv: page_size %d not in {16, 32}", page_size);
+    if (T < 0 || num_kv_heads < 1 || num_blocks < 1)
+        return fail(TQ_ERR_INVALID_ARG, "tq_dequant_kv: bad sizes");
+    if (T == 0) return TQ_OK;
+    if (!k_cache || !v_cache || !slots || !k_out || !v_out)
+        return fail(TQ_ERR_INVALID_ARG, "tq_dequant_kv: NULL pointer");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(slots, 8) || !aligned(k_out, 16) ||
+        !aligned(v_out, 16))
+        return fail(TQ_ERR_INVALID_ARG, "tq_dequant_kv: misaligned pointer");
+    if (T >= (int64_t(1) << 31) || num_kv_heads > 65535)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_dequant_kv: too many slots in one call");
+    const tq::PageGeom g = tq::page_geom(h->codec, page_size);
+    cudaError_t e = tq::launch_dequant(h->codec, g, k_cache, v_cache, num_blocks, num_kv_heads, slots, T, k_out, v_out,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tq_dequant_kv: launch");
+    return TQ_OK;
+}
+
+int tq_decode_splits(tq_handle h, int batch, int num_kv_heads, int max_blocks_per_seq, int page_size)
+{
+    if (!h || batch < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 || page_size < 1) return 1;
+    const int units = batch * num_kv_heads;
+    int splits = (2 * h->num_sms + units - 1) / units;
+    if (splits > 64) splits = 64;
+    if (splits > max_blocks_per_seq) splits = max_blocks_per_seq;
+    return splits < 1 ? 1 : splits;
+}
+
+size_t tq_decode_workspace_bytes(tq_handle h, int batch, int num_q_heads, int splits)
+{
+    if (!h || batch < 0 || num_q_heads < 0 || splits < 1) return 0;
+    return tq::decode_workspace_bytes(h->codec.d, batch, num_q_heads, splits);
+}
+
+tq_status tq_decode_attention(tq_handle h, const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                              const int32_t *block_table, const int32_t *seq_lens, int batch, int num_q_heads,
+                              int num_kv_heads, int page_size, int max_blocks_per_seq, int64_t num_blocks,
+                              float sm_scale, int splits, void *workspace, size_t ws_bytes, uint16_t *out,
+                              void *stream)
+{
+    if (!h) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: NULL handle");
+    if (page_size != 16 && page_size != 32)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_decode_attention: page_size %d not in {16, 32}", page_size);
+    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 || num_blocks < 1 || splits < 0)
+        return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: bad sizes");
+    if (num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > 8)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_decode_attention: num_q_heads / num_kv_heads must be an integer in 1..8");
+    if (!std::isfinite(sm_scale)) return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: sm_scale not finite");
+    if (batch == 0) return TQ_OK;
+    if (batch > 65535 || num_kv_heads > 65535)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_decode_attention: batch / num_kv_heads above 65535");
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !workspace || !out)
+        return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: NULL pointer");
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4) || !aligned(workspace, 256) || !aligned(out, 16))
+        return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: misaligned pointer");
+    if (splits == 0) splits = tq_decode_splits(h, batch, num_kv_heads, max_blocks_per_seq, page_size);
+    if (splits > 1024) return fail(TQ_ERR_UNSUPPORTED, "tq_decode_attention: splits %d above 1024", splits);
+    const size_t need = tq::decode_workspace_bytes(h->codec.d, batch, num_q_heads, splits);
+    if (ws_bytes < need)
+        return fail(TQ_ERR_INVALID_ARG, "tq_decode_attention: workspace %zu bytes < %zu needed", ws_bytes, need);
+    tq::DecodeArgs a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.B = batch;
+    a.Hq = num_q_heads;
+    a.Hkv = num_kv_heads;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.sm_scale = sm_scale;
+    a.splits = splits;
+    a.pages_per_split = (max_blocks_per_seq + splits - 1) / splits;
+    a.ws = tq::carve_decode_workspace(workspace, h->codec.d, batch, num_q_heads, splits);
+    a.out = out;
+    const tq::PageGeom g = tq::page_geom(h->codec, page_size);
+    cudaError_t e = tq::launch_decode(h->codec, g, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tq_decode_attention: launch");
+    return TQ_OK;
+}
+
+tq_status tq_get_status(tq_handle h, uint32_t *device_error_bits, void *stream)
+{
+    if (!h || !device_error_bits) return fail(TQ_ERR_INVALID_ARG, "tq_get_status: NULL argument");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    unsigned v = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&v, h->codec.status, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(h->codec.status, 0, sizeof v);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "tq_get_status");
+    *device_error_bits = v;
+    return TQ_OK;
+}
+
+tq_status tq_export_params(tq_handle h, float *Pi, float *S, float *centroids, float *thresholds)
+{
+    if (!h) return fail(TQ_ERR_INVALID_ARG, "tq_export_params: NULL handle");
+    const size_t dd = static_cast<size_t>(h->codec.d) * h->codec.d;
+    cudaError_t e = cudaSuccess;
+    if (Pi) e = cudaMemcpy(Pi, h->codec.Pi, dd * sizeof(float), cudaMemcpyDeviceToHost);
+    if (S && e == cudaSuccess) e = cudaMemcpy(S, h->codec.S, dd * sizeof(float), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "tq_export_params");
+    const int L = 1 << h->codec.k_bits;
+    if (centroids) std::memcpy(centroids, h->codec.centroids, L * sizeof(float));
+    if (thresholds) std::memcpy(thresholds, h->codec.thresholds, (L - 1) * sizeof(float));
+    return TQ_OK;
+}
+
+}  // extern "C"

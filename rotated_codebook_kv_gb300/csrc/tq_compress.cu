@@ -1,0 +1,435 @@
+// tq_compress.cu -- fused key + value compression into the paged cache.
+//
+// Keys (turbo-attn, "How it works", steps 1-3; 0xsero/turboquant, "Compression
+// Pipeline"; brightcoding blog, "Example 4": normalize -> rotate -> Lloyd-Max
+// quantize -> pack bits):
+//   n = ||k|| (stored bf16), z = sqrt(d) Pi k / n, code_j = #{i : t_i <= z_j},
+//   and when k_bits <= 3 the residual r = z - c[code] (N(0,1) units) gives
+//   sigma_i = [ (S r)_i >= 0 ] and gamma = ||r|| / sqrt(d) (stored bf16).
+// Values (0xsero/turboquant, "Value Compression"): per group of `group`
+//   channels, scale = fp16((max - min) / (2^b - 1)), zero = fp16(min), and
+//   code = #{m < 2^b - 1 : x - zero >= (m + 1/2) scale} (round half up).
+// K and V of the same tokens are compressed in one launch (brightcoding blog,
+// "Key Features": compress_kv fuses key and value compression).
+//
+// Numerics.  The fast path rotates and projects in fp32.  A code whose fp32 z
+// lies within kCodeGuard of a threshold, or a sign whose |p| lies within
+// kSignGuard * ||r|| of zero, sends the whole row through an exact path:
+// compensated (double-fp32) dot products with exact products and fp64 for the
+// O(d) tail, so that codes and signs equal the exactly-rounded decisions up to
+// the fp32 rounding of the Pi / S tables (about 1e-7 in z units).
+#include <cuda_runtime.h>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowsPerBlock = 32;
+constexpr float kCodeGuard = 1e-5f;  // z units
+constexpr float kSignGuard = 2e-5f;  // |p| / ||r||
+
+template <int D>
+struct CompressSmem {
+    static constexpr int TM = kRowsPerBlock;
+    static constexpr int kCodeStride = D + 4;
+    static constexpr size_t kKf = sizeof(float) * TM * D;      // keys, later S r
+    static constexpr size_t kYb = sizeof(float) * TM * D;      // Pi k, later r
+    static constexpr size_t kCodes = ((TM * kCodeStride + 15) / 16) * 16;
+    static constexpr size_t kScratch = sizeof(double) * kWarps * D;
+    static constexpr size_t kBytes = kKf + kYb + kCodes + kScratch;
+};
+
+// acc[rr] += sum_j W[j][i] * X[row(rr)][j] for i = tid % D, rows interleaved by
+// column group.  W is a d x d table in global memory read column-coalesced
+// (every thread of a warp loads consecutive i of the same row j); X rows are
+// broadcast from shared memory.
+template <int D, int TM>
+__device__ __forceinline__ void matvec_rows(const float *__restrict__ W, const float *X, float *Y)
+{
+    constexpr int CG = kThreads / D;
+    constexpr int RPT = TM / CG;
+    const int tid = threadIdx.x;
+    const int i = tid % D, rg = tid / D;
+    float acc[RPT];
+#pragma unroll
+    for (int rr = 0; rr < RPT; ++rr) acc[rr] = 0.f;
+    const float *w = W + i;
+#pragma unroll 2
+    for (int j = 0; j < D; j += 4) {
+        const float w0 = __ldg(w + (j + 0) * D);
+        const float w1 = __ldg(w + (j + 1) * D);
+        const float w2 = __ldg(w + (j + 2) * D);
+        const float w3 = __ldg(w + (j + 3) * D);
+#pragma unroll
+        for (int rr = 0; rr < RPT; ++rr) {
+            const float4 x = *reinterpret_cast<const float4 *>(X + (rg + rr * CG) * D + j);
+            acc[rr] = fmaf(w0, x.x, acc[rr]);
+            acc[rr] = fmaf(w1, x.y, acc[rr]);
+            acc[rr] = fmaf(w2, x.z, acc[rr]);
+            acc[rr] = fmaf(w3, x.w, acc[rr]);
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < RPT; ++rr) Y[(rg + rr * CG) * D + i] = acc[rr];
+}
+
+// Exact path for one key row, run by one warp.  Writes the row's codes, its
+// QJL projections (sign-exact) into p_out, and the bf16 norm / gamma.
+template <int D>
+__device__ void precise_key_row(const Codec &C, const uint16_t *__restrict__ src, uint8_t *codes, float *p_out,
+                                double *scratch, uint16_t *n16, uint16_t *g16)
+{
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    float kx[E];
+    float mx = 0.f;
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        kx[m] = bf16_to_float(src[lane + 32 * m]);
+        mx = fmaxf(mx, fabsf(kx[m]));
+    }
+    mx = warp_max(mx);
+    if (mx == 0.f) {  // zero key: caller writes an all-zero record
+        return;
+    }
+    // Exact power-of-two scaling keeps squares away from underflow/overflow.
+    int ex;
+    frexpf(mx, &ex);
+    const float sc = ldexpf(1.f, -ex);
+    float s = 0.f, c = 0.f;
+    float *kw = reinterpret_cast<float *>(scratch);
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        kx[m] *= sc;
+        dot2_step(s, c, kx[m], kx[m]);
+        kw[lane + 32 * m] = kx[m];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        float t, e;
+        two_sum(s, s2, t, e);
+        s = t;
+        c = __fadd_rn(c, __fadd_rn(c2, e));
+    }
+    const double n_sc = sqrt(static_cast<double>(s) + static_cast<double>(c));
+    __syncwarp();
+    float yh[E], yl[E];
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        const int i = lane + 32 * m;
+        float hs = 0.f, hc = 0.f;
+        for (int j = 0; j < D; ++j) dot2_step(hs, hc, __ldg(C.PiT + j * D + i), kw[j]);
+        yh[m] = hs;
+        yl[m] = hc;
+    }
+    __syncwarp();
+    const double zscale = sqrt(static_cast<double>(D)) / n_sc;
+    const int nthr = (1 << C.k_bits) - 1;
+    double rr = 0.0;
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        const int i = lane + 32 * m;
+        const double z = (static_cast<double>(yh[m]) + static_cast<double>(yl[m])) * zscale;
+        int code = 0;
+        for (int t = 0; t < nthr; ++t) code += (static_cast<double>(C.thresholds[t]) <= z);
+        codes[i] = static_cast<uint8_t>(code);
+        const double r = z - static_cast<double>(C.centroids[code]);
+        scratch[i] = r;
+        rr += r * r;
+    }
+    rr = warp_sum(rr);
+    if (lane == 0) {
+        *n16 = double_to_bf16_bits(ldexp(n_sc, ex));
+        if (C.qjl) *g16 = double_to_bf16_bits(sqrt(rr) / sqrt(static_cast<double>(D)));
+    }
+    __syncwarp();
+    if (!C.qjl) return;
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        const int i = lane + 32 * m;
+        float ps = 0.f, pc = 0.f;
+        for (int j = 0; j < D; ++j) {
+            const double rj = scratch[j];
+            const float rh = static_cast<float>(rj);
+            const float rl = static_cast<float>(rj - static_cast<double>(rh));
+            const float sv = __ldg(C.ST + j * D + i);
+            dot2_step(ps, pc, sv, rh);
+            pc = __fmaf_rn(sv, rl, pc);
+        }
+        p_out[i] = __fadd_rn(ps, pc);
+    }
+    __syncwarp();
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
+                int64_t rows, int Hkv, int64_t ks, int64_t vs, const int64_t *__restrict__ slots,
+                uint8_t *__restrict__ kc, uint8_t *__restrict__ vc, int64_t num_blocks)
+{
+    using SM = CompressSmem<D>;
+    constexpr int TM = SM::TM;
+    constexpr int CS = SM::kCodeStride;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float *kf = reinterpret_cast<float *>(smem_raw);
+    float *yb = reinterpret_cast<float *>(smem_raw + SM::kKf);
+    uint8_t *codes = smem_raw + SM::kKf + SM::kYb;
+    double *scratch = reinterpret_cast<double *>(smem_raw + SM::kKf + SM::kYb + SM::kCodes);
+    __shared__ float s_scale[TM];
+    __shared__ float s_rn[TM];
+    __shared__ int64_t s_dst[TM];
+    __shared__ int s_off[TM];
+    __shared__ int s_flag[TM];  // 0 fast, 1 exact path, 2 zero key
+    __shared__ uint16_t s_n16[TM], s_g16[TM];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * TM;
+    const float sqrtd = sqrtf(static_cast<float>(D));
+
+    if (tid < TM) {
+        const int64_t r = r0 + tid;
+        int64_t dst = -1;
+        int off = 0;
+        if (r < rows) {
+            const int64_t t = r / Hkv;
+            const int h = static_cast<int>(r - t * Hkv);
+            const int64_t s = slots[t];
+            if (s >= 0) {
+                if (s < num_blocks * G.P) {
+                    const int64_t blk = s / G.P;
+                    off = static_cast<int>(s - blk * G.P);
+                    dst = blk * Hkv + h;
+                } else {
+                    atomicOr(C.status, TQ_DEVERR_SLOT_RANGE);
+                }
+            }
+        }
+        s_dst[tid] = dst;
+        s_off[tid] = off;
+    }
+    // ---- load key rows (bf16 -> fp32, exact) ---------------------------------
+    for (int e = tid; e < TM * (D / 8); e += kThreads) {
+        const int row = e / (D / 8), c8 = e - row * (D / 8);
+        const int64_t r = r0 + row;
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (r < rows) {
+            const int64_t t = r / Hkv;
+            const int h = static_cast<int>(r - t * Hkv);
+            u = __ldg(reinterpret_cast<const uint4 *>(kin + t * ks + static_cast<int64_t>(h) * D) + c8);
+        }
+        float4 lo = make_float4(bf16_to_float(u.x & 0xffffu), bf16_to_float(u.x >> 16), bf16_to_float(u.y & 0xffffu),
+                                bf16_to_float(u.y >> 16));
+        float4 hi = make_float4(bf16_to_float(u.z & 0xffffu), bf16_to_float(u.z >> 16), bf16_to_float(u.w & 0xffffu),
+                                bf16_to_float(u.w >> 16));
+        *reinterpret_cast<float4 *>(kf + row * D + c8 * 8) = lo;
+        *reinterpret_cast<float4 *>(kf + row * D + c8 * 8 + 4) = hi;
+    }
+    __syncthreads();
+    // ---- norms; rows with an extreme range take the exact path -------------
+    for (int row = warp; row < TM; row += kWarps) {
+        float ss = 0.f, mx = 0.f;
+        for (int j = lane; j < D; j += 32) {
+            const float x = kf[row * D + j];
+            ss = fmaf(x, x, ss);
+            mx = fmaxf(mx, fabsf(x));
+        }
+        ss = warp_sum(ss);
+        mx = warp_max(mx);
+        if (lane == 0) {
+            int flag = 0;
+            if (mx == 0.f) flag = 2;
+            else if (!(mx >= 0x1p-30f && mx <= 0x1p30f)) flag = 1;
+            const float n = sqrtf(ss);
+            s_scale[row] = (flag == 0) ? sqrtd / n : 0.f;
+            s_flag[row] = flag;
+            s_n16[row] = float_to_bf16_bits(n);
+            s_g16[row] = 0;
+        }
+    }
+    // ---- rotation: yb = Pi k (unnormalised) -----------------------------------
+    matvec_rows<D, TM>(C.PiT, kf, yb);
+    __syncthreads();
+    // ---- codes, guard band, residual -----------------------------------------
+    const int nthr = (1 << C.k_bits) - 1;
+    for (int e = tid; e < TM * D; e += kThreads) {
+        const int row = e / D, i = e - row * D;
+        const int fl = s_flag[row];
+        const float z = yb[e] * s_scale[row];
+        int code = 0;
+        float dmin = INFINITY;
+        for (int t = 0; t < nthr; ++t) {
+            const float th = C.thresholds[t];
+            code += (th <= z);
+            dmin = fminf(dmin, fabsf(z - th));
+        }
+        if (fl == 2) code = 0;
+        codes[row * CS + i] = static_cast<uint8_t>(code);
+        yb[e] = (fl == 2) ? 0.f : z - C.centroids[code];
+        if (fl == 0 && dmin < kCodeGuard) s_flag[row] = 1;
+    }
+    __syncthreads();
+    // ---- QJL: p = S r, gamma, sign guard ---------------------------------------
+    if (C.qjl) {
+        matvec_rows<D, TM>(C.ST, yb, kf);
+        __syncthreads();
+        for (int row = warp; row < TM; row += kWarps) {
+            float ss = 0.f;
+            for (int j = lane; j < D; j += 32) ss = fmaf(yb[row * D + j], yb[row * D + j], ss);
+            ss = warp_sum(ss);
+            const float rn = sqrtf(ss);
+            bool near = false;
+            for (int j = lane; j < D; j += 32) near |= fabsf(kf[row * D + j]) < kSignGuard * rn;
+            near = __any_sync(0xffffffffu, near);
+            if (lane == 0) {
+                s_rn[row] = rn;
+                s_g16[row] = float_to_bf16_bits(rn / sqrtd);
+                if (near && s_flag[row] == 0) s_flag[row] = 1;
+            }
+        }
+        __syncthreads();
+    }
+    // ---- exact path for flagged rows -------------------------------------------
+    for (int row = warp; row < TM; row += kWarps) {
+        if (s_flag[row] != 1 || s_dst[row] < 0) continue;
+        const int64_t r = r0 + row;
+        const int64_t t = r / Hkv;
+        const int h = static_cast<int>(r - t * Hkv);
+        precise_key_row<D>(C, kin + t * ks + static_cast<int64_t>(h) * D, codes + row * CS, kf + row * D,
+                           scratch + warp * D, &s_n16[row], &s_g16[row]);
+    }
+    __syncthreads();
+    // ---- pack and store: one warp per row ------------------------------------
+    for (int row = warp; row < TM; row += kWarps) {
+        const int64_t dst = s_dst[row];
+        if (dst < 0) continue;
+        const int off = s_off[row];
+        const bool zero = (s_flag[row] == 2);
+        uint8_t *krec = kc + dst * G.k_page;
+        const int nw = D * C.k_bits / 32;
+        if (lane < nw) {
+            const uint32_t w = zero ? 0u : pack_word(codes + row * CS, lane, C.k_bits);
+            *reinterpret_cast<uint32_t *>(krec + static_cast<int64_t>(off) * C.k_code_bytes + 4 * lane) = w;
+        }
+        if (C.qjl) {
+#pragma unroll
+            for (int w = 0; w < D / 32; ++w) {
+                uint32_t bits = __ballot_sync(0xffffffffu, kf[row * D + 32 * w + lane] >= 0.f);
+                if (zero) bits = 0u;
+                if (lane == w)
+                    *reinterpret_cast<uint32_t *>(krec + G.k_sign_off + static_cast<int64_t>(off) * C.k_sign_bytes +
+                                                  4 * w) = bits;
+            }
+            if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * off) = zero ? 0 : s_g16[row];
+        }
+        if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * off) = zero ? 0 : s_n16[row];
+
+        // ---- value row -------------------------------------------------------
+        constexpr int E = D / 32;
+        const int64_t r = r0 + row;
+        const int64_t t = r / Hkv;
+        const int h = static_cast<int>(r - t * Hkv);
+        const uint16_t *vsrc = vin + t * vs + static_cast<int64_t>(h) * D + lane * E;
+        float x[E];
+        if constexpr (E == 4) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(vsrc));
+            x[0] = bf16_to_float(u.x & 0xffffu); x[1] = bf16_to_float(u.x >> 16);
+            x[2] = bf16_to_float(u.y & 0xffffu); x[3] = bf16_to_float(u.y >> 16);
+        } else {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(vsrc));
+            x[0] = bf16_to_float(u.x & 0xffffu); x[1] = bf16_to_float(u.x >> 16);
+            x[2] = bf16_to_float(u.y & 0xffffu); x[3] = bf16_to_float(u.y >> 16);
+            x[4] = bf16_to_float(u.z & 0xffffu); x[5] = bf16_to_float(u.z >> 16);
+            x[6] = bf16_to_float(u.w & 0xffffu); x[7] = bf16_to_float(u.w >> 16);
+        }
+        const int lpg = C.group / E;  // lanes per group
+        float mn = x[0], mxv = x[0];
+#pragma unroll
+        for (int m = 1; m < E; ++m) { mn = fminf(mn, x[m]); mxv = fmaxf(mxv, x[m]); }
+        for (int o = lpg >> 1; o > 0; o >>= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mxv = fmaxf(mxv, __shfl_xor_sync(0xffffffffu, mxv, o));
+        }
+        const int L = (1 << C.v_bits) - 1;
+        float dh, de;
+        two_sum(mxv, -mn, dh, de);
+        // (max - min) / L with L in {3, 7, 15} is either exact in fp32 or a
+        // non-terminating binary fraction, so rounding it to fp32 first never
+        // lands on an fp16 rounding midpoint: one rounding to fp16 results.
+        const __half s16 = (de == 0.f) ? __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)))
+                                       : __double2half((static_cast<double>(mxv) - static_cast<double>(mn)) / L);
+        const __half z16 = __float2half_rn(mn);
+        const float sv = __half2float(s16), zv = __half2float(z16);
+        uint8_t *vcodes = codes + row * CS;  // key codes of this row are already packed
+        __syncwarp();
+#pragma unroll
+        for (int m = 0; m < E; ++m) {
+            int q = 0;
+            if (sv != 0.f) {
+                // x - z exactly as a + ea; the code counts midpoints (j + 1/2) s <= x - z.
+                float a, ea;
+                two_sum(x[m], -zv, a, ea);
+                const float qf = floorf(__fdiv_rn(a, sv) + 0.5f);
+                q = static_cast<int>(fminf(fmaxf(qf, 0.f), static_cast<float>(L)));  // NaN -> 0
+                // exact fix-up of the guess against the midpoints
+                while (q < L && __fadd_rn(__fsub_rn(a, (q + 0.5f) * sv), ea) >= 0.f) ++q;
+                while (q > 0 && !(__fadd_rn(__fsub_rn(a, (q - 0.5f) * sv), ea) >= 0.f)) --q;
+            }
+            vcodes[lane * E + m] = static_cast<uint8_t>(q);
+        }
+        __syncwarp();
+        uint8_t *vrec = vc + dst * G.v_page;
+        const int nvw = D * C.v_bits / 32;
+        if (lane < nvw)
+            *reinterpret_cast<uint32_t *>(vrec + static_cast<int64_t>(off) * C.v_code_bytes + 4 * lane) =
+                pack_word(vcodes, lane, C.v_bits);
+        if ((lane % lpg) == 0) {
+            const int gi = lane / lpg;
+            const uint32_t meta = static_cast<uint32_t>(__half_as_ushort(s16)) |
+                                  (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
+            *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + static_cast<int64_t>(off) * C.v_meta_bytes + 4 * gi) =
+                meta;
+        }
+        __syncwarp();
+    }
+}
+
+template <int D>
+cudaError_t launch_compress_d(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
+                              int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
+                              int64_t num_blocks, cudaStream_t st)
+{
+    const size_t smem = CompressSmem<D>::kBytes;
+    static bool attr_set[64] = {};  // the attribute is per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(compress_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    const int64_t rows = T * Hkv;
+    const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+    compress_kernel<D><<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(c, pg, k, v, rows, Hkv, ks, vs, slots,
+                                                                             kc, vc, num_blocks);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
+                            int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
+                            int64_t num_blocks, cudaStream_t st)
+{
+    if (c.d == 128) return launch_compress_d<128>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+    return launch_compress_d<256>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+}
+
+}  // namespace tq

@@ -1,0 +1,96 @@
+// tq_device.cuh -- small device helpers shared by the kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#define TQ_DEVERR_SLOT_RANGE 0x1u
+#define TQ_DEVERR_BLOCK_RANGE 0x2u
+#define TQ_DEVERR_SEQ_RANGE 0x4u
+
+namespace tq {
+
+__device__ __forceinline__ float bf16_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float x)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ uint16_t double_to_bf16_bits(double x)
+{
+    return __bfloat16_as_ushort(__double2bfloat16(x));
+}
+
+// Error-free sum: s + e == a + b exactly (Knuth's TwoSum).  The _rn
+// intrinsics are never contracted into FMAs by the compiler.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Compensated dot-product step (Ogita, Rump & Oishi, "Accurate sum and dot
+// product", 2005): (s, c) accumulates a * b with the product split exactly.
+__device__ __forceinline__ void dot2_step(float &s, float &c, float a, float b)
+{
+    const float p = __fmul_rn(a, b);
+    const float ep = __fmaf_rn(a, b, -p);
+    float t, et;
+    two_sum(s, p, t, et);
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(et, ep));
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ double warp_sum(double v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Word w of the LSB-first bitstream of b-bit codes (one code per byte in `codes`).
+__device__ __forceinline__ uint32_t pack_word(const uint8_t *codes, int w, int b)
+{
+    const int bit0 = 32 * w;
+    int c = bit0 / b;
+    const int sh = bit0 - c * b;
+    uint64_t acc = static_cast<uint64_t>(codes[c]) >> sh;
+    int nb = b - sh;
+    ++c;
+    while (nb < 32) {
+        acc |= static_cast<uint64_t>(codes[c]) << nb;
+        nb += b;
+        ++c;
+    }
+    return static_cast<uint32_t>(acc);
+}
+
+// b-bit code j of an LSB-first bitstream held as 32-bit words.
+__device__ __forceinline__ uint32_t code_from_words(const uint32_t *w, int j, int b)
+{
+    const int o = j * b;
+    const int wi = o >> 5, sh = o & 31;
+    const uint32_t lo = w[wi];
+    const uint32_t hi = (sh + b > 32) ? w[wi + 1] : 0u;
+    return __funnelshift_r(lo, hi, sh) & ((1u << b) - 1u);
+}
+
+}  // namespace tq

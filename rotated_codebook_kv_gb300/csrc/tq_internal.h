@@ -1,0 +1,84 @@
+// tq_internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+namespace tq {
+
+// Host tables in double, built by tq_params.cpp.
+struct HostTables {
+    std::vector<double> Pi, S, centroids, thresholds;
+};
+bool build_tables(int d, int k_bits, uint64_t seed, HostTables *out);
+bool build_codebook(int bits, double *centroids, double *thresholds);
+
+// Codec constants, passed by value to every kernel.
+struct Codec {
+    int d, k_bits, v_bits, group, qjl;
+    int k_code_bytes, k_sign_bytes, v_code_bytes, v_meta_bytes;  // per token-head
+    float centroids[16];   // N(0,1) units, ascending
+    float thresholds[16];  // 2^k_bits - 1 used
+    const float *Pi;       // [d][d] row-major: y_i = sum_j Pi[i][j] k_j
+    const float *PiT;      // [d][d] transpose of Pi
+    const float *S;        // [d][d] row-major QJL matrix
+    const float *ST;       // [d][d] transpose of S
+    unsigned int *status;  // device status word (TQ_DEVERR_* bits)
+};
+
+// Byte offsets of the sub-arrays of one (block, kv head) page record.
+struct PageGeom {
+    int P;
+    int64_t k_page, v_page;
+    int64_t k_sign_off, k_norm_off, k_gamma_off;  // codes start at 0
+    int64_t v_meta_off;                           // codes start at 0
+};
+
+inline PageGeom page_geom(const Codec &c, int P)
+{
+    PageGeom g;
+    g.P = P;
+    g.k_sign_off = static_cast<int64_t>(P) * c.k_code_bytes;
+    g.k_norm_off = g.k_sign_off + static_cast<int64_t>(P) * c.k_sign_bytes;
+    g.k_gamma_off = g.k_norm_off + 2LL * P;
+    g.k_page = g.k_gamma_off + (c.qjl ? 2LL * P : 0);
+    g.v_meta_off = static_cast<int64_t>(P) * c.v_code_bytes;
+    g.v_page = g.v_meta_off + static_cast<int64_t>(P) * c.v_meta_bytes;
+    return g;
+}
+
+// Workspace carve-up of tq_decode_attention (all fp32, 256-byte aligned pieces).
+struct DecodeWorkspace {
+    float *qrot;  // [B][Hq][d]
+    float *qs;    // [B][Hq][d]
+    float *acc;   // [splits][B][Hq][d] unnormalised partial outputs
+    float *ml;    // [splits][B][Hq][2] running max and denominator
+};
+size_t decode_workspace_bytes(int d, int B, int Hq, int splits);
+DecodeWorkspace carve_decode_workspace(void *base, int d, int B, int Hq, int splits);
+
+struct DecodeArgs {
+    const uint16_t *q;
+    const uint8_t *k_cache, *v_cache;
+    const int32_t *block_table, *seq_lens;
+    int B, Hq, Hkv, max_blocks;
+    int64_t num_blocks;
+    float sm_scale;
+    int splits, pages_per_split;
+    DecodeWorkspace ws;
+    uint16_t *out;
+};
+
+cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
+                            int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
+                            int64_t num_blocks, cudaStream_t st);
+
+cudaError_t launch_dequant(const Codec &c, const PageGeom &pg, const uint8_t *kc, const uint8_t *vc,
+                           int64_t num_blocks, int Hkv, const int64_t *slots, int64_t T, uint16_t *k_out,
+                           uint16_t *v_out, cudaStream_t st);
+
+cudaError_t launch_decode(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st);
+
+}  // namespace tq

@@ -1,0 +1,54 @@
+"""The C-ABI library builds, loads and exports every symbol include/tq.h declares.
+
+No compute call is made here (no GPU needed).
+"""
+import os
+import re
+
+import pytest
+
+from rotated_codebook_kv_gb300 import build, native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "tq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return native.load()
+
+
+def test_header_declares_the_boundary():
+    syms = _declared_symbols()
+    for s in ("tq_init", "tq_compress_kv", "tq_dequant_kv", "tq_decode_attention"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for s in _declared_symbols():
+        assert hasattr(lib, s), s
+    assert set(_declared_symbols()) <= set(native.SIGNATURES)
+
+
+def test_invalid_arguments_rejected_without_gpu(lib):
+    # argument validation happens on the host before any CUDA call
+    with pytest.raises(native.TQError) as e:
+        native.tq_init(96, 3, 4, 32, 0)
+    assert e.value.status == native.TQ_ERR_UNSUPPORTED
+    assert "head_dim" in native.tq_last_error()
+    with pytest.raises(native.TQError) as e:
+        native.tq_init(128, 5, 4, 32, 0)
+    assert e.value.status == native.TQ_ERR_UNSUPPORTED
+    with pytest.raises(native.TQError) as e:
+        native.tq_init(128, 3, 4, 48, 0)
+    assert e.value.status == native.TQ_ERR_UNSUPPORTED
+    with pytest.raises(native.TQError) as e:
+        native.tq_compress_kv(None, 0, 0, 1, 1, 128, 128, 0, 0, 0, 16, 1, None)
+    assert e.value.status == native.TQ_ERR_INVALID_ARG
+    assert native.tq_decode_workspace_bytes(None, 1, 1, 1) == 0

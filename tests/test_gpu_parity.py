@@ -1,0 +1,281 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Small cases run the oracle on every row / output; the full-size workloads run
+in the same launch configuration the benchmark times and are checked on
+sampled rows and sampled (sequence, kv head) outputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity import check_decode, check_key_value_records, read_records
+from rotated_codebook_kv_gb300 import Codec
+from rotated_codebook_kv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _codec_pair(w, layer=0):
+    seed = w.codec_seed(layer)
+    return (Codec(w.head_dim, w.k_bits, w.v_bits, w.group, seed),
+            O.Oracle(w.head_dim, w.k_bits, w.v_bits, w.group, seed))
+
+
+def _compress(codec, w, b, fill=0xA5):
+    kc, vc = codec.alloc_cache(b.num_blocks, w.num_kv_heads, w.page_size, fill=fill)
+    codec.compress_kv(b.k, b.v, b.slot_mapping, kc, vc, w.page_size, b.num_blocks)
+    torch.cuda.synchronize()
+    return kc, vc
+
+
+def _rows(t):  # [T, H, d] bf16 tensor -> [T*H, d] uint16
+    return W.as_u16(t).reshape(-1, t.shape[-1])
+
+
+def _check_rows(ora, w, b, kc, vc, token_idx=None):
+    """Compare the records of tokens `token_idx` (all heads) with the oracle."""
+    geo = ora.geometry(w.page_size)
+    sm = b.slot_mapping.cpu().numpy()
+    if token_idx is None:
+        token_idx = np.nonzero(sm >= 0)[0]
+    token_idx = np.asarray(token_idx)
+    slots = sm[token_idx]
+    rec = read_records(kc.cpu().numpy(), vc.cpu().numpy(), geo, w.head_dim, w.k_bits, w.v_bits, w.group,
+                       w.page_size, w.num_kv_heads, slots)
+    tk = torch.as_tensor(token_idx, device=b.k.device)
+    k_rows = _rows(b.k[tk])
+    v_rows = _rows(b.v[tk])
+    return check_key_value_records(ora, k_rows, v_rows, rec)
+
+
+def _decode_gpu(codec, w, b, kc, vc, splits=0):
+    out = codec.decode_attention(b.q, kc, vc, b.block_table, b.seq_lens, w.num_kv_heads, w.page_size,
+                                 b.num_blocks, b.sm_scale, splits=splits)
+    torch.cuda.synchronize()
+    return W.as_u16(out)
+
+
+def _decode_oracle(ora, w, b, kc_np, vc_np, jobs=None):
+    return ora.decode(W.as_u16(b.q), kc_np, vc_np, b.block_table.cpu().numpy(), b.seq_lens.cpu().numpy(),
+                      w.num_kv_heads, w.page_size, b.sm_scale, mode=1, jobs=jobs)
+
+
+def _rows_of_jobs(w, jobs):
+    G = w.num_q_heads // w.num_kv_heads
+    return [(bb, kvh * G + g) for bb, kvh in jobs for g in range(G)]
+
+
+# --------------------------------------------------------------------------- #
+# Parameters                                                                    #
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("d,kb,seed", [(128, 3, 0), (256, 4, 5), (128, 2, 7)])
+def test_parameter_tables_match_oracle(d, kb, seed):
+    lib = Codec(d, kb, 4, 32, seed).export_params()
+    ref = O.Oracle(d, kb, 4, 32, seed).params()
+    for name in ("Pi", "S", "centroids", "thresholds"):
+        a = lib[name].astype(np.float64)
+        r = ref[name]
+        # the library rounds its double tables to fp32 once
+        assert np.all(np.abs(a - r) <= np.abs(r) * 2.0 ** -24 + 1e-13), name
+
+
+# --------------------------------------------------------------------------- #
+# Small workloads: every row and every output against the oracle               #
+# --------------------------------------------------------------------------- #
+
+SMALL = {
+    "pr1_tiny": W.pr1_tiny(),
+    "compress_only_small": W.scaled(W.compress_only(), num_tokens=4999, num_blocks=400),
+    "paged_decode_small": W.scaled(W.paged_decode(), batch=4, seq_len_range=(100, 600)),
+    "wide_head_small": W.scaled(W.wide_head_decode(), batch=2, seq_len=700),
+}
+for _kb, _vb in W.LAYER_BIT_PAIRS:
+    SMALL[f"mixed_k{_kb}v{_vb}_small"] = W.scaled(W.long_context_mixed(), batch=2, seq_len=333, layers=1,
+                                                  layer_bits=(), k_bits=_kb, v_bits=_vb)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_compress_and_decode(name):
+    w = SMALL[name]
+    b = W.generate(w, device="cpu")
+    b = W.Batch(**{f: (getattr(b, f).to(DEV) if isinstance(getattr(b, f), torch.Tensor) else getattr(b, f))
+                   for f in b.__dataclass_fields__})
+    codec, ora = _codec_pair(w)
+    kc, vc = _compress(codec, w, b)
+    assert codec.get_status() == 0
+    stats = _check_rows(ora, w, b, kc, vc)
+    # whole-cache bytes: the oracle writes the same pools (same canary fill)
+    geo = ora.geometry(w.page_size)
+    okc = np.full(b.num_blocks * w.num_kv_heads * geo["k_page"], 0xA5, np.uint8)
+    ovc = np.full(b.num_blocks * w.num_kv_heads * geo["v_page"], 0xA5, np.uint8)
+    ora.compress_kv(W.as_u16(b.k), W.as_u16(b.v), b.slot_mapping.cpu().numpy(), w.page_size, b.num_blocks, okc, ovc)
+    assert np.array_equal(vc.cpu().numpy(), ovc)
+    if stats["code_mismatch"] == 0 and stats["norm_ulp"] == 0 and stats.get("sign_mismatch", 0) == 0 \
+            and stats.get("gamma_ulp", 0) == 0:
+        assert np.array_equal(kc.cpu().numpy(), okc)
+    if not w.decode:
+        return
+    kc_np, vc_np = kc.cpu().numpy(), vc.cpu().numpy()
+    out = _decode_gpu(codec, w, b, kc, vc)
+    # (i) on the GPU-written cache: isolates the decode kernel
+    check_decode(out, _decode_oracle(ora, w, b, kc_np, vc_np))
+    # (ii) end to end: oracle's own cache
+    check_decode(out, _decode_oracle(ora, w, b, okc, ovc))
+    assert codec.get_status() == 0
+
+
+@pytest.mark.parametrize("name", ["pr1_tiny", "wide_head_small", "mixed_k2v2_small"])
+def test_dequant_matches_oracle(name):
+    w = SMALL[name]
+    b = W.generate(w, device="cpu")
+    codec, ora = _codec_pair(w)
+    k, v, sm = b.k.to(DEV), b.v.to(DEV), b.slot_mapping.to(DEV)
+    kc, vc = codec.alloc_cache(b.num_blocks, w.num_kv_heads, w.page_size)
+    codec.compress_kv(k, v, sm, kc, vc, w.page_size, b.num_blocks)
+    slots = sm[:: max(1, len(sm) // 97)].contiguous()
+    ko, vo = codec.dequant_kv(kc, vc, w.page_size, b.num_blocks, w.num_kv_heads, slots)
+    torch.cuda.synchronize()
+    rk, rv = ora.dequant_slots(kc.cpu().numpy(), vc.cpu().numpy(), w.page_size, w.num_kv_heads, slots.cpu().numpy())
+    for got, ref in ((ko, rk), (vo, rv)):
+        g = O.bf16_to_double(W.as_u16(got))
+        ax = np.abs(ref)
+        ulp = 2.0 ** (np.floor(np.log2(np.where(ax > 0, ax, 1.0))) - 7)
+        assert np.all(np.abs(g - ref) <= ulp + 1e-5)
+
+
+# --------------------------------------------------------------------------- #
+# Decode edge cases                                                             #
+# --------------------------------------------------------------------------- #
+
+def _small_case(seq_lens, w=None):
+    w = w or SMALL["paged_decode_small"]
+    w = W.scaled(w, batch=len(seq_lens), seq_len_range=None, seq_len=max(max(seq_lens), 1))
+    b = W.generate(w, device=DEV)
+    b.seq_lens = torch.tensor(seq_lens, dtype=torch.int32, device=DEV)
+    return w, b
+
+
+def test_decode_split_counts_agree():
+    w, b = _small_case([1000, 17, 640, 1])
+    codec, ora = _codec_pair(w)
+    kc, vc = _compress(codec, w, b)
+    raw = [_decode_gpu(codec, w, b, kc, vc, splits=s) for s in (1, 2, 7, 64)]
+    outs = [O.bf16_to_double(r) for r in raw]
+    ax = np.abs(outs[0])
+    ulp = 2.0 ** (np.floor(np.log2(np.where(ax > 0, ax, 1.0))) - 7)
+    for o in outs[1:]:
+        assert np.all(np.abs(o - outs[0]) <= ulp)
+    ref = _decode_oracle(ora, w, b, kc.cpu().numpy(), vc.cpu().numpy())
+    for r in raw:
+        check_decode(r, ref)
+
+
+def test_decode_empty_and_single_token():
+    w, b = _small_case([0, 1, 5])
+    codec, ora = _codec_pair(w)
+    kc, vc = _compress(codec, w, b)
+    out = O.bf16_to_double(_decode_gpu(codec, w, b, kc, vc))
+    assert not out[0].any()
+    slot = int(b.block_table[1, 0]) * w.page_size
+    _, V = ora.dequant_slots(kc.cpu().numpy(), vc.cpu().numpy(), w.page_size, w.num_kv_heads, [slot])
+    G = w.num_q_heads // w.num_kv_heads
+    ref = np.stack([V[0, h // G] for h in range(w.num_q_heads)])
+    assert np.array_equal(out[1], O.bf16_to_double(O.bf16_from_double(ref)))
+
+
+def test_bad_ids_set_status_and_write_nothing_out_of_bounds():
+    w = SMALL["paged_decode_small"]
+    b = W.generate(w, device=DEV)
+    codec, _ = _codec_pair(w)
+    kpb, vpb = codec.cache_layout(w.page_size)
+    guard = 4096
+    kbig = torch.full((guard * 2 + b.num_blocks * w.num_kv_heads * kpb,), 0x5A, dtype=torch.uint8, device=DEV)
+    vbig = torch.full((guard * 2 + b.num_blocks * w.num_kv_heads * vpb,), 0x5A, dtype=torch.uint8, device=DEV)
+    kc, vc = kbig[guard:-guard], vbig[guard:-guard]
+    sm = b.slot_mapping.clone()
+    sm[3] = b.num_blocks * w.page_size + 5     # out of range
+    sm[4] = -1                                  # skipped
+    codec.compress_kv(b.k, b.v, sm, kc, vc, w.page_size, b.num_blocks)
+    assert codec.get_status() & 0x1
+    assert codec.get_status() == 0  # cleared by the read
+    for big in (kbig, vbig):
+        assert torch.all(big[:guard] == 0x5A) and torch.all(big[-guard:] == 0x5A)
+    bt = b.block_table.clone()
+    bt[0, 0] = b.num_blocks + 3
+    out = codec.decode_attention(b.q, kc, vc, bt, b.seq_lens, w.num_kv_heads, w.page_size, b.num_blocks, b.sm_scale)
+    st = codec.get_status()
+    assert st & 0x2
+    assert torch.isfinite(out.float()).all()
+    sl = b.seq_lens.clone()
+    sl[1] = bt.shape[1] * w.page_size + 100     # longer than its block table
+    codec.decode_attention(b.q, kc, vc, b.block_table, sl, w.num_kv_heads, w.page_size, b.num_blocks, b.sm_scale)
+    assert codec.get_status() & 0x4
+
+
+def test_runs_are_deterministic_and_graph_capturable():
+    w = SMALL["paged_decode_small"]
+    b = W.generate(w, device=DEV)
+    codec, _ = _codec_pair(w)
+    kc1, vc1 = _compress(codec, w, b)
+    kc2, vc2 = _compress(codec, w, b)
+    assert torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
+    splits = codec.decode_splits(w.batch, w.num_kv_heads, b.block_table.shape[1], w.page_size)
+    ws = codec.workspace(w.batch, w.num_q_heads, splits)
+    out = torch.empty_like(b.q)
+    ref = codec.decode_attention(b.q, kc1, vc1, b.block_table, b.seq_lens, w.num_kv_heads, w.page_size,
+                                 b.num_blocks, b.sm_scale, splits=splits, workspace=ws).clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        codec.decode_attention(b.q, kc1, vc1, b.block_table, b.seq_lens, w.num_kv_heads, w.page_size,
+                               b.num_blocks, b.sm_scale, splits=splits, workspace=ws, out=out, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
+# --------------------------------------------------------------------------- #
+# Full-size workloads, benchmark launch configuration, sampled checks          #
+# --------------------------------------------------------------------------- #
+
+def _full_case(w, layer, n_rows=3000, n_jobs=6, seed=0):
+    lw = w.for_layer(layer)
+    b = W.generate(lw, layer=layer, device=DEV)
+    codec, ora = _codec_pair(lw, layer)
+    kc, vc = _compress(codec, lw, b, fill=0)
+    assert codec.get_status() == 0
+    rng = np.random.default_rng(seed)
+    T = b.num_tokens
+    tok = np.unique(np.concatenate([rng.integers(0, T, n_rows), [0, T - 1]]))
+    _check_rows(ora, lw, b, kc, vc, tok)
+    if lw.decode:
+        out = _decode_gpu(codec, lw, b, kc, vc)
+        jobs = [(int(rng.integers(0, lw.batch)), int(rng.integers(0, lw.num_kv_heads))) for _ in range(n_jobs)]
+        jobs = sorted(set(jobs))
+        ref = _decode_oracle(ora, lw, b, kc.cpu().numpy(), vc.cpu().numpy(), jobs=jobs)
+        rows = _rows_of_jobs(lw, jobs)
+        idx = tuple(np.array(rows).T)
+        check_decode(out[idx], ref[idx])
+    del kc, vc, b
+    torch.cuda.empty_cache()
+
+
+def test_full_compress_only():
+    _full_case(W.compress_only(), 0)
+
+
+def test_full_paged_decode():
+    _full_case(W.paged_decode(), 0)
+
+
+def test_full_wide_head_decode():
+    _full_case(W.wide_head_decode(), 0)
+
+
+@pytest.mark.parametrize("layer", range(8))
+def test_full_long_context_mixed(layer):
+    _full_case(W.long_context_mixed(), layer, n_rows=1500, n_jobs=3)
