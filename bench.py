@@ -205,7 +205,7 @@ class Layer:
 def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = W.long_context_mixed(seed=rank)
+    w = rank_workload(rank)
     layers = [Layer(w, l, dev, pinned_host=not args.no_e2e) for l in range(w.layers)]
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
@@ -253,7 +253,7 @@ def run_gpu(args, rank, world, local_rank):
     clk = clocks.summary()
 
     step_bytes = sum(L.c_bytes + L.d_bytes for L in layers)
-    value = world * step_bytes / (elapsed * 1e-3) / 1e9
+    value = aggregate_value(step_bytes, elapsed, world)
     c_bytes = sum(L.c_bytes for L in layers)
     d_bytes = sum(L.d_bytes for L in layers)
     c_time = sum(c_ms) / args.steps * 1e-3
@@ -424,6 +424,16 @@ def run_reference(args):
 # --------------------------------------------------------------------------- #
 # Distributed plumbing                                                           #
 # --------------------------------------------------------------------------- #
+
+def rank_workload(rank):
+    """Every rank gets the same shapes and per-layer bits (those of seed 0); only the data seed differs."""
+    return W.scaled(W.long_context_mixed(seed=0), seed=rank)
+
+
+def aggregate_value(step_bytes, step_ms, world):
+    """Whole-job GB/s: every rank moves step_bytes per step; the step takes the slowest rank's time."""
+    return world * step_bytes / (step_ms * 1e-3) / 1e9
+
 
 def barrier(world):
     if world > 1:
