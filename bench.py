@@ -205,7 +205,7 @@ class Layer:
 def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = rank_workload(rank)
+    w = rank_workload(rank, args.layers, args.batch)
     layers = [Layer(w, l, dev, pinned_host=not args.no_e2e) for l in range(w.layers)]
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
@@ -425,9 +425,18 @@ def run_reference(args):
 # Distributed plumbing                                                           #
 # --------------------------------------------------------------------------- #
 
-def rank_workload(rank):
-    """Every rank gets the same shapes and per-layer bits (those of seed 0); only the data seed differs."""
-    return W.scaled(W.long_context_mixed(seed=0), seed=rank)
+def rank_workload(rank, layers=None, batch=None):
+    """Every rank gets the same shapes and per-layer bits (those of seed 0); only the data seed differs.
+
+    layers / batch shrink the workload for profiling captures only; the
+    benchmark line itself always uses the full workload."""
+    w = W.long_context_mixed(seed=0)
+    kw = {"seed": rank}
+    if layers:
+        kw.update(layers=layers, layer_bits=w.layer_bits[:layers])
+    if batch:
+        kw.update(batch=batch)
+    return W.scaled(w, **kw)
 
 
 def aggregate_value(step_bytes, step_ms, world):
@@ -459,6 +468,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=None, help="profiling only: first N layers")
+    ap.add_argument("--batch", type=int, default=None, help="profiling only: fewer sequences")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", 0))

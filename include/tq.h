@@ -61,6 +61,7 @@ typedef enum {
 #define TQ_DEVERR_SLOT_RANGE  0x1u  /* compress: slot >= num_blocks * page_size (token skipped)   */
 #define TQ_DEVERR_BLOCK_RANGE 0x2u  /* decode/dequant: block id < 0 or >= num_blocks (page skipped) */
 #define TQ_DEVERR_SEQ_RANGE   0x4u  /* decode: seq_len > max_blocks_per_seq * page_size (clamped)  */
+#define TQ_DEVERR_TIMEOUT     0x8u  /* compress: a tensor-core completion wait timed out (CTA stopped) */
 
 /*
  * tq_init -- build the codec parameters for one (head_dim, k_bits, v_bits,
@@ -129,8 +130,8 @@ tq_status tq_dequant_kv(tq_handle h, const uint8_t *k_cache, const uint8_t *v_ca
 
 /*
  * tq_decode_splits -- the split count tq_decode_attention uses when called
- * with splits = 0: enough (sequence, kv head, split) work units for two waves
- * over the device's SMs, at least one page per split, at most 64 splits.
+ * with splits = 0: about eight (sequence, kv head, split) work units per SM,
+ * at least one page per split, at most 64 splits.
  */
 int tq_decode_splits(tq_handle h, int batch, int num_kv_heads, int max_blocks_per_seq, int page_size);
 

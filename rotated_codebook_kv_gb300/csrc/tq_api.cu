@@ -8,6 +8,7 @@
 #include <string>
 #include <vector>
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "tq.h"
@@ -68,7 +69,10 @@ tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed
 
     const int d = head_dim;
     const size_t dd = static_cast<size_t>(d) * d;
-    std::vector<float> host(4 * dd);
+    // fp32 tables: Pi, Pi^T, S, S^T, M_hi, M_lo (M = S Pi in double), then the
+    // fp16 tensor-core operand image (d = 128) and the status word.
+    const size_t img_bytes = (d == 128) ? 4 * dd * sizeof(uint16_t) : 0;
+    std::vector<float> host(6 * dd);
     for (int i = 0; i < d; ++i)
         for (int j = 0; j < d; ++j) {
             const size_t a = static_cast<size_t>(i) * d + j, t = static_cast<size_t>(j) * d + i;
@@ -76,7 +80,29 @@ tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed
             host[dd + t] = static_cast<float>(ht.Pi[a]);
             host[2 * dd + a] = static_cast<float>(ht.S[a]);
             host[3 * dd + t] = static_cast<float>(ht.S[a]);
+            double m = 0.0;
+            for (int q = 0; q < d; ++q) m += ht.S[static_cast<size_t>(i) * d + q] * ht.Pi[static_cast<size_t>(q) * d + j];
+            const float mh = static_cast<float>(m);
+            host[4 * dd + a] = mh;
+            host[5 * dd + a] = static_cast<float>(m - static_cast<double>(mh));
         }
+    std::vector<uint16_t> img(img_bytes / 2);
+    if (d == 128) {
+        // B operands (rows = output index i, K = input index j), core matrices of
+        // 8 rows x 8 halfs, row groups of 16 k-chunks: Pi 2^10 and S 2^12 as fp16 hi + lo.
+        auto put = [&](int term, int i, int j, double x) {
+            const size_t off = ((static_cast<size_t>(i >> 3) * (d >> 3) + (j >> 3)) * 128 + (i & 7) * 16 + (j & 7) * 2) / 2;
+            const __half h = __float2half_rn(static_cast<float>(x));
+            const __half l = __float2half_rn(static_cast<float>(x - static_cast<double>(__half2float(h))));
+            img[(2 * term) * dd + off] = __half_as_ushort(h);
+            img[(2 * term + 1) * dd + off] = __half_as_ushort(l);
+        };
+        for (int i = 0; i < d; ++i)
+            for (int j = 0; j < d; ++j) {
+                put(0, i, j, ht.Pi[static_cast<size_t>(i) * d + j] * 1024.0);
+                put(1, i, j, ht.S[static_cast<size_t>(i) * d + j] * 4096.0);
+            }
+    }
     tq_ctx *c = new tq_ctx();
     cudaError_t e = cudaGetDevice(&c->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
@@ -84,14 +110,16 @@ tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed
         delete c;
         return cuda_fail(e, "tq_init: device query");
     }
-    e = cudaMalloc(&c->dev_tables, 4 * dd * sizeof(float) + 256);
+    e = cudaMalloc(&c->dev_tables, 6 * dd * sizeof(float) + img_bytes + 256);
     if (e != cudaSuccess) {
         delete c;
         return fail(TQ_ERR_OOM, "tq_init: cudaMalloc: %s", cudaGetErrorString(e));
     }
     float *base = static_cast<float *>(c->dev_tables);
-    e = cudaMemcpy(base, host.data(), 4 * dd * sizeof(float), cudaMemcpyHostToDevice);
-    unsigned *status = reinterpret_cast<unsigned *>(base + 4 * dd);
+    e = cudaMemcpy(base, host.data(), 6 * dd * sizeof(float), cudaMemcpyHostToDevice);
+    char *img_dev = reinterpret_cast<char *>(base + 6 * dd);
+    if (e == cudaSuccess && img_bytes) e = cudaMemcpy(img_dev, img.data(), img_bytes, cudaMemcpyHostToDevice);
+    unsigned *status = reinterpret_cast<unsigned *>(img_dev + img_bytes);
     if (e == cudaSuccess) e = cudaMemset(status, 0, 256);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -116,7 +144,11 @@ tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed
     k.PiT = base + dd;
     k.S = base + 2 * dd;
     k.ST = base + 3 * dd;
+    k.M_hi = base + 4 * dd;
+    k.M_lo = base + 5 * dd;
+    k.tc_image = img_bytes ? img_dev : nullptr;
     k.status = status;
+    k.num_sms = c->num_sms;
     c->seed = seed;
     *out = c;
     return TQ_OK;
@@ -200,7 +232,7 @@ int tq_decode_splits(tq_handle h, int batch, int num_kv_heads, int max_blocks_pe
 {
     if (!h || batch < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 || page_size < 1) return 1;
     const int units = batch * num_kv_heads;
-    int splits = (2 * h->num_sms + units - 1) / units;
+    int splits = (8 * h->num_sms + units - 1) / units;  // about eight CTAs per SM
     if (splits > 64) splits = 64;
     if (splits > max_blocks_per_seq) splits = max_blocks_per_seq;
     return splits < 1 ? 1 : splits;

@@ -428,7 +428,7 @@ cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *
                             int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
                             int64_t num_blocks, cudaStream_t st)
 {
-    if (c.d == 128) return launch_compress_d<128>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+    if (c.d == 128) return launch_compress_tc(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, c.num_sms, st);
     return launch_compress_d<256>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
 }
 

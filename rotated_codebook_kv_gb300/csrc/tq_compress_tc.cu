@@ -1,0 +1,726 @@
+// tq_compress_tc.cu -- key + value compression with the rotation and the QJL
+// projection on the tensor cores (tcgen05, accumulators in tensor memory), d = 128.
+//
+// Method (turbo-attn "How it works"; 0xsero/turboquant "Compression Pipeline",
+// "Value Compression"; brightcoding blog "Example 4"): see tq_compress.cu.
+//
+// Tile = 128 token-heads; one persistent CTA per SM, 256 threads.
+//  1. Keys are loaded, their norm taken in fp32 (sum of exact squares), and
+//     converted exactly to fp16 after a power-of-two scale 2^e per row.
+//  2. Y = K' (Pi 2^10)^T on the tensor cores: Pi 2^10 is split into fp16 high
+//     and low parts, two MMA terms, ~22-bit operands, fp32 accumulation.
+//  3. Epilogue, one thread per row (its TMEM lane): z = Y * sqrt(d) / (n 2^(10+e)),
+//     codes from a bin table, residual r = z - c[code], gamma = ||r|| / sqrt(d);
+//     r 2^12 is split into fp16 high / low parts for the next MMA.
+//  4. QJL: P = (R 2^12)(S 2^12)^T, three MMA terms (hi.hi, hi.lo, lo.hi); the
+//     sign of P is the sign of S r.
+//  5. Values (all warps, overlapping the MMAs) as in tq_compress.cu.
+//  6. Decisions within a guard band of a threshold, a sign boundary or a bf16
+//     rounding midpoint of gamma are re-taken exactly: a code or a sign by an
+//     O(d) compensated dot product (z_j = sqrt(d) (Pi_j . k) / n,
+//     p_i = sqrt(d) (M_i . k) / n - S_i . c with M = S Pi in double-fp32), and
+//     a row whose code flips or whose gamma sits near a midpoint is redone
+//     entirely in compensated arithmetic.
+// Every mbarrier wait is bounded; a timeout sets TQ_DEVERR_TIMEOUT, the CTA
+// stops, waits (bounded) for its tensor-core work and frees its TMEM.
+#include <cuda_runtime.h>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+#include "tq_umma.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int D = 128;
+constexpr int TM = 128;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr float kCodeGuard = 1e-5f;   // z units
+constexpr float kSignGuard = 2e-5f;   // |p| / ||r||
+constexpr float kGammaGuard = 2e-6f;  // relative distance of gamma to a bf16 rounding midpoint
+constexpr long long kWaitLimit = 2000000000LL;  // cycles (~1 s)
+
+// Shared-memory map (bytes).
+constexpr uint32_t kOffPiH = 0, kOffPiL = 32768, kOffSH = 65536, kOffSL = 98304;  // B operands (fp16)
+constexpr uint32_t kOffTA = 131072;  // K' (fp16) then R hi
+constexpr uint32_t kOffTB = 163840;  // R lo
+constexpr uint32_t kOffCodes = 196608;             // [TM][16] u32 packed key codes
+constexpr uint32_t kOffSigns = kOffCodes + TM * 64;  // [TM][4] u32 sign bits
+constexpr uint32_t kOffMask = kOffSigns + TM * 16;   // [TM][8] u32: code guard mask (4), sign guard mask (4)
+constexpr uint32_t kOffRow = kOffMask + TM * 32;     // per-row scalars
+constexpr uint32_t kOffScratch = kOffRow + TM * 32;  // [kWarps][D] doubles for the exact path
+constexpr uint32_t kOffBins = kOffScratch + kWarps * D * 8;  // [1024] u16 code-bin table
+constexpr uint32_t kOffBook = kOffBins + 2048;       // [16] centroids, [16] thresholds
+constexpr uint32_t kOffMisc = kOffBook + 128;
+constexpr uint32_t kSmemBytes = kOffMisc + 128;
+
+constexpr uint32_t kSBO = (D / 8) * 128;  // 2048
+constexpr uint32_t kIdesc = umma::idesc_f16(128, 128);
+constexpr float kBinScale = 64.f, kBinOrigin = 8.f;  // bin = floor((z + 8) * 64), 1024 bins
+
+struct RowInfo {     // 32 bytes per row
+    int64_t dst;     // record index (block * Hkv + head) or -1
+    int off;         // offset inside the page
+    int flag;        // bit0 code guard, bit1 sign guard, bit2 redo row, bit3 zero key
+    float zscale;    // sqrt(d) / (n 2^(10+e)) applied to Y
+    float rn;        // ||r|| in z units
+    uint32_t n16g16; // bf16 norm | bf16 gamma << 16
+    int pad;
+};
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b)
+{
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Compensated dot product of a global fp32 row with the warp's fp32 key copy, then
+// combined over the warp.  Returns hi + lo as a double.
+__device__ double warp_dot_df(const float *__restrict__ a, const float *kw)
+{
+    const int lane = threadIdx.x & 31;
+    float s = 0.f, c = 0.f;
+#pragma unroll
+    for (int m = 0; m < D / 32; ++m) dot2_step(s, c, __ldg(a + lane + 32 * m), kw[lane + 32 * m]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o), c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        float t, e;
+        two_sum(s, s2, t, e);
+        s = t;
+        c = __fadd_rn(c, __fadd_rn(c2, e));
+    }
+    return static_cast<double>(s) + static_cast<double>(c);
+}
+
+template <int KB>
+__device__ __forceinline__ uint32_t get_code(const uint32_t *w, int j)
+{
+    const int o = j * KB;
+    const uint32_t lo = w[o >> 5];
+    const uint32_t hi = ((o & 31) + KB > 32) ? w[(o >> 5) + 1] : 0u;
+    return __funnelshift_r(lo, hi, o & 31) & ((1u << KB) - 1u);
+}
+
+template <int KB>
+__device__ __forceinline__ void set_code(uint32_t *w, int j, uint32_t v)
+{
+    for (int b = 0; b < KB; ++b) {
+        const int o = j * KB + b;
+        const uint32_t bit = 1u << (o & 31);
+        if ((v >> b) & 1u) w[o >> 5] |= bit;
+        else w[o >> 5] &= ~bit;
+    }
+}
+
+// The whole key row in compensated arithmetic, by one warp (see tq_compress.cu).
+template <int KB>
+__device__ void exact_row(const Codec &C, const float *kw, double n_sc, uint32_t *codes, uint32_t *signs,
+                          uint32_t *n16g16, double *scratch, double n_true)
+{
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    float yh[E], yl[E];
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        const int i = lane + 32 * m;
+        float hs = 0.f, hc = 0.f;
+        for (int j = 0; j < D; ++j) dot2_step(hs, hc, __ldg(C.PiT + j * D + i), kw[j]);
+        yh[m] = hs;
+        yl[m] = hc;
+    }
+    __syncwarp();  // scratch aliases the key copy read above
+    const double zscale = sqrt(static_cast<double>(D)) / n_sc;
+    const int nthr = (1 << KB) - 1;
+    double rr = 0.0;
+    uint32_t cd[E];
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        const int i = lane + 32 * m;
+        const double z = (static_cast<double>(yh[m]) + static_cast<double>(yl[m])) * zscale;
+        int code = 0;
+        for (int t = 0; t < nthr; ++t) code += (static_cast<double>(C.thresholds[t]) <= z);
+        cd[m] = code;
+        const double r = z - static_cast<double>(C.centroids[code]);
+        scratch[i] = r;
+        rr += r * r;
+    }
+    rr = warp_sum(rr);
+    // rewrite the packed codes: lane-parallel over words
+    __syncwarp();
+    for (int w = lane; w < D * KB / 32; w += 32) codes[w] = 0u;
+    __syncwarp();
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        const int i = lane + 32 * m;
+        for (int b = 0; b < KB; ++b)
+            if ((cd[m] >> b) & 1u) atomicOr(&codes[(i * KB + b) >> 5], 1u << ((i * KB + b) & 31));
+    }
+    const uint32_t g16 = C.qjl ? double_to_bf16_bits(sqrt(rr) / sqrt(static_cast<double>(D))) : 0u;
+    if (lane == 0) *n16g16 = double_to_bf16_bits(n_true) | (g16 << 16);
+    __syncwarp();
+    if (!C.qjl) return;
+    // residual as float hi + lo pairs (the inner loop then needs no fp64)
+    float2 *rp = reinterpret_cast<float2 *>(scratch);
+    float2 mine[E];
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        const double rj = scratch[lane + 32 * m];
+        const float rh = static_cast<float>(rj);
+        mine[m] = make_float2(rh, static_cast<float>(rj - static_cast<double>(rh)));
+    }
+    __syncwarp();
+#pragma unroll
+    for (int m = 0; m < E; ++m) rp[lane + 32 * m] = mine[m];
+    __syncwarp();
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        const int i = lane + 32 * m;
+        float ps = 0.f, pc = 0.f;
+        for (int j = 0; j < D; ++j) {
+            const float2 r2 = rp[j];
+            const float sv = __ldg(C.ST + j * D + i);
+            dot2_step(ps, pc, sv, r2.x);
+            pc = __fmaf_rn(sv, r2.y, pc);
+        }
+        const uint32_t bits = __ballot_sync(0xffffffffu, __fadd_rn(ps, pc) >= 0.f);
+        if (lane == 0) signs[m] = bits;
+    }
+    __syncwarp();
+}
+
+template <int KB>
+__global__ void __launch_bounds__(kThreads, 1)
+compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
+                   int64_t rows, int Hkv, int64_t ks, int64_t vs, const int64_t *__restrict__ slots,
+                   uint8_t *__restrict__ kc, uint8_t *__restrict__ vc, int64_t num_blocks, int num_tiles)
+{
+    constexpr int NKW = D * KB / 32;  // code words per row
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint32_t *scodes = reinterpret_cast<uint32_t *>(smem + kOffCodes);
+    uint32_t *ssigns = reinterpret_cast<uint32_t *>(smem + kOffSigns);
+    uint32_t *smask = reinterpret_cast<uint32_t *>(smem + kOffMask);
+    RowInfo *rinfo = reinterpret_cast<RowInfo *>(smem + kOffRow);
+    double *scratch_all = reinterpret_cast<double *>(smem + kOffScratch);
+    uint16_t *bins = reinterpret_cast<uint16_t *>(smem + kOffBins);
+    float *s_cent = reinterpret_cast<float *>(smem + kOffBook);
+    float *s_thr = s_cent + 16;
+    uint64_t *mbarY = reinterpret_cast<uint64_t *>(smem + kOffMisc);
+    uint64_t *mbarP = mbarY + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc + 16);
+    int *s_abort = reinterpret_cast<int *>(smem + kOffMisc + 20);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float sqrtd = sqrtf(static_cast<float>(D));
+    const int nthr = (1 << KB) - 1;
+
+    // ---- once per CTA: B operands, code bins, barriers, tensor memory ----
+    {
+        const uint4 *img = reinterpret_cast<const uint4 *>(C.tc_image);
+        uint4 *dst = reinterpret_cast<uint4 *>(smem);
+        for (int e = tid; e < 131072 / 16; e += kThreads) dst[e] = __ldg(img + e);
+        for (int b = tid; b < 1024; b += kThreads) {
+            const float lo = static_cast<float>(b) / kBinScale - kBinOrigin;
+            const float hi = static_cast<float>(b + 1) / kBinScale - kBinOrigin;
+            int below = 0, idx = -1;
+            for (int t = 0; t < nthr; ++t) {
+                const float th = C.thresholds[t];
+                if (th < lo - 2.f * kCodeGuard) ++below;
+                else if (th <= hi + 2.f * kCodeGuard) idx = t;  // at most one threshold this close to a bin
+            }
+            bins[b] = static_cast<uint16_t>(below | (idx >= 0 ? (0x10 | (idx << 8)) : 0));
+        }
+        if (tid < 16) {
+            s_cent[tid] = C.centroids[tid];
+            s_thr[tid] = C.thresholds[tid];
+        }
+        if (tid == 0) {
+            umma::mbar_init(mbarY, 1);
+            umma::mbar_init(mbarP, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            *s_abort = 0;
+        }
+        if (warp == 0) umma::tmem_alloc(tslot, 256);
+        umma::fence_proxy_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+    }
+    const uint32_t tmem = *tslot;
+    const uint32_t tY = tmem, tP = tmem + 128;
+    const uint32_t sbase = umma::smem_u32(smem);
+    uint32_t phase = 0;
+
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const int64_t r0 = static_cast<int64_t>(tile) * TM;
+        // ---- slots ----
+        if (tid < TM) {
+            const int64_t r = r0 + tid;
+            RowInfo ri;
+            ri.dst = -1;
+            ri.off = 0;
+            ri.flag = 0;
+            ri.zscale = 0.f;
+            ri.rn = 0.f;
+            ri.n16g16 = 0;
+            ri.pad = 0;
+            if (r < rows) {
+                const int64_t t = r / Hkv;
+                const int h = static_cast<int>(r - t * Hkv);
+                const int64_t s = slots[t];
+                if (s >= 0) {
+                    if (s < num_blocks * G.P) {
+                        const int64_t blk = s / G.P;
+                        ri.off = static_cast<int>(s - blk * G.P);
+                        ri.dst = blk * Hkv + h;
+                    } else {
+                        atomicOr(C.status, TQ_DEVERR_SLOT_RANGE);
+                    }
+                }
+            }
+            rinfo[tid] = ri;
+        }
+        __syncthreads();
+        // ---- keys: norm, power-of-two scale, exact fp16 conversion into tile A ----
+        // warp handles 8-row groups; lane: row 8g + (lane & 7), chunks (lane >> 3) + 4 i
+        for (int grp = warp; grp < TM / 8; grp += kWarps) {
+            const int rl = 8 * grp + (lane & 7);
+            const int64_t r = r0 + rl;
+            float x[4][8];
+            float mx = 0.f;
+            const bool live = (r < rows) && rinfo[rl].dst >= 0;
+            const uint16_t *src = nullptr;
+            if (live) {
+                const int64_t t = r / Hkv;
+                src = kin + t * ks + static_cast<int64_t>(r - t * Hkv) * D;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = (lane >> 3) + 4 * i;
+                uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                if (live) u = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+                x[i][0] = bf16_to_float(u.x & 0xffffu); x[i][1] = bf16_to_float(u.x >> 16);
+                x[i][2] = bf16_to_float(u.y & 0xffffu); x[i][3] = bf16_to_float(u.y >> 16);
+                x[i][4] = bf16_to_float(u.z & 0xffffu); x[i][5] = bf16_to_float(u.z >> 16);
+                x[i][6] = bf16_to_float(u.w & 0xffffu); x[i][7] = bf16_to_float(u.w >> 16);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(x[i][e]));
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            int ex = 0;
+            if (mx > 0.f) frexpf(mx, &ex);  // mx in [2^(ex-1), 2^ex)
+            // |k'| < 2^15; keys too small for a finite fp32 scale are redone exactly
+            const bool tiny = (15 - ex) > 126;
+            const float sc = ldexpf(1.f, tiny ? 126 : 15 - ex);
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const float a = x[i][e] * sc, b = x[i][e + 1] * sc;
+                    ss = fmaf(a, a, ss);
+                    ss = fmaf(b, b, ss);
+                    pk[e / 2] = pack_h2(a, b);
+                }
+                const int c = (lane >> 3) + 4 * i;
+                *reinterpret_cast<uint4 *>(smem + kOffTA + umma::core_offset(rl, 8 * c, D)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+            if (lane < 8) {
+                RowInfo &ri = rinfo[rl];
+                if (mx == 0.f) {
+                    ri.flag = 8;  // zero key
+                } else {
+                    if (tiny) ri.flag |= 4;
+                    const float nsc = sqrtf(ss);  // ||k|| 2^(15-ex)
+                    ri.zscale = sqrtd / (nsc * 1024.f);
+                    ri.n16g16 = float_to_bf16_bits(ldexpf(nsc, ex - 15));
+                }
+            }
+        }
+        umma::fence_proxy_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        // ---- rotation MMAs: Y = K' (Pi_lo + Pi_hi)^T ----
+        if (tid == 0) {
+#pragma unroll 1
+            for (int term = 0; term < 2; ++term) {
+                const uint32_t boff = term == 0 ? kOffPiL : kOffPiH;
+#pragma unroll 1
+                for (int s = 0; s < D / 16; ++s) {
+                    const uint64_t a = umma::make_desc(sbase + kOffTA + 256 * s, 128, kSBO);
+                    const uint64_t b = umma::make_desc(sbase + boff + 256 * s, 128, kSBO);
+                    umma::mma_f16(tY, a, b, kIdesc, (term | s) != 0);
+                }
+            }
+            umma::commit(mbarY);
+        }
+        // ---- values (all warps, while the tensor core runs) ----
+        for (int rl = warp; rl < TM; rl += kWarps) {
+            const int64_t dst = rinfo[rl].dst;
+            if (dst < 0) continue;
+            const int off = rinfo[rl].off;
+            const int64_t r = r0 + rl;
+            const int64_t t = r / Hkv;
+            const int h = static_cast<int>(r - t * Hkv);
+            const uint16_t *vsrc = vin + t * vs + static_cast<int64_t>(h) * D + lane * 4;
+            float x[4];
+            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(vsrc));
+            x[0] = bf16_to_float(u.x & 0xffffu); x[1] = bf16_to_float(u.x >> 16);
+            x[2] = bf16_to_float(u.y & 0xffffu); x[3] = bf16_to_float(u.y >> 16);
+            const int lpg = C.group / 4;
+            float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+            float mxv = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            for (int o = lpg >> 1; o > 0; o >>= 1) {
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                mxv = fmaxf(mxv, __shfl_xor_sync(0xffffffffu, mxv, o));
+            }
+            const int L = (1 << C.v_bits) - 1;
+            float dh, de;
+            two_sum(mxv, -mn, dh, de);
+            const __half s16 = (de == 0.f) ? __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)))
+                                           : __double2half((static_cast<double>(mxv) - static_cast<double>(mn)) / L);
+            const __half z16 = __float2half_rn(mn);
+            const float sv = __half2float(s16), zv = __half2float(z16);
+            uint32_t codebits = 0u;  // this lane's 4 codes, LSB-first
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                int q = 0;
+                if (sv != 0.f) {
+                    float a, ea;
+                    two_sum(x[m], -zv, a, ea);
+                    const float qf = floorf(__fdiv_rn(a, sv) + 0.5f);
+                    q = static_cast<int>(fminf(fmaxf(qf, 0.f), static_cast<float>(L)));
+                    while (q < L && __fadd_rn(__fsub_rn(a, (q + 0.5f) * sv), ea) >= 0.f) ++q;
+                    while (q > 0 && !(__fadd_rn(__fsub_rn(a, (q - 0.5f) * sv), ea) >= 0.f)) --q;
+                }
+                codebits |= static_cast<uint32_t>(q) << (m * C.v_bits);
+            }
+            // gather the lanes' 4*vb-bit pieces into 32-bit words of the bitstream
+            uint8_t *vrec = vc + dst * G.v_page;
+            const int piece = 4 * C.v_bits;  // 8, 12 or 16 bits
+            const int nvw = D * C.v_bits / 32;
+            uint32_t word = 0u;
+            for (int w = 0; w < nvw; ++w) {
+                // lanes whose pieces overlap word w
+                const int l0 = (32 * w) / piece, l1 = (32 * w + 31) / piece;
+                uint32_t acc = 0u;
+                for (int l = l0; l <= l1; ++l) {
+                    const uint32_t pcs = __shfl_sync(0xffffffffu, codebits, l);
+                    const int sh = l * piece - 32 * w;  // may be negative
+                    acc |= sh >= 0 ? (pcs << sh) : (pcs >> (-sh));
+                }
+                if (lane == w) word = acc;
+            }
+            if (lane < nvw)
+                *reinterpret_cast<uint32_t *>(vrec + static_cast<int64_t>(off) * C.v_code_bytes + 4 * lane) = word;
+            if ((lane % lpg) == 0) {
+                const int gi = lane / lpg;
+                const uint32_t meta = static_cast<uint32_t>(__half_as_ushort(s16)) |
+                                      (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
+                *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + static_cast<int64_t>(off) * C.v_meta_bytes + 4 * gi) =
+                    meta;
+            }
+        }
+        // ---- key epilogue 1: codes, residual, gamma (thread = row = TMEM lane) ----
+        if (warp < 4) {
+            const int rl = tid;
+            bool ok = umma::mbar_wait_bounded(mbarY, phase, kWaitLimit);
+            if (!ok) {
+                atomicOr(C.status, TQ_DEVERR_TIMEOUT);
+                *s_abort = 1;
+            }
+            umma::fence_after_sync();
+            const RowInfo ri = rinfo[rl];
+            const bool zero = (ri.flag & 8) != 0;
+            uint32_t cw[NKW];
+#pragma unroll
+            for (int w = 0; w < NKW; ++w) cw[w] = 0u;
+            uint32_t cmask[4] = {0u, 0u, 0u, 0u};
+            float gsq = 0.f;
+#pragma unroll
+            for (int cb = 0; cb < D / 32; ++cb) {
+                float y[32];
+                umma::ld32(tY + (static_cast<uint32_t>(32 * warp) << 16) + 32 * cb, y);
+                float rs[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int i = 32 * cb + j;
+                    const float z = y[j] * ri.zscale;
+                    int bi = static_cast<int>(fmaf(z, kBinScale, kBinOrigin * kBinScale));
+                    bi = min(max(bi, 0), 1023);
+                    const uint32_t bt = bins[bi];
+                    uint32_t code = bt & 0xFu;
+                    if (bt & 0x10u) {
+                        const float th = s_thr[bt >> 8];
+                        code += (z >= th) ? 1u : 0u;
+                        if (fabsf(z - th) < kCodeGuard) cmask[cb] |= 1u << j;
+                    }
+                    if (zero) code = 0u;
+                    const float r = zero ? 0.f : z - s_cent[code];
+                    gsq = fmaf(r, r, gsq);
+                    const int o = i * KB;  // compile-time
+                    cw[o >> 5] |= code << (o & 31);
+                    if ((o & 31) + KB > 32) cw[(o >> 5) + 1] |= code >> (32 - (o & 31));
+                    rs[j] = r * 4096.f;
+                }
+                uint32_t rh[16], rlo[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float h0 = __half2float(__float2half_rn(rs[2 * q]));
+                    const float h1 = __half2float(__float2half_rn(rs[2 * q + 1]));
+                    rh[q] = pack_h2(h0, h1);
+                    rlo[q] = pack_h2(rs[2 * q] - h0, rs[2 * q + 1] - h1);
+                }
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const uint32_t off = umma::core_offset(rl, 32 * cb + 8 * c4, D);
+                    *reinterpret_cast<uint4 *>(smem + kOffTA + off) =
+                        make_uint4(rh[4 * c4], rh[4 * c4 + 1], rh[4 * c4 + 2], rh[4 * c4 + 3]);
+                    *reinterpret_cast<uint4 *>(smem + kOffTB + off) =
+                        make_uint4(rlo[4 * c4], rlo[4 * c4 + 1], rlo[4 * c4 + 2], rlo[4 * c4 + 3]);
+                }
+            }
+            const float rn = sqrtf(gsq);
+            int flag = ri.flag;
+            if (cmask[0] | cmask[1] | cmask[2] | cmask[3]) flag |= 1;
+            uint32_t n16g16 = ri.n16g16;
+            if (C.qjl && !zero) {
+                const float gam = rn / sqrtd;
+                n16g16 |= static_cast<uint32_t>(float_to_bf16_bits(gam)) << 16;
+                // distance of gamma to the nearest bf16 rounding midpoint, relative
+                int ge;
+                const float fr = frexpf(gam, &ge);          // gam = fr 2^ge, fr in [0.5, 1)
+                const float u = fr * 256.f;                  // bf16 keeps 8 significant bits
+                const float dm = fabsf(u - floorf(u) - 0.5f) / u;
+                if (dm < kGammaGuard) flag |= 4;
+            }
+#pragma unroll
+            for (int w = 0; w < NKW; ++w) scodes[rl * 16 + w] = cw[w];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) smask[rl * 8 + w] = cmask[w];
+            rinfo[rl].flag = flag;
+            rinfo[rl].rn = rn;
+            rinfo[rl].n16g16 = n16g16;
+            umma::fence_proxy_async();
+            umma::fence_before_sync();
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            umma::fence_after_sync();
+            if (C.qjl) {
+                // ---- projection MMAs: P = (R_hi + R_lo)(S_hi + S_lo)^T, small terms first ----
+                if (tid == 0 && !*s_abort) {
+                    const uint32_t aoff[3] = {kOffTB, kOffTA, kOffTA};
+                    const uint32_t boff[3] = {kOffSH, kOffSL, kOffSH};
+#pragma unroll 1
+                    for (int term = 0; term < 3; ++term)
+#pragma unroll 1
+                        for (int s = 0; s < D / 16; ++s) {
+                            const uint64_t a = umma::make_desc(sbase + aoff[term] + 256 * s, 128, kSBO);
+                            const uint64_t b = umma::make_desc(sbase + boff[term] + 256 * s, 128, kSBO);
+                            umma::mma_f16(tP, a, b, kIdesc, (term | s) != 0);
+                        }
+                    umma::commit(mbarP);
+                }
+                ok = umma::mbar_wait_bounded(mbarP, phase, kWaitLimit);
+                if (!ok) {
+                    atomicOr(C.status, TQ_DEVERR_TIMEOUT);
+                    *s_abort = 1;
+                }
+                umma::fence_after_sync();
+                const float guard = kSignGuard * rn * 16777216.f;  // P = 2^24 p (z units)
+                uint32_t smk[4];
+#pragma unroll 1
+                for (int cb = 0; cb < D / 32; ++cb) {
+                    float p[32];
+                    umma::ld32(tP + (static_cast<uint32_t>(32 * warp) << 16) + 32 * cb, p);
+                    uint32_t bits = 0u, near = 0u;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        bits |= (p[j] >= 0.f ? 1u : 0u) << j;
+                        near |= (fabsf(p[j]) < guard ? 1u : 0u) << j;
+                    }
+                    if (zero) bits = near = 0u;
+                    ssigns[rl * 4 + cb] = bits;
+                    smask[rl * 8 + 4 + cb] = near;
+                    smk[cb] = near;
+                }
+                if (smk[0] | smk[1] | smk[2] | smk[3]) rinfo[rl].flag = flag | 2;
+            }
+        }
+        phase ^= 1u;
+        __syncthreads();
+        if (*s_abort) break;
+        // ---- exact re-decisions, one warp per flagged row ----
+        for (int rl = warp; rl < TM; rl += kWarps) {
+            const int flag = rinfo[rl].flag;
+            if ((flag & 7) == 0 || (flag & 8) || rinfo[rl].dst < 0) continue;
+            // reload the key row (exact fp32), scaled by a power of two
+            const int64_t r = r0 + rl;
+            const int64_t t = r / Hkv;
+            const uint16_t *src = kin + t * ks + static_cast<int64_t>(r - t * Hkv) * D;
+            double *scratch = scratch_all + warp * D;
+            float *kw = reinterpret_cast<float *>(scratch);
+            float kx[D / 32];
+            float mx = 0.f;
+#pragma unroll
+            for (int m = 0; m < D / 32; ++m) {
+                kx[m] = bf16_to_float(src[lane + 32 * m]);
+                mx = fmaxf(mx, fabsf(kx[m]));
+            }
+            mx = warp_max(mx);
+            int ex;
+            frexpf(mx, &ex);
+            const float sc = ldexpf(1.f, -ex);
+            float s = 0.f, c = 0.f;
+#pragma unroll
+            for (int m = 0; m < D / 32; ++m) {
+                kx[m] *= sc;
+                dot2_step(s, c, kx[m], kx[m]);
+                kw[lane + 32 * m] = kx[m];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float s2 = __shfl_xor_sync(0xffffffffu, s, o), c2 = __shfl_xor_sync(0xffffffffu, c, o);
+                float tt, e;
+                two_sum(s, s2, tt, e);
+                s = tt;
+                c = __fadd_rn(c, __fadd_rn(c2, e));
+            }
+            const double n_sc = sqrt(static_cast<double>(s) + static_cast<double>(c));
+            __syncwarp();
+            uint32_t *cw = scodes + rl * 16;
+            bool redo = (flag & 4) != 0;
+            // codes near a threshold
+            if (!redo && (flag & 1)) {
+                for (int w = 0; w < 4 && !redo; ++w) {
+                    uint32_t m = smask[rl * 8 + w];
+                    while (m && !redo) {
+                        const int j = 32 * w + __ffs(m) - 1;
+                        m &= m - 1;
+                        const double z = warp_dot_df(C.Pi + j * D, kw) * (sqrt(static_cast<double>(D)) / n_sc);
+                        uint32_t code = 0;
+                        for (int tt = 0; tt < nthr; ++tt) code += (static_cast<double>(C.thresholds[tt]) <= z);
+                        if (code != get_code<KB>(cw, j)) redo = true;  // the residual changes: redo the row
+                    }
+                }
+            }
+            if (redo) {
+                exact_row<KB>(C, kw, n_sc, cw, ssigns + rl * 4, &rinfo[rl].n16g16, scratch, ldexp(n_sc, ex));
+                continue;
+            }
+            // signs near zero: p_i = sqrt(d) (M_i . k) / n - S_i . c
+            if (flag & 2) {
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t m = smask[rl * 8 + 4 + w];
+                    while (m) {
+                        const int i = 32 * w + __ffs(m) - 1;
+                        m &= m - 1;
+                        const double mk = warp_dot_df(C.M_hi + i * D, kw) + warp_dot_df(C.M_lo + i * D, kw);
+                        // S_i . c in compensated arithmetic
+                        float sh = 0.f, scc = 0.f;
+#pragma unroll
+                        for (int mm = 0; mm < D / 32; ++mm) {
+                            const int j = lane + 32 * mm;
+                            dot2_step(sh, scc, __ldg(C.S + i * D + j), s_cent[get_code<KB>(cw, j)]);
+                        }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            const float s2 = __shfl_xor_sync(0xffffffffu, sh, o), c2 = __shfl_xor_sync(0xffffffffu, scc, o);
+                            float tt, e;
+                            two_sum(sh, s2, tt, e);
+                            sh = tt;
+                            scc = __fadd_rn(scc, __fadd_rn(c2, e));
+                        }
+                        const double sc_dot = static_cast<double>(sh) + static_cast<double>(scc);
+                        const double p = mk * (sqrt(static_cast<double>(D)) / n_sc) - sc_dot;
+                        if (lane == 0) {
+                            uint32_t &sw = ssigns[rl * 4 + w];
+                            const uint32_t bit = 1u << (i & 31);
+                            sw = (p >= 0.0) ? (sw | bit) : (sw & ~bit);
+                        }
+                        __syncwarp();
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        // ---- key records ----
+        if (tid < TM) {
+            const RowInfo ri = rinfo[tid];
+            if (ri.dst >= 0) {
+                const bool zero = (ri.flag & 8) != 0;
+                uint8_t *krec = kc + ri.dst * G.k_page;
+                uint4 *cd = reinterpret_cast<uint4 *>(krec + static_cast<int64_t>(ri.off) * C.k_code_bytes);
+                const uint32_t *cw = scodes + tid * 16;
+#pragma unroll
+                for (int w = 0; w < NKW; w += 4)
+                    cd[w / 4] = zero ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(cw[w], cw[w + 1], cw[w + 2], cw[w + 3]);
+                *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * ri.off) =
+                    zero ? 0 : static_cast<uint16_t>(ri.n16g16 & 0xffffu);
+                if (C.qjl) {
+                    const uint32_t *sw = ssigns + tid * 4;
+                    *reinterpret_cast<uint4 *>(krec + G.k_sign_off + static_cast<int64_t>(ri.off) * C.k_sign_bytes) =
+                        zero ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(sw[0], sw[1], sw[2], sw[3]);
+                    *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * ri.off) =
+                        zero ? 0 : static_cast<uint16_t>(ri.n16g16 >> 16);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    // ---- teardown: no MMA may still run when TMEM is freed ----
+    if (*s_abort && tid == 0) {
+        umma::mbar_wait_bounded(mbarY, phase ^ 1u, kWaitLimit);
+        umma::mbar_wait_bounded(mbarP, phase ^ 1u, kWaitLimit);
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (warp == 0) umma::tmem_dealloc(tmem, 256);
+}
+
+template <int KB>
+cudaError_t launch_tc_kb(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T, int Hkv,
+                         int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc, int64_t num_blocks,
+                         int num_sms, cudaStream_t st)
+{
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(compress_tc_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    const int64_t rows = T * Hkv;
+    const int tiles = static_cast<int>((rows + TM - 1) / TM);
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    compress_tc_kernel<KB><<<grid, kThreads, kSmemBytes, st>>>(c, pg, k, v, rows, Hkv, ks, vs, slots, kc, vc,
+                                                               num_blocks, tiles);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t compress_tc_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_compress_tc(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
+                               int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
+                               int64_t num_blocks, int num_sms, cudaStream_t st)
+{
+    switch (c.k_bits) {
+    case 2: return launch_tc_kb<2>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, num_sms, st);
+    case 3: return launch_tc_kb<3>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, num_sms, st);
+    default: return launch_tc_kb<4>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, num_sms, st);
+    }
+}
+
+}  // namespace tq

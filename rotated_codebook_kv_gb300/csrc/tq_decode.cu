@@ -105,15 +105,15 @@ template <int D, int KB, int VB>
 cudaError_t launch_dmma(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st)
 {
     const size_t smem = dmma::DecSmem<D, KB>::bytes(pg);
-    static bool attr_set[64] = {};
+    static size_t attr_bytes[64] = {};  // per device: the largest size granted so far
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    if (dev < 0 || dev >= 64 || attr_bytes[dev] < smem) {
         e = cudaFuncSetAttribute(dmma::decode_mma_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 96 * 1024);
+                                 static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+        if (dev >= 0 && dev < 64) attr_bytes[dev] = smem;
     }
     dim3 grid(a.splits, a.Hkv, a.B);
     dmma::decode_mma_kernel<D, KB, VB><<<grid, dmma::kThreads, smem, st>>>(c, pg, a);

@@ -14,7 +14,10 @@
 // Coordinates are permuted inside every 16-wide k-step so that the four
 // B-fragment elements of lane quad m are the four consecutive codes
 // 16s + 4m + {0,1,2,3}: pairs of codes index a shared-memory table of fp16
-// centroid pairs (replicated once per lane, so lookups never conflict).
+// centroid pairs (replicated so that lookups never conflict).
+// Queries and centroids are each split into an fp16 high part and a low part
+// scaled by 2^11, so the centroid score keeps ~22 bits: q.c = qh.ch +
+// 2^-11 (ql.ch + qh.cl), three MMAs per k-step into two accumulators.
 // The QJL term sqrt(pi/2)/d * gamma * <S q_rot, 2 sigma - 1> uses a second
 // accumulator with a +-1 operand built the same way from the sign bits.
 // Values: O^T += V^T (P^T scaled per group by the token's fp16 scale), plus a
@@ -29,8 +32,10 @@ namespace dmma {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTile = 16;                 // tokens per warp per chunk
-constexpr int kChunk = kWarps * kTile;    // tokens per chunk
+constexpr int kTile = 16;                      // tokens per MMA tile
+constexpr int kTilesPerWarp = 2;               // tiles per warp per chunk
+constexpr int kChunk = kWarps * kTile * kTilesPerWarp;  // tokens per chunk
+constexpr float kLoScale = 2048.f;             // scale of the fp16 low parts
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -71,6 +76,14 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// 2^x with the hardware approximation (relative error ~2^-22).
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // 64-bit window of two consecutive 32-bit words shifted right by sh (0..63).
 __device__ __forceinline__ uint32_t window(uint32_t w0, uint32_t w1, int sh)
 {
@@ -83,9 +96,13 @@ template <int D, int KB>
 struct DecSmem {
     static constexpr int kPairBits = 2 * KB;
     static constexpr int kPairEntries = 1 << kPairBits;
-    static constexpr size_t kLut = sizeof(uint32_t) * kPairEntries * 32;  // [entry][lane] fp16 pairs
+    // [entry][16 copies] (hi pair, lo pair): a 64-bit load takes two wavefronts of
+    // 16 lanes, so 16 copies (lane & 15) keep every lookup conflict-free.
+    static constexpr size_t kLut = sizeof(uint2) * kPairEntries * 16;
     static constexpr size_t kSignLut = sizeof(uint32_t) * 4 * 32;
-    static constexpr size_t kHeader = kLut + kSignLut + 64;                // + page-valid flags
+    static constexpr size_t kQfrag = sizeof(uint4) * (D / 16) * 32;      // [k-step][lane] (qh0, qh2, ql0, ql2)
+    static constexpr size_t kSfrag = sizeof(uint2) * (D / 16) * 32;      // [k-step][lane] (qs0, qs2)
+    static constexpr size_t kHeader = kLut + kSignLut + kQfrag + kSfrag + 64;  // + page-valid flags
     __host__ __device__ static size_t stage_bytes(const PageGeom &pg)
     {
         return static_cast<size_t>(kChunk / pg.P) * (pg.k_page + pg.v_page);
@@ -99,7 +116,7 @@ struct DecSmem {
 };
 
 template <int D, int KB, int VB>
-__global__ void __launch_bounds__(kThreads) decode_mma_kernel(const Codec C, const PageGeom PG, const DecodeArgs A)
+__global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(const Codec C, const PageGeom PG, const DecodeArgs A)
 {
     using SM = DecSmem<D, KB>;
     constexpr bool QJL = (KB <= 3);
@@ -108,9 +125,11 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const Codec C, con
     constexpr int NWK = D * KB / 32;           // words per key code row
     constexpr int NWS = D / 32;                // words per sign row
     extern __shared__ __align__(16) unsigned char smem[];
-    uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
+    uint2 *lut = reinterpret_cast<uint2 *>(smem);
     uint32_t *slut = reinterpret_cast<uint32_t *>(smem + SM::kLut);
-    int *page_ok = reinterpret_cast<int *>(smem + SM::kLut + SM::kSignLut);  // [2][4]
+    uint4 *qfrag = reinterpret_cast<uint4 *>(smem + SM::kLut + SM::kSignLut);
+    uint2 *sfrag = reinterpret_cast<uint2 *>(smem + SM::kLut + SM::kSignLut + SM::kQfrag);
+    int *page_ok = reinterpret_cast<int *>(smem + SM::kLut + SM::kSignLut + SM::kQfrag + SM::kSfrag);  // [2][8]
     unsigned char *stages = smem + SM::kHeader;
 
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -143,39 +162,42 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const Codec C, con
     }
 
     // ---- tables: fp16 centroid pairs and +-1 sign pairs, one copy per lane ----
-    for (int e = tid; e < SM::kPairEntries * 32; e += kThreads) {
-        const int ent = e >> 5;
+    for (int e = tid; e < SM::kPairEntries * 16; e += kThreads) {
+        const int ent = e >> 4;
         const int c0 = ent & ((1 << KB) - 1), c1 = ent >> KB;
-        lut[e] = pack_half2(C.centroids[c0], C.centroids[c1]);
+        const float x0 = C.centroids[c0], x1 = C.centroids[c1];
+        const float h0 = __half2float(__float2half_rn(x0)), h1 = __half2float(__float2half_rn(x1));
+        lut[e] = make_uint2(pack_half2(h0, h1), pack_half2((x0 - h0) * kLoScale, (x1 - h1) * kLoScale));
     }
     for (int e = tid; e < 4 * 32; e += kThreads) {
         const int ent = e >> 5;
         slut[e] = pack_half2((ent & 1) ? 1.f : -1.f, (ent & 2) ? 1.f : -1.f);
     }
 
-    // ---- query fragments (A operand of the score MMA), permuted coordinates ----
-    uint32_t qa0[KS], qa2[KS], sa0[KS], sa2[KS];
-    {
+    // ---- query fragments (A operand of the score MMA), permuted coordinates;
+    // identical for the four warps, so warp 0 writes them to shared memory ----
+    if (warp == 0) {
         const bool hv = row < G;
         const float *qr = A.ws.qrot + (head0 + (hv ? row : 0)) * D;
         const float *qs = A.ws.qs + (head0 + (hv ? row : 0)) * D;
-#pragma unroll
+#pragma unroll 4
         for (int s = 0; s < KS; ++s) {
             const int j = 16 * s + 4 * quad;
+            uint4 f = make_uint4(0u, 0u, 0u, 0u);
+            uint2 g = make_uint2(0u, 0u);
             if (hv) {
                 const float4 v = *reinterpret_cast<const float4 *>(qr + j);
-                qa0[s] = pack_half2(v.x, v.y);
-                qa2[s] = pack_half2(v.z, v.w);
+                const float hx = __half2float(__float2half_rn(v.x)), hy = __half2float(__float2half_rn(v.y));
+                const float hz = __half2float(__float2half_rn(v.z)), hw = __half2float(__float2half_rn(v.w));
+                f = make_uint4(pack_half2(hx, hy), pack_half2(hz, hw), pack_half2((v.x - hx) * kLoScale, (v.y - hy) * kLoScale),
+                               pack_half2((v.z - hz) * kLoScale, (v.w - hw) * kLoScale));
                 if (QJL) {
                     const float4 w = *reinterpret_cast<const float4 *>(qs + j);
-                    sa0[s] = pack_half2(w.x, w.y);
-                    sa2[s] = pack_half2(w.z, w.w);
-                } else {
-                    sa0[s] = sa2[s] = 0u;
+                    g = make_uint2(pack_half2(w.x, w.y), pack_half2(w.z, w.w));
                 }
-            } else {
-                qa0[s] = qa2[s] = sa0[s] = sa2[s] = 0u;
             }
+            qfrag[s * 32 + lane] = f;
+            sfrag[s * 32 + lane] = g;
         }
     }
 
@@ -211,7 +233,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const Codec C, con
                     atomicOr(C.status, TQ_DEVERR_BLOCK_RANGE);
                 }
             }
-            if (tid == 0) page_ok[st * 4 + q] = ok;
+            if (tid == 0) page_ok[st * 8 + q] = ok;
         }
         cp_async_commit();
     };
@@ -229,20 +251,24 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const Codec C, con
         }
         __syncthreads();
 
-        // ---- this warp's 16 tokens: chunk tokens [16 warp, 16 warp + 16) ----
-        const int q = (kTile * warp) / P;        // page inside the chunk
-        const int o0 = (kTile * warp) - q * P;   // first offset inside the page
+        // ---- this warp's tiles: chunk tokens [16 (warp + 4 i), +16) ----
+#pragma unroll 1
+        for (int ti = 0; ti < kTilesPerWarp; ++ti) {
+        const int tok0 = kTile * (warp + kWarps * ti);
+        const int q = tok0 / P;                  // page inside the chunk
+        const int o0 = tok0 - q * P;             // first offset inside the page
         const int pos0 = (cpage + q) * P + o0;   // sequence position of tile token 0
-        const bool tile_live = (q < min(ppc, pg1 - cpage)) && page_ok[st * 4 + q] && (pos0 < L);
+        const bool tile_live = (q < min(ppc, pg1 - cpage)) && page_ok[st * 8 + q] && (pos0 < L);
         if (tile_live) {
             const unsigned char *kr = stages + st * stage_bytes + static_cast<size_t>(q) * PG.k_page;
             const unsigned char *vr = stages + st * stage_bytes + static_cast<size_t>(ppc) * PG.k_page +
                                       static_cast<size_t>(q) * PG.v_page;
             // ---- scores: two n-tiles of 8 tokens; this lane feeds token tau ----
-            float sc[2][4], ss[2][4];
+            float sc[2][4], sl[2][4], ss[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                sl[nt][0] = sl[nt][1] = sl[nt][2] = sl[nt][3] = 0.f;
                 ss[nt][0] = ss[nt][1] = ss[nt][2] = ss[nt][3] = 0.f;
                 const int tau = 2 * row - (row & 1) + 2 * nt;  // n-tile nt column `row`
                 const uint32_t *cw = reinterpret_cast<const uint32_t *>(kr + (o0 + tau) * C.k_code_bytes);
@@ -271,14 +297,18 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const Codec C, con
                     const uint32_t bits = window(kw[w0], kw[w0 + 1], sh);
                     const uint32_t p0 = bits & ((1u << (2 * KB)) - 1u);
                     const uint32_t p1 = (bits >> (2 * KB)) & ((1u << (2 * KB)) - 1u);
-                    const uint32_t b0 = lut[(p0 << 5) + lane];
-                    const uint32_t b1 = lut[(p1 << 5) + lane];
-                    mma16816(sc[nt], qa0[s], 0u, qa2[s], 0u, b0, b1);
+                    const uint2 b0 = lut[(p0 << 4) + (lane & 15)];
+                    const uint2 b1 = lut[(p1 << 4) + (lane & 15)];
+                    const uint4 qf = qfrag[s * 32 + lane];
+                    mma16816(sc[nt], qf.x, 0u, qf.y, 0u, b0.x, b1.x);
+                    mma16816(sl[nt], qf.z, 0u, qf.w, 0u, b0.x, b1.x);
+                    mma16816(sl[nt], qf.x, 0u, qf.y, 0u, b0.y, b1.y);
                     if (QJL) {
                         const uint32_t sb = (sw[s >> 1] >> (16 * (s & 1) + 4 * quad)) & 0xFu;
                         const uint32_t c0 = slut[((sb & 3u) << 5) + lane];
                         const uint32_t c1 = slut[((sb >> 2) << 5) + lane];
-                        mma16816(ss[nt], sa0[s], 0u, sa2[s], 0u, c0, c1);
+                        const uint2 sf = sfrag[s * 32 + lane];
+                        mma16816(ss[nt], sf.x, 0u, sf.y, 0u, c0, c1);
                     }
                 }
             }
@@ -297,7 +327,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const Codec C, con
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int nt = i >> 1, e = i & 1;
-                float v = nrm[i] * fac_c * sc[nt][e];
+                float v = nrm[i] * fac_c * fmaf(sl[nt][e], 1.f / kLoScale, sc[nt][e]);
                 if (QJL) v = fmaf(nrm[i] * fac_s * gam[i], ss[nt][e], v);
                 const bool valid = (pos0 + t0 + i) < L;
                 x[i] = (row < G) ? (valid ? v : -INFINITY) : 0.f;
@@ -309,9 +339,9 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const Codec C, con
             const float m_new = fmaxf(m_run, mt);
             float alpha = 1.f, p[4] = {0.f, 0.f, 0.f, 0.f};
             if (m_new != -INFINITY) {
-                alpha = exp2f(m_run - m_new);
+                alpha = fast_exp2(m_run - m_new);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) p[i] = exp2f(x[i] - m_new);
+                for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - m_new);
             }
             float ps = (p[0] + p[1]) + (p[2] + p[3]);
             ps += __shfl_xor_sync(0xffffffffu, ps, 1);
@@ -392,6 +422,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const Codec C, con
                 mma16816(o[m2], a0, a1, a2, a3, bs0, bs1);
             }
         }
+        }  // tiles
         __syncthreads();  // the next issue() overwrites this stage
     }
 
@@ -425,7 +456,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const Codec C, con
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
-                const float f = exp2f(r_m[w * 8 + h] - M);
+                const float f = fast_exp2(r_m[w * 8 + h] - M);
                 acc = fmaf(f, r_o[(w * D + j) * 8 + h] + r_z[(w * 8 + j / C.group) * 8 + h], acc);
                 l = fmaf(f, r_l[w * 8 + h], l);
             }

@@ -9,6 +9,7 @@
 #define TQ_DEVERR_SLOT_RANGE 0x1u
 #define TQ_DEVERR_BLOCK_RANGE 0x2u
 #define TQ_DEVERR_SEQ_RANGE 0x4u
+#define TQ_DEVERR_TIMEOUT 0x8u
 
 namespace tq {
 

@@ -25,7 +25,11 @@ struct Codec {
     const float *PiT;      // [d][d] transpose of Pi
     const float *S;        // [d][d] row-major QJL matrix
     const float *ST;       // [d][d] transpose of S
+    const float *M_hi;     // [d][d] M = S Pi (double) as hi + lo fp32, row-major
+    const float *M_lo;
+    const void *tc_image;  // d = 128: fp16 tensor-core operands (Pi 2^10 hi/lo, S 2^12 hi/lo), core-matrix layout
     unsigned int *status;  // device status word (TQ_DEVERR_* bits)
+    int num_sms;
 };
 
 // Byte offsets of the sub-arrays of one (block, kv head) page record.
@@ -74,6 +78,10 @@ struct DecodeArgs {
 cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
                             int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
                             int64_t num_blocks, cudaStream_t st);
+
+cudaError_t launch_compress_tc(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
+                               int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
+                               int64_t num_blocks, int num_sms, cudaStream_t st);
 
 cudaError_t launch_dequant(const Codec &c, const PageGeom &pg, const uint8_t *kc, const uint8_t *vc,
                            int64_t num_blocks, int Hkv, const int64_t *slots, int64_t T, uint16_t *k_out,

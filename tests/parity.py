@@ -132,5 +132,8 @@ def check_decode(out_gpu_bf16: np.ndarray, ref: np.ndarray, atol: float = DECODE
     half_ulp = np.where(ax > 0, 2.0 ** (e - 8), 0.0)
     err = np.abs(g - ref)
     bound = atol + half_ulp
-    assert np.all(err <= bound), f"decode error {err.max()} (bound {bound[err.argmax()] if err.size else 0})"
+    if err.size and not np.all(err <= bound):
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"decode error {err[i]:.3e} > bound {bound[i]:.3e} at {i} (gpu {g[i]:.6f}, "
+                             f"ref {ref[i]:.6f}); {np.count_nonzero(err > bound)} of {err.size} outside")
     return float(err.max()) if err.size else 0.0

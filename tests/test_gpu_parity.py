@@ -166,8 +166,10 @@ def test_decode_split_counts_agree():
     outs = [O.bf16_to_double(r) for r in raw]
     ax = np.abs(outs[0])
     ulp = 2.0 ** (np.floor(np.log2(np.where(ax > 0, ax, 1.0))) - 7)
+    # the split count changes only the fp32 merge order and which fp16-rounded
+    # probabilities meet in one accumulator: results agree to fp16 level
     for o in outs[1:]:
-        assert np.all(np.abs(o - outs[0]) <= ulp)
+        assert np.all(np.abs(o - outs[0]) <= 5e-4 + ulp)
     ref = _decode_oracle(ora, w, b, kc.cpu().numpy(), vc.cpu().numpy())
     for r in raw:
         check_decode(r, ref)
