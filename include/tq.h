@@ -161,6 +161,29 @@ tq_status tq_decode_attention(tq_handle h, const uint16_t *q, const uint8_t *k_c
                               void *stream);
 
 /*
+ * tq_decode_attention_static -- tq_decode_attention without a workspace, for
+ * callers that cannot allocate device memory or own no memory to lend (code
+ * inside another runtime's fixed memory budget, plug-ins in a host process that
+ * owns every allocation, schedulers that must not touch an allocator on their
+ * launch path).  The pages describe no such entry point; it is a deployment
+ * convenience of this library.
+ *
+ * Same arguments and results as tq_decode_attention minus workspace/ws_bytes.
+ * The scratch lives in one file-scope device array of TQ_STATIC_SCRATCH_BYTES
+ * that every GPU loading the library holds until exit.  A call whose scratch
+ * need (tq_decode_workspace_bytes) exceeds it returns TQ_ERR_UNSUPPORTED and
+ * launches nothing.  Allocates nothing.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) while that device is current;
+ * make that first call before any stream capture.  All calls share the array:
+ * calls that overlap on the GPU (other streams, other handles) race.
+ */
+#define TQ_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+tq_status tq_decode_attention_static(tq_handle h, const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                     const int32_t *block_table, const int32_t *seq_lens, int batch, int num_q_heads,
+                                     int num_kv_heads, int page_size, int max_blocks_per_seq, int64_t num_blocks,
+                                     float sm_scale, int splits, uint16_t *out, void *stream);
+
+/*
  * tq_get_status -- synchronises `stream`, returns the device status bits
  * accumulated since the last call (TQ_DEVERR_*), and clears them.
  */

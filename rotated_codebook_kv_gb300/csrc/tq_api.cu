@@ -48,6 +48,17 @@ bool supported_bits(int b) { return b >= 2 && b <= 4; }
 
 }  // namespace
 
+tq_status tq::api_error(tq_status s, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
 extern "C" {
 
 const char *tq_last_error(void) { return g_last_error.c_str(); }

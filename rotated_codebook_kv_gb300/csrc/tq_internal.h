@@ -6,7 +6,12 @@
 
 #include <cuda_runtime.h>
 
+#include "tq.h"
+
 namespace tq {
+
+// Records a printf-style message as this thread's tq_last_error() and returns s.
+tq_status api_error(tq_status s, const char *fmt, ...);
 
 // Host tables in double, built by tq_params.cpp.
 struct HostTables {

@@ -29,6 +29,8 @@ SIGNATURES = {
     "tq_decode_workspace_bytes": (_sz, [_vp, _i32, _i32, _i32]),
     "tq_decode_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _f32, _i32,
                                    _vp, _sz, _vp, _vp]),
+    "tq_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
+                                          _i32, _vp, _vp]),
     "tq_get_status": (_i32, [_vp, _c.POINTER(_c.c_uint32), _vp]),
     "tq_export_params": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "tq_last_error": (_c.c_char_p, []),
@@ -117,6 +119,13 @@ def tq_decode_attention(h, q, k_cache, v_cache, block_table, seq_lens, batch, nu
     _check("tq_decode_attention", load().tq_decode_attention(
         h, q, k_cache, v_cache, block_table, seq_lens, batch, num_q_heads, num_kv_heads, page_size,
         max_blocks_per_seq, num_blocks, sm_scale, splits, workspace, ws_bytes, out, stream))
+
+
+def tq_decode_attention_static(h, q, k_cache, v_cache, block_table, seq_lens, batch, num_q_heads, num_kv_heads,
+                               page_size, max_blocks_per_seq, num_blocks, sm_scale, splits, out, stream) -> None:
+    _check("tq_decode_attention_static", load().tq_decode_attention_static(
+        h, q, k_cache, v_cache, block_table, seq_lens, batch, num_q_heads, num_kv_heads, page_size,
+        max_blocks_per_seq, num_blocks, sm_scale, splits, out, stream))
 
 
 def tq_get_status(h, stream) -> int:
