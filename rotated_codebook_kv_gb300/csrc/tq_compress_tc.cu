@@ -4,23 +4,30 @@
 // Method (turbo-attn "How it works"; 0xsero/turboquant "Compression Pipeline",
 // "Value Compression"; brightcoding blog "Example 4"): see tq_compress.cu.
 //
-// Tile = 128 token-heads; one persistent CTA per SM, 256 threads.
-//  1. Keys are loaded, their norm taken in fp32 (sum of exact squares), and
-//     converted exactly to fp16 after a power-of-two scale 2^e per row.
-//  2. Y = K' (Pi 2^10)^T on the tensor cores: Pi 2^10 is split into fp16 high
-//     and low parts, two MMA terms, ~22-bit operands, fp32 accumulation.
-//  3. Epilogue, one thread per row (its TMEM lane): z = Y * sqrt(d) / (n 2^(10+e)),
-//     codes from a bin table, residual r = z - c[code], gamma = ||r|| / sqrt(d);
-//     r 2^12 is split into fp16 high / low parts for the next MMA.
-//  4. QJL: P = (R 2^12)(S 2^12)^T, three MMA terms (hi.hi, hi.lo, lo.hi); the
-//     sign of P is the sign of S r.
-//  5. Values (all warps, overlapping the MMAs) as in tq_compress.cu.
-//  6. Decisions within a guard band of a threshold, a sign boundary or a bf16
+// Tile = 128 token-heads; one persistent CTA per SM, 384 threads in two roles
+// that overlap consecutive tiles:
+//  producers (warps 8-11)
+//  1. load the keys of the next tile, take the norm in fp32 (sum of exact
+//     squares) and convert exactly to fp16 after a power-of-two scale 2^e per row;
+//  2. issue Y = K' (Pi 2^10)^T on the tensor cores once the epilogue has read
+//     the previous Y: Pi 2^10 is split into fp16 high and low parts, two MMA
+//     terms, ~22-bit operands, fp32 accumulation;
+//  3. compress the values of the tile (as in tq_compress.cu), independent of keys.
+//  epilogue (warps 0-7; warp w reads TMEM lane quarter w % 4, column half w / 4)
+//  4. z = Y sqrt(d) / (n 2^(10+e)), codes from a bin table, residual
+//     r = z - c[code], gamma = ||r|| / sqrt(d); r 2^12 is split into fp16 high /
+//     low parts for the next MMA;
+//  5. QJL: P = (R 2^12)(S 2^12)^T, three MMA terms (hi.hi, hi.lo, lo.hi); the
+//     sign of P is the sign of S r;
+//  6. decisions within a guard band of a threshold, a sign boundary or a bf16
 //     rounding midpoint of gamma are re-taken exactly: a code or a sign by an
 //     O(d) compensated dot product (z_j = sqrt(d) (Pi_j . k) / n,
 //     p_i = sqrt(d) (M_i . k) / n - S_i . c with M = S Pi in double-fp32), and
 //     a row whose code flips or whose gamma sits near a midpoint is redone
-//     entirely in compensated arithmetic.
+//     entirely in compensated arithmetic;
+//  7. key records are written.
+// Hand-offs: mbarriers "keys converted" (producers -> epilogue), "Y ready" and
+// "P ready" (tensor core -> both), "Y read" (epilogue -> producers).
 // Every mbarrier wait is bounded; a timeout sets TQ_DEVERR_TIMEOUT, the CTA
 // stops, waits (bounded) for its tensor-core work and frees its TMEM.
 #include <cuda_runtime.h>
@@ -34,8 +41,11 @@ namespace {
 
 constexpr int D = 128;
 constexpr int TM = 128;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;       // warps 0-7: epilogue; warps 8-11: producers
+constexpr int kEpi = 256;           // epilogue threads: TMEM lane quarter (warp & 3), column half (warp >> 2)
+constexpr int kProd = 128;          // producer threads: key conversion, MMA issue, values
 constexpr int kWarps = kThreads / 32;
+constexpr int kEpiWarps = kEpi / 32;
 constexpr float kCodeGuard = 1e-5f;   // z units
 constexpr float kSignGuard = 2e-5f;   // |p| / ||r||
 constexpr float kGammaGuard = 2e-6f;  // relative distance of gamma to a bf16 rounding midpoint
@@ -44,16 +54,16 @@ constexpr long long kWaitLimit = 2000000000LL;  // cycles (~1 s)
 // Shared-memory map (bytes).
 constexpr uint32_t kOffPiH = 0, kOffPiL = 32768, kOffSH = 65536, kOffSL = 98304;  // B operands (fp16)
 constexpr uint32_t kOffTA = 131072;  // K' (fp16) then R hi
-constexpr uint32_t kOffTB = 163840;  // R lo
-constexpr uint32_t kOffCodes = 196608;             // [TM][16] u32 packed key codes
+constexpr uint32_t kOffTB = 163840;  // R lo, then scratch of the exact path
+constexpr uint32_t kOffCodes = 196608;               // [TM][16] u32 packed key codes
 constexpr uint32_t kOffSigns = kOffCodes + TM * 64;  // [TM][4] u32 sign bits
 constexpr uint32_t kOffMask = kOffSigns + TM * 16;   // [TM][8] u32: code guard mask (4), sign guard mask (4)
-constexpr uint32_t kOffRow = kOffMask + TM * 32;     // per-row scalars
-constexpr uint32_t kOffScratch = kOffRow + TM * 32;  // [kWarps][D] doubles for the exact path
-constexpr uint32_t kOffBins = kOffScratch + kWarps * D * 8;  // [1024] u16 code-bin table
-constexpr uint32_t kOffBook = kOffBins + 2048;       // [16] centroids, [16] thresholds
-constexpr uint32_t kOffMisc = kOffBook + 128;
-constexpr uint32_t kSmemBytes = kOffMisc + 128;
+constexpr uint32_t kOffRow = kOffMask + TM * 32;     // [3][TM] RowInfo (tile index mod 3)
+constexpr uint32_t kOffPart = kOffRow + 3 * TM * 32; // [TM][2] gsq partials, [TM][2] code flags, [TM][2] sign flags
+constexpr uint32_t kOffBins = kOffPart + TM * 24;    // [1024] u16 code-bin table
+constexpr uint32_t kOffBook = kOffBins + 2048;       // [16] centroids, [16] thresholds (times 2^12)
+constexpr uint32_t kOffMisc = kOffBook + 128;        // mbarriers, TMEM slot, abort flags
+constexpr uint32_t kSmemBytes = kOffMisc + 64;
 
 constexpr uint32_t kSBO = (D / 8) * 128;  // 2048
 constexpr uint32_t kIdesc = umma::idesc_f16(128, 128);
@@ -190,6 +200,102 @@ __device__ void exact_row(const Codec &C, const float *kw, double n_sc, uint32_t
     __syncwarp();
 }
 
+
+// Epilogue 1 for one (row, column half): codes, guard mask, residual split into
+// fp16 hi / lo operands, and the partial sum of squares of the residual.
+template <int KB, int HF>
+__device__ __forceinline__ void epilogue_rotation(unsigned char *smem, uint32_t tY, int warp, int row, float zscale,
+                                                  bool zero, bool qjl, const uint16_t *bins, const float *s_cent,
+                                                  const float *s_thr, uint32_t *scodes, uint32_t *smask,
+                                                  float &gsq_out, int &flag_out)
+{
+    constexpr int C0 = 64 * HF;
+    constexpr int W0 = C0 * KB / 32;  // first code word of this half
+    constexpr int NW = 64 * KB / 32;  // code words of this half
+    uint32_t cw[NW + 1];
+#pragma unroll
+    for (int w = 0; w <= NW; ++w) cw[w] = 0u;
+    uint32_t cmask[2] = {0u, 0u};
+    float gsq = 0.f;
+    const float zs = zscale * 4096.f;  // z' = 2^12 z
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        float y[16];
+        umma::ld16(tY + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + C0 + 16 * cb, y);
+        float rs[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int i = 16 * cb + j;  // column inside the half (compile-time)
+            const float z = y[j] * zs;
+            int bi = static_cast<int>(fmaf(z, kBinScale / 4096.f, kBinOrigin * kBinScale));
+            bi = min(max(bi, 0), 1023);
+            const uint32_t bt = bins[bi];
+            uint32_t code = bt & 0xFu;
+            if (bt & 0x10u) {
+                const float th = s_thr[bt >> 8];
+                code += (z >= th) ? 1u : 0u;
+                if (fabsf(z - th) < kCodeGuard * 4096.f) cmask[i >> 5] |= 1u << (i & 31);
+            }
+            if (zero) code = 0u;
+            const float r = zero ? 0.f : z - s_cent[code];
+            gsq = fmaf(r, r, gsq);
+            const int o = i * KB;  // bit offset inside the half (compile-time)
+            cw[o >> 5] |= code << (o & 31);
+            if ((o & 31) + KB > 32) cw[(o >> 5) + 1] |= code >> (32 - (o & 31));
+            rs[j] = r;
+        }
+        uint32_t rh[8], rlo[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const __half2 hh = __floats2half2_rn(rs[2 * q], rs[2 * q + 1]);
+            const float2 hf = __half22float2(hh);
+            rh[q] = *reinterpret_cast<const uint32_t *>(&hh);
+            rlo[q] = pack_h2(rs[2 * q] - hf.x, rs[2 * q + 1] - hf.y);
+        }
+        if (!qjl) continue;  // without QJL the key tile buffer already holds the next tile
+#pragma unroll
+        for (int c4 = 0; c4 < 2; ++c4) {
+            const uint32_t off = umma::core_offset(row, C0 + 16 * cb + 8 * c4, D);
+            *reinterpret_cast<uint4 *>(smem + kOffTA + off) =
+                make_uint4(rh[4 * c4], rh[4 * c4 + 1], rh[4 * c4 + 2], rh[4 * c4 + 3]);
+            *reinterpret_cast<uint4 *>(smem + kOffTB + off) =
+                make_uint4(rlo[4 * c4], rlo[4 * c4 + 1], rlo[4 * c4 + 2], rlo[4 * c4 + 3]);
+        }
+    }
+#pragma unroll
+    for (int w = 0; w < NW; ++w) scodes[row * 16 + W0 + w] = cw[w];
+    smask[row * 8 + 2 * HF] = cmask[0];
+    smask[row * 8 + 2 * HF + 1] = cmask[1];
+    gsq_out = gsq * (1.f / 16777216.f);  // back to z units
+    flag_out = (cmask[0] | cmask[1]) ? 1 : 0;
+}
+
+// Epilogue 2 for one (row, column half): QJL sign bits and the sign guard mask.
+__device__ __forceinline__ int epilogue_signs(uint32_t tP, int warp, int row, int hf, float guard, bool zero,
+                                              uint32_t *ssigns, uint32_t *smask)
+{
+    int flag = 0;
+#pragma unroll
+    for (int cb = 0; cb < 2; ++cb) {
+        uint32_t bits = 0u, near = 0u;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            float p[16];
+            umma::ld16(tP + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 64 * hf + 32 * cb + 16 * part, p);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                bits |= (p[j] >= 0.f ? 1u : 0u) << (16 * part + j);
+                near |= (fabsf(p[j]) < guard ? 1u : 0u) << (16 * part + j);
+            }
+        }
+        if (zero) bits = near = 0u;
+        ssigns[row * 4 + 2 * hf + cb] = bits;
+        smask[row * 8 + 4 + 2 * hf + cb] = near;
+        flag |= near ? 2 : 0;
+    }
+    return flag;
+}
+
 template <int KB>
 __global__ void __launch_bounds__(kThreads, 1)
 compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
@@ -201,15 +307,20 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     uint32_t *scodes = reinterpret_cast<uint32_t *>(smem + kOffCodes);
     uint32_t *ssigns = reinterpret_cast<uint32_t *>(smem + kOffSigns);
     uint32_t *smask = reinterpret_cast<uint32_t *>(smem + kOffMask);
-    RowInfo *rinfo = reinterpret_cast<RowInfo *>(smem + kOffRow);
-    double *scratch_all = reinterpret_cast<double *>(smem + kOffScratch);
+    RowInfo *rinfo_all = reinterpret_cast<RowInfo *>(smem + kOffRow);
+    float *s_gsq = reinterpret_cast<float *>(smem + kOffPart);                 // [TM][2]
+    int *s_flagp = reinterpret_cast<int *>(smem + kOffPart + TM * 8);          // [TM][2]
+    int *s_flags = reinterpret_cast<int *>(smem + kOffPart + TM * 16);         // [TM][2]
     uint16_t *bins = reinterpret_cast<uint16_t *>(smem + kOffBins);
     float *s_cent = reinterpret_cast<float *>(smem + kOffBook);
     float *s_thr = s_cent + 16;
-    uint64_t *mbarY = reinterpret_cast<uint64_t *>(smem + kOffMisc);
-    uint64_t *mbarP = mbarY + 1;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc + 16);
-    int *s_abort = reinterpret_cast<int *>(smem + kOffMisc + 20);
+    uint64_t *mbarY = reinterpret_cast<uint64_t *>(smem + kOffMisc);      // rotation MMA done
+    uint64_t *mbarP = mbarY + 1;                                           // projection MMA done
+    uint64_t *mbarConv = mbarY + 2;                                        // keys of the tile converted
+    uint64_t *mbarYfree = mbarY + 3;                                       // rotation accumulator read
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc + 32);
+    volatile int *e_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 36);
+    volatile int *p_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 40);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float sqrtd = sqrtf(static_cast<float>(D));
@@ -231,15 +342,18 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             }
             bins[b] = static_cast<uint16_t>(below | (idx >= 0 ? (0x10 | (idx << 8)) : 0));
         }
-        if (tid < 16) {
-            s_cent[tid] = C.centroids[tid];
-            s_thr[tid] = C.thresholds[tid];
+        if (tid < 16) {  // in units of 2^-12 so the residual comes out pre-scaled for the MMA
+            s_cent[tid] = C.centroids[tid] * 4096.f;
+            s_thr[tid] = C.thresholds[tid] * 4096.f;
         }
         if (tid == 0) {
             umma::mbar_init(mbarY, 1);
             umma::mbar_init(mbarP, 1);
+            umma::mbar_init(mbarConv, 1);
+            umma::mbar_init(mbarYfree, 1);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-            *s_abort = 0;
+            *e_abort = 0;
+            *p_abort = 0;
         }
         if (warp == 0) umma::tmem_alloc(tslot, 256);
         umma::fence_proxy_async();
@@ -250,271 +364,273 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     const uint32_t tmem = *tslot;
     const uint32_t tY = tmem, tP = tmem + 128;
     const uint32_t sbase = umma::smem_u32(smem);
-    uint32_t phase = 0;
 
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-        const int64_t r0 = static_cast<int64_t>(tile) * TM;
-        // ---- slots ----
-        if (tid < TM) {
-            const int64_t r = r0 + tid;
-            RowInfo ri;
-            ri.dst = -1;
-            ri.off = 0;
-            ri.flag = 0;
-            ri.zscale = 0.f;
-            ri.rn = 0.f;
-            ri.n16g16 = 0;
-            ri.pad = 0;
-            if (r < rows) {
-                const int64_t t = r / Hkv;
-                const int h = static_cast<int>(r - t * Hkv);
-                const int64_t s = slots[t];
-                if (s >= 0) {
-                    if (s < num_blocks * G.P) {
-                        const int64_t blk = s / G.P;
-                        ri.off = static_cast<int>(s - blk * G.P);
-                        ri.dst = blk * Hkv + h;
-                    } else {
-                        atomicOr(C.status, TQ_DEVERR_SLOT_RANGE);
+    if (warp >= kEpiWarps) {
+        // =========================== producers =================================
+        const int ptid = tid - kEpi, pw = warp - kEpiWarps;
+        int it = 0, buf = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it, buf = (buf == 2 ? 0 : buf + 1)) {
+            const int64_t r0 = static_cast<int64_t>(tile) * TM;
+            // three row-info buffers: the epilogue may still finish tile it-2 while tile it is converted
+            RowInfo *rinfo = rinfo_all + buf * TM;
+            // the key tile buffer is free once the previous tile's last MMA finished
+            if (it > 0 && ptid == 0) {
+                if (!umma::mbar_wait_bounded(C.qjl ? mbarP : mbarY, (it - 1) & 1, kWaitLimit)) {
+                    atomicOr(C.status, TQ_DEVERR_TIMEOUT);
+                    *p_abort = 1;
+                }
+            }
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            if (*p_abort) break;
+            // ---- keys: slot, norm, power-of-two scale, exact fp16 conversion ----
+            // warp pw handles 8-row groups pw, pw+4, ...; lane: row 8g + (lane & 7), chunks (lane >> 3) + 4 i
+#pragma unroll 1
+            for (int grp = pw; grp < TM / 8; grp += 4) {
+                const int rl = 8 * grp + (lane & 7);
+                const int64_t r = r0 + rl;
+                int64_t dsti = -1;
+                int offi = 0;
+                const uint16_t *src = nullptr;
+                if (r < rows) {
+                    const int64_t t = r / Hkv;
+                    const int h = static_cast<int>(r - t * Hkv);
+                    const int64_t s = slots[t];
+                    if (s >= 0) {
+                        if (s < num_blocks * G.P) {
+                            const int64_t blk = s / G.P;
+                            offi = static_cast<int>(s - blk * G.P);
+                            dsti = blk * Hkv + h;
+                            src = kin + t * ks + static_cast<int64_t>(h) * D;
+                        } else if ((lane >> 3) == 0) {
+                            atomicOr(C.status, TQ_DEVERR_SLOT_RANGE);
+                        }
                     }
                 }
-            }
-            rinfo[tid] = ri;
-        }
-        __syncthreads();
-        // ---- keys: norm, power-of-two scale, exact fp16 conversion into tile A ----
-        // warp handles 8-row groups; lane: row 8g + (lane & 7), chunks (lane >> 3) + 4 i
-        for (int grp = warp; grp < TM / 8; grp += kWarps) {
-            const int rl = 8 * grp + (lane & 7);
-            const int64_t r = r0 + rl;
-            float x[4][8];
-            float mx = 0.f;
-            const bool live = (r < rows) && rinfo[rl].dst >= 0;
-            const uint16_t *src = nullptr;
-            if (live) {
-                const int64_t t = r / Hkv;
-                src = kin + t * ks + static_cast<int64_t>(r - t * Hkv) * D;
-            }
+                uint4 u[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = (lane >> 3) + 4 * i;
-                uint4 u = make_uint4(0u, 0u, 0u, 0u);
-                if (live) u = __ldg(reinterpret_cast<const uint4 *>(src) + c);
-                x[i][0] = bf16_to_float(u.x & 0xffffu); x[i][1] = bf16_to_float(u.x >> 16);
-                x[i][2] = bf16_to_float(u.y & 0xffffu); x[i][3] = bf16_to_float(u.y >> 16);
-                x[i][4] = bf16_to_float(u.z & 0xffffu); x[i][5] = bf16_to_float(u.z >> 16);
-                x[i][6] = bf16_to_float(u.w & 0xffffu); x[i][7] = bf16_to_float(u.w >> 16);
+                for (int i = 0; i < 4; ++i)
+                    u[i] = src ? __ldg(reinterpret_cast<const uint4 *>(src) + (lane >> 3) + 4 * i) : make_uint4(0u, 0u, 0u, 0u);
+                float x[4][8];
+                float mx = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(x[i][e]));
-            }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            int ex = 0;
-            if (mx > 0.f) frexpf(mx, &ex);  // mx in [2^(ex-1), 2^ex)
-            // |k'| < 2^15; keys too small for a finite fp32 scale are redone exactly
-            const bool tiny = (15 - ex) > 126;
-            const float sc = ldexpf(1.f, tiny ? 126 : 15 - ex);
-            float ss = 0.f;
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const float a = x[i][e] * sc, b = x[i][e + 1] * sc;
-                    ss = fmaf(a, a, ss);
-                    ss = fmaf(b, b, ss);
-                    pk[e / 2] = pack_h2(a, b);
+                    for (int e = 0; e < 4; ++e) {
+                        x[i][2 * e] = bf16_to_float(w[e] & 0xffffu);
+                        x[i][2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+                        mx = fmaxf(mx, fmaxf(fabsf(x[i][2 * e]), fabsf(x[i][2 * e + 1])));
+                    }
                 }
-                const int c = (lane >> 3) + 4 * i;
-                *reinterpret_cast<uint4 *>(smem + kOffTA + umma::core_offset(rl, 8 * c, D)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                int ex = 0;
+                if (mx > 0.f) frexpf(mx, &ex);  // mx in [2^(ex-1), 2^ex)
+                // |k'| < 2^15; keys too small for a finite fp32 scale are redone exactly
+                const bool tiny = (15 - ex) > 126;
+                const float sc = ldexpf(1.f, tiny ? 126 : 15 - ex);
+                float ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        const float a = x[i][e] * sc, b = x[i][e + 1] * sc;
+                        ss = fmaf(a, a, ss);
+                        ss = fmaf(b, b, ss);
+                        pk[e / 2] = pack_h2(a, b);
+                    }
+                    const int c = (lane >> 3) + 4 * i;
+                    *reinterpret_cast<uint4 *>(smem + kOffTA + umma::core_offset(rl, 8 * c, D)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+                if (lane < 8) {
+                    RowInfo ri;
+                    ri.dst = dsti;
+                    ri.off = offi;
+                    ri.flag = 0;
+                    ri.zscale = 0.f;
+                    ri.rn = 0.f;
+                    ri.n16g16 = 0u;
+                    ri.pad = 0;
+                    if (mx == 0.f) {
+                        ri.flag = 8;  // zero key (or no key)
+                    } else {
+                        if (tiny) ri.flag = 4;
+                        const float nsc = sqrtf(ss);  // ||k|| 2^(15-ex)
+                        ri.zscale = sqrtd / (nsc * 1024.f);
+                        ri.n16g16 = float_to_bf16_bits(ldexpf(nsc, ex - 15));
+                    }
+                    rinfo[rl] = ri;
+                }
             }
-            ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-            if (lane < 8) {
-                RowInfo &ri = rinfo[rl];
-                if (mx == 0.f) {
-                    ri.flag = 8;  // zero key
+            umma::fence_proxy_async();
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            if (ptid == 0) {
+                // ---- rotation MMAs: Y = K' (Pi_lo + Pi_hi)^T, once the epilogue has read Y ----
+                bool ok = true;
+                if (it > 0) ok = umma::mbar_wait_bounded(mbarYfree, (it - 1) & 1, kWaitLimit);
+                if (ok) {
+                    umma::fence_after_sync();
+#pragma unroll 1
+                    for (int term = 0; term < 2; ++term) {
+                        const uint32_t boff = term == 0 ? kOffPiL : kOffPiH;
+#pragma unroll 1
+                        for (int s = 0; s < D / 16; ++s) {
+                            const uint64_t a = umma::make_desc(sbase + kOffTA + 256 * s, 128, kSBO);
+                            const uint64_t b = umma::make_desc(sbase + boff + 256 * s, 128, kSBO);
+                            umma::mma_f16(tY, a, b, kIdesc, (term | s) != 0);
+                        }
+                    }
+                    umma::commit(mbarY);
+                    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(mbarConv))
+                                 : "memory");
                 } else {
-                    if (tiny) ri.flag |= 4;
-                    const float nsc = sqrtf(ss);  // ||k|| 2^(15-ex)
-                    ri.zscale = sqrtd / (nsc * 1024.f);
-                    ri.n16g16 = float_to_bf16_bits(ldexpf(nsc, ex - 15));
+                    atomicOr(C.status, TQ_DEVERR_TIMEOUT);
+                    *p_abort = 1;
                 }
             }
-        }
-        umma::fence_proxy_async();
-        umma::fence_before_sync();
-        __syncthreads();
-        umma::fence_after_sync();
-        // ---- rotation MMAs: Y = K' (Pi_lo + Pi_hi)^T ----
-        if (tid == 0) {
-#pragma unroll 1
-            for (int term = 0; term < 2; ++term) {
-                const uint32_t boff = term == 0 ? kOffPiL : kOffPiH;
-#pragma unroll 1
-                for (int s = 0; s < D / 16; ++s) {
-                    const uint64_t a = umma::make_desc(sbase + kOffTA + 256 * s, 128, kSBO);
-                    const uint64_t b = umma::make_desc(sbase + boff + 256 * s, 128, kSBO);
-                    umma::mma_f16(tY, a, b, kIdesc, (term | s) != 0);
+            // ---- values of this tile (8 lanes per row, 16 channels per lane) ----
+            for (int rb = 4 * pw; rb < TM; rb += 16) {
+                const int rl = rb + (lane >> 3), sub = lane & 7;
+                const int64_t r = r0 + rl;
+                int64_t dst = -1;
+                int off = 0;
+                const uint16_t *vrow = nullptr;
+                if (r < rows) {
+                    const int64_t t = r / Hkv;
+                    const int h = static_cast<int>(r - t * Hkv);
+                    const int64_t s = slots[t];
+                    if (s >= 0 && s < num_blocks * G.P) {
+                        const int64_t blk = s / G.P;
+                        off = static_cast<int>(s - blk * G.P);
+                        dst = blk * Hkv + h;
+                        vrow = vin + t * vs + static_cast<int64_t>(h) * D;
+                    }
                 }
-            }
-            umma::commit(mbarY);
-        }
-        // ---- values (all warps, while the tensor core runs) ----
-        for (int rl = warp; rl < TM; rl += kWarps) {
-            const int64_t dst = rinfo[rl].dst;
-            if (dst < 0) continue;
-            const int off = rinfo[rl].off;
-            const int64_t r = r0 + rl;
-            const int64_t t = r / Hkv;
-            const int h = static_cast<int>(r - t * Hkv);
-            const uint16_t *vsrc = vin + t * vs + static_cast<int64_t>(h) * D + lane * 4;
-            float x[4];
-            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(vsrc));
-            x[0] = bf16_to_float(u.x & 0xffffu); x[1] = bf16_to_float(u.x >> 16);
-            x[2] = bf16_to_float(u.y & 0xffffu); x[3] = bf16_to_float(u.y >> 16);
-            const int lpg = C.group / 4;
-            float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
-            float mxv = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-            for (int o = lpg >> 1; o > 0; o >>= 1) {
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-                mxv = fmaxf(mxv, __shfl_xor_sync(0xffffffffu, mxv, o));
-            }
-            const int L = (1 << C.v_bits) - 1;
-            float dh, de;
-            two_sum(mxv, -mn, dh, de);
-            const __half s16 = (de == 0.f) ? __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)))
-                                           : __double2half((static_cast<double>(mxv) - static_cast<double>(mn)) / L);
-            const __half z16 = __float2half_rn(mn);
-            const float sv = __half2float(s16), zv = __half2float(z16);
-            uint32_t codebits = 0u;  // this lane's 4 codes, LSB-first
+                float x[16];
+                if (vrow) {
+                    const uint4 *vsrc = reinterpret_cast<const uint4 *>(vrow) + 2 * sub;
+                    const uint4 u0 = __ldg(vsrc), u1 = __ldg(vsrc + 1);
+                    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                int q = 0;
-                if (sv != 0.f) {
-                    float a, ea;
-                    two_sum(x[m], -zv, a, ea);
-                    const float qf = floorf(__fdiv_rn(a, sv) + 0.5f);
-                    q = static_cast<int>(fminf(fmaxf(qf, 0.f), static_cast<float>(L)));
-                    while (q < L && __fadd_rn(__fsub_rn(a, (q + 0.5f) * sv), ea) >= 0.f) ++q;
-                    while (q > 0 && !(__fadd_rn(__fsub_rn(a, (q - 0.5f) * sv), ea) >= 0.f)) --q;
+                    for (int e = 0; e < 8; ++e) {
+                        x[2 * e] = bf16_to_float(w[e] & 0xffffu);
+                        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) x[e] = 0.f;
                 }
-                codebits |= static_cast<uint32_t>(q) << (m * C.v_bits);
-            }
-            // gather the lanes' 4*vb-bit pieces into 32-bit words of the bitstream
-            uint8_t *vrec = vc + dst * G.v_page;
-            const int piece = 4 * C.v_bits;  // 8, 12 or 16 bits
-            const int nvw = D * C.v_bits / 32;
-            uint32_t word = 0u;
-            for (int w = 0; w < nvw; ++w) {
-                // lanes whose pieces overlap word w
-                const int l0 = (32 * w) / piece, l1 = (32 * w + 31) / piece;
-                uint32_t acc = 0u;
-                for (int l = l0; l <= l1; ++l) {
-                    const uint32_t pcs = __shfl_sync(0xffffffffu, codebits, l);
-                    const int sh = l * piece - 32 * w;  // may be negative
-                    acc |= sh >= 0 ? (pcs << sh) : (pcs >> (-sh));
+                float mn = x[0], mxv = x[0];
+#pragma unroll
+                for (int e = 1; e < 16; ++e) {
+                    mn = fminf(mn, x[e]);
+                    mxv = fmaxf(mxv, x[e]);
                 }
-                if (lane == w) word = acc;
-            }
-            if (lane < nvw)
-                *reinterpret_cast<uint32_t *>(vrec + static_cast<int64_t>(off) * C.v_code_bytes + 4 * lane) = word;
-            if ((lane % lpg) == 0) {
-                const int gi = lane / lpg;
-                const uint32_t meta = static_cast<uint32_t>(__half_as_ushort(s16)) |
-                                      (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
-                *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + static_cast<int64_t>(off) * C.v_meta_bytes + 4 * gi) =
-                    meta;
+                const int lpg = C.group / 16;  // lanes per group: 2, 4 or 8
+                for (int o = lpg >> 1; o > 0; o >>= 1) {
+                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                    mxv = fmaxf(mxv, __shfl_xor_sync(0xffffffffu, mxv, o));
+                }
+                const int L = (1 << C.v_bits) - 1;
+                float dh, de;
+                two_sum(mxv, -mn, dh, de);
+                // (max - min) / L with L in {3, 7, 15} is exact in fp32 or a non-terminating
+                // binary fraction: one rounding to fp32 then fp16 equals one rounding to fp16.
+                const __half s16 = (de == 0.f) ? __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)))
+                                               : __double2half((static_cast<double>(mxv) - static_cast<double>(mn)) / L);
+                const __half z16 = __float2half_rn(mn);
+                const float sv = __half2float(s16), zv = __half2float(z16);
+                const float inv = (sv != 0.f) ? __frcp_rn(sv) : 0.f;
+                uint64_t cbits = 0u;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    int q = 0;
+                    if (sv != 0.f) {
+                        // fp32 guess; exact midpoint comparison only within 1e-3 of a rounding boundary
+                        const float tq = fmaf(x[e] - zv, inv, 0.5f);
+                        const float fl = floorf(tq);
+                        q = static_cast<int>(fminf(fmaxf(fl, 0.f), static_cast<float>(L)));
+                        const float fr = tq - fl;
+                        if (fr < 1e-3f || fr > 0.999f) {
+                            float a, ea;
+                            two_sum(x[e], -zv, a, ea);
+                            while (q < L && __fadd_rn(__fsub_rn(a, (q + 0.5f) * sv), ea) >= 0.f) ++q;
+                            while (q > 0 && !(__fadd_rn(__fsub_rn(a, (q - 0.5f) * sv), ea) >= 0.f)) --q;
+                        }
+                    }
+                    cbits |= static_cast<uint64_t>(q) << (e * C.v_bits);
+                }
+                uint8_t *vrec = (dst >= 0) ? vc + dst * G.v_page : nullptr;
+                uint32_t *vw = vrec ? reinterpret_cast<uint32_t *>(vrec + static_cast<int64_t>(off) * C.v_code_bytes) : nullptr;
+                if (C.v_bits == 3) {  // 48 bits per lane: lanes 2p, 2p+1 share the middle word
+                    const uint64_t other = __shfl_xor_sync(0xffffffffu, cbits, 1);
+                    if (vw) {
+                        const int p = sub >> 1;
+                        if ((sub & 1) == 0) {
+                            vw[3 * p] = static_cast<uint32_t>(cbits);
+                            vw[3 * p + 1] = static_cast<uint32_t>(cbits >> 32) | static_cast<uint32_t>(other << 16);
+                        } else {
+                            vw[3 * p + 2] = static_cast<uint32_t>(cbits >> 16);
+                        }
+                    }
+                } else if (vw) {
+                    if (C.v_bits == 2) {
+                        vw[sub] = static_cast<uint32_t>(cbits);
+                    } else {
+                        vw[2 * sub] = static_cast<uint32_t>(cbits);
+                        vw[2 * sub + 1] = static_cast<uint32_t>(cbits >> 32);
+                    }
+                }
+                if (vrec && (sub % lpg) == 0) {
+                    const uint32_t meta = static_cast<uint32_t>(__half_as_ushort(s16)) |
+                                          (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
+                    *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + static_cast<int64_t>(off) * C.v_meta_bytes +
+                                                  4 * (sub / lpg)) = meta;
+                }
             }
         }
-        // ---- key epilogue 1: codes, residual, gamma (thread = row = TMEM lane) ----
-        if (warp < 4) {
-            const int rl = tid;
-            bool ok = umma::mbar_wait_bounded(mbarY, phase, kWaitLimit);
-            if (!ok) {
+    } else {
+        // =========================== epilogue ==================================
+        const int row = 32 * (warp & 3) + lane, hf = warp >> 2;
+        int it = 0, buf = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it, buf = (buf == 2 ? 0 : buf + 1)) {
+            const int64_t r0 = static_cast<int64_t>(tile) * TM;
+            RowInfo *rinfo = rinfo_all + buf * TM;
+            const uint32_t par = it & 1;
+            if (!umma::mbar_wait_bounded(mbarConv, par, kWaitLimit) || !umma::mbar_wait_bounded(mbarY, par, kWaitLimit)) {
                 atomicOr(C.status, TQ_DEVERR_TIMEOUT);
-                *s_abort = 1;
+                *e_abort = 1;
             }
             umma::fence_after_sync();
-            const RowInfo ri = rinfo[rl];
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (*e_abort) break;
+            const RowInfo ri = rinfo[row];
             const bool zero = (ri.flag & 8) != 0;
-            uint32_t cw[NKW];
-#pragma unroll
-            for (int w = 0; w < NKW; ++w) cw[w] = 0u;
-            uint32_t cmask[4] = {0u, 0u, 0u, 0u};
-            float gsq = 0.f;
-#pragma unroll
-            for (int cb = 0; cb < D / 32; ++cb) {
-                float y[32];
-                umma::ld32(tY + (static_cast<uint32_t>(32 * warp) << 16) + 32 * cb, y);
-                float rs[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int i = 32 * cb + j;
-                    const float z = y[j] * ri.zscale;
-                    int bi = static_cast<int>(fmaf(z, kBinScale, kBinOrigin * kBinScale));
-                    bi = min(max(bi, 0), 1023);
-                    const uint32_t bt = bins[bi];
-                    uint32_t code = bt & 0xFu;
-                    if (bt & 0x10u) {
-                        const float th = s_thr[bt >> 8];
-                        code += (z >= th) ? 1u : 0u;
-                        if (fabsf(z - th) < kCodeGuard) cmask[cb] |= 1u << j;
-                    }
-                    if (zero) code = 0u;
-                    const float r = zero ? 0.f : z - s_cent[code];
-                    gsq = fmaf(r, r, gsq);
-                    const int o = i * KB;  // compile-time
-                    cw[o >> 5] |= code << (o & 31);
-                    if ((o & 31) + KB > 32) cw[(o >> 5) + 1] |= code >> (32 - (o & 31));
-                    rs[j] = r * 4096.f;
-                }
-                uint32_t rh[16], rlo[16];
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float h0 = __half2float(__float2half_rn(rs[2 * q]));
-                    const float h1 = __half2float(__float2half_rn(rs[2 * q + 1]));
-                    rh[q] = pack_h2(h0, h1);
-                    rlo[q] = pack_h2(rs[2 * q] - h0, rs[2 * q + 1] - h1);
-                }
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const uint32_t off = umma::core_offset(rl, 32 * cb + 8 * c4, D);
-                    *reinterpret_cast<uint4 *>(smem + kOffTA + off) =
-                        make_uint4(rh[4 * c4], rh[4 * c4 + 1], rh[4 * c4 + 2], rh[4 * c4 + 3]);
-                    *reinterpret_cast<uint4 *>(smem + kOffTB + off) =
-                        make_uint4(rlo[4 * c4], rlo[4 * c4 + 1], rlo[4 * c4 + 2], rlo[4 * c4 + 3]);
-                }
-            }
-            const float rn = sqrtf(gsq);
-            int flag = ri.flag;
-            if (cmask[0] | cmask[1] | cmask[2] | cmask[3]) flag |= 1;
-            uint32_t n16g16 = ri.n16g16;
-            if (C.qjl && !zero) {
-                const float gam = rn / sqrtd;
-                n16g16 |= static_cast<uint32_t>(float_to_bf16_bits(gam)) << 16;
-                // distance of gamma to the nearest bf16 rounding midpoint, relative
-                int ge;
-                const float fr = frexpf(gam, &ge);          // gam = fr 2^ge, fr in [0.5, 1)
-                const float u = fr * 256.f;                  // bf16 keeps 8 significant bits
-                const float dm = fabsf(u - floorf(u) - 0.5f) / u;
-                if (dm < kGammaGuard) flag |= 4;
-            }
-#pragma unroll
-            for (int w = 0; w < NKW; ++w) scodes[rl * 16 + w] = cw[w];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) smask[rl * 8 + w] = cmask[w];
-            rinfo[rl].flag = flag;
-            rinfo[rl].rn = rn;
-            rinfo[rl].n16g16 = n16g16;
+            float gsq;
+            int fl;
+            if (hf == 0)
+                epilogue_rotation<KB, 0>(smem, tY, warp, row, ri.zscale, zero, C.qjl != 0, bins, s_cent, s_thr, scodes, smask, gsq, fl);
+            else
+                epilogue_rotation<KB, 1>(smem, tY, warp, row, ri.zscale, zero, C.qjl != 0, bins, s_cent, s_thr, scodes, smask, gsq, fl);
+            s_gsq[row * 2 + hf] = gsq;
+            s_flagp[row * 2 + hf] = fl;
             umma::fence_proxy_async();
             umma::fence_before_sync();
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            asm volatile("bar.sync 1, 256;" ::: "memory");
             umma::fence_after_sync();
+            if (tid == 0)
+                asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(mbarYfree))
+                             : "memory");
+            const float rn = sqrtf(s_gsq[row * 2] + s_gsq[row * 2 + 1]);
+            int flag = ri.flag | s_flagp[row * 2] | s_flagp[row * 2 + 1];
+            uint32_t n16g16 = ri.n16g16;
             if (C.qjl) {
-                // ---- projection MMAs: P = (R_hi + R_lo)(S_hi + S_lo)^T, small terms first ----
-                if (tid == 0 && !*s_abort) {
+                if (tid == 0) {
+                    // ---- projection MMAs: P = (R_hi + R_lo)(S_hi + S_lo)^T, small terms first ----
                     const uint32_t aoff[3] = {kOffTB, kOffTA, kOffTA};
                     const uint32_t boff[3] = {kOffSH, kOffSL, kOffSH};
 #pragma unroll 1
@@ -527,157 +643,156 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                         }
                     umma::commit(mbarP);
                 }
-                ok = umma::mbar_wait_bounded(mbarP, phase, kWaitLimit);
-                if (!ok) {
+                if (!umma::mbar_wait_bounded(mbarP, par, kWaitLimit)) {
                     atomicOr(C.status, TQ_DEVERR_TIMEOUT);
-                    *s_abort = 1;
+                    *e_abort = 1;
                 }
                 umma::fence_after_sync();
                 const float guard = kSignGuard * rn * 16777216.f;  // P = 2^24 p (z units)
-                uint32_t smk[4];
-#pragma unroll 1
-                for (int cb = 0; cb < D / 32; ++cb) {
-                    float p[32];
-                    umma::ld32(tP + (static_cast<uint32_t>(32 * warp) << 16) + 32 * cb, p);
-                    uint32_t bits = 0u, near = 0u;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        bits |= (p[j] >= 0.f ? 1u : 0u) << j;
-                        near |= (fabsf(p[j]) < guard ? 1u : 0u) << j;
-                    }
-                    if (zero) bits = near = 0u;
-                    ssigns[rl * 4 + cb] = bits;
-                    smask[rl * 8 + 4 + cb] = near;
-                    smk[cb] = near;
-                }
-                if (smk[0] | smk[1] | smk[2] | smk[3]) rinfo[rl].flag = flag | 2;
-            }
-        }
-        phase ^= 1u;
-        __syncthreads();
-        if (*s_abort) break;
-        // ---- exact re-decisions, one warp per flagged row ----
-        for (int rl = warp; rl < TM; rl += kWarps) {
-            const int flag = rinfo[rl].flag;
-            if ((flag & 7) == 0 || (flag & 8) || rinfo[rl].dst < 0) continue;
-            // reload the key row (exact fp32), scaled by a power of two
-            const int64_t r = r0 + rl;
-            const int64_t t = r / Hkv;
-            const uint16_t *src = kin + t * ks + static_cast<int64_t>(r - t * Hkv) * D;
-            double *scratch = scratch_all + warp * D;
-            float *kw = reinterpret_cast<float *>(scratch);
-            float kx[D / 32];
-            float mx = 0.f;
-#pragma unroll
-            for (int m = 0; m < D / 32; ++m) {
-                kx[m] = bf16_to_float(src[lane + 32 * m]);
-                mx = fmaxf(mx, fabsf(kx[m]));
-            }
-            mx = warp_max(mx);
-            int ex;
-            frexpf(mx, &ex);
-            const float sc = ldexpf(1.f, -ex);
-            float s = 0.f, c = 0.f;
-#pragma unroll
-            for (int m = 0; m < D / 32; ++m) {
-                kx[m] *= sc;
-                dot2_step(s, c, kx[m], kx[m]);
-                kw[lane + 32 * m] = kx[m];
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float s2 = __shfl_xor_sync(0xffffffffu, s, o), c2 = __shfl_xor_sync(0xffffffffu, c, o);
-                float tt, e;
-                two_sum(s, s2, tt, e);
-                s = tt;
-                c = __fadd_rn(c, __fadd_rn(c2, e));
-            }
-            const double n_sc = sqrt(static_cast<double>(s) + static_cast<double>(c));
-            __syncwarp();
-            uint32_t *cw = scodes + rl * 16;
-            bool redo = (flag & 4) != 0;
-            // codes near a threshold
-            if (!redo && (flag & 1)) {
-                for (int w = 0; w < 4 && !redo; ++w) {
-                    uint32_t m = smask[rl * 8 + w];
-                    while (m && !redo) {
-                        const int j = 32 * w + __ffs(m) - 1;
-                        m &= m - 1;
-                        const double z = warp_dot_df(C.Pi + j * D, kw) * (sqrt(static_cast<double>(D)) / n_sc);
-                        uint32_t code = 0;
-                        for (int tt = 0; tt < nthr; ++tt) code += (static_cast<double>(C.thresholds[tt]) <= z);
-                        if (code != get_code<KB>(cw, j)) redo = true;  // the residual changes: redo the row
-                    }
+                const int sf = epilogue_signs(tP, warp, row, hf, guard, zero, ssigns, smask);
+                s_flags[row * 2 + hf] = sf;
+                if (!zero) {
+                    const float gam = rn / sqrtd;
+                    n16g16 |= static_cast<uint32_t>(float_to_bf16_bits(gam)) << 16;
+                    // distance of gamma to the nearest bf16 rounding midpoint, relative
+                    int ge;
+                    const float fr = frexpf(gam, &ge);  // gam = fr 2^ge, fr in [0.5, 1)
+                    const float u = fr * 256.f;         // bf16 keeps 8 significant bits
+                    if (fabsf(u - floorf(u) - 0.5f) / u < kGammaGuard) flag |= 4;
                 }
             }
-            if (redo) {
-                exact_row<KB>(C, kw, n_sc, cw, ssigns + rl * 4, &rinfo[rl].n16g16, scratch, ldexp(n_sc, ex));
-                continue;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (*e_abort) break;
+            if (C.qjl) flag |= s_flags[row * 2] | s_flags[row * 2 + 1];
+            if (zero) flag = 8 | (ri.flag & ~7);
+            if (hf == 0) {
+                rinfo[row].flag = flag;
+                rinfo[row].rn = rn;
+                rinfo[row].n16g16 = n16g16;
             }
-            // signs near zero: p_i = sqrt(d) (M_i . k) / n - S_i . c
-            if (flag & 2) {
-                for (int w = 0; w < 4; ++w) {
-                    uint32_t m = smask[rl * 8 + 4 + w];
-                    while (m) {
-                        const int i = 32 * w + __ffs(m) - 1;
-                        m &= m - 1;
-                        const double mk = warp_dot_df(C.M_hi + i * D, kw) + warp_dot_df(C.M_lo + i * D, kw);
-                        // S_i . c in compensated arithmetic
-                        float sh = 0.f, scc = 0.f;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            // ---- exact re-decisions, one warp per flagged row (scratch in tile B) ----
+            for (int rl = warp; rl < TM; rl += kEpiWarps) {
+                const int flg = rinfo[rl].flag;
+                if ((flg & 7) == 0 || (flg & 8) || rinfo[rl].dst < 0) continue;
+                const int64_t r = r0 + rl;
+                const int64_t t = r / Hkv;
+                const uint16_t *src = kin + t * ks + static_cast<int64_t>(r - t * Hkv) * D;
+                double *scratch = reinterpret_cast<double *>(smem + kOffTB) + warp * D;
+                float *kw = reinterpret_cast<float *>(scratch);
+                float kx[D / 32];
+                float mx = 0.f;
 #pragma unroll
-                        for (int mm = 0; mm < D / 32; ++mm) {
-                            const int j = lane + 32 * mm;
-                            dot2_step(sh, scc, __ldg(C.S + i * D + j), s_cent[get_code<KB>(cw, j)]);
-                        }
+                for (int m = 0; m < D / 32; ++m) {
+                    kx[m] = bf16_to_float(src[lane + 32 * m]);
+                    mx = fmaxf(mx, fabsf(kx[m]));
+                }
+                mx = warp_max(mx);
+                int ex;
+                frexpf(mx, &ex);
+                const float sc = ldexpf(1.f, -ex);
+                float s = 0.f, c = 0.f;
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) {
-                            const float s2 = __shfl_xor_sync(0xffffffffu, sh, o), c2 = __shfl_xor_sync(0xffffffffu, scc, o);
-                            float tt, e;
-                            two_sum(sh, s2, tt, e);
-                            sh = tt;
-                            scc = __fadd_rn(scc, __fadd_rn(c2, e));
+                for (int m = 0; m < D / 32; ++m) {
+                    kx[m] *= sc;
+                    dot2_step(s, c, kx[m], kx[m]);
+                    kw[lane + 32 * m] = kx[m];
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float s2 = __shfl_xor_sync(0xffffffffu, s, o), c2 = __shfl_xor_sync(0xffffffffu, c, o);
+                    float tt, e;
+                    two_sum(s, s2, tt, e);
+                    s = tt;
+                    c = __fadd_rn(c, __fadd_rn(c2, e));
+                }
+                const double n_sc = sqrt(static_cast<double>(s) + static_cast<double>(c));
+                __syncwarp();
+                uint32_t *cw = scodes + rl * 16;
+                bool redo = (flg & 4) != 0;
+                if (!redo && (flg & 1)) {  // codes near a threshold
+                    for (int w = 0; w < 4 && !redo; ++w) {
+                        uint32_t m = smask[rl * 8 + w];
+                        while (m && !redo) {
+                            const int j = 32 * w + __ffs(m) - 1;
+                            m &= m - 1;
+                            const double z = warp_dot_df(C.Pi + j * D, kw) * (sqrt(static_cast<double>(D)) / n_sc);
+                            uint32_t code = 0;
+                            for (int tt = 0; tt < nthr; ++tt) code += (static_cast<double>(C.thresholds[tt]) <= z);
+                            if (code != get_code<KB>(cw, j)) redo = true;  // the residual changes: redo the row
                         }
-                        const double sc_dot = static_cast<double>(sh) + static_cast<double>(scc);
-                        const double p = mk * (sqrt(static_cast<double>(D)) / n_sc) - sc_dot;
-                        if (lane == 0) {
-                            uint32_t &sw = ssigns[rl * 4 + w];
-                            const uint32_t bit = 1u << (i & 31);
-                            sw = (p >= 0.0) ? (sw | bit) : (sw & ~bit);
+                    }
+                }
+                if (redo) {
+                    exact_row<KB>(C, kw, n_sc, cw, ssigns + rl * 4, &rinfo[rl].n16g16, scratch, ldexp(n_sc, ex));
+                    continue;
+                }
+                if (flg & 2) {  // signs near zero: p_i = sqrt(d) (M_i . k) / n - S_i . c
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t m = smask[rl * 8 + 4 + w];
+                        while (m) {
+                            const int i = 32 * w + __ffs(m) - 1;
+                            m &= m - 1;
+                            const double mk = warp_dot_df(C.M_hi + i * D, kw) + warp_dot_df(C.M_lo + i * D, kw);
+                            float sh = 0.f, scc = 0.f;
+#pragma unroll
+                            for (int mm = 0; mm < D / 32; ++mm) {
+                                const int j = lane + 32 * mm;
+                                dot2_step(sh, scc, __ldg(C.S + i * D + j), C.centroids[get_code<KB>(cw, j)]);
+                            }
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) {
+                                const float s2 = __shfl_xor_sync(0xffffffffu, sh, o);
+                                const float c2 = __shfl_xor_sync(0xffffffffu, scc, o);
+                                float tt, e;
+                                two_sum(sh, s2, tt, e);
+                                sh = tt;
+                                scc = __fadd_rn(scc, __fadd_rn(c2, e));
+                            }
+                            const double p = mk * (sqrt(static_cast<double>(D)) / n_sc) -
+                                             (static_cast<double>(sh) + static_cast<double>(scc));
+                            if (lane == 0) {
+                                uint32_t &sw = ssigns[rl * 4 + w];
+                                const uint32_t bit = 1u << (i & 31);
+                                sw = (p >= 0.0) ? (sw | bit) : (sw & ~bit);
+                            }
+                            __syncwarp();
                         }
-                        __syncwarp();
                     }
                 }
             }
-        }
-        __syncthreads();
-        // ---- key records ----
-        if (tid < TM) {
-            const RowInfo ri = rinfo[tid];
-            if (ri.dst >= 0) {
-                const bool zero = (ri.flag & 8) != 0;
-                uint8_t *krec = kc + ri.dst * G.k_page;
-                uint4 *cd = reinterpret_cast<uint4 *>(krec + static_cast<int64_t>(ri.off) * C.k_code_bytes);
-                const uint32_t *cw = scodes + tid * 16;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            // ---- key records: thread (row, half) ----
+            const RowInfo rf = rinfo[row];
+            if (rf.dst >= 0) {
+                const bool z0 = (rf.flag & 8) != 0;
+                uint8_t *krec = kc + rf.dst * G.k_page;
+                uint32_t *cd = reinterpret_cast<uint32_t *>(krec + static_cast<int64_t>(rf.off) * C.k_code_bytes);
+                const uint32_t *cw = scodes + row * 16;
 #pragma unroll
-                for (int w = 0; w < NKW; w += 4)
-                    cd[w / 4] = zero ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(cw[w], cw[w + 1], cw[w + 2], cw[w + 3]);
-                *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * ri.off) =
-                    zero ? 0 : static_cast<uint16_t>(ri.n16g16 & 0xffffu);
+                for (int w = 0; w < NKW / 2; ++w) cd[hf * (NKW / 2) + w] = z0 ? 0u : cw[hf * (NKW / 2) + w];
                 if (C.qjl) {
-                    const uint32_t *sw = ssigns + tid * 4;
-                    *reinterpret_cast<uint4 *>(krec + G.k_sign_off + static_cast<int64_t>(ri.off) * C.k_sign_bytes) =
-                        zero ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(sw[0], sw[1], sw[2], sw[3]);
-                    *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * ri.off) =
-                        zero ? 0 : static_cast<uint16_t>(ri.n16g16 >> 16);
+                    const uint32_t *sw = ssigns + row * 4;
+                    uint2 *sd = reinterpret_cast<uint2 *>(krec + G.k_sign_off + static_cast<int64_t>(rf.off) * C.k_sign_bytes);
+                    sd[hf] = z0 ? make_uint2(0u, 0u) : make_uint2(sw[2 * hf], sw[2 * hf + 1]);
+                }
+                if (hf == 0) {
+                    *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * rf.off) =
+                        z0 ? 0 : static_cast<uint16_t>(rf.n16g16 & 0xffffu);
+                    if (C.qjl)
+                        *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * rf.off) =
+                            z0 ? 0 : static_cast<uint16_t>(rf.n16g16 >> 16);
                 }
             }
+            asm volatile("bar.sync 1, 256;" ::: "memory");
         }
-        __syncthreads();
     }
     // ---- teardown: no MMA may still run when TMEM is freed ----
-    if (*s_abort && tid == 0) {
-        umma::mbar_wait_bounded(mbarY, phase ^ 1u, kWaitLimit);
-        umma::mbar_wait_bounded(mbarP, phase ^ 1u, kWaitLimit);
+    __syncthreads();
+    if (*e_abort || *p_abort) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < 200000000LL) {  // bounded grace period for in-flight tensor-core work
+        }
     }
     umma::fence_before_sync();
     __syncthreads();
