@@ -7,16 +7,20 @@
 // Tile = 128 token-heads; one persistent CTA per SM, 384 threads in two roles
 // that overlap consecutive tiles:
 //  producers (warps 8-11)
-//  1. load the keys of the next tile, take the norm in fp32 (sum of exact
-//     squares) and convert exactly to fp16 after a power-of-two scale 2^e per row;
+//  1. issue every global load of the tile's keys (and the first value rows),
+//     take each key's norm in fp32 (sum of exact squares) and convert it
+//     exactly to fp16 after a power-of-two scale 2^e per row;
 //  2. issue Y = K' (Pi 2^10)^T on the tensor cores once the epilogue has read
 //     the previous Y: Pi 2^10 is split into fp16 high and low parts, two MMA
 //     terms, ~22-bit operands, fp32 accumulation;
-//  3. compress the values of the tile (as in tq_compress.cu), independent of keys.
+//  3. quantise the values of the tile (one lane per 32 channels), loading the
+//     next rows while the current ones are quantised; the next tile is
+//     prefetched into L2 by the bulk-copy engine.
 //  epilogue (warps 0-7; warp w reads TMEM lane quarter w % 4, column half w / 4)
-//  4. z = Y sqrt(d) / (n 2^(10+e)), codes from a bin table, residual
-//     r = z - c[code], gamma = ||r|| / sqrt(d); r 2^12 is split into fp16 high /
-//     low parts for the next MMA;
+//  4. z = Y sqrt(d) / (n 2^(10+e)); a 256-entry bin table gives, in one
+//     shared-memory load, the one threshold near z and the centroids on both
+//     sides of it; residual r = z - c[code], gamma = ||r|| / sqrt(d); r 2^12 is
+//     split into fp16 high / low parts for the next MMA;
 //  5. QJL: P = (R 2^12)(S 2^12)^T, three MMA terms (hi.hi, hi.lo, lo.hi); the
 //     sign of P is the sign of S r;
 //  6. decisions within a guard band of a threshold, a sign boundary or a bf16
@@ -60,14 +64,22 @@ constexpr uint32_t kOffSigns = kOffCodes + TM * 64;  // [TM][4] u32 sign bits
 constexpr uint32_t kOffMask = kOffSigns + TM * 16;   // [TM][8] u32: code guard mask (4), sign guard mask (4)
 constexpr uint32_t kOffRow = kOffMask + TM * 32;     // [3][TM] RowInfo (tile index mod 3)
 constexpr uint32_t kOffPart = kOffRow + 3 * TM * 32; // [TM][2] gsq partials, [TM][2] code flags, [TM][2] sign flags
-constexpr uint32_t kOffBins = kOffPart + TM * 24;    // [1024] u16 code-bin table
-constexpr uint32_t kOffBook = kOffBins + 2048;       // [16] centroids, [16] thresholds (times 2^12)
-constexpr uint32_t kOffMisc = kOffBook + 128;        // mbarriers, TMEM slot, abort flags
+constexpr uint32_t kOffBins = kOffPart + TM * 24;    // [256] float4 code bins (below)
+constexpr uint32_t kOffMisc = kOffBins + 256 * 16;   // mbarriers, TMEM slot, abort flags
 constexpr uint32_t kSmemBytes = kOffMisc + 64;
+static_assert(kSmemBytes <= 232448, "shared memory map exceeds the per-block limit");
 
 constexpr uint32_t kSBO = (D / 8) * 128;  // 2048
 constexpr uint32_t kIdesc = umma::idesc_f16(128, 128);
-constexpr float kBinScale = 64.f, kBinOrigin = 8.f;  // bin = floor((z + 8) * 64), 1024 bins
+
+// Code bins.  The epilogue works on z' = 2^12 z.  Bin b holds the z with
+// round(8 z + 96) = b, i.e. z in [(b - 96.5) / 8, (b - 95.5) / 8]; |z| <= sqrt(d)
+// = 11.4 keeps b in [5, 187].  Adding z' / 512 + 96 to 1.5 * 2^23 in one fused
+// multiply-add rounds to that integer and leaves it in the low mantissa bits.
+// Lloyd-Max thresholds for N(0,1) are at least 0.25 apart for b_k <= 4, so a
+// bin holds at most one threshold.  Entry: {threshold (or +inf), centroid below
+// it, centroid above it, code below it (as raw bits)}, all but the code times 2^12.
+constexpr float kBinMagic = 12582912.f + 96.f;
 
 struct RowInfo {     // 32 bytes per row
     int64_t dst;     // record index (block * Hkv + head) or -1
@@ -126,7 +138,7 @@ __device__ __forceinline__ void set_code(uint32_t *w, int j, uint32_t v)
 
 // The whole key row in compensated arithmetic, by one warp (see tq_compress.cu).
 template <int KB>
-__device__ void exact_row(const Codec &C, const float *kw, double n_sc, uint32_t *codes, uint32_t *signs,
+__device__ __noinline__ void exact_row(const Codec &C, const float *kw, double n_sc, uint32_t *codes, uint32_t *signs,
                           uint32_t *n16g16, double *scratch, double n_true)
 {
     constexpr int E = D / 32;
@@ -201,73 +213,58 @@ __device__ void exact_row(const Codec &C, const float *kw, double n_sc, uint32_t
 }
 
 
-// Epilogue 1 for one (row, column half): codes, guard mask, residual split into
-// fp16 hi / lo operands, and the partial sum of squares of the residual.
-template <int KB, int HF>
-__device__ __forceinline__ void epilogue_rotation(unsigned char *smem, uint32_t tY, int warp, int row, float zscale,
-                                                  bool zero, bool qjl, const uint16_t *bins, const float *s_cent,
-                                                  const float *s_thr, uint32_t *scodes, uint32_t *smask,
-                                                  float &gsq_out, int &flag_out)
+// Epilogue 1 for one (row, 32-column block cb): codes, guard mask, residual
+// split into fp16 hi / lo operands (QJL only), and the block's sum of squares of
+// the residual.  32 columns are exactly KB code words.
+template <int KB>
+__device__ __forceinline__ float epilogue_rotation_block(unsigned char *smem, uint32_t tY, int warp, int row, int cb,
+                                                         float zs, bool qjl, const float4 *bins, uint32_t *scodes,
+                                                         uint32_t *smask)
 {
-    constexpr int C0 = 64 * HF;
-    constexpr int W0 = C0 * KB / 32;  // first code word of this half
-    constexpr int NW = 64 * KB / 32;  // code words of this half
-    uint32_t cw[NW + 1];
+    float y[32];
+    umma::ld32(tY + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 32 * cb, y);
+    uint32_t cw[KB];
 #pragma unroll
-    for (int w = 0; w <= NW; ++w) cw[w] = 0u;
-    uint32_t cmask[2] = {0u, 0u};
+    for (int w = 0; w < KB; ++w) cw[w] = 0u;
+    uint32_t cmask = 0u;
     float gsq = 0.f;
-    const float zs = zscale * 4096.f;  // z' = 2^12 z
 #pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-        float y[16];
-        umma::ld16(tY + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + C0 + 16 * cb, y);
-        float rs[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int i = 16 * cb + j;  // column inside the half (compile-time)
-            const float z = y[j] * zs;
-            int bi = static_cast<int>(fmaf(z, kBinScale / 4096.f, kBinOrigin * kBinScale));
-            bi = min(max(bi, 0), 1023);
-            const uint32_t bt = bins[bi];
-            uint32_t code = bt & 0xFu;
-            if (bt & 0x10u) {
-                const float th = s_thr[bt >> 8];
-                code += (z >= th) ? 1u : 0u;
-                if (fabsf(z - th) < kCodeGuard * 4096.f) cmask[i >> 5] |= 1u << (i & 31);
-            }
-            if (zero) code = 0u;
-            const float r = zero ? 0.f : z - s_cent[code];
-            gsq = fmaf(r, r, gsq);
-            const int o = i * KB;  // bit offset inside the half (compile-time)
-            cw[o >> 5] |= code << (o & 31);
-            if ((o & 31) + KB > 32) cw[(o >> 5) + 1] |= code >> (32 - (o & 31));
-            rs[j] = r;
-        }
-        uint32_t rh[8], rlo[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const __half2 hh = __floats2half2_rn(rs[2 * q], rs[2 * q + 1]);
-            const float2 hf = __half22float2(hh);
-            rh[q] = *reinterpret_cast<const uint32_t *>(&hh);
-            rlo[q] = pack_h2(rs[2 * q] - hf.x, rs[2 * q + 1] - hf.y);
-        }
-        if (!qjl) continue;  // without QJL the key tile buffer already holds the next tile
-#pragma unroll
-        for (int c4 = 0; c4 < 2; ++c4) {
-            const uint32_t off = umma::core_offset(row, C0 + 16 * cb + 8 * c4, D);
-            *reinterpret_cast<uint4 *>(smem + kOffTA + off) =
-                make_uint4(rh[4 * c4], rh[4 * c4 + 1], rh[4 * c4 + 2], rh[4 * c4 + 3]);
-            *reinterpret_cast<uint4 *>(smem + kOffTB + off) =
-                make_uint4(rlo[4 * c4], rlo[4 * c4 + 1], rlo[4 * c4 + 2], rlo[4 * c4 + 3]);
-        }
+    for (int i = 0; i < 32; ++i) {
+        const float z = y[i] * zs;
+        const uint32_t bi = __float_as_uint(fmaf(z, 1.f / 512.f, kBinMagic)) & 0xFFu;
+        const float4 e = bins[bi];
+        const float dz = z - e.x;
+        const bool up = dz >= 0.f;
+        if (fabsf(dz) < kCodeGuard * 4096.f) cmask |= 1u << i;
+        const uint32_t code = __float_as_uint(e.w) + (up ? 1u : 0u);
+        const float r = z - (up ? e.z : e.y);
+        gsq = fmaf(r, r, gsq);
+        const int o = i * KB;  // compile-time bit offset inside the block
+        cw[o >> 5] |= code << (o & 31);
+        if ((o & 31) + KB > 32) cw[(o >> 5) + 1] |= code >> (32 - (o & 31));
+        y[i] = r;
     }
 #pragma unroll
-    for (int w = 0; w < NW; ++w) scodes[row * 16 + W0 + w] = cw[w];
-    smask[row * 8 + 2 * HF] = cmask[0];
-    smask[row * 8 + 2 * HF + 1] = cmask[1];
-    gsq_out = gsq * (1.f / 16777216.f);  // back to z units
-    flag_out = (cmask[0] | cmask[1]) ? 1 : 0;
+    for (int w = 0; w < KB; ++w) scodes[row * 16 + KB * cb + w] = cw[w];
+    smask[row * 8 + cb] = cmask;
+    if (qjl) {  // without QJL the key tile buffer already holds the next tile
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+            uint32_t rh[4], rlo[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float a = y[8 * c8 + 2 * q], b = y[8 * c8 + 2 * q + 1];
+                const __half2 hh = __floats2half2_rn(a, b);
+                const float2 hf = __half22float2(hh);
+                rh[q] = *reinterpret_cast<const uint32_t *>(&hh);
+                rlo[q] = pack_h2(a - hf.x, b - hf.y);
+            }
+            const uint32_t off = umma::core_offset(row, 32 * cb + 8 * c8, D);
+            *reinterpret_cast<uint4 *>(smem + kOffTA + off) = make_uint4(rh[0], rh[1], rh[2], rh[3]);
+            *reinterpret_cast<uint4 *>(smem + kOffTB + off) = make_uint4(rlo[0], rlo[1], rlo[2], rlo[3]);
+        }
+    }
+    return gsq;
 }
 
 // Epilogue 2 for one (row, column half): QJL sign bits and the sign guard mask.
@@ -296,7 +293,107 @@ __device__ __forceinline__ int epilogue_signs(uint32_t tP, int warp, int row, in
     return flag;
 }
 
-template <int KB>
+// Exact re-decision of 32 value codes (see quantize_values32).
+template <int VB>
+__device__ __noinline__ void values32_exact(const uint32_t *wd, float zv, float sv, float inv, uint32_t *cw)
+{
+    constexpr int L = (1 << VB) - 1;
+    for (int k = 0; k < VB; ++k) cw[k] = 0u;
+    for (int e = 0; e < 32; ++e) {
+        const uint32_t wv = wd[e >> 1];
+        const float x = (e & 1) ? __uint_as_float(wv & 0xffff0000u) : __uint_as_float(wv << 16);
+        int q = 0;
+        if (sv != 0.f) {
+            float a, ea;
+            two_sum(x, -zv, a, ea);
+            q = static_cast<int>(fminf(fmaxf(floorf(fmaf(x - zv, inv, 0.5f)), 0.f), static_cast<float>(L)));
+            while (q < L && __fadd_rn(__fsub_rn(a, (q + 0.5f) * sv), ea) >= 0.f) ++q;
+            while (q > 0 && !(__fadd_rn(__fsub_rn(a, (q - 0.5f) * sv), ea) >= 0.f)) --q;
+        }
+        const int o = e * VB;
+        cw[o >> 5] |= static_cast<uint32_t>(q) << (o & 31);
+        if ((o & 31) + VB > 32) cw[(o >> 5) + 1] |= static_cast<uint32_t>(q) >> (32 - (o & 31));
+    }
+}
+
+// Values: one lane holds 32 consecutive channels (four 16-byte words) of a row;
+// lanes_per_group = g / 32 neighbouring lanes share a group.  Computes the
+// group's fp16 scale and zero and the lane's 32 codes packed LSB-first into VB
+// words: code = clamp(floor((x - zero) / scale + 0.5), 0, 2^VB - 1).
+//
+// f = (x - zero) / scale + 0.5 + 192 in one fused multiply-add leaves
+// floor(.) in bits 16.. and the fraction in the low 16 bits of f (the ulp of
+// [128, 256) is 2^-16).  An element whose fraction lies within 4 ulps of an
+// integer n is re-decided exactly: x - zero as an exact float pair against
+// (n - 1/2) scale, which is exact in fp32.  A lane whose zero is not its min
+// exactly (values outside the fp16 normal range) or whose scale is subnormal
+// re-decides every code that way, with clamping.
+template <int VB>
+__device__ __forceinline__ void quantize_values32(const uint4 (&w4)[4], int lanes_per_group, uint32_t (&cw)[VB],
+                                                  uint32_t &meta)
+{
+    constexpr int L = (1 << VB) - 1;
+    const uint32_t wd[16] = {w4[0].x, w4[0].y, w4[0].z, w4[0].w, w4[1].x, w4[1].y, w4[1].z, w4[1].w,
+                             w4[2].x, w4[2].y, w4[2].z, w4[2].w, w4[3].x, w4[3].y, w4[3].z, w4[3].w};
+    __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162 *>(&wd[0]), mx2 = mn2;
+#pragma unroll
+    for (int k = 1; k < 16; ++k) {
+        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&wd[k]);
+        mn2 = __hmin2(mn2, v);
+        mx2 = __hmax2(mx2, v);
+    }
+    float mn = fminf(__low2float(mn2), __high2float(mn2));
+    float mx = fmaxf(__low2float(mx2), __high2float(mx2));
+    if (lanes_per_group >= 2) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    }
+    if (lanes_per_group >= 4) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    }
+    float dh, de;
+    two_sum(mx, -mn, dh, de);
+    // (max - min) / L with L in {3, 7, 15}: exact in fp32 or a non-terminating
+    // binary fraction, so one rounding to fp32 then fp16 equals one rounding to fp16.
+    const __half s16 = (de == 0.f) ? __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)))
+                                   : __double2half((static_cast<double>(mx) - static_cast<double>(mn)) / L);
+    const __half z16 = __float2half_rn(mn);
+    meta = static_cast<uint32_t>(__half_as_ushort(s16)) | (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
+    const float sv = __half2float(s16), zv = __half2float(z16);
+    const float inv = (sv != 0.f) ? __frcp_rn(sv) : 0.f;
+#pragma unroll
+    for (int k = 0; k < VB; ++k) cw[k] = 0u;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        const uint32_t wv = wd[e >> 1];
+        const float x = (e & 1) ? __uint_as_float(wv & 0xffff0000u) : __uint_as_float(wv << 16);
+        const uint32_t fb = __float_as_uint(fmaf(x - zv, inv, 192.5f));
+        uint32_t code = (fb >> 16) & static_cast<uint32_t>(L);
+        if (((fb + 4u) & 0xFFF8u) == 0u) {
+            // within 4 ulps of the boundary (n - 1/2) scale between codes n - 1 and n:
+            // compare x - zero (an exact pair) with it exactly
+            const uint32_t n = ((fb + 0x8000u) >> 16) & 0x1Fu;
+            const float m = fmaf(static_cast<float>(n), sv, -0.5f * sv);
+            float a, ea;
+            two_sum(x, -zv, a, ea);
+            code = (__fadd_rn(__fsub_rn(a, m), ea) >= 0.f) ? n : n - 1u;
+        }
+        const int o = e * VB;
+        cw[o >> 5] |= code << (o & 31);
+        if ((o & 31) + VB > 32) cw[(o >> 5) + 1] |= code >> (32 - (o & 31));
+    }
+    if (zv != mn || (sv != 0.f && sv < 6.103515625e-05f)) {
+        uint32_t wl[16], cl[VB];  // local copies: the rare exact path keeps the hot one in registers
+#pragma unroll
+        for (int k = 0; k < 16; ++k) wl[k] = wd[k];
+        values32_exact<VB>(wl, zv, sv, inv, cl);
+#pragma unroll
+        for (int k = 0; k < VB; ++k) cw[k] = cl[k];
+    }
+}
+
+template <int KB, int VB>
 __global__ void __launch_bounds__(kThreads, 1)
 compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
                    int64_t rows, int Hkv, int64_t ks, int64_t vs, const int64_t *__restrict__ slots,
@@ -311,9 +408,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     float *s_gsq = reinterpret_cast<float *>(smem + kOffPart);                 // [TM][2]
     int *s_flagp = reinterpret_cast<int *>(smem + kOffPart + TM * 8);          // [TM][2]
     int *s_flags = reinterpret_cast<int *>(smem + kOffPart + TM * 16);         // [TM][2]
-    uint16_t *bins = reinterpret_cast<uint16_t *>(smem + kOffBins);
-    float *s_cent = reinterpret_cast<float *>(smem + kOffBook);
-    float *s_thr = s_cent + 16;
+    float4 *bins = reinterpret_cast<float4 *>(smem + kOffBins);
     uint64_t *mbarY = reinterpret_cast<uint64_t *>(smem + kOffMisc);      // rotation MMA done
     uint64_t *mbarP = mbarY + 1;                                           // projection MMA done
     uint64_t *mbarConv = mbarY + 2;                                        // keys of the tile converted
@@ -325,26 +420,30 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float sqrtd = sqrtf(static_cast<float>(D));
     const int nthr = (1 << KB) - 1;
+    const bool small_rows = rows <= 0x7fffffffLL;
+    const int pshift = __ffs(G.P) - 1;  // the page size is a power of two
+    const int64_t cache_slots = num_blocks * G.P;
 
     // ---- once per CTA: B operands, code bins, barriers, tensor memory ----
     {
         const uint4 *img = reinterpret_cast<const uint4 *>(C.tc_image);
         uint4 *dst = reinterpret_cast<uint4 *>(smem);
         for (int e = tid; e < 131072 / 16; e += kThreads) dst[e] = __ldg(img + e);
-        for (int b = tid; b < 1024; b += kThreads) {
-            const float lo = static_cast<float>(b) / kBinScale - kBinOrigin;
-            const float hi = static_cast<float>(b + 1) / kBinScale - kBinOrigin;
+        if (tid < 256) {
+            const float lo = (static_cast<float>(tid) - 96.5f) * 0.125f - 1.f / 64.f;
+            const float hi = (static_cast<float>(tid) - 95.5f) * 0.125f + 1.f / 64.f;
             int below = 0, idx = -1;
             for (int t = 0; t < nthr; ++t) {
                 const float th = C.thresholds[t];
-                if (th < lo - 2.f * kCodeGuard) ++below;
-                else if (th <= hi + 2.f * kCodeGuard) idx = t;  // at most one threshold this close to a bin
+                if (th < lo) ++below;
+                else if (th <= hi) idx = t;
             }
-            bins[b] = static_cast<uint16_t>(below | (idx >= 0 ? (0x10 | (idx << 8)) : 0));
-        }
-        if (tid < 16) {  // in units of 2^-12 so the residual comes out pre-scaled for the MMA
-            s_cent[tid] = C.centroids[tid] * 4096.f;
-            s_thr[tid] = C.thresholds[tid] * 4096.f;
+            float4 e;
+            e.x = idx >= 0 ? C.thresholds[idx] * 4096.f : __int_as_float(0x7f800000);
+            e.y = C.centroids[below] * 4096.f;
+            e.z = C.centroids[idx >= 0 ? below + 1 : below] * 4096.f;
+            e.w = __uint_as_float(static_cast<uint32_t>(below));
+            bins[tid] = e;
         }
         if (tid == 0) {
             umma::mbar_init(mbarY, 1);
@@ -373,6 +472,54 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             const int64_t r0 = static_cast<int64_t>(tile) * TM;
             // three row-info buffers: the epilogue may still finish tile it-2 while tile it is converted
             RowInfo *rinfo = rinfo_all + buf * TM;
+            // keys and values of this CTA's next tile start streaming into L2 now
+            if (ptid < 2 && tile + static_cast<int>(gridDim.x) < num_tiles) {
+                const int64_t n0 = r0 + static_cast<int64_t>(gridDim.x) * TM;
+                const int64_t n1 = min(n0 + TM, rows);
+                const uint16_t *base = ptid == 0 ? kin : vin;
+                const int64_t stride = ptid == 0 ? ks : vs;
+                if (stride == static_cast<int64_t>(Hkv) * D) {
+                    l2_prefetch_bulk(base + n0 * D, static_cast<uint32_t>((n1 - n0) * D * 2));
+                } else {
+                    for (int64_t t = n0 / Hkv; t <= (n1 - 1) / Hkv; ++t)
+                        l2_prefetch_bulk(base + t * stride, static_cast<uint32_t>(Hkv * D * 2));
+                }
+            }
+            // ---- issue the tile's key loads (and the first value rows) before waiting:
+            // pass p covers rows 32 pw + 8 p + lane / 4; lane & 3 = sub takes key
+            // chunks sub + 4 j and value channels [32 sub, 32 sub + 32) ----
+            const int sub = lane & 3;
+            uint4 kr[4][4], va[4];
+            int64_t sl[4];
+            int hh[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const int64_t r = r0 + 32 * pw + 8 * p + (lane >> 2);
+                sl[p] = -1;
+                hh[p] = 0;
+                if (r < rows) {
+                    const int64_t t = small_rows ? static_cast<int64_t>(static_cast<uint32_t>(r) / static_cast<uint32_t>(Hkv))
+                                                 : r / Hkv;
+                    const int h = static_cast<int>(r - t * Hkv);
+                    hh[p] = h;
+                    const uint4 *ksrc = reinterpret_cast<const uint4 *>(kin + t * ks + static_cast<int64_t>(h) * D);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) kr[p][j] = ld_pinned(ksrc + sub + 4 * j);
+                    if (p == 0) {
+                        const uint4 *vsrc = reinterpret_cast<const uint4 *>(vin + t * vs + static_cast<int64_t>(h) * D);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) va[j] = ld_pinned(vsrc + 4 * sub + j);
+                    }
+                    sl[p] = ld_pinned_s64(slots + t);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) kr[p][j] = make_uint4(0u, 0u, 0u, 0u);
+                    if (p == 0) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) va[j] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            }
             // the key tile buffer is free once the previous tile's last MMA finished
             if (it > 0 && ptid == 0) {
                 if (!umma::mbar_wait_bounded(C.qjl ? mbarP : mbarY, (it - 1) & 1, kWaitLimit)) {
@@ -382,48 +529,33 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             }
             asm volatile("bar.sync 2, 128;" ::: "memory");
             if (*p_abort) break;
-            // ---- keys: slot, norm, power-of-two scale, exact fp16 conversion ----
-            // warp pw handles 8-row groups pw, pw+4, ...; lane: row 8g + (lane & 7), chunks (lane >> 3) + 4 i
-#pragma unroll 1
-            for (int grp = pw; grp < TM / 8; grp += 4) {
-                const int rl = 8 * grp + (lane & 7);
-                const int64_t r = r0 + rl;
-                int64_t dsti = -1;
-                int offi = 0;
-                const uint16_t *src = nullptr;
-                if (r < rows) {
-                    const int64_t t = r / Hkv;
-                    const int h = static_cast<int>(r - t * Hkv);
-                    const int64_t s = slots[t];
-                    if (s >= 0) {
-                        if (s < num_blocks * G.P) {
-                            const int64_t blk = s / G.P;
-                            offi = static_cast<int>(s - blk * G.P);
-                            dsti = blk * Hkv + h;
-                            src = kin + t * ks + static_cast<int64_t>(h) * D;
-                        } else if ((lane >> 3) == 0) {
-                            atomicOr(C.status, TQ_DEVERR_SLOT_RANGE);
-                        }
+            // ---- keys: norm, power-of-two scale, exact fp16 conversion into the A tile ----
+            int64_t dst[4];
+            int offs[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const int rl = 32 * pw + 8 * p + (lane >> 2);
+                const int64_t sp = sl[p];
+                dst[p] = -1;
+                offs[p] = 0;
+                if (sp >= 0) {
+                    if (sp < cache_slots) {
+                        dst[p] = (sp >> pshift) * Hkv + hh[p];
+                        offs[p] = static_cast<int>(sp & (G.P - 1));
+                    } else if (sub == 0) {
+                        atomicOr(C.status, TQ_DEVERR_SLOT_RANGE);
                     }
                 }
-                uint4 u[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    u[i] = src ? __ldg(reinterpret_cast<const uint4 *>(src) + (lane >> 3) + 4 * i) : make_uint4(0u, 0u, 0u, 0u);
-                float x[4][8];
                 float mx = 0.f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t w[4] = {kr[p][j].x, kr[p][j].y, kr[p][j].z, kr[p][j].w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        x[i][2 * e] = bf16_to_float(w[e] & 0xffffu);
-                        x[i][2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-                        mx = fmaxf(mx, fmaxf(fabsf(x[i][2 * e]), fabsf(x[i][2 * e + 1])));
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xffff0000u))));
                 }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
                 int ex = 0;
                 if (mx > 0.f) frexpf(mx, &ex);  // mx in [2^(ex-1), 2^ex)
                 // |k'| < 2^15; keys too small for a finite fp32 scale are redone exactly
@@ -431,25 +563,25 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 const float sc = ldexpf(1.f, tiny ? 126 : 15 - ex);
                 float ss = 0.f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t w[4] = {kr[p][j].x, kr[p][j].y, kr[p][j].z, kr[p][j].w};
                     uint32_t pk[4];
 #pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        const float a = x[i][e] * sc, b = x[i][e + 1] * sc;
+                    for (int e = 0; e < 4; ++e) {
+                        const float a = __uint_as_float(w[e] << 16) * sc, b = __uint_as_float(w[e] & 0xffff0000u) * sc;
                         ss = fmaf(a, a, ss);
                         ss = fmaf(b, b, ss);
-                        pk[e / 2] = pack_h2(a, b);
+                        pk[e] = pack_h2(a, b);
                     }
-                    const int c = (lane >> 3) + 4 * i;
-                    *reinterpret_cast<uint4 *>(smem + kOffTA + umma::core_offset(rl, 8 * c, D)) =
+                    *reinterpret_cast<uint4 *>(smem + kOffTA + umma::core_offset(rl, 8 * (sub + 4 * j), D)) =
                         make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
-                ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-                ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-                if (lane < 8) {
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                if (sub == 0) {
                     RowInfo ri;
-                    ri.dst = dsti;
-                    ri.off = offi;
+                    ri.dst = dst[p];
+                    ri.off = offs[p];
                     ri.flag = 0;
                     ri.zscale = 0.f;
                     ri.rn = 0.f;
@@ -492,105 +624,44 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                     *p_abort = 1;
                 }
             }
-            // ---- values of this tile (8 lanes per row, 16 channels per lane) ----
-            for (int rb = 4 * pw; rb < TM; rb += 16) {
-                const int rl = rb + (lane >> 3), sub = lane & 7;
-                const int64_t r = r0 + rl;
-                int64_t dst = -1;
-                int off = 0;
-                const uint16_t *vrow = nullptr;
-                if (r < rows) {
-                    const int64_t t = r / Hkv;
-                    const int h = static_cast<int>(r - t * Hkv);
-                    const int64_t s = slots[t];
-                    if (s >= 0 && s < num_blocks * G.P) {
-                        const int64_t blk = s / G.P;
-                        off = static_cast<int>(s - blk * G.P);
-                        dst = blk * Hkv + h;
-                        vrow = vin + t * vs + static_cast<int64_t>(h) * D;
-                    }
-                }
-                float x[16];
-                if (vrow) {
-                    const uint4 *vsrc = reinterpret_cast<const uint4 *>(vrow) + 2 * sub;
-                    const uint4 u0 = __ldg(vsrc), u1 = __ldg(vsrc + 1);
-                    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            // ---- values of this tile: pass p + 1 is loaded while pass p is quantised ----
+            const int lpg = C.group >> 5;  // lanes per group: 1, 2 or 4
+#pragma unroll 1
+            for (int p = 0; p < 4; ++p) {
+                uint4 vb[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        x[2 * e] = bf16_to_float(w[e] & 0xffffu);
-                        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-                    }
-                } else {
+                for (int j = 0; j < 4; ++j) vb[j] = make_uint4(0u, 0u, 0u, 0u);
+                const int64_t rn1 = r0 + 32 * pw + 8 * (p + 1) + (lane >> 2);
+                if (p < 3 && rn1 < rows) {
+                    const int64_t t = small_rows ? static_cast<int64_t>(static_cast<uint32_t>(rn1) / static_cast<uint32_t>(Hkv))
+                                                 : rn1 / Hkv;
+                    const uint4 *vsrc = reinterpret_cast<const uint4 *>(vin + t * vs + (rn1 - t * Hkv) * D);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) x[e] = 0.f;
+                    for (int j = 0; j < 4; ++j) vb[j] = ld_pinned(vsrc + 4 * sub + j);
                 }
-                float mn = x[0], mxv = x[0];
-#pragma unroll
-                for (int e = 1; e < 16; ++e) {
-                    mn = fminf(mn, x[e]);
-                    mxv = fmaxf(mxv, x[e]);
-                }
-                const int lpg = C.group / 16;  // lanes per group: 2, 4 or 8
-                for (int o = lpg >> 1; o > 0; o >>= 1) {
-                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-                    mxv = fmaxf(mxv, __shfl_xor_sync(0xffffffffu, mxv, o));
-                }
-                const int L = (1 << C.v_bits) - 1;
-                float dh, de;
-                two_sum(mxv, -mn, dh, de);
-                // (max - min) / L with L in {3, 7, 15} is exact in fp32 or a non-terminating
-                // binary fraction: one rounding to fp32 then fp16 equals one rounding to fp16.
-                const __half s16 = (de == 0.f) ? __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)))
-                                               : __double2half((static_cast<double>(mxv) - static_cast<double>(mn)) / L);
-                const __half z16 = __float2half_rn(mn);
-                const float sv = __half2float(s16), zv = __half2float(z16);
-                const float inv = (sv != 0.f) ? __frcp_rn(sv) : 0.f;
-                uint64_t cbits = 0u;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    int q = 0;
-                    if (sv != 0.f) {
-                        // fp32 guess; exact midpoint comparison only within 1e-3 of a rounding boundary
-                        const float tq = fmaf(x[e] - zv, inv, 0.5f);
-                        const float fl = floorf(tq);
-                        q = static_cast<int>(fminf(fmaxf(fl, 0.f), static_cast<float>(L)));
-                        const float fr = tq - fl;
-                        if (fr < 1e-3f || fr > 0.999f) {
-                            float a, ea;
-                            two_sum(x[e], -zv, a, ea);
-                            while (q < L && __fadd_rn(__fsub_rn(a, (q + 0.5f) * sv), ea) >= 0.f) ++q;
-                            while (q > 0 && !(__fadd_rn(__fsub_rn(a, (q - 0.5f) * sv), ea) >= 0.f)) --q;
-                        }
-                    }
-                    cbits |= static_cast<uint64_t>(q) << (e * C.v_bits);
-                }
-                uint8_t *vrec = (dst >= 0) ? vc + dst * G.v_page : nullptr;
-                uint32_t *vw = vrec ? reinterpret_cast<uint32_t *>(vrec + static_cast<int64_t>(off) * C.v_code_bytes) : nullptr;
-                if (C.v_bits == 3) {  // 48 bits per lane: lanes 2p, 2p+1 share the middle word
-                    const uint64_t other = __shfl_xor_sync(0xffffffffu, cbits, 1);
-                    if (vw) {
-                        const int p = sub >> 1;
-                        if ((sub & 1) == 0) {
-                            vw[3 * p] = static_cast<uint32_t>(cbits);
-                            vw[3 * p + 1] = static_cast<uint32_t>(cbits >> 32) | static_cast<uint32_t>(other << 16);
-                        } else {
-                            vw[3 * p + 2] = static_cast<uint32_t>(cbits >> 16);
-                        }
-                    }
-                } else if (vw) {
-                    if (C.v_bits == 2) {
-                        vw[sub] = static_cast<uint32_t>(cbits);
+                uint32_t cw[VB], meta;
+                quantize_values32<VB>(va, lpg, cw, meta);
+                const int rl = 32 * pw + 8 * p + (lane >> 2);
+                const int64_t vdst = rinfo[rl].dst;
+                if (vdst >= 0) {
+                    const int voff = rinfo[rl].off;
+                    uint8_t *vrec = vc + vdst * G.v_page;
+                    uint8_t *vcode = vrec + static_cast<int64_t>(voff) * (D * VB / 8);
+                    if constexpr (VB == 2) {
+                        reinterpret_cast<uint2 *>(vcode)[sub] = make_uint2(cw[0], cw[1]);
+                    } else if constexpr (VB == 4) {
+                        reinterpret_cast<uint4 *>(vcode)[sub] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
                     } else {
-                        vw[2 * sub] = static_cast<uint32_t>(cbits);
-                        vw[2 * sub + 1] = static_cast<uint32_t>(cbits >> 32);
+                        uint32_t *vw = reinterpret_cast<uint32_t *>(vcode) + VB * sub;
+#pragma unroll
+                        for (int k = 0; k < VB; ++k) vw[k] = cw[k];
                     }
+                    if ((sub & (lpg - 1)) == 0)
+                        *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + static_cast<int64_t>(voff) * C.v_meta_bytes +
+                                                      4 * (sub / lpg)) = meta;
                 }
-                if (vrec && (sub % lpg) == 0) {
-                    const uint32_t meta = static_cast<uint32_t>(__half_as_ushort(s16)) |
-                                          (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
-                    *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + static_cast<int64_t>(off) * C.v_meta_bytes +
-                                                  4 * (sub / lpg)) = meta;
-                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) va[j] = vb[j];
             }
         }
     } else {
@@ -610,12 +681,16 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             if (*e_abort) break;
             const RowInfo ri = rinfo[row];
             const bool zero = (ri.flag & 8) != 0;
-            float gsq;
-            int fl;
-            if (hf == 0)
-                epilogue_rotation<KB, 0>(smem, tY, warp, row, ri.zscale, zero, C.qjl != 0, bins, s_cent, s_thr, scodes, smask, gsq, fl);
-            else
-                epilogue_rotation<KB, 1>(smem, tY, warp, row, ri.zscale, zero, C.qjl != 0, bins, s_cent, s_thr, scodes, smask, gsq, fl);
+            float gsq = 0.f;
+            int fl = 0;
+            {
+                const float zs = ri.zscale * 4096.f;  // z' = 2^12 z
+#pragma unroll 1
+                for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb)
+                    gsq += epilogue_rotation_block<KB>(smem, tY, warp, row, cb, zs, C.qjl != 0, bins, scodes, smask);
+                gsq *= 1.f / 16777216.f;  // back to z units
+                fl = (smask[row * 8 + 2 * hf] | smask[row * 8 + 2 * hf + 1]) ? 1 : 0;
+            }
             s_gsq[row * 2 + hf] = gsq;
             s_flagp[row * 2 + hf] = fl;
             umma::fence_proxy_async();
@@ -671,10 +746,14 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 rinfo[row].n16g16 = n16g16;
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            // ---- exact re-decisions, one warp per flagged row (scratch in tile B) ----
-            for (int rl = warp; rl < TM; rl += kEpiWarps) {
+            // ---- exact re-decisions, one warp per flagged row (scratch in tile B): the two
+            // warps of a lane quarter take alternate flagged rows of that quarter ----
+            uint32_t pend = __ballot_sync(0xffffffffu, (flag & 7) != 0 && (flag & 8) == 0 && ri.dst >= 0);
+            for (int k = 0; pend != 0u; ++k) {
+                const int rl = 32 * (warp & 3) + __ffs(pend) - 1;
+                pend &= pend - 1u;
+                if ((k & 1) != hf) continue;
                 const int flg = rinfo[rl].flag;
-                if ((flg & 7) == 0 || (flg & 8) || rinfo[rl].dst < 0) continue;
                 const int64_t r = r0 + rl;
                 const int64_t t = r / Hkv;
                 const uint16_t *src = kin + t * ks + static_cast<int64_t>(r - t * Hkv) * D;
@@ -800,17 +879,17 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     if (warp == 0) umma::tmem_dealloc(tmem, 256);
 }
 
-template <int KB>
-cudaError_t launch_tc_kb(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T, int Hkv,
-                         int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc, int64_t num_blocks,
-                         int num_sms, cudaStream_t st)
+template <int KB, int VB>
+cudaError_t launch_tc(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T, int Hkv,
+                      int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc, int64_t num_blocks,
+                      int num_sms, cudaStream_t st)
 {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(compress_tc_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(compress_tc_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
@@ -818,9 +897,21 @@ cudaError_t launch_tc_kb(const Codec &c, const PageGeom &pg, const uint16_t *k, 
     const int64_t rows = T * Hkv;
     const int tiles = static_cast<int>((rows + TM - 1) / TM);
     const int grid = tiles < num_sms ? tiles : num_sms;
-    compress_tc_kernel<KB><<<grid, kThreads, kSmemBytes, st>>>(c, pg, k, v, rows, Hkv, ks, vs, slots, kc, vc,
-                                                               num_blocks, tiles);
+    compress_tc_kernel<KB, VB><<<grid, kThreads, kSmemBytes, st>>>(c, pg, k, v, rows, Hkv, ks, vs, slots, kc, vc,
+                                                                   num_blocks, tiles);
     return cudaGetLastError();
+}
+
+template <int KB>
+cudaError_t launch_tc_kb(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T, int Hkv,
+                         int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc, int64_t num_blocks,
+                         int num_sms, cudaStream_t st)
+{
+    switch (c.v_bits) {
+    case 2: return launch_tc<KB, 2>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, num_sms, st);
+    case 3: return launch_tc<KB, 3>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, num_sms, st);
+    default: return launch_tc<KB, 4>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, num_sms, st);
+    }
 }
 
 }  // namespace

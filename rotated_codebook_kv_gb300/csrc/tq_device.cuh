@@ -67,6 +67,33 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
+// Asynchronous prefetch of [p, p + bytes) into L2 by the bulk-copy engine; no
+// registers or shared memory are held.  p and bytes must be multiples of 16
+// and the range must lie inside one allocation.
+__device__ __forceinline__ void l2_prefetch_bulk(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// 16-byte global load issued exactly where written: a volatile asm statement
+// is neither sunk past a barrier to its first use nor re-issued later, which
+// the compiler may do with read-only loads.  p must be 16-byte aligned.
+__device__ __forceinline__ uint4 ld_pinned(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ int64_t ld_pinned_s64(const int64_t *p)
+{
+    int64_t v;
+    asm volatile("ld.global.nc.s64 %0, [%1];" : "=l"(v) : "l"(p));
+    return v;
+}
+
 // Word w of the LSB-first bitstream of b-bit codes (one code per byte in `codes`).
 __device__ __forceinline__ uint32_t pack_word(const uint8_t *codes, int w, int b)
 {
