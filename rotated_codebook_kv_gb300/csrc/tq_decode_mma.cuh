@@ -1,27 +1,26 @@
 // tq_decode_mma.cuh -- split-K paged decode on the tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate).
 //
-// One CTA = (split, kv head, sequence); 4 warps, each owns 16 tokens of every
-// 64-token chunk, with its own online softmax; the warps merge at the end.
+// One CTA = (split, kv head, sequence); 4 warps, each owns 16-token tiles of
+// every 128-token chunk (tokens 16 (warp + 4 i)), with its own online softmax;
+// the warps merge at the end.
 //
-// Scores are computed transposed, S^T[h][t] = sum_j q[h][j] Khat[t][j] with
-// the G query heads as the M dimension (padded to 16) and tokens as N, so the
-// fp32 score accumulators of two 8-token n-tiles are, after exp and fp16
-// conversion, exactly the B operand of O^T[j][h] = sum_t V[t][j] P[h][t]
-// (coordinates as M, heads as N = 8, tokens as K) -- no data exchange between
-// lanes.  Tokens are ordered inside a tile so that lane quad m owns tokens
-// 4m..4m+3 in the P.V step.
+// Scores: S[t][h] = sum_j Khat[t][j] q[h][j] with the 16 tokens of a tile as
+// the M dimension and the G <= 8 query heads as N.  Coordinates are permuted
+// inside every 16-wide k-step so that the A-fragment elements of lane quad m
+// are the four consecutive codes 16 s + 4 m + {0,1,2,3} of a token: pairs of
+// codes index a shared-memory table of fp16 centroid pairs (high part and a
+// low part scaled by 2^11, so the centroid score keeps ~22 bits:
+// q.c = qh.ch + 2^-11 (ql.ch + qh.cl), three MMAs per k-step into two
+// accumulators).  The QJL term sqrt(pi/2)/d * gamma * <S q_rot, 2 sigma - 1>
+// uses a fourth MMA whose A operand is +-1 from the sign bits.
 //
-// Coordinates are permuted inside every 16-wide k-step so that the four
-// B-fragment elements of lane quad m are the four consecutive codes
-// 16s + 4m + {0,1,2,3}: pairs of codes index a shared-memory table of fp16
-// centroid pairs (replicated so that lookups never conflict).
-// Queries and centroids are each split into an fp16 high part and a low part
-// scaled by 2^11, so the centroid score keeps ~22 bits: q.c = qh.ch +
-// 2^-11 (ql.ch + qh.cl), three MMAs per k-step into two accumulators.
-// The QJL term sqrt(pi/2)/d * gamma * <S q_rot, 2 sigma - 1> uses a second
-// accumulator with a +-1 operand built the same way from the sign bits.
-// Values: O^T += V^T (P^T scaled per group by the token's fp16 scale), plus a
-// small MMA with the zero points for sum_t zero_t * p_t.
+// Values: O^T[j][h] += sum_t V[t][j] P[t][h] with coordinates as M.  The score
+// accumulator of a tile, converted to fp16 and transposed in registers
+// (movmatrix), is exactly the B operand.  Rows of every 16-coordinate m-tile
+// are permuted (row r <-> coordinate 16 mt + 2 r, row r + 8 <-> 16 mt + 2 r + 1)
+// so that a lane's two codes per m-tile are adjacent and every m-tile lies in
+// one value group; codes enter the MMA as exact fp16 integers, the group scale
+// multiplies the B operand, and sum_t zero_t p_t is one small MMA per tile.
 #pragma once
 
 #include "tq_device.cuh"
@@ -32,7 +31,7 @@ namespace dmma {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTile = 16;                      // tokens per MMA tile
+constexpr int kTile = 16;                      // tokens per MMA tile (M of the score MMA)
 constexpr int kTilesPerWarp = 2;               // tiles per warp per chunk
 constexpr int kChunk = kWarps * kTile * kTilesPerWarp;  // tokens per chunk
 constexpr float kLoScale = 2048.f;             // scale of the fp16 low parts
@@ -47,6 +46,15 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8x8 b16 matrix held in the accumulator-fragment layout
+// (lane holds row lane / 4, columns 2 (lane % 4) + {0, 1}).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
+{
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
 {
     const __half2 h = __floats2half2_rn(lo, hi);
@@ -59,11 +67,11 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// Two small unsigned codes as an exact fp16 pair: (1024 + c) - 1024.
-__device__ __forceinline__ uint32_t codes_to_half2(uint32_t c_lo, uint32_t c_hi)
+// x holds (1024 + c0) | (1024 + c1) << 16 as fp16 bit patterns; returns the exact pair (c0, c1).
+__device__ __forceinline__ uint32_t unbias_half2(uint32_t x)
 {
-    const uint32_t x = (c_lo | (c_hi << 16)) | 0x64006400u;
-    __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&x), __float2half2_rn(1024.f));
+    const uint32_t k = 0x64006400u;
+    __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&x), *reinterpret_cast<const __half2 *>(&k));
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
@@ -84,13 +92,6 @@ __device__ __forceinline__ float fast_exp2(float x)
     return y;
 }
 
-// 64-bit window of two consecutive 32-bit words shifted right by sh (0..63).
-__device__ __forceinline__ uint32_t window(uint32_t w0, uint32_t w1, int sh)
-{
-    const uint64_t v = (static_cast<uint64_t>(w1) << 32) | w0;
-    return static_cast<uint32_t>(v >> sh);
-}
-
 // Dynamic shared memory layout of the tensor-core decode kernel.
 template <int D, int KB>
 struct DecSmem {
@@ -99,7 +100,7 @@ struct DecSmem {
     // [entry][16 copies] (hi pair, lo pair): a 64-bit load takes two wavefronts of
     // 16 lanes, so 16 copies (lane & 15) keep every lookup conflict-free.
     static constexpr size_t kLut = sizeof(uint2) * kPairEntries * 16;
-    static constexpr size_t kSignLut = sizeof(uint32_t) * 4 * 32;
+    static constexpr size_t kSignLut = sizeof(uint2) * 16;               // 4 sign bits -> two +-1 fp16 pairs
     static constexpr size_t kQfrag = sizeof(uint4) * (D / 16) * 32;      // [k-step][lane] (qh0, qh2, ql0, ql2)
     static constexpr size_t kSfrag = sizeof(uint2) * (D / 16) * 32;      // [k-step][lane] (qs0, qs2)
     static constexpr size_t kHeader = kLut + kSignLut + kQfrag + kSfrag + 64;  // + page-valid flags
@@ -115,6 +116,20 @@ struct DecSmem {
     }
 };
 
+// The 4 KB-bit codes 16 s + 4 m .. 16 s + 4 m + 3 of a packed code row, in the low 4 KB bits.
+template <int KB>
+__device__ __forceinline__ uint32_t code_quad(const uint32_t *row, int s, int m)
+{
+    if constexpr (KB == 2) {
+        return row[s] >> (8 * m);
+    } else if constexpr (KB == 4) {
+        return row[2 * s + (m >> 1)] >> (16 * (m & 1));
+    } else {
+        const int bit = 48 * s + 12 * m;
+        return __funnelshift_r(row[bit >> 5], row[(bit >> 5) + 1], bit & 31);
+    }
+}
+
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(const Codec C, const PageGeom PG, const DecodeArgs A)
 {
@@ -122,11 +137,9 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     constexpr bool QJL = (KB <= 3);
     constexpr int KS = D / 16;                 // k-steps over coordinates
     constexpr int MT = D / 16;                 // m-tiles of output coordinates
-    constexpr int NWK = D * KB / 32;           // words per key code row
-    constexpr int NWS = D / 32;                // words per sign row
     extern __shared__ __align__(16) unsigned char smem[];
     uint2 *lut = reinterpret_cast<uint2 *>(smem);
-    uint32_t *slut = reinterpret_cast<uint32_t *>(smem + SM::kLut);
+    uint2 *slut = reinterpret_cast<uint2 *>(smem + SM::kLut);
     uint4 *qfrag = reinterpret_cast<uint4 *>(smem + SM::kLut + SM::kSignLut);
     uint2 *sfrag = reinterpret_cast<uint2 *>(smem + SM::kLut + SM::kSignLut + SM::kQfrag);
     int *page_ok = reinterpret_cast<int *>(smem + SM::kLut + SM::kSignLut + SM::kQfrag + SM::kSfrag);  // [2][8]
@@ -161,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
         return;
     }
 
-    // ---- tables: fp16 centroid pairs and +-1 sign pairs, one copy per lane ----
+    // ---- tables: fp16 centroid pairs (16 copies) and +-1 sign pairs ----
     for (int e = tid; e < SM::kPairEntries * 16; e += kThreads) {
         const int ent = e >> 4;
         const int c0 = ent & ((1 << KB) - 1), c1 = ent >> KB;
@@ -169,13 +182,13 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
         const float h0 = __half2float(__float2half_rn(x0)), h1 = __half2float(__float2half_rn(x1));
         lut[e] = make_uint2(pack_half2(h0, h1), pack_half2((x0 - h0) * kLoScale, (x1 - h1) * kLoScale));
     }
-    for (int e = tid; e < 4 * 32; e += kThreads) {
-        const int ent = e >> 5;
-        slut[e] = pack_half2((ent & 1) ? 1.f : -1.f, (ent & 2) ? 1.f : -1.f);
+    if (tid < 16) {
+        auto pm = [](int bit) { return bit ? 1.f : -1.f; };
+        slut[tid] = make_uint2(pack_half2(pm(tid & 1), pm(tid & 2)), pack_half2(pm(tid & 4), pm(tid & 8)));
     }
 
-    // ---- query fragments (A operand of the score MMA), permuted coordinates;
-    // identical for the four warps, so warp 0 writes them to shared memory ----
+    // ---- query fragments (B operand of the score MMA, head = lane / 4), permuted
+    // coordinates; identical for the four warps, so warp 0 writes them ----
     if (warp == 0) {
         const bool hv = row < G;
         const float *qr = A.ws.qrot + (head0 + (hv ? row : 0)) * D;
@@ -201,15 +214,21 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
         }
     }
 
-    // ---- accumulators ---------------------------------------------------------
+    // ---- accumulators: O^T rows (coordinates, permuted) x heads 2 quad, 2 quad + 1 ----
     float o[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float zt[4] = {0.f, 0.f, 0.f, 0.f};  // sum_t zero[t][g] p[h][t], rows = groups
-    float m_run = -INFINITY, l_run = 0.f;  // head `row`, replicated across the quad
+    float zt[4] = {0.f, 0.f, 0.f, 0.f};       // sum_t zero[t][g] p[t][h]: rows = groups
+    float m_run[2] = {-INFINITY, -INFINITY};  // heads 2 quad + e
+    float l_run[2] = {0.f, 0.f};
 
     const float fac_c = A.sm_scale * rsqrtf(static_cast<float>(D)) * kLog2e;
     const float fac_s = A.sm_scale * (1.2533141373155003f / static_cast<float>(D)) * kLog2e;
+    const uint32_t lut_lane = static_cast<uint32_t>(__cvta_generic_to_shared(lut)) + 8u * (lane & 15);
+    const uint32_t slut_base = static_cast<uint32_t>(__cvta_generic_to_shared(slut));
+    const uint2 *lutl = lut + (lane & 15);
+    (void)lut_lane;
+    (void)slut_base;
 
     // ---- stage loader --------------------------------------------------------
     auto issue = [&](int chunk_page, int st) {
@@ -251,7 +270,6 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
         }
         __syncthreads();
 
-        // ---- this warp's tiles: chunk tokens [16 (warp + 4 i), +16) ----
 #pragma unroll 1
         for (int ti = 0; ti < kTilesPerWarp; ++ti) {
         const int tok0 = kTile * (warp + kWarps * ti);
@@ -263,163 +281,143 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
             const unsigned char *kr = stages + st * stage_bytes + static_cast<size_t>(q) * PG.k_page;
             const unsigned char *vr = stages + st * stage_bytes + static_cast<size_t>(ppc) * PG.k_page +
                                       static_cast<size_t>(q) * PG.v_page;
-            // ---- scores: two n-tiles of 8 tokens; this lane feeds token tau ----
-            float sc[2][4], sl[2][4], ss[2][4];
+            // ---- scores S[token][head]: this lane feeds tokens row, row + 8 ----
+            float sc[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f}, ss[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t *krow0 = reinterpret_cast<const uint32_t *>(kr + (o0 + row) * C.k_code_bytes);
+            const uint32_t *krow1 = reinterpret_cast<const uint32_t *>(kr + (o0 + row + 8) * C.k_code_bytes);
+            const uint32_t *srow0 = reinterpret_cast<const uint32_t *>(kr + PG.k_sign_off + (o0 + row) * C.k_sign_bytes);
+            const uint32_t *srow1 = reinterpret_cast<const uint32_t *>(kr + PG.k_sign_off + (o0 + row + 8) * C.k_sign_bytes);
+            constexpr uint32_t PM = (1u << (2 * KB)) - 1u;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-                sl[nt][0] = sl[nt][1] = sl[nt][2] = sl[nt][3] = 0.f;
-                ss[nt][0] = ss[nt][1] = ss[nt][2] = ss[nt][3] = 0.f;
-                const int tau = 2 * row - (row & 1) + 2 * nt;  // n-tile nt column `row`
-                const uint32_t *cw = reinterpret_cast<const uint32_t *>(kr + (o0 + tau) * C.k_code_bytes);
-                uint32_t kw[NWK + 1];
-#pragma unroll
-                for (int w = 0; w < NWK; w += 4) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(cw + w);
-                    kw[w] = u.x; kw[w + 1] = u.y; kw[w + 2] = u.z; kw[w + 3] = u.w;
-                }
-                kw[NWK] = 0u;
-                uint32_t sw[NWS];
+            for (int s = 0; s < KS; ++s) {
+                const uint32_t f0 = code_quad<KB>(krow0, s, quad);
+                const uint32_t f1 = code_quad<KB>(krow1, s, quad);
+                const uint2 e00 = lutl[(f0 & PM) << 4], e01 = lutl[((f0 >> (2 * KB)) & PM) << 4];
+                const uint2 e10 = lutl[(f1 & PM) << 4], e11 = lutl[((f1 >> (2 * KB)) & PM) << 4];
+                const uint4 qf = qfrag[s * 32 + lane];
+                mma16816(sc, e00.x, e10.x, e01.x, e11.x, qf.x, qf.y);
+                mma16816(sl, e00.x, e10.x, e01.x, e11.x, qf.z, qf.w);
+                mma16816(sl, e00.y, e10.y, e01.y, e11.y, qf.x, qf.y);
                 if (QJL) {
-                    const uint32_t *sp = reinterpret_cast<const uint32_t *>(kr + PG.k_sign_off + (o0 + tau) * C.k_sign_bytes);
-#pragma unroll
-                    for (int w = 0; w < NWS; w += 4) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(sp + w);
-                        sw[w] = u.x; sw[w + 1] = u.y; sw[w + 2] = u.z; sw[w + 3] = u.w;
-                    }
-                }
-#pragma unroll
-                for (int s = 0; s < KS; ++s) {
-                    // four codes 16s + 4 quad + {0..3}: bit offset KB * (16 s + 4 quad)
-                    const int base = KB * 16 * s;             // compile-time
-                    const int w0 = base >> 5;                 // compile-time word
-                    const int sh = (base & 31) + KB * 4 * quad;  // 0..(31 + 12)
-                    const uint32_t bits = window(kw[w0], kw[w0 + 1], sh);
-                    const uint32_t p0 = bits & ((1u << (2 * KB)) - 1u);
-                    const uint32_t p1 = (bits >> (2 * KB)) & ((1u << (2 * KB)) - 1u);
-                    const uint2 b0 = lut[(p0 << 4) + (lane & 15)];
-                    const uint2 b1 = lut[(p1 << 4) + (lane & 15)];
-                    const uint4 qf = qfrag[s * 32 + lane];
-                    mma16816(sc[nt], qf.x, 0u, qf.y, 0u, b0.x, b1.x);
-                    mma16816(sl[nt], qf.z, 0u, qf.w, 0u, b0.x, b1.x);
-                    mma16816(sl[nt], qf.x, 0u, qf.y, 0u, b0.y, b1.y);
-                    if (QJL) {
-                        const uint32_t sb = (sw[s >> 1] >> (16 * (s & 1) + 4 * quad)) & 0xFu;
-                        const uint32_t c0 = slut[((sb & 3u) << 5) + lane];
-                        const uint32_t c1 = slut[((sb >> 2) << 5) + lane];
-                        const uint2 sf = sfrag[s * 32 + lane];
-                        mma16816(ss[nt], sf.x, 0u, sf.y, 0u, c0, c1);
-                    }
+                    const int sh = 16 * (s & 1) + 4 * quad;
+                    const uint2 g0 = slut[(srow0[s >> 1] >> sh) & 15u];
+                    const uint2 g1 = slut[(srow1[s >> 1] >> sh) & 15u];
+                    const uint2 sf = sfrag[s * 32 + lane];
+                    mma16816(ss, g0.x, g1.x, g0.y, g1.y, sf.x, sf.y);
                 }
             }
-            // ---- scale: lane holds head `row`, tokens 4 quad + {0,1,2,3} ----
-            const int t0 = 4 * quad;
-            const uint2 nb = *reinterpret_cast<const uint2 *>(kr + PG.k_norm_off + 2 * (o0 + t0));
-            float nrm[4] = {bf16_to_float(nb.x & 0xffffu), bf16_to_float(nb.x >> 16), bf16_to_float(nb.y & 0xffffu),
-                            bf16_to_float(nb.y >> 16)};
-            float gam[4] = {0.f, 0.f, 0.f, 0.f};
+            // ---- scale and mask: x[hh][e] = token row + 8 hh, head 2 quad + e ----
+            const uint16_t *nrow = reinterpret_cast<const uint16_t *>(kr + PG.k_norm_off) + o0 + row;
+            const float nrm[2] = {bf16_to_float(nrow[0]), bf16_to_float(nrow[8])};
+            float gam[2] = {0.f, 0.f};
             if (QJL) {
-                const uint2 gb = *reinterpret_cast<const uint2 *>(kr + PG.k_gamma_off + 2 * (o0 + t0));
-                gam[0] = bf16_to_float(gb.x & 0xffffu); gam[1] = bf16_to_float(gb.x >> 16);
-                gam[2] = bf16_to_float(gb.y & 0xffffu); gam[3] = bf16_to_float(gb.y >> 16);
+                const uint16_t *grow = reinterpret_cast<const uint16_t *>(kr + PG.k_gamma_off) + o0 + row;
+                gam[0] = bf16_to_float(grow[0]);
+                gam[1] = bf16_to_float(grow[8]);
             }
-            float x[4];
+            float x[2][2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int nt = i >> 1, e = i & 1;
-                float v = nrm[i] * fac_c * fmaf(sl[nt][e], 1.f / kLoScale, sc[nt][e]);
-                if (QJL) v = fmaf(nrm[i] * fac_s * gam[i], ss[nt][e], v);
-                const bool valid = (pos0 + t0 + i) < L;
-                x[i] = (row < G) ? (valid ? v : -INFINITY) : 0.f;
-            }
-            // ---- online softmax (base 2) ----
-            float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-            const float m_new = fmaxf(m_run, mt);
-            float alpha = 1.f, p[4] = {0.f, 0.f, 0.f, 0.f};
-            if (m_new != -INFINITY) {
-                alpha = fast_exp2(m_run - m_new);
+            for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - m_new);
-            }
-            float ps = (p[0] + p[1]) + (p[2] + p[3]);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-            l_run = l_run * alpha + ps;
-            m_run = m_new;
-            // rescale O^T columns (heads 2 quad, 2 quad + 1) when any running max moved
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * quad);
-                const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * quad + 4);
-#pragma unroll
-                for (int m2 = 0; m2 < MT; ++m2) {
-                    o[m2][0] *= a_lo; o[m2][1] *= a_hi; o[m2][2] *= a_lo; o[m2][3] *= a_hi;
+                for (int e = 0; e < 2; ++e) {
+                    const int i = 2 * hh + e;
+                    float v = nrm[hh] * fac_c * fmaf(sl[i], 1.f / kLoScale, sc[i]);
+                    if (QJL) v = fmaf(nrm[hh] * fac_s * gam[hh], ss[i], v);
+                    const bool valid = (pos0 + row + 8 * hh) < L;
+                    x[hh][e] = (2 * quad + e < G) ? (valid ? v : -INFINITY) : 0.f;
                 }
-                zt[0] *= a_lo; zt[1] *= a_hi; zt[2] *= a_lo; zt[3] *= a_hi;
+            // ---- online softmax (base 2) per head 2 quad + e over the tile's 16 tokens ----
+            float p[2][2], alpha[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float mt = fmaxf(x[0][e], x[1][e]);
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+                const float m_new = fmaxf(m_run[e], mt);
+                alpha[e] = 1.f;
+                p[0][e] = p[1][e] = 0.f;
+                if (m_new != -INFINITY) {
+                    alpha[e] = fast_exp2(m_run[e] - m_new);
+                    p[0][e] = fast_exp2(x[0][e] - m_new);
+                    p[1][e] = fast_exp2(x[1][e] - m_new);
+                }
+                float ps = p[0][e] + p[1][e];
+                ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+                l_run[e] = l_run[e] * alpha[e] + ps;
+                m_run[e] = m_new;
             }
-            // ---- P^T fragments (tokens 4 quad + {0,1} | {2,3}, head `row`) ----
-            const uint32_t pb0 = pack_half2(p[0], p[1]);
-            const uint32_t pb1 = pack_half2(p[2], p[3]);
-            // ---- per-token value metadata of tokens t0..t0+3 (zero for masked tokens,
-            // whose never-written bytes may hold any fp16 pattern) ----
-            const unsigned char *meta = vr + PG.v_meta_off + (o0 + t0) * C.v_meta_bytes;
-            const int nval = min(4, max(0, L - (pos0 + t0)));
-            auto meta_word = [&](int t, int g) -> uint32_t {
-                return t < nval ? *reinterpret_cast<const uint32_t *>(meta + t * C.v_meta_bytes + 4 * g) : 0u;
+            // O^T columns of this lane are exactly its heads 2 quad, 2 quad + 1
+            if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    o[mt][0] *= alpha[0]; o[mt][1] *= alpha[1]; o[mt][2] *= alpha[0]; o[mt][3] *= alpha[1];
+                }
+                zt[0] *= alpha[0]; zt[1] *= alpha[1]; zt[2] *= alpha[0]; zt[3] *= alpha[1];
+            }
+            // ---- P^T as the B operand: tokens 2 quad + {0,1} (+8), head `row` ----
+            const uint32_t b0 = movmatrix_trans(pack_half2(p[0][0], p[0][1]));
+            const uint32_t b1 = movmatrix_trans(pack_half2(p[1][0], p[1][1]));
+            // value metadata of tokens 2 quad, 2 quad + 1, 2 quad + 8, 2 quad + 9 (zero for
+            // masked tokens, whose never-written bytes may hold any fp16 pattern)
+            const int tq[4] = {2 * quad, 2 * quad + 1, 2 * quad + 8, 2 * quad + 9};
+            const unsigned char *meta = vr + PG.v_meta_off + o0 * C.v_meta_bytes;
+            bool tv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tv[i] = (pos0 + tq[i]) < L;
+            auto meta_word = [&](int i, int g) -> uint32_t {
+                return tv[i] ? *reinterpret_cast<const uint32_t *>(meta + tq[i] * C.v_meta_bytes + 4 * g) : 0u;
             };
-            // zero-term: rows = groups (`row` < ng), tokens t0..t0+3
-            uint32_t za0 = 0u, za2 = 0u;
-            if (row < ng) {
-                const uint32_t m0 = meta_word(0, row), m1 = meta_word(1, row);
-                const uint32_t m2 = meta_word(2, row), m3 = meta_word(3, row);
-                za0 = __byte_perm(m0, m1, 0x7632);
-                za2 = __byte_perm(m2, m3, 0x7632);
+            // zero term: A rows = groups (`row` < ng), columns = tokens
+            {
+                uint32_t za0 = 0u, za2 = 0u;
+                if (row < ng) {
+                    za0 = __byte_perm(meta_word(0, row), meta_word(1, row), 0x7632);
+                    za2 = __byte_perm(meta_word(2, row), meta_word(3, row), 0x7632);
+                }
+                mma16816(zt, za0, 0u, za2, 0u, b0, b1);
             }
-            mma16816(zt, za0, 0u, za2, 0u, pb0, pb1);
-            // ---- P.V over coordinate m-tiles ----
-            const unsigned char *vc0 = vr + (o0 + t0) * C.v_code_bytes;
-            int g_cur = -1;
+            // ---- P.V over coordinate m-tiles: row r <-> 16 mt + 2 r, row r + 8 <-> 16 mt + 2 r + 1 ----
+            const uint32_t *vrow[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vrow[i] = reinterpret_cast<const uint32_t *>(vr + (o0 + tq[i]) * C.v_code_bytes);
+            constexpr uint32_t VM = ((1u << VB) - 1u) * 0x00010001u;
+            const uint32_t bias = 0x64006400u;
+            const int mt_per_group = C.group >> 4;
             uint32_t bs0 = 0u, bs1 = 0u;
 #pragma unroll
-            for (int m2 = 0; m2 < MT; ++m2) {
-                const int g = (16 * m2) / C.group;
-                if (g != g_cur) {  // group changes every group/16 m-tiles
-                    g_cur = g;
-                    const uint32_t s0 = meta_word(0, g), s1 = meta_word(1, g);
-                    const uint32_t s2 = meta_word(2, g), s3 = meta_word(3, g);
-                    bs0 = hmul2_u32(pb0, __byte_perm(s0, s1, 0x5410));
-                    bs1 = hmul2_u32(pb1, __byte_perm(s2, s3, 0x5410));
+            for (int mt = 0; mt < MT; ++mt) {
+                if (mt % mt_per_group == 0) {  // a new value group: scale the B operand
+                    const int g = mt / mt_per_group;
+                    bs0 = hmul2_u32(b0, __byte_perm(meta_word(0, g), meta_word(1, g), 0x5410));
+                    bs1 = hmul2_u32(b1, __byte_perm(meta_word(2, g), meta_word(3, g), 0x5410));
                 }
-                // codes of coordinates j0 = 16 m2 + row and j0 + 8 for tokens t0..t0+3
-                const int j0 = 16 * m2 + row;
-                uint32_t c[4][2];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const unsigned char *cb = vc0 + t * C.v_code_bytes;
-                    if (VB == 2) {
-                        const uint32_t w = *reinterpret_cast<const uint32_t *>(cb + 4 * m2);
-                        c[t][0] = (w >> (2 * row)) & 3u;
-                        c[t][1] = (w >> (16 + 2 * row)) & 3u;
-                    } else if (VB == 4) {
-                        const uint2 w = *reinterpret_cast<const uint2 *>(cb + 8 * m2);
-                        c[t][0] = (w.x >> (4 * row)) & 15u;
-                        c[t][1] = (w.y >> (4 * row)) & 15u;
-                    } else {  // 3-bit: 64-bit window starting at word floor(48 m2 / 32)
-                        const int wb = (48 * m2) >> 5;
-                        const uint32_t *cw = reinterpret_cast<const uint32_t *>(cb);
-                        const uint32_t lo = cw[wb], hi = cw[wb + 1];
-                        const int sh0 = 48 * m2 - 32 * wb + 3 * row;
-                        c[t][0] = window(lo, hi, sh0) & 7u;
-                        c[t][1] = window(lo, hi, sh0 + 24) & 7u;
-                    }
+                uint32_t xa, xb;  // codes of coordinates 16 mt + 2 row (+1): tokens (0, 1) | (2, 3)
+                if constexpr (VB == 2) {
+                    const uint32_t sel = static_cast<uint32_t>(row >> 1) | (static_cast<uint32_t>(4 + (row >> 1)) << 8);
+                    const int sh = 4 * (row & 1);
+                    xa = __byte_perm(vrow[0][mt], vrow[1][mt], sel) >> sh;
+                    xb = __byte_perm(vrow[2][mt], vrow[3][mt], sel) >> sh;
+                } else if constexpr (VB == 4) {
+                    const uint32_t sel = static_cast<uint32_t>(row & 3) | (static_cast<uint32_t>(4 + (row & 3)) << 8);
+                    const int w = 2 * mt + (row >> 2);
+                    xa = __byte_perm(vrow[0][w], vrow[1][w], sel);
+                    xb = __byte_perm(vrow[2][w], vrow[3][w], sel);
+                } else {
+                    const int bit = 48 * mt + 6 * row;
+                    const int w = bit >> 5, sh = bit & 31;
+                    xa = __byte_perm(__funnelshift_r(vrow[0][w], vrow[0][w + 1], sh),
+                                     __funnelshift_r(vrow[1][w], vrow[1][w + 1], sh), 0x5410);
+                    xb = __byte_perm(__funnelshift_r(vrow[2][w], vrow[2][w + 1], sh),
+                                     __funnelshift_r(vrow[3][w], vrow[3][w + 1], sh), 0x5410);
                 }
-                (void)j0;
-                const uint32_t a0 = codes_to_half2(c[0][0], c[1][0]);
-                const uint32_t a1 = codes_to_half2(c[0][1], c[1][1]);
-                const uint32_t a2 = codes_to_half2(c[2][0], c[3][0]);
-                const uint32_t a3 = codes_to_half2(c[2][1], c[3][1]);
-                mma16816(o[m2], a0, a1, a2, a3, bs0, bs1);
+                const uint32_t a0 = unbias_half2((xa & VM) | bias);
+                const uint32_t a1 = unbias_half2(((xa >> VB) & VM) | bias);
+                const uint32_t a2 = unbias_half2((xb & VM) | bias);
+                const uint32_t a3 = unbias_half2(((xb >> VB) & VM) | bias);
+                mma16816(o[mt], a0, a1, a2, a3, bs0, bs1);
             }
         }
         }  // tiles
@@ -432,17 +430,19 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     float *r_l = r_m + kWarps * 8;          // [warps][8]
     float *r_o = r_l + kWarps * 8;          // [warps][D][8]
     float *r_z = r_o + kWarps * D * 8;      // [warps][8 groups][8 heads]
-    if (quad == 0) {
-        r_m[warp * 8 + row] = m_run;
-        r_l[warp * 8 + row] = l_run;
+    if (row == 0) {
+        r_m[warp * 8 + 2 * quad] = m_run[0];
+        r_m[warp * 8 + 2 * quad + 1] = m_run[1];
+        r_l[warp * 8 + 2 * quad] = l_run[0];
+        r_l[warp * 8 + 2 * quad + 1] = l_run[1];
     }
 #pragma unroll
-    for (int m2 = 0; m2 < MT; ++m2) {
-        const int j = 16 * m2 + row;
-        r_o[(warp * D + j) * 8 + 2 * quad] = o[m2][0];
-        r_o[(warp * D + j) * 8 + 2 * quad + 1] = o[m2][1];
-        r_o[(warp * D + j + 8) * 8 + 2 * quad] = o[m2][2];
-        r_o[(warp * D + j + 8) * 8 + 2 * quad + 1] = o[m2][3];
+    for (int mt = 0; mt < MT; ++mt) {
+        const int j = 16 * mt + 2 * row;
+        r_o[(warp * D + j) * 8 + 2 * quad] = o[mt][0];
+        r_o[(warp * D + j) * 8 + 2 * quad + 1] = o[mt][1];
+        r_o[(warp * D + j + 1) * 8 + 2 * quad] = o[mt][2];
+        r_o[(warp * D + j + 1) * 8 + 2 * quad + 1] = o[mt][3];
     }
     r_z[(warp * 8 + row) * 8 + 2 * quad] = zt[0];
     r_z[(warp * 8 + row) * 8 + 2 * quad + 1] = zt[1];
