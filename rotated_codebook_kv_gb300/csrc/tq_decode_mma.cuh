@@ -97,13 +97,14 @@ template <int D, int KB>
 struct DecSmem {
     static constexpr int kPairBits = 2 * KB;
     static constexpr int kPairEntries = 1 << kPairBits;
-    // [entry][16 copies] (hi pair, lo pair): a 64-bit load takes two wavefronts of
-    // 16 lanes, so 16 copies (lane & 15) keep every lookup conflict-free.
-    static constexpr size_t kLut = sizeof(uint2) * kPairEntries * 16;
+    // [entry][copies] (hi pair, lo pair).  2-bit codes: 16 entries fill the 32 banks
+    // once, so lookups never conflict.  3- and 4-bit codes: 4 copies (lane & 3).
+    static constexpr int kLutCopies = (KB == 2) ? 1 : 4;
+    static constexpr size_t kLut = sizeof(uint2) * kPairEntries * kLutCopies;  // a multiple of 128
     static constexpr size_t kSignLut = sizeof(uint2) * 16;               // 4 sign bits -> two +-1 fp16 pairs
     static constexpr size_t kQfrag = sizeof(uint4) * (D / 16) * 32;      // [k-step][lane] (qh0, qh2, ql0, ql2)
     static constexpr size_t kSfrag = sizeof(uint2) * (D / 16) * 32;      // [k-step][lane] (qs0, qs2)
-    static constexpr size_t kHeader = kLut + kSignLut + kQfrag + kSfrag + 64;  // + page-valid flags
+    static constexpr size_t kHeader = kLut + kSignLut + kQfrag + kSfrag + 256;  // + page flags, zeros, mbarriers
     __host__ __device__ static size_t stage_bytes(const PageGeom &pg)
     {
         return static_cast<size_t>(kChunk / pg.P) * (pg.k_page + pg.v_page);
@@ -116,18 +117,23 @@ struct DecSmem {
     }
 };
 
-// The 4 KB-bit codes 16 s + 4 m .. 16 s + 4 m + 3 of a packed code row, in the low 4 KB bits.
-template <int KB>
-__device__ __forceinline__ uint32_t code_quad(const uint32_t *row, int s, int m)
+// The 4 KB-bit codes 16 s + 4 m .. 16 s + 4 m + 3 of the packed code row at shared
+// offset `row`, in the low 4 KB bits (3- and 4-bit codes).
+template <int KB, typename LD>
+__device__ __forceinline__ uint32_t code_quad_off(const LD &ld32, uint32_t row, int s, int m)
 {
-    if constexpr (KB == 2) {
-        return row[s] >> (8 * m);
-    } else if constexpr (KB == 4) {
-        return row[2 * s + (m >> 1)] >> (16 * (m & 1));
+    if constexpr (KB == 4) {
+        return ld32(row + 8 * s + 4 * (m >> 1)) >> (16 * (m & 1));
     } else {
         const int bit = 48 * s + 12 * m;
-        return __funnelshift_r(row[bit >> 5], row[(bit >> 5) + 1], bit & 31);
+        return __funnelshift_r(ld32(row + 4 * (bit >> 5)), ld32(row + 4 * ((bit >> 5) + 1)), bit & 31);
     }
+}
+
+__device__ __forceinline__ void mbar_init_cta(uint64_t *mbar, int count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(mbar))),
+                 "r"(count));
 }
 
 template <int D, int KB, int VB>
@@ -143,6 +149,9 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     uint4 *qfrag = reinterpret_cast<uint4 *>(smem + SM::kLut + SM::kSignLut);
     uint2 *sfrag = reinterpret_cast<uint2 *>(smem + SM::kLut + SM::kSignLut + SM::kQfrag);
     int *page_ok = reinterpret_cast<int *>(smem + SM::kLut + SM::kSignLut + SM::kQfrag + SM::kSfrag);  // [2][8]
+    uint32_t *zero_meta = reinterpret_cast<uint32_t *>(page_ok + 16);  // [16] zeros: metadata of masked tokens
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(page_ok + 32);        // [2] stage barriers
+    const uint32_t zero_off = static_cast<uint32_t>(SM::kLut + SM::kSignLut + SM::kQfrag + SM::kSfrag + 64);
     unsigned char *stages = smem + SM::kHeader;
 
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -153,6 +162,8 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     const int ng = D / C.group;
     const size_t stage_bytes = SM::stage_bytes(PG);
     const int ppc = kChunk / P;
+    const int pshift = __ffs(P) - 1;                 // page size and value group are powers of two
+    const int gshift = __ffs(C.group) - 1;
 
     int L = A.seq_lens[b];
     if (L < 0) L = 0;
@@ -175,14 +186,15 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     }
 
     // ---- tables: fp16 centroid pairs (16 copies) and +-1 sign pairs ----
-    for (int e = tid; e < SM::kPairEntries * 16; e += kThreads) {
-        const int ent = e >> 4;
+    for (int e = tid; e < SM::kPairEntries * SM::kLutCopies; e += kThreads) {
+        const int ent = e / SM::kLutCopies;
         const int c0 = ent & ((1 << KB) - 1), c1 = ent >> KB;
         const float x0 = C.centroids[c0], x1 = C.centroids[c1];
         const float h0 = __half2float(__float2half_rn(x0)), h1 = __half2float(__float2half_rn(x1));
         lut[e] = make_uint2(pack_half2(h0, h1), pack_half2((x0 - h0) * kLoScale, (x1 - h1) * kLoScale));
     }
     if (tid < 16) {
+        zero_meta[tid] = 0u;
         auto pm = [](int bit) { return bit ? 1.f : -1.f; };
         slut[tid] = make_uint2(pack_half2(pm(tid & 1), pm(tid & 2)), pack_half2(pm(tid & 4), pm(tid & 8)));
     }
@@ -224,125 +236,186 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
 
     const float fac_c = A.sm_scale * rsqrtf(static_cast<float>(D)) * kLog2e;
     const float fac_s = A.sm_scale * (1.2533141373155003f / static_cast<float>(D)) * kLog2e;
-    const uint32_t lut_lane = static_cast<uint32_t>(__cvta_generic_to_shared(lut)) + 8u * (lane & 15);
-    const uint32_t slut_base = static_cast<uint32_t>(__cvta_generic_to_shared(slut));
-    const uint2 *lutl = lut + (lane & 15);
-    (void)lut_lane;
-    (void)slut_base;
+    // shared-memory reads by 32-bit byte offset
+    auto ld32 = [&](uint32_t off) -> uint32_t { return *reinterpret_cast<const uint32_t *>(smem + off); };
+    auto ld64 = [&](uint32_t off) -> uint2 { return *reinterpret_cast<const uint2 *>(smem + off); };
+    auto ldu16 = [&](uint32_t off) -> uint32_t { return *reinterpret_cast<const uint16_t *>(smem + off); };
+    constexpr uint32_t PM = (1u << (2 * KB)) - 1u;
+    // 2-bit codes: code pair (4 quad, 4 quad + 1) / (4 quad + 2, 4 quad + 3) of a k-step word
+    // rotated to bits 3..6 is the byte offset of its table entry
+    const int rot0 = (8 * quad + 29) & 31, rot1 = (8 * quad + 1) & 31;
+    const uint32_t lut_lane = 8u * (lane & 3);  // 3- and 4-bit codes: this lane's table copy
+    const uint32_t slut_off = static_cast<uint32_t>(SM::kLut);
+    const int mt_mask = (C.group >> 4) - 1;     // m-tiles per value group - 1
+    // value codes of coordinates 16 mt + 2 row (+1): byte (2-bit) or nibble pair (4-bit) of the row
+    const uint32_t vsel = (VB == 2) ? (static_cast<uint32_t>(row >> 1) | (static_cast<uint32_t>(4 + (row >> 1)) << 8))
+                                    : (static_cast<uint32_t>(row & 3) | (static_cast<uint32_t>(4 + (row & 3)) << 8));
+    const int vsh = 4 * (row & 1);
+    const uint32_t vwoff = 4u * (row >> 2);
 
-    // ---- stage loader --------------------------------------------------------
-    auto issue = [&](int chunk_page, int st) {
-        unsigned char *kst = stages + st * stage_bytes;
-        unsigned char *vst = kst + static_cast<size_t>(ppc) * PG.k_page;
-        const int np = min(ppc, pg1 - chunk_page);
-        for (int q = 0; q < ppc; ++q) {
-            int ok = 0;
-            if (q < np) {
-                const int blk = A.block_table[static_cast<int64_t>(b) * A.max_blocks + chunk_page + q];
-                ok = (blk >= 0 && blk < A.num_blocks);
-                if (ok) {
-                    const size_t rec = static_cast<size_t>(blk) * A.Hkv + kvh;
-                    const unsigned char *ks = A.k_cache + rec * PG.k_page;
-                    const unsigned char *vs = A.v_cache + rec * PG.v_page;
-                    for (int e = tid; e < PG.k_page / 16; e += kThreads)
-                        cp_async16(kst + q * PG.k_page + 16 * e, ks + 16 * e);
-                    for (int e = tid; e < PG.v_page / 16; e += kThreads)
-                        cp_async16(vst + q * PG.v_page + 16 * e, vs + 16 * e);
-                } else if (tid == 0) {
-                    atomicOr(C.status, TQ_DEVERR_BLOCK_RANGE);
-                }
-            }
-            if (tid == 0) page_ok[st * 8 + q] = ok;
+    // ---- page loader: thread q < ppc copies page q of a chunk with two bulk copies
+    // (keys, values) that complete on the stage's mbarrier; block ids are read one
+    // chunk ahead ----
+    auto fetch_id = [&](int chunk_page) -> int {
+        int blk = -1;
+        if (tid < ppc && chunk_page + tid < pg1)
+            blk = A.block_table[static_cast<int64_t>(b) * A.max_blocks + chunk_page + tid];
+        return blk;
+    };
+    auto issue = [&](int chunk_page, int st, int blk) {  // by threads tid < ppc
+        const int q = tid;
+        int ok = 0;
+        if (chunk_page + q < pg1) {
+            ok = (blk >= 0 && blk < A.num_blocks);
+            if (!ok) atomicOr(C.status, TQ_DEVERR_BLOCK_RANGE);
         }
-        cp_async_commit();
+        page_ok[st * 8 + q] = ok;
+        const uint32_t bytes = ok ? static_cast<uint32_t>(PG.k_page + PG.v_page) : 0u;
+        const uint32_t mb = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[st]));
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
+        if (ok) {
+            const size_t rec = static_cast<size_t>(blk) * A.Hkv + kvh;
+            const uint32_t kd = static_cast<uint32_t>(__cvta_generic_to_shared(stages + st * stage_bytes + q * PG.k_page));
+            const uint32_t vd = static_cast<uint32_t>(__cvta_generic_to_shared(stages + st * stage_bytes +
+                                                                               ppc * PG.k_page + q * PG.v_page));
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                         ::"r"(kd), "l"(A.k_cache + rec * PG.k_page), "r"(static_cast<uint32_t>(PG.k_page)), "r"(mb)
+                         : "memory");
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                         ::"r"(vd), "l"(A.v_cache + rec * PG.v_page), "r"(static_cast<uint32_t>(PG.v_page)), "r"(mb)
+                         : "memory");
+        }
     };
 
     const int nchunks = (pg1 - pg0 + ppc - 1) / ppc;
-    issue(pg0, 0);
+    if (tid == 0) {
+        mbar_init_cta(&mbar[0], ppc);
+        mbar_init_cta(&mbar[1], ppc);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();  // tables, query fragments and barriers are ready
+    int bnext = fetch_id(pg0);
+    if (tid < ppc) issue(pg0, 0, bnext);
+    bnext = fetch_id(pg0 + ppc);
     for (int c = 0; c < nchunks; ++c) {
         const int st = c & 1;
         const int cpage = pg0 + c * ppc;
-        if (c + 1 < nchunks) {
-            issue(cpage + ppc, st ^ 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+        if (c + 1 < nchunks && tid < ppc) {
+            issue(cpage + ppc, st ^ 1, bnext);
+            bnext = fetch_id(cpage + 2 * ppc);
         }
-        __syncthreads();
+        {
+            const uint32_t mb = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[st]));
+            const uint32_t par = static_cast<uint32_t>((c >> 1) & 1);
+            const long long t0 = clock64();
+            for (;;) {
+                uint32_t done;
+                asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                             : "=r"(done) : "r"(mb), "r"(par) : "memory");
+                if (done) break;
+                if (clock64() - t0 > 2000000000LL) {  // ~1 s: report instead of hanging
+                    if (lane == 0) atomicOr(C.status, TQ_DEVERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
 
-#pragma unroll 1
-        for (int ti = 0; ti < kTilesPerWarp; ++ti) {
-        const int tok0 = kTile * (warp + kWarps * ti);
-        const int q = tok0 / P;                  // page inside the chunk
-        const int o0 = tok0 - q * P;             // first offset inside the page
-        const int pos0 = (cpage + q) * P + o0;   // sequence position of tile token 0
-        const bool tile_live = (q < min(ppc, pg1 - cpage)) && page_ok[st * 8 + q] && (pos0 < L);
-        if (tile_live) {
-            const unsigned char *kr = stages + st * stage_bytes + static_cast<size_t>(q) * PG.k_page;
-            const unsigned char *vr = stages + st * stage_bytes + static_cast<size_t>(ppc) * PG.k_page +
-                                      static_cast<size_t>(q) * PG.v_page;
-            // ---- scores S[token][head]: this lane feeds tokens row, row + 8 ----
-            float sc[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f}, ss[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint32_t *krow0 = reinterpret_cast<const uint32_t *>(kr + (o0 + row) * C.k_code_bytes);
-            const uint32_t *krow1 = reinterpret_cast<const uint32_t *>(kr + (o0 + row + 8) * C.k_code_bytes);
-            const uint32_t *srow0 = reinterpret_cast<const uint32_t *>(kr + PG.k_sign_off + (o0 + row) * C.k_sign_bytes);
-            const uint32_t *srow1 = reinterpret_cast<const uint32_t *>(kr + PG.k_sign_off + (o0 + row + 8) * C.k_sign_bytes);
-            constexpr uint32_t PM = (1u << (2 * KB)) - 1u;
+        // ---- this warp's two tiles of the chunk: tokens 16 (warp + 4 j) ----
+        int kp[2], vp[2], o0[2], pos0[2];
+        bool live[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int tok0 = kTile * (warp + kWarps * j);
+            const int q = tok0 >> pshift;
+            o0[j] = tok0 & (P - 1);
+            pos0[j] = (cpage + q) * P + o0[j];
+            live[j] = (cpage + q < pg1) && page_ok[st * 8 + q] && (pos0[j] < L);
+            kp[j] = static_cast<int>(SM::kHeader + st * stage_bytes + q * PG.k_page);
+            vp[j] = static_cast<int>(SM::kHeader + st * stage_bytes + ppc * PG.k_page + q * PG.v_page);
+        }
+        if (live[0] || live[1]) {
+            // ---- scores S[token][head]: this lane feeds tokens row, row + 8 of both tiles ----
+            float sc[2][4], sl[2][4], ss[2][4];
+            uint32_t krow[2][2], srow[2][2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sc[j][i] = sl[j][i] = ss[j][i] = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    krow[j][hh] = kp[j] + (o0[j] + row + 8 * hh) * C.k_code_bytes;
+                    srow[j][hh] = kp[j] + PG.k_sign_off + (o0[j] + row + 8 * hh) * C.k_sign_bytes;
+                }
+            }
 #pragma unroll
             for (int s = 0; s < KS; ++s) {
-                const uint32_t f0 = code_quad<KB>(krow0, s, quad);
-                const uint32_t f1 = code_quad<KB>(krow1, s, quad);
-                const uint2 e00 = lutl[(f0 & PM) << 4], e01 = lutl[((f0 >> (2 * KB)) & PM) << 4];
-                const uint2 e10 = lutl[(f1 & PM) << 4], e11 = lutl[((f1 >> (2 * KB)) & PM) << 4];
                 const uint4 qf = qfrag[s * 32 + lane];
-                mma16816(sc, e00.x, e10.x, e01.x, e11.x, qf.x, qf.y);
-                mma16816(sl, e00.x, e10.x, e01.x, e11.x, qf.z, qf.w);
-                mma16816(sl, e00.y, e10.y, e01.y, e11.y, qf.x, qf.y);
-                if (QJL) {
-                    const int sh = 16 * (s & 1) + 4 * quad;
-                    const uint2 g0 = slut[(srow0[s >> 1] >> sh) & 15u];
-                    const uint2 g1 = slut[(srow1[s >> 1] >> sh) & 15u];
-                    const uint2 sf = sfrag[s * 32 + lane];
-                    mma16816(ss, g0.x, g1.x, g0.y, g1.y, sf.x, sf.y);
+                uint2 sf = make_uint2(0u, 0u);
+                if (QJL) sf = sfrag[s * 32 + lane];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    uint2 e[2][2];  // [token hh][pair]
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if constexpr (KB == 2) {
+                            const uint32_t w = ld32(krow[j][hh] + 4 * s);
+                            e[hh][0] = ld64(__funnelshift_r(w, w, rot0) & 0x78u);
+                            e[hh][1] = ld64(__funnelshift_r(w, w, rot1) & 0x78u);
+                        } else {
+                            const uint32_t f = code_quad_off<KB>(ld32, krow[j][hh], s, quad);
+                            e[hh][0] = ld64(lut_lane + ((f & PM) << 5));
+                            e[hh][1] = ld64(lut_lane + (((f >> (2 * KB)) & PM) << 5));
+                        }
+                    }
+                    mma16816(sc[j], e[0][0].x, e[1][0].x, e[0][1].x, e[1][1].x, qf.x, qf.y);
+                    mma16816(sl[j], e[0][0].x, e[1][0].x, e[0][1].x, e[1][1].x, qf.z, qf.w);
+                    mma16816(sl[j], e[0][0].y, e[1][0].y, e[0][1].y, e[1][1].y, qf.x, qf.y);
+                    if (QJL) {
+                        const int rot = (16 * (s & 1) + 4 * quad + 29) & 31;
+                        const uint32_t w0 = ld32(srow[j][0] + 4 * (s >> 1)), w1 = ld32(srow[j][1] + 4 * (s >> 1));
+                        const uint2 g0 = ld64((__funnelshift_r(w0, w0, rot) & 0x78u) | slut_off);
+                        const uint2 g1 = ld64((__funnelshift_r(w1, w1, rot) & 0x78u) | slut_off);
+                        mma16816(ss[j], g0.x, g1.x, g0.y, g1.y, sf.x, sf.y);
+                    }
                 }
             }
-            // ---- scale and mask: x[hh][e] = token row + 8 hh, head 2 quad + e ----
-            const uint16_t *nrow = reinterpret_cast<const uint16_t *>(kr + PG.k_norm_off) + o0 + row;
-            const float nrm[2] = {bf16_to_float(nrow[0]), bf16_to_float(nrow[8])};
-            float gam[2] = {0.f, 0.f};
-            if (QJL) {
-                const uint16_t *grow = reinterpret_cast<const uint16_t *>(kr + PG.k_gamma_off) + o0 + row;
-                gam[0] = bf16_to_float(grow[0]);
-                gam[1] = bf16_to_float(grow[8]);
-            }
-            float x[2][2];
+            // ---- scale and mask: x[j][hh][e] = tile j, token row + 8 hh, head 2 quad + e ----
+            float x[2][2][2];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int i = 2 * hh + e;
-                    float v = nrm[hh] * fac_c * fmaf(sl[i], 1.f / kLoScale, sc[i]);
-                    if (QJL) v = fmaf(nrm[hh] * fac_s * gam[hh], ss[i], v);
-                    const bool valid = (pos0 + row + 8 * hh) < L;
-                    x[hh][e] = (2 * quad + e < G) ? (valid ? v : -INFINITY) : 0.f;
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int t = o0[j] + row + 8 * hh;
+                    const float nrm = bf16_to_float(ldu16(kp[j] + PG.k_norm_off + 2 * t));
+                    const float gam = QJL ? bf16_to_float(ldu16(kp[j] + PG.k_gamma_off + 2 * t)) : 0.f;
+                    const bool valid = live[j] && (pos0[j] + row + 8 * hh) < L;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int i = 2 * hh + e;
+                        float v = nrm * fac_c * fmaf(sl[j][i], 1.f / kLoScale, sc[j][i]);
+                        if (QJL) v = fmaf(nrm * fac_s * gam, ss[j][i], v);
+                        x[j][hh][e] = (2 * quad + e < G) ? (valid ? v : -INFINITY) : 0.f;
+                    }
                 }
-            // ---- online softmax (base 2) per head 2 quad + e over the tile's 16 tokens ----
-            float p[2][2], alpha[2];
+            // ---- online softmax (base 2) per head 2 quad + e over the 32 tokens ----
+            float p[2][2][2], alpha[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                float mt = fmaxf(x[0][e], x[1][e]);
+                float mt = fmaxf(fmaxf(x[0][0][e], x[0][1][e]), fmaxf(x[1][0][e], x[1][1][e]));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
                 mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
                 const float m_new = fmaxf(m_run[e], mt);
                 alpha[e] = 1.f;
-                p[0][e] = p[1][e] = 0.f;
-                if (m_new != -INFINITY) {
-                    alpha[e] = fast_exp2(m_run[e] - m_new);
-                    p[0][e] = fast_exp2(x[0][e] - m_new);
-                    p[1][e] = fast_exp2(x[1][e] - m_new);
-                }
-                float ps = p[0][e] + p[1][e];
+                float ps = 0.f;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        p[j][hh][e] = (m_new != -INFINITY) ? fast_exp2(x[j][hh][e] - m_new) : 0.f;
+                        ps += p[j][hh][e];
+                    }
+                if (m_new != -INFINITY) alpha[e] = fast_exp2(m_run[e] - m_new);
                 ps += __shfl_xor_sync(0xffffffffu, ps, 4);
                 ps += __shfl_xor_sync(0xffffffffu, ps, 8);
                 ps += __shfl_xor_sync(0xffffffffu, ps, 16);
@@ -357,70 +430,70 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
                 }
                 zt[0] *= alpha[0]; zt[1] *= alpha[1]; zt[2] *= alpha[0]; zt[3] *= alpha[1];
             }
-            // ---- P^T as the B operand: tokens 2 quad + {0,1} (+8), head `row` ----
-            const uint32_t b0 = movmatrix_trans(pack_half2(p[0][0], p[0][1]));
-            const uint32_t b1 = movmatrix_trans(pack_half2(p[1][0], p[1][1]));
-            // value metadata of tokens 2 quad, 2 quad + 1, 2 quad + 8, 2 quad + 9 (zero for
-            // masked tokens, whose never-written bytes may hold any fp16 pattern)
+            // ---- values: per tile, P^T as the B operand (tokens 2 quad + {0,1} (+8), head `row`) ----
+            uint32_t b0[2], b1[2];
+            uint32_t mrow[2][4], vrow[2][4];
             const int tq[4] = {2 * quad, 2 * quad + 1, 2 * quad + 8, 2 * quad + 9};
-            const unsigned char *meta = vr + PG.v_meta_off + o0 * C.v_meta_bytes;
-            bool tv[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) tv[i] = (pos0 + tq[i]) < L;
-            auto meta_word = [&](int i, int g) -> uint32_t {
-                return tv[i] ? *reinterpret_cast<const uint32_t *>(meta + tq[i] * C.v_meta_bytes + 4 * g) : 0u;
-            };
-            // zero term: A rows = groups (`row` < ng), columns = tokens
-            {
+            for (int j = 0; j < 2; ++j) {
+                b0[j] = movmatrix_trans(pack_half2(p[j][0][0], p[j][0][1]));
+                b1[j] = movmatrix_trans(pack_half2(p[j][1][0], p[j][1][1]));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = o0[j] + tq[i];
+                    // metadata of masked tokens (never-written bytes may hold any fp16 pattern) reads zeros
+                    mrow[j][i] = (live[j] && pos0[j] + tq[i] < L) ? vp[j] + PG.v_meta_off + t * C.v_meta_bytes : zero_off;
+                    vrow[j][i] = vp[j] + t * C.v_code_bytes;
+                }
+                // zero term: A rows = groups (`row` < ng), columns = tokens
                 uint32_t za0 = 0u, za2 = 0u;
                 if (row < ng) {
-                    za0 = __byte_perm(meta_word(0, row), meta_word(1, row), 0x7632);
-                    za2 = __byte_perm(meta_word(2, row), meta_word(3, row), 0x7632);
+                    za0 = __byte_perm(ld32(mrow[j][0] + 4 * row), ld32(mrow[j][1] + 4 * row), 0x7632);
+                    za2 = __byte_perm(ld32(mrow[j][2] + 4 * row), ld32(mrow[j][3] + 4 * row), 0x7632);
                 }
-                mma16816(zt, za0, 0u, za2, 0u, b0, b1);
+                mma16816(zt, za0, 0u, za2, 0u, b0[j], b1[j]);
             }
             // ---- P.V over coordinate m-tiles: row r <-> 16 mt + 2 r, row r + 8 <-> 16 mt + 2 r + 1 ----
-            const uint32_t *vrow[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) vrow[i] = reinterpret_cast<const uint32_t *>(vr + (o0 + tq[i]) * C.v_code_bytes);
             constexpr uint32_t VM = ((1u << VB) - 1u) * 0x00010001u;
             const uint32_t bias = 0x64006400u;
-            const int mt_per_group = C.group >> 4;
-            uint32_t bs0 = 0u, bs1 = 0u;
+            uint32_t bs0[2] = {0u, 0u}, bs1[2] = {0u, 0u};
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                if (mt % mt_per_group == 0) {  // a new value group: scale the B operand
-                    const int g = mt / mt_per_group;
-                    bs0 = hmul2_u32(b0, __byte_perm(meta_word(0, g), meta_word(1, g), 0x5410));
-                    bs1 = hmul2_u32(b1, __byte_perm(meta_word(2, g), meta_word(3, g), 0x5410));
+                if ((mt & mt_mask) == 0) {  // a new value group: scale the B operands
+                    const int g4 = 4 * ((16 * mt) >> gshift);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        bs0[j] = hmul2_u32(b0[j], __byte_perm(ld32(mrow[j][0] + g4), ld32(mrow[j][1] + g4), 0x5410));
+                        bs1[j] = hmul2_u32(b1[j], __byte_perm(ld32(mrow[j][2] + g4), ld32(mrow[j][3] + g4), 0x5410));
+                    }
                 }
-                uint32_t xa, xb;  // codes of coordinates 16 mt + 2 row (+1): tokens (0, 1) | (2, 3)
-                if constexpr (VB == 2) {
-                    const uint32_t sel = static_cast<uint32_t>(row >> 1) | (static_cast<uint32_t>(4 + (row >> 1)) << 8);
-                    const int sh = 4 * (row & 1);
-                    xa = __byte_perm(vrow[0][mt], vrow[1][mt], sel) >> sh;
-                    xb = __byte_perm(vrow[2][mt], vrow[3][mt], sel) >> sh;
-                } else if constexpr (VB == 4) {
-                    const uint32_t sel = static_cast<uint32_t>(row & 3) | (static_cast<uint32_t>(4 + (row & 3)) << 8);
-                    const int w = 2 * mt + (row >> 2);
-                    xa = __byte_perm(vrow[0][w], vrow[1][w], sel);
-                    xb = __byte_perm(vrow[2][w], vrow[3][w], sel);
-                } else {
-                    const int bit = 48 * mt + 6 * row;
-                    const int w = bit >> 5, sh = bit & 31;
-                    xa = __byte_perm(__funnelshift_r(vrow[0][w], vrow[0][w + 1], sh),
-                                     __funnelshift_r(vrow[1][w], vrow[1][w + 1], sh), 0x5410);
-                    xb = __byte_perm(__funnelshift_r(vrow[2][w], vrow[2][w + 1], sh),
-                                     __funnelshift_r(vrow[3][w], vrow[3][w + 1], sh), 0x5410);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    uint32_t xa, xb;  // codes of coordinates 16 mt + 2 row (+1): tokens (0, 1) | (2, 3)
+                    if constexpr (VB == 2) {
+                        xa = __byte_perm(ld32(vrow[j][0] + 4 * mt), ld32(vrow[j][1] + 4 * mt), vsel) >> vsh;
+                        xb = __byte_perm(ld32(vrow[j][2] + 4 * mt), ld32(vrow[j][3] + 4 * mt), vsel) >> vsh;
+                    } else if constexpr (VB == 4) {
+                        const uint32_t w = 8 * mt + vwoff;
+                        xa = __byte_perm(ld32(vrow[j][0] + w), ld32(vrow[j][1] + w), vsel);
+                        xb = __byte_perm(ld32(vrow[j][2] + w), ld32(vrow[j][3] + w), vsel);
+                    } else {
+                        const int bit = 48 * mt + 6 * row;
+                        const uint32_t w = 4 * (bit >> 5);
+                        const int sh = bit & 31;
+                        xa = __byte_perm(__funnelshift_r(ld32(vrow[j][0] + w), ld32(vrow[j][0] + w + 4), sh),
+                                         __funnelshift_r(ld32(vrow[j][1] + w), ld32(vrow[j][1] + w + 4), sh), 0x5410);
+                        xb = __byte_perm(__funnelshift_r(ld32(vrow[j][2] + w), ld32(vrow[j][2] + w + 4), sh),
+                                         __funnelshift_r(ld32(vrow[j][3] + w), ld32(vrow[j][3] + w + 4), sh), 0x5410);
+                    }
+                    const uint32_t a0 = unbias_half2((xa & VM) | bias);
+                    const uint32_t a1 = unbias_half2(((xa >> VB) & VM) | bias);
+                    const uint32_t a2 = unbias_half2((xb & VM) | bias);
+                    const uint32_t a3 = unbias_half2(((xb >> VB) & VM) | bias);
+                    mma16816(o[mt], a0, a1, a2, a3, bs0[j], bs1[j]);
                 }
-                const uint32_t a0 = unbias_half2((xa & VM) | bias);
-                const uint32_t a1 = unbias_half2(((xa >> VB) & VM) | bias);
-                const uint32_t a2 = unbias_half2((xb & VM) | bias);
-                const uint32_t a3 = unbias_half2(((xb >> VB) & VM) | bias);
-                mma16816(o[mt], a0, a1, a2, a3, bs0, bs1);
             }
         }
-        }  // tiles
         __syncthreads();  // the next issue() overwrites this stage
     }
 
@@ -457,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
                 const float f = fast_exp2(r_m[w * 8 + h] - M);
-                acc = fmaf(f, r_o[(w * D + j) * 8 + h] + r_z[(w * 8 + j / C.group) * 8 + h], acc);
+                acc = fmaf(f, r_o[(w * D + j) * 8 + h] + r_z[(w * 8 + (j >> gshift)) * 8 + h], acc);
                 l = fmaf(f, r_l[w * 8 + h], l);
             }
         }
