@@ -6,7 +6,7 @@
 //
 // Tile = 128 token-heads; one persistent CTA per SM, 384 threads in two roles
 // that overlap consecutive tiles:
-//  producers (warps 8-11)
+//  producers (warps 8-15)
 //  1. issue every global load of the tile's keys (and the first value rows),
 //     take each key's norm in fp32 (sum of exact squares) and convert it
 //     exactly to fp16 after a power-of-two scale 2^e per row;
@@ -45,9 +45,10 @@ namespace {
 
 constexpr int D = 128;
 constexpr int TM = 128;
-constexpr int kThreads = 384;       // warps 0-7: epilogue; warps 8-11: producers
+constexpr int kThreads = 512;       // warps 0-7: epilogue; warps 8-15: producers
 constexpr int kEpi = 256;           // epilogue threads: TMEM lane quarter (warp & 3), column half (warp >> 2)
-constexpr int kProd = 128;          // producer threads: key conversion, MMA issue, values
+constexpr int kProd = 256;          // producer threads: key conversion, MMA issue, values
+constexpr int kPasses = TM / (8 * (kProd / 32));  // 8-row passes per producer warp and tile
 constexpr int kWarps = kThreads / 32;
 constexpr int kEpiWarps = kEpi / 32;
 constexpr float kCodeGuard = 1e-5f;   // z units
@@ -489,12 +490,12 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             // pass p covers rows 32 pw + 8 p + lane / 4; lane & 3 = sub takes key
             // chunks sub + 4 j and value channels [32 sub, 32 sub + 32) ----
             const int sub = lane & 3;
-            uint4 kr[4][4], va[4];
-            int64_t sl[4];
-            int hh[4];
+            uint4 kr[kPasses][4], va[4];
+            int64_t sl[kPasses];
+            int hh[kPasses];
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const int64_t r = r0 + 32 * pw + 8 * p + (lane >> 2);
+            for (int p = 0; p < kPasses; ++p) {
+                const int64_t r = r0 + 8 * kPasses * pw + 8 * p + (lane >> 2);
                 sl[p] = -1;
                 hh[p] = 0;
                 if (r < rows) {
@@ -527,14 +528,14 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                     *p_abort = 1;
                 }
             }
-            asm volatile("bar.sync 2, 128;" ::: "memory");
+            asm volatile("bar.sync 2, 256;" ::: "memory");
             if (*p_abort) break;
             // ---- keys: norm, power-of-two scale, exact fp16 conversion into the A tile ----
-            int64_t dst[4];
-            int offs[4];
+            int64_t dst[kPasses];
+            int offs[kPasses];
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const int rl = 32 * pw + 8 * p + (lane >> 2);
+            for (int p = 0; p < kPasses; ++p) {
+                const int rl = 8 * kPasses * pw + 8 * p + (lane >> 2);
                 const int64_t sp = sl[p];
                 dst[p] = -1;
                 offs[p] = 0;
@@ -599,7 +600,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 }
             }
             umma::fence_proxy_async();
-            asm volatile("bar.sync 2, 128;" ::: "memory");
+            asm volatile("bar.sync 2, 256;" ::: "memory");
             if (ptid == 0) {
                 // ---- rotation MMAs: Y = K' (Pi_lo + Pi_hi)^T, once the epilogue has read Y ----
                 bool ok = true;
@@ -627,12 +628,12 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             // ---- values of this tile: pass p + 1 is loaded while pass p is quantised ----
             const int lpg = C.group >> 5;  // lanes per group: 1, 2 or 4
 #pragma unroll 1
-            for (int p = 0; p < 4; ++p) {
+            for (int p = 0; p < kPasses; ++p) {
                 uint4 vb[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) vb[j] = make_uint4(0u, 0u, 0u, 0u);
-                const int64_t rn1 = r0 + 32 * pw + 8 * (p + 1) + (lane >> 2);
-                if (p < 3 && rn1 < rows) {
+                const int64_t rn1 = r0 + 8 * kPasses * pw + 8 * (p + 1) + (lane >> 2);
+                if (p + 1 < kPasses && rn1 < rows) {
                     const int64_t t = small_rows ? static_cast<int64_t>(static_cast<uint32_t>(rn1) / static_cast<uint32_t>(Hkv))
                                                  : rn1 / Hkv;
                     const uint4 *vsrc = reinterpret_cast<const uint4 *>(vin + t * vs + (rn1 - t * Hkv) * D);
@@ -641,7 +642,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 }
                 uint32_t cw[VB], meta;
                 quantize_values32<VB>(va, lpg, cw, meta);
-                const int rl = 32 * pw + 8 * p + (lane >> 2);
+                const int rl = 8 * kPasses * pw + 8 * p + (lane >> 2);
                 const int64_t vdst = rinfo[rl].dst;
                 if (vdst >= 0) {
                     const int voff = rinfo[rl].off;

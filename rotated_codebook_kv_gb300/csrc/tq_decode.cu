@@ -53,51 +53,123 @@ namespace {
 
 
 // ---- (1) query pre-rotation ------------------------------------------------
+// kQRows query rows per block of 2 D threads: thread (i, half) sums coordinate i
+// of each row over half of the inner index, so every element of Pi (and S)
+// read from L2 feeds kQRows independent FMA chains; the halves add in shared memory.
+constexpr int kQRows = 4;
+
 template <int D>
-__global__ void __launch_bounds__(D) qrot_kernel(const Codec C, const uint16_t *__restrict__ q, float *qrot, float *qs)
+__global__ void __launch_bounds__(2 * D) qrot_kernel(const Codec C, const uint16_t *__restrict__ q, float *qrot,
+                                                     float *qs, int rows)
 {
-    __shared__ float sq[D];
-    __shared__ float sr[D];
-    const int row = blockIdx.x, i = threadIdx.x;
-    sq[i] = bf16_to_float(q[static_cast<int64_t>(row) * D + i]);
+    __shared__ float sq[kQRows][D];
+    __shared__ float part[kQRows][D];
+    const int r0 = blockIdx.x * kQRows;
+    const int i = threadIdx.x % D, hf = threadIdx.x / D;
+    const int nr = min(kQRows, rows - r0);
+    if (hf == 0) {
+#pragma unroll
+        for (int r = 0; r < kQRows; ++r) sq[r][i] = (r < nr) ? bf16_to_float(q[static_cast<int64_t>(r0 + r) * D + i]) : 0.f;
+    }
     __syncthreads();
-    float a = 0.f;
-    for (int j = 0; j < D; ++j) a = fmaf(__ldg(C.PiT + j * D + i), sq[j], a);
-    sr[i] = a;
-    qrot[static_cast<int64_t>(row) * D + i] = a;
+    auto matvec = [&](const float *__restrict__ MT, float (&a)[kQRows]) {  // a[r] = sum_j MT[j][i] sq[r][j], j in this half
+#pragma unroll
+        for (int r = 0; r < kQRows; ++r) a[r] = 0.f;
+        const int j0 = hf * (D / 2);
+#pragma unroll 16
+        for (int j = j0; j < j0 + D / 2; ++j) {
+            const float m = __ldg(MT + j * D + i);
+#pragma unroll
+            for (int r = 0; r < kQRows; ++r) a[r] = fmaf(m, sq[r][j], a[r]);
+        }
+        if (hf == 1) {
+#pragma unroll
+            for (int r = 0; r < kQRows; ++r) part[r][i] = a[r];
+        }
+        __syncthreads();
+        if (hf == 0) {
+#pragma unroll
+            for (int r = 0; r < kQRows; ++r) a[r] += part[r][i];
+        }
+    };
+    float a[kQRows];
+    matvec(C.PiT, a);
+    if (hf == 0)
+        for (int r = 0; r < nr; ++r) qrot[static_cast<int64_t>(r0 + r) * D + i] = a[r];
     if (!C.qjl) return;
+    __syncthreads();  // every thread has read sq and part
+    if (hf == 0) {
+#pragma unroll
+        for (int r = 0; r < kQRows; ++r) sq[r][i] = a[r];
+    }
     __syncthreads();
-    float b = 0.f;
-    for (int j = 0; j < D; ++j) b = fmaf(__ldg(C.ST + j * D + i), sr[j], b);
-    qs[static_cast<int64_t>(row) * D + i] = b;
+    matvec(C.ST, a);
+    if (hf == 0)
+        for (int r = 0; r < nr; ++r) qs[static_cast<int64_t>(r0 + r) * D + i] = a[r];
 }
 
 // ---- (2) split-K decode: see tq_decode_mma.cuh ---------------------------------
 
 // ---- (3) log-sum-exp combine -------------------------------------------------
+// One block per (b, h): the split weights 2^(m_s - M) are computed once into
+// shared memory, then thread j sums its coordinate over the splits.
+constexpr int kMaxSplits = 1024;
+
 template <int D>
 __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs A)
 {
+    __shared__ float sw[kMaxSplits];
+    __shared__ float red[D / 32];
+    __shared__ float s_den;
     const int row = blockIdx.x;  // b * Hq + h
-    const int j = threadIdx.x;
+    const int j = threadIdx.x, lane = j & 31, warp = j >> 5;
     const size_t rows = static_cast<size_t>(A.B) * A.Hq;
+    // M = max over splits with l > 0
     float M = -INFINITY;
-    for (int s = 0; s < A.splits; ++s) {
-        const float l = A.ws.ml[(s * rows + row) * 2 + 1];
-        if (l > 0.f) M = fmaxf(M, A.ws.ml[(s * rows + row) * 2]);
+    for (int s = j; s < A.splits; s += D) {
+        const float2 ml = *reinterpret_cast<const float2 *>(A.ws.ml + (s * rows + row) * 2);
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
     }
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < A.splits; ++s) {
-            const float m = A.ws.ml[(s * rows + row) * 2];
-            const float l = A.ws.ml[(s * rows + row) * 2 + 1];
-            if (!(l > 0.f)) continue;
-            const float w = exp2f(m - M);
-            den = fmaf(w, l, den);
-            num = fmaf(w, A.ws.acc[(s * rows + row) * D + j], num);
-        }
+    M = warp_max(M);
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
+    __syncthreads();
+    float den = 0.f;
+    for (int s = j; s < A.splits; s += D) {
+        const float2 ml = *reinterpret_cast<const float2 *>(A.ws.ml + (s * rows + row) * 2);
+        const float w = (ml.y > 0.f && M != -INFINITY) ? exp2f(ml.x - M) : 0.f;
+        sw[s] = w;
+        den = fmaf(w, (ml.y > 0.f) ? ml.y : 0.f, den);
     }
-    const float o = (den > 0.f) ? num / den : 0.f;
+    den = warp_sum(den);
+    if (lane == 0) red[warp] = den;
+    __syncthreads();
+    if (j == 0) {
+        float d = 0.f;
+#pragma unroll
+        for (int w = 0; w < D / 32; ++w) d += red[w];
+        s_den = d;
+    }
+    __syncthreads();
+    const float* acc = A.ws.acc + row * D + j;
+    float n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
+    int s = 0;
+    for (; s + 4 <= A.splits; s += 4) {
+        const float w0 = sw[s], w1 = sw[s + 1], w2 = sw[s + 2], w3 = sw[s + 3];
+        // skipped splits may hold stale partials: read only those with weight
+        if (w0 != 0.f) n0 = fmaf(w0, acc[(s + 0) * rows * D], n0);
+        if (w1 != 0.f) n1 = fmaf(w1, acc[(s + 1) * rows * D], n1);
+        if (w2 != 0.f) n2 = fmaf(w2, acc[(s + 2) * rows * D], n2);
+        if (w3 != 0.f) n3 = fmaf(w3, acc[(s + 3) * rows * D], n3);
+    }
+    for (; s < A.splits; ++s)
+        if (sw[s] != 0.f) n0 = fmaf(sw[s], acc[s * rows * D], n0);
+    const float num = (n0 + n1) + (n2 + n3);
+    const float dd = s_den;
+    const float o = (dd > 0.f) ? num / dd : 0.f;
     A.out[static_cast<size_t>(row) * D + j] = float_to_bf16_bits(o);
 }
 
@@ -133,7 +205,8 @@ cudaError_t launch_dmma_kb(const Codec &c, const PageGeom &pg, const DecodeArgs 
 template <int D>
 cudaError_t launch_decode_d(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st)
 {
-    qrot_kernel<D><<<a.B * a.Hq, D, 0, st>>>(c, a.q, a.ws.qrot, a.ws.qs);
+    const int qrows = a.B * a.Hq;
+    qrot_kernel<D><<<(qrows + kQRows - 1) / kQRows, 2 * D, 0, st>>>(c, a.q, a.ws.qrot, a.ws.qs, qrows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     switch (c.k_bits) {
