@@ -85,7 +85,7 @@ constexpr float kBinMagic = 12582912.f + 96.f;
 struct RowInfo {     // 32 bytes per row
     int64_t dst;     // record index (block * Hkv + head) or -1
     int off;         // offset inside the page
-    int flag;        // bit0 code guard, bit1 sign guard, bit2 redo row, bit3 zero key
+    int flag;        // bit0 code guard, bit1 sign guard, bit2 tiny key, bit3 zero key, bit4 gamma near a bf16 midpoint
     float zscale;    // sqrt(d) / (n 2^(10+e)) applied to Y
     float rn;        // ||r|| in z units
     uint32_t n16g16; // bf16 norm | bf16 gamma << 16
@@ -138,20 +138,24 @@ __device__ __forceinline__ void set_code(uint32_t *w, int j, uint32_t v)
 }
 
 // The whole key row in compensated arithmetic, by one warp (see tq_compress.cu).
+// Lane l owns coordinates l + 32 m (m < 4): the four compensated sums are
+// independent chains and the inner loop is unrolled, so many row reads of Pi^T
+// (and S^T) are in flight at once.  signs_too = false keeps the sign bits (a
+// row redone only because gamma sits near a bf16 rounding midpoint).
 template <int KB>
 __device__ __noinline__ void exact_row(const Codec &C, const float *kw, double n_sc, uint32_t *codes, uint32_t *signs,
-                          uint32_t *n16g16, double *scratch, double n_true)
+                                       uint32_t *n16g16, double *scratch, double n_true, bool signs_too)
 {
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
     float yh[E], yl[E];
 #pragma unroll
-    for (int m = 0; m < E; ++m) {
-        const int i = lane + 32 * m;
-        float hs = 0.f, hc = 0.f;
-        for (int j = 0; j < D; ++j) dot2_step(hs, hc, __ldg(C.PiT + j * D + i), kw[j]);
-        yh[m] = hs;
-        yl[m] = hc;
+    for (int m = 0; m < E; ++m) yh[m] = yl[m] = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < D; ++j) {
+        const float kj = kw[j];
+#pragma unroll
+        for (int m = 0; m < E; ++m) dot2_step(yh[m], yl[m], __ldg(C.PiT + j * D + lane + 32 * m), kj);
     }
     __syncwarp();  // scratch aliases the key copy read above
     const double zscale = sqrt(static_cast<double>(D)) / n_sc;
@@ -183,7 +187,7 @@ __device__ __noinline__ void exact_row(const Codec &C, const float *kw, double n
     const uint32_t g16 = C.qjl ? double_to_bf16_bits(sqrt(rr) / sqrt(static_cast<double>(D))) : 0u;
     if (lane == 0) *n16g16 = double_to_bf16_bits(n_true) | (g16 << 16);
     __syncwarp();
-    if (!C.qjl) return;
+    if (!C.qjl || !signs_too) return;
     // residual as float hi + lo pairs (the inner loop then needs no fp64)
     float2 *rp = reinterpret_cast<float2 *>(scratch);
     float2 mine[E];
@@ -197,22 +201,26 @@ __device__ __noinline__ void exact_row(const Codec &C, const float *kw, double n
 #pragma unroll
     for (int m = 0; m < E; ++m) rp[lane + 32 * m] = mine[m];
     __syncwarp();
+    float ps[E], pc[E];
+#pragma unroll
+    for (int m = 0; m < E; ++m) ps[m] = pc[m] = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < D; ++j) {
+        const float2 r2 = rp[j];
+#pragma unroll
+        for (int m = 0; m < E; ++m) {
+            const float sv = __ldg(C.ST + j * D + lane + 32 * m);
+            dot2_step(ps[m], pc[m], sv, r2.x);
+            pc[m] = __fmaf_rn(sv, r2.y, pc[m]);
+        }
+    }
 #pragma unroll
     for (int m = 0; m < E; ++m) {
-        const int i = lane + 32 * m;
-        float ps = 0.f, pc = 0.f;
-        for (int j = 0; j < D; ++j) {
-            const float2 r2 = rp[j];
-            const float sv = __ldg(C.ST + j * D + i);
-            dot2_step(ps, pc, sv, r2.x);
-            pc = __fmaf_rn(sv, r2.y, pc);
-        }
-        const uint32_t bits = __ballot_sync(0xffffffffu, __fadd_rn(ps, pc) >= 0.f);
+        const uint32_t bits = __ballot_sync(0xffffffffu, __fadd_rn(ps[m], pc[m]) >= 0.f);
         if (lane == 0) signs[m] = bits;
     }
     __syncwarp();
 }
-
 
 // Epilogue 1 for one (row, 32-column block cb): codes, guard mask, residual
 // split into fp16 hi / lo operands (QJL only), and the block's sum of squares of
@@ -719,6 +727,20 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                         }
                     umma::commit(mbarP);
                 }
+            }
+            // ---- while the projection runs: code words and norm of this row's record
+            // (a row whose decisions are re-taken exactly rewrites them below) ----
+            if (ri.dst >= 0) {
+                uint8_t *krec = kc + ri.dst * G.k_page;
+                uint32_t *cd = reinterpret_cast<uint32_t *>(krec + static_cast<int64_t>(ri.off) * C.k_code_bytes);
+                const uint32_t *cw = scodes + row * 16;
+#pragma unroll
+                for (int w = 0; w < NKW / 2; ++w) cd[hf * (NKW / 2) + w] = zero ? 0u : cw[hf * (NKW / 2) + w];
+                if (hf == 0)
+                    *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * ri.off) =
+                        zero ? 0 : static_cast<uint16_t>(ri.n16g16 & 0xffffu);
+            }
+            if (C.qjl) {
                 if (!umma::mbar_wait_bounded(mbarP, par, kWaitLimit)) {
                     atomicOr(C.status, TQ_DEVERR_TIMEOUT);
                     *e_abort = 1;
@@ -734,13 +756,13 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                     int ge;
                     const float fr = frexpf(gam, &ge);  // gam = fr 2^ge, fr in [0.5, 1)
                     const float u = fr * 256.f;         // bf16 keeps 8 significant bits
-                    if (fabsf(u - floorf(u) - 0.5f) / u < kGammaGuard) flag |= 4;
+                    if (fabsf(u - floorf(u) - 0.5f) / u < kGammaGuard) flag |= 16;
                 }
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
             if (*e_abort) break;
             if (C.qjl) flag |= s_flags[row * 2] | s_flags[row * 2 + 1];
-            if (zero) flag = 8 | (ri.flag & ~7);
+            if (zero) flag = 8;
             if (hf == 0) {
                 rinfo[row].flag = flag;
                 rinfo[row].rn = rn;
@@ -749,7 +771,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             asm volatile("bar.sync 1, 256;" ::: "memory");
             // ---- exact re-decisions, one warp per flagged row (scratch in tile B): the two
             // warps of a lane quarter take alternate flagged rows of that quarter ----
-            uint32_t pend = __ballot_sync(0xffffffffu, (flag & 7) != 0 && (flag & 8) == 0 && ri.dst >= 0);
+            uint32_t pend = __ballot_sync(0xffffffffu, (flag & 23) != 0 && (flag & 8) == 0 && ri.dst >= 0);
             for (int k = 0; pend != 0u; ++k) {
                 const int rl = 32 * (warp & 3) + __ffs(pend) - 1;
                 pend &= pend - 1u;
@@ -789,7 +811,8 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 const double n_sc = sqrt(static_cast<double>(s) + static_cast<double>(c));
                 __syncwarp();
                 uint32_t *cw = scodes + rl * 16;
-                bool redo = (flg & 4) != 0;
+                bool redo = (flg & 20) != 0;   // tiny key or gamma near a rounding midpoint
+                bool signs_too = (flg & 6) != 0;
                 if (!redo && (flg & 1)) {  // codes near a threshold
                     for (int w = 0; w < 4 && !redo; ++w) {
                         uint32_t m = smask[rl * 8 + w];
@@ -799,12 +822,12 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                             const double z = warp_dot_df(C.Pi + j * D, kw) * (sqrt(static_cast<double>(D)) / n_sc);
                             uint32_t code = 0;
                             for (int tt = 0; tt < nthr; ++tt) code += (static_cast<double>(C.thresholds[tt]) <= z);
-                            if (code != get_code<KB>(cw, j)) redo = true;  // the residual changes: redo the row
+                            if (code != get_code<KB>(cw, j)) redo = signs_too = true;  // the residual changes: redo the row
                         }
                     }
                 }
                 if (redo) {
-                    exact_row<KB>(C, kw, n_sc, cw, ssigns + rl * 4, &rinfo[rl].n16g16, scratch, ldexp(n_sc, ex));
+                    exact_row<KB>(C, kw, n_sc, cw, ssigns + rl * 4, &rinfo[rl].n16g16, scratch, ldexp(n_sc, ex), signs_too);
                     continue;
                 }
                 if (flg & 2) {  // signs near zero: p_i = sqrt(d) (M_i . k) / n - S_i . c
@@ -842,27 +865,30 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 }
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            // ---- key records: thread (row, half) ----
+            // ---- key records, rest: signs and gamma; codes and norm again for rows
+            // re-decided exactly ----
             const RowInfo rf = rinfo[row];
             if (rf.dst >= 0) {
                 const bool z0 = (rf.flag & 8) != 0;
+                const bool redone = (rf.flag & 23) != 0 && !z0;
                 uint8_t *krec = kc + rf.dst * G.k_page;
-                uint32_t *cd = reinterpret_cast<uint32_t *>(krec + static_cast<int64_t>(rf.off) * C.k_code_bytes);
-                const uint32_t *cw = scodes + row * 16;
+                if (redone) {
+                    uint32_t *cd = reinterpret_cast<uint32_t *>(krec + static_cast<int64_t>(rf.off) * C.k_code_bytes);
+                    const uint32_t *cw = scodes + row * 16;
 #pragma unroll
-                for (int w = 0; w < NKW / 2; ++w) cd[hf * (NKW / 2) + w] = z0 ? 0u : cw[hf * (NKW / 2) + w];
+                    for (int w = 0; w < NKW / 2; ++w) cd[hf * (NKW / 2) + w] = cw[hf * (NKW / 2) + w];
+                    if (hf == 0)
+                        *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * rf.off) =
+                            static_cast<uint16_t>(rf.n16g16 & 0xffffu);
+                }
                 if (C.qjl) {
                     const uint32_t *sw = ssigns + row * 4;
                     uint2 *sd = reinterpret_cast<uint2 *>(krec + G.k_sign_off + static_cast<int64_t>(rf.off) * C.k_sign_bytes);
                     sd[hf] = z0 ? make_uint2(0u, 0u) : make_uint2(sw[2 * hf], sw[2 * hf + 1]);
                 }
-                if (hf == 0) {
-                    *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * rf.off) =
-                        z0 ? 0 : static_cast<uint16_t>(rf.n16g16 & 0xffffu);
-                    if (C.qjl)
-                        *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * rf.off) =
-                            z0 ? 0 : static_cast<uint16_t>(rf.n16g16 >> 16);
-                }
+                if (hf == 0 && C.qjl)
+                    *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * rf.off) =
+                        z0 ? 0 : static_cast<uint16_t>(rf.n16g16 >> 16);
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
         }
