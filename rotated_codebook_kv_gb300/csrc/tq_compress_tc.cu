@@ -66,7 +66,9 @@ constexpr uint32_t kOffMask = kOffSigns + TM * 16;   // [TM][8] u32: code guard 
 constexpr uint32_t kOffRow = kOffMask + TM * 32;     // [3][TM] RowInfo (tile index mod 3)
 constexpr uint32_t kOffPart = kOffRow + 3 * TM * 32; // [TM][2] gsq partials, [TM][2] code flags, [TM][2] sign flags
 constexpr uint32_t kOffBins = kOffPart + TM * 24;    // [256] float4 code bins (below)
-constexpr uint32_t kOffMisc = kOffBins + 256 * 16;   // mbarriers, TMEM slot, abort flags
+constexpr int kMaxDefer = 24;                        // rows awaiting exact re-decision
+constexpr uint32_t kOffDefer = kOffBins + 256 * 16;  // [kMaxDefer] Deferred
+constexpr uint32_t kOffMisc = kOffDefer + kMaxDefer * 64;  // mbarriers, TMEM slot, abort flags
 constexpr uint32_t kSmemBytes = kOffMisc + 64;
 static_assert(kSmemBytes <= 232448, "shared memory map exceeds the per-block limit");
 
@@ -81,6 +83,18 @@ constexpr uint32_t kIdesc = umma::idesc_f16(128, 128);
 // bin holds at most one threshold.  Entry: {threshold (or +inf), centroid below
 // it, centroid above it, code below it (as raw bits)}, all but the code times 2^12.
 constexpr float kBinMagic = 12582912.f + 96.f;
+
+// A row whose decisions are re-taken exactly after its record was written with
+// the fast-path results.
+struct Deferred {      // 64 bytes
+    int64_t r;         // token-head row of the input
+    int64_t dst;       // record index (block * Hkv + head)
+    int off;           // offset inside the page
+    int flag;          // as RowInfo::flag
+    uint32_t cmask[4]; // codes within the guard band of a threshold
+    uint32_t smask[4]; // sign bits within the guard band of zero
+    int pad[2];
+};
 
 struct RowInfo {     // 32 bytes per row
     int64_t dst;     // record index (block * Hkv + head) or -1
@@ -220,6 +234,119 @@ __device__ __noinline__ void exact_row(const Codec &C, const float *kw, double n
         if (lane == 0) signs[m] = bits;
     }
     __syncwarp();
+}
+
+// Exact re-decision of one deferred row by one warp: the fast-path codes and
+// signs are read back from its record, decisions inside a guard band are taken
+// again in compensated arithmetic, and what changed is written back.
+// cw (16 words), sw (4 words), n16 (1 word) and scratch (d doubles) are this
+// warp's shared-memory space.
+template <int KB>
+__device__ __noinline__ void fix_row(const Codec &C, const PageGeom &G, const uint16_t *__restrict__ kin, int64_t ks,
+                                     int Hkv, uint8_t *__restrict__ kc, const Deferred &df, uint32_t *cw, uint32_t *sw,
+                                     uint32_t *n16, double *scratch)
+{
+    constexpr int NKW = D * KB / 32;
+    const int lane = threadIdx.x & 31;
+    const int nthr = (1 << KB) - 1;
+    const int flg = df.flag;
+    uint8_t *krec = kc + df.dst * G.k_page;
+    uint32_t *cd = reinterpret_cast<uint32_t *>(krec + static_cast<int64_t>(df.off) * C.k_code_bytes);
+    uint32_t *sd = reinterpret_cast<uint32_t *>(krec + G.k_sign_off + static_cast<int64_t>(df.off) * C.k_sign_bytes);
+    if (lane < NKW) cw[lane] = __ldcg(cd + lane);
+    if (C.qjl && lane < 4) sw[lane] = __ldcg(sd + lane);
+    const int64_t t = df.r / Hkv;
+    const uint16_t *src = kin + t * ks + static_cast<int64_t>(df.r - t * Hkv) * D;
+    float *kw = reinterpret_cast<float *>(scratch);
+    float kx[D / 32];
+    float mx = 0.f;
+#pragma unroll
+    for (int m = 0; m < D / 32; ++m) {
+        kx[m] = bf16_to_float(src[lane + 32 * m]);
+        mx = fmaxf(mx, fabsf(kx[m]));
+    }
+    mx = warp_max(mx);
+    int ex;
+    frexpf(mx, &ex);
+    const float sc = ldexpf(1.f, -ex);
+    float s = 0.f, c = 0.f;
+#pragma unroll
+    for (int m = 0; m < D / 32; ++m) {
+        kx[m] *= sc;
+        dot2_step(s, c, kx[m], kx[m]);
+        kw[lane + 32 * m] = kx[m];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o), c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        float tt, e;
+        two_sum(s, s2, tt, e);
+        s = tt;
+        c = __fadd_rn(c, __fadd_rn(c2, e));
+    }
+    const double n_sc = sqrt(static_cast<double>(s) + static_cast<double>(c));
+    __syncwarp();
+    bool redo = (flg & 20) != 0;  // tiny key or gamma near a rounding midpoint
+    bool signs_too = (flg & 6) != 0;
+    if (!redo && (flg & 1)) {  // codes near a threshold
+        for (int w = 0; w < 4 && !redo; ++w) {
+            uint32_t m = df.cmask[w];
+            while (m && !redo) {
+                const int j = 32 * w + __ffs(m) - 1;
+                m &= m - 1;
+                const double z = warp_dot_df(C.Pi + j * D, kw) * (sqrt(static_cast<double>(D)) / n_sc);
+                uint32_t code = 0;
+                for (int tt = 0; tt < nthr; ++tt) code += (static_cast<double>(C.thresholds[tt]) <= z);
+                if (code != get_code<KB>(cw, j)) redo = signs_too = true;  // the residual changes: redo the row
+            }
+        }
+    }
+    bool signs_changed = false;
+    if (redo) {
+        exact_row<KB>(C, kw, n_sc, cw, sw, n16, scratch, ldexp(n_sc, ex), signs_too);
+        signs_changed = C.qjl && signs_too;
+    } else if (flg & 2) {  // signs near zero: p_i = sqrt(d) (M_i . k) / n - S_i . c
+        signs_changed = true;
+        for (int w = 0; w < 4; ++w) {
+            uint32_t m = df.smask[w];
+            while (m) {
+                const int i = 32 * w + __ffs(m) - 1;
+                m &= m - 1;
+                const double mk = warp_dot_df(C.M_hi + i * D, kw) + warp_dot_df(C.M_lo + i * D, kw);
+                float sh = 0.f, scc = 0.f;
+#pragma unroll
+                for (int mm = 0; mm < D / 32; ++mm) {
+                    const int j = lane + 32 * mm;
+                    dot2_step(sh, scc, __ldg(C.S + i * D + j), C.centroids[get_code<KB>(cw, j)]);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float s2 = __shfl_xor_sync(0xffffffffu, sh, o);
+                    const float c2 = __shfl_xor_sync(0xffffffffu, scc, o);
+                    float tt, e;
+                    two_sum(sh, s2, tt, e);
+                    sh = tt;
+                    scc = __fadd_rn(scc, __fadd_rn(c2, e));
+                }
+                const double p = mk * (sqrt(static_cast<double>(D)) / n_sc) - (static_cast<double>(sh) + static_cast<double>(scc));
+                if (lane == 0) {
+                    const uint32_t bit = 1u << (i & 31);
+                    sw[w] = (p >= 0.0) ? (sw[w] | bit) : (sw[w] & ~bit);
+                }
+                __syncwarp();
+            }
+        }
+    }
+    __syncwarp();
+    if (redo) {
+        if (lane < NKW) cd[lane] = cw[lane];
+        if (lane == 0) {
+            *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * df.off) = static_cast<uint16_t>(*n16 & 0xffffu);
+            if (C.qjl)
+                *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * df.off) = static_cast<uint16_t>(*n16 >> 16);
+        }
+    }
+    if (signs_changed && lane < 4) sd[lane] = sw[lane];
 }
 
 // Epilogue 1 for one (row, 32-column block cb): codes, guard mask, residual
@@ -676,6 +803,17 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     } else {
         // =========================== epilogue ==================================
         const int row = 32 * (warp & 3) + lane, hf = warp >> 2;
+        Deferred *defer = reinterpret_cast<Deferred *>(smem + kOffDefer);
+        int *s_qcount = reinterpret_cast<int *>(smem + kOffMisc + 44);  // [4] flagged rows per lane quarter
+        int ndefer = 0;  // same value in every epilogue thread
+        auto drain = [&](int n) {  // all epilogue threads; warp w fixes entries w, w + 8, ...
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            double *scr = reinterpret_cast<double *>(smem + kOffTB) + warp * D;
+            for (int e = warp; e < n; e += kEpiWarps)
+                fix_row<KB>(C, G, kin, ks, Hkv, kc, defer[e], scodes + warp * 16, ssigns + warp * 4,
+                            reinterpret_cast<uint32_t *>(s_gsq) + warp, scr);
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+        };
         int it = 0, buf = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it, buf = (buf == 2 ? 0 : buf + 1)) {
             const int64_t r0 = static_cast<int64_t>(tile) * TM;
@@ -769,118 +907,11 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 rinfo[row].n16g16 = n16g16;
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            // ---- exact re-decisions, one warp per flagged row (scratch in tile B): the two
-            // warps of a lane quarter take alternate flagged rows of that quarter ----
-            uint32_t pend = __ballot_sync(0xffffffffu, (flag & 23) != 0 && (flag & 8) == 0 && ri.dst >= 0);
-            for (int k = 0; pend != 0u; ++k) {
-                const int rl = 32 * (warp & 3) + __ffs(pend) - 1;
-                pend &= pend - 1u;
-                if ((k & 1) != hf) continue;
-                const int flg = rinfo[rl].flag;
-                const int64_t r = r0 + rl;
-                const int64_t t = r / Hkv;
-                const uint16_t *src = kin + t * ks + static_cast<int64_t>(r - t * Hkv) * D;
-                double *scratch = reinterpret_cast<double *>(smem + kOffTB) + warp * D;
-                float *kw = reinterpret_cast<float *>(scratch);
-                float kx[D / 32];
-                float mx = 0.f;
-#pragma unroll
-                for (int m = 0; m < D / 32; ++m) {
-                    kx[m] = bf16_to_float(src[lane + 32 * m]);
-                    mx = fmaxf(mx, fabsf(kx[m]));
-                }
-                mx = warp_max(mx);
-                int ex;
-                frexpf(mx, &ex);
-                const float sc = ldexpf(1.f, -ex);
-                float s = 0.f, c = 0.f;
-#pragma unroll
-                for (int m = 0; m < D / 32; ++m) {
-                    kx[m] *= sc;
-                    dot2_step(s, c, kx[m], kx[m]);
-                    kw[lane + 32 * m] = kx[m];
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float s2 = __shfl_xor_sync(0xffffffffu, s, o), c2 = __shfl_xor_sync(0xffffffffu, c, o);
-                    float tt, e;
-                    two_sum(s, s2, tt, e);
-                    s = tt;
-                    c = __fadd_rn(c, __fadd_rn(c2, e));
-                }
-                const double n_sc = sqrt(static_cast<double>(s) + static_cast<double>(c));
-                __syncwarp();
-                uint32_t *cw = scodes + rl * 16;
-                bool redo = (flg & 20) != 0;   // tiny key or gamma near a rounding midpoint
-                bool signs_too = (flg & 6) != 0;
-                if (!redo && (flg & 1)) {  // codes near a threshold
-                    for (int w = 0; w < 4 && !redo; ++w) {
-                        uint32_t m = smask[rl * 8 + w];
-                        while (m && !redo) {
-                            const int j = 32 * w + __ffs(m) - 1;
-                            m &= m - 1;
-                            const double z = warp_dot_df(C.Pi + j * D, kw) * (sqrt(static_cast<double>(D)) / n_sc);
-                            uint32_t code = 0;
-                            for (int tt = 0; tt < nthr; ++tt) code += (static_cast<double>(C.thresholds[tt]) <= z);
-                            if (code != get_code<KB>(cw, j)) redo = signs_too = true;  // the residual changes: redo the row
-                        }
-                    }
-                }
-                if (redo) {
-                    exact_row<KB>(C, kw, n_sc, cw, ssigns + rl * 4, &rinfo[rl].n16g16, scratch, ldexp(n_sc, ex), signs_too);
-                    continue;
-                }
-                if (flg & 2) {  // signs near zero: p_i = sqrt(d) (M_i . k) / n - S_i . c
-                    for (int w = 0; w < 4; ++w) {
-                        uint32_t m = smask[rl * 8 + 4 + w];
-                        while (m) {
-                            const int i = 32 * w + __ffs(m) - 1;
-                            m &= m - 1;
-                            const double mk = warp_dot_df(C.M_hi + i * D, kw) + warp_dot_df(C.M_lo + i * D, kw);
-                            float sh = 0.f, scc = 0.f;
-#pragma unroll
-                            for (int mm = 0; mm < D / 32; ++mm) {
-                                const int j = lane + 32 * mm;
-                                dot2_step(sh, scc, __ldg(C.S + i * D + j), C.centroids[get_code<KB>(cw, j)]);
-                            }
-#pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) {
-                                const float s2 = __shfl_xor_sync(0xffffffffu, sh, o);
-                                const float c2 = __shfl_xor_sync(0xffffffffu, scc, o);
-                                float tt, e;
-                                two_sum(sh, s2, tt, e);
-                                sh = tt;
-                                scc = __fadd_rn(scc, __fadd_rn(c2, e));
-                            }
-                            const double p = mk * (sqrt(static_cast<double>(D)) / n_sc) -
-                                             (static_cast<double>(sh) + static_cast<double>(scc));
-                            if (lane == 0) {
-                                uint32_t &sw = ssigns[rl * 4 + w];
-                                const uint32_t bit = 1u << (i & 31);
-                                sw = (p >= 0.0) ? (sw | bit) : (sw & ~bit);
-                            }
-                            __syncwarp();
-                        }
-                    }
-                }
-            }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            // ---- key records, rest: signs and gamma; codes and norm again for rows
-            // re-decided exactly ----
+            // ---- key records, rest: signs and gamma (deferred rows are rewritten when drained) ----
             const RowInfo rf = rinfo[row];
             if (rf.dst >= 0) {
                 const bool z0 = (rf.flag & 8) != 0;
-                const bool redone = (rf.flag & 23) != 0 && !z0;
                 uint8_t *krec = kc + rf.dst * G.k_page;
-                if (redone) {
-                    uint32_t *cd = reinterpret_cast<uint32_t *>(krec + static_cast<int64_t>(rf.off) * C.k_code_bytes);
-                    const uint32_t *cw = scodes + row * 16;
-#pragma unroll
-                    for (int w = 0; w < NKW / 2; ++w) cd[hf * (NKW / 2) + w] = cw[hf * (NKW / 2) + w];
-                    if (hf == 0)
-                        *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * rf.off) =
-                            static_cast<uint16_t>(rf.n16g16 & 0xffffu);
-                }
                 if (C.qjl) {
                     const uint32_t *sw = ssigns + row * 4;
                     uint2 *sd = reinterpret_cast<uint2 *>(krec + G.k_sign_off + static_cast<int64_t>(rf.off) * C.k_sign_bytes);
@@ -891,7 +922,47 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                         z0 ? 0 : static_cast<uint16_t>(rf.n16g16 >> 16);
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
+            // ---- rows needing exact re-decisions join the deferred list; it is drained
+            // by all epilogue warps together whenever it would overflow ----
+            {
+                const bool mine = hf == 0 && (flag & 23) != 0 && !zero && ri.dst >= 0;
+                const uint32_t pend = __ballot_sync(0xffffffffu, mine);
+                if (hf == 0 && lane == 0) s_qcount[warp] = __popc(pend);
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                int prefix = 0, n_t = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int cq = s_qcount[q];
+                    if (q < (warp & 3)) prefix += cq;
+                    n_t += cq;
+                }
+                const int rank = prefix + __popc(pend & ((1u << lane) - 1u));
+                int done = 0;
+                while (done < n_t) {
+                    if (ndefer == kMaxDefer) {
+                        drain(ndefer);
+                        ndefer = 0;
+                    }
+                    const int take = min(kMaxDefer - ndefer, n_t - done);
+                    if (mine && rank >= done && rank < done + take) {
+                        Deferred &d = defer[ndefer + rank - done];
+                        d.r = r0 + row;
+                        d.dst = ri.dst;
+                        d.off = ri.off;
+                        d.flag = flag;
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            d.cmask[w] = smask[row * 8 + w];
+                            d.smask[w] = smask[row * 8 + 4 + w];
+                        }
+                    }
+                    ndefer += take;
+                    done += take;
+                }
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");
         }
+        if (ndefer > 0 && !*e_abort) drain(ndefer);
     }
     // ---- teardown: no MMA may still run when TMEM is freed ----
     __syncthreads();
