@@ -359,6 +359,7 @@ __device__ __forceinline__ float epilogue_rotation_block(unsigned char *smem, ui
 {
     float y[32];
     umma::ld32(tY + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 32 * cb, y);
+    const float zs512 = zs * (1.f / 512.f);
     uint32_t cw[KB];
 #pragma unroll
     for (int w = 0; w < KB; ++w) cw[w] = 0u;
@@ -366,14 +367,14 @@ __device__ __forceinline__ float epilogue_rotation_block(unsigned char *smem, ui
     float gsq = 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const float z = y[i] * zs;
-        const uint32_t bi = __float_as_uint(fmaf(z, 1.f / 512.f, kBinMagic)) & 0xFFu;
+        // z' = y zs is folded into each fused multiply-add
+        const uint32_t bi = __float_as_uint(fmaf(y[i], zs512, kBinMagic)) & 0xFFu;
         const float4 e = bins[bi];
-        const float dz = z - e.x;
+        const float dz = fmaf(y[i], zs, -e.x);
         const bool up = dz >= 0.f;
         if (fabsf(dz) < kCodeGuard * 4096.f) cmask |= 1u << i;
         const uint32_t code = __float_as_uint(e.w) + (up ? 1u : 0u);
-        const float r = z - (up ? e.z : e.y);
+        const float r = fmaf(y[i], zs, -(up ? e.z : e.y));
         gsq = fmaf(r, r, gsq);
         const int o = i * KB;  // compile-time bit offset inside the block
         cw[o >> 5] |= code << (o & 31);
@@ -844,9 +845,6 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             umma::fence_before_sync();
             asm volatile("bar.sync 1, 256;" ::: "memory");
             umma::fence_after_sync();
-            if (tid == 0)
-                asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(mbarYfree))
-                             : "memory");
             const float rn = sqrtf(s_gsq[row * 2] + s_gsq[row * 2 + 1]);
             int flag = ri.flag | s_flagp[row * 2] | s_flagp[row * 2 + 1];
             uint32_t n16g16 = ri.n16g16;
@@ -866,6 +864,10 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                     umma::commit(mbarP);
                 }
             }
+            // Y may be overwritten now: the next tile's rotation queues behind the projection
+            if (tid == 0)
+                asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(mbarYfree))
+                             : "memory");
             // ---- while the projection runs: code words and norm of this row's record
             // (a row whose decisions are re-taken exactly rewrites them below) ----
             if (ri.dst >= 0) {
