@@ -21,6 +21,7 @@ workload (weak scaling, no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -107,7 +108,7 @@ class ClockSampler:
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
@@ -119,11 +120,20 @@ class ClockSampler:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=self.file, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
+        self.window = None
         return self
+
+    def mark(self, start):
+        """Host time of the timed region's start / end: samples outside it are dropped."""
+        now = time.time()
+        if start:
+            self.window = [now, None]
+        elif self.window is not None:
+            self.window[1] = now
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -146,6 +156,17 @@ class ClockSampler:
         os.unlink(self.file.name)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        if self.window is not None and self.window[1] is not None:
+            inside = []
+            for r in rows:
+                try:
+                    ts = datetime.datetime.strptime(r[9], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except (ValueError, IndexError):
+                    continue
+                if self.window[0] <= ts <= self.window[1]:
+                    inside.append(r)
+            if inside:
+                rows = inside
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -241,11 +262,13 @@ def run_gpu(args, rank, world, local_rank):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clocks:
         torch.cuda.synchronize()
+        clocks.mark(True)
         t0.record(stream)
         for s_ in range(args.steps):
             step(s_)
         t1.record(stream)
         torch.cuda.synchronize()
+        clocks.mark(False)
     c_ms = [sum(c_ev[s_][i][0].elapsed_time(c_ev[s_][i][1]) for s_ in range(args.steps)) for i in range(len(layers))]
     d_ms = [sum(d_ev[s_][i][0].elapsed_time(d_ev[s_][i][1]) for s_ in range(args.steps)) for i in range(len(layers))]
     elapsed = t0.elapsed_time(t1) / args.steps
