@@ -4,15 +4,17 @@
 // every 128-token chunk (tokens 16 (warp + 4 i)), with its own online softmax;
 // the warps merge at the end.
 //
-// Scores: S[t][h] = sum_j Khat[t][j] q[h][j] with the 16 tokens of a tile as
-// the M dimension and the G <= 8 query heads as N.  Coordinates are permuted
-// inside every 16-wide k-step so that the A-fragment elements of lane quad m
-// are the four consecutive codes 16 s + 4 m + {0,1,2,3} of a token: pairs of
-// codes index a shared-memory table of fp16 centroid pairs (high part and a
-// low part scaled by 2^11, so the centroid score keeps ~22 bits:
-// q.c = qh.ch + 2^-11 (ql.ch + qh.cl), three MMAs per k-step into two
-// accumulators).  The QJL term sqrt(pi/2)/d * gamma * <S q_rot, 2 sigma - 1>
-// uses a fourth MMA whose A operand is +-1 from the sign bits.
+// Scores: S[t][h] = sum_j Khat[t][j] q[h][j] with tokens as the M dimension and
+// the G <= 8 query heads as N.  Coordinates are permuted inside every 16-wide
+// k-step so that the A-fragment elements of lane quad m are the four
+// consecutive codes 16 s + 4 m + {0,1,2,3} of a token: pairs of codes index a
+// shared-memory table of fp16 centroid pairs (a high part and a low part scaled
+// by 2^11, so the centroid score keeps ~22 bits: q.c = qh.ch + 2^-11 (ql.ch +
+// qh.cl)).  M rows r and r + 8 hold the high and the low parts of the same
+// token, so one 64-bit table load fills two adjacent A registers; MMAs against
+// qh and ql give qh.ch, qh.cl and ql.ch for 8 tokens.  The QJL term
+// sqrt(pi/2)/d * gamma * <S q_rot, 2 sigma - 1> is one more MMA whose A
+// operand is +-1 from the sign bits (rows = 16 tokens).
 //
 // Values: O^T[j][h] += sum_t V[t][j] P[t][h] with coordinates as M.  The score
 // accumulator of a tile, converted to fp16 and transposed in registers
@@ -335,12 +337,13 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
         }
         if (live[0] || live[1]) {
             // ---- scores S[token][head]: this lane feeds tokens row, row + 8 of both tiles ----
-            float sc[2][4], sl[2][4], ss[2][4];
+            // per tile j and token row + 8 hh: a[.][.][0..1] = hi.qh, a[2..3] = lo.qh; b[0..1] = hi.ql
+            float sa[2][2][4], sb[2][2][4], ss[2][4];
             uint32_t krow[2][2], srow[2][2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) sc[j][i] = sl[j][i] = ss[j][i] = 0.f;
+                for (int i = 0; i < 4; ++i) sa[j][0][i] = sa[j][1][i] = sb[j][0][i] = sb[j][1][i] = ss[j][i] = 0.f;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     krow[j][hh] = kp[j] + (o0[j] + row + 8 * hh) * C.k_code_bytes;
@@ -367,9 +370,13 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
                             e[hh][1] = ld64(lut_lane + (((f >> (2 * KB)) & PM) << 5));
                         }
                     }
-                    mma16816(sc[j], e[0][0].x, e[1][0].x, e[0][1].x, e[1][1].x, qf.x, qf.y);
-                    mma16816(sl[j], e[0][0].x, e[1][0].x, e[0][1].x, e[1][1].x, qf.z, qf.w);
-                    mma16816(sl[j], e[0][0].y, e[1][0].y, e[0][1].y, e[1][1].y, qf.x, qf.y);
+                    // M rows r / r + 8 = high / low centroid parts of one token: each table load
+                    // (hi, lo) fills two adjacent A registers
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        mma16816(sa[j][hh], e[hh][0].x, e[hh][0].y, e[hh][1].x, e[hh][1].y, qf.x, qf.y);
+                        mma16816(sb[j][hh], e[hh][0].x, e[hh][0].y, e[hh][1].x, e[hh][1].y, qf.z, qf.w);
+                    }
                     if (QJL) {
                         const int rot = (16 * (s & 1) + 4 * quad + 29) & 31;
                         const uint32_t w0 = ld32(srow[j][0] + 4 * (s >> 1)), w1 = ld32(srow[j][1] + 4 * (s >> 1));
@@ -392,7 +399,8 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int i = 2 * hh + e;
-                        float v = nrm * fac_c * fmaf(sl[j][i], 1.f / kLoScale, sc[j][i]);
+                        const float lo = sa[j][hh][2 + e] + sb[j][hh][e];  // lo.qh + hi.ql
+                        float v = nrm * fac_c * fmaf(lo, 1.f / kLoScale, sa[j][hh][e]);
                         if (QJL) v = fmaf(nrm * fac_s * gam, ss[j][i], v);
                         x[j][hh][e] = (2 * quad + e < G) ? (valid ? v : -INFINITY) : 0.f;
                     }
