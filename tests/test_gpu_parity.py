@@ -127,6 +127,37 @@ def test_small_compress_and_decode(name):
     assert codec.get_status() == 0
 
 
+@pytest.mark.parametrize("name", ["pr1_tiny", "mixed_k2v2_small", "mixed_k4v4_small"])
+def test_tiny_magnitudes_take_the_exact_paths(name):
+    """Keys below the fast path's power-of-two row scale are re-decided exactly (every
+    such row, many per 128-row tile, so the deferred list fills and drains several
+    times); values whose group minimum is not an fp16 normal number are quantised
+    by the exact value path.  Both must still match the oracle bit for bit."""
+    w = SMALL[name]
+    b = W.generate(w, device="cpu")
+    T = b.k.shape[0]
+    tiny = torch.zeros(T, dtype=torch.bool)
+    tiny[::3] = True          # keys around 1e-36: beyond the row scale, rows redone exactly
+    small = torch.zeros(T, dtype=torch.bool)
+    small[1::3] = True        # values around 1e-6: fp16 subnormal zero points
+    k = b.k.float()
+    k[tiny] *= 1e-36
+    v = b.v.float()
+    v[small] *= 1e-6
+    b.k, b.v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    b = W.Batch(**{f: (getattr(b, f).to(DEV) if isinstance(getattr(b, f), torch.Tensor) else getattr(b, f))
+                   for f in b.__dataclass_fields__})
+    codec, ora = _codec_pair(w)
+    kc, vc = _compress(codec, w, b)
+    assert codec.get_status() == 0
+    _check_rows(ora, w, b, kc, vc)
+    geo = ora.geometry(w.page_size)
+    ovc = np.full(b.num_blocks * w.num_kv_heads * geo["v_page"], 0xA5, np.uint8)
+    okc = np.full(b.num_blocks * w.num_kv_heads * geo["k_page"], 0xA5, np.uint8)
+    ora.compress_kv(W.as_u16(b.k), W.as_u16(b.v), b.slot_mapping.cpu().numpy(), w.page_size, b.num_blocks, okc, ovc)
+    assert np.array_equal(vc.cpu().numpy(), ovc)
+
+
 @pytest.mark.parametrize("name", ["pr1_tiny", "wide_head_small", "mixed_k2v2_small"])
 def test_dequant_matches_oracle(name):
     w = SMALL[name]
