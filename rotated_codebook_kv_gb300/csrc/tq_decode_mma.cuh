@@ -150,9 +150,9 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     uint2 *slut = reinterpret_cast<uint2 *>(smem + SM::kLut);
     uint4 *qfrag = reinterpret_cast<uint4 *>(smem + SM::kLut + SM::kSignLut);
     uint2 *sfrag = reinterpret_cast<uint2 *>(smem + SM::kLut + SM::kSignLut + SM::kQfrag);
-    int *page_ok = reinterpret_cast<int *>(smem + SM::kLut + SM::kSignLut + SM::kQfrag + SM::kSfrag);  // [2][8]
+    int *page_ok = reinterpret_cast<int *>(smem + SM::kLut + SM::kSignLut + SM::kQfrag + SM::kSfrag);  // [4][2][2]
     uint32_t *zero_meta = reinterpret_cast<uint32_t *>(page_ok + 16);  // [16] zeros: metadata of masked tokens
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(page_ok + 32);        // [2] stage barriers
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(page_ok + 32);        // [4 warps][2 stages] barriers
     const uint32_t zero_off = static_cast<uint32_t>(SM::kLut + SM::kSignLut + SM::kQfrag + SM::kSfrag + 64);
     unsigned char *stages = smem + SM::kHeader;
 
@@ -255,31 +255,38 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     const int vsh = 4 * (row & 1);
     const uint32_t vwoff = 4u * (row >> 2);
 
-    // ---- page loader: thread q < ppc copies page q of a chunk with two bulk copies
-    // (keys, values) that complete on the stage's mbarrier; block ids are read one
-    // chunk ahead ----
-    auto fetch_id = [&](int chunk_page) -> int {
+    // ---- per-warp page pipelines: warp w takes the 32-token rounds w, w + 4, ... of the
+    // split (wpc pages each), with its own two stages and mbarriers, so the warps of a
+    // CTA never wait for one another before the final merge.  Lane q < wpc copies page
+    // q of a round with two bulk copies (keys, values) completing on the stage's
+    // mbarrier; block ids are read one round ahead ----
+    const int wpc = (kTile * kTilesPerWarp) >> pshift;   // pages per round: 2 (P = 16) or 1 (P = 32)
+    const uint32_t page_bytes = static_cast<uint32_t>(PG.k_page + PG.v_page);
+    auto stage_off = [&](int st) -> uint32_t {            // this warp's stage st: wpc pages, K then V each
+        return static_cast<uint32_t>(SM::kHeader) + static_cast<uint32_t>((warp * 2 + st) * wpc) * page_bytes;
+    };
+    auto round_page = [&](int r) -> int { return pg0 + (4 * r + warp) * wpc; };
+    auto fetch_id = [&](int r) -> int {
         int blk = -1;
-        if (tid < ppc && chunk_page + tid < pg1)
-            blk = A.block_table[static_cast<int64_t>(b) * A.max_blocks + chunk_page + tid];
+        const int pgq = round_page(r) + lane;
+        if (lane < wpc && pgq < pg1) blk = A.block_table[static_cast<int64_t>(b) * A.max_blocks + pgq];
         return blk;
     };
-    auto issue = [&](int chunk_page, int st, int blk) {  // by threads tid < ppc
-        const int q = tid;
+    auto issue = [&](int r, int st, int blk) {  // by lanes q < wpc
+        const int q = lane;
         int ok = 0;
-        if (chunk_page + q < pg1) {
+        if (round_page(r) + q < pg1) {
             ok = (blk >= 0 && blk < A.num_blocks);
             if (!ok) atomicOr(C.status, TQ_DEVERR_BLOCK_RANGE);
         }
-        page_ok[st * 8 + q] = ok;
-        const uint32_t bytes = ok ? static_cast<uint32_t>(PG.k_page + PG.v_page) : 0u;
-        const uint32_t mb = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[st]));
+        page_ok[(warp * 2 + st) * 2 + q] = ok;
+        const uint32_t bytes = ok ? page_bytes : 0u;
+        const uint32_t mb = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * 2 + st]));
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes) : "memory");
         if (ok) {
             const size_t rec = static_cast<size_t>(blk) * A.Hkv + kvh;
-            const uint32_t kd = static_cast<uint32_t>(__cvta_generic_to_shared(stages + st * stage_bytes + q * PG.k_page));
-            const uint32_t vd = static_cast<uint32_t>(__cvta_generic_to_shared(stages + st * stage_bytes +
-                                                                               ppc * PG.k_page + q * PG.v_page));
+            const uint32_t kd = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + stage_off(st) + q * page_bytes;
+            const uint32_t vd = kd + static_cast<uint32_t>(PG.k_page);
             asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                          ::"r"(kd), "l"(A.k_cache + rec * PG.k_page), "r"(static_cast<uint32_t>(PG.k_page)), "r"(mb)
                          : "memory");
@@ -289,25 +296,21 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
         }
     };
 
-    const int nchunks = (pg1 - pg0 + ppc - 1) / ppc;
-    if (tid == 0) {
-        mbar_init_cta(&mbar[0], ppc);
-        mbar_init_cta(&mbar[1], ppc);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
+    const int nrounds = (pg1 - pg0 + 4 * wpc - 1) / (4 * wpc);
+    if (tid < 8) mbar_init_cta(&mbar[tid], wpc);
+    if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();  // tables, query fragments and barriers are ready
-    int bnext = fetch_id(pg0);
-    if (tid < ppc) issue(pg0, 0, bnext);
-    bnext = fetch_id(pg0 + ppc);
-    for (int c = 0; c < nchunks; ++c) {
+    int bnext = fetch_id(0);
+    if (lane < wpc) issue(0, 0, bnext);
+    bnext = fetch_id(1);
+    for (int c = 0; c < nrounds; ++c) {
         const int st = c & 1;
-        const int cpage = pg0 + c * ppc;
-        if (c + 1 < nchunks && tid < ppc) {
-            issue(cpage + ppc, st ^ 1, bnext);
-            bnext = fetch_id(cpage + 2 * ppc);
+        if (c + 1 < nrounds && lane < wpc) {
+            issue(c + 1, st ^ 1, bnext);
+            bnext = fetch_id(c + 2);
         }
         {
-            const uint32_t mb = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[st]));
+            const uint32_t mb = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * 2 + st]));
             const uint32_t par = static_cast<uint32_t>((c >> 1) & 1);
             const long long t0 = clock64();
             for (;;) {
@@ -322,18 +325,18 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
             }
         }
 
-        // ---- this warp's two tiles of the chunk: tokens 16 (warp + 4 j) ----
+        // ---- the round's two tiles: tokens 16 j of the round ----
         int kp[2], vp[2], o0[2], pos0[2];
         bool live[2];
+        const int rpage = round_page(c);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int tok0 = kTile * (warp + kWarps * j);
-            const int q = tok0 >> pshift;
-            o0[j] = tok0 & (P - 1);
-            pos0[j] = (cpage + q) * P + o0[j];
-            live[j] = (cpage + q < pg1) && page_ok[st * 8 + q] && (pos0[j] < L);
-            kp[j] = static_cast<int>(SM::kHeader + st * stage_bytes + q * PG.k_page);
-            vp[j] = static_cast<int>(SM::kHeader + st * stage_bytes + ppc * PG.k_page + q * PG.v_page);
+            const int q = (kTile * j) >> pshift;
+            o0[j] = (kTile * j) & (P - 1);
+            pos0[j] = (rpage + q) * P + o0[j];
+            live[j] = (rpage + q < pg1) && page_ok[(warp * 2 + st) * 2 + q] && (pos0[j] < L);
+            kp[j] = static_cast<int>(stage_off(st) + q * page_bytes);
+            vp[j] = kp[j] + static_cast<int>(PG.k_page);
         }
         if (live[0] || live[1]) {
             // ---- scores S[token][head]: this lane feeds tokens row, row + 8 of both tiles ----
@@ -502,8 +505,9 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
                 }
             }
         }
-        __syncthreads();  // the next issue() overwrites this stage
+        __syncwarp();  // the next issue() overwrites this stage
     }
+    __syncthreads();  // every warp is done with the stages before they hold merge data
 
     // ---- merge the four warps ---------------------------------------------------
     float *red = reinterpret_cast<float *>(stages);
