@@ -119,14 +119,16 @@ __device__ void precise_key_row(const Codec &C, const uint16_t *__restrict__ src
     }
     const double n_sc = sqrt(static_cast<double>(s) + static_cast<double>(c));
     __syncwarp();
+    // the lane's E compensated sums are independent chains; with the inner loop
+    // unrolled many row reads of Pi^T are in flight at once
     float yh[E], yl[E];
 #pragma unroll
-    for (int m = 0; m < E; ++m) {
-        const int i = lane + 32 * m;
-        float hs = 0.f, hc = 0.f;
-        for (int j = 0; j < D; ++j) dot2_step(hs, hc, __ldg(C.PiT + j * D + i), kw[j]);
-        yh[m] = hs;
-        yl[m] = hc;
+    for (int m = 0; m < E; ++m) yh[m] = yl[m] = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < D; ++j) {
+        const float kj = kw[j];
+#pragma unroll
+        for (int m = 0; m < E; ++m) dot2_step(yh[m], yl[m], __ldg(C.PiT + j * D + lane + 32 * m), kj);
     }
     __syncwarp();
     const double zscale = sqrt(static_cast<double>(D)) / n_sc;
@@ -150,20 +152,23 @@ __device__ void precise_key_row(const Codec &C, const uint16_t *__restrict__ src
     }
     __syncwarp();
     if (!C.qjl) return;
+    float ps[E], pc[E];
 #pragma unroll
-    for (int m = 0; m < E; ++m) {
-        const int i = lane + 32 * m;
-        float ps = 0.f, pc = 0.f;
-        for (int j = 0; j < D; ++j) {
-            const double rj = scratch[j];
-            const float rh = static_cast<float>(rj);
-            const float rl = static_cast<float>(rj - static_cast<double>(rh));
-            const float sv = __ldg(C.ST + j * D + i);
-            dot2_step(ps, pc, sv, rh);
-            pc = __fmaf_rn(sv, rl, pc);
+    for (int m = 0; m < E; ++m) ps[m] = pc[m] = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < D; ++j) {
+        const double rj = scratch[j];
+        const float rh = static_cast<float>(rj);
+        const float rl = static_cast<float>(rj - static_cast<double>(rh));
+#pragma unroll
+        for (int m = 0; m < E; ++m) {
+            const float sv = __ldg(C.ST + j * D + lane + 32 * m);
+            dot2_step(ps[m], pc[m], sv, rh);
+            pc[m] = __fmaf_rn(sv, rl, pc[m]);
         }
-        p_out[i] = __fadd_rn(ps, pc);
     }
+#pragma unroll
+    for (int m = 0; m < E; ++m) p_out[lane + 32 * m] = __fadd_rn(ps[m], pc[m]);
     __syncwarp();
 }
 
