@@ -69,7 +69,7 @@ constexpr uint32_t kOffBins = kOffPart + TM * 24;    // [256] float4 code bins (
 constexpr int kMaxDefer = 24;                        // rows awaiting exact re-decision
 constexpr uint32_t kOffDefer = kOffBins + 256 * 16;  // [kMaxDefer] Deferred
 constexpr uint32_t kOffMisc = kOffDefer + kMaxDefer * 64;  // mbarriers, TMEM slot, abort flags
-constexpr uint32_t kSmemBytes = kOffMisc + 64;
+constexpr uint32_t kSmemBytes = kOffMisc + 128;  // + 7 descriptor words at kOffMisc + 64
 static_assert(kSmemBytes <= 232448, "shared memory map exceeds the per-block limit");
 
 constexpr uint32_t kSBO = (D / 8) * 128;  // 2048
@@ -583,6 +583,16 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             bins[tid] = e;
         }
         if (tid == 0) {
+            uint32_t *dw = reinterpret_cast<uint32_t *>(smem + kOffMisc + 64);
+            const uint32_t sb = umma::smem_u32(smem);
+            const uint64_t dta = umma::make_desc(sb + kOffTA, 128, kSBO);
+            dw[0] = static_cast<uint32_t>(dta >> 32);
+            dw[1] = static_cast<uint32_t>(dta);
+            dw[2] = static_cast<uint32_t>(umma::make_desc(sb + kOffTB, 128, kSBO));
+            dw[3] = static_cast<uint32_t>(umma::make_desc(sb + kOffPiL, 128, kSBO));
+            dw[4] = static_cast<uint32_t>(umma::make_desc(sb + kOffPiH, 128, kSBO));
+            dw[5] = static_cast<uint32_t>(umma::make_desc(sb + kOffSH, 128, kSBO));
+            dw[6] = static_cast<uint32_t>(umma::make_desc(sb + kOffSL, 128, kSBO));
             umma::mbar_init(mbarY, 1);
             umma::mbar_init(mbarP, 1);
             umma::mbar_init(mbarConv, 1);
@@ -600,6 +610,9 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     const uint32_t tmem = *tslot;
     const uint32_t tY = tmem, tP = tmem + 128;
     const uint32_t sbase = umma::smem_u32(smem);
+    // shared-memory descriptors of the operand tiles as (low, high) halves, kept in
+    // shared memory (only the issuing thread reads them): [high, TA, TB, PiL, PiH, SH, SL]
+    const uint32_t *sdesc = reinterpret_cast<const uint32_t *>(smem + kOffMisc + 64);
 
     if (warp >= kEpiWarps) {
         // =========================== producers =================================
@@ -743,15 +756,13 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 if (it > 0) ok = umma::mbar_wait_bounded(mbarYfree, (it - 1) & 1, kWaitLimit);
                 if (ok) {
                     umma::fence_after_sync();
-#pragma unroll 1
+                    const uint32_t d_hi = sdesc[0], dTA_lo = sdesc[1], dPiL_lo = sdesc[3], dPiH_lo = sdesc[4];
+#pragma unroll
                     for (int term = 0; term < 2; ++term) {
-                        const uint32_t boff = term == 0 ? kOffPiL : kOffPiH;
-#pragma unroll 1
-                        for (int s = 0; s < D / 16; ++s) {
-                            const uint64_t a = umma::make_desc(sbase + kOffTA + 256 * s, 128, kSBO);
-                            const uint64_t b = umma::make_desc(sbase + boff + 256 * s, 128, kSBO);
-                            umma::mma_f16(tY, a, b, kIdesc, (term | s) != 0);
-                        }
+                        const uint32_t blo = term == 0 ? dPiL_lo : dPiH_lo;
+#pragma unroll
+                        for (int s = 0; s < D / 16; ++s)  // k-step s starts 256 bytes (16 in the >> 4 field) further
+                            umma::mma_f16_lohi(tY, dTA_lo + 16u * s, d_hi, blo + 16u * s, d_hi, kIdesc, (term | s) != 0);
                     }
                     umma::commit(mbarY);
                     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(umma::smem_u32(mbarConv))
@@ -851,16 +862,15 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             if (C.qjl) {
                 if (tid == 0) {
                     // ---- projection MMAs: P = (R_hi + R_lo)(S_hi + S_lo)^T, small terms first ----
-                    const uint32_t aoff[3] = {kOffTB, kOffTA, kOffTA};
-                    const uint32_t boff[3] = {kOffSH, kOffSL, kOffSH};
-#pragma unroll 1
-                    for (int term = 0; term < 3; ++term)
-#pragma unroll 1
-                        for (int s = 0; s < D / 16; ++s) {
-                            const uint64_t a = umma::make_desc(sbase + aoff[term] + 256 * s, 128, kSBO);
-                            const uint64_t b = umma::make_desc(sbase + boff[term] + 256 * s, 128, kSBO);
-                            umma::mma_f16(tP, a, b, kIdesc, (term | s) != 0);
-                        }
+                    const uint32_t d_hi = sdesc[0], dTA_lo = sdesc[1], dTB_lo = sdesc[2], dSH_lo = sdesc[5], dSL_lo = sdesc[6];
+#pragma unroll
+                    for (int term = 0; term < 3; ++term) {
+                        const uint32_t alo = term == 0 ? dTB_lo : dTA_lo;
+                        const uint32_t blo = term == 1 ? dSL_lo : dSH_lo;
+#pragma unroll
+                        for (int s = 0; s < D / 16; ++s)
+                            umma::mma_f16_lohi(tP, alo + 16u * s, d_hi, blo + 16u * s, d_hi, kIdesc, (term | s) != 0);
+                    }
                     umma::commit(mbarP);
                 }
             }

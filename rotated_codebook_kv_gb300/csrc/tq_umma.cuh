@@ -51,6 +51,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
                  ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accum));
 }
 
+// The same MMA with both descriptors given as (low, high) 32-bit halves: a k-step
+// advance only adds to the low half (the start-address field), so an unrolled
+// issue loop needs one add per operand instead of rebuilding the descriptor.
+__device__ __forceinline__ void mma_f16_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
+                                             uint32_t idesc, int accum)
+{
+    asm volatile("{\n.reg .pred p;\n.reg .b64 da, db;\nsetp.ne.b32 p, %5, 0;\nmov.b64 da, {%1, %2};\n"
+                 "mov.b64 db, {%3, %4};\ntcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %6, p;\n}\n"
+                 ::"r"(d_tmem), "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(accum), "r"(idesc));
+}
+
 // Arrive on `mbar` when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void commit(uint64_t *mbar)
 {
