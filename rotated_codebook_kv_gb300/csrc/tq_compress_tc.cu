@@ -472,13 +472,23 @@ __device__ __forceinline__ void quantize_values32(const uint4 (&w4)[4], int lane
     constexpr int L = (1 << VB) - 1;
     const uint32_t wd[16] = {w4[0].x, w4[0].y, w4[0].z, w4[0].w, w4[1].x, w4[1].y, w4[1].z, w4[1].w,
                              w4[2].x, w4[2].y, w4[2].z, w4[2].w, w4[3].x, w4[3].y, w4[3].z, w4[3].w};
-    __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162 *>(&wd[0]), mx2 = mn2;
+    // min / max as a 4-deep tree over the 16 bf16 pairs
+    __nv_bfloat162 tmn[8], tmx[8];
 #pragma unroll
-    for (int k = 1; k < 16; ++k) {
-        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&wd[k]);
-        mn2 = __hmin2(mn2, v);
-        mx2 = __hmax2(mx2, v);
+    for (int k = 0; k < 8; ++k) {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&wd[2 * k]);
+        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162 *>(&wd[2 * k + 1]);
+        tmn[k] = __hmin2(a, c);
+        tmx[k] = __hmax2(a, c);
     }
+#pragma unroll
+    for (int n = 4; n > 0; n >>= 1)
+#pragma unroll
+        for (int k = 0; k < n; ++k) {
+            tmn[k] = __hmin2(tmn[k], tmn[k + n]);
+            tmx[k] = __hmax2(tmx[k], tmx[k + n]);
+        }
+    const __nv_bfloat162 mn2 = tmn[0], mx2 = tmx[0];
     float mn = fminf(__low2float(mn2), __high2float(mn2));
     float mx = fmaxf(__low2float(mx2), __high2float(mx2));
     if (lanes_per_group >= 2) {
@@ -493,12 +503,23 @@ __device__ __forceinline__ void quantize_values32(const uint4 (&w4)[4], int lane
     two_sum(mx, -mn, dh, de);
     // (max - min) / L with L in {3, 7, 15}: exact in fp32 or a non-terminating
     // binary fraction, so one rounding to fp32 then fp16 equals one rounding to fp16.
-    const __half s16 = (de == 0.f) ? __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)))
-                                   : __double2half((static_cast<double>(mx) - static_cast<double>(mn)) / L);
+    // dh (1/L) is within 2 ulps of dh / L; unless it lies within 4 ulps of an fp16
+    // rounding midpoint (its low 13 mantissa bits near 0x1000) or below the fp16
+    // normal range, both round to the same fp16 value.
+    const float qm = dh * (1.f / static_cast<float>(L));
+    const uint32_t qlow = __float_as_uint(qm) & 0x1FFFu;
+    const bool qsafe = de == 0.f && qm >= 6.103515625e-05f && (qlow + 4u - 0x1000u) > 8u;
+    __half s16;
+    if (qsafe) s16 = __float2half_rn(qm);
+    else if (de == 0.f) s16 = __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)));
+    else s16 = __double2half((static_cast<double>(mx) - static_cast<double>(mn)) / L);
     const __half z16 = __float2half_rn(mn);
     meta = static_cast<uint32_t>(__half_as_ushort(s16)) | (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
     const float sv = __half2float(s16), zv = __half2float(z16);
-    const float inv = (sv != 0.f) ? __frcp_rn(sv) : 0.f;
+    // the reciprocal only feeds the fast estimate: its error (~2^-23) is far inside
+    // the 4-ulp (2^-14) window that sends a code to the exact comparison
+    float inv = 0.f;
+    if (sv != 0.f) asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sv));
 #pragma unroll
     for (int k = 0; k < VB; ++k) cw[k] = 0u;
 #pragma unroll
