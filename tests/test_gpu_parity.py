@@ -219,6 +219,30 @@ def test_decode_empty_and_single_token():
     assert np.array_equal(out[1], O.bf16_to_double(O.bf16_from_double(ref)))
 
 
+@pytest.mark.parametrize("name", ["mixed_k3v2_small", "mixed_k4v4_small"])
+def test_strided_token_rows(name):
+    """K and V whose token stride exceeds heads x head_dim (views into wider
+    buffers, as in fused QKV projections) give the same records as contiguous ones."""
+    w = SMALL[name]
+    b = W.generate(w, device="cpu")
+    T, H, d = b.k.shape
+    kw = torch.zeros(T, H + 3, d, dtype=torch.bfloat16)
+    vw = torch.zeros(T, H + 1, d, dtype=torch.bfloat16)
+    kw[:, 1:H + 1] = b.k
+    vw[:, :H] = b.v
+    b = W.Batch(**{f: (getattr(b, f).to(DEV) if isinstance(getattr(b, f), torch.Tensor) else getattr(b, f))
+                   for f in b.__dataclass_fields__})
+    ks, vs = kw.to(DEV)[:, 1:H + 1], vw.to(DEV)[:, :H]
+    assert ks.stride(0) == (H + 3) * d and vs.stride(0) == (H + 1) * d
+    codec, _ = _codec_pair(w)
+    kc_ref, vc_ref = _compress(codec, w, b)
+    kc, vc = codec.alloc_cache(b.num_blocks, w.num_kv_heads, w.page_size, fill=0xA5)
+    codec.compress_kv(ks, vs, b.slot_mapping, kc, vc, w.page_size, b.num_blocks)
+    torch.cuda.synchronize()
+    assert codec.get_status() == 0
+    assert torch.equal(kc, kc_ref) and torch.equal(vc, vc_ref)
+
+
 def test_bad_ids_set_status_and_write_nothing_out_of_bounds():
     w = SMALL["paged_decode_small"]
     b = W.generate(w, device=DEV)
