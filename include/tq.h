@@ -131,7 +131,9 @@ tq_status tq_dequant_kv(tq_handle h, const uint8_t *k_cache, const uint8_t *v_ca
 /*
  * tq_decode_splits -- the split count tq_decode_attention uses when called
  * with splits = 0: about eight (sequence, kv head, split) work units per SM,
- * at least one page per split, at most 64 splits.
+ * raised to fill whole waves of resident decode CTAs (4 per SM at d = 128, 2 at
+ * d = 256) when the last wave would be less than half full, at least one page
+ * per split, at most 64 splits.  Reads no device memory.
  */
 int tq_decode_splits(tq_handle h, int batch, int num_kv_heads, int max_blocks_per_seq, int page_size);
 

@@ -244,6 +244,13 @@ int tq_decode_splits(tq_handle h, int batch, int num_kv_heads, int max_blocks_pe
     if (!h || batch < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 || page_size < 1) return 1;
     const int units = batch * num_kv_heads;
     int splits = (8 * h->num_sms + units - 1) / units;  // about eight CTAs per SM
+    // resident decode CTAs per SM: 4 at d = 128, 2 at d = 256 (registers).  A last
+    // wave less than half full mostly idles the GPU: round up to whole waves.
+    const int slots = h->num_sms * (h->codec.d == 128 ? 4 : 2);
+    const long long ctas = static_cast<long long>(units) * splits;
+    const long long waves = (ctas + slots - 1) / slots;
+    if (ctas % slots != 0 && 2 * (ctas - (waves - 1) * slots) < slots)
+        splits = static_cast<int>((waves * slots + units - 1) / units);
     if (splits > 64) splits = 64;
     if (splits > max_blocks_per_seq) splits = max_blocks_per_seq;
     return splits < 1 ? 1 : splits;

@@ -1,8 +1,8 @@
 // tq_decode_mma.cuh -- split-K paged decode on the tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate).
 //
-// One CTA = (split, kv head, sequence); 4 warps, each owns 16-token tiles of
-// every 128-token chunk (tokens 16 (warp + 4 i)), with its own online softmax;
-// the warps merge at the end.
+// One CTA = (split, kv head, sequence); 4 warps.  Warp w takes the 32-token
+// rounds w, w + 4, w + 8, ... of the split (two 16-token tiles each), fetches
+// their pages itself and keeps its own online softmax; the warps merge at the end.
 //
 // Scores: S[t][h] = sum_j Khat[t][j] q[h][j] with tokens as the M dimension and
 // the G <= 8 query heads as N.  Coordinates are permuted inside every 16-wide

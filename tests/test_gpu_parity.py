@@ -219,6 +219,20 @@ def test_decode_empty_and_single_token():
     assert np.array_equal(out[1], O.bf16_to_double(O.bf16_from_double(ref)))
 
 
+@pytest.mark.parametrize("P", [16, 32])
+def test_decode_round_remainders(P):
+    """Each warp of a decode CTA fetches 32-token rounds w, w + 4, ... of its
+    split: lengths and split counts chosen so that splits end inside a round,
+    inside a page, and after fewer rounds than warps."""
+    lens = [12 * P + 1, 5 * P, 31, 33, 9 * P - 1, 2 * P + 7, 3 * P]
+    w, b = _small_case(lens, W.scaled(SMALL["paged_decode_small"], page_size=P))
+    codec, ora = _codec_pair(w)
+    kc, vc = _compress(codec, w, b)
+    ref = _decode_oracle(ora, w, b, kc.cpu().numpy(), vc.cpu().numpy())
+    for s in (1, 3, 5):
+        check_decode(_decode_gpu(codec, w, b, kc, vc, splits=s), ref)
+
+
 @pytest.mark.parametrize("name", ["mixed_k3v2_small", "mixed_k4v4_small"])
 def test_strided_token_rows(name):
     """K and V whose token stride exceeds heads x head_dim (views into wider
