@@ -58,14 +58,14 @@ constexpr long long kWaitLimit = 2000000000LL;  // cycles (~1 s)
 
 // Shared-memory map (bytes).
 constexpr uint32_t kOffPiH = 0, kOffPiL = 32768, kOffSH = 65536, kOffSL = 98304;  // B operands (fp16)
-constexpr uint32_t kOffTA = 131072;  // K' (fp16) then R hi
-constexpr uint32_t kOffTB = 163840;  // R lo, then scratch of the exact path
+constexpr uint32_t kOffTA = 131072;  // K' (fp16), the A operand of the rotation MMA
+constexpr uint32_t kOffTB = 163840;  // scratch of the exact path
 constexpr uint32_t kOffCodes = 196608;               // [TM][16] u32 packed key codes
 constexpr uint32_t kOffSigns = kOffCodes + TM * 64;  // [TM][4] u32 sign bits
 constexpr uint32_t kOffMask = kOffSigns + TM * 16;   // [TM][8] u32: code guard mask (4), sign guard mask (4)
 constexpr uint32_t kOffRow = kOffMask + TM * 32;     // [3][TM] RowInfo (tile index mod 3)
 constexpr uint32_t kOffPart = kOffRow + 3 * TM * 32; // [TM][2] gsq partials, [TM][2] code flags, [TM][2] sign flags
-constexpr uint32_t kOffBins = kOffPart + TM * 24;    // [256] float4 code bins (below)
+constexpr uint32_t kOffBins = kOffPart + TM * 24;    // [64 bins][4 copies] float4 code bins (below)
 constexpr int kMaxDefer = 24;                        // rows awaiting exact re-decision
 constexpr uint32_t kOffDefer = kOffBins + 256 * 16;  // [kMaxDefer] Deferred
 constexpr uint32_t kOffMisc = kOffDefer + kMaxDefer * 64;  // mbarriers, TMEM slot, abort flags
@@ -75,14 +75,22 @@ static_assert(kSmemBytes <= 232448, "shared memory map exceeds the per-block lim
 constexpr uint32_t kSBO = (D / 8) * 128;  // 2048
 constexpr uint32_t kIdesc = umma::idesc_f16(128, 128);
 
-// Code bins.  The epilogue works on z' = 2^12 z.  Bin b holds the z with
-// round(8 z + 96) = b, i.e. z in [(b - 96.5) / 8, (b - 95.5) / 8]; |z| <= sqrt(d)
-// = 11.4 keeps b in [5, 187].  Adding z' / 512 + 96 to 1.5 * 2^23 in one fused
-// multiply-add rounds to that integer and leaves it in the low mantissa bits.
-// Lloyd-Max thresholds for N(0,1) are at least 0.25 apart for b_k <= 4, so a
-// bin holds at most one threshold.  Entry: {threshold (or +inf), centroid below
-// it, centroid above it, code below it (as raw bits)}, all but the code times 2^12.
-constexpr float kBinMagic = 12582912.f + 96.f;
+// Code bins.  The epilogue works on z' = 2^12 z.  u = sat(z / 8 + 1/2) clamps z
+// to [-4, 4] (every Lloyd-Max threshold for N(0,1) with b_k <= 4 lies inside
+// +-2.5); bin b holds the u with floor(round(4032 u) / 64) = b, i.e. z in about
+// [b / 7.875 - 4, (b + 1) / 7.875 - 4].  Adding 4032 u to 1.5 * 2^23 rounds to
+// that integer and leaves it in the low mantissa bits, so bits 6..11 are 64 b,
+// the byte offset of the bin.  Thresholds are at least 0.25 apart, so a bin
+// (0.127 wide plus margins) holds at most one.  Each bin is stored in 4 copies
+// side by side, lane l reading copy l % 4: of the 8 lanes that share a 128-byte
+// shared-memory wavefront only lanes l and l + 4 can meet in a bank.
+// Entry: {threshold (or +inf), centroid below it, centroid above minus below
+// (0 without a threshold), 2^23 + code below it}, centroids and threshold times 2^12.
+constexpr float kBinU = 1.f / 32768.f;    // z' / 2^15 = z / 8
+constexpr float kBinScale = 4032.f;       // 63 * 64
+constexpr float kRoundMagic = 12582912.f; // 1.5 * 2^23: adding it rounds to an integer
+constexpr uint32_t kRoundBits = 0x4B400000u;
+constexpr uint32_t kCode23Bits = 0x4B000000u;  // bits of 2^23
 
 // A row whose decisions are re-taken exactly after its record was written with
 // the fast-path results.
@@ -350,56 +358,63 @@ __device__ __noinline__ void fix_row(const Codec &C, const PageGeom &G, const ui
 }
 
 // Epilogue 1 for one (row, 32-column block cb): codes, guard mask, residual
-// split into fp16 hi / lo operands (QJL only), and the block's sum of squares of
-// the residual.  32 columns are exactly KB code words.
+// split into fp16 hi / lo (QJL only) stored to tensor memory as the A operand
+// of the projection (hi at tR, lo at tR + 64; the caller waits for the stores),
+// and the block's sum of squares of the residual.  32 columns are exactly KB
+// code words.
 template <int KB>
-__device__ __forceinline__ float epilogue_rotation_block(unsigned char *smem, uint32_t tY, int warp, int row, int cb,
-                                                         float zs, bool qjl, const float4 *bins, uint32_t *scodes,
+__device__ __forceinline__ float epilogue_rotation_block(unsigned char *smem, uint32_t tY, uint32_t tR, int warp, int row,
+                                                         int cb, float zs, bool qjl, uint32_t *scodes,
                                                          uint32_t *smask)
 {
     float y[32];
     umma::ld32(tY + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 32 * cb, y);
-    const float zs512 = zs * (1.f / 512.f);
-    uint32_t cw[KB];
+    const float zsu = zs * kBinU;
+    const unsigned char *binb = smem + kOffBins + ((row & 3) << 4);  // this lane's copy
+    // codes are summed as 2^23 + code shifted into place; the constant parts
+    // (known at compile time) are subtracted at the end
+    uint32_t cw[KB], bias[KB];
 #pragma unroll
-    for (int w = 0; w < KB; ++w) cw[w] = 0u;
+    for (int w = 0; w < KB; ++w) cw[w] = bias[w] = 0u;
     uint32_t cmask = 0u;
     float gsq = 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         // z' = y zs is folded into each fused multiply-add
-        const uint32_t bi = __float_as_uint(fmaf(y[i], zs512, kBinMagic)) & 0xFFu;
-        const float4 e = bins[bi];
+        const float u = __saturatef(fmaf(y[i], zsu, 0.5f));
+        const uint32_t a = __float_as_uint(fmaf(u, kBinScale, kRoundMagic)) & 0xFC0u;
+        const float4 e = *reinterpret_cast<const float4 *>(binb + a);
         const float dz = fmaf(y[i], zs, -e.x);
-        const bool up = dz >= 0.f;
+        // 1 above the bin's threshold, 0 below it or without one; a dz of zero or
+        // below the normal range counts as below (it is inside the guard band)
+        float up;
+        asm("mul.rn.ftz.sat.f32 %0, %1, 0f7E800000;" : "=f"(up) : "f"(dz));  // dz * 2^126
         if (fabsf(dz) < kCodeGuard * 4096.f) cmask |= 1u << i;
-        const uint32_t code = __float_as_uint(e.w) + (up ? 1u : 0u);
-        const float r = fmaf(y[i], zs, -(up ? e.z : e.y));
+        const float r = fmaf(y[i], zs, -fmaf(up, e.z, e.y));
         gsq = fmaf(r, r, gsq);
+        const uint32_t cb23 = __float_as_uint(e.w + up);  // 2^23 + code
         const int o = i * KB;  // compile-time bit offset inside the block
-        cw[o >> 5] |= code << (o & 31);
-        if ((o & 31) + KB > 32) cw[(o >> 5) + 1] |= code >> (32 - (o & 31));
+        cw[o >> 5] += cb23 << (o & 31);
+        bias[o >> 5] += kCode23Bits << (o & 31);
+        if ((o & 31) + KB > 32) cw[(o >> 5) + 1] += (cb23 - kCode23Bits) >> (32 - (o & 31));
         y[i] = r;
     }
 #pragma unroll
-    for (int w = 0; w < KB; ++w) scodes[row * 16 + KB * cb + w] = cw[w];
+    for (int w = 0; w < KB; ++w) scodes[row * 16 + KB * cb + w] = cw[w] - bias[w];
     smask[row * 8 + cb] = cmask;
-    if (qjl) {  // without QJL the key tile buffer already holds the next tile
+    if (qjl) {
+        uint32_t rh[16], rlo[16];
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-            uint32_t rh[4], rlo[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float a = y[8 * c8 + 2 * q], b = y[8 * c8 + 2 * q + 1];
-                const __half2 hh = __floats2half2_rn(a, b);
-                const float2 hf = __half22float2(hh);
-                rh[q] = *reinterpret_cast<const uint32_t *>(&hh);
-                rlo[q] = pack_h2(a - hf.x, b - hf.y);
-            }
-            const uint32_t off = umma::core_offset(row, 32 * cb + 8 * c8, D);
-            *reinterpret_cast<uint4 *>(smem + kOffTA + off) = make_uint4(rh[0], rh[1], rh[2], rh[3]);
-            *reinterpret_cast<uint4 *>(smem + kOffTB + off) = make_uint4(rlo[0], rlo[1], rlo[2], rlo[3]);
+        for (int q = 0; q < 16; ++q) {
+            const float a = y[2 * q], b = y[2 * q + 1];
+            const __half2 hh = __floats2half2_rn(a, b);
+            const float2 hf = __half22float2(hh);
+            rh[q] = *reinterpret_cast<const uint32_t *>(&hh);
+            rlo[q] = pack_h2(a - hf.x, b - hf.y);
         }
+        const uint32_t ta = tR + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 16 * cb;
+        umma::st16(ta, rh);
+        umma::st16(ta + 64, rlo);
     }
     return gsq;
 }
@@ -458,13 +473,14 @@ __device__ __noinline__ void values32_exact(const uint32_t *wd, float zv, float 
 // group's fp16 scale and zero and the lane's 32 codes packed LSB-first into VB
 // words: code = clamp(floor((x - zero) / scale + 0.5), 0, 2^VB - 1).
 //
-// f = (x - zero) / scale + 0.5 + 192 in one fused multiply-add leaves
-// floor(.) in bits 16.. and the fraction in the low 16 bits of f (the ulp of
-// [128, 256) is 2^-16).  An element whose fraction lies within 4 ulps of an
-// integer n is re-decided exactly: x - zero as an exact float pair against
-// (n - 1/2) scale, which is exact in fp32.  A lane whose zero is not its min
-// exactly (values outside the fp16 normal range) or whose scale is subnormal
-// re-decides every code that way, with clamping.
+// Two fused multiply-adds per element: (x - zero) / scale + 1.5 * 2^23 rounds
+// to the code in the low mantissa bits, and (x - zero) / scale + 192.5 + 2^-14
+// (ulp 2^-16 in [128, 256)) has its low 16 bits below 8 exactly when the
+// quotient lies within 4 ulps of a boundary n - 1/2 between codes n - 1 and n.
+// Such an element is re-decided exactly: x - zero as an exact float pair
+// against (n - 1/2) scale, which is exact in fp32.  A lane whose zero is not its
+// min exactly (values outside the fp16 normal range) or whose scale is
+// subnormal re-decides every code that way, with clamping.
 template <int VB>
 __device__ __forceinline__ void quantize_values32(const uint4 (&w4)[4], int lanes_per_group, uint32_t (&cw)[VB],
                                                   uint32_t &meta)
@@ -520,27 +536,36 @@ __device__ __forceinline__ void quantize_values32(const uint4 (&w4)[4], int lane
     // the 4-ulp (2^-14) window that sends a code to the exact comparison
     float inv = 0.f;
     if (sv != 0.f) asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sv));
+    // codes are summed as 1.5 * 2^23 + code shifted into place; the constant
+    // parts (known at compile time) are subtracted at the end
+    uint32_t bias[VB];
 #pragma unroll
-    for (int k = 0; k < VB; ++k) cw[k] = 0u;
+    for (int k = 0; k < VB; ++k) cw[k] = bias[k] = 0u;
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
         const uint32_t wv = wd[e >> 1];
         const float x = (e & 1) ? __uint_as_float(wv & 0xffff0000u) : __uint_as_float(wv << 16);
-        const uint32_t fb = __float_as_uint(fmaf(x - zv, inv, 192.5f));
-        uint32_t code = (fb >> 16) & static_cast<uint32_t>(L);
-        if (((fb + 4u) & 0xFFF8u) == 0u) {
-            // within 4 ulps of the boundary (n - 1/2) scale between codes n - 1 and n:
-            // compare x - zero (an exact pair) with it exactly
-            const uint32_t n = ((fb + 0x8000u) >> 16) & 0x1Fu;
+        const float dx = x - zv;
+        // (x - zero) / scale rounded to the nearest integer: the code, except at a tie
+        uint32_t cb = __float_as_uint(fmaf(dx, inv, kRoundMagic));
+        // the same plus 1/2 + 4 ulps, in [192, 256) where the ulp is 2^-16: its low
+        // 16 bits are below 8 within 4 ulps of a boundary (n - 1/2) scale
+        const uint32_t tb = __float_as_uint(fmaf(dx, inv, 192.5f + 4.f / 65536.f));
+        if ((tb & 0xFFF8u) == 0u) {
+            // compare x - zero (an exact pair) with the boundary exactly
+            const uint32_t n = (tb >> 16) & 0x1Fu;
             const float m = fmaf(static_cast<float>(n), sv, -0.5f * sv);
             float a, ea;
             two_sum(x, -zv, a, ea);
-            code = (__fadd_rn(__fsub_rn(a, m), ea) >= 0.f) ? n : n - 1u;
+            cb = kRoundBits + ((__fadd_rn(__fsub_rn(a, m), ea) >= 0.f) ? n : n - 1u);
         }
         const int o = e * VB;
-        cw[o >> 5] |= code << (o & 31);
-        if ((o & 31) + VB > 32) cw[(o >> 5) + 1] |= code >> (32 - (o & 31));
+        cw[o >> 5] += cb << (o & 31);
+        bias[o >> 5] += kRoundBits << (o & 31);
+        if ((o & 31) + VB > 32) cw[(o >> 5) + 1] += (cb - kRoundBits) >> (32 - (o & 31));
     }
+#pragma unroll
+    for (int k = 0; k < VB; ++k) cw[k] -= bias[k];
     if (zv != mn || (sv != 0.f && sv < 6.103515625e-05f)) {
         uint32_t wl[16], cl[VB];  // local copies: the rare exact path keeps the hot one in registers
 #pragma unroll
@@ -587,9 +612,10 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
         const uint4 *img = reinterpret_cast<const uint4 *>(C.tc_image);
         uint4 *dst = reinterpret_cast<uint4 *>(smem);
         for (int e = tid; e < 131072 / 16; e += kThreads) dst[e] = __ldg(img + e);
-        if (tid < 256) {
-            const float lo = (static_cast<float>(tid) - 96.5f) * 0.125f - 1.f / 64.f;
-            const float hi = (static_cast<float>(tid) - 95.5f) * 0.125f + 1.f / 64.f;
+        if (tid < 256) {  // bin tid / 4, copy tid % 4
+            const float b = static_cast<float>(tid >> 2);
+            const float lo = 8.f * (64.f * b - 0.5f) / kBinScale - 4.f - 1.f / 64.f;
+            const float hi = 8.f * (64.f * b + 63.5f) / kBinScale - 4.f + 1.f / 64.f;
             int below = 0, idx = -1;
             for (int t = 0; t < nthr; ++t) {
                 const float th = C.thresholds[t];
@@ -599,8 +625,8 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             float4 e;
             e.x = idx >= 0 ? C.thresholds[idx] * 4096.f : __int_as_float(0x7f800000);
             e.y = C.centroids[below] * 4096.f;
-            e.z = C.centroids[idx >= 0 ? below + 1 : below] * 4096.f;
-            e.w = __uint_as_float(static_cast<uint32_t>(below));
+            e.z = idx >= 0 ? C.centroids[below + 1] * 4096.f - e.y : 0.f;
+            e.w = __uint_as_float(kCode23Bits + static_cast<uint32_t>(below));
             bins[tid] = e;
         }
         if (tid == 0) {
@@ -622,14 +648,15 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             *e_abort = 0;
             *p_abort = 0;
         }
-        if (warp == 0) umma::tmem_alloc(tslot, 256);
+        if (warp == 0) umma::tmem_alloc(tslot, 512);
         umma::fence_proxy_async();
         umma::fence_before_sync();
         __syncthreads();
         umma::fence_after_sync();
     }
     const uint32_t tmem = *tslot;
-    const uint32_t tY = tmem, tP = tmem + 128;
+    // columns: Y [0, 128), P [128, 256), R hi [256, 320), R lo [320, 384)
+    const uint32_t tY = tmem, tP = tmem + 128, tR = tmem + 256;
     const uint32_t sbase = umma::smem_u32(smem);
     // shared-memory descriptors of the operand tiles as (low, high) halves, kept in
     // shared memory (only the issuing thread reads them): [high, TA, TB, PiL, PiH, SH, SL]
@@ -691,9 +718,9 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                     }
                 }
             }
-            // the key tile buffer is free once the previous tile's last MMA finished
+            // the key tile buffer is free once the previous tile's rotation MMA finished
             if (it > 0 && ptid == 0) {
-                if (!umma::mbar_wait_bounded(C.qjl ? mbarP : mbarY, (it - 1) & 1, kWaitLimit)) {
+                if (!umma::mbar_wait_bounded(mbarY, (it - 1) & 1, kWaitLimit)) {
                     atomicOr(C.status, TQ_DEVERR_TIMEOUT);
                     *p_abort = 1;
                 }
@@ -867,13 +894,13 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 const float zs = ri.zscale * 4096.f;  // z' = 2^12 z
 #pragma unroll 1
                 for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb)
-                    gsq += epilogue_rotation_block<KB>(smem, tY, warp, row, cb, zs, C.qjl != 0, bins, scodes, smask);
+                    gsq += epilogue_rotation_block<KB>(smem, tY, tR, warp, row, cb, zs, C.qjl != 0, scodes, smask);
                 gsq *= 1.f / 16777216.f;  // back to z units
                 fl = (smask[row * 8 + 2 * hf] | smask[row * 8 + 2 * hf + 1]) ? 1 : 0;
             }
             s_gsq[row * 2 + hf] = gsq;
             s_flagp[row * 2 + hf] = fl;
-            umma::fence_proxy_async();
+            if (C.qjl) umma::wait_st();  // the residual operand is in tensor memory
             umma::fence_before_sync();
             asm volatile("bar.sync 1, 256;" ::: "memory");
             umma::fence_after_sync();
@@ -882,15 +909,16 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             uint32_t n16g16 = ri.n16g16;
             if (C.qjl) {
                 if (tid == 0) {
-                    // ---- projection MMAs: P = (R_hi + R_lo)(S_hi + S_lo)^T, small terms first ----
-                    const uint32_t d_hi = sdesc[0], dTA_lo = sdesc[1], dTB_lo = sdesc[2], dSH_lo = sdesc[5], dSL_lo = sdesc[6];
+                    // ---- projection MMAs: P = (R_hi + R_lo)(S_hi + S_lo)^T, small terms first;
+                    // R from tensor memory, so the key tile buffer is already the next tile's ----
+                    const uint32_t d_hi = sdesc[0], dSH_lo = sdesc[5], dSL_lo = sdesc[6];
 #pragma unroll
                     for (int term = 0; term < 3; ++term) {
-                        const uint32_t alo = term == 0 ? dTB_lo : dTA_lo;
+                        const uint32_t ta = term == 0 ? tR + 64 : tR;
                         const uint32_t blo = term == 1 ? dSL_lo : dSH_lo;
 #pragma unroll
                         for (int s = 0; s < D / 16; ++s)
-                            umma::mma_f16_lohi(tP, alo + 16u * s, d_hi, blo + 16u * s, d_hi, kIdesc, (term | s) != 0);
+                            umma::mma_f16_tmem_a(tP, ta + 8u * s, blo + 16u * s, d_hi, kIdesc, (term | s) != 0);
                     }
                     umma::commit(mbarP);
                 }
@@ -1007,7 +1035,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
-    if (warp == 0) umma::tmem_dealloc(tmem, 256);
+    if (warp == 0) umma::tmem_dealloc(tmem, 512);
 }
 
 template <int KB, int VB>

@@ -62,6 +62,17 @@ __device__ __forceinline__ void mma_f16_lohi(uint32_t d_tmem, uint32_t a_lo, uin
                  ::"r"(d_tmem), "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(accum), "r"(idesc));
 }
 
+// The same MMA with A read from tensor memory: row m of A in lane m, elements
+// 2c and 2c + 1 of a row packed (low, high) in column c; a k-step of 16 elements
+// advances a_tmem by 8 columns.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                               uint32_t idesc, int accum)
+{
+    asm volatile("{\n.reg .pred p;\n.reg .b64 db;\nsetp.ne.b32 p, %4, 0;\nmov.b64 db, {%2, %3};\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %5, p;\n}\n"
+                 ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(accum), "r"(idesc));
+}
+
 // Arrive on `mbar` when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void commit(uint64_t *mbar)
 {
@@ -139,6 +150,18 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16])
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane from registers; the
+// caller waits with wait_st() before the data is used by another thread or the MMA.
+__device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                   "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 }  // namespace umma
 }  // namespace tq
