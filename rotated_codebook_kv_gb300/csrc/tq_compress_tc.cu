@@ -59,16 +59,17 @@ constexpr long long kWaitLimit = 2000000000LL;  // cycles (~1 s)
 // Shared-memory map (bytes).
 constexpr uint32_t kOffPiH = 0, kOffPiL = 32768, kOffSH = 65536, kOffSL = 98304;  // B operands (fp16)
 constexpr uint32_t kOffTA = 131072;  // K' (fp16), the A operand of the rotation MMA
-constexpr uint32_t kOffTB = 163840;  // scratch of the exact path
+constexpr uint32_t kOffTB = 163840;  // exact path: [16 warps][d] double scratch, then the deferred-row list
 constexpr uint32_t kOffCodes = 196608;               // [TM][16] u32 packed key codes
 constexpr uint32_t kOffSigns = kOffCodes + TM * 64;  // [TM][4] u32 sign bits
 constexpr uint32_t kOffMask = kOffSigns + TM * 16;   // [TM][8] u32: code guard mask (4), sign guard mask (4)
 constexpr uint32_t kOffRow = kOffMask + TM * 32;     // [3][TM] RowInfo (tile index mod 3)
 constexpr uint32_t kOffPart = kOffRow + 3 * TM * 32; // [TM][2] gsq partials, [TM][2] code flags, [TM][2] sign flags
 constexpr uint32_t kOffBins = kOffPart + TM * 24;    // [64 bins][4 copies] float4 code bins (below)
-constexpr int kMaxDefer = 24;                        // rows awaiting exact re-decision
-constexpr uint32_t kOffDefer = kOffBins + 256 * 16;  // [kMaxDefer] Deferred
-constexpr uint32_t kOffMisc = kOffDefer + kMaxDefer * 64;  // mbarriers, TMEM slot, abort flags
+constexpr int kMaxDefer = 256;                       // rows awaiting exact re-decision
+constexpr uint32_t kOffDefer = kOffTB + 16 * D * 8;  // [kMaxDefer] Deferred
+static_assert(kOffDefer + kMaxDefer * 64 <= kOffCodes, "deferred-row list overlaps the code words");
+constexpr uint32_t kOffMisc = kOffBins + 256 * 16;   // mbarriers, TMEM slot, abort flags
 constexpr uint32_t kSmemBytes = kOffMisc + 128;  // + 7 descriptor words at kOffMisc + 64
 static_assert(kSmemBytes <= 232448, "shared memory map exceeds the per-block limit");
 
@@ -599,6 +600,8 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc + 32);
     volatile int *e_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 36);
     volatile int *p_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 40);
+    int *s_ndefer = reinterpret_cast<int *>(smem + kOffMisc + 96);  // rows left on the deferred list
+    int *s_next = reinterpret_cast<int *>(smem + kOffMisc + 100);   // next list entry to fix
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float sqrtd = sqrtf(static_cast<float>(D));
@@ -866,6 +869,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
         Deferred *defer = reinterpret_cast<Deferred *>(smem + kOffDefer);
         int *s_qcount = reinterpret_cast<int *>(smem + kOffMisc + 44);  // [4] flagged rows per lane quarter
         int ndefer = 0;  // same value in every epilogue thread
+        // a full list is drained by the epilogue warps alone; the rest waits for the end
         auto drain = [&](int n) {  // all epilogue threads; warp w fixes entries w, w + 8, ...
             asm volatile("bar.sync 1, 256;" ::: "memory");
             double *scr = reinterpret_cast<double *>(smem + kOffTB) + warp * D;
@@ -1023,7 +1027,35 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
         }
-        if (ndefer > 0 && !*e_abort) drain(ndefer);
+        if (tid == 0) *s_ndefer = ndefer;
+    }
+    // ---- rows still awaiting exact re-decisions: every warp takes the next one in
+    // turn, the ones that redo the whole row first (they take longest) ----
+    __syncthreads();
+    {
+        const int nd = *s_ndefer;
+        if (nd > 0 && !*e_abort && !*p_abort) {
+            const Deferred *defer = reinterpret_cast<const Deferred *>(smem + kOffDefer);
+            uint8_t *order = smem + kOffBins;  // the code bins are no longer needed
+            if (tid == 0) {
+                int h = 0;
+                for (int e = 0; e < nd; ++e)
+                    if (defer[e].flag & 20) order[h++] = static_cast<uint8_t>(e);
+                for (int e = 0; e < nd; ++e)
+                    if (!(defer[e].flag & 20)) order[h++] = static_cast<uint8_t>(e);
+                *s_next = 0;
+            }
+            __syncthreads();
+            double *scr = reinterpret_cast<double *>(smem + kOffTB) + warp * D;
+            for (;;) {
+                int e = 0;
+                if (lane == 0) e = atomicAdd(s_next, 1);
+                e = __shfl_sync(0xffffffffu, e, 0);
+                if (e >= nd) break;
+                fix_row<KB>(C, G, kin, ks, Hkv, kc, defer[order[e]], scodes + warp * 16, ssigns + warp * 4,
+                            reinterpret_cast<uint32_t *>(s_gsq) + warp, scr);
+            }
+        }
     }
     // ---- teardown: no MMA may still run when TMEM is freed ----
     __syncthreads();
