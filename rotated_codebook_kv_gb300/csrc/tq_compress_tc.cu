@@ -60,9 +60,10 @@ constexpr long long kWaitLimit = 2000000000LL;  // cycles (~1 s)
 constexpr uint32_t kOffPiH = 0, kOffPiL = 32768, kOffSH = 65536, kOffSL = 98304;  // B operands (fp16)
 constexpr uint32_t kOffTA = 131072;  // K' (fp16), the A operand of the rotation MMA
 constexpr uint32_t kOffTB = 163840;  // exact path: [16 warps][d] double scratch, then the deferred-row list
-constexpr uint32_t kOffCodes = 196608;               // [TM][16] u32 packed key codes
-constexpr uint32_t kOffSigns = kOffCodes + TM * 64;  // [TM][4] u32 sign bits
-constexpr uint32_t kOffMask = kOffSigns + TM * 16;   // [TM][8] u32: code guard mask (4), sign guard mask (4)
+// Per-row arrays are stored [item][row], so that the 32 rows of a warp use 32 banks.
+constexpr uint32_t kOffCodes = 196608;               // [16][TM] u32 packed key codes
+constexpr uint32_t kOffSigns = kOffCodes + TM * 64;  // [4][TM] u32 sign bits
+constexpr uint32_t kOffMask = kOffSigns + TM * 16;   // [8][TM] u32: code guard mask (4), sign guard mask (4)
 constexpr uint32_t kOffRow = kOffMask + TM * 32;     // [3][TM] RowInfo (tile index mod 3)
 constexpr uint32_t kOffPart = kOffRow + 3 * TM * 32; // [TM][2] gsq partials, [TM][2] code flags, [TM][2] sign flags
 constexpr uint32_t kOffBins = kOffPart + TM * 24;    // [64 bins][4 copies] float4 code bins (below)
@@ -401,8 +402,8 @@ __device__ __forceinline__ float epilogue_rotation_block(unsigned char *smem, ui
         y[i] = r;
     }
 #pragma unroll
-    for (int w = 0; w < KB; ++w) scodes[row * 16 + KB * cb + w] = cw[w] - bias[w];
-    smask[row * 8 + cb] = cmask;
+    for (int w = 0; w < KB; ++w) scodes[(KB * cb + w) * TM + row] = cw[w] - bias[w];
+    smask[cb * TM + row] = cmask;
     if (qjl) {
         uint32_t rh[16], rlo[16];
 #pragma unroll
@@ -439,8 +440,8 @@ __device__ __forceinline__ int epilogue_signs(uint32_t tP, int warp, int row, in
             }
         }
         if (zero) bits = near = 0u;
-        ssigns[row * 4 + 2 * hf + cb] = bits;
-        smask[row * 8 + 4 + 2 * hf + cb] = near;
+        ssigns[(2 * hf + cb) * TM + row] = bits;
+        smask[(4 + 2 * hf + cb) * TM + row] = near;
         flag |= near ? 2 : 0;
     }
     return flag;
@@ -589,9 +590,9 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     uint32_t *ssigns = reinterpret_cast<uint32_t *>(smem + kOffSigns);
     uint32_t *smask = reinterpret_cast<uint32_t *>(smem + kOffMask);
     RowInfo *rinfo_all = reinterpret_cast<RowInfo *>(smem + kOffRow);
-    float *s_gsq = reinterpret_cast<float *>(smem + kOffPart);                 // [TM][2]
-    int *s_flagp = reinterpret_cast<int *>(smem + kOffPart + TM * 8);          // [TM][2]
-    int *s_flags = reinterpret_cast<int *>(smem + kOffPart + TM * 16);         // [TM][2]
+    float *s_gsq = reinterpret_cast<float *>(smem + kOffPart);                 // [2][TM]
+    int *s_flagp = reinterpret_cast<int *>(smem + kOffPart + TM * 8);          // [2][TM]
+    int *s_flags = reinterpret_cast<int *>(smem + kOffPart + TM * 16);         // [2][TM]
     float4 *bins = reinterpret_cast<float4 *>(smem + kOffBins);
     uint64_t *mbarY = reinterpret_cast<uint64_t *>(smem + kOffMisc);      // rotation MMA done
     uint64_t *mbarP = mbarY + 1;                                           // projection MMA done
@@ -687,7 +688,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 }
             }
             // ---- issue the tile's key loads (and the first value rows) before waiting:
-            // pass p covers rows 32 pw + 8 p + lane / 4; lane & 3 = sub takes key
+            // pass p covers rows 16 pw + 8 p + lane / 4; lane & 3 = sub takes key
             // chunks sub + 4 j and value channels [32 sub, 32 sub + 32) ----
             const int sub = lane & 3;
             uint4 kr[kPasses][4], va[4];
@@ -900,16 +901,16 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb)
                     gsq += epilogue_rotation_block<KB>(smem, tY, tR, warp, row, cb, zs, C.qjl != 0, scodes, smask);
                 gsq *= 1.f / 16777216.f;  // back to z units
-                fl = (smask[row * 8 + 2 * hf] | smask[row * 8 + 2 * hf + 1]) ? 1 : 0;
+                fl = (smask[(2 * hf) * TM + row] | smask[(2 * hf + 1) * TM + row]) ? 1 : 0;
             }
-            s_gsq[row * 2 + hf] = gsq;
-            s_flagp[row * 2 + hf] = fl;
+            s_gsq[hf * TM + row] = gsq;
+            s_flagp[hf * TM + row] = fl;
             if (C.qjl) umma::wait_st();  // the residual operand is in tensor memory
             umma::fence_before_sync();
             asm volatile("bar.sync 1, 256;" ::: "memory");
             umma::fence_after_sync();
-            const float rn = sqrtf(s_gsq[row * 2] + s_gsq[row * 2 + 1]);
-            int flag = ri.flag | s_flagp[row * 2] | s_flagp[row * 2 + 1];
+            const float rn = sqrtf(s_gsq[row] + s_gsq[TM + row]);
+            int flag = ri.flag | s_flagp[row] | s_flagp[TM + row];
             uint32_t n16g16 = ri.n16g16;
             if (C.qjl) {
                 if (tid == 0) {
@@ -936,9 +937,9 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             if (ri.dst >= 0) {
                 uint8_t *krec = kc + ri.dst * G.k_page;
                 uint32_t *cd = reinterpret_cast<uint32_t *>(krec + static_cast<int64_t>(ri.off) * C.k_code_bytes);
-                const uint32_t *cw = scodes + row * 16;
+                const uint32_t *cw = scodes + row;
 #pragma unroll
-                for (int w = 0; w < NKW / 2; ++w) cd[hf * (NKW / 2) + w] = zero ? 0u : cw[hf * (NKW / 2) + w];
+                for (int w = 0; w < NKW / 2; ++w) cd[hf * (NKW / 2) + w] = zero ? 0u : cw[(hf * (NKW / 2) + w) * TM];
                 if (hf == 0)
                     *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * ri.off) =
                         zero ? 0 : static_cast<uint16_t>(ri.n16g16 & 0xffffu);
@@ -951,7 +952,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 umma::fence_after_sync();
                 const float guard = kSignGuard * rn * 16777216.f;  // P = 2^24 p (z units)
                 const int sf = epilogue_signs(tP, warp, row, hf, guard, zero, ssigns, smask);
-                s_flags[row * 2 + hf] = sf;
+                s_flags[hf * TM + row] = sf;
                 if (!zero) {
                     const float gam = rn / sqrtd;
                     n16g16 |= static_cast<uint32_t>(float_to_bf16_bits(gam)) << 16;
@@ -964,7 +965,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
             if (*e_abort) break;
-            if (C.qjl) flag |= s_flags[row * 2] | s_flags[row * 2 + 1];
+            if (C.qjl) flag |= s_flags[row] | s_flags[TM + row];
             if (zero) flag = 8;
             if (hf == 0) {
                 rinfo[row].flag = flag;
@@ -978,9 +979,9 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 const bool z0 = (rf.flag & 8) != 0;
                 uint8_t *krec = kc + rf.dst * G.k_page;
                 if (C.qjl) {
-                    const uint32_t *sw = ssigns + row * 4;
+                    const uint32_t *sw = ssigns + row;
                     uint2 *sd = reinterpret_cast<uint2 *>(krec + G.k_sign_off + static_cast<int64_t>(rf.off) * C.k_sign_bytes);
-                    sd[hf] = z0 ? make_uint2(0u, 0u) : make_uint2(sw[2 * hf], sw[2 * hf + 1]);
+                    sd[hf] = z0 ? make_uint2(0u, 0u) : make_uint2(sw[(2 * hf) * TM], sw[(2 * hf + 1) * TM]);
                 }
                 if (hf == 0 && C.qjl)
                     *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * rf.off) =
@@ -1017,8 +1018,8 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                         d.flag = flag;
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {
-                            d.cmask[w] = smask[row * 8 + w];
-                            d.smask[w] = smask[row * 8 + 4 + w];
+                            d.cmask[w] = smask[w * TM + row];
+                            d.smask[w] = smask[(4 + w) * TM + row];
                         }
                     }
                     ndefer += take;
