@@ -49,7 +49,6 @@ constexpr int kThreads = 512;       // warps 0-7: epilogue; warps 8-15: producer
 constexpr int kEpi = 256;           // epilogue threads: TMEM lane quarter (warp & 3), column half (warp >> 2)
 constexpr int kProd = 256;          // producer threads: key conversion, MMA issue, values
 constexpr int kPasses = TM / (8 * (kProd / 32));  // 8-row passes per producer warp and tile
-constexpr int kWarps = kThreads / 32;
 constexpr int kEpiWarps = kEpi / 32;
 constexpr float kCodeGuard = 1e-5f;   // z units
 constexpr float kSignGuard = 2e-5f;   // |p| / ||r||
@@ -608,6 +607,12 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     const float sqrtd = sqrtf(static_cast<float>(D));
     const int nthr = (1 << KB) - 1;
     const bool small_rows = rows <= 0x7fffffffLL;
+    // token of a row: a shift when the head count is a power of two (the usual case)
+    const int hshift = (Hkv & (Hkv - 1)) == 0 ? __ffs(Hkv) - 1 : -1;
+    auto token_of = [&](int64_t r) -> int64_t {
+        if (hshift >= 0) return r >> hshift;
+        return small_rows ? static_cast<int64_t>(static_cast<uint32_t>(r) / static_cast<uint32_t>(Hkv)) : r / Hkv;
+    };
     const int pshift = __ffs(G.P) - 1;  // the page size is a power of two
     const int64_t cache_slots = num_blocks * G.P;
 
@@ -700,8 +705,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 sl[p] = -1;
                 hh[p] = 0;
                 if (r < rows) {
-                    const int64_t t = small_rows ? static_cast<int64_t>(static_cast<uint32_t>(r) / static_cast<uint32_t>(Hkv))
-                                                 : r / Hkv;
+                    const int64_t t = token_of(r);
                     const int h = static_cast<int>(r - t * Hkv);
                     hh[p] = h;
                     const uint4 *ksrc = reinterpret_cast<const uint4 *>(kin + t * ks + static_cast<int64_t>(h) * D);
@@ -833,8 +837,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 for (int j = 0; j < 4; ++j) vb[j] = make_uint4(0u, 0u, 0u, 0u);
                 const int64_t rn1 = r0 + 8 * kPasses * pw + 8 * (p + 1) + (lane >> 2);
                 if (p + 1 < kPasses && rn1 < rows) {
-                    const int64_t t = small_rows ? static_cast<int64_t>(static_cast<uint32_t>(rn1) / static_cast<uint32_t>(Hkv))
-                                                 : rn1 / Hkv;
+                    const int64_t t = token_of(rn1);
                     const uint4 *vsrc = reinterpret_cast<const uint4 *>(vin + t * vs + (rn1 - t * Hkv) * D);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) vb[j] = ld_pinned(vsrc + 4 * sub + j);
