@@ -427,17 +427,18 @@ __device__ __forceinline__ int epilogue_signs(uint32_t tP, int warp, int row, in
     int flag = 0;
 #pragma unroll
     for (int cb = 0; cb < 2; ++cb) {
-        uint32_t bits = 0u, near = 0u;
+        // sign bits shifted in from the last column to the first: bit j of neg is the
+        // sign of p_j, bit j of near that of |p_j| - guard (a zero p, whose sign bit may
+        // be set, lies inside the guard band and is re-decided exactly)
+        uint32_t neg = 0u, near = 0u;
+        float p[32];
+        umma::ld32(tP + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 64 * hf + 32 * cb, p);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            float p[16];
-            umma::ld16(tP + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 64 * hf + 32 * cb + 16 * part, p);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                bits |= (p[j] >= 0.f ? 1u : 0u) << (16 * part + j);
-                near |= (fabsf(p[j]) < guard ? 1u : 0u) << (16 * part + j);
-            }
+        for (int j = 31; j >= 0; --j) {
+            neg = __funnelshift_l(__float_as_uint(p[j]), neg, 1);  // (neg << 1) | (p_j >> 31)
+            near = __funnelshift_l(__float_as_uint(fabsf(p[j]) - guard), near, 1);
         }
+        uint32_t bits = ~neg;
         if (zero) bits = near = 0u;
         ssigns[(2 * hf + cb) * TM + row] = bits;
         smask[(4 + 2 * hf + cb) * TM + row] = near;

@@ -130,9 +130,9 @@ def test_small_compress_and_decode(name):
 @pytest.mark.parametrize("name", ["pr1_tiny", "mixed_k2v2_small", "mixed_k4v4_small"])
 def test_tiny_magnitudes_take_the_exact_paths(name):
     """Keys below the fast path's power-of-two row scale are re-decided exactly (every
-    such row, many per 128-row tile, so the deferred list fills and drains several
-    times); values whose group minimum is not an fp16 normal number are quantised
-    by the exact value path.  Both must still match the oracle bit for bit."""
+    such row, many per 128-row tile); values whose group minimum is not an fp16
+    normal number are quantised by the exact value path.  Both must still match
+    the oracle bit for bit."""
     w = SMALL[name]
     b = W.generate(w, device="cpu")
     T = b.k.shape[0]
@@ -156,6 +156,25 @@ def test_tiny_magnitudes_take_the_exact_paths(name):
     okc = np.full(b.num_blocks * w.num_kv_heads * geo["k_page"], 0xA5, np.uint8)
     ora.compress_kv(W.as_u16(b.k), W.as_u16(b.v), b.slot_mapping.cpu().numpy(), w.page_size, b.num_blocks, okc, ovc)
     assert np.array_equal(vc.cpu().numpy(), ovc)
+
+
+def test_deferred_list_overflows_mid_kernel():
+    """A third of the tokens with keys around 1e-36: ~43 rows of every 128-row tile
+    take the exact path, so each CTA's 256-row deferred list fills after six tiles
+    and is drained by the epilogue between tiles, the rest at the end of the
+    kernel.  Sampled records (tiny and normal rows) must match the oracle."""
+    w = W.scaled(W.long_context_mixed(), batch=1, seq_len=20000, layers=1, layer_bits=(), k_bits=3, v_bits=2)
+    b = W.generate(w, device=DEV)
+    k = b.k.float()
+    k[::3] *= 1e-36
+    b.k = k.to(torch.bfloat16)
+    codec, ora = _codec_pair(w)
+    kc, vc = _compress(codec, w, b)
+    assert codec.get_status() == 0
+    rng = np.random.default_rng(5)
+    T = b.num_tokens
+    tok = np.unique(np.concatenate([rng.integers(0, T, 1500), np.arange(0, 300), [T - 1]]))
+    _check_rows(ora, w, b, kc, vc, tok)
 
 
 @pytest.mark.parametrize("name", ["pr1_tiny", "wide_head_small", "mixed_k2v2_small"])
