@@ -217,6 +217,14 @@ class Layer:
                 getattr(self.b, n).copy_(t, non_blocking=True)
         return sum(t.numel() * t.element_size() for t in self.host.values())
 
+    def h2d_split(self, streams):
+        """The same copies on two copy streams: keys on the first, values and the small
+        tensors on the second, so that two copy engines run at once."""
+        for n, t in self.host.items():
+            with torch.cuda.stream(streams[0] if n == "k" else streams[1]):
+                getattr(self.b, n).copy_(t, non_blocking=True)
+        return sum(t.numel() * t.element_size() for t in self.host.values())
+
     def d2h(self, stream):
         with torch.cuda.stream(stream):
             self.out_host.copy_(self.out, non_blocking=True)
@@ -289,28 +297,43 @@ def run_gpu(args, rank, world, local_rank):
     launches = args.steps * len(layers) * 4
 
     # ---- end to end: host buffers, copies inside the timed region ------------
+    # The next layer's inputs are copied on two copy streams while this layer is
+    # compressed; a layer's buffers are refilled only after its decode of the
+    # previous step.  Every copy and kernel lies between the two events on `stream`.
     e2e = None
     if not args.no_e2e:
-        for _ in range(1):
-            for L in layers:
-                L.h2d(stream)
+        cps = [torch.cuda.Stream(device=dev) for _ in range(2)]
+        dec_done = [None] * len(layers)
+
+        def e2e_step():
+            h2d = d2h = 0
+            for i, L in enumerate(layers):
+                for s in cps:
+                    if dec_done[i] is not None:
+                        s.wait_event(dec_done[i])
+                h2d += L.h2d_split(cps)
+                for s in cps:
+                    ev = torch.cuda.Event()
+                    ev.record(s)
+                    stream.wait_event(ev)
                 L.compress(stream)
-            for L in layers:
+            for i, L in enumerate(layers):
                 L.decode(stream)
-                L.d2h(stream)
+                d2h += L.d2h(stream)
+                dec_done[i] = torch.cuda.Event()
+                dec_done[i].record(stream)
+            return h2d, d2h
+
+        e2e_step()
         torch.cuda.synchronize()
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         h2d = d2h = 0
         e0.record(stream)
+        for s in cps:
+            s.wait_event(e0)
         for _ in range(args.steps):
-            h2d = d2h = 0
-            for L in layers:
-                h2d += L.h2d(stream)
-                L.compress(stream)
-            for L in layers:
-                L.decode(stream)
-                d2h += L.d2h(stream)
+            h2d, d2h = e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
