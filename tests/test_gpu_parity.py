@@ -158,6 +158,21 @@ def test_tiny_magnitudes_take_the_exact_paths(name):
     assert np.array_equal(vc.cpu().numpy(), ovc)
 
 
+@pytest.mark.parametrize("kb,vb,hkv", [(3, 2, 3), (4, 4, 5), (2, 3, 1)])
+def test_head_counts_not_a_power_of_two(kb, vb, hkv):
+    """Rows map to (token, head) by division when the head count is not a power of
+    two (and by a shift when it is); tiles then start inside a token."""
+    w = W.scaled(W.long_context_mixed(), batch=2, seq_len=700, layers=1, layer_bits=(), k_bits=kb, v_bits=vb,
+                 num_kv_heads=hkv, num_q_heads=2 * hkv)
+    b = W.generate(w, device=DEV)
+    codec, ora = _codec_pair(w)
+    kc, vc = _compress(codec, w, b)
+    assert codec.get_status() == 0
+    _check_rows(ora, w, b, kc, vc)
+    out = _decode_gpu(codec, w, b, kc, vc)
+    check_decode(out, _decode_oracle(ora, w, b, kc.cpu().numpy(), vc.cpu().numpy()))
+
+
 def test_deferred_list_overflows_mid_kernel():
     """A third of the tokens with keys around 1e-36: ~43 rows of every 128-row tile
     take the exact path, so each CTA's 256-row deferred list fills after six tiles
