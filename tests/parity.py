@@ -1,6 +1,7 @@
 """Helpers for comparing the CUDA library's cache bytes and outputs with the oracle.
 
-Acceptance rules (spec criteria, readings as stated in the design doc):
+Acceptance rules (the decision windows and the decode tolerance of the parity
+criteria, with the readings of them that the tests apply):
 * value codes, scales, zeros and the page layout: bit-exact;
 * key codes: equal except where the oracle's z lies within 1e-6 (N(0,1)
   units) of a threshold; QJL signs: equal except where the oracle's |p_i| / gamma
