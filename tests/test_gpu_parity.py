@@ -341,6 +341,14 @@ def test_runs_are_deterministic_and_graph_capturable():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+    # compression captured in a graph writes the same records
+    kc3, vc3 = codec.alloc_cache(b.num_blocks, w.num_kv_heads, w.page_size, fill=0xA5)
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s):
+        codec.compress_kv(b.k, b.v, b.slot_mapping, kc3, vc3, w.page_size, b.num_blocks, stream=s)
+    g2.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(kc3, kc1) and torch.equal(vc3, vc1)
 
 
 # --------------------------------------------------------------------------- #
