@@ -4,7 +4,7 @@
 // Method (turbo-attn "How it works"; 0xsero/turboquant "Compression Pipeline",
 // "Value Compression"; brightcoding blog "Example 4"): see tq_compress.cu.
 //
-// Tile = 128 token-heads; one persistent CTA per SM, 384 threads in two roles
+// Tile = 128 token-heads; one persistent CTA per SM, 512 threads in two roles
 // that overlap consecutive tiles:
 //  producers (warps 8-15)
 //  1. issue every global load of the tile's keys (and the first value rows),
@@ -17,19 +17,23 @@
 //     next rows while the current ones are quantised; the next tile is
 //     prefetched into L2 by the bulk-copy engine.
 //  epilogue (warps 0-7; warp w reads TMEM lane quarter w % 4, column half w / 4)
-//  4. z = Y sqrt(d) / (n 2^(10+e)); a 256-entry bin table gives, in one
-//     shared-memory load, the one threshold near z and the centroids on both
-//     sides of it; residual r = z - c[code], gamma = ||r|| / sqrt(d); r 2^12 is
-//     split into fp16 high / low parts for the next MMA;
-//  5. QJL: P = (R 2^12)(S 2^12)^T, three MMA terms (hi.hi, hi.lo, lo.hi); the
-//     sign of P is the sign of S r;
+//  4. z = Y sqrt(d) / (n 2^(10+e)); a clamped bin table (64 bins in 4 copies)
+//     gives, in one shared-memory load, the one threshold near z and the
+//     centroids on both sides of it; residual r = z - c[code], gamma =
+//     ||r|| / sqrt(d); r 2^12 is split into fp16 high / low parts and stored to
+//     tensor memory as the A operand of the next MMA;
+//  5. QJL: P = (R 2^12)(S 2^12)^T, three MMA terms (hi.hi, hi.lo, lo.hi) with A
+//     read from tensor memory; the sign of P is the sign of S r.  The key tile in
+//     shared memory is free as soon as Y is done, so step 1 of the next tile
+//     overlaps steps 4-7 of this one;
 //  6. decisions within a guard band of a threshold, a sign boundary or a bf16
 //     rounding midpoint of gamma are re-taken exactly: a code or a sign by an
 //     O(d) compensated dot product (z_j = sqrt(d) (Pi_j . k) / n,
 //     p_i = sqrt(d) (M_i . k) / n - S_i . c with M = S Pi in double-fp32), and
 //     a row whose code flips or whose gamma sits near a midpoint is redone
-//     entirely in compensated arithmetic;
-//  7. key records are written.
+//     entirely in compensated arithmetic.  Such rows are listed in shared memory
+//     and fixed by all 16 warps at the end (or by the epilogue when the list fills);
+//  7. key records are written with the fast-path results first.
 // Hand-offs: mbarriers "keys converted" (producers -> epilogue), "Y ready" and
 // "P ready" (tensor core -> both), "Y read" (epilogue -> producers).
 // Every mbarrier wait is bounded; a timeout sets TQ_DEVERR_TIMEOUT, the CTA
