@@ -52,3 +52,24 @@ def test_invalid_arguments_rejected_without_gpu(lib):
         native.tq_compress_kv(None, 0, 0, 1, 1, 128, 128, 0, 0, 0, 16, 1, None)
     assert e.value.status == native.TQ_ERR_INVALID_ARG
     assert native.tq_decode_workspace_bytes(None, 1, 1, 1) == 0
+
+
+def test_every_entry_point_rejects_a_null_handle(lib):
+    # host-side checks only: no CUDA call is reached with a NULL handle
+    calls = {
+        "tq_cache_layout": lambda: native.tq_cache_layout(None, 16),
+        "tq_dequant_kv": lambda: native.tq_dequant_kv(None, 0, 0, 16, 1, 1, 0, 1, 0, 0, None),
+        "tq_decode_attention": lambda: native.tq_decode_attention(None, 0, 0, 0, 0, 0, 1, 1, 1, 16, 1, 1, 1.0, 1, 0, 0,
+                                                                  0, None),
+        "tq_decode_attention_static": lambda: native.tq_decode_attention_static(None, 0, 0, 0, 0, 0, 1, 1, 1, 16, 1,
+                                                                                1, 1.0, 1, 0, None),
+        "tq_get_status": lambda: native.tq_get_status(None, None),
+        "tq_export_params": lambda: native.tq_export_params(None, None, None, None, None),
+    }
+    for name, call in calls.items():
+        with pytest.raises(native.TQError) as e:
+            call()
+        assert e.value.status == native.TQ_ERR_INVALID_ARG, name
+        assert "NULL" in native.tq_last_error(), name
+    native.tq_destroy(None)  # a NULL handle is a no-op
+    assert native.tq_decode_splits(None, 1, 1, 1, 16) == 1
