@@ -973,29 +973,21 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
             if (*e_abort) break;
+            // both threads of a row hold the same flag, rn and gamma (from both halves' partials)
             if (C.qjl) flag |= s_flags[row] | s_flags[TM + row];
             if (zero) flag = 8;
-            if (hf == 0) {
-                rinfo[row].flag = flag;
-                rinfo[row].rn = rn;
-                rinfo[row].n16g16 = n16g16;
-            }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
             // ---- key records, rest: signs and gamma (deferred rows are rewritten when drained) ----
-            const RowInfo rf = rinfo[row];
-            if (rf.dst >= 0) {
-                const bool z0 = (rf.flag & 8) != 0;
-                uint8_t *krec = kc + rf.dst * G.k_page;
+            if (ri.dst >= 0) {
+                uint8_t *krec = kc + ri.dst * G.k_page;
                 if (C.qjl) {
                     const uint32_t *sw = ssigns + row;
-                    uint2 *sd = reinterpret_cast<uint2 *>(krec + G.k_sign_off + static_cast<int64_t>(rf.off) * C.k_sign_bytes);
-                    sd[hf] = z0 ? make_uint2(0u, 0u) : make_uint2(sw[(2 * hf) * TM], sw[(2 * hf + 1) * TM]);
+                    uint2 *sd = reinterpret_cast<uint2 *>(krec + G.k_sign_off + static_cast<int64_t>(ri.off) * C.k_sign_bytes);
+                    sd[hf] = zero ? make_uint2(0u, 0u) : make_uint2(sw[(2 * hf) * TM], sw[(2 * hf + 1) * TM]);
                 }
                 if (hf == 0 && C.qjl)
-                    *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * rf.off) =
-                        z0 ? 0 : static_cast<uint16_t>(rf.n16g16 >> 16);
+                    *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * ri.off) =
+                        zero ? 0 : static_cast<uint16_t>(n16g16 >> 16);
             }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
             // ---- rows needing exact re-decisions join the deferred list; it is drained
             // by all epilogue warps together whenever it would overflow ----
             {
