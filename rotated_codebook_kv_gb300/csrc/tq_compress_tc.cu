@@ -114,7 +114,7 @@ struct RowInfo {     // 32 bytes per row
     int off;         // offset inside the page
     int flag;        // bit0 code guard, bit1 sign guard, bit2 tiny key, bit3 zero key, bit4 gamma near a bf16 midpoint
     float zscale;    // sqrt(d) / (n 2^(10+e)) applied to Y
-    float rn;        // ||r|| in z units
+    float rn;        // unused (the epilogue keeps ||r|| in registers); keeps the 32-byte layout
     uint32_t n16g16; // bf16 norm | bf16 gamma << 16
     int pad;
 };
