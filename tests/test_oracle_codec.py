@@ -308,3 +308,122 @@ def test_decode_identical_keys_average_values():
     _, V = ora.dequant_slots(kc, vc, P, Hkv, slots)
     assert np.allclose(out[0, 0], V[:, 0].mean(axis=0), atol=1e-12)
     assert np.allclose(out[0, 1], V[:, 0].mean(axis=0), atol=1e-12)
+
+
+# --------------------------------------------------------------------------- #
+# Reading records back: dequant_slots and the QJL half for given codes          #
+# --------------------------------------------------------------------------- #
+
+def _paged_rows(d, kb, vb, g, P, T=40, Hkv=3, seed=11):
+    """Random keys and values (with constant and all-zero value groups) written to
+    shuffled slots of a small paged pool by the oracle."""
+    ora = O.Oracle(d, kb, vb, g, seed=seed)
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((T, Hkv, d)) * np.exp(rng.standard_normal((T, Hkv, 1)))
+    v = rng.standard_normal((T, Hkv, d)) * np.exp(rng.standard_normal((T, Hkv, 1)))
+    v[0, 0, :g] = 0.75          # a constant group
+    v[1, 1, g:2 * g if 2 * g <= d else d] = 0.0  # an all-zero group (or the whole row at g = d)
+    nb = (T + P - 1) // P + 2
+    slots = rng.permutation(nb * P)[:T].astype(np.int64)
+    kk, vv = _bf16(k), _bf16(v)
+    kc, vc = ora.compress_kv(kk, vv, slots, P, nb)
+    return ora, kk, vv, slots, kc, vc
+
+
+@pytest.mark.parametrize("d,kb,vb,g,P", [(128, 3, 4, 32, 16), (128, 2, 2, 64, 16), (128, 4, 3, 128, 32),
+                                         (256, 4, 4, 64, 32)])
+def test_dequant_values_reconstruct_the_inputs(d, kb, vb, g, P):
+    """V~ read back by dequant_slots: within half a quantisation step of the bf16
+    input inside the group's range, exact for constant groups, and equal to
+    code * scale + zero with every field decoded by numpy from the raw bytes
+    (the record reader in tests/parity.py), so a slip in the group index or a
+    swap of scale and zero in the read-back fails."""
+    from parity import read_records
+    ora, kk, vv, slots, kc, vc = _paged_rows(d, kb, vb, g, P)
+    T, Hkv, _ = vv.shape
+    _, V = ora.dequant_slots(kc, vc, P, Hkv, slots)
+    geo = ora.geometry(P)
+    rec = read_records(kc, vc, geo, d, kb, vb, g, P, Hkv, slots)
+    s = rec["v_meta"][..., 0].view(np.float16).astype(np.float64)   # [T, Hkv, d/g]
+    z = rec["v_meta"][..., 1].view(np.float16).astype(np.float64)
+    code = rec["v_code"].astype(np.float64)                          # [T, Hkv, d]
+    s_e, z_e = np.repeat(s, g, axis=-1), np.repeat(z, g, axis=-1)
+    assert np.array_equal(V, code * s_e + z_e)
+    x = O.bf16_to_double(vv)
+    xg = x.reshape(T, Hkv, d // g, g)
+    mn, mx = xg.min(-1), xg.max(-1)
+    L = (1 << vb) - 1
+    # half a step inside [mn, mx], plus what the fp16 roundings of zero and scale move the grid
+    slack = np.abs(mn - z) + L * np.abs(s - (mx - mn) / L)
+    err = np.abs(V - x).reshape(T, Hkv, d // g, g)
+    assert np.all(err <= (s / 2 + slack + 1e-12)[..., None])
+    const = (mx == mn)
+    assert const.any()
+    assert np.all(err[const] == 0.0)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_dequant_keys_rotate_back_to_the_codebook(bits):
+    """K~ read back by dequant_slots, rotated by Pi (pinned orthogonal) and scaled
+    by sqrt(d) / n16, gives back the centroids of the stored codes (decoded by
+    numpy from the raw bytes) exactly when there is no QJL term; with QJL the
+    difference is the sign-sketch correction, whose size follows from gamma and
+    the Gaussian S.  Without QJL the distance to the input key is the Lloyd-Max
+    distortion of the codebook (J. Max 1960)."""
+    from parity import read_records
+    d, P = 128, 16
+    ora, kk, vv, slots, kc, vc = _paged_rows(d, bits, 4, 32, P, T=300, Hkv=2, seed=20 + bits)
+    T, Hkv, _ = kk.shape
+    K, _ = ora.dequant_slots(kc, vc, P, Hkv, slots)
+    prm = ora.params()
+    rec = read_records(kc, vc, ora.geometry(P), d, bits, 4, 32, P, Hkv, slots)
+    n16 = O.bf16_to_double(rec["k_norm"])                            # [T, Hkv]
+    u = np.einsum("ij,thj->thi", prm["Pi"], K) * math.sqrt(d) / n16[..., None]
+    cz = prm["centroids"][rec["k_code"]]
+    if bits == 4:
+        assert np.abs(u - cz).max() < 1e-10
+    else:
+        # the QJL term sqrt(pi/2)/d * gamma * S^T(2 sigma - 1), in z units, has norm
+        # about sqrt(pi/2) gamma sqrt(d) ||S^T(2 sigma - 1)|| / d ~ sqrt(pi/2) * gamma * sqrt(d)
+        gam = O.bf16_to_double(rec["k_gamma"])
+        corr = np.linalg.norm(u - cz, axis=-1)
+        ratio = corr / (gam * math.sqrt(d) * math.sqrt(math.pi / 2))
+        assert 0.7 < ratio.mean() < 1.4
+    k = O.bf16_to_double(kk)
+    kn = np.linalg.norm(k, axis=-1)
+    rel = np.sum((K - k) ** 2, axis=-1) / kn ** 2   # = ||z - c||^2 / d: the per-coordinate MSE in z units
+    if bits == 4:
+        assert abs(rel.mean() - MAX_MSE[bits]) < 0.08 * MAX_MSE[bits]
+
+
+@pytest.mark.parametrize("bits", [2, 3])
+def test_qjl_given_codes_reproduces_the_compressor(bits):
+    """The QJL half for given codes, fed the compressor's own codes, gives the
+    compressor's signs, gamma and projections bit for bit; fed a code moved by one
+    level on one coordinate, gamma changes exactly as the residual definition says
+    (r_j = z_j / sqrt(d) - c[code_j] / sqrt(d))."""
+    d = 128
+    ora = O.Oracle(d, bits, 4, 32, seed=31)
+    rng = np.random.default_rng(31 + bits)
+    k = _bf16(rng.standard_normal((50, d)) * 2.0)
+    rec = ora.compress_rows(k=k)
+    codes = np.stack([O.unpack(r, d, bits) for r in rec["k_code"]])
+    alt = ora.key_qjl_given_codes(k, codes)
+    assert np.array_equal(alt["k_sign"], rec["k_sign"])
+    assert np.array_equal(alt["k_gamma"], rec["k_gamma"])
+    assert np.array_equal(alt["gamma"], rec["gamma"])
+    assert np.array_equal(alt["pg"], rec["pg"])
+    c = ora.params()["centroids"]
+    L = 1 << bits
+    moved = codes.copy()
+    j = 17
+    moved[:, j] = np.where(moved[:, j] + 1 < L, moved[:, j] + 1, moved[:, j] - 1)
+    alt2 = ora.key_qjl_given_codes(k, moved)
+    r_old = (rec["z"][:, j] - c[codes[:, j]]) / math.sqrt(d)
+    r_new = (rec["z"][:, j] - c[moved[:, j]]) / math.sqrt(d)
+    want = np.sqrt(rec["gamma"] ** 2 - r_old ** 2 + r_new ** 2)
+    assert np.allclose(alt2["gamma"], want, rtol=1e-12)
+    assert np.array_equal(alt2["k_gamma"], _bf16(alt2["gamma"]))
+    # the signs follow the moved residual: most agree, the ones that change are where
+    # the projection of the moved coordinate's column shifts p across zero
+    assert (alt2["k_sign"] != rec["k_sign"]).any()
