@@ -374,14 +374,14 @@ def run_gpu(args, rank, world, local_rank):
         "decode_kv_tokens_per_s": round(world * sum(sum(L.seq_lens) * L.w.num_kv_heads for L in layers) / d_time, 1),
         "decode_query_tokens_per_s": round(world * w.batch * w.layers / d_time, 1),
         "roofline": {
-            "bound": "hbm", "kernel": "compress_kernel (tq_compress_kv)",
+            "bound": "hbm", "kernel": "compress_tc_kernel (tq_compress_kv)",
             "achieved": round(c_gbs, 1), "peak": peak, "peak_kind": f"of {peak_kind}",
             "unit": "GB/s", "frac": round(c_gbs / peak, 4),
             "traffic": None if traffic is None else traffic.get("bytes_per_launch"),
             "algorithmic_bytes_per_launch": round(c_bytes / len(layers)),
         },
         "roofline_decode": {
-            "bound": "hbm", "kernel": "qrot + decode_kernel + combine (tq_decode_attention)",
+            "bound": "hbm", "kernel": "qrot_kernel + decode_mma_kernel + combine_kernel (tq_decode_attention)",
             "achieved": round(d_gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(d_gbs / peak, 4),
             "algorithmic_bytes_per_call": round(d_bytes / len(layers)),
         },
@@ -390,9 +390,77 @@ def run_gpu(args, rank, world, local_rank):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if not args.no_per_config:
+        line["per_config"] = per_config(dev, peak, args.config_reps)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     return line
+
+
+# --------------------------------------------------------------------------- #
+# The other full-size workloads                                                 #
+# --------------------------------------------------------------------------- #
+
+L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024  # twice the GB300's L2
+
+
+def per_config(dev, peak, reps):
+    """Compress-only, paged-decode and wide-head workloads at full size, each call
+    timed alone with CUDA events on its stream after an L2 flush (a write of twice
+    the L2 size outside the timed region), so no call reads its inputs from L2.
+    Median over `reps` calls after two warm-up calls."""
+    from rotated_codebook_kv_gb300 import Codec
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        ms = []
+        for i in range(reps + 2):
+            with torch.cuda.stream(stream):
+                flush.fill_(i & 0xff)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            stream.synchronize()
+            if i >= 2:
+                ms.append(a.elapsed_time(b))
+        return statistics.median(ms) * 1e-3
+
+    out = {}
+    for name, w in (("compress_only", W.compress_only()), ("paged_decode", W.paged_decode()),
+                    ("wide_head_decode", W.wide_head_decode())):
+        b = W.generate(w, device=dev)
+        codec = Codec(w.head_dim, w.k_bits, w.v_bits, w.group, w.codec_seed())
+        kc, vc = codec.alloc_cache(b.num_blocks, w.num_kv_heads, w.page_size, device=dev)
+        T = b.num_tokens
+        t_c = timed(lambda: codec.compress_kv(b.k, b.v, b.slot_mapping, kc, vc, w.page_size, b.num_blocks,
+                                              stream=stream))
+        cb = compress_bytes(w, T)
+        ent = {"compress_mtoken_heads_per_s": round(T * w.num_kv_heads / t_c / 1e6, 1),
+               "compress_gbs": round(cb / t_c / 1e9, 1), "compress_frac": round(cb / t_c / 1e9 / peak, 4),
+               "compress_us": round(t_c * 1e6, 1)}
+        if w.decode:
+            maxb = b.block_table.shape[1]
+            splits = codec.decode_splits(w.batch, w.num_kv_heads, maxb, w.page_size)
+            ws = codec.workspace(w.batch, w.num_q_heads, splits, device=dev)
+            o = torch.empty_like(b.q)
+            t_d = timed(lambda: codec.decode_attention(b.q, kc, vc, b.block_table, b.seq_lens, w.num_kv_heads,
+                                                       w.page_size, b.num_blocks, b.sm_scale, splits=splits,
+                                                       workspace=ws, out=o, stream=stream))
+            lens = b.seq_lens.cpu().tolist()
+            db = decode_bytes(w, lens, maxb)
+            ent.update({"decode_gbs": round(db / t_d / 1e9, 1), "decode_frac": round(db / t_d / 1e9 / peak, 4),
+                        "decode_us": round(t_d * 1e6, 1), "decode_splits": splits,
+                        "decode_kv_tokens_per_s": round(sum(lens) * w.num_kv_heads / t_d, 1),
+                        "decode_query_tokens_per_s": round(w.batch / t_d, 1)})
+        if codec.get_status(stream) != 0:
+            raise RuntimeError(f"device status bits set in the {name} workload")
+        out[name] = ent
+        del b, kc, vc, codec
+        torch.cuda.empty_cache()
+    out["timing"] = f"median of {reps} calls after 2 warm-up calls; L2 flushed before each call"
+    return out
 
 
 # --------------------------------------------------------------------------- #
@@ -429,6 +497,26 @@ class OracleSample:
             ora.decode(q, kc, vc, bt, sl, lw.num_kv_heads, lw.page_size, b.sm_scale, mode=1, nthreads=nthreads)
 
 
+def cpu_model():
+    try:  # lscpu names Arm cores too ("Neoverse-V2"); /proc/cpuinfo does not on aarch64
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip().lower() == "model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(w, budget_s=12.0):
     s = OracleSample(w)
     cores = os.cpu_count() or 1
@@ -440,8 +528,16 @@ def cpu_baseline(w, budget_s=12.0):
     for _ in range(reps):
         s.run()
     el = time.perf_counter() - t
+    # one thread on the first layer of the sample, for the per-core rate
+    one_layer = OracleSample(W.scaled(w, layers=1, layer_bits=w.layer_bits[:1]))
+    t = time.perf_counter()
+    one_layer.run(nthreads=1)
+    el1 = time.perf_counter() - t
     return {"value": round(s.bytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{s.desc}; {reps} repetitions, {el:.1f} s", "seconds": round(el, 2)}
+            "sample": f"{s.desc}; {reps} repetitions, {el:.1f} s", "seconds": round(el, 2),
+            "single_thread_gbs": round(one_layer.bytes / el1 / 1e9, 5),
+            "single_thread_sample": f"layer 0 of the sample on one thread, {el1:.1f} s",
+            "cpu_model": cpu_model()}
 
 
 def run_reference(args):
@@ -514,6 +610,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-per-config", action="store_true", help="skip the other full-size workloads")
+    ap.add_argument("--config-reps", type=int, default=10)
     ap.add_argument("--layers", type=int, default=None, help="profiling only: first N layers")
     ap.add_argument("--batch", type=int, default=None, help="profiling only: fewer sequences")
     args = ap.parse_args()

@@ -61,7 +61,11 @@ typedef enum {
 #define TQ_DEVERR_SLOT_RANGE  0x1u  /* compress: slot >= num_blocks * page_size (token skipped)   */
 #define TQ_DEVERR_BLOCK_RANGE 0x2u  /* decode/dequant: block id < 0 or >= num_blocks (page skipped) */
 #define TQ_DEVERR_SEQ_RANGE   0x4u  /* decode: seq_len > max_blocks_per_seq * page_size (clamped)  */
-#define TQ_DEVERR_TIMEOUT     0x8u  /* compress: a tensor-core completion wait timed out (CTA stopped) */
+#define TQ_DEVERR_TIMEOUT     0x8u  /* a barrier wait ran past the handle's wait limit (tq_set_wait_limit):
+                                       compress -- a tensor-core completion or hand-off wait; the CTA stops
+                                       and the rows of its unfinished tiles are left unwritten;
+                                       decode -- a page-copy wait; the CTA stops issuing copies, waits
+                                       (bounded) for those in flight and drops its split from the result */
 
 /*
  * tq_init -- build the codec parameters for one (head_dim, k_bits, v_bits,
@@ -86,6 +90,9 @@ tq_status tq_destroy(tq_handle h);
 
 /*
  * tq_cache_layout -- bytes of one page record for one (block, kv head).
+ * The record size does not depend on the number of kv heads, so unlike the
+ * pool sizes it takes no head count: a pool holds num_blocks * num_kv_heads
+ * records.
  *
  * The K pool is laid out [num_blocks][num_kv_heads][k_page_bytes] and the V
  * pool [num_blocks][num_kv_heads][v_page_bytes].  Token slot s lives in block
@@ -152,7 +159,9 @@ size_t tq_decode_workspace_bytes(tq_handle h, int batch, int num_q_heads, int sp
  * sm_scale: score scale (usually 1/sqrt(d)).
  * splits: split-K count, 0 = tq_decode_splits(...).
  * workspace: device scratch of ws_bytes >= tq_decode_workspace_bytes(splits),
- *   256-byte aligned; holds rotated queries and per-split partial outputs.
+ *   256-byte aligned; holds rotated queries and per-split partial outputs.  It
+ *   starts with the outputs in fp32 before their bf16 rounding, float
+ *   [B][Hq][d] at offset 0, which the caller may read after the call.
  * out: device bf16 [B][Hq][d].
  * Three launches on `stream` (query rotation, split-K decode, combine).
  */
@@ -174,16 +183,31 @@ tq_status tq_decode_attention(tq_handle h, const uint16_t *q, const uint8_t *k_c
  * The scratch lives in one file-scope device array of TQ_STATIC_SCRATCH_BYTES
  * that every GPU loading the library holds until exit.  A call whose scratch
  * need (tq_decode_workspace_bytes) exceeds it returns TQ_ERR_UNSUPPORTED and
- * launches nothing.  Allocates nothing.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) while that device is current;
- * make that first call before any stream capture.  All calls share the array:
- * calls that overlap on the GPU (other streams, other handles) race.
+ * launches nothing.  Allocates nothing.  tq_init looks up the array's device
+ * address (cudaGetSymbolAddress) in the context current when the handle is
+ * created and keeps it in the handle, so use the handle in that context.  All
+ * calls share the array: calls that overlap on the GPU (other streams, other
+ * handles) race.
  */
 #define TQ_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
 tq_status tq_decode_attention_static(tq_handle h, const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
                                      const int32_t *block_table, const int32_t *seq_lens, int batch, int num_q_heads,
                                      int num_kv_heads, int page_size, int max_blocks_per_seq, int64_t num_blocks,
                                      float sm_scale, int splits, uint16_t *out, void *stream);
+
+/*
+ * tq_set_wait_limit -- the number of SM clock cycles a kernel of this handle
+ * polls one barrier (a tensor-core completion, a page copy, a hand-off between
+ * warps) before it gives up, sets TQ_DEVERR_TIMEOUT and winds its CTA down.
+ * The default, TQ_DEFAULT_WAIT_LIMIT, is about one second at the maximum
+ * clock; no correct run comes near it.  A limit of 0 makes every wait test its
+ * barrier once without blocking and give up if it has not completed, so that
+ * the error path can be exercised on purpose without any real hang (the waits
+ * for work already in flight keep a fixed bound of their own).  Host-only;
+ * affects later launches of this handle.
+ */
+#define TQ_DEFAULT_WAIT_LIMIT 2000000000LL
+tq_status tq_set_wait_limit(tq_handle h, int64_t cycles);
 
 /*
  * tq_get_status -- synchronises `stream`, returns the device status bits

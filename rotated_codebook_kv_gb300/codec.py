@@ -97,6 +97,9 @@ class Codec:
                                    splits, _ptr(workspace), workspace.numel(), _ptr(out), _stream(stream))
         return out
 
+    def set_wait_limit(self, cycles: int):
+        native.tq_set_wait_limit(self.handle, cycles)
+
     def get_status(self, stream=None) -> int:
         return native.tq_get_status(self.handle, _stream(stream))
 

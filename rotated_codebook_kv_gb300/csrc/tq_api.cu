@@ -5,7 +5,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include <cuda_fp16.h>
@@ -16,7 +19,8 @@
 
 struct tq_ctx {
     tq::Codec codec;
-    void *dev_tables;  // Pi, PiT, S, ST (fp32) then the status word
+    void *dev_tables;      // Pi, PiT, S, ST (fp32) then the status word
+    void *static_scratch;  // device address of the no-allocation decode's array in this handle's context
     int device;
     int num_sms;
     uint64_t seed;
@@ -47,6 +51,23 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 bool supported_bits(int b) { return b >= 2 && b <= 4; }
 
 }  // namespace
+
+void *tq::handle_static_scratch(tq_handle h) { return h ? h->static_scratch : nullptr; }
+
+cudaError_t tq::ensure_smem_attr(const void *func, size_t bytes)
+{
+    static std::mutex lock;
+    static std::map<std::pair<const void *, int>, size_t> granted;  // (kernel, device) -> bytes
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> guard(lock);
+    size_t &g = granted[std::make_pair(func, dev)];
+    if (g >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess) g = bytes;
+    return e;
+}
 
 tq_status tq::api_error(tq_status s, const char *fmt, ...)
 {
@@ -121,6 +142,12 @@ tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed
         delete c;
         return cuda_fail(e, "tq_init: device query");
     }
+    // the no-allocation decode's static array: its device address in this context
+    e = tq::static_scratch_lookup(&c->static_scratch);
+    if (e != cudaSuccess) {
+        delete c;
+        return cuda_fail(e, "tq_init: cudaGetSymbolAddress of the static decode scratch");
+    }
     e = cudaMalloc(&c->dev_tables, 6 * dd * sizeof(float) + img_bytes + 256);
     if (e != cudaSuccess) {
         delete c;
@@ -159,6 +186,7 @@ tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed
     k.M_lo = base + 5 * dd;
     k.tc_image = img_bytes ? img_dev : nullptr;
     k.status = status;
+    k.wait_limit = tq::kDefaultWaitLimit;
     k.num_sms = c->num_sms;
     c->seed = seed;
     *out = c;
@@ -308,6 +336,14 @@ tq_status tq_decode_attention(tq_handle h, const uint16_t *q, const uint8_t *k_c
     const tq::PageGeom g = tq::page_geom(h->codec, page_size);
     cudaError_t e = tq::launch_decode(h->codec, g, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tq_decode_attention: launch");
+    return TQ_OK;
+}
+
+tq_status tq_set_wait_limit(tq_handle h, int64_t cycles)
+{
+    if (!h) return fail(TQ_ERR_INVALID_ARG, "tq_set_wait_limit: NULL handle");
+    if (cycles < 0) return fail(TQ_ERR_INVALID_ARG, "tq_set_wait_limit: negative limit");
+    h->codec.wait_limit = cycles;
     return TQ_OK;
 }
 

@@ -57,7 +57,6 @@ constexpr int kEpiWarps = kEpi / 32;
 constexpr float kCodeGuard = 1e-5f;   // z units
 constexpr float kSignGuard = 2e-5f;   // |p| / ||r||
 constexpr float kGammaGuard = 2e-6f;  // relative distance of gamma to a bf16 rounding midpoint
-constexpr long long kWaitLimit = 2000000000LL;  // cycles (~1 s)
 
 // Shared-memory map (bytes).
 constexpr uint32_t kOffPiH = 0, kOffPiL = 32768, kOffSH = 65536, kOffSL = 98304;  // B operands (fp16)
@@ -733,7 +732,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             }
             // the key tile buffer is free once the previous tile's rotation MMA finished
             if (it > 0 && ptid == 0) {
-                if (!umma::mbar_wait_bounded(mbarY, (it - 1) & 1, kWaitLimit)) {
+                if (!umma::mbar_wait_bounded(mbarY, (it - 1) & 1, C.wait_limit)) {
                     atomicOr(C.status, TQ_DEVERR_TIMEOUT);
                     *p_abort = 1;
                 }
@@ -814,7 +813,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             if (ptid == 0) {
                 // ---- rotation MMAs: Y = K' (Pi_lo + Pi_hi)^T, once the epilogue has read Y ----
                 bool ok = true;
-                if (it > 0) ok = umma::mbar_wait_bounded(mbarYfree, (it - 1) & 1, kWaitLimit);
+                if (it > 0) ok = umma::mbar_wait_bounded(mbarYfree, (it - 1) & 1, C.wait_limit);
                 if (ok) {
                     umma::fence_after_sync();
                     const uint32_t d_hi = sdesc[0], dTA_lo = sdesc[1], dPiL_lo = sdesc[3], dPiH_lo = sdesc[4];
@@ -892,7 +891,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             const int64_t r0 = static_cast<int64_t>(tile) * TM;
             RowInfo *rinfo = rinfo_all + buf * TM;
             const uint32_t par = it & 1;
-            if (!umma::mbar_wait_bounded(mbarConv, par, kWaitLimit) || !umma::mbar_wait_bounded(mbarY, par, kWaitLimit)) {
+            if (!umma::mbar_wait_bounded(mbarConv, par, C.wait_limit) || !umma::mbar_wait_bounded(mbarY, par, C.wait_limit)) {
                 atomicOr(C.status, TQ_DEVERR_TIMEOUT);
                 *e_abort = 1;
             }
@@ -953,7 +952,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                         zero ? 0 : static_cast<uint16_t>(ri.n16g16 & 0xffffu);
             }
             if (C.qjl) {
-                if (!umma::mbar_wait_bounded(mbarP, par, kWaitLimit)) {
+                if (!umma::mbar_wait_bounded(mbarP, par, C.wait_limit)) {
                     atomicOr(C.status, TQ_DEVERR_TIMEOUT);
                     *e_abort = 1;
                 }
@@ -1062,7 +1061,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     __syncthreads();
     if (*e_abort || *p_abort) {
         const long long t0 = clock64();
-        while (clock64() - t0 < 200000000LL) {  // bounded grace period for in-flight tensor-core work
+        while (clock64() - t0 < kDrainLimit / 20) {  // fixed grace period (~0.1 s) for in-flight tensor-core work
         }
     }
     umma::fence_before_sync();
@@ -1076,16 +1075,8 @@ cudaError_t launch_tc(const Codec &c, const PageGeom &pg, const uint16_t *k, con
                       int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc, int64_t num_blocks,
                       int num_sms, cudaStream_t st)
 {
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(compress_tc_kernel<KB, VB>), kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(compress_tc_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
     const int64_t rows = T * Hkv;
     const int tiles = static_cast<int>((rows + TM - 1) / TM);
     const int grid = tiles < num_sms ? tiles : num_sms;

@@ -29,7 +29,7 @@ size_t decode_workspace_bytes(int d, int B, int Hq, int splits)
 {
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t rows = static_cast<size_t>(B) * Hq;
-    return al(rows * d * 4) * 2 + al(static_cast<size_t>(splits) * rows * d * 4) +
+    return al(rows * d * 4) * 3 + al(static_cast<size_t>(splits) * rows * d * 4) +
            al(static_cast<size_t>(splits) * rows * 2 * 4);
 }
 
@@ -39,6 +39,8 @@ DecodeWorkspace carve_decode_workspace(void *base, int d, int B, int Hq, int spl
     const size_t rows = static_cast<size_t>(B) * Hq;
     char *p = static_cast<char *>(base);
     DecodeWorkspace w;
+    w.out32 = reinterpret_cast<float *>(p);
+    p += al(rows * d * 4);
     w.qrot = reinterpret_cast<float *>(p);
     p += al(rows * d * 4);
     w.qs = reinterpret_cast<float *>(p);
@@ -170,6 +172,7 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs A)
     const float num = (n0 + n1) + (n2 + n3);
     const float dd = s_den;
     const float o = (dd > 0.f) ? num / dd : 0.f;
+    A.ws.out32[static_cast<size_t>(row) * D + j] = o;
     A.out[static_cast<size_t>(row) * D + j] = float_to_bf16_bits(o);
 }
 
@@ -177,16 +180,8 @@ template <int D, int KB, int VB>
 cudaError_t launch_dmma(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st)
 {
     const size_t smem = dmma::DecSmem<D, KB>::bytes(pg);
-    static size_t attr_bytes[64] = {};  // per device: the largest size granted so far
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(dmma::decode_mma_kernel<D, KB, VB>), smem);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || attr_bytes[dev] < smem) {
-        e = cudaFuncSetAttribute(dmma::decode_mma_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_bytes[dev] = smem;
-    }
     dim3 grid(a.splits, a.Hkv, a.B);
     dmma::decode_mma_kernel<D, KB, VB><<<grid, dmma::kThreads, smem, st>>>(c, pg, a);
     return cudaGetLastError();

@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     int *page_ok = reinterpret_cast<int *>(smem + SM::kLut + SM::kSignLut + SM::kQfrag + SM::kSfrag);  // [4][2][2]
     uint32_t *zero_meta = reinterpret_cast<uint32_t *>(page_ok + 16);  // [16] zeros: metadata of masked tokens
     uint64_t *mbar = reinterpret_cast<uint64_t *>(page_ok + 32);        // [4 warps][2 stages] barriers
+    volatile int *cta_abort = page_ok + 48;                             // a warp gave up waiting for its pages
     const uint32_t zero_off = static_cast<uint32_t>(SM::kLut + SM::kSignLut + SM::kQfrag + SM::kSfrag + 64);
     unsigned char *stages = smem + SM::kHeader;
 
@@ -162,8 +163,6 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     const int P = PG.P;
     const int G = A.Hq / A.Hkv;
     const int ng = D / C.group;
-    const size_t stage_bytes = SM::stage_bytes(PG);
-    const int ppc = kChunk / P;
     const int pshift = __ffs(P) - 1;                 // page size and value group are powers of two
     const int gshift = __ffs(C.group) - 1;
 
@@ -297,7 +296,27 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     };
 
     const int nrounds = (pg1 - pg0 + 4 * wpc - 1) / (4 * wpc);
+    auto stage_ready = [&](int st, uint32_t par) -> bool {
+        const uint32_t mb = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * 2 + st]));
+        uint32_t done;
+        asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(done) : "r"(mb), "r"(par) : "memory");
+        return done != 0;
+    };
+    auto stage_tested = [&](int st, uint32_t par) -> bool {
+        const uint32_t mb = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * 2 + st]));
+        uint32_t done;
+        asm volatile("{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(done) : "r"(mb), "r"(par) : "memory");
+        return done != 0;
+    };
+    auto drain = [&](int st, uint32_t par) {  // copies in flight must land before the CTA exits
+        const long long t0 = clock64();
+        while (!stage_ready(st, par) && clock64() - t0 < kDrainLimit) {
+        }
+    };
     if (tid < 8) mbar_init_cta(&mbar[tid], wpc);
+    if (tid == 0) *cta_abort = 0;
     if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();  // tables, query fragments and barriers are ready
     int bnext = fetch_id(0);
@@ -310,18 +329,30 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
             bnext = fetch_id(c + 2);
         }
         {
-            const uint32_t mb = static_cast<uint32_t>(__cvta_generic_to_shared(&mbar[warp * 2 + st]));
-            const uint32_t par = static_cast<uint32_t>((c >> 1) & 1);
-            const long long t0 = clock64();
-            for (;;) {
-                uint32_t done;
-                asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-                             : "=r"(done) : "r"(mb), "r"(par) : "memory");
-                if (done) break;
-                if (clock64() - t0 > 2000000000LL) {  // ~1 s: report instead of hanging
-                    if (lane == 0) atomicOr(C.status, TQ_DEVERR_TIMEOUT);
-                    break;
+            // bounded wait for this round's pages; on a timeout the warp stops issuing,
+            // waits (with a fixed, longer bound) for the copies it still has in flight,
+            // and the CTA drops its split (the combine then gives it no weight)
+            bool ok = true;
+            if (C.wait_limit <= 0) {  // a zero limit tests once without blocking
+                ok = stage_tested(st, (c >> 1) & 1);
+            } else {
+                const long long t0 = clock64();
+                while (!stage_ready(st, (c >> 1) & 1)) {
+                    if (clock64() - t0 > C.wait_limit) {
+                        ok = false;
+                        break;
+                    }
                 }
+            }
+            ok = __all_sync(0xffffffffu, ok);  // the lanes poll separately: decide as a warp
+            if (!ok) {
+                if (lane == 0) {
+                    atomicOr(C.status, TQ_DEVERR_TIMEOUT);
+                    *cta_abort = 1;
+                }
+                drain(st, (c >> 1) & 1);
+                if (c + 1 < nrounds) drain(st ^ 1, ((c + 1) >> 1) & 1);
+                break;
             }
         }
 
@@ -508,6 +539,13 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
         __syncwarp();  // the next issue() overwrites this stage
     }
     __syncthreads();  // every warp is done with the stages before they hold merge data
+    if (*cta_abort) {  // a page wait timed out: this split contributes nothing
+        if (tid < G) {
+            ml_out[2 * tid] = -INFINITY;
+            ml_out[2 * tid + 1] = 0.f;
+        }
+        return;
+    }
 
     // ---- merge the four warps ---------------------------------------------------
     float *red = reinterpret_cast<float *>(stages);

@@ -34,6 +34,7 @@ struct Codec {
     const float *M_lo;
     const void *tc_image;  // d = 128: fp16 tensor-core operands (Pi 2^10 hi/lo, S 2^12 hi/lo), core-matrix layout
     unsigned int *status;  // device status word (TQ_DEVERR_* bits)
+    long long wait_limit;  // clock cycles a kernel waits on one barrier before it reports TQ_DEVERR_TIMEOUT
     int num_sms;
 };
 
@@ -60,6 +61,7 @@ inline PageGeom page_geom(const Codec &c, int P)
 
 // Workspace carve-up of tq_decode_attention (all fp32, 256-byte aligned pieces).
 struct DecodeWorkspace {
+    float *out32; // [B][Hq][d] the outputs in fp32, before the bf16 rounding (offset 0 of the workspace)
     float *qrot;  // [B][Hq][d]
     float *qs;    // [B][Hq][d]
     float *acc;   // [splits][B][Hq][d] unnormalised partial outputs
@@ -93,5 +95,20 @@ cudaError_t launch_dequant(const Codec &c, const PageGeom &pg, const uint8_t *kc
                            uint16_t *v_out, cudaStream_t st);
 
 cudaError_t launch_decode(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st);
+
+// Device address of the no-allocation decode's static scratch array for the
+// context current on the calling thread (looked up, not cached).
+cudaError_t static_scratch_lookup(void **out);
+// The address tq_init looked up for a handle.
+void *handle_static_scratch(tq_handle h);
+
+// Sets a kernel's dynamic shared-memory limit once per (function, device); thread safe.
+cudaError_t ensure_smem_attr(const void *func, size_t bytes);
+
+// Default barrier wait limit: about one second at the GB300's maximum SM clock.
+constexpr long long kDefaultWaitLimit = TQ_DEFAULT_WAIT_LIMIT;
+// Limit of the waits that drain copies or tensor-core work still in flight after
+// a CTA gave up: fixed, so that a tiny tq_set_wait_limit never frees memory early.
+constexpr long long kDrainLimit = 4000000000LL;
 
 }  // namespace tq

@@ -13,8 +13,6 @@
 // it and it keeps the last call's contents; nothing in it needs to start at zero,
 // because each call writes every byte it later reads.  Calls that overlap on the
 // GPU -- on two streams, or through two handles -- race on the array.
-#include <mutex>
-
 #include <cuda_runtime.h>
 
 #include "tq.h"
@@ -24,31 +22,19 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_decode_scratch[TQ_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_lock;
-void *g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the array on the current device.  In host code the array's
-// name is only a stand-in, so the address is looked up with cudaGetSymbolAddress,
-// once per device, while that device is current.
-cudaError_t scratch_address(void **out)
-{
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> guard(g_scratch_lock);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
-    return cudaSuccess;
-}
-
 }  // namespace
+
+// In host code the array's name is only a stand-in, not a device address: the
+// address belongs to the CUDA context and is looked up with cudaGetSymbolAddress.
+// tq_init calls this while its device (and context) is current and keeps the
+// result in the handle, so the entry point below never looks it up again.
+cudaError_t tq::static_scratch_lookup(void **out)
+{
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e == cudaSuccess) *out = p;
+    return e;
+}
 
 extern "C" tq_status tq_decode_attention_static(tq_handle h, const uint16_t *q, const uint8_t *k_cache,
                                                 const uint8_t *v_cache, const int32_t *block_table,
@@ -70,11 +56,8 @@ extern "C" tq_status tq_decode_attention_static(tq_handle h, const uint16_t *q, 
                                  "with a workspace",
                                  need, static_cast<size_t>(TQ_STATIC_SCRATCH_BYTES));
     }
-    void *ws = nullptr;
-    const cudaError_t e = scratch_address(&ws);
-    if (e != cudaSuccess)
-        return tq::api_error(TQ_ERR_CUDA, "tq_decode_attention_static: cudaGetSymbolAddress: %s",
-                             cudaGetErrorString(e));
+    void *ws = tq::handle_static_scratch(h);
+    if (!ws) return tq::api_error(TQ_ERR_CUDA, "tq_decode_attention_static: the handle has no scratch address");
     return tq_decode_attention(h, q, k_cache, v_cache, block_table, seq_lens, batch, num_q_heads, num_kv_heads,
                                page_size, max_blocks_per_seq, num_blocks, sm_scale, splits, ws, TQ_STATIC_SCRATCH_BYTES,
                                out, stream);

@@ -95,9 +95,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *mbar, uint32_t parity)
     return ok != 0;
 }
 
-// Waits for phase `parity` of `mbar`, giving up after `limit` clock cycles.
+// Non-blocking test of phase `parity` of `mbar`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *mbar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(ok)
+                 : "r"(smem_u32(mbar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Waits for phase `parity` of `mbar`, giving up after `limit` clock cycles.  A
+// limit of 0 or less tests the phase once without blocking (try_wait may itself
+// block for a while, so only test_wait makes a zero limit give up at once).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *mbar, uint32_t parity, long long limit)
 {
+    if (limit <= 0) return mbar_test_wait(mbar, parity);
     const long long t0 = clock64();
     while (!mbar_try_wait(mbar, parity))
         if (clock64() - t0 > limit) return false;

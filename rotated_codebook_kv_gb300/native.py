@@ -14,7 +14,8 @@ import threading
 from . import build as _build
 
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_OOM = range(5)
-TQ_DEVERR_SLOT_RANGE, TQ_DEVERR_BLOCK_RANGE, TQ_DEVERR_SEQ_RANGE = 0x1, 0x2, 0x4
+TQ_DEVERR_SLOT_RANGE, TQ_DEVERR_BLOCK_RANGE, TQ_DEVERR_SEQ_RANGE, TQ_DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+TQ_DEFAULT_WAIT_LIMIT = 2000000000
 
 # Every symbol include/tq.h declares, with (restype, argtypes).
 _c = ctypes
@@ -31,6 +32,7 @@ SIGNATURES = {
                                    _vp, _sz, _vp, _vp]),
     "tq_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
                                           _i32, _vp, _vp]),
+    "tq_set_wait_limit": (_i32, [_vp, _i64]),
     "tq_get_status": (_i32, [_vp, _c.POINTER(_c.c_uint32), _vp]),
     "tq_export_params": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "tq_last_error": (_c.c_char_p, []),
@@ -126,6 +128,10 @@ def tq_decode_attention_static(h, q, k_cache, v_cache, block_table, seq_lens, ba
     _check("tq_decode_attention_static", load().tq_decode_attention_static(
         h, q, k_cache, v_cache, block_table, seq_lens, batch, num_q_heads, num_kv_heads, page_size,
         max_blocks_per_seq, num_blocks, sm_scale, splits, out, stream))
+
+
+def tq_set_wait_limit(h, cycles: int) -> None:
+    _check("tq_set_wait_limit", load().tq_set_wait_limit(h, cycles))
 
 
 def tq_get_status(h, stream) -> int:

@@ -392,3 +392,35 @@ def test_full_wide_head_decode():
 @pytest.mark.parametrize("layer", range(8))
 def test_full_long_context_mixed(layer):
     _full_case(W.long_context_mixed(), layer, n_rows=1500, n_jobs=3)
+
+
+# --------------------------------------------------------------------------- #
+# Barrier waits that run out                                                    #
+# --------------------------------------------------------------------------- #
+
+def test_wait_timeouts_report_and_recover():
+    """With a wait limit of 0 every barrier wait tests once and gives up if its
+    phase has not completed: the first page-copy wait of each decode warp and the
+    first hand-off wait of each compress CTA certainly have not.  The kernels must
+    set TQ_DEVERR_TIMEOUT, wind down (copies and tensor-core work in flight are
+    drained with their own bound) and leave the context usable: with the default
+    limit restored, both calls give the normal results again.  No wait is made to
+    hang: nothing here blocks longer than the fixed drain bound."""
+    from rotated_codebook_kv_gb300 import native
+    w = SMALL["paged_decode_small"]
+    b = W.generate(w, device=DEV)
+    codec, _ = _codec_pair(w)
+    kc, vc = _compress(codec, w, b)
+    ref = _decode_gpu(codec, w, b, kc, vc)
+    codec.set_wait_limit(0)
+    out = _decode_gpu(codec, w, b, kc, vc)
+    assert codec.get_status() & native.TQ_DEVERR_TIMEOUT
+    assert np.all(np.isfinite(O.bf16_to_double(out)))
+    kc2, vc2 = codec.alloc_cache(b.num_blocks, w.num_kv_heads, w.page_size, fill=0xA5)
+    codec.compress_kv(b.k, b.v, b.slot_mapping, kc2, vc2, w.page_size, b.num_blocks)
+    assert codec.get_status() & native.TQ_DEVERR_TIMEOUT
+    codec.set_wait_limit(native.TQ_DEFAULT_WAIT_LIMIT)
+    assert np.array_equal(_decode_gpu(codec, w, b, kc, vc), ref)
+    kc3, vc3 = _compress(codec, w, b)
+    assert codec.get_status() == 0
+    assert torch.equal(kc3, kc) and torch.equal(vc3, vc)
