@@ -100,8 +100,12 @@ struct DecSmem {
     static constexpr int kPairBits = 2 * KB;
     static constexpr int kPairEntries = 1 << kPairBits;
     // [entry][copies] (hi pair, lo pair).  2-bit codes: 16 entries fill the 32 banks
-    // once, so lookups never conflict.  3- and 4-bit codes: 4 copies (lane & 3).
-    static constexpr int kLutCopies = (KB == 2) ? 1 : 4;
+    // once, so lookups never conflict.  3-bit codes: 16 copies, lane l reading copy
+    // l % 16, so the 16 lanes of a 64-bit wavefront read 16 different bank pairs;
+    // 4-bit codes: 4 copies at d = 128 (8 KB, so that four CTAs still fit an SM)
+    // and 8 at d = 256 (two CTAs per SM).
+    static constexpr int kLutCopies = (KB == 2) ? 1 : (KB == 3 ? 16 : (D == 256 ? 8 : 4));
+    static constexpr int kLutShift = (KB == 2) ? 3 : (KB == 3 ? 7 : (D == 256 ? 6 : 5));  // log2(entry bytes, all copies)
     static constexpr size_t kLut = sizeof(uint2) * kPairEntries * kLutCopies;  // a multiple of 128
     static constexpr size_t kSignLut = sizeof(uint2) * 16;               // 4 sign bits -> two +-1 fp16 pairs
     static constexpr size_t kQfrag = sizeof(uint4) * (D / 16) * 32;      // [k-step][lane] (qh0, qh2, ql0, ql2)
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     // 2-bit codes: code pair (4 quad, 4 quad + 1) / (4 quad + 2, 4 quad + 3) of a k-step word
     // rotated to bits 3..6 is the byte offset of its table entry
     const int rot0 = (8 * quad + 29) & 31, rot1 = (8 * quad + 1) & 31;
-    const uint32_t lut_lane = 8u * (lane & 3);  // 3- and 4-bit codes: this lane's table copy
+    const uint32_t lut_lane = 8u * (lane & (SM::kLutCopies - 1));  // 3- and 4-bit codes: this lane's table copy
     const uint32_t slut_off = static_cast<uint32_t>(SM::kLut);
     const int mt_mask = (C.group >> 4) - 1;     // m-tiles per value group - 1
     // value codes of coordinates 16 mt + 2 row (+1): byte (2-bit) or nibble pair (4-bit) of the row
@@ -400,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
                             e[hh][1] = ld64(__funnelshift_r(w, w, rot1) & 0x78u);
                         } else {
                             const uint32_t f = code_quad_off<KB>(ld32, krow[j][hh], s, quad);
-                            e[hh][0] = ld64(lut_lane + ((f & PM) << 5));
-                            e[hh][1] = ld64(lut_lane + (((f >> (2 * KB)) & PM) << 5));
+                            e[hh][0] = ld64(lut_lane + ((f & PM) << SM::kLutShift));
+                            e[hh][1] = ld64(lut_lane + (((f >> (2 * KB)) & PM) << SM::kLutShift));
                         }
                     }
                     // M rows r / r + 8 = high / low centroid parts of one token: each table load
