@@ -428,10 +428,11 @@ def per_config(dev, peak, reps):
         return statistics.median(ms) * 1e-3
 
     out = {}
-    for name, w in (("compress_only", W.compress_only()), ("paged_decode", W.paged_decode()),
-                    ("wide_head_decode", W.wide_head_decode())):
+    for name, w, rot in (("compress_only", W.compress_only(), 0), ("paged_decode", W.paged_decode(), 0),
+                         ("wide_head_decode", W.wide_head_decode(), 0),
+                         ("wide_head_decode_hadamard", W.wide_head_decode(), 1)):
         b = W.generate(w, device=dev)
-        codec = Codec(w.head_dim, w.k_bits, w.v_bits, w.group, w.codec_seed())
+        codec = Codec(w.head_dim, w.k_bits, w.v_bits, w.group, w.codec_seed(), rotation=rot)
         kc, vc = codec.alloc_cache(b.num_blocks, w.num_kv_heads, w.page_size, device=dev)
         T = b.num_tokens
         t_c = timed(lambda: codec.compress_kv(b.k, b.v, b.slot_mapping, kc, vc, w.page_size, b.num_blocks,
@@ -460,6 +461,7 @@ def per_config(dev, peak, reps):
         del b, kc, vc, codec
         torch.cuda.empty_cache()
     out["timing"] = f"median of {reps} calls after 2 warm-up calls; L2 flushed before each call"
+    out["wide_head_decode_hadamard"]["rotation"] = "randomized Hadamard (tq_init_rotation)"
     return out
 
 

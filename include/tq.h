@@ -85,6 +85,23 @@ typedef enum {
  */
 tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed, tq_handle *out);
 
+/*
+ * tq_init_rotation -- tq_init with a choice of rotation Pi:
+ *   TQ_ROTATION_DENSE     the Haar rotation described above (what tq_init builds);
+ *   TQ_ROTATION_HADAMARD  a randomized Hadamard rotation Pi = H D / sqrt(d)
+ *     (turbo-attn, "How it works", step 1: a fast Walsh-Hadamard transform), with
+ *     H the Sylvester Hadamard matrix, H[i][j] = (-1)^popcount(i & j), and
+ *     D = diag(s), s_j = -1 when the top bit of the j-th output of SplitMix64
+ *     stream 0 (the stream the dense rotation draws from) is set, else +1.
+ * Everything else -- S, the codebook, the records, decode -- is unchanged; the
+ * rotation is applied by butterflies instead of a dense product where that pays
+ * (key compression at head_dim 256).
+ */
+#define TQ_ROTATION_DENSE 0
+#define TQ_ROTATION_HADAMARD 1
+tq_status tq_init_rotation(int head_dim, int k_bits, int v_bits, int group, uint64_t seed, int rotation,
+                           tq_handle *out);
+
 /* Frees the handle's device tables.  Accepts NULL. */
 tq_status tq_destroy(tq_handle h);
 

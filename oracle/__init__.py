@@ -63,6 +63,9 @@ def _load():
             "tq_or_create": (vp, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64]),
             "tq_or_create2": (vp, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
                                    ctypes.c_uint64]),
+            "tq_or_create3": (vp, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
+                                   ctypes.c_uint64, ctypes.c_int]),
+            "tq_or_hadamard_rotation": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint64, dp]),
             "tq_or_destroy": (None, [vp]),
             "tq_or_get_params": (None, [vp, dp, dp, dp, dp]),
             "tq_or_geometry": (None, [vp, ctypes.c_int, i64p]),
@@ -113,6 +116,13 @@ def gaussians(seed: int, stream: int, n: int) -> np.ndarray:
 def rotation(d: int, seed: int) -> np.ndarray:
     out = np.zeros((d, d), dtype=np.float64)
     rc = _load().tq_or_rotation(d, ctypes.c_uint64(seed), _ptr(out, ctypes.c_double))
+    assert rc == 0
+    return out
+
+
+def hadamard_rotation(d: int, seed: int) -> np.ndarray:
+    out = np.zeros((d, d), dtype=np.float64)
+    rc = _load().tq_or_hadamard_rotation(d, ctypes.c_uint64(seed), _ptr(out, ctypes.c_double))
     assert rc == 0
     return out
 
@@ -180,14 +190,15 @@ class Oracle:
     QJL is on iff ``k_bits <= 3``.
     """
 
+    ROTATION_DENSE, ROTATION_HADAMARD = 0, 1
+
     def __init__(self, head_dim: int, k_bits: int, v_bits: int, group: int, seed: int,
-                 qjl_seed: int | None = None):
+                 qjl_seed: int | None = None, rotation: int = 0):
         self._lib = _load()
-        if qjl_seed is None:
-            self._h = self._lib.tq_or_create(head_dim, k_bits, v_bits, group, ctypes.c_uint64(seed))
-        else:  # separate S seed: only for Monte-Carlo checks of the QJL estimator
-            self._h = self._lib.tq_or_create2(head_dim, k_bits, v_bits, group, ctypes.c_uint64(seed),
-                                              ctypes.c_uint64(qjl_seed))
+        # a separate S seed is only for Monte-Carlo checks of the QJL estimator
+        self._h = self._lib.tq_or_create3(head_dim, k_bits, v_bits, group, ctypes.c_uint64(seed),
+                                          ctypes.c_uint64(seed if qjl_seed is None else qjl_seed), rotation)
+        self.rotation = rotation
         if not self._h:
             raise ValueError("unsupported oracle parameters")
         self.d, self.k_bits, self.v_bits, self.group, self.seed = head_dim, k_bits, v_bits, group, seed

@@ -281,16 +281,50 @@ typedef struct or_ctx {
     int kcode, ksign, vcode, vmeta;
 } or_ctx;
 
+/*
+ * O2': randomized Hadamard rotation ([turbo-attn] "How it works", step 1: a
+ * fast Walsh-Hadamard transform).  Pi = H diag(s) / sqrt(d), H the Hadamard
+ * matrix of Sylvester's construction (H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]]),
+ * s_j = -1 when the top bit of the j-th raw output of SplitMix64 stream 0 is
+ * set, else +1 (the pages name no sign source: this stream is the reading).
+ * d must be a power of two.
+ */
+int tq_or_hadamard_rotation(int d, uint64_t seed, double *Pi)
+{
+    if (d <= 0 || (d & (d - 1))) return -1;
+    double *H = malloc(sizeof(double) * d * d);
+    if (!H) return -1;
+    H[0] = 1.0;
+    for (int n = 1; n < d; n *= 2) /* grow H_n (top-left n x n) into H_2n */
+        for (int i = 0; i < n; ++i)
+            for (int j = 0; j < n; ++j) {
+                double h = H[i * d + j];
+                H[i * d + (j + n)] = h;
+                H[(i + n) * d + j] = h;
+                H[(i + n) * d + (j + n)] = -h;
+            }
+    uint64_t state = seed ^ 0x9E3779B97F4A7C15ULL; /* stream 0 */
+    double inv = 1.0 / sqrt((double)d);
+    for (int j = 0; j < d; ++j) {
+        double sj = (or_splitmix64(&state) >> 63) ? -1.0 : 1.0;
+        for (int i = 0; i < d; ++i) Pi[i * d + j] = H[i * d + j] * sj * inv;
+    }
+    free(H);
+    return 0;
+}
+
 /* QJL is used iff k_bits <= 3 (one sign bit per coordinate, m = d).
- * Pi comes from seed_rot, S from seed_qjl; the codec uses one seed for both. */
-or_ctx *tq_or_create2(int d, int kb, int vb, int g, uint64_t seed_rot, uint64_t seed_qjl)
+ * Pi comes from seed_rot, S from seed_qjl; the codec uses one seed for both.
+ * rotation 0 is the Haar rotation (O2), 1 the randomized Hadamard one (O2'). */
+or_ctx *tq_or_create3(int d, int kb, int vb, int g, uint64_t seed_rot, uint64_t seed_qjl, int rotation)
 {
     if (d <= 0 || d % 8 || kb < 1 || kb > 4 || vb < 1 || vb > 8 || g <= 0 || d % g) return NULL;
     or_ctx *c = calloc(1, sizeof(or_ctx));
     c->d = d; c->kb = kb; c->vb = vb; c->g = g; c->qjl = kb <= 3;
     c->Pi = malloc(sizeof(double) * d * d);
     c->S = malloc(sizeof(double) * d * d);
-    if (tq_or_rotation(d, seed_rot, c->Pi) != 0 || tq_or_codebook(kb, c->cent, c->thr) < 0) {
+    int rc = rotation == 1 ? tq_or_hadamard_rotation(d, seed_rot, c->Pi) : tq_or_rotation(d, seed_rot, c->Pi);
+    if (rc != 0 || tq_or_codebook(kb, c->cent, c->thr) < 0) {
         free(c->Pi); free(c->S); free(c);
         return NULL;
     }
@@ -302,9 +336,14 @@ or_ctx *tq_or_create2(int d, int kb, int vb, int g, uint64_t seed_rot, uint64_t 
     return c;
 }
 
+or_ctx *tq_or_create2(int d, int kb, int vb, int g, uint64_t seed_rot, uint64_t seed_qjl)
+{
+    return tq_or_create3(d, kb, vb, g, seed_rot, seed_qjl, 0);
+}
+
 or_ctx *tq_or_create(int d, int kb, int vb, int g, uint64_t seed)
 {
-    return tq_or_create2(d, kb, vb, g, seed, seed);
+    return tq_or_create3(d, kb, vb, g, seed, seed, 0);
 }
 
 void tq_or_destroy(or_ctx *c)

@@ -28,10 +28,12 @@ def _stream(stream) -> int:
 class Codec:
     """One set of codec tables (Pi, S, codebook) on the current device."""
 
-    def __init__(self, head_dim: int, k_bits: int, v_bits: int, group: int, seed: int = 0):
+    def __init__(self, head_dim: int, k_bits: int, v_bits: int, group: int, seed: int = 0, rotation: int = 0):
+        """rotation: native.TQ_ROTATION_DENSE (Haar) or native.TQ_ROTATION_HADAMARD."""
         self.head_dim, self.k_bits, self.v_bits, self.group, self.seed = head_dim, k_bits, v_bits, group, seed
         self.qjl = k_bits <= 3
-        self.handle = native.tq_init(head_dim, k_bits, v_bits, group, seed)
+        self.rotation = rotation
+        self.handle = native.tq_init_rotation(head_dim, k_bits, v_bits, group, seed, rotation)
 
     def close(self):
         if getattr(self, "handle", None):

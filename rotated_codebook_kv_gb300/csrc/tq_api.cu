@@ -86,8 +86,17 @@ const char *tq_last_error(void) { return g_last_error.c_str(); }
 
 tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed, tq_handle *out)
 {
+    return tq_init_rotation(head_dim, k_bits, v_bits, group, seed, TQ_ROTATION_DENSE, out);
+}
+
+tq_status tq_init_rotation(int head_dim, int k_bits, int v_bits, int group, uint64_t seed, int rotation,
+                           tq_handle *out)
+{
     if (!out) return fail(TQ_ERR_INVALID_ARG, "tq_init: out is NULL");
     *out = nullptr;
+    if (rotation != TQ_ROTATION_DENSE && rotation != TQ_ROTATION_HADAMARD)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_init: rotation %d is neither TQ_ROTATION_DENSE nor TQ_ROTATION_HADAMARD",
+                    rotation);
     if (head_dim != 128 && head_dim != 256)
         return fail(TQ_ERR_UNSUPPORTED, "tq_init: head_dim %d not in {128, 256}", head_dim);
     if (!supported_bits(k_bits) || !supported_bits(v_bits))
@@ -96,7 +105,7 @@ tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed
         return fail(TQ_ERR_UNSUPPORTED, "tq_init: group %d not in {32, 64, 128} or does not divide %d", group,
                     head_dim);
     tq::HostTables ht;
-    if (!tq::build_tables(head_dim, k_bits, seed, &ht))
+    if (!tq::build_tables(head_dim, k_bits, seed, rotation, &ht))
         return fail(TQ_ERR_CUDA, "tq_init: Lloyd-Max iteration did not converge");
 
     const int d = head_dim;
@@ -104,7 +113,9 @@ tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed
     // fp32 tables: Pi, Pi^T, S, S^T, M_hi, M_lo (M = S Pi in double), then the
     // fp16 tensor-core operand image (d = 128) and the status word.
     const size_t img_bytes = (d == 128) ? 4 * dd * sizeof(uint16_t) : 0;
-    std::vector<float> host(6 * dd);
+    const size_t nf = 6 * dd + static_cast<size_t>(d);  // six d x d tables, then the Hadamard signs
+    std::vector<float> host(nf);
+    for (int j = 0; j < d; ++j) host[6 * dd + j] = static_cast<float>(ht.hsign[j]);
     for (int i = 0; i < d; ++i)
         for (int j = 0; j < d; ++j) {
             const size_t a = static_cast<size_t>(i) * d + j, t = static_cast<size_t>(j) * d + i;
@@ -148,14 +159,14 @@ tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed
         delete c;
         return cuda_fail(e, "tq_init: cudaGetSymbolAddress of the static decode scratch");
     }
-    e = cudaMalloc(&c->dev_tables, 6 * dd * sizeof(float) + img_bytes + 256);
+    e = cudaMalloc(&c->dev_tables, nf * sizeof(float) + img_bytes + 256);
     if (e != cudaSuccess) {
         delete c;
         return fail(TQ_ERR_OOM, "tq_init: cudaMalloc: %s", cudaGetErrorString(e));
     }
     float *base = static_cast<float *>(c->dev_tables);
-    e = cudaMemcpy(base, host.data(), 6 * dd * sizeof(float), cudaMemcpyHostToDevice);
-    char *img_dev = reinterpret_cast<char *>(base + 6 * dd);
+    e = cudaMemcpy(base, host.data(), nf * sizeof(float), cudaMemcpyHostToDevice);
+    char *img_dev = reinterpret_cast<char *>(base + nf);
     if (e == cudaSuccess && img_bytes) e = cudaMemcpy(img_dev, img.data(), img_bytes, cudaMemcpyHostToDevice);
     unsigned *status = reinterpret_cast<unsigned *>(img_dev + img_bytes);
     if (e == cudaSuccess) e = cudaMemset(status, 0, 256);
@@ -185,6 +196,8 @@ tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed
     k.M_hi = base + 4 * dd;
     k.M_lo = base + 5 * dd;
     k.tc_image = img_bytes ? img_dev : nullptr;
+    k.hsign = base + 6 * dd;
+    k.rotation = rotation;
     k.status = status;
     k.wait_limit = tq::kDefaultWaitLimit;
     k.num_sms = c->num_sms;

@@ -77,6 +77,56 @@ __device__ __forceinline__ void matvec_rows(const float *__restrict__ W, const f
     for (int rr = 0; rr < RPT; ++rr) Y[(rg + rr * CG) * D + i] = acc[rr];
 }
 
+// Hadamard rotation of TM rows (turbo-attn, "How it works", step 1):
+// Y[row] = H (s * X[row]) / sqrt(D) with H the Sylvester Hadamard matrix, by the
+// fast Walsh-Hadamard butterfly.  One warp per row; lane l holds the E = D / 32
+// consecutive elements E l .. E l + E - 1, so the first log2(E) stages stay in
+// registers and the last five pair lanes l and l ^ h by shuffles.  Every stage
+// is a sum or a difference of two fp32 values (the bf16 keys enter exactly).
+template <int D, int TM>
+__device__ __forceinline__ void fwht_rows(const float *__restrict__ hsign, const float *X, float *Y)
+{
+    constexpr int E = D / 32;
+    const float inv = static_cast<float>(1.0 / __dsqrt_rn(static_cast<double>(D)));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float sg[E];
+#pragma unroll
+    for (int m = 0; m < E; ++m) sg[m] = __ldg(hsign + E * lane + m);
+    for (int row = warp; row < TM; row += kWarps) {
+        float x[E];
+#pragma unroll
+        for (int m = 0; m < E; m += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(X + row * D + E * lane + m);
+            x[m] = v.x * sg[m];
+            x[m + 1] = v.y * sg[m + 1];
+            x[m + 2] = v.z * sg[m + 2];
+            x[m + 3] = v.w * sg[m + 3];
+        }
+#pragma unroll
+        for (int h = 1; h < E; h <<= 1)
+#pragma unroll
+            for (int m = 0; m < E; ++m)
+                if (!(m & h)) {
+                    const float a = x[m], b = x[m + h];
+                    x[m] = a + b;
+                    x[m + h] = a - b;
+                }
+#pragma unroll
+        for (int h = 1; h < 32; h <<= 1) {
+            const bool upper = (lane & h) != 0;
+#pragma unroll
+            for (int m = 0; m < E; ++m) {
+                const float y = __shfl_xor_sync(0xffffffffu, x[m], h);
+                x[m] = upper ? (y - x[m]) : (x[m] + y);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < E; m += 4)
+            *reinterpret_cast<float4 *>(Y + row * D + E * lane + m) =
+                make_float4(x[m] * inv, x[m + 1] * inv, x[m + 2] * inv, x[m + 3] * inv);
+    }
+}
+
 // Exact path for one key row, run by one warp.  Writes the row's codes, its
 // QJL projections (sign-exact) into p_out, and the bf16 norm / gamma.
 template <int D>
@@ -172,8 +222,8 @@ __device__ void precise_key_row(const Codec &C, const uint16_t *__restrict__ src
     __syncwarp();
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads)
+template <int D, bool HAD>
+__global__ void __launch_bounds__(kThreads, 2)
 compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
                 int64_t rows, int Hkv, int64_t ks, int64_t vs, const int64_t *__restrict__ slots,
                 uint8_t *__restrict__ kc, uint8_t *__restrict__ vc, int64_t num_blocks)
@@ -192,10 +242,15 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     __shared__ int s_off[TM];
     __shared__ int s_flag[TM];  // 0 fast, 1 exact path, 2 zero key
     __shared__ uint16_t s_n16[TM], s_g16[TM];
+    __shared__ float s_thr[18];   // -inf, thresholds ascending, +inf (codes by binary search)
+    __shared__ float s_cent[16];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * TM;
     const float sqrtd = sqrtf(static_cast<float>(D));
+    const int nthr = (1 << C.k_bits) - 1;
+    if (tid < 18) s_thr[tid] = tid == 0 ? -INFINITY : (tid <= nthr ? C.thresholds[tid - 1] : INFINITY);
+    if (tid < 16) s_cent[tid] = C.centroids[tid];
 
     if (tid < TM) {
         const int64_t r = r0 + tid;
@@ -258,24 +313,25 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         }
     }
     // ---- rotation: yb = Pi k (unnormalised) -----------------------------------
-    matvec_rows<D, TM>(C.PiT, kf, yb);
+    if constexpr (HAD) fwht_rows<D, TM>(C.hsign, kf, yb);
+    else matvec_rows<D, TM>(C.PiT, kf, yb);
     __syncthreads();
     // ---- codes, guard band, residual -----------------------------------------
-    const int nthr = (1 << C.k_bits) - 1;
+    // code = #{t : threshold_t <= z} by a binary search over the sorted thresholds
+    // (s_thr[c + 1] is threshold c); the distance to the nearest threshold is to
+    // one of the two that bracket z
+    const int kb = C.k_bits;
     for (int e = tid; e < TM * D; e += kThreads) {
         const int row = e / D, i = e - row * D;
         const int fl = s_flag[row];
         const float z = yb[e] * s_scale[row];
         int code = 0;
-        float dmin = INFINITY;
-        for (int t = 0; t < nthr; ++t) {
-            const float th = C.thresholds[t];
-            code += (th <= z);
-            dmin = fminf(dmin, fabsf(z - th));
-        }
+        for (int step = 1 << (kb - 1); step > 0; step >>= 1)
+            if (s_thr[code + step] <= z) code += step;
+        const float dmin = fminf(z - s_thr[code], s_thr[code + 1] - z);
         if (fl == 2) code = 0;
         codes[row * CS + i] = static_cast<uint8_t>(code);
-        yb[e] = (fl == 2) ? 0.f : z - C.centroids[code];
+        yb[e] = (fl == 2) ? 0.f : z - s_cent[code];
         if (fl == 0 && dmin < kCodeGuard) s_flag[row] = 1;
     }
     __syncthreads();
@@ -404,25 +460,17 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     }
 }
 
-template <int D>
+template <int D, bool HAD>
 cudaError_t launch_compress_d(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
                               int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
                               int64_t num_blocks, cudaStream_t st)
 {
     const size_t smem = CompressSmem<D>::kBytes;
-    static bool attr_set[64] = {};  // the attribute is per device
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(compress_kernel<D, HAD>), smem);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(compress_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
     const int64_t rows = T * Hkv;
     const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-    compress_kernel<D><<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(c, pg, k, v, rows, Hkv, ks, vs, slots,
+    compress_kernel<D, HAD><<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(c, pg, k, v, rows, Hkv, ks, vs, slots,
                                                                              kc, vc, num_blocks);
     return cudaGetLastError();
 }
@@ -434,7 +482,9 @@ cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *
                             int64_t num_blocks, cudaStream_t st)
 {
     if (c.d == 128) return launch_compress_tc(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, c.num_sms, st);
-    return launch_compress_d<256>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+    if (c.rotation == TQ_ROTATION_HADAMARD)
+        return launch_compress_d<256, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+    return launch_compress_d<256, false>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
 }
 
 }  // namespace tq

@@ -16,8 +16,9 @@ tq_status api_error(tq_status s, const char *fmt, ...);
 // Host tables in double, built by tq_params.cpp.
 struct HostTables {
     std::vector<double> Pi, S, centroids, thresholds;
+    std::vector<double> hsign;  // Hadamard rotation: the random signs D (all +1 for the dense rotation)
 };
-bool build_tables(int d, int k_bits, uint64_t seed, HostTables *out);
+bool build_tables(int d, int k_bits, uint64_t seed, int rotation, HostTables *out);
 bool build_codebook(int bits, double *centroids, double *thresholds);
 
 // Codec constants, passed by value to every kernel.
@@ -33,6 +34,8 @@ struct Codec {
     const float *M_hi;     // [d][d] M = S Pi (double) as hi + lo fp32, row-major
     const float *M_lo;
     const void *tc_image;  // d = 128: fp16 tensor-core operands (Pi 2^10 hi/lo, S 2^12 hi/lo), core-matrix layout
+    const float *hsign;    // [d] random signs of the Hadamard rotation (Pi = H diag(hsign) / sqrt(d))
+    int rotation;          // TQ_ROTATION_DENSE or TQ_ROTATION_HADAMARD
     unsigned int *status;  // device status word (TQ_DEVERR_* bits)
     long long wait_limit;  // clock cycles a kernel waits on one barrier before it reports TQ_DEVERR_TIMEOUT
     int num_sms;

@@ -19,6 +19,12 @@
 // r cos(2 pi u2), r sin(2 pi u2) with r = sqrt(-2 ln u1).  Matrices fill
 // row-major.
 //
+// Randomized Hadamard rotation (turbo-attn, "How it works", step 1: a fast
+// Walsh-Hadamard transform): Pi = H D / sqrt(d), H the Sylvester Hadamard
+// matrix H[i][j] = (-1)^popcount(i & j) and D = diag(s_j) with random signs
+// s_j = -1 when the top bit of the j-th output of SplitMix64 stream 0 is set.
+// Pi is orthogonal and y = Pi k costs an O(d log d) butterfly.
+//
 // Codebook: the Lloyd-Max quantiser of N(0,1) (brightcoding blog: Lloyd-Max is
 // optimal for Gaussian sources; 0xsero/turboquant "Compression Pipeline":
 // Lloyd-Max scalar codebooks) found by the Lloyd fixed-point iteration.
@@ -87,6 +93,25 @@ std::vector<double> haar_rotation(int d, uint64_t seed)
     return Q;
 }
 
+std::vector<double> hadamard_signs(int d, uint64_t seed)
+{
+    SplitMix64 rng{seed ^ 0x9E3779B97F4A7C15ULL};  // stream 0
+    std::vector<double> sg(d);
+    for (int j = 0; j < d; ++j) sg[j] = (rng.next() >> 63) ? -1.0 : 1.0;
+    return sg;
+}
+
+std::vector<double> hadamard_rotation(int d, uint64_t seed)
+{
+    const std::vector<double> sg = hadamard_signs(d, seed);
+    const double inv = 1.0 / std::sqrt(static_cast<double>(d));
+    std::vector<double> Q(static_cast<size_t>(d) * d);
+    for (int i = 0; i < d; ++i)
+        for (int j = 0; j < d; ++j)
+            Q[static_cast<size_t>(i) * d + j] = ((__builtin_popcount(static_cast<unsigned>(i & j)) & 1) ? -inv : inv) * sg[j];
+    return Q;
+}
+
 double std_normal_pdf(double x) { return std::isinf(x) ? 0.0 : std::exp(-0.5 * x * x) * 0.3989422804014327; }
 
 // Upper-tail probability Q(x) = P(X > x).
@@ -126,9 +151,15 @@ bool build_codebook(int bits, double *centroids, double *thresholds)
     return false;
 }
 
-bool build_tables(int d, int k_bits, uint64_t seed, HostTables *out)
+bool build_tables(int d, int k_bits, uint64_t seed, int rotation, HostTables *out)
 {
-    out->Pi = haar_rotation(d, seed);
+    if (rotation == TQ_ROTATION_HADAMARD) {
+        out->Pi = hadamard_rotation(d, seed);
+        out->hsign = hadamard_signs(d, seed);
+    } else {
+        out->Pi = haar_rotation(d, seed);
+        out->hsign.assign(d, 1.0);
+    }
     out->S = gaussian_matrix(d, seed, 1);
     out->centroids.assign(1 << k_bits, 0.0);
     out->thresholds.assign((1 << k_bits) - 1, 0.0);

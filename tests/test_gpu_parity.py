@@ -424,3 +424,39 @@ def test_wait_timeouts_report_and_recover():
     kc3, vc3 = _compress(codec, w, b)
     assert codec.get_status() == 0
     assert torch.equal(kc3, kc) and torch.equal(vc3, vc)
+
+
+# --------------------------------------------------------------------------- #
+# Randomized Hadamard rotation                                                  #
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("d,kb,vb,g,P,G", [(128, 3, 2, 32, 16, 4), (128, 4, 4, 64, 16, 8), (256, 4, 4, 64, 32, 2),
+                                           (256, 2, 3, 32, 16, 3), (256, 3, 2, 128, 32, 1)])
+def test_hadamard_rotation(d, kb, vb, g, P, G):
+    """The same records, decode and dequant with Pi = H D / sqrt(d): at head_dim 128
+    through the tensor-core kernel (Pi as its B operand), at 256 through the
+    butterfly kernel; the rotation tables equal the oracle's."""
+    from rotated_codebook_kv_gb300 import native
+    Hkv = 2
+    w = W.Workload("hadamard", d, kb, vb, g, P, num_kv_heads=Hkv, num_q_heads=Hkv * G, batch=3,
+                   seq_len_range=(200, 700), seed=d + kb)
+    b = W.generate(w, device="cpu")
+    b = W.Batch(**{f: (getattr(b, f).to(DEV) if isinstance(getattr(b, f), torch.Tensor) else getattr(b, f))
+                   for f in b.__dataclass_fields__})
+    codec = Codec(d, kb, vb, g, w.codec_seed(), rotation=native.TQ_ROTATION_HADAMARD)
+    ora = O.Oracle(d, kb, vb, g, w.codec_seed(), rotation=O.Oracle.ROTATION_HADAMARD)
+    lib, ref = codec.export_params(), ora.params()
+    assert np.all(np.abs(lib["Pi"].astype(np.float64) - ref["Pi"]) <= np.abs(ref["Pi"]) * 2.0 ** -24)
+    kc, vc = _compress(codec, w, b)
+    assert codec.get_status() == 0
+    _check_rows(ora, w, b, kc, vc)
+    kc_np, vc_np = kc.cpu().numpy(), vc.cpu().numpy()
+    check_decode(_decode_gpu(codec, w, b, kc, vc), _decode_oracle(ora, w, b, kc_np, vc_np))
+    slots = b.slot_mapping[::7].contiguous()
+    ko, vo = codec.dequant_kv(kc, vc, P, b.num_blocks, Hkv, slots)
+    torch.cuda.synchronize()
+    rk, _ = ora.dequant_slots(kc_np, vc_np, P, Hkv, slots.cpu().numpy())
+    gk = O.bf16_to_double(W.as_u16(ko))
+    ax = np.abs(rk)
+    ulp = 2.0 ** (np.floor(np.log2(np.where(ax > 0, ax, 1.0))) - 7)
+    assert np.all(np.abs(gk - rk) <= ulp + 1e-5)

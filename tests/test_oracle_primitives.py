@@ -208,3 +208,52 @@ def test_pack_byte_patterns():
     assert list(O.pack(codes, 3)) == [bits & 0xFF, (bits >> 8) & 0xFF, (bits >> 16) & 0xFF]
     # sign bits: bit i of byte i // 8
     assert list(O.pack([1, 0, 0, 0, 0, 0, 0, 1, 0, 1, 0, 0, 0, 0, 0, 0], 1)) == [0x81, 0x02]
+
+
+# --------------------------------------------------------------------------- #
+# Randomized Hadamard rotation                                                  #
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("d,seed", [(128, 0), (256, 7), (64, 123)])
+def test_hadamard_rotation_matches_scipy(d, seed):
+    """Pi = H diag(s) / sqrt(d): H from scipy's Sylvester construction, s_j the sign
+    of the top bit of the j-th raw output of SplitMix64 stream 0 (pinned above)."""
+    from scipy.linalg import hadamard
+    raw = O.splitmix64(seed ^ 0x9E3779B97F4A7C15, d)
+    s = np.where(raw >> np.uint64(63), -1.0, 1.0)
+    want = hadamard(d).astype(np.float64) * s[None, :] / np.sqrt(d)
+    got = O.hadamard_rotation(d, seed)
+    assert np.array_equal(got, want)
+    assert np.abs(got.T @ got - np.eye(d)).max() < 1e-12
+
+
+def test_hadamard_rotation_is_a_butterfly():
+    """Pi x equals the fast Walsh-Hadamard butterfly of s * x, divided by sqrt(d)."""
+    d, seed = 256, 3
+    Pi = O.hadamard_rotation(d, seed)
+    s = np.sign(Pi[0]) * 1.0  # row 0 of H is all ones: its signs are s
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal(d)
+    y = (s * x).copy()
+    h = 1
+    while h < d:
+        for i in range(0, d, 2 * h):
+            a, b = y[i:i + h].copy(), y[i + h:i + 2 * h].copy()
+            y[i:i + h], y[i + h:i + 2 * h] = a + b, a - b
+        h *= 2
+    assert np.allclose(Pi @ x, y / np.sqrt(d), atol=1e-12)
+
+
+def test_hadamard_codebook_distortion():
+    """Keys rotated by the randomized Hadamard matrix have N(0,1)-like coordinates,
+    so the Lloyd-Max distortion of the codebook (J. Max 1960) is met as with the
+    Haar rotation."""
+    d, bits = 128, 3
+    ora = O.Oracle(d, bits, 4, 32, seed=1, rotation=1)
+    rng = np.random.default_rng(3)
+    k = O.bf16_from_double(rng.standard_normal((3000, d)))
+    rec = ora.compress_rows(k=k)
+    c = ora.params()["centroids"]
+    codes = np.stack([O.unpack(r, d, bits) for r in rec["k_code"]])
+    mse = np.mean((rec["z"] - c[codes]) ** 2)
+    assert abs(mse - 0.03454) < 0.05 * 0.03454
