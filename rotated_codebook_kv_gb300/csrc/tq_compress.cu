@@ -460,6 +460,263 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     }
 }
 
+// ---------------------------------------------------------------------------
+// Streaming kernel for the randomized Hadamard rotation without QJL (k_bits = 4):
+// one warp per token-head row, rows strided over all warps of the grid, the next
+// row's key, value and slot loaded while the current one is processed.  Lane l
+// holds the E = D / 32 consecutive coordinates E l .. E l + E - 1 of the key and
+// of the value, so the butterfly's first log2(E) stages stay in registers, its
+// last five pair lanes by shuffles, and the lane's E codes are E * b consecutive
+// bits of the record (b bytes at byte offset b l).  No shared-memory staging and
+// no block barrier: the kernel is a row pipeline bounded by HBM.
+// ---------------------------------------------------------------------------
+constexpr int kStreamWarps = 8;
+constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23: adding it rounds to an integer
+constexpr uint32_t kRoundBits = 0x4B400000u;
+
+template <int E>
+__device__ __forceinline__ void unpack_bf16(const uint32_t (&w)[E / 2], float (&x)[E])
+{
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// Codes of the lane's E values of one group shared by lpg lanes:
+// code = clamp(floor((x - zero) / scale + 1/2), 0, 2^VB - 1) with the group's fp16
+// scale = (max - min) / (2^VB - 1) and zero = min.  The rounding is one fused
+// multiply-add; a quotient within 4 ulps (2^-14) of a boundary n - 1/2 is
+// re-decided exactly (x - zero as an exact float pair against (n - 1/2) scale,
+// which is exact in fp32).  Groups whose zero is not their minimum exactly
+// (outside the fp16 normal range) or whose scale is subnormal decide every
+// element that way, with clamping.  Returns (scale | zero << 16) as fp16 bits.
+template <int E, int VB>
+__device__ __forceinline__ uint32_t quantize_values_lane(const float (&x)[E], int lpg, uint32_t &codes)
+{
+    constexpr int L = (1 << VB) - 1;
+    float mn = x[0], mx = x[0];
+#pragma unroll
+    for (int m = 1; m < E; ++m) {
+        mn = fminf(mn, x[m]);
+        mx = fmaxf(mx, x[m]);
+    }
+    for (int o = lpg >> 1; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    float dh, de;
+    two_sum(mx, -mn, dh, de);
+    // (max - min) / L with L in {3, 7, 15}: exact in fp32 or a non-terminating binary
+    // fraction, so rounding to fp32 first never lands on an fp16 midpoint; dh * (1/L)
+    // is within 2 ulps of dh / L, safe unless near a midpoint or below fp16 normals
+    const float qm = dh * (1.f / static_cast<float>(L));
+    const uint32_t qlow = __float_as_uint(qm) & 0x1FFFu;
+    const bool qsafe = de == 0.f && qm >= 6.103515625e-05f && (qlow + 4u - 0x1000u) > 8u;
+    __half s16;
+    if (qsafe) s16 = __float2half_rn(qm);
+    else if (de == 0.f) s16 = __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)));
+    else s16 = __double2half((static_cast<double>(mx) - static_cast<double>(mn)) / L);
+    const __half z16 = __float2half_rn(mn);
+    const float sv = __half2float(s16), zv = __half2float(z16);
+    float inv = 0.f;
+    if (sv != 0.f) asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sv));
+    const bool exact_all = zv != mn || (sv != 0.f && sv < 6.103515625e-05f);
+    codes = 0u;
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        uint32_t q;
+        if (!exact_all) {
+            const float dx = x[m] - zv;
+            q = __float_as_uint(fmaf(dx, inv, kRoundMagic)) - kRoundBits;
+            const uint32_t tb = __float_as_uint(fmaf(dx, inv, 192.5f + 4.f / 65536.f));
+            if ((tb & 0xFFF8u) == 0u) {
+                const uint32_t n = (tb >> 16) & 0x1Fu;
+                const float b = fmaf(static_cast<float>(n), sv, -0.5f * sv);
+                float a, ea;
+                two_sum(x[m], -zv, a, ea);
+                q = (__fadd_rn(__fsub_rn(a, b), ea) >= 0.f) ? n : n - 1u;
+            }
+        } else {
+            int qi = 0;
+            if (sv != 0.f) {
+                float a, ea;
+                two_sum(x[m], -zv, a, ea);
+                qi = static_cast<int>(fminf(fmaxf(floorf(fmaf(x[m] - zv, inv, 0.5f)), 0.f), static_cast<float>(L)));
+                while (qi < L && __fadd_rn(__fsub_rn(a, (qi + 0.5f) * sv), ea) >= 0.f) ++qi;
+                while (qi > 0 && !(__fadd_rn(__fsub_rn(a, (qi - 0.5f) * sv), ea) >= 0.f)) --qi;
+            }
+            q = static_cast<uint32_t>(qi);
+        }
+        codes |= q << (VB * m);
+    }
+    return static_cast<uint32_t>(__half_as_ushort(s16)) | (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
+}
+
+// Stores the lane's nbytes (2, 3 or 4) code bytes at p (aligned to nbytes when 2 or 4).
+__device__ __forceinline__ void store_code_bytes(uint8_t *p, uint32_t w, int nbytes)
+{
+    if (nbytes == 4) *reinterpret_cast<uint32_t *>(p) = w;
+    else if (nbytes == 2) *reinterpret_cast<uint16_t *>(p) = static_cast<uint16_t>(w);
+    else {
+        p[0] = static_cast<uint8_t>(w);
+        p[1] = static_cast<uint8_t>(w >> 8);
+        p[2] = static_cast<uint8_t>(w >> 16);
+    }
+}
+
+template <int D, int VB>
+__global__ void __launch_bounds__(kStreamWarps * 32, 3)
+compress_stream_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin,
+                       const uint16_t *__restrict__ vin, int64_t rows, int Hkv, int64_t ks, int64_t vs,
+                       const int64_t *__restrict__ slots, uint8_t *__restrict__ kc, uint8_t *__restrict__ vc,
+                       int64_t num_blocks)
+{
+    constexpr int E = D / 32;  // coordinates per lane
+    constexpr int KB = 4;      // no QJL
+    static_assert(E == 8, "head_dim 256: a lane's codes are whole bytes for every value width");
+    using Raw = uint4;
+    __shared__ float s_thr[18];  // -inf, thresholds ascending, +inf
+    __shared__ double s_scr[kStreamWarps][D];
+    __shared__ uint8_t s_codes[kStreamWarps][D];
+    __shared__ uint16_t s_n16[kStreamWarps], s_g16[kStreamWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nthr = (1 << KB) - 1;
+    if (threadIdx.x < 18)
+        s_thr[threadIdx.x] = threadIdx.x == 0 ? -INFINITY : (threadIdx.x <= nthr ? C.thresholds[threadIdx.x - 1] : INFINITY);
+    __syncthreads();
+    float sg[E];
+#pragma unroll
+    for (int m = 0; m < E; ++m) sg[m] = __ldg(C.hsign + E * lane + m);
+    const int hshift = (Hkv & (Hkv - 1)) == 0 ? __ffs(Hkv) - 1 : -1;
+    const int pshift = __ffs(G.P) - 1;
+    const int64_t cache_slots = num_blocks * G.P;
+    const int lpg = C.group / E;  // lanes per value group: 4, 8 or 16 at D = 256
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * kStreamWarps;
+    auto fetch = [&](int64_t r, Raw &k4, Raw &v4, int64_t &sl) {
+        const int64_t t = hshift >= 0 ? (r >> hshift) : r / Hkv;
+        const int64_t h = r - t * Hkv;
+        k4 = *reinterpret_cast<const Raw *>(kin + t * ks + h * D + E * lane);
+        v4 = *reinterpret_cast<const Raw *>(vin + t * vs + h * D + E * lane);
+        sl = __ldg(slots + t);
+    };
+    int64_t r = static_cast<int64_t>(blockIdx.x) * kStreamWarps + warp;
+    Raw kn{}, vn{};
+    int64_t sn = -1;
+    if (r < rows) fetch(r, kn, vn, sn);
+    for (; r < rows; r += nw) {
+        const Raw k4 = kn, v4 = vn;
+        const int64_t slot = sn;
+        if (r + nw < rows) fetch(r + nw, kn, vn, sn);  // the next row streams in while this one is worked on
+        if (slot < 0) continue;
+        if (slot >= cache_slots) {
+            if (lane == 0) atomicOr(C.status, TQ_DEVERR_SLOT_RANGE);
+            continue;
+        }
+        const int64_t t = hshift >= 0 ? (r >> hshift) : r / Hkv;
+        const int64_t h = r - t * Hkv;
+        const int64_t dst = (slot >> pshift) * Hkv + h;
+        const int off = static_cast<int>(slot & (G.P - 1));
+        uint8_t *krec = kc + dst * G.k_page;
+        uint8_t *vrec = vc + dst * G.v_page;
+        // ---- key: norm, butterfly rotation, codes -----------------------------
+        float x[E];
+        {
+            uint32_t w[E / 2];
+            w[0] = k4.x; w[1] = k4.y; w[2] = k4.z; w[3] = k4.w;
+            unpack_bf16<E>(w, x);
+        }
+        float ss = 0.f, mx = 0.f;
+#pragma unroll
+        for (int m = 0; m < E; ++m) {
+            ss = fmaf(x[m], x[m], ss);
+            mx = fmaxf(mx, fabsf(x[m]));
+        }
+        ss = warp_sum(ss);
+        mx = warp_max(mx);
+        const bool zero = mx == 0.f;
+        bool exact = !zero && !(mx >= 0x1p-30f && mx <= 0x1p30f);
+#pragma unroll
+        for (int m = 0; m < E; ++m) x[m] *= sg[m];
+#pragma unroll
+        for (int hh = 1; hh < E; hh <<= 1)
+#pragma unroll
+            for (int m = 0; m < E; ++m)
+                if (!(m & hh)) {
+                    const float a = x[m], b = x[m + hh];
+                    x[m] = a + b;
+                    x[m + hh] = a - b;
+                }
+#pragma unroll
+        for (int hh = 1; hh < 32; hh <<= 1) {
+            const bool upper = (lane & hh) != 0;
+#pragma unroll
+            for (int m = 0; m < E; ++m) {
+                const float y = __shfl_xor_sync(0xffffffffu, x[m], hh);
+                x[m] = upper ? (y - x[m]) : (x[m] + y);
+            }
+        }
+        // z_j = sqrt(d) (Pi k)_j / n = (H (s * k))_j / n
+        const float n = sqrtf(ss);
+        const float inv_n = zero ? 0.f : 1.f / n;
+        uint32_t kw = 0u;
+        bool near = false;
+#pragma unroll
+        for (int m = 0; m < E; ++m) {
+            const float z = x[m] * inv_n;
+            int code = 0;
+#pragma unroll
+            for (int step = 8; step > 0; step >>= 1)
+                if (s_thr[code + step] <= z) code += step;
+            near |= fminf(z - s_thr[code], s_thr[code + 1] - z) < kCodeGuard;
+            kw |= static_cast<uint32_t>(code) << (4 * m);
+        }
+        exact = __any_sync(0xffffffffu, exact || (near && !zero));
+        uint16_t n16 = zero ? 0 : float_to_bf16_bits(n);
+        if (exact) {  // codes near a threshold, or an extreme range: the whole row exactly
+            precise_key_row<D>(C, kin + t * ks + h * D, s_codes[warp], nullptr, s_scr[warp], &s_n16[warp],
+                               &s_g16[warp]);
+            __syncwarp();
+            kw = 0u;
+#pragma unroll
+            for (int m = 0; m < E; ++m) kw |= static_cast<uint32_t>(s_codes[warp][E * lane + m]) << (4 * m);
+            n16 = s_n16[warp];
+            __syncwarp();
+        }
+        if (zero) kw = 0u;
+        store_code_bytes(krec + static_cast<int64_t>(off) * C.k_code_bytes + (E / 2) * lane, kw, E / 2);
+        if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * off) = n16;
+        // ---- value: group scale / zero and codes ----------------------------------
+        float v[E];
+        {
+            uint32_t w[E / 2];
+            w[0] = v4.x; w[1] = v4.y; w[2] = v4.z; w[3] = v4.w;
+            unpack_bf16<E>(w, v);
+        }
+        uint32_t vw;
+        const uint32_t meta = quantize_values_lane<E, VB>(v, lpg, vw);
+        store_code_bytes(vrec + static_cast<int64_t>(off) * C.v_code_bytes + (E * VB / 8) * lane, vw, E * VB / 8);
+        if ((lane & (lpg - 1)) == 0)
+            *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + static_cast<int64_t>(off) * C.v_meta_bytes +
+                                          4 * (lane / lpg)) = meta;
+    }
+}
+
+template <int D, int VB>
+cudaError_t launch_stream(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
+                          int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
+                          int64_t num_blocks, cudaStream_t st)
+{
+    const int64_t rows = T * Hkv;
+    int64_t blocks = (rows + kStreamWarps - 1) / kStreamWarps;
+    const int64_t cap = static_cast<int64_t>(c.num_sms) * 3;  // one wave: three resident CTAs per SM
+    if (blocks > cap) blocks = cap;
+    compress_stream_kernel<D, VB><<<static_cast<unsigned>(blocks), kStreamWarps * 32, 0, st>>>(
+        c, pg, k, v, rows, Hkv, ks, vs, slots, kc, vc, num_blocks);
+    return cudaGetLastError();
+}
+
 template <int D, bool HAD>
 cudaError_t launch_compress_d(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
                               int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
@@ -482,6 +739,13 @@ cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *
                             int64_t num_blocks, cudaStream_t st)
 {
     if (c.d == 128) return launch_compress_tc(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, c.num_sms, st);
+    if (c.rotation == TQ_ROTATION_HADAMARD && !c.qjl) {
+        switch (c.v_bits) {
+        case 2: return launch_stream<256, 2>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+        case 3: return launch_stream<256, 3>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+        default: return launch_stream<256, 4>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+        }
+    }
     if (c.rotation == TQ_ROTATION_HADAMARD)
         return launch_compress_d<256, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
     return launch_compress_d<256, false>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
