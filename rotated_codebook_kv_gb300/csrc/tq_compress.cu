@@ -578,9 +578,6 @@ compress_stream_kernel(const Codec C, const PageGeom G, const uint16_t *__restri
     static_assert(E == 8, "head_dim 256: a lane's codes are whole bytes for every value width");
     using Raw = uint4;
     __shared__ float s_thr[18];  // -inf, thresholds ascending, +inf
-    __shared__ double s_scr[kStreamWarps][D];
-    __shared__ uint8_t s_codes[kStreamWarps][D];
-    __shared__ uint16_t s_n16[kStreamWarps], s_g16[kStreamWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nthr = (1 << KB) - 1;
     if (threadIdx.x < 18)
@@ -674,15 +671,57 @@ compress_stream_kernel(const Codec C, const PageGeom G, const uint16_t *__restri
         }
         exact = __any_sync(0xffffffffu, exact || (near && !zero));
         uint16_t n16 = zero ? 0 : float_to_bf16_bits(n);
-        if (exact) {  // codes near a threshold, or an extreme range: the whole row exactly
-            precise_key_row<D>(C, kin + t * ks + h * D, s_codes[warp], nullptr, s_scr[warp], &s_n16[warp],
-                               &s_g16[warp]);
-            __syncwarp();
+        if (exact) {
+            // codes near a threshold, or an extreme range: the row again in double.  Every
+            // bf16 square and every butterfly sum of bf16 keys is exact in double (up to
+            // 2^-53 of the row's largest term), so these decisions are the exact ones up
+            // to the fp32 rounding of the thresholds.
+            double xd[E];
+            {
+                uint32_t w[E / 2];
+                w[0] = k4.x; w[1] = k4.y; w[2] = k4.z; w[3] = k4.w;
+                float xr[E];
+                unpack_bf16<E>(w, xr);
+#pragma unroll
+                for (int m = 0; m < E; ++m) xd[m] = static_cast<double>(xr[m]);
+            }
+            double ssd = 0.0;
+#pragma unroll
+            for (int m = 0; m < E; ++m) {
+                ssd = fma(xd[m], xd[m], ssd);
+                xd[m] *= static_cast<double>(sg[m]);
+            }
+            ssd = warp_sum(ssd);
+#pragma unroll
+            for (int hh = 1; hh < E; hh <<= 1)
+#pragma unroll
+                for (int m = 0; m < E; ++m)
+                    if (!(m & hh)) {
+                        const double a = xd[m], b = xd[m + hh];
+                        xd[m] = a + b;
+                        xd[m + hh] = a - b;
+                    }
+#pragma unroll
+            for (int hh = 1; hh < 32; hh <<= 1) {
+                const bool upper = (lane & hh) != 0;
+#pragma unroll
+                for (int m = 0; m < E; ++m) {
+                    const double y = __shfl_xor_sync(0xffffffffu, xd[m], hh);
+                    xd[m] = upper ? (y - xd[m]) : (xd[m] + y);
+                }
+            }
+            const double nd = sqrt(ssd);
             kw = 0u;
 #pragma unroll
-            for (int m = 0; m < E; ++m) kw |= static_cast<uint32_t>(s_codes[warp][E * lane + m]) << (4 * m);
-            n16 = s_n16[warp];
-            __syncwarp();
+            for (int m = 0; m < E; ++m) {
+                const double z = xd[m] / nd;
+                int code = 0;
+#pragma unroll
+                for (int step = 8; step > 0; step >>= 1)
+                    if (static_cast<double>(s_thr[code + step]) <= z) code += step;
+                kw |= static_cast<uint32_t>(code) << (4 * m);
+            }
+            n16 = double_to_bf16_bits(nd);
         }
         if (zero) kw = 0u;
         store_code_bytes(krec + static_cast<int64_t>(off) * C.k_code_bytes + (E / 2) * lane, kw, E / 2);

@@ -460,3 +460,35 @@ def test_hadamard_rotation(d, kb, vb, g, P, G):
     ax = np.abs(rk)
     ulp = 2.0 ** (np.floor(np.log2(np.where(ax > 0, ax, 1.0))) - 7)
     assert np.all(np.abs(gk - rk) <= ulp + 1e-5)
+
+
+@pytest.mark.parametrize("vb,g", [(4, 64), (2, 32), (3, 128)])
+def test_hadamard_streaming_kernel_special_rows(vb, g):
+    """head_dim 256, 4-bit keys, Hadamard rotation (the streaming kernel): zero keys,
+    keys around 1e-36 and around 1e30 (redone in double), constant and zero value
+    groups, and values whose minimum is an fp16 subnormal match the oracle."""
+    from rotated_codebook_kv_gb300 import native
+    d, kb, P, Hkv = 256, 4, 32, 2
+    w = W.Workload("hadamard_stream", d, kb, vb, g, P, num_kv_heads=Hkv, num_q_heads=Hkv * 2, batch=2,
+                   seq_len_range=(300, 500), seed=77 + vb)
+    b = W.generate(w, device="cpu")
+    k, v = b.k.float(), b.v.float()
+    k[3] = 0.0
+    k[10::17] *= 1e-36
+    k[11::29] *= 1e30
+    v[5, :, :g] = 2.5
+    v[6] = 0.0
+    v[12::13] *= 1e-6
+    b.k, b.v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    b = W.Batch(**{f: (getattr(b, f).to(DEV) if isinstance(getattr(b, f), torch.Tensor) else getattr(b, f))
+                   for f in b.__dataclass_fields__})
+    codec = Codec(d, kb, vb, g, w.codec_seed(), rotation=native.TQ_ROTATION_HADAMARD)
+    ora = O.Oracle(d, kb, vb, g, w.codec_seed(), rotation=O.Oracle.ROTATION_HADAMARD)
+    kc, vc = _compress(codec, w, b)
+    assert codec.get_status() == 0
+    _check_rows(ora, w, b, kc, vc)
+    geo = ora.geometry(P)
+    okc = np.full(b.num_blocks * Hkv * geo["k_page"], 0xA5, np.uint8)
+    ovc = np.full(b.num_blocks * Hkv * geo["v_page"], 0xA5, np.uint8)
+    ora.compress_kv(W.as_u16(b.k), W.as_u16(b.v), b.slot_mapping.cpu().numpy(), P, b.num_blocks, okc, ovc)
+    assert np.array_equal(vc.cpu().numpy(), ovc)
