@@ -566,6 +566,70 @@ __device__ __forceinline__ void store_code_bytes(uint8_t *p, uint32_t w, int nby
     }
 }
 
+// The lane's 4-bit codes of one row taken again in double (rows with a code near a
+// threshold or an extreme range).  Every bf16 square and every butterfly sum of
+// bf16 keys is exact in double up to 2^-53 of the row's largest term, so the
+// decisions are the exact ones up to the fp32 rounding of the thresholds.
+// Returns the 8 codes packed LSB-first; *n16 gets the bf16 norm.
+__device__ __noinline__ uint32_t stream_exact_codes(uint4 k4, const float *__restrict__ hsign, const float *s_thr,
+                                                    uint16_t *n16)
+{
+    constexpr int E = 8;
+    const int lane = threadIdx.x & 31;
+    const uint32_t w[4] = {k4.x, k4.y, k4.z, k4.w};
+    double xd[E];
+    double ssd = 0.0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        xd[2 * i] = static_cast<double>(__uint_as_float(w[i] << 16));
+        xd[2 * i + 1] = static_cast<double>(__uint_as_float(w[i] & 0xffff0000u));
+    }
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        ssd = fma(xd[m], xd[m], ssd);
+        xd[m] *= static_cast<double>(__ldg(hsign + E * lane + m));
+    }
+    ssd = warp_sum(ssd);
+#pragma unroll
+    for (int hh = 1; hh < E; hh <<= 1)
+#pragma unroll
+        for (int m = 0; m < E; ++m)
+            if (!(m & hh)) {
+                const double a = xd[m], b = xd[m + hh];
+                xd[m] = a + b;
+                xd[m + hh] = a - b;
+            }
+#pragma unroll
+    for (int hh = 1; hh < 32; hh <<= 1) {
+        const double sgn = (lane & hh) ? -1.0 : 1.0;
+#pragma unroll
+        for (int m = 0; m < E; ++m) xd[m] = fma(xd[m], sgn, __shfl_xor_sync(0xffffffffu, xd[m], hh));
+    }
+    const double nd = sqrt(ssd);
+    uint32_t kw = 0u;
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        const double z = xd[m] / nd;
+        int code = 0;
+#pragma unroll
+        for (int step = 8; step > 0; step >>= 1)
+            if (static_cast<double>(s_thr[code + step]) <= z) code += step;
+        kw |= static_cast<uint32_t>(code) << (4 * m);
+    }
+    *n16 = double_to_bf16_bits(nd);
+    return kw;
+}
+
+// Code bins of the streaming kernel: u = sat(z / 8 + 1/2) clamps z to [-4, 4]
+// (every 4-bit Lloyd-Max threshold lies inside +-2.8); adding 8064 u to
+// 1.5 * 2^23 rounds to an integer whose bits 7..12 are 128 b, b = bin index, the
+// byte offset of the bin; bins are 8 / 63 wide in z with 1/64 margins, so a bin
+// holds at most one threshold (they are >= 0.12 apart).  Entry {threshold or
+// +inf, 2^23 + number of thresholds below the bin} as two floats, in 16 copies
+// side by side (lane l reads copy l % 16: the 16 lanes of a 64-bit wavefront hit
+// 16 different bank pairs).
+constexpr float kSBinScale = 8064.f;  // 63 bins * 128 bytes
+
 template <int D, int VB>
 __global__ void __launch_bounds__(kStreamWarps * 32, 3)
 compress_stream_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin,
@@ -574,36 +638,48 @@ compress_stream_kernel(const Codec C, const PageGeom G, const uint16_t *__restri
                        int64_t num_blocks)
 {
     constexpr int E = D / 32;  // coordinates per lane
-    constexpr int KB = 4;      // no QJL
     static_assert(E == 8, "head_dim 256: a lane's codes are whole bytes for every value width");
-    using Raw = uint4;
-    __shared__ float s_thr[18];  // -inf, thresholds ascending, +inf
+    __shared__ float s_thr[18];                  // -inf, thresholds ascending, +inf (exact path)
+    __shared__ __align__(16) float2 s_bins[64 * 16];  // [bin][copy]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nthr = (1 << KB) - 1;
+    constexpr int nthr = 15;
     if (threadIdx.x < 18)
         s_thr[threadIdx.x] = threadIdx.x == 0 ? -INFINITY : (threadIdx.x <= nthr ? C.thresholds[threadIdx.x - 1] : INFINITY);
+    for (int e = threadIdx.x; e < 64 * 16; e += blockDim.x) {
+        const float b = static_cast<float>(e >> 4);
+        const float lo = 8.f * (128.f * b - 0.5f) / kSBinScale - 4.f - 1.f / 64.f;
+        const float hi = 8.f * (128.f * b + 127.5f) / kSBinScale - 4.f + 1.f / 64.f;
+        int below = 0, idx = -1;
+        for (int t = 0; t < nthr; ++t) {
+            const float th = C.thresholds[t];
+            if (th < lo) ++below;
+            else if (th <= hi) idx = t;
+        }
+        s_bins[e] = make_float2(idx >= 0 ? C.thresholds[idx] : INFINITY, __uint_as_float(0x4B000000u + below));
+    }
     __syncthreads();
+    const unsigned char *binb = reinterpret_cast<const unsigned char *>(s_bins) + 8 * (lane & 15);
     float sg[E];
 #pragma unroll
     for (int m = 0; m < E; ++m) sg[m] = __ldg(C.hsign + E * lane + m);
     const int hshift = (Hkv & (Hkv - 1)) == 0 ? __ffs(Hkv) - 1 : -1;
     const int pshift = __ffs(G.P) - 1;
     const int64_t cache_slots = num_blocks * G.P;
-    const int lpg = C.group / E;  // lanes per value group: 4, 8 or 16 at D = 256
+    const int lpg = C.group / E;  // lanes per value group: 4, 8 or 16
     const int64_t nw = static_cast<int64_t>(gridDim.x) * kStreamWarps;
-    auto fetch = [&](int64_t r, Raw &k4, Raw &v4, int64_t &sl) {
+    auto fetch = [&](int64_t r, uint4 &k4, uint4 &v4, int64_t &sl) {
         const int64_t t = hshift >= 0 ? (r >> hshift) : r / Hkv;
         const int64_t h = r - t * Hkv;
-        k4 = *reinterpret_cast<const Raw *>(kin + t * ks + h * D + E * lane);
-        v4 = *reinterpret_cast<const Raw *>(vin + t * vs + h * D + E * lane);
-        sl = __ldg(slots + t);
+        k4 = ld_pinned(kin + t * ks + h * D + E * lane);
+        v4 = ld_pinned(vin + t * vs + h * D + E * lane);
+        sl = ld_pinned_s64(slots + t);
     };
     int64_t r = static_cast<int64_t>(blockIdx.x) * kStreamWarps + warp;
-    Raw kn{}, vn{};
+    uint4 kn = make_uint4(0u, 0u, 0u, 0u), vn = kn;
     int64_t sn = -1;
     if (r < rows) fetch(r, kn, vn, sn);
     for (; r < rows; r += nw) {
-        const Raw k4 = kn, v4 = vn;
+        const uint4 k4 = kn, v4 = vn;
         const int64_t slot = sn;
         if (r + nw < rows) fetch(r + nw, kn, vn, sn);  // the next row streams in while this one is worked on
         if (slot < 0) continue;
@@ -620,8 +696,7 @@ compress_stream_kernel(const Codec C, const PageGeom G, const uint16_t *__restri
         // ---- key: norm, butterfly rotation, codes -----------------------------
         float x[E];
         {
-            uint32_t w[E / 2];
-            w[0] = k4.x; w[1] = k4.y; w[2] = k4.z; w[3] = k4.w;
+            const uint32_t w[E / 2] = {k4.x, k4.y, k4.z, k4.w};
             unpack_bf16<E>(w, x);
         }
         float ss = 0.f, mx = 0.f;
@@ -629,13 +704,12 @@ compress_stream_kernel(const Codec C, const PageGeom G, const uint16_t *__restri
         for (int m = 0; m < E; ++m) {
             ss = fmaf(x[m], x[m], ss);
             mx = fmaxf(mx, fabsf(x[m]));
+            x[m] *= sg[m];
         }
         ss = warp_sum(ss);
         mx = warp_max(mx);
         const bool zero = mx == 0.f;
-        bool exact = !zero && !(mx >= 0x1p-30f && mx <= 0x1p30f);
-#pragma unroll
-        for (int m = 0; m < E; ++m) x[m] *= sg[m];
+        const bool extreme = !zero && !(mx >= 0x1p-30f && mx <= 0x1p30f);
 #pragma unroll
         for (int hh = 1; hh < E; hh <<= 1)
 #pragma unroll
@@ -647,90 +721,37 @@ compress_stream_kernel(const Codec C, const PageGeom G, const uint16_t *__restri
                 }
 #pragma unroll
         for (int hh = 1; hh < 32; hh <<= 1) {
-            const bool upper = (lane & hh) != 0;
+            // the lower lane of a pair keeps x + y, the upper y - x: one exact +-1 multiply-add
+            const float sgn = (lane & hh) ? -1.f : 1.f;
 #pragma unroll
-            for (int m = 0; m < E; ++m) {
-                const float y = __shfl_xor_sync(0xffffffffu, x[m], hh);
-                x[m] = upper ? (y - x[m]) : (x[m] + y);
-            }
+            for (int m = 0; m < E; ++m) x[m] = fmaf(x[m], sgn, __shfl_xor_sync(0xffffffffu, x[m], hh));
         }
         // z_j = sqrt(d) (Pi k)_j / n = (H (s * k))_j / n
         const float n = sqrtf(ss);
         const float inv_n = zero ? 0.f : 1.f / n;
+        const float zsu = inv_n * 0.125f;
         uint32_t kw = 0u;
         bool near = false;
 #pragma unroll
         for (int m = 0; m < E; ++m) {
-            const float z = x[m] * inv_n;
-            int code = 0;
-#pragma unroll
-            for (int step = 8; step > 0; step >>= 1)
-                if (s_thr[code + step] <= z) code += step;
-            near |= fminf(z - s_thr[code], s_thr[code + 1] - z) < kCodeGuard;
-            kw |= static_cast<uint32_t>(code) << (4 * m);
+            const float u = __saturatef(fmaf(x[m], zsu, 0.5f));
+            const uint32_t a = __float_as_uint(fmaf(u, kSBinScale, kRoundMagic)) & 0x1F80u;
+            const float2 e = *reinterpret_cast<const float2 *>(binb + a);
+            const float dz = fmaf(x[m], inv_n, -e.x);
+            float up;  // 1 at or above the bin's threshold, 0 below it or without one
+            asm("mul.rn.ftz.sat.f32 %0, %1, 0f7E800000;" : "=f"(up) : "f"(dz));  // dz * 2^126
+            near |= fabsf(dz) < kCodeGuard;
+            kw |= (__float_as_uint(e.y + up) - 0x4B000000u) << (4 * m);
         }
-        exact = __any_sync(0xffffffffu, exact || (near && !zero));
         uint16_t n16 = zero ? 0 : float_to_bf16_bits(n);
-        if (exact) {
-            // codes near a threshold, or an extreme range: the row again in double.  Every
-            // bf16 square and every butterfly sum of bf16 keys is exact in double (up to
-            // 2^-53 of the row's largest term), so these decisions are the exact ones up
-            // to the fp32 rounding of the thresholds.
-            double xd[E];
-            {
-                uint32_t w[E / 2];
-                w[0] = k4.x; w[1] = k4.y; w[2] = k4.z; w[3] = k4.w;
-                float xr[E];
-                unpack_bf16<E>(w, xr);
-#pragma unroll
-                for (int m = 0; m < E; ++m) xd[m] = static_cast<double>(xr[m]);
-            }
-            double ssd = 0.0;
-#pragma unroll
-            for (int m = 0; m < E; ++m) {
-                ssd = fma(xd[m], xd[m], ssd);
-                xd[m] *= static_cast<double>(sg[m]);
-            }
-            ssd = warp_sum(ssd);
-#pragma unroll
-            for (int hh = 1; hh < E; hh <<= 1)
-#pragma unroll
-                for (int m = 0; m < E; ++m)
-                    if (!(m & hh)) {
-                        const double a = xd[m], b = xd[m + hh];
-                        xd[m] = a + b;
-                        xd[m + hh] = a - b;
-                    }
-#pragma unroll
-            for (int hh = 1; hh < 32; hh <<= 1) {
-                const bool upper = (lane & hh) != 0;
-#pragma unroll
-                for (int m = 0; m < E; ++m) {
-                    const double y = __shfl_xor_sync(0xffffffffu, xd[m], hh);
-                    xd[m] = upper ? (y - xd[m]) : (xd[m] + y);
-                }
-            }
-            const double nd = sqrt(ssd);
-            kw = 0u;
-#pragma unroll
-            for (int m = 0; m < E; ++m) {
-                const double z = xd[m] / nd;
-                int code = 0;
-#pragma unroll
-                for (int step = 8; step > 0; step >>= 1)
-                    if (static_cast<double>(s_thr[code + step]) <= z) code += step;
-                kw |= static_cast<uint32_t>(code) << (4 * m);
-            }
-            n16 = double_to_bf16_bits(nd);
-        }
+        if (__any_sync(0xffffffffu, extreme || (near && !zero))) kw = stream_exact_codes(k4, C.hsign, s_thr, &n16);
         if (zero) kw = 0u;
         store_code_bytes(krec + static_cast<int64_t>(off) * C.k_code_bytes + (E / 2) * lane, kw, E / 2);
         if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * off) = n16;
         // ---- value: group scale / zero and codes ----------------------------------
         float v[E];
         {
-            uint32_t w[E / 2];
-            w[0] = v4.x; w[1] = v4.y; w[2] = v4.z; w[3] = v4.w;
+            const uint32_t w[E / 2] = {v4.x, v4.y, v4.z, v4.w};
             unpack_bf16<E>(w, v);
         }
         uint32_t vw;
