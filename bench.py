@@ -460,6 +460,38 @@ def per_config(dev, peak, reps):
         out[name] = ent
         del b, kc, vc, codec
         torch.cuda.empty_cache()
+    # the bypass decode (plain bf16 pages, same skeleton) on the long-context and paged shapes:
+    # the bandwidth control of the compressed decode
+    for name, w in (("bypass_bf16_long_context", W.long_context_mixed().for_layer(0)),
+                    ("bypass_bf16_paged_decode", W.paged_decode())):
+        b = W.generate(w, device=dev)
+        codec = Codec(w.head_dim, 4, 4, 32, 0)
+        P, H, d = w.page_size, w.num_kv_heads, w.head_dim
+        kp = torch.empty(b.num_blocks * H * P, d, dtype=torch.bfloat16, device=dev)
+        vp = torch.empty_like(kp)
+        sm = b.slot_mapping
+        rows = (((sm // P) * H)[:, None] + torch.arange(H, device=dev)[None, :]) * P + (sm % P)[:, None]
+        kp[rows.reshape(-1)] = b.k.reshape(-1, d)
+        vp[rows.reshape(-1)] = b.v.reshape(-1, d)
+        del b.k, b.v
+        maxb = b.block_table.shape[1]
+        splits = codec.decode_splits(w.batch, H, maxb, P)
+        ws = codec.workspace(w.batch, w.num_q_heads, splits, device=dev)
+        o = torch.empty_like(b.q)
+        t_d = timed(lambda: codec.decode_attention_bf16(b.q, kp, vp, b.block_table, b.seq_lens, H, P, b.num_blocks,
+                                                        b.sm_scale, splits=splits, workspace=ws, out=o,
+                                                        stream=stream))
+        lens = b.seq_lens.cpu().tolist()
+        db = sum(lens) * H * 4 * d + 2 * w.batch * w.num_q_heads * d * 2 + \
+            sum((x + P - 1) // P for x in lens) * 4 + w.batch * 4
+        if codec.get_status(stream) != 0:
+            raise RuntimeError(f"device status bits set in the {name} workload")
+        out[name] = {"decode_gbs": round(db / t_d / 1e9, 1), "decode_frac": round(db / t_d / 1e9 / peak, 4),
+                     "decode_us": round(t_d * 1e6, 1), "decode_splits": splits,
+                     "decode_kv_tokens_per_s": round(sum(lens) * H / t_d, 1),
+                     "bytes_per_token_head": 4 * d}
+        del kp, vp, b, codec
+        torch.cuda.empty_cache()
     out["timing"] = f"median of {reps} calls after 2 warm-up calls; L2 flushed before each call"
     out["wide_head_decode_hadamard"]["rotation"] = "randomized Hadamard (tq_init_rotation)"
     return out

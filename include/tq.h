@@ -213,6 +213,28 @@ tq_status tq_decode_attention_static(tq_handle h, const uint16_t *q, const uint8
                                      float sm_scale, int splits, uint16_t *out, void *stream);
 
 /*
+ * tq_decode_attention_bf16 -- the bypass decode: the same split-K paged decode
+ * (splits, workspace, combine, status bits and outputs as tq_decode_attention)
+ * over an ordinary bf16 paged KV cache instead of the compressed one
+ * (turbo-attn, "Two independently-usable pieces", item 2: a bypass loader that
+ * reads plain bf16 pages in the same decode kernel).  It serves as the
+ * bandwidth control of the compressed decode on identical shapes.
+ *
+ * k_pool, v_pool: device bf16 [num_blocks][num_kv_heads][page_size][head_dim]
+ *   (head_dim from the handle), 16-byte aligned; token position t of sequence b
+ *   is row t % page_size of block block_table[b][t / page_size].
+ * The scores are sm_scale * <q, k> with exact bf16 products and fp32 sums; the
+ * probabilities enter the value product as two bf16 terms (~16 bits).
+ * Two launches on `stream` (decode, combine); the pools are read through tensor
+ * maps encoded on the host for each call (no allocation, no synchronisation).
+ */
+tq_status tq_decode_attention_bf16(tq_handle h, const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                                   const int32_t *block_table, const int32_t *seq_lens, int batch, int num_q_heads,
+                                   int num_kv_heads, int page_size, int max_blocks_per_seq, int64_t num_blocks,
+                                   float sm_scale, int splits, void *workspace, size_t ws_bytes, uint16_t *out,
+                                   void *stream);
+
+/*
  * tq_set_wait_limit -- the number of SM clock cycles a kernel of this handle
  * polls one barrier (a tensor-core completion, a page copy, a hand-off between
  * warps) before it gives up, sets TQ_DEVERR_TIMEOUT and winds its CTA down.

@@ -78,6 +78,8 @@ def _load():
                                                    ctypes.c_int]),
             "tq_or_dequant_slots": (None, [vp, u8p, u8p, ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int64, dp, dp]),
             "tq_or_key_qjl_given_codes": (None, [vp, u16p, u8p, ctypes.c_int64, u8p, u16p, dp, dp]),
+            "tq_or_decode_bf16": (None, [u16p, u16p, u16p, i32p, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, dp]),
             "tq_or_decode": (None, [vp, u16p, u8p, u8p, i32p, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, i32p,
                                     ctypes.c_int64, dp, ctypes.c_int]),
@@ -177,6 +179,23 @@ def unpack(packed, n: int, bits: int) -> np.ndarray:
     packed = np.ascontiguousarray(packed, dtype=np.uint8)
     out = np.zeros(n, dtype=np.uint8)
     _load().tq_or_unpack(_ptr(packed, ctypes.c_uint8), n, bits, _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def decode_bf16(q, k_pool, v_pool, block_table, seq_lens, Hkv: int, page_size: int, sm_scale: float):
+    """Softmax attention of one query token per sequence over plain bf16 pages.
+
+    q: [B, Hq, d] bf16 bits; pools: [num_blocks, Hkv, P, d] bf16 bits.  Returns [B, Hq, d] doubles."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    B, Hq, d = q.shape
+    kp = np.ascontiguousarray(k_pool, dtype=np.uint16)
+    vp = np.ascontiguousarray(v_pool, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    out = np.zeros((B, Hq, d))
+    _load().tq_or_decode_bf16(_ptr(q, ctypes.c_uint16), _ptr(kp, ctypes.c_uint16), _ptr(vp, ctypes.c_uint16),
+                              _ptr(bt, ctypes.c_int32), _ptr(sl, ctypes.c_int32), B, Hq, Hkv, d, page_size,
+                              bt.shape[1], float(sm_scale), _ptr(out, ctypes.c_double))
     return out
 
 

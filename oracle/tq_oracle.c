@@ -870,3 +870,54 @@ void tq_or_decode(const or_ctx *c, const uint16_t *q, const uint8_t *kc, const u
     or_parallel(or_dec_run, &J, n_jobs, nthreads);
     free(all);
 }
+
+/* ------------------------------------------------------------------------- */
+/* Bypass decode over plain bf16 pages                                        */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * [turbo-attn] "Two independently-usable pieces", item 2: the decode kernel with
+ * a bypass loader reads ordinary bf16 pages.  What it computes is plain softmax
+ * attention of one query token per sequence over its paged bf16 context:
+ * pools [num_blocks][Hkv][P][d]; position t of sequence b is row t % P of block
+ * bt[b][t / P]; query head h reads kv head h / (Hq / Hkv); s_t = sm_scale <q, k_t>,
+ * p = softmax(s) (max-subtracted), o = sum_t p_t v_t, in double; seq_len 0 gives
+ * zeros.  out: [B][Hq][d] doubles.
+ */
+void tq_or_decode_bf16(const uint16_t *q, const uint16_t *kpool, const uint16_t *vpool, const int32_t *bt,
+                       const int32_t *lens, int B, int Hq, int Hkv, int d, int P, int maxblk, double sm_scale,
+                       double *out)
+{
+    int G = Hq / Hkv;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < Hq; ++h) {
+            int kvh = h / G;
+            int L = lens[b];
+            double *o = out + ((int64_t)b * Hq + h) * d;
+            for (int j = 0; j < d; ++j) o[j] = 0.0;
+            if (L <= 0) continue;
+            double *s = malloc(sizeof(double) * L);
+            double mx = -INFINITY;
+            for (int t = 0; t < L; ++t) {
+                int64_t rowi = ((int64_t)bt[(int64_t)b * maxblk + t / P] * Hkv + kvh) * P + t % P;
+                double acc = 0.0;
+                for (int j = 0; j < d; ++j)
+                    acc += tq_or_bf16_to_double(q[((int64_t)b * Hq + h) * d + j]) *
+                           tq_or_bf16_to_double(kpool[rowi * d + j]);
+                s[t] = sm_scale * acc;
+                if (s[t] > mx) mx = s[t];
+            }
+            double den = 0.0;
+            for (int t = 0; t < L; ++t) {
+                s[t] = exp(s[t] - mx);
+                den += s[t];
+            }
+            for (int t = 0; t < L; ++t) {
+                int64_t rowi = ((int64_t)bt[(int64_t)b * maxblk + t / P] * Hkv + kvh) * P + t % P;
+                double w = s[t] / den;
+                for (int j = 0; j < d; ++j) o[j] += w * tq_or_bf16_to_double(vpool[rowi * d + j]);
+            }
+            free(s);
+        }
+}
+

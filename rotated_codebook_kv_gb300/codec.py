@@ -102,6 +102,26 @@ class Codec:
     def set_wait_limit(self, cycles: int):
         native.tq_set_wait_limit(self.handle, cycles)
 
+    def decode_attention_bf16(self, q, k_pool, v_pool, block_table, seq_lens, num_kv_heads: int, page_size: int,
+                              num_blocks: int, sm_scale: float, splits: int = 0, workspace=None, out=None,
+                              stream=None):
+        """Bypass decode over plain bf16 pools [num_blocks][num_kv_heads][page_size][head_dim]."""
+        B, Hq, d = q.shape
+        assert d == self.head_dim and q.dtype == torch.bfloat16 and q.is_contiguous()
+        assert k_pool.dtype == torch.bfloat16 and v_pool.dtype == torch.bfloat16
+        maxb = block_table.shape[1]
+        if splits == 0:
+            splits = self.decode_splits(B, num_kv_heads, maxb, page_size)
+        if workspace is None:
+            workspace = self.workspace(B, Hq, splits, device=q.device)
+        if out is None:
+            out = torch.empty_like(q)
+        native.tq_decode_attention_bf16(self.handle, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                        _ptr(seq_lens), B, Hq, num_kv_heads, page_size, maxb, num_blocks,
+                                        float(sm_scale), splits, _ptr(workspace), workspace.numel(), _ptr(out),
+                                        _stream(stream))
+        return out
+
     def get_status(self, stream=None) -> int:
         return native.tq_get_status(self.handle, _stream(stream))
 

@@ -54,6 +54,8 @@ bool supported_bits(int b) { return b >= 2 && b <= 4; }
 
 void *tq::handle_static_scratch(tq_handle h) { return h ? h->static_scratch : nullptr; }
 
+const tq::Codec &tq::handle_codec(tq_handle h) { return h->codec; }
+
 cudaError_t tq::ensure_smem_attr(const void *func, size_t bytes)
 {
     static std::mutex lock;

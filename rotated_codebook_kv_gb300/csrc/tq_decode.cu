@@ -216,6 +216,13 @@ cudaError_t launch_decode_d(const Codec &c, const PageGeom &pg, const DecodeArgs
 
 }  // namespace
 
+cudaError_t launch_combine(const Codec &c, const DecodeArgs &a, cudaStream_t st)
+{
+    if (c.d == 128) combine_kernel<128><<<a.B * a.Hq, 128, 0, st>>>(a);
+    else combine_kernel<256><<<a.B * a.Hq, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st)
 {
     if (c.d == 128) return launch_decode_d<128>(c, pg, a, st);

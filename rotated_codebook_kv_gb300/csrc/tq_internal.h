@@ -98,12 +98,16 @@ cudaError_t launch_dequant(const Codec &c, const PageGeom &pg, const uint8_t *kc
                            uint16_t *v_out, cudaStream_t st);
 
 cudaError_t launch_decode(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st);
+// The log-sum-exp merge of split partials into bf16 (and fp32) outputs.
+cudaError_t launch_combine(const Codec &c, const DecodeArgs &a, cudaStream_t st);
 
 // Device address of the no-allocation decode's static scratch array for the
 // context current on the calling thread (looked up, not cached).
 cudaError_t static_scratch_lookup(void **out);
 // The address tq_init looked up for a handle.
 void *handle_static_scratch(tq_handle h);
+// The codec constants of a (non-NULL) handle.
+const Codec &handle_codec(tq_handle h);
 
 // Sets a kernel's dynamic shared-memory limit once per (function, device); thread safe.
 cudaError_t ensure_smem_attr(const void *func, size_t bytes);

@@ -32,6 +32,8 @@ SIGNATURES = {
     "tq_decode_workspace_bytes": (_sz, [_vp, _i32, _i32, _i32]),
     "tq_decode_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _f32, _i32,
                                    _vp, _sz, _vp, _vp]),
+    "tq_decode_attention_bf16": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
+                                        _i32, _vp, _sz, _vp, _vp]),
     "tq_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
                                           _i32, _vp, _vp]),
     "tq_set_wait_limit": (_i32, [_vp, _i64]),
@@ -129,6 +131,14 @@ def tq_decode_attention(h, q, k_cache, v_cache, block_table, seq_lens, batch, nu
                         max_blocks_per_seq, num_blocks, sm_scale, splits, workspace, ws_bytes, out, stream) -> None:
     _check("tq_decode_attention", load().tq_decode_attention(
         h, q, k_cache, v_cache, block_table, seq_lens, batch, num_q_heads, num_kv_heads, page_size,
+        max_blocks_per_seq, num_blocks, sm_scale, splits, workspace, ws_bytes, out, stream))
+
+
+def tq_decode_attention_bf16(h, q, k_pool, v_pool, block_table, seq_lens, batch, num_q_heads, num_kv_heads,
+                             page_size, max_blocks_per_seq, num_blocks, sm_scale, splits, workspace, ws_bytes, out,
+                             stream) -> None:
+    _check("tq_decode_attention_bf16", load().tq_decode_attention_bf16(
+        h, q, k_pool, v_pool, block_table, seq_lens, batch, num_q_heads, num_kv_heads, page_size,
         max_blocks_per_seq, num_blocks, sm_scale, splits, workspace, ws_bytes, out, stream))
 
 

@@ -427,3 +427,59 @@ def test_qjl_given_codes_reproduces_the_compressor(bits):
     # the signs follow the moved residual: most agree, the ones that change are where
     # the projection of the moved coordinate's column shifts p across zero
     assert (alt2["k_sign"] != rec["k_sign"]).any()
+
+
+# --------------------------------------------------------------------------- #
+# Bypass decode over plain bf16 pages                                            #
+# --------------------------------------------------------------------------- #
+
+def _bf16_pages(rng, B, Hkv, G, d, P, lens, nb_extra=2):
+    lens = np.asarray(lens, np.int32)
+    npg = (lens + P - 1) // P
+    nb = int(npg.sum()) + nb_extra
+    perm = rng.permutation(nb).astype(np.int32)
+    bt = np.full((B, max(int(npg.max()), 1)), -1, np.int32)
+    st = 0
+    for b in range(B):
+        bt[b, : npg[b]] = perm[st: st + npg[b]]
+        st += npg[b]
+    kp = _bf16(rng.standard_normal((nb, Hkv, P, d)))
+    vp = _bf16(rng.standard_normal((nb, Hkv, P, d)))
+    q = _bf16(rng.standard_normal((B, Hkv * G, d)))
+    return q, kp, vp, bt, lens
+
+
+def test_bypass_decode_is_softmax_attention():
+    """Against scipy's softmax over the gathered rows (a library routine) on tiny inputs."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(41)
+    B, Hkv, G, d, P = 3, 2, 3, 64, 16
+    q, kp, vp, bt, lens = _bf16_pages(rng, B, Hkv, G, d, P, (37, 16, 5))
+    sm = d ** -0.5
+    out = O.decode_bf16(q, kp, vp, bt, lens, Hkv, P, sm)
+    qd, kd, vd = O.bf16_to_double(q), O.bf16_to_double(kp), O.bf16_to_double(vp)
+    for b in range(B):
+        pos = np.arange(lens[b])
+        blk, off = bt[b, pos // P], pos % P
+        for h in range(Hkv * G):
+            K = kd[blk, h // G, off]
+            V = vd[blk, h // G, off]
+            want = softmax(sm * (K @ qd[b, h])) @ V
+            assert np.abs(out[b, h] - want).max() < 1e-12
+
+
+def test_bypass_decode_special_cases():
+    rng = np.random.default_rng(42)
+    B, Hkv, G, d, P = 4, 1, 2, 32, 16
+    q, kp, vp, bt, lens = _bf16_pages(rng, B, Hkv, G, d, P, (1, 0, 20, 20))
+    kp[bt[2, 0], 0] = kp[bt[2, 0], 0, :1]  # identical keys on the first page of sequence 2
+    kp[bt[2, 1], 0] = kp[bt[2, 0], 0, :1]
+    q[3] = 0                                # zero query on sequence 3
+    out = O.decode_bf16(q, kp, vp, bt, lens, Hkv, P, d ** -0.5)
+    vd = O.bf16_to_double(vp)
+    assert np.array_equal(out[0, 0], vd[bt[0, 0], 0, 0])   # one token: its value
+    assert not out[1].any()                                  # no tokens: zeros
+    rows = np.concatenate([vd[bt[2, 0], 0, :16], vd[bt[2, 1], 0, :4]])
+    assert np.allclose(out[2, 0], rows.mean(0), atol=1e-12)  # identical keys: the mean value
+    rows3 = np.concatenate([vd[bt[3, 0], 0, :16], vd[bt[3, 1], 0, :4]])
+    assert np.allclose(out[3, 1], rows3.mean(0), atol=1e-12)  # zero query: the mean value
