@@ -86,21 +86,30 @@ typedef enum {
 tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed, tq_handle *out);
 
 /*
- * tq_init_rotation -- tq_init with a choice of rotation Pi:
- *   TQ_ROTATION_DENSE     the Haar rotation described above (what tq_init builds);
- *   TQ_ROTATION_HADAMARD  a randomized Hadamard rotation Pi = H D / sqrt(d)
+ * tq_init_ex -- tq_init with options, flags = bitwise OR of:
+ *   TQ_ROTATION_HADAMARD  Pi is a randomized Hadamard rotation H D / sqrt(d)
  *     (turbo-attn, "How it works", step 1: a fast Walsh-Hadamard transform), with
  *     H the Sylvester Hadamard matrix, H[i][j] = (-1)^popcount(i & j), and
  *     D = diag(s), s_j = -1 when the top bit of the j-th output of SplitMix64
  *     stream 0 (the stream the dense rotation draws from) is set, else +1.
- * Everything else -- S, the codebook, the records, decode -- is unchanged; the
- * rotation is applied by butterflies instead of a dense product where that pays
- * (key compression at head_dim 256).
+ *     S, the codebook and the records are unchanged; the rotation runs as
+ *     butterflies where that pays (key compression at head_dim 256).
+ *     Without this flag Pi is the dense Haar rotation described above.
+ *   TQ_VALUES_MSE  values are coded like keys without the QJL sketch
+ *     (brightcoding blog, "What is TurboQuant-GPU?" and "Example 4": 3-bit MSE
+ *     values; normalize -> rotate -> Lloyd-Max quantize -> pack): the value's
+ *     norm is stored as bf16 and every coordinate of z = sqrt(d) Pi v / ||v||
+ *     is coded against the v_bits-bit Lloyd-Max codebook of N(0,1); `group` is
+ *     then unused (it must still be a supported value).  The V record becomes
+ *     codes [P][d*v_bits/8] | norms [P] bf16, and dequant / decode use
+ *     V~ = n Pi^T c[code] / sqrt(d) (decode accumulates in the rotated space and
+ *     rotates the output back once per query head).
+ * tq_init(...) is tq_init_ex(..., 0, ...).
  */
-#define TQ_ROTATION_DENSE 0
-#define TQ_ROTATION_HADAMARD 1
-tq_status tq_init_rotation(int head_dim, int k_bits, int v_bits, int group, uint64_t seed, int rotation,
-                           tq_handle *out);
+#define TQ_ROTATION_HADAMARD 1u
+#define TQ_VALUES_MSE 2u
+tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t seed, unsigned flags,
+                     tq_handle *out);
 
 /* Frees the handle's device tables.  Accepts NULL. */
 tq_status tq_destroy(tq_handle h);
@@ -116,6 +125,7 @@ tq_status tq_destroy(tq_handle h);
  * s / page_size at offset o = s % page_size.  Inside a record (P = page_size):
  *   K: codes [P][d*k_bits/8] | signs [P][d/8] (QJL) | norms [P] bf16 | gammas [P] bf16 (QJL)
  *   V: codes [P][d*v_bits/8] | meta  [P][d/group][2] fp16 (scale, zero)
+ *      (with TQ_VALUES_MSE: codes [P][d*v_bits/8] | norms [P] bf16)
  * Codes are LSB-first bitstreams (code j in bits [b*j, b*j+b)); sign bit i is
  * bit i%8 of byte i/8.  Every sub-array is a multiple of 16 bytes.
  */

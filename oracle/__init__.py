@@ -72,7 +72,7 @@ def _load():
             "tq_or_pack": (None, [u8p, ctypes.c_int, ctypes.c_int, u8p]),
             "tq_or_unpack": (None, [u8p, ctypes.c_int, ctypes.c_int, u8p]),
             "tq_or_compress_rows": (None, [vp, u16p, u16p, ctypes.c_int64, u8p, u8p, u16p, u16p, u8p, u16p,
-                                           dp, dp, dp, dp, ctypes.c_int]),
+                                           dp, dp, dp, dp, dp, ctypes.c_int]),
             "tq_or_compress_kv": (ctypes.c_int64, [vp, u16p, u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
                                                    ctypes.c_int64, i64p, u8p, u8p, ctypes.c_int, ctypes.c_int64,
                                                    ctypes.c_int]),
@@ -212,12 +212,15 @@ class Oracle:
     ROTATION_DENSE, ROTATION_HADAMARD = 0, 1
 
     def __init__(self, head_dim: int, k_bits: int, v_bits: int, group: int, seed: int,
-                 qjl_seed: int | None = None, rotation: int = 0):
+                 qjl_seed: int | None = None, rotation: int = 0, values: str = "group"):
+        """values: "group" (per-group scale / zero) or "mse" (rotation + Lloyd-Max codebook)."""
         self._lib = _load()
+        options = (1 if rotation == self.ROTATION_HADAMARD else 0) | (2 if values == "mse" else 0)
         # a separate S seed is only for Monte-Carlo checks of the QJL estimator
         self._h = self._lib.tq_or_create3(head_dim, k_bits, v_bits, group, ctypes.c_uint64(seed),
-                                          ctypes.c_uint64(seed if qjl_seed is None else qjl_seed), rotation)
+                                          ctypes.c_uint64(seed if qjl_seed is None else qjl_seed), options)
         self.rotation = rotation
+        self.values = values
         if not self._h:
             raise ValueError("unsupported oracle parameters")
         self.d, self.k_bits, self.v_bits, self.group, self.seed = head_dim, k_bits, v_bits, group, seed
@@ -235,7 +238,11 @@ class Oracle:
         c, t = np.zeros(L), np.zeros(L - 1)
         self._lib.tq_or_get_params(self._h, _ptr(Pi, ctypes.c_double), _ptr(S, ctypes.c_double),
                                    _ptr(c, ctypes.c_double), _ptr(t, ctypes.c_double))
-        return {"Pi": Pi, "S": S, "centroids": c, "thresholds": t}
+        out = {"Pi": Pi, "S": S, "centroids": c, "thresholds": t}
+        if self.values == "mse":
+            vc, vt, _ = codebook(self.v_bits)
+            out.update(v_centroids=vc, v_thresholds=vt)
+        return out
 
     def geometry(self, page_size: int) -> dict:
         s = np.zeros(6, dtype=np.int64)
@@ -259,14 +266,16 @@ class Oracle:
             "v_meta": np.zeros((n, g["v_meta"] // 2), np.uint16),
         }
         if diag:
-            out.update(z=np.zeros((n, self.d)), pg=np.zeros((n, self.d)), norm=np.zeros(n), gamma=np.zeros(n))
+            out.update(z=np.zeros((n, self.d)), pg=np.zeros((n, self.d)), norm=np.zeros(n), gamma=np.zeros(n),
+                       vz=np.zeros((n, self.d)))
         self._lib.tq_or_compress_rows(
             self._h, _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16), n,
             _ptr(out["k_code"], ctypes.c_uint8), _ptr(out["k_sign"], ctypes.c_uint8),
             _ptr(out["k_norm"], ctypes.c_uint16), _ptr(out["k_gamma"], ctypes.c_uint16),
             _ptr(out["v_code"], ctypes.c_uint8), _ptr(out["v_meta"], ctypes.c_uint16),
             _ptr(out.get("z"), ctypes.c_double), _ptr(out.get("pg"), ctypes.c_double),
-            _ptr(out.get("norm"), ctypes.c_double), _ptr(out.get("gamma"), ctypes.c_double), nthreads)
+            _ptr(out.get("norm"), ctypes.c_double), _ptr(out.get("gamma"), ctypes.c_double),
+            _ptr(out.get("vz"), ctypes.c_double), nthreads)
         if not self.qjl:
             out["k_sign"] = out["k_sign"][:, :0]
         return out

@@ -274,6 +274,9 @@ double tq_or_f16_to_double(uint16_t h)
 
 typedef struct or_ctx {
     int d, kb, vb, g, qjl;
+    int vmse;           /* values coded by rotation + Lloyd-Max codebook (else group scale/zero) */
+    double vcent[16];   /* 2^vb value centroids (vmse) */
+    double vthr[15];
     double *Pi, *S;     /* d x d each, row-major */
     double cent[16];    /* 2^kb centroids, ascending, N(0,1) units */
     double thr[15];     /* 2^kb - 1 thresholds */
@@ -315,9 +318,11 @@ int tq_or_hadamard_rotation(int d, uint64_t seed, double *Pi)
 
 /* QJL is used iff k_bits <= 3 (one sign bit per coordinate, m = d).
  * Pi comes from seed_rot, S from seed_qjl; the codec uses one seed for both.
- * rotation 0 is the Haar rotation (O2), 1 the randomized Hadamard one (O2'). */
-or_ctx *tq_or_create3(int d, int kb, int vb, int g, uint64_t seed_rot, uint64_t seed_qjl, int rotation)
+ * options: bit 0 -- the randomized Hadamard rotation (O2') instead of the Haar
+ * one (O2); bit 1 -- values coded like keys without QJL (O5'). */
+or_ctx *tq_or_create3(int d, int kb, int vb, int g, uint64_t seed_rot, uint64_t seed_qjl, int options)
 {
+    int rotation = options & 1;
     if (d <= 0 || d % 8 || kb < 1 || kb > 4 || vb < 1 || vb > 8 || g <= 0 || d % g) return NULL;
     or_ctx *c = calloc(1, sizeof(or_ctx));
     c->d = d; c->kb = kb; c->vb = vb; c->g = g; c->qjl = kb <= 3;
@@ -329,10 +334,15 @@ or_ctx *tq_or_create3(int d, int kb, int vb, int g, uint64_t seed_rot, uint64_t 
         return NULL;
     }
     tq_or_qjl_matrix(d, seed_qjl, c->S);
+    c->vmse = (options >> 1) & 1;
+    if (c->vmse && tq_or_codebook(vb, c->vcent, c->vthr) < 0) {
+        free(c->Pi); free(c->S); free(c);
+        return NULL;
+    }
     c->kcode = d * kb / 8;
     c->ksign = c->qjl ? d / 8 : 0;
     c->vcode = d * vb / 8;
-    c->vmeta = (d / g) * 4;
+    c->vmeta = c->vmse ? 2 : (d / g) * 4; /* a bf16 norm, or (scale, zero) fp16 per group */
     return c;
 }
 
@@ -460,9 +470,49 @@ static void or_compress_key(const or_ctx *c, const uint16_t *kin, uint8_t *kcode
     }
 }
 
-/* Value record: vcode bytes of codes, (d/g) x (scale, zero) fp16 pairs. */
+/*
+ * O5': value record with the MSE codebook ([brightcoding] "What is TurboQuant-GPU?":
+ * values get MSE quantization; "Example 4": normalize -> rotate -> Lloyd-Max
+ * quantize -> pack): the key steps without QJL, with the v_bits codebook --
+ * n = ||v|| stored bf16, z = sqrt(d) Pi v / n, code_j = #{i : t_i <= z_j}.
+ * vmeta[0] receives the bf16 norm.  vz (optional) receives z.
+ */
+static void or_compress_value_mse(const or_ctx *c, const uint16_t *vin, uint8_t *vcode, uint16_t *vmeta, double *vz)
+{
+    int d = c->d, L = 1 << c->vb;
+    double v[256];
+    uint8_t code[256];
+    double nsq = 0.0;
+    for (int j = 0; j < d; ++j) {
+        v[j] = tq_or_bf16_to_double(vin[j]);
+        nsq += v[j] * v[j];
+    }
+    double n = sqrt(nsq);
+    vmeta[0] = tq_or_bf16_from_double(n);
+    double sd = sqrt((double)d);
+    for (int i = 0; i < d; ++i) {
+        int cnt = 0;
+        double z = 0.0;
+        if (n > 0.0) {
+            double acc = 0.0;
+            for (int j = 0; j < d; ++j) acc += c->Pi[i * d + j] * v[j];
+            z = sd * acc / n;
+            for (int t = 0; t < L - 1; ++t) cnt += (c->vthr[t] <= z);
+        }
+        code[i] = (uint8_t)cnt; /* a zero value: all-zero codes and norm */
+        if (vz) vz[i] = z;
+    }
+    tq_or_pack(code, d, c->vb, vcode);
+}
+
+/* Value record: vcode bytes of codes, (d/g) x (scale, zero) fp16 pairs (O5), or
+ * the codes and the bf16 norm (O5'). */
 static void or_compress_value(const or_ctx *c, const uint16_t *vin, uint8_t *vcode, uint16_t *vmeta)
 {
+    if (c->vmse) {
+        or_compress_value_mse(c, vin, vcode, vmeta, NULL);
+        return;
+    }
     int d = c->d, g = c->g, L = (1 << c->vb) - 1;
     uint8_t code[256];
     for (int gi = 0; gi < d / g; ++gi) {
@@ -572,7 +622,7 @@ typedef struct {
     const uint16_t *k, *v;
     uint8_t *kcode, *ksign, *vcode;
     uint16_t *knorm, *kgamma, *vmeta;
-    double *z, *pg, *norm, *gamma;
+    double *z, *pg, *norm, *gamma, *vz;
 } or_rows_job;
 
 static void or_rows_run(void *p, int64_t lo, int64_t hi)
@@ -590,7 +640,13 @@ static void or_rows_run(void *p, int64_t lo, int64_t hi)
                             c->qjl ? J->ksign + i * c->ksign : sdummy, J->knorm + i,
                             c->qjl ? J->kgamma + i : &gdummy, &dg);
         }
-        if (J->v) or_compress_value(c, J->v + i * d, J->vcode + i * c->vcode, J->vmeta + i * (c->vmeta / 2));
+        if (J->v) {
+            if (c->vmse)
+                or_compress_value_mse(c, J->v + i * d, J->vcode + i * c->vcode, J->vmeta + i * (c->vmeta / 2),
+                                      J->vz ? J->vz + i * d : NULL);
+            else
+                or_compress_value(c, J->v + i * d, J->vcode + i * c->vcode, J->vmeta + i * (c->vmeta / 2));
+        }
     }
 }
 
@@ -602,9 +658,9 @@ static void or_rows_run(void *p, int64_t lo, int64_t hi)
 void tq_or_compress_rows(const or_ctx *c, const uint16_t *k, const uint16_t *v, int64_t n,
                          uint8_t *kcode, uint8_t *ksign, uint16_t *knorm, uint16_t *kgamma,
                          uint8_t *vcode, uint16_t *vmeta,
-                         double *z, double *pg, double *norm, double *gamma, int nthreads)
+                         double *z, double *pg, double *norm, double *gamma, double *vz, int nthreads)
 {
-    or_rows_job J = {c, k, v, kcode, ksign, vcode, knorm, kgamma, vmeta, z, pg, norm, gamma};
+    or_rows_job J = {c, k, v, kcode, ksign, vcode, knorm, kgamma, vmeta, z, pg, norm, gamma, vz};
     or_parallel(or_rows_run, &J, n, nthreads);
 }
 
@@ -684,6 +740,7 @@ typedef struct {
     uint8_t sig[256];
     double n, gamma;
     double vs[64], vz[64];
+    double vn; /* value norm (O5') */
     uint8_t vcode[256];
 } or_rec;
 
@@ -707,6 +764,11 @@ static void or_read(const or_ctx *c, const uint8_t *kc, const uint8_t *vc, int P
     }
     tq_or_unpack(vr + (int64_t)off * c->vcode, c->d, c->vb, R->vcode);
     const uint8_t *meta = vr + (int64_t)P * c->vcode + (int64_t)off * c->vmeta;
+    if (c->vmse) {
+        memcpy(&b, meta, 2);
+        R->vn = tq_or_bf16_to_double(b);
+        return;
+    }
     for (int gi = 0; gi < c->d / c->g; ++gi) {
         uint16_t s16, z16;
         memcpy(&s16, meta + 4 * gi, 2);
@@ -734,6 +796,14 @@ static void or_dequant_rec(const or_ctx *c, const or_rec *R, double *kout, doubl
         double a = 0.0;
         for (int i = 0; i < d; ++i) a += c->Pi[i * d + j] * u[i];
         kout[j] = R->n * a;
+    }
+    if (c->vmse) { /* O5': V~ = n Pi^T c[code] / sqrt(d) */
+        for (int j = 0; j < d; ++j) {
+            double a = 0.0;
+            for (int i = 0; i < d; ++i) a += c->Pi[i * d + j] * c->vcent[R->vcode[i]];
+            vout[j] = R->vn * a / sd;
+        }
+        return;
     }
     for (int j = 0; j < d; ++j) vout[j] = R->vcode[j] * R->vs[j / c->g] + R->vz[j / c->g];
 }
@@ -832,6 +902,21 @@ static void or_dec_run(void *p, int64_t lo, int64_t hi)
             for (int t = 0; t < L; ++t) if (s[(int64_t)t * G + gh] > m) m = s[(int64_t)t * G + gh];
             double den = 0.0;
             for (int t = 0; t < L; ++t) den += exp(s[(int64_t)t * G + gh] - m);
+            if (c->vmse) { /* O5' values: sum in the rotated space, then Pi^T once */
+                for (int i = 0; i < d; ++i) vt[i] = 0.0;
+                for (int t = 0; t < L; ++t) {
+                    double w = exp(s[(int64_t)t * G + gh] - m) / den;
+                    int64_t slot = (int64_t)J->bt[(int64_t)b * J->maxblk + t / J->P] * J->P + t % J->P;
+                    or_read(c, J->kc, J->vc, J->P, J->Hkv, slot, kvh, &R);
+                    for (int i = 0; i < d; ++i) vt[i] += w * R.vn * c->vcent[R.vcode[i]] / sd;
+                }
+                for (int j = 0; j < d; ++j) {
+                    double a = 0.0;
+                    for (int i = 0; i < d; ++i) a += c->Pi[i * d + j] * vt[i];
+                    o[j] = a;
+                }
+                continue;
+            }
             for (int t = 0; t < L; ++t) {
                 double w = exp(s[(int64_t)t * G + gh] - m) / den;
                 int64_t slot = (int64_t)J->bt[(int64_t)b * J->maxblk + t / J->P] * J->P + t % J->P;

@@ -28,12 +28,17 @@ def _stream(stream) -> int:
 class Codec:
     """One set of codec tables (Pi, S, codebook) on the current device."""
 
-    def __init__(self, head_dim: int, k_bits: int, v_bits: int, group: int, seed: int = 0, rotation: int = 0):
-        """rotation: native.TQ_ROTATION_DENSE (Haar) or native.TQ_ROTATION_HADAMARD."""
+    def __init__(self, head_dim: int, k_bits: int, v_bits: int, group: int, seed: int = 0, rotation: int = 0,
+                 values: str = "group"):
+        """rotation: native.TQ_ROTATION_DENSE (Haar) or native.TQ_ROTATION_HADAMARD;
+        values: "group" (per-group scale / zero) or "mse" (rotation + Lloyd-Max codebook)."""
         self.head_dim, self.k_bits, self.v_bits, self.group, self.seed = head_dim, k_bits, v_bits, group, seed
         self.qjl = k_bits <= 3
         self.rotation = rotation
-        self.handle = native.tq_init_rotation(head_dim, k_bits, v_bits, group, seed, rotation)
+        self.values = values
+        flags = (native.TQ_ROTATION_HADAMARD if rotation == native.TQ_ROTATION_HADAMARD else 0) | \
+            (native.TQ_VALUES_MSE if values == "mse" else 0)
+        self.handle = native.tq_init_ex(head_dim, k_bits, v_bits, group, seed, flags)
 
     def close(self):
         if getattr(self, "handle", None):

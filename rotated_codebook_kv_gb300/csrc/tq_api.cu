@@ -88,17 +88,17 @@ const char *tq_last_error(void) { return g_last_error.c_str(); }
 
 tq_status tq_init(int head_dim, int k_bits, int v_bits, int group, uint64_t seed, tq_handle *out)
 {
-    return tq_init_rotation(head_dim, k_bits, v_bits, group, seed, TQ_ROTATION_DENSE, out);
+    return tq_init_ex(head_dim, k_bits, v_bits, group, seed, 0u, out);
 }
 
-tq_status tq_init_rotation(int head_dim, int k_bits, int v_bits, int group, uint64_t seed, int rotation,
-                           tq_handle *out)
+tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t seed, unsigned flags, tq_handle *out)
 {
     if (!out) return fail(TQ_ERR_INVALID_ARG, "tq_init: out is NULL");
     *out = nullptr;
-    if (rotation != TQ_ROTATION_DENSE && rotation != TQ_ROTATION_HADAMARD)
-        return fail(TQ_ERR_UNSUPPORTED, "tq_init: rotation %d is neither TQ_ROTATION_DENSE nor TQ_ROTATION_HADAMARD",
-                    rotation);
+    if (flags & ~(TQ_ROTATION_HADAMARD | TQ_VALUES_MSE))
+        return fail(TQ_ERR_UNSUPPORTED, "tq_init: unknown flags 0x%x", flags);
+    const int rotation = (flags & TQ_ROTATION_HADAMARD) ? 1 : 0;
+    const bool vmse = (flags & TQ_VALUES_MSE) != 0;
     if (head_dim != 128 && head_dim != 256)
         return fail(TQ_ERR_UNSUPPORTED, "tq_init: head_dim %d not in {128, 256}", head_dim);
     if (!supported_bits(k_bits) || !supported_bits(v_bits))
@@ -108,6 +108,9 @@ tq_status tq_init_rotation(int head_dim, int k_bits, int v_bits, int group, uint
                     head_dim);
     tq::HostTables ht;
     if (!tq::build_tables(head_dim, k_bits, seed, rotation, &ht))
+        return fail(TQ_ERR_CUDA, "tq_init: Lloyd-Max iteration did not converge");
+    double vcent[16] = {}, vthr[16] = {};
+    if (vmse && !tq::build_codebook(v_bits, vcent, vthr))
         return fail(TQ_ERR_CUDA, "tq_init: Lloyd-Max iteration did not converge");
 
     const int d = head_dim;
@@ -188,7 +191,10 @@ tq_status tq_init_rotation(int head_dim, int k_bits, int v_bits, int group, uint
     k.k_code_bytes = d * k_bits / 8;
     k.k_sign_bytes = k.qjl ? d / 8 : 0;
     k.v_code_bytes = d * v_bits / 8;
-    k.v_meta_bytes = (d / group) * 4;
+    k.vmse = vmse ? 1 : 0;
+    k.v_meta_bytes = vmse ? 2 : (d / group) * 4;  // a bf16 norm, or (scale, zero) per group
+    for (int i = 0; vmse && i < (1 << v_bits); ++i) k.vcentroids[i] = static_cast<float>(vcent[i]);
+    for (int i = 0; vmse && i + 1 < (1 << v_bits); ++i) k.vthresholds[i] = static_cast<float>(vthr[i]);
     for (int i = 0; i < (1 << k_bits); ++i) k.centroids[i] = static_cast<float>(ht.centroids[i]);
     for (int i = 0; i + 1 < (1 << k_bits); ++i) k.thresholds[i] = static_cast<float>(ht.thresholds[i]);
     k.Pi = base;

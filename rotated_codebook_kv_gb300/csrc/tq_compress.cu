@@ -799,14 +799,14 @@ cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *
                             int64_t num_blocks, cudaStream_t st)
 {
     if (c.d == 128) return launch_compress_tc(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, c.num_sms, st);
-    if (c.rotation == TQ_ROTATION_HADAMARD && !c.qjl) {
+    if (c.rotation == 1 && !c.qjl) {
         switch (c.v_bits) {
         case 2: return launch_stream<256, 2>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
         case 3: return launch_stream<256, 3>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
         default: return launch_stream<256, 4>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
         }
     }
-    if (c.rotation == TQ_ROTATION_HADAMARD)
+    if (c.rotation == 1)
         return launch_compress_d<256, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
     return launch_compress_d<256, false>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
 }

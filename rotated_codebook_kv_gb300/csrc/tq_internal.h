@@ -35,7 +35,10 @@ struct Codec {
     const float *M_lo;
     const void *tc_image;  // d = 128: fp16 tensor-core operands (Pi 2^10 hi/lo, S 2^12 hi/lo), core-matrix layout
     const float *hsign;    // [d] random signs of the Hadamard rotation (Pi = H diag(hsign) / sqrt(d))
-    int rotation;          // TQ_ROTATION_DENSE or TQ_ROTATION_HADAMARD
+    int rotation;          // 0: dense Haar, 1: randomized Hadamard
+    int vmse;              // values coded by the rotation and a Lloyd-Max codebook (TQ_VALUES_MSE)
+    float vcentroids[16];  // value codebook (vmse), N(0,1) units, ascending
+    float vthresholds[16];
     unsigned int *status;  // device status word (TQ_DEVERR_* bits)
     long long wait_limit;  // clock cycles a kernel waits on one barrier before it reports TQ_DEVERR_TIMEOUT
     int num_sms;

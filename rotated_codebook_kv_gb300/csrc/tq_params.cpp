@@ -153,7 +153,7 @@ bool build_codebook(int bits, double *centroids, double *thresholds)
 
 bool build_tables(int d, int k_bits, uint64_t seed, int rotation, HostTables *out)
 {
-    if (rotation == TQ_ROTATION_HADAMARD) {
+    if (rotation == 1) {  // randomized Hadamard
         out->Pi = hadamard_rotation(d, seed);
         out->hsign = hadamard_signs(d, seed);
     } else {

@@ -14,7 +14,7 @@ import threading
 from . import build as _build
 
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_OOM = range(5)
-TQ_ROTATION_DENSE, TQ_ROTATION_HADAMARD = 0, 1
+TQ_ROTATION_DENSE, TQ_ROTATION_HADAMARD, TQ_VALUES_MSE = 0, 1, 2
 TQ_DEVERR_SLOT_RANGE, TQ_DEVERR_BLOCK_RANGE, TQ_DEVERR_SEQ_RANGE, TQ_DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 TQ_DEFAULT_WAIT_LIMIT = 2000000000
 
@@ -23,7 +23,7 @@ _c = ctypes
 _vp, _i32, _i64, _u64, _sz, _f32 = _c.c_void_p, _c.c_int, _c.c_int64, _c.c_uint64, _c.c_size_t, _c.c_float
 SIGNATURES = {
     "tq_init": (_i32, [_i32, _i32, _i32, _i32, _u64, _c.POINTER(_vp)]),
-    "tq_init_rotation": (_i32, [_i32, _i32, _i32, _i32, _u64, _i32, _c.POINTER(_vp)]),
+    "tq_init_ex": (_i32, [_i32, _i32, _i32, _i32, _u64, _c.c_uint, _c.POINTER(_vp)]),
     "tq_destroy": (_i32, [_vp]),
     "tq_cache_layout": (_i32, [_vp, _i32, _c.POINTER(_sz), _c.POINTER(_sz)]),
     "tq_compress_kv": (_i32, [_vp, _vp, _vp, _i64, _i32, _i64, _i64, _vp, _vp, _vp, _i32, _i64, _vp]),
@@ -91,10 +91,9 @@ def tq_init(head_dim: int, k_bits: int, v_bits: int, group: int, seed: int) -> i
     return h.value
 
 
-def tq_init_rotation(head_dim: int, k_bits: int, v_bits: int, group: int, seed: int, rotation: int) -> int:
+def tq_init_ex(head_dim: int, k_bits: int, v_bits: int, group: int, seed: int, flags: int) -> int:
     h = _vp()
-    _check("tq_init_rotation", load().tq_init_rotation(head_dim, k_bits, v_bits, group, seed, rotation,
-                                                       ctypes.byref(h)))
+    _check("tq_init_ex", load().tq_init_ex(head_dim, k_bits, v_bits, group, seed, flags, ctypes.byref(h)))
     return h.value
 
 

@@ -207,8 +207,9 @@ def test_compression_ratios_from_record_sizes():
     # 2-bit key codebook + QJL: key record bytes from the oracle's geometry
     k_rec = O.Oracle(d, 2, 3, 32, seed=0).geometry(16)["k_page"] // 16
     assert k_rec == 32 + 16 + 2 + 2
-    # 3-bit MSE value: 3-bit codes (oracle geometry) plus one 16-bit norm
-    v_rec = O.Oracle(d, 4, 3, 128, seed=0).geometry(16)["v_code"] + 2
+    # 3-bit MSE value: 3-bit codes plus one 16-bit norm, from the MSE-value record geometry
+    v_rec = O.Oracle(d, 4, 3, 128, seed=0, values="mse").geometry(16)["v_page"] // 16
+    assert v_rec == 48 + 2
     ratio = fp16_bytes / (k_rec + v_rec)
     assert round(ratio, 2) == gold["turboquant_2bit_k_qjl_3bit_v_vs_fp16"]["value"]
     assert round(16 / (4 + 8 / 32), 2) == gold["mxfp4_vs_fp16"]["value"]
@@ -483,3 +484,79 @@ def test_bypass_decode_special_cases():
     assert np.allclose(out[2, 0], rows.mean(0), atol=1e-12)  # identical keys: the mean value
     rows3 = np.concatenate([vd[bt[3, 0], 0, :16], vd[bt[3, 1], 0, :4]])
     assert np.allclose(out[3, 1], rows3.mean(0), atol=1e-12)  # zero query: the mean value
+
+
+
+# --------------------------------------------------------------------------- #
+# Values coded by the rotation and the Lloyd-Max codebook                        #
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("vbits", [2, 3, 4])
+def test_mse_values_codebook_distortion(vbits):
+    """Rotated unit values scaled by sqrt(d) are ~N(0,1): the coding error per
+    coordinate is the Lloyd-Max distortion of N(0,1) at v_bits (J. Max 1960), the
+    stored norm is bf16(||v||), a zero value is an all-zero record."""
+    d = 128
+    ora = O.Oracle(d, 4, vbits, 32, seed=5, values="mse")
+    rng = np.random.default_rng(50 + vbits)
+    v = _bf16(rng.standard_normal((3000, d)) * np.exp(rng.standard_normal((3000, 1))))
+    v[7] = 0
+    rec = ora.compress_rows(v=v)
+    vc = ora.params()["v_centroids"]
+    codes = np.stack([O.unpack(r, d, vbits) for r in rec["v_code"]])
+    rows = np.arange(len(v)) != 7
+    mse = np.mean((rec["vz"][rows] - vc[codes[rows]]) ** 2)
+    assert abs(mse - MAX_MSE[vbits]) < 0.05 * MAX_MSE[vbits]
+    assert np.array_equal(rec["v_meta"][:, 0], _bf16(np.linalg.norm(O.bf16_to_double(v), axis=1)))
+    assert not rec["v_code"][7].any() and rec["v_meta"][7, 0] == 0
+
+
+@pytest.mark.parametrize("d,rotation", [(128, 0), (256, 1)])
+def test_mse_values_dequant_rotates_back_to_the_codebook(d, rotation):
+    """V~ read back by dequant_slots, rotated by Pi and scaled by sqrt(d) / n16, is
+    exactly the value centroids of the codes numpy decodes from the raw bytes."""
+    from parity import read_records
+    P, Hkv, T = 16, 2, 40
+    ora = O.Oracle(d, 3, 3, 32, seed=12, rotation=rotation, values="mse")
+    rng = np.random.default_rng(12)
+    k = _bf16(rng.standard_normal((T, Hkv, d)))
+    v = _bf16(rng.standard_normal((T, Hkv, d)) * 2.0)
+    nb = T // P + 2
+    slots = rng.permutation(nb * P)[:T].astype(np.int64)
+    kc, vc = ora.compress_kv(k, v, slots, P, nb)
+    _, V = ora.dequant_slots(kc, vc, P, Hkv, slots)
+    rec = read_records(kc, vc, ora.geometry(P), d, 3, 3, 32, P, Hkv, slots, vmse=True)
+    n16 = O.bf16_to_double(rec["v_norm"])
+    u = np.einsum("ij,thj->thi", ora.params()["Pi"], V) * math.sqrt(d) / n16[..., None]
+    assert np.abs(u - ora.params()["v_centroids"][rec["v_code"]]).max() < 1e-10
+
+
+def test_mse_values_decode_matches_dense_attention():
+    """Decode accumulating the MSE values in the rotated space and rotating back
+    once equals dense softmax attention over the dequantised K~, V~ (numpy), and
+    equals the original-space decode."""
+    ora = O.Oracle(128, 3, 3, 32, seed=4, values="mse")
+    rng = np.random.default_rng(4)
+    B, Hkv, G, d, P = 2, 2, 2, 128, 16
+    lens = np.array([37, 5], np.int32)
+    npg = (lens + P - 1) // P
+    nb = int(npg.sum()) + 1
+    perm = rng.permutation(nb).astype(np.int32)
+    bt = np.full((B, int(npg.max())), -1, np.int32)
+    st = 0
+    for b in range(B):
+        bt[b, : npg[b]] = perm[st: st + npg[b]]
+        st += npg[b]
+    T = int(lens.sum())
+    k = _bf16(rng.standard_normal((T, Hkv, d)))
+    v = _bf16(rng.standard_normal((T, Hkv, d)))
+    slots = np.concatenate([bt[b, np.arange(lens[b]) // P].astype(np.int64) * P + np.arange(lens[b]) % P
+                            for b in range(B)])
+    kc, vc = ora.compress_kv(k, v, slots, P, nb)
+    q = _bf16(rng.standard_normal((B, Hkv * G, d)))
+    c = dict(q=q, kc=kc, vc=vc, bt=bt, lens=lens, P=P, Hkv=Hkv, slots=slots, d=d)
+    sm = d ** -0.5
+    ref = _numpy_attention(ora, c, sm)
+    for mode in (0, 1):
+        out = ora.decode(q, kc, vc, bt, lens, Hkv, P, sm, mode=mode)
+        assert np.abs(out - ref).max() < 1e-10 * max(1.0, np.abs(ref).max())
