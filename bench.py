@@ -47,22 +47,23 @@ FALLBACK_HBM_GBS = 6800.0
 # Algorithmic bytes                                                             #
 # --------------------------------------------------------------------------- #
 
-def record_bytes(d, kb, vb, g):
+def record_bytes(d, kb, vb, g, vmse=False):
+    """Key and value record bytes per token-head (vmse: values as codes + a bf16 norm)."""
     qjl = kb <= 3
     k = d * kb // 8 + (d // 8 + 2 if qjl else 0) + 2
-    v = d * vb // 8 + 4 * (d // g)
+    v = d * vb // 8 + (2 if vmse else 4 * (d // g))
     return k, v
 
 
-def compress_bytes(w, T):
+def compress_bytes(w, T, vmse=False):
     """Read K and V rows and the slot, write both records, per token-head."""
-    k, v = record_bytes(w.head_dim, w.k_bits, w.v_bits, w.group)
+    k, v = record_bytes(w.head_dim, w.k_bits, w.v_bits, w.group, vmse)
     rows = T * w.num_kv_heads
     return rows * (4 * w.head_dim + k + v) + T * 8
 
 
-def decode_bytes(w, seq_lens, max_blocks):
-    k, v = record_bytes(w.head_dim, w.k_bits, w.v_bits, w.group)
+def decode_bytes(w, seq_lens, max_blocks, vmse=False):
+    k, v = record_bytes(w.head_dim, w.k_bits, w.v_bits, w.group, vmse)
     toks = int(sum(seq_lens))
     pages = sum((int(s) + w.page_size - 1) // w.page_size for s in seq_lens)
     qo = 2 * w.batch * w.num_q_heads * w.head_dim * 2
@@ -428,16 +429,18 @@ def per_config(dev, peak, reps):
         return statistics.median(ms) * 1e-3
 
     out = {}
-    for name, w, rot in (("compress_only", W.compress_only(), 0), ("paged_decode", W.paged_decode(), 0),
-                         ("wide_head_decode", W.wide_head_decode(), 0),
-                         ("wide_head_decode_hadamard", W.wide_head_decode(), 1)):
+    for name, w, rot, vals in (("compress_only", W.compress_only(), 0, "group"),
+                               ("paged_decode", W.paged_decode(), 0, "group"),
+                               ("wide_head_decode", W.wide_head_decode(), 0, "group"),
+                               ("wide_head_decode_hadamard", W.wide_head_decode(), 1, "group"),
+                               ("paged_decode_mse_values", W.paged_decode(), 0, "mse")):
         b = W.generate(w, device=dev)
-        codec = Codec(w.head_dim, w.k_bits, w.v_bits, w.group, w.codec_seed(), rotation=rot)
+        codec = Codec(w.head_dim, w.k_bits, w.v_bits, w.group, w.codec_seed(), rotation=rot, values=vals)
         kc, vc = codec.alloc_cache(b.num_blocks, w.num_kv_heads, w.page_size, device=dev)
         T = b.num_tokens
         t_c = timed(lambda: codec.compress_kv(b.k, b.v, b.slot_mapping, kc, vc, w.page_size, b.num_blocks,
                                               stream=stream))
-        cb = compress_bytes(w, T)
+        cb = compress_bytes(w, T, vals == "mse")
         ent = {"compress_mtoken_heads_per_s": round(T * w.num_kv_heads / t_c / 1e6, 1),
                "compress_gbs": round(cb / t_c / 1e9, 1), "compress_frac": round(cb / t_c / 1e9 / peak, 4),
                "compress_us": round(t_c * 1e6, 1)}
@@ -450,7 +453,7 @@ def per_config(dev, peak, reps):
                                                        w.page_size, b.num_blocks, b.sm_scale, splits=splits,
                                                        workspace=ws, out=o, stream=stream))
             lens = b.seq_lens.cpu().tolist()
-            db = decode_bytes(w, lens, maxb)
+            db = decode_bytes(w, lens, maxb, vals == "mse")
             ent.update({"decode_gbs": round(db / t_d / 1e9, 1), "decode_frac": round(db / t_d / 1e9 / peak, 4),
                         "decode_us": round(t_d * 1e6, 1), "decode_splits": splits,
                         "decode_kv_tokens_per_s": round(sum(lens) * w.num_kv_heads / t_d, 1),
@@ -493,7 +496,8 @@ def per_config(dev, peak, reps):
         del kp, vp, b, codec
         torch.cuda.empty_cache()
     out["timing"] = f"median of {reps} calls after 2 warm-up calls; L2 flushed before each call"
-    out["wide_head_decode_hadamard"]["rotation"] = "randomized Hadamard (tq_init_rotation)"
+    out["wide_head_decode_hadamard"]["rotation"] = "randomized Hadamard (tq_init_ex)"
+    out["paged_decode_mse_values"]["values"] = "rotation + Lloyd-Max codebook (tq_init_ex, TQ_VALUES_MSE)"
     return out
 
 

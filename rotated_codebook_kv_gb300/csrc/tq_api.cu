@@ -50,6 +50,30 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 bool supported_bits(int b) { return b >= 2 && b <= 4; }
 
+// The scale s in [1, 2) (steps of 2^-16) that brings every s * c closest, relative
+// to its size, to an fp16 value: decode multiplies fp16(s c) and divides s out
+// once at the end, so the centroids lose less than the 2^-12 of a plain fp16 rounding.
+float fp16_friendly_scale(const double *c, int n)
+{
+    double best = 1e300;
+    float best_s = 1.f;
+    for (int k = 0; k < 65536; ++k) {
+        const float sc = 1.f + static_cast<float>(k) / 65536.f;
+        double worst = 0.0;
+        for (int i = 0; i < n && worst < best; ++i) {
+            const double x = static_cast<double>(sc) * c[i];
+            if (x == 0.0) continue;
+            const double h = static_cast<double>(__half2float(__float2half_rn(static_cast<float>(x))));
+            worst = std::fmax(worst, std::fabs(h - x) / std::fabs(x));
+        }
+        if (worst < best) {
+            best = worst;
+            best_s = sc;
+        }
+    }
+    return best_s;
+}
+
 }  // namespace
 
 void *tq::handle_static_scratch(tq_handle h) { return h ? h->static_scratch : nullptr; }
@@ -195,6 +219,7 @@ tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t s
     k.v_meta_bytes = vmse ? 2 : (d / group) * 4;  // a bf16 norm, or (scale, zero) per group
     for (int i = 0; vmse && i < (1 << v_bits); ++i) k.vcentroids[i] = static_cast<float>(vcent[i]);
     for (int i = 0; vmse && i + 1 < (1 << v_bits); ++i) k.vthresholds[i] = static_cast<float>(vthr[i]);
+    k.vlut_scale = vmse ? fp16_friendly_scale(vcent, 1 << v_bits) : 1.f;
     for (int i = 0; i < (1 << k_bits); ++i) k.centroids[i] = static_cast<float>(ht.centroids[i]);
     for (int i = 0; i + 1 < (1 << k_bits); ++i) k.thresholds[i] = static_cast<float>(ht.thresholds[i]);
     k.Pi = base;

@@ -127,11 +127,14 @@ __device__ __forceinline__ void fwht_rows(const float *__restrict__ hsign, const
     }
 }
 
-// Exact path for one key row, run by one warp.  Writes the row's codes, its
-// QJL projections (sign-exact) into p_out, and the bf16 norm / gamma.
+// Exact path for one row, run by one warp, against the codebook (thr, cent,
+// bits): a key row (with QJL when qjl) or a value row coded like keys.  Writes
+// the row's codes, its QJL projections (sign-exact) into p_out, and the bf16
+// norm / gamma.
 template <int D>
 __device__ void precise_key_row(const Codec &C, const uint16_t *__restrict__ src, uint8_t *codes, float *p_out,
-                                double *scratch, uint16_t *n16, uint16_t *g16)
+                                double *scratch, uint16_t *n16, uint16_t *g16, const float *thr, const float *cent,
+                                int bits, bool qjl)
 {
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
@@ -182,26 +185,26 @@ __device__ void precise_key_row(const Codec &C, const uint16_t *__restrict__ src
     }
     __syncwarp();
     const double zscale = sqrt(static_cast<double>(D)) / n_sc;
-    const int nthr = (1 << C.k_bits) - 1;
+    const int nthr = (1 << bits) - 1;
     double rr = 0.0;
 #pragma unroll
     for (int m = 0; m < E; ++m) {
         const int i = lane + 32 * m;
         const double z = (static_cast<double>(yh[m]) + static_cast<double>(yl[m])) * zscale;
         int code = 0;
-        for (int t = 0; t < nthr; ++t) code += (static_cast<double>(C.thresholds[t]) <= z);
+        for (int t = 0; t < nthr; ++t) code += (static_cast<double>(thr[t]) <= z);
         codes[i] = static_cast<uint8_t>(code);
-        const double r = z - static_cast<double>(C.centroids[code]);
+        const double r = z - static_cast<double>(cent[code]);
         scratch[i] = r;
         rr += r * r;
     }
     rr = warp_sum(rr);
     if (lane == 0) {
         *n16 = double_to_bf16_bits(ldexp(n_sc, ex));
-        if (C.qjl) *g16 = double_to_bf16_bits(sqrt(rr) / sqrt(static_cast<double>(D)));
+        if (qjl) *g16 = double_to_bf16_bits(sqrt(rr) / sqrt(static_cast<double>(D)));
     }
     __syncwarp();
-    if (!C.qjl) return;
+    if (!qjl) return;
     float ps[E], pc[E];
 #pragma unroll
     for (int m = 0; m < E; ++m) ps[m] = pc[m] = 0.f;
@@ -222,7 +225,7 @@ __device__ void precise_key_row(const Codec &C, const uint16_t *__restrict__ src
     __syncwarp();
 }
 
-template <int D, bool HAD>
+template <int D, bool HAD, bool VMSE>
 __global__ void __launch_bounds__(kThreads, 2)
 compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
                 int64_t rows, int Hkv, int64_t ks, int64_t vs, const int64_t *__restrict__ slots,
@@ -362,7 +365,8 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         const int64_t t = r / Hkv;
         const int h = static_cast<int>(r - t * Hkv);
         precise_key_row<D>(C, kin + t * ks + static_cast<int64_t>(h) * D, codes + row * CS, kf + row * D,
-                           scratch + warp * D, &s_n16[row], &s_g16[row]);
+                           scratch + warp * D, &s_n16[row], &s_g16[row], C.thresholds, C.centroids, C.k_bits,
+                           C.qjl != 0);
     }
     __syncthreads();
     // ---- pack and store: one warp per row ------------------------------------
@@ -389,6 +393,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * off) = zero ? 0 : s_g16[row];
         }
         if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * off) = zero ? 0 : s_n16[row];
+        if constexpr (VMSE) continue;  // values take the codebook pass below
 
         // ---- value row -------------------------------------------------------
         constexpr int E = D / 32;
@@ -457,6 +462,87 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
                 meta;
         }
         __syncwarp();
+    }
+    if constexpr (VMSE) {
+        // ==== values coded like keys without QJL (brightcoding blog, "What is
+        // TurboQuant-GPU?" / "Example 4"): norm, rotation, Lloyd-Max codes ====
+        __syncthreads();  // the key pass is done with kf, yb and codes
+        if (tid < 18) s_thr[tid] = tid == 0 ? -INFINITY : (tid <= (1 << C.v_bits) - 1 ? C.vthresholds[tid - 1] : INFINITY);
+        if (tid < 16) s_cent[tid] = C.vcentroids[tid];
+        for (int e = tid; e < TM * (D / 8); e += kThreads) {
+            const int row = e / (D / 8), c8 = e - row * (D / 8);
+            const int64_t r = r0 + row;
+            uint4 u = make_uint4(0, 0, 0, 0);
+            if (r < rows) {
+                const int64_t t = r / Hkv;
+                const int h = static_cast<int>(r - t * Hkv);
+                u = __ldg(reinterpret_cast<const uint4 *>(vin + t * vs + static_cast<int64_t>(h) * D) + c8);
+            }
+            *reinterpret_cast<float4 *>(kf + row * D + c8 * 8) =
+                make_float4(bf16_to_float(u.x & 0xffffu), bf16_to_float(u.x >> 16), bf16_to_float(u.y & 0xffffu),
+                            bf16_to_float(u.y >> 16));
+            *reinterpret_cast<float4 *>(kf + row * D + c8 * 8 + 4) =
+                make_float4(bf16_to_float(u.z & 0xffffu), bf16_to_float(u.z >> 16), bf16_to_float(u.w & 0xffffu),
+                            bf16_to_float(u.w >> 16));
+        }
+        __syncthreads();
+        for (int row = warp; row < TM; row += kWarps) {
+            float ss = 0.f, mx = 0.f;
+            for (int j = lane; j < D; j += 32) {
+                const float x = kf[row * D + j];
+                ss = fmaf(x, x, ss);
+                mx = fmaxf(mx, fabsf(x));
+            }
+            ss = warp_sum(ss);
+            mx = warp_max(mx);
+            if (lane == 0) {
+                int flag = 0;
+                if (mx == 0.f) flag = 2;
+                else if (!(mx >= 0x1p-30f && mx <= 0x1p30f)) flag = 1;
+                const float n = sqrtf(ss);
+                s_scale[row] = (flag == 0) ? sqrtd / n : 0.f;
+                s_flag[row] = flag;
+                s_n16[row] = flag == 2 ? 0 : float_to_bf16_bits(n);
+            }
+        }
+        if constexpr (HAD) fwht_rows<D, TM>(C.hsign, kf, yb);
+        else matvec_rows<D, TM>(C.PiT, kf, yb);
+        __syncthreads();
+        const int vb = C.v_bits;
+        for (int e = tid; e < TM * D; e += kThreads) {
+            const int row = e / D, i = e - row * D;
+            const int fl = s_flag[row];
+            const float z = yb[e] * s_scale[row];
+            int code = 0;
+            for (int step = 1 << (vb - 1); step > 0; step >>= 1)
+                if (s_thr[code + step] <= z) code += step;
+            const float dmin = fminf(z - s_thr[code], s_thr[code + 1] - z);
+            codes[row * CS + i] = static_cast<uint8_t>(fl == 2 ? 0 : code);
+            if (fl == 0 && dmin < kCodeGuard) s_flag[row] = 1;
+        }
+        __syncthreads();
+        for (int row = warp; row < TM; row += kWarps) {
+            if (s_flag[row] != 1 || s_dst[row] < 0) continue;
+            const int64_t r = r0 + row;
+            const int64_t t = r / Hkv;
+            const int h = static_cast<int>(r - t * Hkv);
+            precise_key_row<D>(C, vin + t * vs + static_cast<int64_t>(h) * D, codes + row * CS, kf + row * D,
+                               scratch + warp * D, &s_n16[row], &s_g16[row], C.vthresholds, C.vcentroids, C.v_bits,
+                               false);
+        }
+        __syncthreads();
+        for (int row = warp; row < TM; row += kWarps) {
+            const int64_t dst = s_dst[row];
+            if (dst < 0) continue;
+            const int off = s_off[row];
+            const bool zero = (s_flag[row] == 2);
+            uint8_t *vrec = vc + dst * G.v_page;
+            const int nw = D * C.v_bits / 32;
+            if (lane < nw)
+                *reinterpret_cast<uint32_t *>(vrec + static_cast<int64_t>(off) * C.v_code_bytes + 4 * lane) =
+                    zero ? 0u : pack_word(codes + row * CS, lane, C.v_bits);
+            if (lane == 0) *reinterpret_cast<uint16_t *>(vrec + G.v_meta_off + 2 * off) = zero ? 0 : s_n16[row];
+        }
     }
 }
 
@@ -777,17 +863,17 @@ cudaError_t launch_stream(const Codec &c, const PageGeom &pg, const uint16_t *k,
     return cudaGetLastError();
 }
 
-template <int D, bool HAD>
+template <int D, bool HAD, bool VMSE>
 cudaError_t launch_compress_d(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
                               int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
                               int64_t num_blocks, cudaStream_t st)
 {
     const size_t smem = CompressSmem<D>::kBytes;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(compress_kernel<D, HAD>), smem);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(compress_kernel<D, HAD, VMSE>), smem);
     if (e != cudaSuccess) return e;
     const int64_t rows = T * Hkv;
     const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-    compress_kernel<D, HAD><<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(c, pg, k, v, rows, Hkv, ks, vs, slots,
+    compress_kernel<D, HAD, VMSE><<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(c, pg, k, v, rows, Hkv, ks, vs, slots,
                                                                              kc, vc, num_blocks);
     return cudaGetLastError();
 }
@@ -798,6 +884,14 @@ cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *
                             int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
                             int64_t num_blocks, cudaStream_t st)
 {
+    if (c.vmse) {  // values coded like keys: the two-pass SIMT kernel at either head dim
+        const bool had = c.rotation == 1;
+        if (c.d == 128)
+            return had ? launch_compress_d<128, true, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st)
+                       : launch_compress_d<128, false, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+        return had ? launch_compress_d<256, true, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st)
+                   : launch_compress_d<256, false, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+    }
     if (c.d == 128) return launch_compress_tc(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, c.num_sms, st);
     if (c.rotation == 1 && !c.qjl) {
         switch (c.v_bits) {
@@ -807,8 +901,8 @@ cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *
         }
     }
     if (c.rotation == 1)
-        return launch_compress_d<256, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
-    return launch_compress_d<256, false>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+        return launch_compress_d<256, true, false>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+    return launch_compress_d<256, false, false>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
 }
 
 }  // namespace tq

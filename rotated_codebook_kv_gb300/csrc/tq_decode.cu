@@ -117,10 +117,11 @@ __global__ void __launch_bounds__(2 * D) qrot_kernel(const Codec C, const uint16
 // shared memory, then thread j sums its coordinate over the splits.
 constexpr int kMaxSplits = 1024;
 
-template <int D>
-__global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs A)
+template <int D, bool UNROT>
+__global__ void __launch_bounds__(D) combine_kernel(const Codec C, const DecodeArgs A)
 {
     __shared__ float sw[kMaxSplits];
+    __shared__ float so[UNROT ? D : 1];
     __shared__ float red[D / 32];
     __shared__ float s_den;
     const int row = blockIdx.x;  // b * Hq + h
@@ -171,7 +172,18 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs A)
         if (sw[s] != 0.f) n0 = fmaf(sw[s], acc[s * rows * D], n0);
     const float num = (n0 + n1) + (n2 + n3);
     const float dd = s_den;
-    const float o = (dd > 0.f) ? num / dd : 0.f;
+    float o = (dd > 0.f) ? num / dd : 0.f;
+    if constexpr (UNROT) {
+        // values coded by the rotation: the merged output is in the rotated space (with
+        // the table's fp16 scale, the 2^-4 of the weights and 1/sqrt(d) left to apply):
+        // o = Pi^T o_rot, d^2 FMAs per query head
+        so[j] = o * (16.f / (C.vlut_scale * sqrtf(static_cast<float>(D))));
+        __syncthreads();
+        float a = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < D; ++i) a = fmaf(__ldg(C.Pi + i * D + j), so[i], a);
+        o = a;
+    }
     A.ws.out32[static_cast<size_t>(row) * D + j] = o;
     A.out[static_cast<size_t>(row) * D + j] = float_to_bf16_bits(o);
 }
@@ -179,11 +191,12 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeArgs A)
 template <int D, int KB, int VB>
 cudaError_t launch_dmma(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st)
 {
+    if (c.vmse) return launch_dmma_vmse(c, pg, a, st);
     const size_t smem = dmma::DecSmem<D, KB>::bytes(pg);
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(dmma::decode_mma_kernel<D, KB, VB>), smem);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(dmma::decode_mma_kernel<D, KB, VB, false>), smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.splits, a.Hkv, a.B);
-    dmma::decode_mma_kernel<D, KB, VB><<<grid, dmma::kThreads, smem, st>>>(c, pg, a);
+    dmma::decode_mma_kernel<D, KB, VB, false><<<grid, dmma::kThreads, smem, st>>>(c, pg, a);
     return cudaGetLastError();
 }
 
@@ -210,16 +223,20 @@ cudaError_t launch_decode_d(const Codec &c, const PageGeom &pg, const DecodeArgs
     default: e = launch_dmma_kb<D, 4>(c, pg, a, st); break;
     }
     if (e != cudaSuccess) return e;
-    combine_kernel<D><<<a.B * a.Hq, D, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_combine(c, a, st, c.vmse != 0);
 }
 
 }  // namespace
 
-cudaError_t launch_combine(const Codec &c, const DecodeArgs &a, cudaStream_t st)
+cudaError_t launch_combine(const Codec &c, const DecodeArgs &a, cudaStream_t st, bool unrotate)
 {
-    if (c.d == 128) combine_kernel<128><<<a.B * a.Hq, 128, 0, st>>>(a);
-    else combine_kernel<256><<<a.B * a.Hq, 256, 0, st>>>(a);
+    if (c.d == 128) {
+        if (unrotate) combine_kernel<128, true><<<a.B * a.Hq, 128, 0, st>>>(c, a);
+        else combine_kernel<128, false><<<a.B * a.Hq, 128, 0, st>>>(c, a);
+    } else {
+        if (unrotate) combine_kernel<256, true><<<a.B * a.Hq, 256, 0, st>>>(c, a);
+        else combine_kernel<256, false><<<a.B * a.Hq, 256, 0, st>>>(c, a);
+    }
     return cudaGetLastError();
 }
 

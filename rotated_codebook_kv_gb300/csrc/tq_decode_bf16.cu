@@ -418,7 +418,7 @@ cudaError_t launch_bypass(const CUtensorMap &tk, const CUtensorMap &tv, const Co
     decode_bf16_kernel<D><<<grid, kThreads, smem, st>>>(tk, tv, c, P, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_combine(c, a, st);
+    return launch_combine(c, a, st, false);
 }
 
 }  // namespace

@@ -94,8 +94,10 @@ __device__ __forceinline__ float fast_exp2(float x)
     return y;
 }
 
-// Dynamic shared memory layout of the tensor-core decode kernel.
-template <int D, int KB>
+// Dynamic shared memory layout of the tensor-core decode kernel.  VM: values
+// coded by the rotation and a Lloyd-Max codebook, whose fp16 centroid pairs
+// (indexed by the codes of two tokens) follow the key tables in 8 copies.
+template <int D, int KB, int VB = 2, bool VM = false>
 struct DecSmem {
     static constexpr int kPairBits = 2 * KB;
     static constexpr int kPairEntries = 1 << kPairBits;
@@ -110,7 +112,8 @@ struct DecSmem {
     static constexpr size_t kSignLut = sizeof(uint2) * 16;               // 4 sign bits -> two +-1 fp16 pairs
     static constexpr size_t kQfrag = sizeof(uint4) * (D / 16) * 32;      // [k-step][lane] (qh0, qh2, ql0, ql2)
     static constexpr size_t kSfrag = sizeof(uint2) * (D / 16) * 32;      // [k-step][lane] (qs0, qs2)
-    static constexpr size_t kHeader = kLut + kSignLut + kQfrag + kSfrag + 256;  // + page flags, zeros, mbarriers
+    static constexpr size_t kVLut = VM ? sizeof(uint32_t) * (1u << (2 * VB)) * 8 : 0;
+    static constexpr size_t kHeader = kLut + kSignLut + kQfrag + kSfrag + 256 + kVLut;  // + flags, zeros, mbarriers
     __host__ __device__ static size_t stage_bytes(const PageGeom &pg)
     {
         return static_cast<size_t>(kChunk / pg.P) * (pg.k_page + pg.v_page);
@@ -142,10 +145,19 @@ __device__ __forceinline__ void mbar_init_cta(uint64_t *mbar, int count)
                  "r"(count));
 }
 
-template <int D, int KB, int VB>
+// A value code pair of two tokens (low / high 16-bit halves of x, bits [sh, sh + VB))
+// as the byte offset of its entry in the value centroid table.
+template <int VB>
+__device__ __forceinline__ uint32_t vpair_off(uint32_t x, int sh)
+{
+    constexpr uint32_t M = (1u << VB) - 1u;
+    return ((((x >> sh) & M) | (((x >> (16 + sh)) & M) << VB)) << 5);  // 8 copies x 4 bytes per entry
+}
+
+template <int D, int KB, int VB, bool VM>
 __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(const Codec C, const PageGeom PG, const DecodeArgs A)
 {
-    using SM = DecSmem<D, KB>;
+    using SM = DecSmem<D, KB, VB, VM>;
     constexpr bool QJL = (KB <= 3);
     constexpr int KS = D / 16;                 // k-steps over coordinates
     constexpr int MT = D / 16;                 // m-tiles of output coordinates
@@ -197,6 +209,14 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
         const float x0 = C.centroids[c0], x1 = C.centroids[c1];
         const float h0 = __half2float(__float2half_rn(x0)), h1 = __half2float(__float2half_rn(x1));
         lut[e] = make_uint2(pack_half2(h0, h1), pack_half2((x0 - h0) * kLoScale, (x1 - h1) * kLoScale));
+    }
+    const uint32_t vlut_off = static_cast<uint32_t>(SM::kLut + SM::kSignLut + SM::kQfrag + SM::kSfrag + 256);
+    if constexpr (VM) {  // value centroid pairs, fp16 of vlut_scale * c (the scale keeps them near fp16 points)
+        uint32_t *vlut = reinterpret_cast<uint32_t *>(smem + vlut_off);
+        for (int e = tid; e < (1 << (2 * VB)) * 8; e += kThreads) {
+            const int ent = e >> 3;
+            vlut[e] = pack_half2(C.vcentroids[ent & ((1 << VB) - 1)] * C.vlut_scale, C.vcentroids[ent >> VB] * C.vlut_scale);
+        }
     }
     if (tid < 16) {
         zero_meta[tid] = 0u;
@@ -491,21 +511,37 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
                     mrow[j][i] = (live[j] && pos0[j] + tq[i] < L) ? vp[j] + PG.v_meta_off + t * C.v_meta_bytes : zero_off;
                     vrow[j][i] = vp[j] + t * C.v_code_bytes;
                 }
-                // zero term: A rows = groups (`row` < ng), columns = tokens
-                uint32_t za0 = 0u, za2 = 0u;
-                if (row < ng) {
-                    za0 = __byte_perm(ld32(mrow[j][0] + 4 * row), ld32(mrow[j][1] + 4 * row), 0x7632);
-                    za2 = __byte_perm(ld32(mrow[j][2] + 4 * row), ld32(mrow[j][3] + 4 * row), 0x7632);
+                if constexpr (!VM) {
+                    // zero term: A rows = groups (`row` < ng), columns = tokens
+                    uint32_t za0 = 0u, za2 = 0u;
+                    if (row < ng) {
+                        za0 = __byte_perm(ld32(mrow[j][0] + 4 * row), ld32(mrow[j][1] + 4 * row), 0x7632);
+                        za2 = __byte_perm(ld32(mrow[j][2] + 4 * row), ld32(mrow[j][3] + 4 * row), 0x7632);
+                    }
+                    mma16816(zt, za0, 0u, za2, 0u, b0[j], b1[j]);
                 }
-                mma16816(zt, za0, 0u, za2, 0u, b0[j], b1[j]);
             }
             // ---- P.V over coordinate m-tiles: row r <-> 16 mt + 2 r, row r + 8 <-> 16 mt + 2 r + 1 ----
-            constexpr uint32_t VM = ((1u << VB) - 1u) * 0x00010001u;
+            constexpr uint32_t VCM = ((1u << VB) - 1u) * 0x00010001u;
             const uint32_t bias = 0x64006400u;
             uint32_t bs0[2] = {0u, 0u}, bs1[2] = {0u, 0u};
+            if constexpr (VM) {  // one weight per token: its value norm, times 2^-4 to stay inside fp16
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        w[i] = (mrow[j][i] != zero_off)
+                                   ? bf16_to_float(ldu16(vp[j] + PG.v_meta_off + 2 * (o0[j] + tq[i]))) * 0.0625f
+                                   : 0.f;
+                    bs0[j] = hmul2_u32(b0[j], pack_half2(w[0], w[1]));
+                    bs1[j] = hmul2_u32(b1[j], pack_half2(w[2], w[3]));
+                }
+            }
+            const uint32_t vlut_lane = vlut_off + 4u * (lane & 7);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                if ((mt & mt_mask) == 0) {  // a new value group: scale the B operands
+                if (!VM && (mt & mt_mask) == 0) {  // a new value group: scale the B operands
                     const int g4 = 4 * ((16 * mt) >> gshift);
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
@@ -532,10 +568,18 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
                         xb = __byte_perm(__funnelshift_r(ld32(vrow[j][2] + w), ld32(vrow[j][2] + w + 4), sh),
                                          __funnelshift_r(ld32(vrow[j][3] + w), ld32(vrow[j][3] + w + 4), sh), 0x5410);
                     }
-                    const uint32_t a0 = unbias_half2((xa & VM) | bias);
-                    const uint32_t a1 = unbias_half2(((xa >> VB) & VM) | bias);
-                    const uint32_t a2 = unbias_half2((xb & VM) | bias);
-                    const uint32_t a3 = unbias_half2(((xb >> VB) & VM) | bias);
+                    uint32_t a0, a1, a2, a3;
+                    if constexpr (VM) {  // value centroids of the two tokens' codes
+                        a0 = ld32(vlut_lane + vpair_off<VB>(xa, 0));
+                        a1 = ld32(vlut_lane + vpair_off<VB>(xa, VB));
+                        a2 = ld32(vlut_lane + vpair_off<VB>(xb, 0));
+                        a3 = ld32(vlut_lane + vpair_off<VB>(xb, VB));
+                    } else {
+                        a0 = unbias_half2((xa & VCM) | bias);
+                        a1 = unbias_half2(((xa >> VB) & VCM) | bias);
+                        a2 = unbias_half2((xb & VCM) | bias);
+                        a3 = unbias_half2(((xb >> VB) & VCM) | bias);
+                    }
                     mma16816(o[mt], a0, a1, a2, a3, bs0[j], bs1[j]);
                 }
             }

@@ -4,7 +4,9 @@
 // bf16 for any third-party attention.  Keys return to the original space:
 //   K~ = n Pi^T ( c[code] / sqrt(d) + [QJL] sqrt(pi/2)/d * gamma * S^T (2 sigma - 1) )
 // and values are code * scale + zero per group (0xsero/turboquant, "Value
-// Compression").  One CTA per (slot, kv head), d threads, fp32 arithmetic.
+// Compression"), or -- values coded by the rotation and their own Lloyd-Max
+// codebook -- V~ = n Pi^T c[code] / sqrt(d).  One CTA per (slot, kv head), d
+// threads, fp32 arithmetic.
 #include <cuda_runtime.h>
 
 #include "tq_device.cuh"
@@ -60,6 +62,16 @@ dequant_kernel(const Codec C, const PageGeom G, const uint8_t *__restrict__ kc, 
     const int vbit = j * C.v_bits;
     const uint32_t vw = vb[vbit >> 3] | (static_cast<uint32_t>(vb[min((vbit >> 3) + 1, C.v_code_bytes - 1)]) << 8);
     const uint32_t vcode = (vw >> (vbit & 7)) & ((1u << C.v_bits) - 1u);
+    if (C.vmse) {  // V~ = n Pi^T c[code] / sqrt(d) (values coded like keys, no QJL)
+        __syncthreads();  // every thread has read u
+        u[j] = C.vcentroids[vcode] * rsqrtf(static_cast<float>(D));
+        __syncthreads();
+        float a = 0.f;
+        for (int i = 0; i < D; ++i) a = fmaf(__ldg(C.Pi + i * D + j), u[i], a);
+        const float vn = bf16_to_float(*reinterpret_cast<const uint16_t *>(vr + G.v_meta_off + 2 * off));
+        vout[o] = float_to_bf16_bits(vn * a);
+        return;
+    }
     const __half2 sz = *reinterpret_cast<const __half2 *>(vr + G.v_meta_off + static_cast<int64_t>(off) * C.v_meta_bytes +
                                                          4 * (j / C.group));
     const float2 f = __half22float2(sz);

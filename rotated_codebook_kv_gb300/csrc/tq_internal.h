@@ -39,6 +39,7 @@ struct Codec {
     int vmse;              // values coded by the rotation and a Lloyd-Max codebook (TQ_VALUES_MSE)
     float vcentroids[16];  // value codebook (vmse), N(0,1) units, ascending
     float vthresholds[16];
+    float vlut_scale;      // vmse: decode keeps fp16(vlut_scale * c) (a scale chosen so these are near fp16 points)
     unsigned int *status;  // device status word (TQ_DEVERR_* bits)
     long long wait_limit;  // clock cycles a kernel waits on one barrier before it reports TQ_DEVERR_TIMEOUT
     int num_sms;
@@ -101,8 +102,11 @@ cudaError_t launch_dequant(const Codec &c, const PageGeom &pg, const uint8_t *kc
                            uint16_t *v_out, cudaStream_t st);
 
 cudaError_t launch_decode(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st);
-// The log-sum-exp merge of split partials into bf16 (and fp32) outputs.
-cudaError_t launch_combine(const Codec &c, const DecodeArgs &a, cudaStream_t st);
+// The log-sum-exp merge of split partials into bf16 (and fp32) outputs; with
+// `unrotate` the merged output is rotated back by Pi^T (values coded by the rotation).
+cudaError_t launch_combine(const Codec &c, const DecodeArgs &a, cudaStream_t st, bool unrotate);
+// The split-K decode kernel for values coded by the rotation (its own translation unit).
+cudaError_t launch_dmma_vmse(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st);
 
 // Device address of the no-allocation decode's static scratch array for the
 // context current on the calling thread (looked up, not cached).
