@@ -89,6 +89,15 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s (burst) from MEASURED_PEAKS.json, else the recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, ValueError, KeyError, TypeError):
+        return 1900.0
+
+
 def committed_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
     import hashlib
@@ -495,6 +504,32 @@ def per_config(dev, peak, reps):
                      "bytes_per_token_head": 4 * d}
         del kp, vp, b, codec
         torch.cuda.empty_cache()
+    # chunked prefill over the compressed cache: the last 64 positions of every sequence of
+    # the paged workload attend causally to their compressed context
+    w = W.paged_decode()
+    b = W.generate(w, device=dev)
+    codec = Codec(w.head_dim, w.k_bits, w.v_bits, w.group, w.codec_seed())
+    kc, vc = codec.alloc_cache(b.num_blocks, w.num_kv_heads, w.page_size, device=dev)
+    codec.compress_kv(b.k, b.v, b.slot_mapping, kc, vc, w.page_size, b.num_blocks, stream=stream)
+    Tq = 64
+    gq = torch.Generator(device=dev).manual_seed(5)
+    q = torch.randn(w.batch, Tq, w.num_q_heads, w.head_dim, generator=gq, device=dev).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    t_p = timed(lambda: codec.prefill_attention(q, kc, vc, b.block_table, b.seq_lens, w.num_kv_heads, w.page_size,
+                                                b.num_blocks, b.sm_scale, out=o, stream=stream))
+    lens = b.seq_lens.cpu().tolist()
+    pairs = sum(sum(max(L - Tq + i + 1, 0) for i in range(Tq)) for L in lens) * w.num_q_heads
+    flops = pairs * 4 * w.head_dim  # q.k and p.v per (query token, head, key token)
+    tf_peak = measured_tensor_peak()
+    if codec.get_status(stream) != 0:
+        raise RuntimeError("device status bits set in the prefill workload")
+    out["prefill_paged_decode_chunk64"] = {
+        "prefill_us": round(t_p * 1e6, 1), "prefill_query_tokens_per_s": round(w.batch * Tq / t_p, 1),
+        "attention_tflops": round(flops / t_p / 1e12, 2), "tensor_peak_tflops": tf_peak,
+        "tensor_frac": round(flops / t_p / 1e12 / tf_peak, 4),
+        "note": "useful attention math (4 d flops per query-head-key pair) over the measured bf16 peak"}
+    del q, o, kc, vc, b, codec
+    torch.cuda.empty_cache()
     out["timing"] = f"median of {reps} calls after 2 warm-up calls; L2 flushed before each call"
     out["wide_head_decode_hadamard"]["rotation"] = "randomized Hadamard (tq_init_ex)"
     out["paged_decode_mse_values"]["values"] = "rotation + Lloyd-Max codebook (tq_init_ex, TQ_VALUES_MSE)"

@@ -199,6 +199,36 @@ tq_status tq_decode_attention(tq_handle h, const uint16_t *q, const uint8_t *k_c
                               void *stream);
 
 /*
+ * tq_prefill_attention -- chunked prefill over the compressed cache (turbo-attn,
+ * "How it works": the prefill path dequantises the codec inline in the
+ * attention mainloop, with no decompress buffer): the last q_tokens positions of
+ * every sequence attend causally to its compressed context, their own (already
+ * compressed) keys and values included.
+ *
+ * q: device bf16 [B][q_tokens][Hq][d]; query token i of sequence b sits at
+ *   position seq_lens[b] - q_tokens + i and attends to positions 0 .. that one
+ *   (positions below 0 -- a sequence shorter than q_tokens -- see nothing and
+ *   give zero rows).  Query head qh reads kv head qh / (Hq / Hkv).
+ * block_table, seq_lens, pools, sm_scale, splits, status bits: as in
+ *   tq_decode_attention; splits = 0 picks tq_decode_splits over
+ *   B * ceil(q_tokens / tq_prefill_queries_per_cta(...)) work units.
+ * workspace: ws_bytes >= tq_decode_workspace_bytes(h, B * q_tokens, Hq, splits),
+ *   256-byte aligned; it starts with the fp32 outputs [B][q_tokens][Hq][d].
+ * out: device bf16 [B][q_tokens][Hq][d].
+ * The split-K kernel of the decode gives each CTA tq_prefill_queries_per_cta
+ * consecutive query tokens (their (token, head) pairs are the N columns of its
+ * tensor-core products, so every key and value operand built from the codes
+ * serves all of them), each column with its own causal limit and online
+ * softmax.  Three launches on `stream` (query rotation, split-K, combine).
+ */
+int tq_prefill_queries_per_cta(tq_handle h, int num_q_heads, int num_kv_heads);
+tq_status tq_prefill_attention(tq_handle h, const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                               const int32_t *block_table, const int32_t *seq_lens, int batch, int q_tokens,
+                               int num_q_heads, int num_kv_heads, int page_size, int max_blocks_per_seq,
+                               int64_t num_blocks, float sm_scale, int splits, void *workspace, size_t ws_bytes,
+                               uint16_t *out, void *stream);
+
+/*
  * tq_decode_attention_static -- tq_decode_attention without a workspace, for
  * callers that cannot allocate device memory or own no memory to lend (code
  * inside another runtime's fixed memory budget, plug-ins in a host process that

@@ -310,6 +310,25 @@ class Oracle:
                                             _ptr(out["pg"], ctypes.c_double), _ptr(out["gamma"], ctypes.c_double))
         return out
 
+    def prefill(self, q, k_cache, v_cache, block_table, seq_lens, Hkv: int, page_size: int, sm_scale: float,
+                mode: int = 1, nthreads: int = 0):
+        """Causal attention of the last Tq positions of every sequence ([B, Tq, Hq, d] bf16 bits).
+
+        Query token i of sequence b sits at position p = seq_lens[b] - Tq + i and
+        attends to positions 0..p: by definition that is the one-token attention of
+        that query over the first p + 1 tokens, so each (b, i) is one decode row with
+        sequence length max(p + 1, 0) and sequence b's block table.  Returns
+        [B, Tq, Hq, d] doubles."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        B, Tq, Hq, d = q.shape
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        sl = np.asarray(seq_lens, dtype=np.int64)
+        lens = np.maximum(sl[:, None] - Tq + np.arange(Tq)[None, :] + 1, 0).astype(np.int32).reshape(-1)
+        bt_rows = np.repeat(bt, Tq, axis=0)
+        out = self.decode(q.reshape(B * Tq, Hq, d), k_cache, v_cache, bt_rows, lens, Hkv, page_size, sm_scale,
+                          mode=mode, nthreads=nthreads)
+        return out.reshape(B, Tq, Hq, d)
+
     def dequant_slots(self, k_cache, v_cache, page_size: int, Hkv: int, slots):
         """K~ (original space) and V~ as doubles, [n_slots, Hkv, d]."""
         slots = np.ascontiguousarray(slots, dtype=np.int64)

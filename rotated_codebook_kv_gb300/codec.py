@@ -107,6 +107,27 @@ class Codec:
     def set_wait_limit(self, cycles: int):
         native.tq_set_wait_limit(self.handle, cycles)
 
+    def prefill_attention(self, q, k_cache, v_cache, block_table, seq_lens, num_kv_heads: int, page_size: int,
+                          num_blocks: int, sm_scale: float, splits: int = 0, workspace=None, out=None, stream=None):
+        """Causal attention of the last q.shape[1] positions of every sequence over its compressed cache.
+
+        q: [B, Tq, Hq, d] bf16; returns [B, Tq, Hq, d] bf16."""
+        B, Tq, Hq, d = q.shape
+        assert d == self.head_dim and q.dtype == torch.bfloat16 and q.is_contiguous()
+        maxb = block_table.shape[1]
+        if splits == 0:
+            qpc = native.tq_prefill_queries_per_cta(self.handle, Hq, num_kv_heads)
+            splits = self.decode_splits(B * ((Tq + qpc - 1) // qpc), num_kv_heads, maxb, page_size)
+        if workspace is None:
+            workspace = self.workspace(B * Tq, Hq, splits, device=q.device)
+        if out is None:
+            out = torch.empty_like(q)
+        native.tq_prefill_attention(self.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                    _ptr(seq_lens), B, Tq, Hq, num_kv_heads, page_size, maxb, num_blocks,
+                                    float(sm_scale), splits, _ptr(workspace), workspace.numel(), _ptr(out),
+                                    _stream(stream))
+        return out
+
     def decode_attention_bf16(self, q, k_pool, v_pool, block_table, seq_lens, num_kv_heads: int, page_size: int,
                               num_blocks: int, sm_scale: float, splits: int = 0, workspace=None, out=None,
                               stream=None):

@@ -377,11 +377,75 @@ tq_status tq_decode_attention(tq_handle h, const uint16_t *q, const uint8_t *k_c
     a.sm_scale = sm_scale;
     a.splits = splits;
     a.pages_per_split = (max_blocks_per_seq + splits - 1) / splits;
+    a.Tq = 1;
+    a.qpc = 1;
     a.ws = tq::carve_decode_workspace(workspace, h->codec.d, batch, num_q_heads, splits);
     a.out = out;
     const tq::PageGeom g = tq::page_geom(h->codec, page_size);
     cudaError_t e = tq::launch_decode(h->codec, g, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tq_decode_attention: launch");
+    return TQ_OK;
+}
+
+int tq_prefill_queries_per_cta(tq_handle h, int num_q_heads, int num_kv_heads)
+{
+    if (!h || num_kv_heads < 1 || num_q_heads < num_kv_heads) return 1;
+    const int G = num_q_heads / num_kv_heads;
+    return G >= 8 ? 1 : 8 / G;
+}
+
+tq_status tq_prefill_attention(tq_handle h, const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                               const int32_t *block_table, const int32_t *seq_lens, int batch, int q_tokens,
+                               int num_q_heads, int num_kv_heads, int page_size, int max_blocks_per_seq,
+                               int64_t num_blocks, float sm_scale, int splits, void *workspace, size_t ws_bytes,
+                               uint16_t *out, void *stream)
+{
+    if (!h) return fail(TQ_ERR_INVALID_ARG, "tq_prefill_attention: NULL handle");
+    if (page_size != 16 && page_size != 32)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_prefill_attention: page_size %d not in {16, 32}", page_size);
+    if (batch < 0 || q_tokens < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 ||
+        num_blocks < 1 || splits < 0)
+        return fail(TQ_ERR_INVALID_ARG, "tq_prefill_attention: bad sizes");
+    if (num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > 8)
+        return fail(TQ_ERR_UNSUPPORTED, "tq_prefill_attention: num_q_heads / num_kv_heads must be an integer in 1..8");
+    if (!std::isfinite(sm_scale)) return fail(TQ_ERR_INVALID_ARG, "tq_prefill_attention: sm_scale not finite");
+    if (batch == 0) return TQ_OK;
+    const int qpc = tq_prefill_queries_per_cta(h, num_q_heads, num_kv_heads);
+    const int64_t ctas_z = static_cast<int64_t>(batch) * ((q_tokens + qpc - 1) / qpc);
+    if (ctas_z > 65535 || num_kv_heads > 65535 || static_cast<int64_t>(batch) * q_tokens * num_q_heads >= (1LL << 31))
+        return fail(TQ_ERR_UNSUPPORTED, "tq_prefill_attention: too many sequences x query tokens in one call");
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !workspace || !out)
+        return fail(TQ_ERR_INVALID_ARG, "tq_prefill_attention: NULL pointer");
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4) || !aligned(workspace, 256) || !aligned(out, 16))
+        return fail(TQ_ERR_INVALID_ARG, "tq_prefill_attention: misaligned pointer");
+    if (splits == 0)
+        splits = tq_decode_splits(h, static_cast<int>(ctas_z), num_kv_heads, max_blocks_per_seq, page_size);
+    if (splits > 1024) return fail(TQ_ERR_UNSUPPORTED, "tq_prefill_attention: splits %d above 1024", splits);
+    const size_t need = tq::decode_workspace_bytes(h->codec.d, batch * q_tokens, num_q_heads, splits);
+    if (ws_bytes < need)
+        return fail(TQ_ERR_INVALID_ARG, "tq_prefill_attention: workspace %zu bytes < %zu needed", ws_bytes, need);
+    tq::DecodeArgs a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.B = batch;
+    a.Hq = num_q_heads;
+    a.Hkv = num_kv_heads;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.sm_scale = sm_scale;
+    a.splits = splits;
+    a.pages_per_split = (max_blocks_per_seq + splits - 1) / splits;
+    a.Tq = q_tokens;
+    a.qpc = qpc;
+    a.ws = tq::carve_decode_workspace(workspace, h->codec.d, batch * q_tokens, num_q_heads, splits);
+    a.out = out;
+    const tq::PageGeom g = tq::page_geom(h->codec, page_size);
+    cudaError_t e = tq::launch_decode(h->codec, g, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tq_prefill_attention: launch");
     return TQ_OK;
 }
 

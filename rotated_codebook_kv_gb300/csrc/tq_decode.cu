@@ -195,7 +195,7 @@ cudaError_t launch_dmma(const Codec &c, const PageGeom &pg, const DecodeArgs &a,
     const size_t smem = dmma::DecSmem<D, KB>::bytes(pg);
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(dmma::decode_mma_kernel<D, KB, VB, false>), smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.splits, a.Hkv, a.B);
+    dim3 grid(a.splits, a.Hkv, a.B * ((a.Tq + a.qpc - 1) / a.qpc));
     dmma::decode_mma_kernel<D, KB, VB, false><<<grid, dmma::kThreads, smem, st>>>(c, pg, a);
     return cudaGetLastError();
 }
@@ -213,7 +213,7 @@ cudaError_t launch_dmma_kb(const Codec &c, const PageGeom &pg, const DecodeArgs 
 template <int D>
 cudaError_t launch_decode_d(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st)
 {
-    const int qrows = a.B * a.Hq;
+    const int qrows = a.B * a.Tq * a.Hq;
     qrot_kernel<D><<<(qrows + kQRows - 1) / kQRows, 2 * D, 0, st>>>(c, a.q, a.ws.qrot, a.ws.qs, qrows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -223,7 +223,10 @@ cudaError_t launch_decode_d(const Codec &c, const PageGeom &pg, const DecodeArgs
     default: e = launch_dmma_kb<D, 4>(c, pg, a, st); break;
     }
     if (e != cudaSuccess) return e;
-    return launch_combine(c, a, st, c.vmse != 0);
+    DecodeArgs rows = a;  // the combine merges B * Tq * Hq output rows
+    rows.B = a.B * a.Tq;
+    rows.Tq = 1;
+    return launch_combine(c, rows, st, c.vmse != 0);
 }
 
 }  // namespace

@@ -478,6 +478,8 @@ extern "C" tq_status tq_decode_attention_bf16(tq_handle h, const uint16_t *q, co
     a.sm_scale = sm_scale;
     a.splits = splits;
     a.pages_per_split = (max_blocks_per_seq + splits - 1) / splits;
+    a.Tq = 1;
+    a.qpc = 1;
     a.ws = tq::carve_decode_workspace(workspace, c.d, batch, num_q_heads, splits);
     a.out = out;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -173,7 +173,12 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     const uint32_t zero_off = static_cast<uint32_t>(SM::kLut + SM::kSignLut + SM::kQfrag + SM::kSfrag + 64);
     unsigned char *stages = smem + SM::kHeader;
 
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    // Columns of the score and value MMAs are (query token, head) pairs: decode has
+    // one query token per sequence (columns = the G heads of the kv head); prefill
+    // gives a CTA qpc consecutive query tokens of its sequence (qpc * G <= 8 columns),
+    // each masked causally.
+    const int nqt = (A.Tq + A.qpc - 1) / A.qpc;
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z / nqt, qt = blockIdx.z % nqt;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int quad = lane & 3, row = lane >> 2;
     const int P = PG.P;
@@ -185,19 +190,28 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     int L = A.seq_lens[b];
     if (L < 0) L = 0;
     if (L > A.max_blocks * P) {
-        if (split == 0 && kvh == 0 && tid == 0) atomicOr(C.status, TQ_DEVERR_SEQ_RANGE);
+        if (split == 0 && kvh == 0 && qt == 0 && tid == 0) atomicOr(C.status, TQ_DEVERR_SEQ_RANGE);
         L = A.max_blocks * P;
     }
-    const int npages = (L + P - 1) / P;
+    const int q0 = qt * A.qpc;                  // first query token of this CTA
+    const int ncol = min(A.qpc, A.Tq - q0) * G; // columns: (query q0 + c / G, head c % G)
+    const size_t rows_total = static_cast<size_t>(A.B) * A.Tq * A.Hq;
+    // query row of column c, and its causal limit: query token i of a sequence of L
+    // tokens sits at position L - Tq + i and sees positions below L - Tq + i + 1
+    auto col_row = [&](int c) -> size_t {
+        return (static_cast<size_t>(b) * A.Tq + q0 + c / G) * A.Hq + static_cast<size_t>(kvh) * G + c % G;
+    };
+    auto col_lim = [&](int c) -> int { return max(0, L - A.Tq + q0 + c / G + 1); };
+    const int Lmax = col_lim(ncol - 1);          // the last column sees the most tokens
+    const int npages = (Lmax + P - 1) / P;
     const int pg0 = split * A.pages_per_split;
     const int pg1 = min(npages, pg0 + A.pages_per_split);
-    const size_t head0 = static_cast<size_t>(b) * A.Hq + static_cast<size_t>(kvh) * G;
-    float *ml_out = A.ws.ml + (static_cast<size_t>(split) * A.B * A.Hq + head0) * 2;
-    float *acc_out = A.ws.acc + (static_cast<size_t>(split) * A.B * A.Hq + head0) * D;
+    float *ml_base = A.ws.ml + static_cast<size_t>(split) * rows_total * 2;
+    float *acc_base = A.ws.acc + static_cast<size_t>(split) * rows_total * D;
     if (pg0 >= pg1) {
-        if (tid < G) {
-            ml_out[2 * tid] = -INFINITY;
-            ml_out[2 * tid + 1] = 0.f;
+        if (tid < ncol) {
+            ml_base[2 * col_row(tid)] = -INFINITY;
+            ml_base[2 * col_row(tid) + 1] = 0.f;
         }
         return;
     }
@@ -227,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     // ---- query fragments (B operand of the score MMA, head = lane / 4), permuted
     // coordinates; identical for the four warps, so warp 0 writes them ----
     if (warp == 0) {
-        const bool hv = row < G;
-        const float *qr = A.ws.qrot + (head0 + (hv ? row : 0)) * D;
-        const float *qs = A.ws.qs + (head0 + (hv ? row : 0)) * D;
+        const bool hv = row < ncol;
+        const float *qr = A.ws.qrot + col_row(hv ? row : 0) * D;
+        const float *qs = A.ws.qs + col_row(hv ? row : 0) * D;
 #pragma unroll 4
         for (int s = 0; s < KS; ++s) {
             const int j = 16 * s + 4 * quad;
@@ -249,6 +263,15 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
             qfrag[s * 32 + lane] = f;
             sfrag[s * 32 + lane] = g;
         }
+    }
+
+    // this lane's two columns 2 quad + e: present, and their causal limits
+    bool colv[2];
+    int lim[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        colv[e] = 2 * quad + e < ncol;
+        lim[e] = colv[e] ? col_lim(2 * quad + e) : 0;
     }
 
     // ---- accumulators: O^T rows (coordinates, permuted) x heads 2 quad, 2 quad + 1 ----
@@ -453,14 +476,14 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
                     const int t = o0[j] + row + 8 * hh;
                     const float nrm = bf16_to_float(ldu16(kp[j] + PG.k_norm_off + 2 * t));
                     const float gam = QJL ? bf16_to_float(ldu16(kp[j] + PG.k_gamma_off + 2 * t)) : 0.f;
-                    const bool valid = live[j] && (pos0[j] + row + 8 * hh) < L;
+                    const int pos = pos0[j] + row + 8 * hh;
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int i = 2 * hh + e;
                         const float lo = sa[j][hh][2 + e] + sb[j][hh][e];  // lo.qh + hi.ql
                         float v = nrm * fac_c * fmaf(lo, 1.f / kLoScale, sa[j][hh][e]);
                         if (QJL) v = fmaf(nrm * fac_s * gam, ss[j][i], v);
-                        x[j][hh][e] = (2 * quad + e < G) ? (valid ? v : -INFINITY) : 0.f;
+                        x[j][hh][e] = colv[e] ? ((live[j] && pos < lim[e]) ? v : -INFINITY) : 0.f;
                     }
                 }
             // ---- online softmax (base 2) per head 2 quad + e over the 32 tokens ----
@@ -508,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
                 for (int i = 0; i < 4; ++i) {
                     const int t = o0[j] + tq[i];
                     // metadata of masked tokens (never-written bytes may hold any fp16 pattern) reads zeros
-                    mrow[j][i] = (live[j] && pos0[j] + tq[i] < L) ? vp[j] + PG.v_meta_off + t * C.v_meta_bytes : zero_off;
+                    mrow[j][i] = (live[j] && pos0[j] + tq[i] < Lmax) ? vp[j] + PG.v_meta_off + t * C.v_meta_bytes : zero_off;
                     vrow[j][i] = vp[j] + t * C.v_code_bytes;
                 }
                 if constexpr (!VM) {
@@ -588,9 +611,9 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     }
     __syncthreads();  // every warp is done with the stages before they hold merge data
     if (*cta_abort) {  // a page wait timed out: this split contributes nothing
-        if (tid < G) {
-            ml_out[2 * tid] = -INFINITY;
-            ml_out[2 * tid + 1] = 0.f;
+        if (tid < ncol) {
+            ml_base[2 * col_row(tid)] = -INFINITY;
+            ml_base[2 * col_row(tid) + 1] = 0.f;
         }
         return;
     }
@@ -618,8 +641,8 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     r_z[(warp * 8 + row) * 8 + 2 * quad] = zt[0];
     r_z[(warp * 8 + row) * 8 + 2 * quad + 1] = zt[1];
     __syncthreads();
-    for (int e = tid; e < G * D; e += kThreads) {
-        const int h = e / D, j = e - h * D;
+    for (int e = tid; e < ncol * D; e += kThreads) {
+        const int h = e / D, j = e - h * D;  // column h
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, r_m[w * 8 + h]);
@@ -632,10 +655,11 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
                 l = fmaf(f, r_l[w * 8 + h], l);
             }
         }
-        acc_out[static_cast<size_t>(h) * D + j] = acc;
+        const size_t rr = col_row(h);
+        acc_base[rr * D + j] = acc;
         if (j == 0) {
-            ml_out[2 * h] = M;
-            ml_out[2 * h + 1] = l;
+            ml_base[2 * rr] = M;
+            ml_base[2 * rr + 1] = l;
         }
     }
 }

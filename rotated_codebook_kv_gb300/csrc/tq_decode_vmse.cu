@@ -19,7 +19,7 @@ cudaError_t launch_vm(const Codec &c, const PageGeom &pg, const DecodeArgs &a, c
     const size_t smem = dmma::DecSmem<D, KB, VB, true>::bytes(pg);
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(dmma::decode_mma_kernel<D, KB, VB, true>), smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.splits, a.Hkv, a.B);
+    dim3 grid(a.splits, a.Hkv, a.B * ((a.Tq + a.qpc - 1) / a.qpc));
     dmma::decode_mma_kernel<D, KB, VB, true><<<grid, dmma::kThreads, smem, st>>>(c, pg, a);
     return cudaGetLastError();
 }

@@ -85,6 +85,7 @@ struct DecodeArgs {
     int64_t num_blocks;
     float sm_scale;
     int splits, pages_per_split;
+    int Tq, qpc;  // query tokens per sequence (1 for decode; the last Tq positions, causal) and per CTA
     DecodeWorkspace ws;
     uint16_t *out;
 };

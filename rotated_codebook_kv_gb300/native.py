@@ -32,6 +32,9 @@ SIGNATURES = {
     "tq_decode_workspace_bytes": (_sz, [_vp, _i32, _i32, _i32]),
     "tq_decode_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _f32, _i32,
                                    _vp, _sz, _vp, _vp]),
+    "tq_prefill_queries_per_cta": (_i32, [_vp, _i32, _i32]),
+    "tq_prefill_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
+                                    _i32, _vp, _sz, _vp, _vp]),
     "tq_decode_attention_bf16": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
                                         _i32, _vp, _sz, _vp, _vp]),
     "tq_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
@@ -130,6 +133,18 @@ def tq_decode_attention(h, q, k_cache, v_cache, block_table, seq_lens, batch, nu
                         max_blocks_per_seq, num_blocks, sm_scale, splits, workspace, ws_bytes, out, stream) -> None:
     _check("tq_decode_attention", load().tq_decode_attention(
         h, q, k_cache, v_cache, block_table, seq_lens, batch, num_q_heads, num_kv_heads, page_size,
+        max_blocks_per_seq, num_blocks, sm_scale, splits, workspace, ws_bytes, out, stream))
+
+
+def tq_prefill_queries_per_cta(h, num_q_heads, num_kv_heads) -> int:
+    return load().tq_prefill_queries_per_cta(h, num_q_heads, num_kv_heads)
+
+
+def tq_prefill_attention(h, q, k_cache, v_cache, block_table, seq_lens, batch, q_tokens, num_q_heads, num_kv_heads,
+                         page_size, max_blocks_per_seq, num_blocks, sm_scale, splits, workspace, ws_bytes, out,
+                         stream) -> None:
+    _check("tq_prefill_attention", load().tq_prefill_attention(
+        h, q, k_cache, v_cache, block_table, seq_lens, batch, q_tokens, num_q_heads, num_kv_heads, page_size,
         max_blocks_per_seq, num_blocks, sm_scale, splits, workspace, ws_bytes, out, stream))
 
 

@@ -560,3 +560,43 @@ def test_mse_values_decode_matches_dense_attention():
     for mode in (0, 1):
         out = ora.decode(q, kc, vc, bt, lens, Hkv, P, sm, mode=mode)
         assert np.abs(out - ref).max() < 1e-10 * max(1.0, np.abs(ref).max())
+
+
+# --------------------------------------------------------------------------- #
+# Prefill: causal attention of the last positions of every sequence              #
+# --------------------------------------------------------------------------- #
+
+def test_prefill_is_causal_dense_attention():
+    """Against numpy causal softmax attention over the dequantised K~, V~; the last
+    query token equals the decode of the whole sequence; a query at position 0
+    returns the first value."""
+    ora, c = _tiny_case(lens=(37, 16, 5))
+    d, Hkv, P = c["d"], c["Hkv"], c["P"]
+    B, Tq, Hq = 3, 5, c["q"].shape[1]
+    G = Hq // Hkv
+    rng = np.random.default_rng(77)
+    q = _bf16(rng.standard_normal((B, Tq, Hq, d)))
+    sm = d ** -0.5
+    out = ora.prefill(q, c["kc"], c["vc"], c["bt"], c["lens"], Hkv, P, sm)
+    qd = O.bf16_to_double(q)
+    for b in range(B):
+        L = int(c["lens"][b])
+        pos = np.arange(L)
+        slots = c["bt"][b, pos // P].astype(np.int64) * P + pos % P
+        K, V = ora.dequant_slots(c["kc"], c["vc"], P, Hkv, slots)
+        for i in range(Tq):
+            p_i = L - Tq + i
+            for h in range(Hq):
+                if p_i < 0:
+                    assert not out[b, i, h].any()
+                    continue
+                s = sm * K[: p_i + 1, h // G] @ qd[b, i, h]
+                w = np.exp(s - s.max())
+                want = (w / w.sum()) @ V[: p_i + 1, h // G]
+                assert np.abs(out[b, i, h] - want).max() < 1e-10 * max(1.0, np.abs(want).max())
+    dec = ora.decode(q[:, -1], c["kc"], c["vc"], c["bt"], c["lens"], Hkv, P, sm)
+    assert np.array_equal(out[:, -1], dec)
+    # sequence 2 has 5 tokens and 5 queries: its first query sits at position 0
+    _, V = ora.dequant_slots(c["kc"], c["vc"], P, Hkv, [int(c["bt"][2, 0]) * P])
+    for h in range(Hq):
+        assert np.allclose(out[2, 0, h], V[0, h // G], atol=1e-12)
