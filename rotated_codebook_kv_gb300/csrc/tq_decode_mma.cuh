@@ -154,7 +154,7 @@ __device__ __forceinline__ uint32_t vpair_off(uint32_t x, int sh)
     return ((((x >> sh) & M) | (((x >> (16 + sh)) & M) << VB)) << 5);  // 8 copies x 4 bytes per entry
 }
 
-template <int D, int KB, int VB, bool VM>
+template <int D, int KB, int VB, bool VM, bool PF = false>
 __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(const Codec C, const PageGeom PG, const DecodeArgs A)
 {
     using SM = DecSmem<D, KB, VB, VM>;
@@ -177,8 +177,11 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     // one query token per sequence (columns = the G heads of the kv head); prefill
     // gives a CTA qpc consecutive query tokens of its sequence (qpc * G <= 8 columns),
     // each masked causally.
-    const int nqt = (A.Tq + A.qpc - 1) / A.qpc;
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z / nqt, qt = blockIdx.z % nqt;
+    // (PF: prefill; otherwise Tq = qpc = 1 at compile time)
+    const int Tq = PF ? A.Tq : 1, qpc = PF ? A.qpc : 1;
+    const int nqt = PF ? (Tq + qpc - 1) / qpc : 1;
+    const int split = blockIdx.x, kvh = blockIdx.y, b = PF ? blockIdx.z / nqt : blockIdx.z;
+    const int qt = PF ? blockIdx.z % nqt : 0;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int quad = lane & 3, row = lane >> 2;
     const int P = PG.P;
@@ -193,15 +196,16 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
         if (split == 0 && kvh == 0 && qt == 0 && tid == 0) atomicOr(C.status, TQ_DEVERR_SEQ_RANGE);
         L = A.max_blocks * P;
     }
-    const int q0 = qt * A.qpc;                  // first query token of this CTA
-    const int ncol = min(A.qpc, A.Tq - q0) * G; // columns: (query q0 + c / G, head c % G)
-    const size_t rows_total = static_cast<size_t>(A.B) * A.Tq * A.Hq;
+    const int q0 = qt * qpc;                    // first query token of this CTA
+    const int ncol = min(qpc, Tq - q0) * G;     // columns: (query q0 + c / G, head c % G)
+    const size_t rows_total = static_cast<size_t>(A.B) * Tq * A.Hq;
     // query row of column c, and its causal limit: query token i of a sequence of L
     // tokens sits at position L - Tq + i and sees positions below L - Tq + i + 1
     auto col_row = [&](int c) -> size_t {
-        return (static_cast<size_t>(b) * A.Tq + q0 + c / G) * A.Hq + static_cast<size_t>(kvh) * G + c % G;
+        if (!PF) return static_cast<size_t>(b) * A.Hq + static_cast<size_t>(kvh) * G + c;
+        return (static_cast<size_t>(b) * Tq + q0 + c / G) * A.Hq + static_cast<size_t>(kvh) * G + c % G;
     };
-    auto col_lim = [&](int c) -> int { return max(0, L - A.Tq + q0 + c / G + 1); };
+    auto col_lim = [&](int c) -> int { return PF ? max(0, L - Tq + q0 + c / G + 1) : L; };
     const int Lmax = col_lim(ncol - 1);          // the last column sees the most tokens
     const int npages = (Lmax + P - 1) / P;
     const int pg0 = split * A.pages_per_split;

@@ -66,3 +66,20 @@ def test_prefill_matches_oracle(d, kb, vb, g, P, G, lens, Tq):
 def test_prefill_queries_per_cta():
     codec = Codec(128, 4, 4, 32, 0)
     assert [native.tq_prefill_queries_per_cta(codec.handle, 2 * G, 2) for G in (1, 2, 3, 4, 8)] == [8, 4, 2, 2, 1]
+
+
+def test_prefill_with_mse_values():
+    """Prefill on a handle whose values are coded by the rotation (TQ_VALUES_MSE)."""
+    d, kb, vb, P, G, Hkv = 128, 2, 3, 16, 4, 2
+    w, b, q = _case(d, kb, vb, 32, P, G, [260, 70], 6, Hkv=Hkv, seed=9)
+    codec = Codec(d, kb, vb, 32, w.codec_seed(), values="mse")
+    ora = O.Oracle(d, kb, vb, 32, w.codec_seed(), values="mse")
+    kc, vc = codec.alloc_cache(b.num_blocks, Hkv, P)
+    codec.compress_kv(b.k.to(DEV), b.v.to(DEV), b.slot_mapping.to(DEV), kc, vc, P, b.num_blocks)
+    out = codec.prefill_attention(q.to(DEV), kc, vc, b.block_table.to(DEV), b.seq_lens.to(DEV), Hkv, P,
+                                  b.num_blocks, b.sm_scale)
+    torch.cuda.synchronize()
+    ref = ora.prefill(W.as_u16(q), kc.cpu().numpy(), vc.cpu().numpy(), b.block_table.numpy(), b.seq_lens.numpy(),
+                      Hkv, P, b.sm_scale)
+    check_decode(W.as_u16(out), ref)
+    assert codec.get_status() == 0
