@@ -414,7 +414,7 @@ def run_gpu(args, rank, world, local_rank):
 L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024  # twice the GB300's L2
 
 
-def per_config(dev, peak, reps):
+def per_config(dev, peak, reps, only=None):
     """Compress-only, paged-decode and wide-head workloads at full size, each call
     timed alone with CUDA events on its stream after an L2 flush (a write of twice
     the L2 size outside the timed region), so no call reads its inputs from L2.
@@ -443,6 +443,8 @@ def per_config(dev, peak, reps):
                                ("wide_head_decode", W.wide_head_decode(), 0, "group"),
                                ("wide_head_decode_hadamard", W.wide_head_decode(), 1, "group"),
                                ("paged_decode_mse_values", W.paged_decode(), 0, "mse")):
+        if only is not None and name != only:
+            continue
         b = W.generate(w, device=dev)
         codec = Codec(w.head_dim, w.k_bits, w.v_bits, w.group, w.codec_seed(), rotation=rot, values=vals)
         kc, vc = codec.alloc_cache(b.num_blocks, w.num_kv_heads, w.page_size, device=dev)
@@ -476,6 +478,8 @@ def per_config(dev, peak, reps):
     # the bandwidth control of the compressed decode
     for name, w in (("bypass_bf16_long_context", W.long_context_mixed().for_layer(0)),
                     ("bypass_bf16_paged_decode", W.paged_decode())):
+        if only is not None and name != only:
+            continue
         b = W.generate(w, device=dev)
         codec = Codec(w.head_dim, 4, 4, 32, 0)
         P, H, d = w.page_size, w.num_kv_heads, w.head_dim
@@ -506,6 +510,8 @@ def per_config(dev, peak, reps):
         torch.cuda.empty_cache()
     # chunked prefill over the compressed cache: the last 64 positions of every sequence of
     # the paged workload attend causally to their compressed context
+    if only is not None and only != "prefill_paged_decode_chunk64":
+        return out
     w = W.paged_decode()
     b = W.generate(w, device=dev)
     codec = Codec(w.head_dim, w.k_bits, w.v_bits, w.group, w.codec_seed())
@@ -531,8 +537,10 @@ def per_config(dev, peak, reps):
     del q, o, kc, vc, b, codec
     torch.cuda.empty_cache()
     out["timing"] = f"median of {reps} calls after 2 warm-up calls; L2 flushed before each call"
-    out["wide_head_decode_hadamard"]["rotation"] = "randomized Hadamard (tq_init_ex)"
-    out["paged_decode_mse_values"]["values"] = "rotation + Lloyd-Max codebook (tq_init_ex, TQ_VALUES_MSE)"
+    if "wide_head_decode_hadamard" in out:
+        out["wide_head_decode_hadamard"]["rotation"] = "randomized Hadamard (tq_init_ex)"
+    if "paged_decode_mse_values" in out:
+        out["paged_decode_mse_values"]["values"] = "rotation + Lloyd-Max codebook (tq_init_ex, TQ_VALUES_MSE)"
     return out
 
 
@@ -685,6 +693,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-per-config", action="store_true", help="skip the other full-size workloads")
     ap.add_argument("--config-reps", type=int, default=10)
+    ap.add_argument("--only", default=None,
+                    help="profiling only: run just this entry of the other full-size workloads (one timed call)")
     ap.add_argument("--layers", type=int, default=None, help="profiling only: first N layers")
     ap.add_argument("--batch", type=int, default=None, help="profiling only: fewer sequences")
     args = ap.parse_args()
@@ -703,6 +713,11 @@ def main():
         import torch.distributed as dist
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.only:  # profiling: one workload's calls (two warm-up calls and one timed), no benchmark line
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        print(json.dumps(per_config(dev, measured_peak()[0], 1, only=args.only)))
+        return 0
     line = run_gpu(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line))
