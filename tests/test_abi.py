@@ -51,6 +51,9 @@ def test_invalid_arguments_rejected_without_gpu(lib):
     with pytest.raises(native.TQError) as e:
         native.tq_compress_kv(None, 0, 0, 1, 1, 128, 128, 0, 0, 0, 16, 1, None)
     assert e.value.status == native.TQ_ERR_INVALID_ARG
+    with pytest.raises(native.TQError) as e:  # an option flag the library does not know
+        native.tq_init_ex(128, 3, 4, 32, 0, 0x10)
+    assert e.value.status == native.TQ_ERR_UNSUPPORTED and "flags" in native.tq_last_error()
     assert native.tq_decode_workspace_bytes(None, 1, 1, 1) == 0
 
 
@@ -63,6 +66,11 @@ def test_every_entry_point_rejects_a_null_handle(lib):
                                                                   0, None),
         "tq_decode_attention_static": lambda: native.tq_decode_attention_static(None, 0, 0, 0, 0, 0, 1, 1, 1, 16, 1,
                                                                                 1, 1.0, 1, 0, None),
+        "tq_prefill_attention": lambda: native.tq_prefill_attention(None, 0, 0, 0, 0, 0, 1, 1, 1, 1, 16, 1, 1, 1.0,
+                                                                    1, 0, 0, 0, None),
+        "tq_decode_attention_bf16": lambda: native.tq_decode_attention_bf16(None, 0, 0, 0, 0, 0, 1, 1, 1, 16, 1, 1,
+                                                                            1.0, 1, 0, 0, 0, None),
+        "tq_set_wait_limit": lambda: native.tq_set_wait_limit(None, 5),
         "tq_get_status": lambda: native.tq_get_status(None, None),
         "tq_export_params": lambda: native.tq_export_params(None, None, None, None, None),
     }

@@ -492,3 +492,51 @@ def test_hadamard_streaming_kernel_special_rows(vb, g):
     ovc = np.full(b.num_blocks * Hkv * geo["v_page"], 0xA5, np.uint8)
     ora.compress_kv(W.as_u16(b.k), W.as_u16(b.v), b.slot_mapping.cpu().numpy(), P, b.num_blocks, okc, ovc)
     assert np.array_equal(vc.cpu().numpy(), ovc)
+
+
+# --------------------------------------------------------------------------- #
+# Sizes at the edges of what the calls accept                                   #
+# --------------------------------------------------------------------------- #
+
+def test_size_edges():
+    """Empty calls launch nothing and touch nothing; the largest accepted split count
+    (1024, far more splits than pages) decodes correctly; 65535 sequences (the
+    largest batch) of length 0 and 1 decode to zeros and to their single value;
+    one past the largest batch and split count is refused on the host."""
+    from rotated_codebook_kv_gb300 import native
+    w = W.scaled(SMALL["paged_decode_small"], batch=3, seq_len_range=(50, 120))
+    b = W.generate(w, device=DEV)
+    codec, ora = _codec_pair(w)
+    kc, vc = _compress(codec, w, b, fill=0x3C)
+    before = (kc.clone(), vc.clone())
+    codec.compress_kv(b.k[:0], b.v[:0], b.slot_mapping[:0], kc, vc, w.page_size, b.num_blocks)  # T = 0
+    torch.cuda.synchronize()
+    assert torch.equal(kc, before[0]) and torch.equal(vc, before[1])
+    ref = _decode_oracle(ora, w, b, kc.cpu().numpy(), vc.cpu().numpy())
+    check_decode(_decode_gpu(codec, w, b, kc, vc, splits=1024), ref)
+    assert codec.get_status() == 0
+    # the largest batch: 65535 sequences, alternately empty and of one token (the first slot of a page)
+    Bmax = 65535
+    q = torch.randn(Bmax, w.num_q_heads, w.head_dim, device=DEV).to(torch.bfloat16)
+    bt = torch.zeros(Bmax, 1, dtype=torch.int32, device=DEV)
+    bt[:, 0] = b.block_table[0, 0]
+    sl = (torch.arange(Bmax, device=DEV, dtype=torch.int32) % 2)
+    out = codec.decode_attention(q, kc, vc, bt, sl, w.num_kv_heads, w.page_size, b.num_blocks, b.sm_scale)
+    torch.cuda.synchronize()
+    assert codec.get_status() == 0
+    o = O.bf16_to_double(W.as_u16(out))
+    assert not o[0::2].any()
+    _, V = ora.dequant_slots(kc.cpu().numpy(), vc.cpu().numpy(), w.page_size, w.num_kv_heads,
+                             [int(b.block_table[0, 0]) * w.page_size])
+    G = w.num_q_heads // w.num_kv_heads
+    want = O.bf16_to_double(O.bf16_from_double(np.stack([V[0, h // G] for h in range(w.num_q_heads)])))
+    assert np.array_equal(o[1], want) and np.array_equal(o[-2], want)
+    ws = codec.workspace(1, w.num_q_heads, 1)
+    with pytest.raises(native.TQError):  # one sequence too many
+        native.tq_decode_attention(codec.handle, q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(),
+                                   sl.data_ptr(), Bmax + 1, w.num_q_heads, w.num_kv_heads, w.page_size, 1,
+                                   b.num_blocks, b.sm_scale, 1, ws.data_ptr(), ws.numel(), out.data_ptr(), 0)
+    with pytest.raises(native.TQError):  # one split too many
+        native.tq_decode_attention(codec.handle, q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(),
+                                   sl.data_ptr(), 1, w.num_q_heads, w.num_kv_heads, w.page_size, 1,
+                                   b.num_blocks, b.sm_scale, 1025, ws.data_ptr(), ws.numel(), out.data_ptr(), 0)
