@@ -175,6 +175,34 @@ tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t s
                 put(1, i, j, ht.S[static_cast<size_t>(i) * d + j] * 4096.0);
             }
     }
+    // Pi 2^10 as fp16 high / low parts in the fragment order of mma.sync m16n8k16's B
+    // operand (B[k][n] = Pi[n][k]): for n-tile nt, k-step ks and lane (r, q) the
+    // pairs (k0, k0 + 1) and (k0 + 8, k0 + 9) of row n = 8 nt + r, k0 = 16 ks + 2 q
+    const size_t frag_words = static_cast<size_t>(d / 8) * (d / 16) * 32 * 4;
+    std::vector<uint32_t> frag(frag_words);
+    {
+        auto hl = [&](int n, int kk, uint16_t *hi, uint16_t *lo) {
+            const double x = ht.Pi[static_cast<size_t>(n) * d + kk] * 1024.0;
+            const __half h = __float2half_rn(static_cast<float>(x));
+            *hi = __half_as_ushort(h);
+            *lo = __half_as_ushort(__float2half_rn(static_cast<float>(x - static_cast<double>(__half2float(h)))));
+        };
+        size_t w = 0;
+        for (int nt = 0; nt < d / 8; ++nt)
+            for (int ks = 0; ks < d / 16; ++ks)
+                for (int lane = 0; lane < 32; ++lane) {
+                    const int n = 8 * nt + lane / 4, k0 = 16 * ks + 2 * (lane % 4);
+                    uint16_t h[4], l[4];
+                    hl(n, k0, &h[0], &l[0]);
+                    hl(n, k0 + 1, &h[1], &l[1]);
+                    hl(n, k0 + 8, &h[2], &l[2]);
+                    hl(n, k0 + 9, &h[3], &l[3]);
+                    frag[w++] = h[0] | (static_cast<uint32_t>(h[1]) << 16);
+                    frag[w++] = h[2] | (static_cast<uint32_t>(h[3]) << 16);
+                    frag[w++] = l[0] | (static_cast<uint32_t>(l[1]) << 16);
+                    frag[w++] = l[2] | (static_cast<uint32_t>(l[3]) << 16);
+                }
+    }
     tq_ctx *c = new tq_ctx();
     cudaError_t e = cudaGetDevice(&c->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
@@ -188,7 +216,7 @@ tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t s
         delete c;
         return cuda_fail(e, "tq_init: cudaGetSymbolAddress of the static decode scratch");
     }
-    e = cudaMalloc(&c->dev_tables, nf * sizeof(float) + img_bytes + 256);
+    e = cudaMalloc(&c->dev_tables, nf * sizeof(float) + img_bytes + frag_words * 4 + 256);
     if (e != cudaSuccess) {
         delete c;
         return fail(TQ_ERR_OOM, "tq_init: cudaMalloc: %s", cudaGetErrorString(e));
@@ -197,7 +225,9 @@ tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t s
     e = cudaMemcpy(base, host.data(), nf * sizeof(float), cudaMemcpyHostToDevice);
     char *img_dev = reinterpret_cast<char *>(base + nf);
     if (e == cudaSuccess && img_bytes) e = cudaMemcpy(img_dev, img.data(), img_bytes, cudaMemcpyHostToDevice);
-    unsigned *status = reinterpret_cast<unsigned *>(img_dev + img_bytes);
+    char *frag_dev = img_dev + img_bytes;
+    if (e == cudaSuccess) e = cudaMemcpy(frag_dev, frag.data(), frag_words * 4, cudaMemcpyHostToDevice);
+    unsigned *status = reinterpret_cast<unsigned *>(frag_dev + frag_words * 4);
     if (e == cudaSuccess) e = cudaMemset(status, 0, 256);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -230,6 +260,7 @@ tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t s
     k.M_lo = base + 5 * dd;
     k.tc_image = img_bytes ? img_dev : nullptr;
     k.hsign = base + 6 * dd;
+    k.pi_frag = reinterpret_cast<const uint4 *>(frag_dev);
     k.rotation = rotation;
     k.status = status;
     k.wait_limit = tq::kDefaultWaitLimit;

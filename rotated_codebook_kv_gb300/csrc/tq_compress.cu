@@ -40,7 +40,8 @@ struct CompressSmem {
     static constexpr size_t kYb = sizeof(float) * TM * D;      // Pi k, later r
     static constexpr size_t kCodes = ((TM * kCodeStride + 15) / 16) * 16;
     static constexpr size_t kScratch = sizeof(double) * kWarps * D;
-    static constexpr size_t kBytes = kKf + kYb + kCodes + kScratch;
+    static constexpr size_t kKa = sizeof(__half) * TM * (D + 8);  // fp16 keys for the tensor-core rotation
+    static constexpr size_t kBytes = kKf + kYb + kCodes + kScratch + kKa;
 };
 
 // acc[rr] += sum_j W[j][i] * X[row(rr)][j] for i = tid % D, rows interleaved by
@@ -75,6 +76,183 @@ __device__ __forceinline__ void matvec_rows(const float *__restrict__ W, const f
     }
 #pragma unroll
     for (int rr = 0; rr < RPT; ++rr) Y[(rg + rr * CG) * D + i] = acc[rr];
+}
+
+constexpr int kStreamWarps = 8;
+constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23: adding it rounds to an integer
+constexpr uint32_t kRoundBits = 0x4B400000u;
+
+template <int E>
+__device__ __forceinline__ void unpack_bf16(const uint32_t (&w)[E / 2], float (&x)[E])
+{
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// Codes of the lane's E values of one group shared by lpg lanes:
+// code = clamp(floor((x - zero) / scale + 1/2), 0, 2^VB - 1) with the group's fp16
+// scale = (max - min) / (2^VB - 1) and zero = min.  The rounding is one fused
+// multiply-add; a quotient within 4 ulps (2^-14) of a boundary n - 1/2 is
+// re-decided exactly (x - zero as an exact float pair against (n - 1/2) scale,
+// which is exact in fp32).  Groups whose zero is not their minimum exactly
+// (outside the fp16 normal range) or whose scale is subnormal decide every
+// element that way, with clamping.  Returns (scale | zero << 16) as fp16 bits.
+template <int E, int VB>
+__device__ __forceinline__ uint32_t quantize_values_lane(const float (&x)[E], int lpg, uint32_t &codes)
+{
+    constexpr int L = (1 << VB) - 1;
+    float mn = x[0], mx = x[0];
+#pragma unroll
+    for (int m = 1; m < E; ++m) {
+        mn = fminf(mn, x[m]);
+        mx = fmaxf(mx, x[m]);
+    }
+    for (int o = lpg >> 1; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    float dh, de;
+    two_sum(mx, -mn, dh, de);
+    // (max - min) / L with L in {3, 7, 15}: exact in fp32 or a non-terminating binary
+    // fraction, so rounding to fp32 first never lands on an fp16 midpoint; dh * (1/L)
+    // is within 2 ulps of dh / L, safe unless near a midpoint or below fp16 normals
+    const float qm = dh * (1.f / static_cast<float>(L));
+    const uint32_t qlow = __float_as_uint(qm) & 0x1FFFu;
+    const bool qsafe = de == 0.f && qm >= 6.103515625e-05f && (qlow + 4u - 0x1000u) > 8u;
+    __half s16;
+    if (qsafe) s16 = __float2half_rn(qm);
+    else if (de == 0.f) s16 = __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)));
+    else s16 = __double2half((static_cast<double>(mx) - static_cast<double>(mn)) / L);
+    const __half z16 = __float2half_rn(mn);
+    const float sv = __half2float(s16), zv = __half2float(z16);
+    float inv = 0.f;
+    if (sv != 0.f) asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sv));
+    const bool exact_all = zv != mn || (sv != 0.f && sv < 6.103515625e-05f);
+    codes = 0u;
+#pragma unroll
+    for (int m = 0; m < E; ++m) {
+        uint32_t q;
+        if (!exact_all) {
+            const float dx = x[m] - zv;
+            q = __float_as_uint(fmaf(dx, inv, kRoundMagic)) - kRoundBits;
+            const uint32_t tb = __float_as_uint(fmaf(dx, inv, 192.5f + 4.f / 65536.f));
+            if ((tb & 0xFFF8u) == 0u) {
+                const uint32_t n = (tb >> 16) & 0x1Fu;
+                const float b = fmaf(static_cast<float>(n), sv, -0.5f * sv);
+                float a, ea;
+                two_sum(x[m], -zv, a, ea);
+                q = (__fadd_rn(__fsub_rn(a, b), ea) >= 0.f) ? n : n - 1u;
+            }
+        } else {
+            int qi = 0;
+            if (sv != 0.f) {
+                float a, ea;
+                two_sum(x[m], -zv, a, ea);
+                qi = static_cast<int>(fminf(fmaxf(floorf(fmaf(x[m] - zv, inv, 0.5f)), 0.f), static_cast<float>(L)));
+                while (qi < L && __fadd_rn(__fsub_rn(a, (qi + 0.5f) * sv), ea) >= 0.f) ++qi;
+                while (qi > 0 && !(__fadd_rn(__fsub_rn(a, (qi - 0.5f) * sv), ea) >= 0.f)) --qi;
+            }
+            q = static_cast<uint32_t>(qi);
+        }
+        codes |= q << (VB * m);
+    }
+    return static_cast<uint32_t>(__half_as_ushort(s16)) | (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
+}
+
+// Stores the lane's nbytes (2, 3 or 4) code bytes at p (aligned to nbytes when 2 or 4).
+__device__ __forceinline__ void store_code_bytes(uint8_t *p, uint32_t w, int nbytes)
+{
+    if (nbytes == 4) *reinterpret_cast<uint32_t *>(p) = w;
+    else if (nbytes == 2) *reinterpret_cast<uint16_t *>(p) = static_cast<uint16_t>(w);
+    else {
+        p[0] = static_cast<uint8_t>(w);
+        p[1] = static_cast<uint8_t>(w >> 8);
+        p[2] = static_cast<uint8_t>(w >> 16);
+    }
+}
+
+// One row of fp32 keys (exact bf16 values) staged as fp16 after the power-of-two
+// scale 2^(15 - e), max |k| in [2^(e-1), 2^e): every bf16 value within 2^29 of the
+// row's maximum is exact in fp16 and smaller ones change Pi k by less than 2^-29 of
+// it.  ysc[row] = 2^(e - 25) undoes the scale and Pi's 2^10.  By one warp; rows
+// without a finite scale (zero or extreme, taken exactly) stage zeros.
+template <int D>
+__device__ __forceinline__ void stage_fp16_row(const float *kf, __half *ka, int row, float mx, float *ysc)
+{
+    const int lane = threadIdx.x & 31;
+    int ex = 0;
+    const bool ok = mx >= 0x1p-30f && mx <= 0x1p30f;
+    if (ok) frexpf(mx, &ex);
+    const float sc = ok ? ldexpf(1.f, 15 - ex) : 0.f;
+    for (int j = 2 * lane; j < D; j += 64) {
+        const float2 x = *reinterpret_cast<const float2 *>(kf + row * D + j);
+        *reinterpret_cast<__half2 *>(ka + row * (D + 8) + j) = __floats2half2_rn(x.x * sc, x.y * sc);
+    }
+    if (lane == 0) ysc[row] = ok ? ldexpf(1.f, ex - 25) : 0.f;
+}
+
+// Dense rotation of TM rows on the tensor cores (mma.sync m16n8k16, fp16 in,
+// fp32 accumulate): Y = K' (Pi 2^10)^T with K' the keys scaled by a power of two
+// per row so that they are exact in fp16 (staged in ka, row stride D + 8 halves so
+// that ldmatrix rows fall in different banks), and Pi 2^10 as fp16 high and low
+// parts (~22 significant bits) in a fragment-ordered image read from L2:
+// [n-tile][k-step][lane] = (high b0, high b1, low b0, low b1).  Warp w computes the
+// output columns [D/8 w, D/8 (w + 1)) of both 16-row m-tiles; Y[row] is written to
+// Yo scaled back by ysc[row].
+__device__ __forceinline__ void mma16816_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int D, int TM>
+__device__ __forceinline__ void mma_rows(const uint4 *__restrict__ pi_frag, const __half *ka, const float *ysc,
+                                         float *Yo)
+{
+    constexpr int KS = D / 16, NPW = D / 64, MTS = TM / 16, KA = D + 8;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = lane >> 2, q = lane & 3;
+    float acc[MTS][NPW][4];
+#pragma unroll
+    for (int m = 0; m < MTS; ++m)
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) acc[m][n][0] = acc[m][n][1] = acc[m][n][2] = acc[m][n][3] = 0.f;
+    const uint32_t kab = static_cast<uint32_t>(__cvta_generic_to_shared(ka));
+#pragma unroll 2
+    for (int s = 0; s < KS; ++s) {
+        uint4 bf[NPW];
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) bf[n] = __ldg(pi_frag + ((warp * NPW + n) * KS + s) * 32 + lane);
+#pragma unroll
+        for (int m = 0; m < MTS; ++m) {
+            uint32_t a0, a1, a2, a3;
+            const uint32_t addr = kab + 2u * ((16 * m + (lane & 15)) * KA + 16 * s + 8 * (lane >> 4));
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(addr));
+#pragma unroll
+            for (int n = 0; n < NPW; ++n) {
+                mma16816_f16(acc[m][n], a0, a1, a2, a3, bf[n].z, bf[n].w);  // low parts first
+                mma16816_f16(acc[m][n], a0, a1, a2, a3, bf[n].x, bf[n].y);
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MTS; ++m) {
+        const int row = 16 * m + r;
+        const float s0 = ysc[row], s1 = ysc[row + 8];
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) {
+            const int col = 8 * (warp * NPW + n) + 2 * q;
+            *reinterpret_cast<float2 *>(Yo + row * D + col) = make_float2(acc[m][n][0] * s0, acc[m][n][1] * s0);
+            *reinterpret_cast<float2 *>(Yo + (row + 8) * D + col) = make_float2(acc[m][n][2] * s1, acc[m][n][3] * s1);
+        }
+    }
 }
 
 // Hadamard rotation of TM rows (turbo-attn, "How it works", step 1):
@@ -239,6 +417,8 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     float *yb = reinterpret_cast<float *>(smem_raw + SM::kKf);
     uint8_t *codes = smem_raw + SM::kKf + SM::kYb;
     double *scratch = reinterpret_cast<double *>(smem_raw + SM::kKf + SM::kYb + SM::kCodes);
+    __half *ka = reinterpret_cast<__half *>(smem_raw + SM::kKf + SM::kYb + SM::kCodes + SM::kScratch);
+    __shared__ float s_ysc[TM];  // 2^-(10 + row scale): the tensor-core rotation's output back to Pi k
     __shared__ float s_scale[TM];
     __shared__ float s_rn[TM];
     __shared__ int64_t s_dst[TM];
@@ -314,10 +494,15 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             s_n16[row] = float_to_bf16_bits(n);
             s_g16[row] = 0;
         }
+        if constexpr (!HAD) stage_fp16_row<D>(kf, ka, row, mx, s_ysc);
     }
     // ---- rotation: yb = Pi k (unnormalised) -----------------------------------
-    if constexpr (HAD) fwht_rows<D, TM>(C.hsign, kf, yb);
-    else matvec_rows<D, TM>(C.PiT, kf, yb);
+    if constexpr (HAD) {
+        fwht_rows<D, TM>(C.hsign, kf, yb);
+    } else {
+        __syncthreads();  // ka and s_ysc of every row are staged
+        mma_rows<D, TM>(C.pi_frag, ka, s_ysc, yb);
+    }
     __syncthreads();
     // ---- codes, guard band, residual -----------------------------------------
     // code = #{t : threshold_t <= z} by a binary search over the sorted thresholds
@@ -414,6 +599,21 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             x[6] = bf16_to_float(u.w & 0xffffu); x[7] = bf16_to_float(u.w >> 16);
         }
         const int lpg = C.group / E;  // lanes per group
+        if constexpr (E == 8) {
+            // the lane's 8 codes are VB whole bytes: one fused multiply-add per element with
+            // an exact decision near ties (as in the streaming kernel)
+            uint32_t vw = 0u, meta = 0u;
+            const int vb = C.v_bits;
+            if (vb == 2) meta = quantize_values_lane<8, 2>(x, lpg, vw);
+            else if (vb == 3) meta = quantize_values_lane<8, 3>(x, lpg, vw);
+            else meta = quantize_values_lane<8, 4>(x, lpg, vw);
+            uint8_t *vrec = vc + dst * G.v_page;
+            store_code_bytes(vrec + static_cast<int64_t>(off) * C.v_code_bytes + vb * lane, vw, vb);
+            if ((lane & (lpg - 1)) == 0)
+                *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + static_cast<int64_t>(off) * C.v_meta_bytes +
+                                              4 * (lane / lpg)) = meta;
+            continue;
+        }
         float mn = x[0], mxv = x[0];
 #pragma unroll
         for (int m = 1; m < E; ++m) { mn = fminf(mn, x[m]); mxv = fmaxf(mxv, x[m]); }
@@ -504,9 +704,14 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
                 s_flag[row] = flag;
                 s_n16[row] = flag == 2 ? 0 : float_to_bf16_bits(n);
             }
+            if constexpr (!HAD) stage_fp16_row<D>(kf, ka, row, mx, s_ysc);
         }
-        if constexpr (HAD) fwht_rows<D, TM>(C.hsign, kf, yb);
-        else matvec_rows<D, TM>(C.PiT, kf, yb);
+        if constexpr (HAD) {
+            fwht_rows<D, TM>(C.hsign, kf, yb);
+        } else {
+            __syncthreads();
+            mma_rows<D, TM>(C.pi_frag, ka, s_ysc, yb);
+        }
         __syncthreads();
         const int vb = C.v_bits;
         for (int e = tid; e < TM * D; e += kThreads) {
@@ -556,102 +761,6 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
 // bits of the record (b bytes at byte offset b l).  No shared-memory staging and
 // no block barrier: the kernel is a row pipeline bounded by HBM.
 // ---------------------------------------------------------------------------
-constexpr int kStreamWarps = 8;
-constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23: adding it rounds to an integer
-constexpr uint32_t kRoundBits = 0x4B400000u;
-
-template <int E>
-__device__ __forceinline__ void unpack_bf16(const uint32_t (&w)[E / 2], float (&x)[E])
-{
-#pragma unroll
-    for (int i = 0; i < E / 2; ++i) {
-        x[2 * i] = __uint_as_float(w[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-}
-
-// Codes of the lane's E values of one group shared by lpg lanes:
-// code = clamp(floor((x - zero) / scale + 1/2), 0, 2^VB - 1) with the group's fp16
-// scale = (max - min) / (2^VB - 1) and zero = min.  The rounding is one fused
-// multiply-add; a quotient within 4 ulps (2^-14) of a boundary n - 1/2 is
-// re-decided exactly (x - zero as an exact float pair against (n - 1/2) scale,
-// which is exact in fp32).  Groups whose zero is not their minimum exactly
-// (outside the fp16 normal range) or whose scale is subnormal decide every
-// element that way, with clamping.  Returns (scale | zero << 16) as fp16 bits.
-template <int E, int VB>
-__device__ __forceinline__ uint32_t quantize_values_lane(const float (&x)[E], int lpg, uint32_t &codes)
-{
-    constexpr int L = (1 << VB) - 1;
-    float mn = x[0], mx = x[0];
-#pragma unroll
-    for (int m = 1; m < E; ++m) {
-        mn = fminf(mn, x[m]);
-        mx = fmaxf(mx, x[m]);
-    }
-    for (int o = lpg >> 1; o > 0; o >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    float dh, de;
-    two_sum(mx, -mn, dh, de);
-    // (max - min) / L with L in {3, 7, 15}: exact in fp32 or a non-terminating binary
-    // fraction, so rounding to fp32 first never lands on an fp16 midpoint; dh * (1/L)
-    // is within 2 ulps of dh / L, safe unless near a midpoint or below fp16 normals
-    const float qm = dh * (1.f / static_cast<float>(L));
-    const uint32_t qlow = __float_as_uint(qm) & 0x1FFFu;
-    const bool qsafe = de == 0.f && qm >= 6.103515625e-05f && (qlow + 4u - 0x1000u) > 8u;
-    __half s16;
-    if (qsafe) s16 = __float2half_rn(qm);
-    else if (de == 0.f) s16 = __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)));
-    else s16 = __double2half((static_cast<double>(mx) - static_cast<double>(mn)) / L);
-    const __half z16 = __float2half_rn(mn);
-    const float sv = __half2float(s16), zv = __half2float(z16);
-    float inv = 0.f;
-    if (sv != 0.f) asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sv));
-    const bool exact_all = zv != mn || (sv != 0.f && sv < 6.103515625e-05f);
-    codes = 0u;
-#pragma unroll
-    for (int m = 0; m < E; ++m) {
-        uint32_t q;
-        if (!exact_all) {
-            const float dx = x[m] - zv;
-            q = __float_as_uint(fmaf(dx, inv, kRoundMagic)) - kRoundBits;
-            const uint32_t tb = __float_as_uint(fmaf(dx, inv, 192.5f + 4.f / 65536.f));
-            if ((tb & 0xFFF8u) == 0u) {
-                const uint32_t n = (tb >> 16) & 0x1Fu;
-                const float b = fmaf(static_cast<float>(n), sv, -0.5f * sv);
-                float a, ea;
-                two_sum(x[m], -zv, a, ea);
-                q = (__fadd_rn(__fsub_rn(a, b), ea) >= 0.f) ? n : n - 1u;
-            }
-        } else {
-            int qi = 0;
-            if (sv != 0.f) {
-                float a, ea;
-                two_sum(x[m], -zv, a, ea);
-                qi = static_cast<int>(fminf(fmaxf(floorf(fmaf(x[m] - zv, inv, 0.5f)), 0.f), static_cast<float>(L)));
-                while (qi < L && __fadd_rn(__fsub_rn(a, (qi + 0.5f) * sv), ea) >= 0.f) ++qi;
-                while (qi > 0 && !(__fadd_rn(__fsub_rn(a, (qi - 0.5f) * sv), ea) >= 0.f)) --qi;
-            }
-            q = static_cast<uint32_t>(qi);
-        }
-        codes |= q << (VB * m);
-    }
-    return static_cast<uint32_t>(__half_as_ushort(s16)) | (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
-}
-
-// Stores the lane's nbytes (2, 3 or 4) code bytes at p (aligned to nbytes when 2 or 4).
-__device__ __forceinline__ void store_code_bytes(uint8_t *p, uint32_t w, int nbytes)
-{
-    if (nbytes == 4) *reinterpret_cast<uint32_t *>(p) = w;
-    else if (nbytes == 2) *reinterpret_cast<uint16_t *>(p) = static_cast<uint16_t>(w);
-    else {
-        p[0] = static_cast<uint8_t>(w);
-        p[1] = static_cast<uint8_t>(w >> 8);
-        p[2] = static_cast<uint8_t>(w >> 16);
-    }
-}
-
 // The lane's 4-bit codes of one row taken again in double (rows with a code near a
 // threshold or an extreme range).  Every bf16 square and every butterfly sum of
 // bf16 keys is exact in double up to 2^-53 of the row's largest term, so the
