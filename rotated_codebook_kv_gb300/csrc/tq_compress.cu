@@ -403,6 +403,62 @@ __device__ void precise_key_row(const Codec &C, const uint16_t *__restrict__ src
     __syncwarp();
 }
 
+// Re-decides the marked codes of one row exactly, by one warp: the row's codes in
+// `codes` carry 0x80 where the fast z fell inside the guard band of a threshold;
+// for each such coordinate z_j = sqrt(d) (Pi_j . k) / ||k|| is recomputed with
+// compensated (double-fp32) sums of exact products and the code re-taken against
+// the thresholds (thr, nthr).  The row must have a normal range (no power-of-two
+// scaling is needed for its squares).  Returns whether any code changed (the same
+// in every lane).  O(d) per marked coordinate, instead of the O(d^2) of a whole row.
+template <int D>
+__device__ __noinline__ bool refine_marked_codes(const float *__restrict__ Pi, const uint16_t *__restrict__ src,
+                                                 uint8_t *codes, const float *thr, int nthr)
+{
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    float kx[E];
+#pragma unroll
+    for (int m = 0; m < E; ++m) kx[m] = bf16_to_float(src[lane + 32 * m]);
+    auto warp_dd = [&](float s, float c) -> double {  // compensated warp sum, lane 0's value to all
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, o), c2 = __shfl_xor_sync(0xffffffffu, c, o);
+            float t, e;
+            two_sum(s, s2, t, e);
+            s = t;
+            c = __fadd_rn(c, __fadd_rn(c2, e));
+        }
+        s = __shfl_sync(0xffffffffu, s, 0);
+        c = __shfl_sync(0xffffffffu, c, 0);
+        return static_cast<double>(s) + static_cast<double>(c);
+    };
+    float ns = 0.f, nc = 0.f;
+#pragma unroll
+    for (int m = 0; m < E; ++m) dot2_step(ns, nc, kx[m], kx[m]);
+    const double zscale = sqrt(static_cast<double>(D)) / sqrt(warp_dd(ns, nc));
+    bool changed = false;
+#pragma unroll 1
+    for (int m = 0; m < E; ++m) {
+        uint32_t mask = __ballot_sync(0xffffffffu, (codes[lane + 32 * m] & 0x80u) != 0);
+        while (mask) {
+            const int j = __ffs(mask) - 1 + 32 * m;
+            mask &= mask - 1;
+            float ds = 0.f, dc = 0.f;
+#pragma unroll
+            for (int mm = 0; mm < E; ++mm) dot2_step(ds, dc, __ldg(Pi + j * D + lane + 32 * mm), kx[mm]);
+            const double z = warp_dd(ds, dc) * zscale;
+            int code = 0;
+            for (int t = 0; t < nthr; ++t) code += (static_cast<double>(thr[t]) <= z);
+            const int old = codes[j] & 0x7F;
+            changed |= code != old;
+            __syncwarp();
+            if (lane == 0) codes[j] = static_cast<uint8_t>(code);
+            __syncwarp();
+        }
+    }
+    return changed;
+}
+
 template <int D, bool HAD, bool VMSE>
 __global__ void __launch_bounds__(kThreads, 2)
 compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
@@ -518,9 +574,12 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             if (s_thr[code + step] <= z) code += step;
         const float dmin = fminf(z - s_thr[code], s_thr[code + 1] - z);
         if (fl == 2) code = 0;
-        codes[row * CS + i] = static_cast<uint8_t>(code);
+        // a code inside the guard band of a threshold is marked (0x80) and its row
+        // flagged 3: the exact pass re-decides just the marked codes
+        const bool mark = (fl == 0 || fl == 3) && dmin < kCodeGuard;
+        codes[row * CS + i] = static_cast<uint8_t>(code | (mark ? 0x80 : 0));
         yb[e] = (fl == 2) ? 0.f : z - s_cent[code];
-        if (fl == 0 && dmin < kCodeGuard) s_flag[row] = 1;
+        if (mark) s_flag[row] = 3;
     }
     __syncthreads();
     // ---- QJL: p = S r, gamma, sign guard ---------------------------------------
@@ -538,17 +597,25 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             if (lane == 0) {
                 s_rn[row] = rn;
                 s_g16[row] = float_to_bf16_bits(rn / sqrtd);
-                if (near && s_flag[row] == 0) s_flag[row] = 1;
+                if (near && (s_flag[row] == 0 || s_flag[row] == 3)) s_flag[row] = 1;
             }
         }
         __syncthreads();
     }
-    // ---- exact path for flagged rows -------------------------------------------
+    // ---- exact path for flagged rows: marked codes re-decided one by one (a changed
+    // code under QJL changes the residual: the whole row is redone), other flagged
+    // rows redone entirely ------------------------------------------------------
     for (int row = warp; row < TM; row += kWarps) {
-        if (s_flag[row] != 1 || s_dst[row] < 0) continue;
+        int fl = s_flag[row];
+        if ((fl != 1 && fl != 3) || s_dst[row] < 0) continue;
         const int64_t r = r0 + row;
         const int64_t t = r / Hkv;
         const int h = static_cast<int>(r - t * Hkv);
+        if (fl == 3) {
+            const bool changed = refine_marked_codes<D>(C.Pi, kin + t * ks + static_cast<int64_t>(h) * D,
+                                                        codes + row * CS, C.thresholds, (1 << C.k_bits) - 1);
+            if (!(changed && C.qjl)) continue;
+        }
         precise_key_row<D>(C, kin + t * ks + static_cast<int64_t>(h) * D, codes + row * CS, kf + row * D,
                            scratch + warp * D, &s_n16[row], &s_g16[row], C.thresholds, C.centroids, C.k_bits,
                            C.qjl != 0);
@@ -722,15 +789,22 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             for (int step = 1 << (vb - 1); step > 0; step >>= 1)
                 if (s_thr[code + step] <= z) code += step;
             const float dmin = fminf(z - s_thr[code], s_thr[code + 1] - z);
-            codes[row * CS + i] = static_cast<uint8_t>(fl == 2 ? 0 : code);
-            if (fl == 0 && dmin < kCodeGuard) s_flag[row] = 1;
+            const bool mark = (fl == 0 || fl == 3) && dmin < kCodeGuard;
+            codes[row * CS + i] = static_cast<uint8_t>((fl == 2 ? 0 : code) | (mark ? 0x80 : 0));
+            if (mark) s_flag[row] = 3;
         }
         __syncthreads();
         for (int row = warp; row < TM; row += kWarps) {
-            if (s_flag[row] != 1 || s_dst[row] < 0) continue;
+            const int fl = s_flag[row];
+            if ((fl != 1 && fl != 3) || s_dst[row] < 0) continue;
             const int64_t r = r0 + row;
             const int64_t t = r / Hkv;
             const int h = static_cast<int>(r - t * Hkv);
+            if (fl == 3) {  // no QJL on values: the re-decided codes are final
+                refine_marked_codes<D>(C.Pi, vin + t * vs + static_cast<int64_t>(h) * D, codes + row * CS,
+                                       C.vthresholds, (1 << C.v_bits) - 1);
+                continue;
+            }
             precise_key_row<D>(C, vin + t * vs + static_cast<int64_t>(h) * D, codes + row * CS, kf + row * D,
                                scratch + warp * D, &s_n16[row], &s_g16[row], C.vthresholds, C.vcentroids, C.v_bits,
                                false);
