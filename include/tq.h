@@ -210,18 +210,27 @@ tq_status tq_decode_attention(tq_handle h, const uint16_t *q, const uint8_t *k_c
  *   (positions below 0 -- a sequence shorter than q_tokens -- see nothing and
  *   give zero rows).  Query head qh reads kv head qh / (Hq / Hkv).
  * block_table, seq_lens, pools, sm_scale, splits, status bits: as in
- *   tq_decode_attention; splits = 0 picks tq_decode_splits over
- *   B * ceil(q_tokens / tq_prefill_queries_per_cta(...)) work units.
+ *   tq_decode_attention; splits = 0 picks tq_prefill_splits(...).
  * workspace: ws_bytes >= tq_decode_workspace_bytes(h, B * q_tokens, Hq, splits),
  *   256-byte aligned; it starts with the fp32 outputs [B][q_tokens][Hq][d].
  * out: device bf16 [B][q_tokens][Hq][d].
- * The split-K kernel of the decode gives each CTA tq_prefill_queries_per_cta
- * consecutive query tokens (their (token, head) pairs are the N columns of its
- * tensor-core products, so every key and value operand built from the codes
- * serves all of them), each column with its own causal limit and online
- * softmax.  Three launches on `stream` (query rotation, split-K, combine).
+ * A CTA takes tq_prefill_queries_per_cta consecutive query tokens of one
+ * sequence and kv head; their (token, head) pairs are the columns of its
+ * tensor-core products, so every key and value operand decoded from the codes
+ * serves all of them, and each column keeps its own causal limit and online
+ * softmax.  head_dim 128: 128 columns per CTA (128 / G query tokens), the pages
+ * of each 64-token tile decoded once into shared-memory operand tiles, scores
+ * and P.V on tcgen05.mma with the accumulators in tensor memory.  head_dim 256:
+ * the decode's split-K kernel with 8 columns per CTA (8 / G query tokens).
+ * Three launches on `stream` (query rotation, split-K, combine).
+ *
+ * tq_prefill_queries_per_cta: query tokens per CTA for this handle and G.
+ * tq_prefill_splits: the split count tq_prefill_attention picks for splits = 0
+ *   (from the sizes only: it never reads seq_lens).
  */
 int tq_prefill_queries_per_cta(tq_handle h, int num_q_heads, int num_kv_heads);
+int tq_prefill_splits(tq_handle h, int batch, int q_tokens, int num_q_heads, int num_kv_heads,
+                      int max_blocks_per_seq, int page_size);
 tq_status tq_prefill_attention(tq_handle h, const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
                                const int32_t *block_table, const int32_t *seq_lens, int batch, int q_tokens,
                                int num_q_heads, int num_kv_heads, int page_size, int max_blocks_per_seq,

@@ -116,8 +116,7 @@ class Codec:
         assert d == self.head_dim and q.dtype == torch.bfloat16 and q.is_contiguous()
         maxb = block_table.shape[1]
         if splits == 0:
-            qpc = native.tq_prefill_queries_per_cta(self.handle, Hq, num_kv_heads)
-            splits = self.decode_splits(B * ((Tq + qpc - 1) // qpc), num_kv_heads, maxb, page_size)
+            splits = native.tq_prefill_splits(self.handle, B, Tq, Hq, num_kv_heads, maxb, page_size)
         if workspace is None:
             workspace = self.workspace(B * Tq, Hq, splits, device=q.device)
         if out is None:

@@ -422,7 +422,29 @@ int tq_prefill_queries_per_cta(tq_handle h, int num_q_heads, int num_kv_heads)
 {
     if (!h || num_kv_heads < 1 || num_q_heads < num_kv_heads) return 1;
     const int G = num_q_heads / num_kv_heads;
+    if (h->codec.d == 128) return 128 / G;  // the tensor-memory kernel's 128 columns
     return G >= 8 ? 1 : 8 / G;
+}
+
+int tq_prefill_splits(tq_handle h, int batch, int q_tokens, int num_q_heads, int num_kv_heads,
+                      int max_blocks_per_seq, int page_size)
+{
+    if (!h || batch < 1 || q_tokens < 1 || num_kv_heads < 1 || num_q_heads < num_kv_heads || max_blocks_per_seq < 1 ||
+        page_size < 1)
+        return 1;
+    const int qpc = tq_prefill_queries_per_cta(h, num_q_heads, num_kv_heads);
+    const long long units_z = static_cast<long long>(batch) * ((q_tokens + qpc - 1) / qpc);
+    if (h->codec.d != 128)
+        return tq_decode_splits(h, static_cast<int>(units_z < 65535 ? units_z : 65535), num_kv_heads,
+                                max_blocks_per_seq, page_size);
+    // one CTA per SM: about two waves, each split keeping at least four 64-token tiles
+    const long long units = units_z * num_kv_heads;
+    long long splits = (2LL * h->num_sms + units - 1) / units;
+    const int tiles = (max_blocks_per_seq * page_size + 63) / 64;
+    const int most = tiles / 4 > 1 ? tiles / 4 : 1;
+    if (splits > most) splits = most;
+    if (splits > 64) splits = 64;
+    return splits < 1 ? 1 : static_cast<int>(splits);
 }
 
 tq_status tq_prefill_attention(tq_handle h, const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
@@ -451,7 +473,7 @@ tq_status tq_prefill_attention(tq_handle h, const uint16_t *q, const uint8_t *k_
         !aligned(seq_lens, 4) || !aligned(workspace, 256) || !aligned(out, 16))
         return fail(TQ_ERR_INVALID_ARG, "tq_prefill_attention: misaligned pointer");
     if (splits == 0)
-        splits = tq_decode_splits(h, static_cast<int>(ctas_z), num_kv_heads, max_blocks_per_seq, page_size);
+        splits = tq_prefill_splits(h, batch, q_tokens, num_q_heads, num_kv_heads, max_blocks_per_seq, page_size);
     if (splits > 1024) return fail(TQ_ERR_UNSUPPORTED, "tq_prefill_attention: splits %d above 1024", splits);
     const size_t need = tq::decode_workspace_bytes(h->codec.d, batch * q_tokens, num_q_heads, splits);
     if (ws_bytes < need)

@@ -191,8 +191,11 @@ __global__ void __launch_bounds__(D) combine_kernel(const Codec C, const DecodeA
 template <int D, int KB, int VB>
 cudaError_t launch_dmma(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st)
 {
+    if (a.Tq > 1) {  // prefill: head_dim 128 on tensor memory, 256 on this kernel with query columns
+        if (c.d == 128) return launch_prefill_tc(c, pg, a, st);
+        return c.vmse ? launch_dmma_vmse(c, pg, a, st) : launch_dmma_prefill(c, pg, a, st);
+    }
     if (c.vmse) return launch_dmma_vmse(c, pg, a, st);
-    if (a.Tq > 1) return launch_dmma_prefill(c, pg, a, st);
     const size_t smem = dmma::DecSmem<D, KB>::bytes(pg);
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(dmma::decode_mma_kernel<D, KB, VB, false>), smem);
     if (e != cudaSuccess) return e;

@@ -18,12 +18,14 @@ cudaError_t launch_vm(const Codec &c, const PageGeom &pg, const DecodeArgs &a, c
 {
     const size_t smem = dmma::DecSmem<D, KB, VB, true>::bytes(pg);
     dim3 grid(a.splits, a.Hkv, a.B * ((a.Tq + a.qpc - 1) / a.qpc));
-    if (a.Tq > 1) {  // prefill with values coded by the rotation
-        cudaError_t e =
-            ensure_smem_attr(reinterpret_cast<const void *>(dmma::decode_mma_kernel<D, KB, VB, true, true>), smem);
-        if (e != cudaSuccess) return e;
-        dmma::decode_mma_kernel<D, KB, VB, true, true><<<grid, dmma::kThreads, smem, st>>>(c, pg, a);
-        return cudaGetLastError();
+    if constexpr (D == 256) {
+        if (a.Tq > 1) {  // prefill with values coded by the rotation (head_dim 128 runs the tensor-memory kernel)
+            cudaError_t e = ensure_smem_attr(
+                reinterpret_cast<const void *>(dmma::decode_mma_kernel<D, KB, VB, true, true>), smem);
+            if (e != cudaSuccess) return e;
+            dmma::decode_mma_kernel<D, KB, VB, true, true><<<grid, dmma::kThreads, smem, st>>>(c, pg, a);
+            return cudaGetLastError();
+        }
     }
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(dmma::decode_mma_kernel<D, KB, VB, true>), smem);
     if (e != cudaSuccess) return e;

@@ -109,8 +109,13 @@ cudaError_t launch_decode(const Codec &c, const PageGeom &pg, const DecodeArgs &
 cudaError_t launch_combine(const Codec &c, const DecodeArgs &a, cudaStream_t st, bool unrotate);
 // The split-K decode kernel for values coded by the rotation (its own translation unit).
 cudaError_t launch_dmma_vmse(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st);
-// The split-K kernel with several causal query tokens per sequence (prefill; its own translation unit).
+// The split-K kernel with several causal query tokens per sequence (prefill at head_dim 256; its own
+// translation unit).
 cudaError_t launch_dmma_prefill(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st);
+// Prefill at head_dim 128 on the tensor cores with accumulators in tensor memory:
+// 128 (query token, head) columns per CTA, qpc = 128 / G query tokens.
+cudaError_t launch_prefill_tc(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st);
+size_t prefill_tc_smem_bytes(const PageGeom &pg);
 
 // Device address of the no-allocation decode's static scratch array for the
 // context current on the calling thread (looked up, not cached).

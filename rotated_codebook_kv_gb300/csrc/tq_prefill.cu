@@ -1,5 +1,5 @@
 // tq_prefill.cu -- the split-K kernel instantiated for chunked prefill over the
-// compressed cache (turbo-attn, "How it works": the prefill path dequantises the
+// compressed cache at head_dim 256 (turbo-attn, "How it works": the prefill path dequantises the
 // codec inline, with no decompress buffer).  Each CTA takes qpc consecutive
 // query tokens of one sequence; their (token, head) pairs are the N columns of
 // the score and value products, each with its own causal limit and online
@@ -49,7 +49,9 @@ cudaError_t launch_pf_d(const Codec &c, const PageGeom &pg, const DecodeArgs &a,
 
 cudaError_t launch_dmma_prefill(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st)
 {
-    return c.d == 128 ? launch_pf_d<128>(c, pg, a, st) : launch_pf_d<256>(c, pg, a, st);
+    // head_dim 256 only: 128 runs the tensor-memory kernel (tq_prefill_tc.cu), whose
+    // query operands and output would not fit tensor memory next to the scores at 256
+    return launch_pf_d<256>(c, pg, a, st);
 }
 
 }  // namespace tq

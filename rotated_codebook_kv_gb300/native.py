@@ -33,6 +33,7 @@ SIGNATURES = {
     "tq_decode_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _f32, _i32,
                                    _vp, _sz, _vp, _vp]),
     "tq_prefill_queries_per_cta": (_i32, [_vp, _i32, _i32]),
+    "tq_prefill_splits": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32]),
     "tq_prefill_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
                                     _i32, _vp, _sz, _vp, _vp]),
     "tq_decode_attention_bf16": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64, _f32,
@@ -138,6 +139,10 @@ def tq_decode_attention(h, q, k_cache, v_cache, block_table, seq_lens, batch, nu
 
 def tq_prefill_queries_per_cta(h, num_q_heads, num_kv_heads) -> int:
     return load().tq_prefill_queries_per_cta(h, num_q_heads, num_kv_heads)
+
+
+def tq_prefill_splits(h, batch, q_tokens, num_q_heads, num_kv_heads, max_blocks_per_seq, page_size) -> int:
+    return load().tq_prefill_splits(h, batch, q_tokens, num_q_heads, num_kv_heads, max_blocks_per_seq, page_size)
 
 
 def tq_prefill_attention(h, q, k_cache, v_cache, block_table, seq_lens, batch, q_tokens, num_q_heads, num_kv_heads,
