@@ -28,8 +28,8 @@
 //               softmax with a lazy rescale of O (only when the running maximum grows
 //               by more than 2^8, so P <= 2^8 stays exact in fp16), P into tensor
 //               memory, the partial outputs at the end;
-//   warps 4-11  page copies (cp.async.bulk, three stages) and the decode of a tile
-//               into fp16 operand tiles (two stages);
+//   warps 4-11  page copies (cp.async.bulk, two stages) and the decode of a tile
+//               into fp16 operand tiles (three stages);
 //   warp 12     tensor-memory allocation; lane 0 issues the MMAs.
 // Every wait is bounded by the codec's wait limit; a timeout sets
 // TQ_DEVERR_TIMEOUT, stops the CTA (its split then carries no weight), lets
@@ -51,7 +51,8 @@ constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kCols = 128;                 // columns per CTA (M of every MMA)
 constexpr int kTok = 64;                   // tokens per tile
-constexpr int kRaw = 3;                    // page stages
+constexpr int kRaw = 2;                    // page stages
+constexpr int kOps = 3;                    // operand stages
 constexpr float kKScale = 256.f;           // centroids enter the MMA as 2^8 c
 constexpr float kLazy = 8.f;               // rescale O only when the maximum grows by more than this (log2 units)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -67,25 +68,25 @@ constexpr uint32_t kTmCols = 512;
 // shared memory (bytes)
 constexpr uint32_t kTileBytes = kTok * D * 2;          // one fp16 operand tile, 16 KB
 constexpr uint32_t kOpBytes = 4 * kTileBytes;          // Kh, Kl, Ks (signed gamma), Vt per stage
-constexpr uint32_t kLutOff = 2 * kOpBytes;             // key centroid pairs: 256 x (high pair, low pair)
-constexpr uint32_t kSlutOff = kLutOff + 2048;          // 4 sign bits -> 4 fp16 +-1
-constexpr uint32_t kVlutOff = kSlutOff + 128;          // value centroid pairs (values coded by the rotation)
-constexpr uint32_t kTokOff = kVlutOff + 1024;          // [2][64] float: n_t sm_scale log2(e) / sqrt(d)
-constexpr uint32_t kOkOff = kTokOff + 512;             // [2] uint64: tokens of a valid page
-constexpr uint32_t kPageOkOff = kOkOff + 16;           // [3][4] int
+constexpr uint32_t kLutOff = kOps * kOpBytes;          // key centroid pairs (high pair, low pair), in copies
+constexpr uint32_t kLutBytes = 8192;
+constexpr uint32_t kVlutOff = kLutOff + kLutBytes;     // value centroid pairs (values coded by the rotation)
+constexpr uint32_t kTokOff = kVlutOff + 1024;          // [3][64] float: n_t sm_scale log2(e) / sqrt(d)
+constexpr uint32_t kOkOff = kTokOff + 768;             // [3] uint64: tokens of a valid page
+constexpr uint32_t kPageOkOff = kOkOff + 32;           // [kRaw <= 3][4] int
 constexpr uint32_t kMbarOff = kPageOkOff + 48;
-constexpr int kNumMbar = 14;
+constexpr int kNumMbar = 16;
 constexpr uint32_t kMiscOff = kMbarOff + 8 * kNumMbar;  // tensor-memory base, abort flag
 constexpr uint32_t kRawOff = (kMiscOff + 16 + 127) / 128 * 128;
 // mbarrier indices
-constexpr int kBarRaw = 0;       // [3] a page stage landed (ppt arrivals + bytes)
-constexpr int kBarOpFull = 3;    // [2] an operand stage is decoded (256 producer arrivals)
-constexpr int kBarOpFree = 5;    // [2] the MMAs reading an operand stage are done (commit)
-constexpr int kBarSFull = 7;     // [2] scores of a tile are in tensor memory (commit)
-constexpr int kBarSFree = 9;     // [2] the softmax threads have read a score buffer (128 arrivals)
-constexpr int kBarPFull = 11;    // P of a tile is in tensor memory, O rescaled (128 arrivals)
-constexpr int kBarPvDone = 12;   // O += P V of a tile is done (commit)
-constexpr int kBarMmaDone = 13;  // teardown: every MMA issued is done (commit)
+constexpr int kBarRaw = 0;       // [kRaw <= 3] a page stage landed (ppt arrivals + bytes)
+constexpr int kBarOpFull = 3;    // [3] an operand stage is decoded (256 producer arrivals)
+constexpr int kBarOpFree = 6;    // [3] the MMAs reading an operand stage are done (commit)
+constexpr int kBarSFull = 9;     // [2] scores of a tile are in tensor memory (commit)
+constexpr int kBarSFree = 11;    // [2] the softmax threads have read a score buffer (128 arrivals)
+constexpr int kBarPFull = 13;    // P of a tile is in tensor memory, O rescaled (128 arrivals)
+constexpr int kBarPvDone = 14;   // O += P V of a tile is done (commit)
+constexpr int kBarMmaDone = 15;  // teardown: every MMA issued is done (commit)
 
 __host__ __device__ inline uint32_t raw_stage_bytes(const PageGeom &pg)
 {
@@ -131,6 +132,32 @@ __device__ __forceinline__ void tm_st32(uint32_t taddr, const uint32_t (&r)[32])
                  : "memory");
 }
 
+// 64 consecutive fp32 columns of this thread's tensor-memory lane (one wait).
+__device__ __forceinline__ void tm_ld64(uint32_t taddr, float (&v)[64])
+{
+    uint32_t r[64];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,"
+                 "%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]),
+                   "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+                   "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+                   "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
+                   "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Copies of the key centroid-pair table (8 KB at most): 2-bit codes fill the 32 banks
+// once, 3-bit codes 16 copies (conflict-free), 4-bit codes 4 copies.
+__host__ __device__ constexpr int lut_copies(int kb) { return kb == 2 ? 1 : (kb == 3 ? 16 : 4); }
+
 // (fp16 hi, fp16 lo) of x with hi + lo ~ x to ~22 bits.
 __device__ __forceinline__ void split_half(float x, __half &hi, __half &lo)
 {
@@ -147,6 +174,77 @@ __device__ __forceinline__ float fast_exp2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+struct KeyItem {
+    const unsigned char *raw;  // page stage
+    const int *pok;            // page validity of the stage
+    uint32_t page_bytes;
+    int pshift, P, pt;         // pt: producer thread 0..255
+    int64_t sign_off, gamma_off;
+};
+
+// The producer thread's 4 key items (token t, 8-coordinate chunk c): fp16 high and low
+// parts of 2^8 c[code] from the pair table (the thread's copy `lut`), and with QJL the
+// 8 values +-2^8 g_t (sign bit set where the QJL bit is 0).  Items (it = pt + 256 k)
+// map the 8 lanes of a store phase to the 8 rows of one core matrix.  All loads are
+// issued before any table lookup.
+template <int KB>
+__device__ __forceinline__ void decode_keys(const KeyItem &ki, const uint2 *lut, unsigned char *kh,
+                                            unsigned char *kl, unsigned char *ksg)
+{
+    constexpr bool QJL = KB <= 3;
+    constexpr int CP = lut_copies(KB);
+    constexpr uint32_t PM = (1u << (2 * KB)) - 1u;
+    constexpr int CODE_BYTES = D * KB / 8, SIGN_BYTES = D / 8;
+    uint32_t w[4], sb[4], g[4], off[4];
+    bool tv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int it = ki.pt + kProdThreads * k;
+        const int t = ((it >> 7) << 3) | (it & 7), c = (it >> 3) & 15;
+        const int q = t >> ki.pshift, o = t & (ki.P - 1);
+        tv[k] = ki.pok[q] != 0;
+        const unsigned char *kp = ki.raw + q * ki.page_bytes;
+        const unsigned char *crow = kp + o * CODE_BYTES;
+        if constexpr (KB == 4) {
+            w[k] = *reinterpret_cast<const uint32_t *>(crow + 4 * c);
+        } else if constexpr (KB == 2) {
+            w[k] = *reinterpret_cast<const uint16_t *>(crow + 2 * c);
+        } else {
+            const int by = 3 * c;
+            const uint32_t *wp = reinterpret_cast<const uint32_t *>(crow + (by & ~3));
+            w[k] = __funnelshift_r(wp[0], wp[1], 8 * (by & 3));
+        }
+        if constexpr (QJL) {
+            sb[k] = kp[ki.sign_off + o * SIGN_BYTES + c];
+            g[k] = *reinterpret_cast<const uint16_t *>(kp + ki.gamma_off + 2 * o);
+        }
+        off[k] = umma::core_offset(t, 8 * c, D);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = hv;
+        if (tv[k]) {
+            const uint2 e0 = lut[(w[k] & PM) * CP], e1 = lut[((w[k] >> (2 * KB)) & PM) * CP];
+            const uint2 e2 = lut[((w[k] >> (4 * KB)) & PM) * CP], e3 = lut[((w[k] >> (6 * KB)) & PM) * CP];
+            hv = make_uint4(e0.x, e1.x, e2.x, e3.x);
+            lv = make_uint4(e0.y, e1.y, e2.y, e3.y);
+        }
+        st128(kh + off[k], hv);
+        st128(kl + off[k], lv);
+        if constexpr (QJL) {
+            uint4 sv = make_uint4(0u, 0u, 0u, 0u);
+            if (tv[k]) {
+                // fp16 2^8 g (exact: a bf16 times 2^8, g >= 0), sign bit set where the bit is 0
+                const uint32_t g2 = half2_bits(__float2half2_rn(bf16_to_float(g[k]) * kKScale));
+                const uint32_t nb = ~sb[k];
+                auto sg = [&](int m) { return g2 | (((nb >> (2 * m)) & 1u) << 15) | (((nb >> (2 * m + 1)) & 1u) << 31); };
+                sv = make_uint4(sg(0), sg(1), sg(2), sg(3));
+            }
+            st128(ksg + off[k], sv);
+        }
+    }
 }
 
 struct ValueItem {
@@ -283,19 +381,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
     // ---- set-up: tensor memory, tables, barriers --------------------------------
     if (warp == kMmaWarp) umma::tmem_alloc(tmem_slot, kTmCols);
     {
+        // entry e (two codes) in lut_copies(kb) copies at (e * copies + copy): lane l reads
+        // copy l % copies, so 3-bit lookups never share a bank pair within a half warp
         uint2 *lut = reinterpret_cast<uint2 *>(smem + kLutOff);
-        const int M = (1 << kb) - 1;
-        for (int e = tid; e < (1 << (2 * kb)); e += kThreads) {
+        const int M = (1 << kb) - 1, cp = lut_copies(kb);
+        for (int x = tid; x < (1 << (2 * kb)) * cp; x += kThreads) {
+            const int e = x / cp;
             __half h0, l0, h1, l1;
             split_half(kKScale * C.centroids[e & M], h0, l0);
             split_half(kKScale * C.centroids[e >> kb], h1, l1);
-            lut[e] = make_uint2(half2_bits(__halves2half2(h0, h1)), half2_bits(__halves2half2(l0, l1)));
-        }
-        if (tid < 16) {
-            uint2 *slut = reinterpret_cast<uint2 *>(smem + kSlutOff);
-            auto pm = [](int bit) { return __float2half_rn(bit ? 1.f : -1.f); };
-            slut[tid] = make_uint2(half2_bits(__halves2half2(pm(tid & 1), pm(tid & 2))),
-                                   half2_bits(__halves2half2(pm(tid & 4), pm(tid & 8))));
+            lut[x] = make_uint2(half2_bits(__halves2half2(h0, h1)), half2_bits(__halves2half2(l0, l1)));
         }
         if (C.vmse) {  // value centroid pairs: fp16(lambda c) of two tokens' codes
             uint32_t *vlut = reinterpret_cast<uint32_t *>(smem + kVlutOff);
@@ -307,9 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
     }
     if (tid == 0) {
         for (int i = 0; i < kRaw; ++i) umma::mbar_init(&mbar[kBarRaw + i], ppt);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kOps; ++i) {
             umma::mbar_init(&mbar[kBarOpFull + i], kProdThreads);
             umma::mbar_init(&mbar[kBarOpFree + i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             umma::mbar_init(&mbar[kBarSFull + i], 1);
             umma::mbar_init(&mbar[kBarSFree + i], kSoftWarps * 32);
         }
@@ -345,14 +442,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
         return false;
     };
 
-    // page copies of tile i into stage i % 3, by lanes q < ppt of the first producer warp
-    auto issue = [&](int i) {
+    // page copies of tile i into stage i % kRaw, by lanes q < ppt of the first producer warp
+    // block id of this lane's page of tile i (-1 past the split); read a tile ahead of its
+    // issue so that the global load's latency is not paid on the producers' path
+    auto fetch_blk = [&](int i) -> int {
+        const int pg = pg0 + i * ppt + lane;
+        return (i < ntiles && pg < pg1) ? A.block_table[static_cast<int64_t>(b) * A.max_blocks + pg] : -1;
+    };
+    auto issue = [&](int i, int blk) {
         const int r = i % kRaw, q = lane;
         const int pg = pg0 + i * ppt + q;
         int ok = 0;
-        int blk = -1;
         if (pg < pg1) {
-            blk = A.block_table[static_cast<int64_t>(b) * A.max_blocks + pg];
             ok = (blk >= 0 && blk < A.num_blocks);
             if (!ok) atomicOr(C.status, TQ_DEVERR_BLOCK_RANGE);
         }
@@ -435,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
         umma::wait_st();
         umma::fence_before_sync();
     } else if (warp == kSoftWarps && lane < ppt) {
-        for (int i = 0; i < kRaw && i < ntiles; ++i) issue(i);
+        for (int i = 0; i < kRaw && i < ntiles; ++i) issue(i, fetch_blk(i));
     }
     __syncthreads();  // query operands in tensor memory; the first page copies are on their way
     umma::fence_after_sync();
@@ -445,24 +546,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
         // ================= producers: page copies and operand decode =================
         const int pt = tid - kSoftWarps * 32;
         const float afac = A.sm_scale * rsqrtf(static_cast<float>(D)) * kLog2e;
-        const uint2 *lut = reinterpret_cast<const uint2 *>(smem + kLutOff);
-        const uint2 *slut = reinterpret_cast<const uint2 *>(smem + kSlutOff);
+        const uint2 *lut = reinterpret_cast<const uint2 *>(smem + kLutOff) + (lane & (lut_copies(kb) - 1));
         const uint32_t *vlut = reinterpret_cast<const uint32_t *>(smem + kVlutOff);
-        const uint32_t PM = (1u << (2 * kb)) - 1u;
         int issued = min(kRaw, ntiles);
+        int bnext = (warp == kSoftWarps && lane < ppt) ? fetch_blk(kRaw) : -1;  // the next tile to issue
         int i = 0;
         for (; i < ntiles; ++i) {
-            const int r = i % kRaw, s = i & 1;
+            const int r = i % kRaw, s = i % kOps;
             bool ok = wait_bar(kBarRaw + r, (i / kRaw) & 1);
-            if (ok && i >= 2) ok = wait_bar(kBarOpFree + s, ((i - 2) >> 1) & 1);
+            if (ok && i >= kOps) ok = wait_bar(kBarOpFree + s, ((i - kOps) / kOps) & 1);
             // every producer is past tile i - 1: its page stage may be refilled
             const bool fail = bar_or(1, kProdThreads, !ok);
             if (fail) {
                 aborted = true;
                 break;
             }
-            if (i >= 1 && warp == kSoftWarps && lane < ppt && i + 2 < ntiles) issue(i + 2);
-            if (i >= 1) issued = max(issued, min(i + 3, ntiles));
+            if (i >= 1 && warp == kSoftWarps && lane < ppt) {
+                if (i + kRaw - 1 < ntiles) issue(i + kRaw - 1, bnext);
+                bnext = fetch_blk(i + kRaw);
+            }
+            if (i >= 1) issued = max(issued, min(i + kRaw, ntiles));
 
             const unsigned char *raw = smem + kRawOff + r * raw_bytes;
             const int *pok = page_ok + r * 4;
@@ -484,46 +587,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
             }
             // ---- keys: item (token t, 8-coordinate chunk c); the 8 lanes of a store phase
             // write the 8 rows of one core matrix ----
-#pragma unroll 1
-            for (int k = 0; k < 4; ++k) {
-                const int it = pt + kProdThreads * k;
-                const int t = ((it >> 7) << 3) | (it & 7), c = (it >> 3) & 15;
-                const int q = t >> pshift, o = t & (P - 1);
-                const bool tv = pok[q] != 0;
-                const unsigned char *kp = raw + q * page_bytes;
-                const unsigned char *crow = kp + o * C.k_code_bytes;
-                uint32_t w;
-                if (kb == 4) {
-                    w = *reinterpret_cast<const uint32_t *>(crow + 4 * c);
-                } else if (kb == 2) {
-                    w = *reinterpret_cast<const uint16_t *>(crow + 2 * c);
-                } else {
-                    const int by = 3 * c;
-                    const uint32_t *wp = reinterpret_cast<const uint32_t *>(crow + (by & ~3));
-                    w = __funnelshift_r(wp[0], wp[1], 8 * (by & 3));
-                }
-                uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = hv;
-                if (tv) {
-                    const uint2 e0 = lut[w & PM], e1 = lut[(w >> (2 * kb)) & PM];
-                    const uint2 e2 = lut[(w >> (4 * kb)) & PM], e3 = lut[(w >> (6 * kb)) & PM];
-                    hv = make_uint4(e0.x, e1.x, e2.x, e3.x);
-                    lv = make_uint4(e0.y, e1.y, e2.y, e3.y);
-                }
-                const uint32_t off = umma::core_offset(t, 8 * c, D);
-                st128(kh + off, hv);
-                st128(kl + off, lv);
-                if (qjl) {
-                    uint4 sv = make_uint4(0u, 0u, 0u, 0u);
-                    if (tv) {
-                        const uint32_t sb = kp[PG.k_sign_off + o * C.k_sign_bytes + c];
-                        const float g = bf16_to_float(*reinterpret_cast<const uint16_t *>(kp + PG.k_gamma_off + 2 * o));
-                        const __half2 g2 = __float2half2_rn(g * kKScale);  // exact: bf16 times 2^8
-                        const uint2 a = slut[sb & 15u], bb = slut[sb >> 4];
-                        sv = make_uint4(half2_bits(__hmul2(bits_half2(a.x), g2)), half2_bits(__hmul2(bits_half2(a.y), g2)),
-                                        half2_bits(__hmul2(bits_half2(bb.x), g2)), half2_bits(__hmul2(bits_half2(bb.y), g2)));
-                    }
-                    st128(ksg + off, sv);
-                }
+            {
+                const KeyItem ki{raw, pok, page_bytes, pshift, P, pt, PG.k_sign_off, PG.k_gamma_off};
+                if (kb == 2) decode_keys<2>(ki, lut, kh, kl, ksg);
+                else if (kb == 3) decode_keys<3>(ki, lut, kh, kl, ksg);
+                else decode_keys<4>(ki, lut, kh, kl, ksg);
             }
             // ---- values: item (32-coordinate block jb, token chunk tc, row j7): coordinates
             // 32 jb + 8 k + j7 (k = 0..3) of tokens 8 tc .. 8 tc + 7, one 16-byte core-matrix
@@ -556,29 +624,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
             // the value tile 128 x 64 (LBO 128, SBO 1024); a 16-wide k-step adds 256 bytes
             auto desc = [&](uint32_t addr, uint32_t sbo) { return umma::make_desc(addr, 128, sbo); };
             auto pv = [&](int j) {  // O += P V of tile j
-                const int s = j & 1;
+                const int s = j % kOps;
                 const uint32_t vaddr = sbase + s * kOpBytes + 3 * kTileBytes;
 #pragma unroll
-                for (int k = 0; k < kTok / 16; ++k)
-                    umma::mma_f16_tmem_a(tbase + kTmO, tbase + kTmP + 8 * k,
-                                         static_cast<uint32_t>(desc(vaddr + 256 * k, 1024)),
-                                         static_cast<uint32_t>(desc(vaddr + 256 * k, 1024) >> 32), id_o,
-                                         (j > 0 || k > 0) ? 1 : 0);
+                for (int k = 0; k < kTok / 16; ++k) {
+                    const uint64_t dv = desc(vaddr + 256 * k, 1024);
+                    umma::mma_f16_tmem_a(tbase + kTmO, tbase + kTmP + 8 * k, static_cast<uint32_t>(dv),
+                                         static_cast<uint32_t>(dv >> 32), id_o, (j > 0 || k > 0) ? 1 : 0);
+                }
                 umma::commit(&mbar[kBarPvDone]);
                 umma::commit(&mbar[kBarOpFree + s]);
             };
-            int i = 0;
-            for (; i < ntiles; ++i) {
-                const int s = i & 1;
-                bool ok = wait_bar(kBarOpFull + s, (i >> 1) & 1);
-                if (ok && i >= 2) ok = wait_bar(kBarSFree + s, ((i - 2) >> 1) & 1);
-                if (!ok) {
-                    aborted = true;
-                    break;
-                }
-                umma::fence_after_sync();
+            auto scores = [&](int j) {  // S = Q' K'^T (+ QJL) of tile j into score buffer j % 2
+                const int s = j % kOps;
                 const uint32_t kaddr = sbase + s * kOpBytes;
-                const uint32_t d_s = tbase + kTmS + 64 * s;
+                const uint32_t d_s = tbase + kTmS + 64 * (j & 1);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint64_t dh = desc(kaddr + 256 * k, 2048);
@@ -595,22 +655,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
                                              static_cast<uint32_t>(dg >> 32), id_s, 1);
                     }
                 }
-                umma::commit(&mbar[kBarSFull + s]);
-                if (i >= 1) {
-                    if (!wait_bar(kBarPFull, (i - 1) & 1)) {
-                        aborted = true;
-                        break;
-                    }
+                umma::commit(&mbar[kBarSFull + (j & 1)]);
+            };
+            // issue in the order the hand-offs complete: P.V of tile npv as soon as its P
+            // is in tensor memory (that frees an operand stage for the producers), the
+            // scores of tile ns as soon as its operands are decoded and its score buffer
+            // has been read; give up after the wait limit without progress
+            int ns = 0, npv = 0;
+            long long t_last = clock64();
+            while (npv < ntiles) {
+                if (npv < ns && umma::mbar_test_wait(&mbar[kBarPFull], npv & 1)) {
                     umma::fence_after_sync();
-                    pv(i - 1);
+                    pv(npv++);
+                    t_last = clock64();
+                    continue;
                 }
-            }
-            if (!aborted) {
-                if (wait_bar(kBarPFull, (ntiles - 1) & 1)) {
+                if (ns < ntiles && umma::mbar_test_wait(&mbar[kBarOpFull + ns % kOps], (ns / kOps) & 1) &&
+                    (ns < 2 || umma::mbar_test_wait(&mbar[kBarSFree + (ns & 1)], ((ns - 2) >> 1) & 1))) {
                     umma::fence_after_sync();
-                    pv(ntiles - 1);
-                } else {
+                    scores(ns++);
+                    t_last = clock64();
+                    continue;
+                }
+                if (*abort_flag) {
                     aborted = true;
+                    break;
+                }
+                if (C.wait_limit <= 0 || clock64() - t_last > C.wait_limit) {
+                    *abort_flag = 1;
+                    atomicOr(C.status, TQ_DEVERR_TIMEOUT);
+                    aborted = true;
+                    break;
                 }
             }
             // every MMA issued must be done before tensor memory is freed
@@ -625,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
         float m_run = -INFINITY, l_run = 0.f;
         int i = 0;
         for (; i < ntiles; ++i) {
-            const int s = i & 1;
+            const int s = i & 1, s3 = i % kOps;
             const bool ok = __all_sync(0xffffffffu, wait_bar(kBarSFull + s, (i >> 1) & 1));
             if (!ok) {
                 aborted = true;
@@ -633,36 +708,41 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
             }
             umma::fence_after_sync();
             float y[kTok];
-            {
-                float a[32], c2[32];
-                umma::ld32(lane_base + kTmS + 64 * s, a);
-                umma::ld32(lane_base + kTmS + 64 * s + 32, c2);
-#pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    y[t] = a[t];
-                    y[32 + t] = c2[t];
-                }
-            }
+            tm_ld64(lane_base + kTmS + 64 * s, y);
             umma::fence_before_sync();
             mbar_arrive(&mbar[kBarSFree + s]);
             // scores (in units of 2^(e + 8) before fc), masked: a token counts if its page
             // is valid and its position is below the column's causal limit
-            const float4 *ta4 = reinterpret_cast<const float4 *>(tok_a + s * kTok);
-            const uint32_t ok0 = tok_ok[2 * s], ok1 = tok_ok[2 * s + 1];
+            const float4 *ta4 = reinterpret_cast<const float4 *>(tok_a + s3 * kTok);
+            const uint32_t ok0 = tok_ok[2 * s3], ok1 = tok_ok[2 * s3 + 1];
             const int rem = lim - (pg0 + i * ppt) * P;
-            float ymax = -INFINITY;
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (rem >= kTok && (ok0 & ok1) == 0xffffffffu) {  // the whole tile is visible
 #pragma unroll
-            for (int t4 = 0; t4 < kTok / 4; ++t4) {
-                const float4 a4 = ta4[t4];
-                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                for (int t4 = 0; t4 < kTok / 4; ++t4) {
+                    const float4 a4 = ta4[t4];
+                    y[4 * t4] *= a4.x;
+                    y[4 * t4 + 1] *= a4.y;
+                    y[4 * t4 + 2] *= a4.z;
+                    y[4 * t4 + 3] *= a4.w;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = 4 * t4 + e;
-                    const bool keep = ((t < 32 ? ok0 >> t : ok1 >> (t - 32)) & 1u) && t < rem;
-                    y[t] = keep ? y[t] * av[e] : -INFINITY;
-                    ymax = fmaxf(ymax, y[t]);
+                    for (int e = 0; e < 4; ++e) mx4[e] = fmaxf(mx4[e], y[4 * t4 + e]);
+                }
+            } else {
+#pragma unroll
+                for (int t4 = 0; t4 < kTok / 4; ++t4) {
+                    const float4 a4 = ta4[t4];
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int t = 4 * t4 + e;
+                        const bool keep = ((t < 32 ? ok0 >> t : ok1 >> (t - 32)) & 1u) && t < rem;
+                        y[t] = keep ? y[t] * av[e] : -INFINITY;
+                        mx4[e] = fmaxf(mx4[e], y[t]);
+                    }
                 }
             }
+            const float ymax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             const float m_tile = ymax * fc;  // log2 units (fc > 0)
             if (i >= 1) {
                 const bool ok2 = __all_sync(0xffffffffu, wait_bar(kBarPvDone, (i - 1) & 1));
