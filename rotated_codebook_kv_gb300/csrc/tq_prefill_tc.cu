@@ -23,14 +23,14 @@
 // by the rotation: fp16(lambda c[code]) * fp16(n / 16), the combine rotates the
 // merged output back).
 //
-// Warp roles (416 threads, one CTA per SM):
+// Warp roles (448 threads, one CTA per SM):
 //   warps 0-3   one thread per column (tensor-memory lane): query operands, online
 //               softmax with a lazy rescale of O (only when the running maximum grows
 //               by more than 2^8, so P <= 2^8 stays exact in fp16), P into tensor
 //               memory, the partial outputs at the end;
-//   warps 4-11  page copies (cp.async.bulk, two stages) and the decode of a tile
-//               into fp16 operand tiles (three stages);
-//   warp 12     tensor-memory allocation; lane 0 issues the MMAs.
+//   warps 4-11  the decode of a tile's pages into fp16 operand tiles (three stages);
+//   warp 12     tensor-memory allocation; lane 0 issues the MMAs;
+//   warp 13     page copies (cp.async.bulk, two stages), block ids read ahead.
 // Every wait is bounded by the codec's wait limit; a timeout sets
 // TQ_DEVERR_TIMEOUT, stops the CTA (its split then carries no weight), lets
 // copies and MMAs in flight finish, and frees tensor memory.
@@ -47,7 +47,8 @@ constexpr int D = 128;
 constexpr int kSoftWarps = 4;
 constexpr int kProdWarps = 8;
 constexpr int kMmaWarp = kSoftWarps + kProdWarps;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kLoadWarp = kMmaWarp + 1;
+constexpr int kThreads = (kLoadWarp + 1) * 32;
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kCols = 128;                 // columns per CTA (M of every MMA)
 constexpr int kTok = 64;                   // tokens per tile
@@ -75,18 +76,19 @@ constexpr uint32_t kTokOff = kVlutOff + 1024;          // [3][64] float: n_t sm_
 constexpr uint32_t kOkOff = kTokOff + 768;             // [3] uint64: tokens of a valid page
 constexpr uint32_t kPageOkOff = kOkOff + 32;           // [kRaw <= 3][4] int
 constexpr uint32_t kMbarOff = kPageOkOff + 48;
-constexpr int kNumMbar = 16;
+constexpr int kNumMbar = 18;
 constexpr uint32_t kMiscOff = kMbarOff + 8 * kNumMbar;  // tensor-memory base, abort flag
 constexpr uint32_t kRawOff = (kMiscOff + 16 + 127) / 128 * 128;
 // mbarrier indices
 constexpr int kBarRaw = 0;       // [kRaw <= 3] a page stage landed (ppt arrivals + bytes)
-constexpr int kBarOpFull = 3;    // [3] an operand stage is decoded (256 producer arrivals)
+constexpr int kBarOpFull = 3;    // [3] an operand stage is decoded (one arrival per producer warp)
 constexpr int kBarOpFree = 6;    // [3] the MMAs reading an operand stage are done (commit)
 constexpr int kBarSFull = 9;     // [2] scores of a tile are in tensor memory (commit)
-constexpr int kBarSFree = 11;    // [2] the softmax threads have read a score buffer (128 arrivals)
-constexpr int kBarPFull = 13;    // P of a tile is in tensor memory, O rescaled (128 arrivals)
+constexpr int kBarSFree = 11;    // [2] the softmax warps have read a score buffer (4 arrivals)
+constexpr int kBarPFull = 13;    // P of a tile is in tensor memory, O rescaled (4 arrivals)
 constexpr int kBarPvDone = 14;   // O += P V of a tile is done (commit)
 constexpr int kBarMmaDone = 15;  // teardown: every MMA issued is done (commit)
+constexpr int kBarRawFree = 16;  // [kRaw <= 2] the producer warps are done reading a page stage (8 arrivals)
 
 __host__ __device__ inline uint32_t raw_stage_bytes(const PageGeom &pg)
 {
@@ -100,6 +102,39 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) { return static_cas
 
 __device__ __forceinline__ void st128(unsigned char *p, uint4 v) { *reinterpret_cast<uint4 *>(p) = v; }
 
+// Shared-memory accesses by 32-bit shared address (explicit ld/st.shared: the decode
+// helpers get their stage addresses as integers, so no access falls back to a
+// generic load).  Volatile, so they stay in program order with the barrier waits.
+__device__ __forceinline__ uint32_t lds32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds8(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t half2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 bits_half2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
@@ -108,15 +143,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *mb)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(mb)) : "memory");
 }
 
-// OR of `pred` over the `nthreads` threads that meet at named barrier `id`.
-__device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred)
+// One arrival per warp: the warp's lanes meet first (their earlier shared-memory and
+// tensor-memory work ordered before lane 0's arrival), so a barrier counts warps
+// rather than threads and takes a few atomic updates per hand-off instead of hundreds.
+__device__ __forceinline__ void warp_arrive(uint64_t *mb)
 {
-    uint32_t r;
-    asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\nbar.red.or.pred p, %2, %3, q;\nselp.u32 %0, 1, 0, p;\n}\n"
-                 : "=r"(r)
-                 : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
-                 : "memory");
-    return r != 0;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(mb);
 }
 
 // 32 consecutive 32-bit columns of this thread's tensor-memory lane from registers.
@@ -177,11 +210,11 @@ __device__ __forceinline__ float fast_exp2(float x)
 }
 
 struct KeyItem {
-    const unsigned char *raw;  // page stage
-    const int *pok;            // page validity of the stage
+    uint32_t raw;              // shared address of the page stage
+    uint32_t pok;              // shared address of the stage's page validity flags (int)
     uint32_t page_bytes;
     int pshift, P, pt;         // pt: producer thread 0..255
-    int64_t sign_off, gamma_off;
+    uint32_t sign_off, gamma_off;
 };
 
 // The producer thread's 4 key items (token t, 8-coordinate chunk c): fp16 high and low
@@ -190,8 +223,7 @@ struct KeyItem {
 // map the 8 lanes of a store phase to the 8 rows of one core matrix.  All loads are
 // issued before any table lookup.
 template <int KB>
-__device__ __forceinline__ void decode_keys(const KeyItem &ki, const uint2 *lut, unsigned char *kh,
-                                            unsigned char *kl, unsigned char *ksg)
+__device__ __forceinline__ void decode_keys(const KeyItem &ki, uint32_t lut, uint32_t kh, uint32_t kl, uint32_t ksg)
 {
     constexpr bool QJL = KB <= 3;
     constexpr int CP = lut_copies(KB);
@@ -204,21 +236,21 @@ __device__ __forceinline__ void decode_keys(const KeyItem &ki, const uint2 *lut,
         const int it = ki.pt + kProdThreads * k;
         const int t = ((it >> 7) << 3) | (it & 7), c = (it >> 3) & 15;
         const int q = t >> ki.pshift, o = t & (ki.P - 1);
-        tv[k] = ki.pok[q] != 0;
-        const unsigned char *kp = ki.raw + q * ki.page_bytes;
-        const unsigned char *crow = kp + o * CODE_BYTES;
+        tv[k] = lds32(ki.pok + 4 * q) != 0;
+        const uint32_t kp = ki.raw + q * ki.page_bytes;
+        const uint32_t crow = kp + o * CODE_BYTES;
         if constexpr (KB == 4) {
-            w[k] = *reinterpret_cast<const uint32_t *>(crow + 4 * c);
+            w[k] = lds32(crow + 4 * c);
         } else if constexpr (KB == 2) {
-            w[k] = *reinterpret_cast<const uint16_t *>(crow + 2 * c);
+            w[k] = lds16(crow + 2 * c);
         } else {
             const int by = 3 * c;
-            const uint32_t *wp = reinterpret_cast<const uint32_t *>(crow + (by & ~3));
-            w[k] = __funnelshift_r(wp[0], wp[1], 8 * (by & 3));
+            const uint32_t wa = crow + (by & ~3);
+            w[k] = __funnelshift_r(lds32(wa), lds32(wa + 4), 8 * (by & 3));
         }
         if constexpr (QJL) {
-            sb[k] = kp[ki.sign_off + o * SIGN_BYTES + c];
-            g[k] = *reinterpret_cast<const uint16_t *>(kp + ki.gamma_off + 2 * o);
+            sb[k] = lds8(kp + ki.sign_off + o * SIGN_BYTES + c);
+            g[k] = lds16(kp + ki.gamma_off + 2 * o);
         }
         off[k] = umma::core_offset(t, 8 * c, D);
     }
@@ -226,13 +258,14 @@ __device__ __forceinline__ void decode_keys(const KeyItem &ki, const uint2 *lut,
     for (int k = 0; k < 4; ++k) {
         uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = hv;
         if (tv[k]) {
-            const uint2 e0 = lut[(w[k] & PM) * CP], e1 = lut[((w[k] >> (2 * KB)) & PM) * CP];
-            const uint2 e2 = lut[((w[k] >> (4 * KB)) & PM) * CP], e3 = lut[((w[k] >> (6 * KB)) & PM) * CP];
+            const uint2 e0 = lds64(lut + (w[k] & PM) * (8 * CP)), e1 = lds64(lut + ((w[k] >> (2 * KB)) & PM) * (8 * CP));
+            const uint2 e2 = lds64(lut + ((w[k] >> (4 * KB)) & PM) * (8 * CP));
+            const uint2 e3 = lds64(lut + ((w[k] >> (6 * KB)) & PM) * (8 * CP));
             hv = make_uint4(e0.x, e1.x, e2.x, e3.x);
             lv = make_uint4(e0.y, e1.y, e2.y, e3.y);
         }
-        st128(kh + off[k], hv);
-        st128(kl + off[k], lv);
+        sts128(kh + off[k], hv);
+        sts128(kl + off[k], lv);
         if constexpr (QJL) {
             uint4 sv = make_uint4(0u, 0u, 0u, 0u);
             if (tv[k]) {
@@ -242,14 +275,14 @@ __device__ __forceinline__ void decode_keys(const KeyItem &ki, const uint2 *lut,
                 auto sg = [&](int m) { return g2 | (((nb >> (2 * m)) & 1u) << 15) | (((nb >> (2 * m + 1)) & 1u) << 31); };
                 sv = make_uint4(sg(0), sg(1), sg(2), sg(3));
             }
-            st128(ksg + off[k], sv);
+            sts128(ksg + off[k], sv);
         }
     }
 }
 
 struct ValueItem {
-    const unsigned char *raw;  // page stage
-    const int *pok;            // page validity of the stage
+    uint32_t raw;              // shared address of the page stage
+    uint32_t pok;              // shared address of the stage's page validity flags (int)
     uint32_t page_bytes;
     int pos0, L, pshift, P, gshift;
     int j7, tc, jb;
@@ -260,8 +293,8 @@ struct ValueItem {
 // fp16(lambda c[code]) * fp16(n / 16); tokens of an invalid page or past the
 // sequence's end are zero (their records may hold any bit pattern).
 template <int VB>
-__device__ __forceinline__ void decode_values(const Codec &C, const PageGeom &PG, const ValueItem &it,
-                                              const uint32_t *vlut, unsigned char *vt)
+__device__ __forceinline__ void decode_values(const Codec &C, const PageGeom &PG, const ValueItem &it, uint32_t vlut,
+                                              uint32_t vt)
 {
     constexpr uint32_t M = (1u << VB) - 1u;
     uint32_t w[8][VB];  // the 32 coordinates' codes of each token: VB words
@@ -270,16 +303,16 @@ __device__ __forceinline__ void decode_values(const Codec &C, const PageGeom &PG
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
         const int t = 8 * it.tc + u, q = t >> it.pshift, o = t & (it.P - 1);
-        vv[u] = it.pok[q] != 0 && it.pos0 + t < it.L;
-        const unsigned char *vp = it.raw + q * it.page_bytes + PG.k_page;
-        const uint32_t *cw = reinterpret_cast<const uint32_t *>(vp + o * C.v_code_bytes + 4 * VB * it.jb);
+        vv[u] = lds32(it.pok + 4 * q) != 0 && it.pos0 + t < it.L;
+        const uint32_t vp = it.raw + q * it.page_bytes + static_cast<uint32_t>(PG.k_page);
+        const uint32_t cw = vp + o * C.v_code_bytes + 4 * VB * it.jb;
 #pragma unroll
-        for (int x = 0; x < VB; ++x) w[u][x] = cw[x];
+        for (int x = 0; x < VB; ++x) w[u][x] = lds32(cw + 4 * x);
         if (C.vmse)
-            meta[u] = *reinterpret_cast<const uint16_t *>(vp + PG.v_meta_off + 2 * o);
+            meta[u] = lds16(vp + static_cast<uint32_t>(PG.v_meta_off) + 2 * o);
         else
-            meta[u] = *reinterpret_cast<const uint32_t *>(vp + PG.v_meta_off + o * C.v_meta_bytes +
-                                                          4 * ((32 * it.jb) >> it.gshift));
+            meta[u] = lds32(vp + static_cast<uint32_t>(PG.v_meta_off) + o * C.v_meta_bytes +
+                            4 * ((32 * it.jb) >> it.gshift));
     }
     uint32_t row[4][4];  // [k][token pair]
 #pragma unroll
@@ -311,7 +344,7 @@ __device__ __forceinline__ void decode_values(const Codec &C, const PageGeom &PG
             const uint32_t c0 = code(u0), c1 = code(u1);
             uint32_t v;
             if (C.vmse) {
-                v = half2_bits(__hmul2(bits_half2(vlut[c0 | (c1 << VB)]), sc2));
+                v = half2_bits(__hmul2(bits_half2(lds32(vlut + 4 * (c0 | (c1 << VB)))), sc2));
             } else {
                 const uint32_t x = c0 | (c1 << 16) | 0x64006400u;  // (1024 + c0, 1024 + c1) in fp16
                 const __half2 cf = __hsub2(bits_half2(x), bits_half2(0x64006400u));
@@ -323,7 +356,7 @@ __device__ __forceinline__ void decode_values(const Codec &C, const PageGeom &PG
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int j = 32 * it.jb + 8 * k + it.j7;
-        st128(vt + umma::core_offset(j, 8 * it.tc, kTok), make_uint4(row[k][0], row[k][1], row[k][2], row[k][3]));
+        sts128(vt + umma::core_offset(j, 8 * it.tc, kTok), make_uint4(row[k][0], row[k][1], row[k][2], row[k][3]));
     }
 }
 
@@ -401,16 +434,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
         }
     }
     if (tid == 0) {
-        for (int i = 0; i < kRaw; ++i) umma::mbar_init(&mbar[kBarRaw + i], ppt);
+        for (int i = 0; i < kRaw; ++i) {
+            umma::mbar_init(&mbar[kBarRaw + i], ppt);
+            umma::mbar_init(&mbar[kBarRawFree + i], kProdWarps);
+        }
         for (int i = 0; i < kOps; ++i) {
-            umma::mbar_init(&mbar[kBarOpFull + i], kProdThreads);
+            umma::mbar_init(&mbar[kBarOpFull + i], kProdWarps);
             umma::mbar_init(&mbar[kBarOpFree + i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             umma::mbar_init(&mbar[kBarSFull + i], 1);
-            umma::mbar_init(&mbar[kBarSFree + i], kSoftWarps * 32);
+            umma::mbar_init(&mbar[kBarSFree + i], kSoftWarps);
         }
-        umma::mbar_init(&mbar[kBarPFull], kSoftWarps * 32);
+        umma::mbar_init(&mbar[kBarPFull], kSoftWarps);
         umma::mbar_init(&mbar[kBarPvDone], 1);
         umma::mbar_init(&mbar[kBarMmaDone], 1);
         *abort_flag = 0;
@@ -442,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
         return false;
     };
 
-    // page copies of tile i into stage i % kRaw, by lanes q < ppt of the first producer warp
+    // page copies of tile i into stage i % kRaw, by lanes q < ppt of the loader warp
     // block id of this lane's page of tile i (-1 past the split); read a tile ahead of its
     // issue so that the global load's latency is not paid on the producers' path
     auto fetch_blk = [&](int i) -> int {
@@ -535,10 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
         }
         umma::wait_st();
         umma::fence_before_sync();
-    } else if (warp == kSoftWarps && lane < ppt) {
-        for (int i = 0; i < kRaw && i < ntiles; ++i) issue(i, fetch_blk(i));
     }
-    __syncthreads();  // query operands in tensor memory; the first page copies are on their way
+    __syncthreads();  // query operands in tensor memory
     umma::fence_after_sync();
 
     bool aborted = false;
@@ -546,33 +580,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
         // ================= producers: page copies and operand decode =================
         const int pt = tid - kSoftWarps * 32;
         const float afac = A.sm_scale * rsqrtf(static_cast<float>(D)) * kLog2e;
-        const uint2 *lut = reinterpret_cast<const uint2 *>(smem + kLutOff) + (lane & (lut_copies(kb) - 1));
-        const uint32_t *vlut = reinterpret_cast<const uint32_t *>(smem + kVlutOff);
-        int issued = min(kRaw, ntiles);
-        int bnext = (warp == kSoftWarps && lane < ppt) ? fetch_blk(kRaw) : -1;  // the next tile to issue
-        int i = 0;
-        for (; i < ntiles; ++i) {
+        const uint32_t sbase = smem_addr(smem);
+        const uint32_t lut = sbase + kLutOff + 8 * (lane & (lut_copies(kb) - 1));  // this lane's table copy
+        const uint32_t vlut = sbase + kVlutOff;
+        for (int i = 0; i < ntiles; ++i) {
             const int r = i % kRaw, s = i % kOps;
             bool ok = wait_bar(kBarRaw + r, (i / kRaw) & 1);
             if (ok && i >= kOps) ok = wait_bar(kBarOpFree + s, ((i - kOps) / kOps) & 1);
-            // every producer is past tile i - 1: its page stage may be refilled
-            const bool fail = bar_or(1, kProdThreads, !ok);
-            if (fail) {
+            if (!__all_sync(0xffffffffu, ok)) {  // the lanes poll separately: decide as a warp
                 aborted = true;
                 break;
             }
-            if (i >= 1 && warp == kSoftWarps && lane < ppt) {
-                if (i + kRaw - 1 < ntiles) issue(i + kRaw - 1, bnext);
-                bnext = fetch_blk(i + kRaw);
-            }
-            if (i >= 1) issued = max(issued, min(i + kRaw, ntiles));
 
             const unsigned char *raw = smem + kRawOff + r * raw_bytes;
             const int *pok = page_ok + r * 4;
-            unsigned char *kh = smem + s * kOpBytes;
-            unsigned char *kl = kh + kTileBytes;
-            unsigned char *ksg = kl + kTileBytes;
-            unsigned char *vt = ksg + kTileBytes;
+            const uint32_t raw_s = sbase + kRawOff + r * raw_bytes;
+            const uint32_t pok_s = sbase + kPageOkOff + 16 * r;
+            const uint32_t kh = sbase + s * kOpBytes;
+            const uint32_t kl = kh + kTileBytes;
+            const uint32_t ksg = kl + kTileBytes;
+            const uint32_t vt = ksg + kTileBytes;
             const int pos0 = (pg0 + i * ppt) * P;  // sequence position of the tile's token 0
 
             // ---- token factors and the valid-page mask (tokens 0..63: warps 4 and 5) ----
@@ -588,7 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
             // ---- keys: item (token t, 8-coordinate chunk c); the 8 lanes of a store phase
             // write the 8 rows of one core matrix ----
             {
-                const KeyItem ki{raw, pok, page_bytes, pshift, P, pt, PG.k_sign_off, PG.k_gamma_off};
+                const KeyItem ki{raw_s, pok_s, page_bytes, pshift, P, pt, static_cast<uint32_t>(PG.k_sign_off),
+                                 static_cast<uint32_t>(PG.k_gamma_off)};
                 if (kb == 2) decode_keys<2>(ki, lut, kh, kl, ksg);
                 else if (kb == 3) decode_keys<3>(ki, lut, kh, kl, ksg);
                 else decode_keys<4>(ki, lut, kh, kl, ksg);
@@ -598,17 +626,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
             // row (8 tokens of one coordinate) per k; the 8 lanes of a store phase (j7 = 0..7)
             // write the 8 rows of one core matrix ----
             {
-                const ValueItem vi{raw, pok, page_bytes, pos0, L, pshift, P, gshift, pt & 7, (pt >> 3) & 7, pt >> 6};
+                const ValueItem vi{raw_s, pok_s, page_bytes, pos0, L, pshift, P, gshift, pt & 7, (pt >> 3) & 7, pt >> 6};
                 if (vb == 2) decode_values<2>(C, PG, vi, vlut, vt);
                 else if (vb == 3) decode_values<3>(C, PG, vi, vlut, vt);
                 else decode_values<4>(C, PG, vi, vlut, vt);
             }
             umma::fence_proxy_async();
-            mbar_arrive(&mbar[kBarOpFull + s]);
+            warp_arrive(&mbar[kBarRawFree + r]);  // the page stage may be refilled
+            warp_arrive(&mbar[kBarOpFull + s]);
         }
-        // ---- teardown: copies still in flight must land before the CTA exits ----
-        if (aborted && warp == kSoftWarps && lane < ppt) {
-            for (int t = i; t < issued; ++t) {
+    } else if (warp == kLoadWarp) {
+        // ================= page copies: lanes q < ppt, a stage refilled as soon as the
+        // producers are done with it; block ids read before the wait =================
+        int issued = 0;
+        for (int i = 0; i < ntiles; ++i) {
+            const int r = i % kRaw;
+            const int blk = (lane < ppt) ? fetch_blk(i) : -1;
+            bool ok = true;
+            if (i >= kRaw) ok = __all_sync(0xffffffffu, wait_bar(kBarRawFree + r, ((i - kRaw) / kRaw) & 1));
+            if (!ok) {
+                aborted = true;
+                break;
+            }
+            if (lane < ppt) issue(i, blk);
+            issued = i + 1;
+        }
+        // copies still in flight must land before the CTA exits: the last issue of each stage
+        if (aborted && lane < ppt) {
+            for (int t = max(0, issued - kRaw); t < issued; ++t) {
                 const long long t0 = clock64();
                 while (!umma::mbar_try_wait(&mbar[kBarRaw + t % kRaw], (t / kRaw) & 1) && clock64() - t0 < kDrainLimit) {
                 }
@@ -710,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
             float y[kTok];
             tm_ld64(lane_base + kTmS + 64 * s, y);
             umma::fence_before_sync();
-            mbar_arrive(&mbar[kBarSFree + s]);
+            warp_arrive(&mbar[kBarSFree + s]);
             // scores (in units of 2^(e + 8) before fc), masked: a token counts if its page
             // is valid and its position is below the column's causal limit
             const float4 *ta4 = reinterpret_cast<const float4 *>(tok_a + s3 * kTok);
@@ -793,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
             tm_st32(lane_base + kTmP, pp);
             umma::wait_st();
             umma::fence_before_sync();
-            mbar_arrive(&mbar[kBarPFull]);
+            warp_arrive(&mbar[kBarPFull]);
         }
         if (!aborted) {
             const bool ok = __all_sync(0xffffffffu, wait_bar(kBarPvDone, (ntiles - 1) & 1));
