@@ -58,9 +58,10 @@ namespace {
 // kQRows query rows per block of 2 D threads: thread (i, half) sums coordinate i
 // of each row over half of the inner index, so every element of Pi (and S)
 // read from L2 feeds kQRows independent FMA chains; the halves add in shared memory.
-constexpr int kQRows = 4;
-
-template <int D>
+// Decode (a few rows per kv head) takes 4 rows per block for parallelism; prefill
+// (thousands of rows) takes 32 (16 at head_dim 256) so that Pi and S are read from
+// L2 once per 32 rows instead of once per 4.
+template <int D, int kQRows>
 __global__ void __launch_bounds__(2 * D) qrot_kernel(const Codec C, const uint16_t *__restrict__ q, float *qrot,
                                                      float *qs, int rows)
 {
@@ -96,8 +97,11 @@ __global__ void __launch_bounds__(2 * D) qrot_kernel(const Codec C, const uint16
     };
     float a[kQRows];
     matvec(C.PiT, a);
-    if (hf == 0)
-        for (int r = 0; r < nr; ++r) qrot[static_cast<int64_t>(r0 + r) * D + i] = a[r];
+    if (hf == 0) {
+#pragma unroll
+        for (int r = 0; r < kQRows; ++r)
+            if (r < nr) qrot[static_cast<int64_t>(r0 + r) * D + i] = a[r];
+    }
     if (!C.qjl) return;
     __syncthreads();  // every thread has read sq and part
     if (hf == 0) {
@@ -106,8 +110,11 @@ __global__ void __launch_bounds__(2 * D) qrot_kernel(const Codec C, const uint16
     }
     __syncthreads();
     matvec(C.ST, a);
-    if (hf == 0)
-        for (int r = 0; r < nr; ++r) qs[static_cast<int64_t>(r0 + r) * D + i] = a[r];
+    if (hf == 0) {
+#pragma unroll
+        for (int r = 0; r < kQRows; ++r)
+            if (r < nr) qs[static_cast<int64_t>(r0 + r) * D + i] = a[r];
+    }
 }
 
 // ---- (2) split-K decode: see tq_decode_mma.cuh ---------------------------------
@@ -218,7 +225,11 @@ template <int D>
 cudaError_t launch_decode_d(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st)
 {
     const int qrows = a.B * a.Tq * a.Hq;
-    qrot_kernel<D><<<(qrows + kQRows - 1) / kQRows, 2 * D, 0, st>>>(c, a.q, a.ws.qrot, a.ws.qs, qrows);
+    constexpr int kBig = (D == 128) ? 32 : 16;
+    if (qrows >= 64 * kBig)
+        qrot_kernel<D, kBig><<<(qrows + kBig - 1) / kBig, 2 * D, 0, st>>>(c, a.q, a.ws.qrot, a.ws.qs, qrows);
+    else
+        qrot_kernel<D, 4><<<(qrows + 3) / 4, 2 * D, 0, st>>>(c, a.q, a.ws.qrot, a.ws.qs, qrows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     switch (c.k_bits) {
