@@ -144,6 +144,7 @@ tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t s
     const size_t img_bytes = (d == 128) ? 4 * dd * sizeof(uint16_t) : 0;
     const size_t nf = 6 * dd + static_cast<size_t>(d);  // six d x d tables, then the Hadamard signs
     std::vector<float> host(nf);
+    std::vector<double> Md(dd);  // M = S Pi in double
     for (int j = 0; j < d; ++j) host[6 * dd + j] = static_cast<float>(ht.hsign[j]);
     for (int i = 0; i < d; ++i)
         for (int j = 0; j < d; ++j) {
@@ -154,6 +155,7 @@ tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t s
             host[3 * dd + t] = static_cast<float>(ht.S[a]);
             double m = 0.0;
             for (int q = 0; q < d; ++q) m += ht.S[static_cast<size_t>(i) * d + q] * ht.Pi[static_cast<size_t>(q) * d + j];
+            Md[a] = m;
             const float mh = static_cast<float>(m);
             host[4 * dd + a] = mh;
             host[5 * dd + a] = static_cast<float>(m - static_cast<double>(mh));
@@ -175,19 +177,22 @@ tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t s
                 put(1, i, j, ht.S[static_cast<size_t>(i) * d + j] * 4096.0);
             }
     }
-    // Pi 2^10 as fp16 high / low parts in the fragment order of mma.sync m16n8k16's B
-    // operand (B[k][n] = Pi[n][k]): for n-tile nt, k-step ks and lane (r, q) the
-    // pairs (k0, k0 + 1) and (k0 + 8, k0 + 9) of row n = 8 nt + r, k0 = 16 ks + 2 q
-    const size_t frag_words = static_cast<size_t>(d / 8) * (d / 16) * 32 * 4;
+    // Pi 2^10 (and M 2^10 after it, M = S Pi) as fp16 high / low parts in the fragment
+    // order of mma.sync m16n8k16's B operand (B[k][n] = W[n][k]): for n-tile nt, k-step
+    // ks and lane (r, q) the pairs (k0, k0 + 1) and (k0 + 8, k0 + 9) of row n = 8 nt + r,
+    // k0 = 16 ks + 2 q
+    const size_t frag_one = static_cast<size_t>(d / 8) * (d / 16) * 32 * 4;
+    const size_t frag_words = 2 * frag_one;
     std::vector<uint32_t> frag(frag_words);
-    {
+    for (int mat = 0; mat < 2; ++mat) {
+        const double *W = mat ? Md.data() : ht.Pi.data();
         auto hl = [&](int n, int kk, uint16_t *hi, uint16_t *lo) {
-            const double x = ht.Pi[static_cast<size_t>(n) * d + kk] * 1024.0;
+            const double x = W[static_cast<size_t>(n) * d + kk] * 1024.0;
             const __half h = __float2half_rn(static_cast<float>(x));
             *hi = __half_as_ushort(h);
             *lo = __half_as_ushort(__float2half_rn(static_cast<float>(x - static_cast<double>(__half2float(h)))));
         };
-        size_t w = 0;
+        size_t w = mat * frag_one;
         for (int nt = 0; nt < d / 8; ++nt)
             for (int ks = 0; ks < d / 16; ++ks)
                 for (int lane = 0; lane < 32; ++lane) {
@@ -261,6 +266,7 @@ tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t s
     k.tc_image = img_bytes ? img_dev : nullptr;
     k.hsign = base + 6 * dd;
     k.pi_frag = reinterpret_cast<const uint4 *>(frag_dev);
+    k.m_frag = reinterpret_cast<const uint4 *>(frag_dev) + frag_one / 4;
     k.rotation = rotation;
     k.status = status;
     k.wait_limit = tq::kDefaultWaitLimit;

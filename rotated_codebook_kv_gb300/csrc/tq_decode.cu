@@ -58,9 +58,6 @@ namespace {
 // kQRows query rows per block of 2 D threads: thread (i, half) sums coordinate i
 // of each row over half of the inner index, so every element of Pi (and S)
 // read from L2 feeds kQRows independent FMA chains; the halves add in shared memory.
-// Decode (a few rows per kv head) takes 4 rows per block for parallelism; prefill
-// (thousands of rows) takes 32 (16 at head_dim 256) so that Pi and S are read from
-// L2 once per 32 rows instead of once per 4.
 template <int D, int kQRows>
 __global__ void __launch_bounds__(2 * D) qrot_kernel(const Codec C, const uint16_t *__restrict__ q, float *qrot,
                                                      float *qs, int rows)
@@ -114,6 +111,98 @@ __global__ void __launch_bounds__(2 * D) qrot_kernel(const Codec C, const uint16
 #pragma unroll
         for (int r = 0; r < kQRows; ++r)
             if (r < nr) qs[static_cast<int64_t>(r0 + r) * D + i] = a[r];
+    }
+}
+
+// Query pre-rotation for many rows (prefill) on the tensor cores: q_rot = Pi q and
+// q_s = M q with M = S Pi (equal to S q_rot), by mma.sync m16n8k16 from the bf16
+// query made exact in fp16 by a power-of-two row scale, times Pi 2^10 and M 2^10 as
+// fp16 high + low fragment images read from L2 (products exact, fp32 accumulation,
+// ~22 significant bits).  64 rows per CTA of 8 warps; warp w computes the output
+// columns [D/8 w, D/8 (w + 1)) of all 64 rows.
+constexpr int kQmRows = 64;
+
+__device__ __forceinline__ void qm_mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                       uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) qrot_mma_kernel(const Codec C, const uint16_t *__restrict__ q, float *qrot,
+                                                       float *qs, int rows)
+{
+    constexpr int TM = kQmRows, KA = D + 8, KS = D / 16, NPW = D / 64, E = D / 32;
+    __shared__ __align__(16) __half qa[TM * KA];
+    __shared__ float rsc[TM];  // 2^-(10 + row exponent): back to Pi q
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = blockIdx.x * TM;
+    for (int row = warp; row < TM; row += 8) {
+        const int r = r0 + row;
+        float x[E];
+        float mx = 0.f;
+#pragma unroll
+        for (int m = 0; m < E; ++m) {
+            x[m] = (r < rows) ? bf16_to_float(q[static_cast<int64_t>(r) * D + lane + 32 * m]) : 0.f;
+            mx = fmaxf(mx, fabsf(x[m]));
+        }
+        mx = warp_max(mx);
+        // mx < 2^ex; the row times 2^(15 - ex) has its largest element in [2^14, 2^15)
+        int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 126;
+        if (ex < -100) ex = -100;
+        const bool ok = mx > 0.f && mx <= 3.0e38f;
+        const float sc = ok ? __uint_as_float(static_cast<uint32_t>(15 - ex + 127) << 23) : 0.f;
+#pragma unroll
+        for (int m = 0; m < E; ++m) qa[row * KA + lane + 32 * m] = __float2half_rn(x[m] * sc);
+        if (lane == 0) rsc[row] = ok ? __uint_as_float(static_cast<uint32_t>(127 - 25 + ex) << 23) : 0.f;
+    }
+    __syncthreads();
+    const int rr = lane >> 2, qq = lane & 3;
+    const uint32_t qab = static_cast<uint32_t>(__cvta_generic_to_shared(qa));
+    for (int mat = 0; mat < (C.qjl ? 2 : 1); ++mat) {
+        const uint4 *__restrict__ frag = mat ? C.m_frag : C.pi_frag;
+        float *out = mat ? qs : qrot;
+        float acc[TM / 16][NPW][4];
+#pragma unroll
+        for (int m = 0; m < TM / 16; ++m)
+#pragma unroll
+            for (int n = 0; n < NPW; ++n) acc[m][n][0] = acc[m][n][1] = acc[m][n][2] = acc[m][n][3] = 0.f;
+#pragma unroll 2
+        for (int s = 0; s < KS; ++s) {
+            uint4 bf[NPW];
+#pragma unroll
+            for (int n = 0; n < NPW; ++n) bf[n] = __ldg(frag + ((warp * NPW + n) * KS + s) * 32 + lane);
+#pragma unroll
+            for (int m = 0; m < TM / 16; ++m) {
+                uint32_t a0, a1, a2, a3;
+                const uint32_t addr = qab + 2u * ((16 * m + (lane & 15)) * KA + 16 * s + 8 * (lane >> 4));
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(addr));
+#pragma unroll
+                for (int n = 0; n < NPW; ++n) {
+                    qm_mma(acc[m][n], a0, a1, a2, a3, bf[n].z, bf[n].w);  // low parts first
+                    qm_mma(acc[m][n], a0, a1, a2, a3, bf[n].x, bf[n].y);
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < TM / 16; ++m) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = 16 * m + rr + 8 * h;
+                if (r0 + row >= rows) continue;
+                const float f = rsc[row];
+#pragma unroll
+                for (int n = 0; n < NPW; ++n) {
+                    const int col = 8 * (warp * NPW + n) + 2 * qq;
+                    *reinterpret_cast<float2 *>(out + static_cast<int64_t>(r0 + row) * D + col) =
+                        make_float2(acc[m][n][2 * h] * f, acc[m][n][2 * h + 1] * f);
+                }
+            }
+        }
     }
 }
 
@@ -195,6 +284,25 @@ __global__ void __launch_bounds__(D) combine_kernel(const Codec C, const DecodeA
     A.out[static_cast<size_t>(row) * D + j] = float_to_bf16_bits(o);
 }
 
+// One split and no un-rotation: o = acc / l per row (what combine_kernel computes
+// when there is one split), four coordinates per thread.
+template <int D>
+__global__ void __launch_bounds__(256) combine1_kernel(const DecodeArgs A)
+{
+    const int64_t rows = static_cast<int64_t>(A.B) * A.Hq;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;  // float4 index
+    if (idx >= rows * (D / 4)) return;
+    const int64_t row = idx / (D / 4);
+    const float2 ml = *reinterpret_cast<const float2 *>(A.ws.ml + row * 2);
+    const float4 a = reinterpret_cast<const float4 *>(A.ws.acc)[idx];
+    const bool live = ml.y > 0.f;
+    const float4 o = live ? make_float4(a.x / ml.y, a.y / ml.y, a.z / ml.y, a.w / ml.y) : make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4 *>(A.ws.out32)[idx] = o;
+    const uint32_t lo = float_to_bf16_bits(o.x) | (static_cast<uint32_t>(float_to_bf16_bits(o.y)) << 16);
+    const uint32_t hi = float_to_bf16_bits(o.z) | (static_cast<uint32_t>(float_to_bf16_bits(o.w)) << 16);
+    reinterpret_cast<uint2 *>(A.out)[idx] = make_uint2(lo, hi);
+}
+
 template <int D, int KB, int VB>
 cudaError_t launch_dmma(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st)
 {
@@ -225,9 +333,9 @@ template <int D>
 cudaError_t launch_decode_d(const Codec &c, const PageGeom &pg, const DecodeArgs &a, cudaStream_t st)
 {
     const int qrows = a.B * a.Tq * a.Hq;
-    constexpr int kBig = (D == 128) ? 32 : 16;
-    if (qrows >= 64 * kBig)
-        qrot_kernel<D, kBig><<<(qrows + kBig - 1) / kBig, 2 * D, 0, st>>>(c, a.q, a.ws.qrot, a.ws.qs, qrows);
+    // thousands of rows (prefill): tensor cores; a few rows per kv head (decode): fp32
+    if (qrows >= 32 * kQmRows)
+        qrot_mma_kernel<D><<<(qrows + kQmRows - 1) / kQmRows, 256, 0, st>>>(c, a.q, a.ws.qrot, a.ws.qs, qrows);
     else
         qrot_kernel<D, 4><<<(qrows + 3) / 4, 2 * D, 0, st>>>(c, a.q, a.ws.qrot, a.ws.qs, qrows);
     cudaError_t e = cudaGetLastError();
@@ -248,6 +356,13 @@ cudaError_t launch_decode_d(const Codec &c, const PageGeom &pg, const DecodeArgs
 
 cudaError_t launch_combine(const Codec &c, const DecodeArgs &a, cudaStream_t st, bool unrotate)
 {
+    if (a.splits == 1 && !unrotate) {
+        const int64_t n4 = static_cast<int64_t>(a.B) * a.Hq * (c.d / 4);
+        const unsigned blocks = static_cast<unsigned>((n4 + 255) / 256);
+        if (c.d == 128) combine1_kernel<128><<<blocks, 256, 0, st>>>(a);
+        else combine1_kernel<256><<<blocks, 256, 0, st>>>(a);
+        return cudaGetLastError();
+    }
     if (c.d == 128) {
         if (unrotate) combine_kernel<128, true><<<a.B * a.Hq, 128, 0, st>>>(c, a);
         else combine_kernel<128, false><<<a.B * a.Hq, 128, 0, st>>>(c, a);
