@@ -183,15 +183,15 @@ template <int D>
 __device__ __forceinline__ void stage_fp16_row(const float *kf, __half *ka, int row, float mx, float *ysc)
 {
     const int lane = threadIdx.x & 31;
-    int ex = 0;
+    // mx = f 2^ex with f in [0.5, 1): ex from the exponent field (mx is normal here)
     const bool ok = mx >= 0x1p-30f && mx <= 0x1p30f;
-    if (ok) frexpf(mx, &ex);
-    const float sc = ok ? ldexpf(1.f, 15 - ex) : 0.f;
+    const int ex = ok ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 126 : 0;
+    const float sc = ok ? __uint_as_float(static_cast<uint32_t>(127 + 15 - ex) << 23) : 0.f;
     for (int j = 2 * lane; j < D; j += 64) {
         const float2 x = *reinterpret_cast<const float2 *>(kf + row * D + j);
         *reinterpret_cast<__half2 *>(ka + row * (D + 8) + j) = __floats2half2_rn(x.x * sc, x.y * sc);
     }
-    if (lane == 0) ysc[row] = ok ? ldexpf(1.f, ex - 25) : 0.f;
+    if (lane == 0) ysc[row] = ok ? __uint_as_float(static_cast<uint32_t>(127 + ex - 25) << 23) : 0.f;
 }
 
 // Dense rotation of TM rows on the tensor cores (mma.sync m16n8k16, fp16 in,
@@ -459,6 +459,46 @@ __device__ __noinline__ bool refine_marked_codes(const float *__restrict__ Pi, c
     return changed;
 }
 
+// Codes by a table of 64 bins on u = z / 8 + 1/2 (z in [-4, 4]; outside it the end
+// bins, which hold no threshold), each bin widened by 1/64 on both sides so that a
+// threshold within the guard band of any z of the bin is the bin's own.  Entry
+// [bin][copy] = {that threshold or +inf, 2^23 + number of thresholds below the
+// widened bin}, in kBinCopies copies (lane l reads copy l % kBinCopies).  A bin that
+// would hold two thresholds makes the build report failure (the codes then take the
+// binary search); the Lloyd-Max thresholds are >= 0.25 apart, wider than a bin.
+constexpr int kBinCopies = 8;
+constexpr float kBinScale = 8064.f;  // 63 bins * 128: round(u * 8064) / 128 is the bin
+
+__device__ __forceinline__ bool build_code_bins(float2 *bins, const float *thr, int nthr)
+{
+    bool bad = false;
+    for (int e = threadIdx.x; e < 64 * kBinCopies; e += blockDim.x) {
+        const float b = static_cast<float>(e / kBinCopies);
+        const float lo = 8.f * (128.f * b - 0.5f) / kBinScale - 4.f - 1.f / 64.f;
+        const float hi = 8.f * (128.f * b + 127.5f) / kBinScale - 4.f + 1.f / 64.f;
+        int below = 0, idx = -1, hits = 0;
+        for (int t = 0; t < nthr; ++t) {
+            const float th = thr[t];
+            if (th < lo) ++below;
+            else if (th <= hi) { idx = t; ++hits; }
+        }
+        bins[e] = make_float2(idx >= 0 ? thr[idx] : INFINITY, __uint_as_float(0x4B000000u + below));
+        bad |= hits > 1;
+    }
+    return bad;
+}
+
+// code = number of thresholds <= z; near: a threshold lies within kCodeGuard of z
+__device__ __forceinline__ int bin_code(float z, const unsigned char *binb, bool &near)
+{
+    const float u = __saturatef(fmaf(z, 0.125f, 0.5f));
+    const uint32_t a = (__float_as_uint(fmaf(u, kBinScale, kRoundMagic)) & 0x1F80u) >> 1;  // bin * 64 bytes
+    const float2 e = *reinterpret_cast<const float2 *>(binb + a);
+    const float dz = z - e.x;
+    near = fabsf(dz) < kCodeGuard;
+    return static_cast<int>(__float_as_uint(e.y) - 0x4B000000u) + (dz >= 0.f ? 1 : 0);
+}
+
 template <int D, bool HAD, bool VMSE>
 __global__ void __launch_bounds__(kThreads, 2)
 compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
@@ -483,6 +523,8 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     __shared__ uint16_t s_n16[TM], s_g16[TM];
     __shared__ float s_thr[18];   // -inf, thresholds ascending, +inf (codes by binary search)
     __shared__ float s_cent[16];
+    __shared__ __align__(16) float2 s_bins[64 * kBinCopies];
+    __shared__ int64_t s_tok[TM];  // token of each row
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * TM;
@@ -497,6 +539,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         int off = 0;
         if (r < rows) {
             const int64_t t = r / Hkv;
+            s_tok[tid] = t;
             const int h = static_cast<int>(r - t * Hkv);
             const int64_t s = slots[t];
             if (s >= 0) {
@@ -512,13 +555,16 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         s_dst[tid] = dst;
         s_off[tid] = off;
     }
+    // the key codebook's bin table; the barrier also publishes the rows' tokens
+    const unsigned char *binb = reinterpret_cast<const unsigned char *>(s_bins) + 8 * (lane % kBinCopies);
+    bool binbad = __syncthreads_or(build_code_bins(s_bins, C.thresholds, nthr));
     // ---- load key rows (bf16 -> fp32, exact) ---------------------------------
     for (int e = tid; e < TM * (D / 8); e += kThreads) {
         const int row = e / (D / 8), c8 = e - row * (D / 8);
         const int64_t r = r0 + row;
         uint4 u = make_uint4(0, 0, 0, 0);
         if (r < rows) {
-            const int64_t t = r / Hkv;
+            const int64_t t = s_tok[row];
             const int h = static_cast<int>(r - t * Hkv);
             u = __ldg(reinterpret_cast<const uint4 *>(kin + t * ks + static_cast<int64_t>(h) * D) + c8);
         }
@@ -569,14 +615,20 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         const int row = e / D, i = e - row * D;
         const int fl = s_flag[row];
         const float z = yb[e] * s_scale[row];
-        int code = 0;
-        for (int step = 1 << (kb - 1); step > 0; step >>= 1)
-            if (s_thr[code + step] <= z) code += step;
-        const float dmin = fminf(z - s_thr[code], s_thr[code + 1] - z);
+        bool near;
+        int code;
+        if (!binbad) {
+            code = bin_code(z, binb, near);
+        } else {
+            code = 0;
+            for (int step = 1 << (kb - 1); step > 0; step >>= 1)
+                if (s_thr[code + step] <= z) code += step;
+            near = fminf(z - s_thr[code], s_thr[code + 1] - z) < kCodeGuard;
+        }
         if (fl == 2) code = 0;
         // a code inside the guard band of a threshold is marked (0x80) and its row
         // flagged 3: the exact pass re-decides just the marked codes
-        const bool mark = (fl == 0 || fl == 3) && dmin < kCodeGuard;
+        const bool mark = (fl == 0 || fl == 3) && near;
         codes[row * CS + i] = static_cast<uint8_t>(code | (mark ? 0x80 : 0));
         yb[e] = (fl == 2) ? 0.f : z - s_cent[code];
         if (mark) s_flag[row] = 3;
@@ -736,12 +788,13 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         __syncthreads();  // the key pass is done with kf, yb and codes
         if (tid < 18) s_thr[tid] = tid == 0 ? -INFINITY : (tid <= (1 << C.v_bits) - 1 ? C.vthresholds[tid - 1] : INFINITY);
         if (tid < 16) s_cent[tid] = C.vcentroids[tid];
+        binbad = __syncthreads_or(build_code_bins(s_bins, C.vthresholds, (1 << C.v_bits) - 1));
         for (int e = tid; e < TM * (D / 8); e += kThreads) {
             const int row = e / (D / 8), c8 = e - row * (D / 8);
             const int64_t r = r0 + row;
             uint4 u = make_uint4(0, 0, 0, 0);
             if (r < rows) {
-                const int64_t t = r / Hkv;
+                const int64_t t = s_tok[row];
                 const int h = static_cast<int>(r - t * Hkv);
                 u = __ldg(reinterpret_cast<const uint4 *>(vin + t * vs + static_cast<int64_t>(h) * D) + c8);
             }
@@ -785,11 +838,17 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             const int row = e / D, i = e - row * D;
             const int fl = s_flag[row];
             const float z = yb[e] * s_scale[row];
-            int code = 0;
-            for (int step = 1 << (vb - 1); step > 0; step >>= 1)
-                if (s_thr[code + step] <= z) code += step;
-            const float dmin = fminf(z - s_thr[code], s_thr[code + 1] - z);
-            const bool mark = (fl == 0 || fl == 3) && dmin < kCodeGuard;
+            bool near;
+            int code;
+            if (!binbad) {
+                code = bin_code(z, binb, near);
+            } else {
+                code = 0;
+                for (int step = 1 << (vb - 1); step > 0; step >>= 1)
+                    if (s_thr[code + step] <= z) code += step;
+                near = fminf(z - s_thr[code], s_thr[code + 1] - z) < kCodeGuard;
+            }
+            const bool mark = (fl == 0 || fl == 3) && near;
             codes[row * CS + i] = static_cast<uint8_t>((fl == 2 ? 0 : code) | (mark ? 0x80 : 0));
             if (mark) s_flag[row] = 3;
         }
