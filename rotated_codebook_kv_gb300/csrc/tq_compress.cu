@@ -44,40 +44,6 @@ struct CompressSmem {
     static constexpr size_t kBytes = kKf + kYb + kCodes + kScratch + kKa;
 };
 
-// acc[rr] += sum_j W[j][i] * X[row(rr)][j] for i = tid % D, rows interleaved by
-// column group.  W is a d x d table in global memory read column-coalesced
-// (every thread of a warp loads consecutive i of the same row j); X rows are
-// broadcast from shared memory.
-template <int D, int TM>
-__device__ __forceinline__ void matvec_rows(const float *__restrict__ W, const float *X, float *Y)
-{
-    constexpr int CG = kThreads / D;
-    constexpr int RPT = TM / CG;
-    const int tid = threadIdx.x;
-    const int i = tid % D, rg = tid / D;
-    float acc[RPT];
-#pragma unroll
-    for (int rr = 0; rr < RPT; ++rr) acc[rr] = 0.f;
-    const float *w = W + i;
-#pragma unroll 2
-    for (int j = 0; j < D; j += 4) {
-        const float w0 = __ldg(w + (j + 0) * D);
-        const float w1 = __ldg(w + (j + 1) * D);
-        const float w2 = __ldg(w + (j + 2) * D);
-        const float w3 = __ldg(w + (j + 3) * D);
-#pragma unroll
-        for (int rr = 0; rr < RPT; ++rr) {
-            const float4 x = *reinterpret_cast<const float4 *>(X + (rg + rr * CG) * D + j);
-            acc[rr] = fmaf(w0, x.x, acc[rr]);
-            acc[rr] = fmaf(w1, x.y, acc[rr]);
-            acc[rr] = fmaf(w2, x.z, acc[rr]);
-            acc[rr] = fmaf(w3, x.w, acc[rr]);
-        }
-    }
-#pragma unroll
-    for (int rr = 0; rr < RPT; ++rr) Y[(rg + rr * CG) * D + i] = acc[rr];
-}
-
 constexpr int kStreamWarps = 8;
 constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23: adding it rounds to an integer
 constexpr uint32_t kRoundBits = 0x4B400000u;
@@ -238,6 +204,58 @@ __device__ __forceinline__ void mma_rows(const uint4 *__restrict__ pi_frag, cons
 #pragma unroll
             for (int n = 0; n < NPW; ++n) {
                 mma16816_f16(acc[m][n], a0, a1, a2, a3, bf[n].z, bf[n].w);  // low parts first
+                mma16816_f16(acc[m][n], a0, a1, a2, a3, bf[n].x, bf[n].y);
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MTS; ++m) {
+        const int row = 16 * m + r;
+        const float s0 = ysc[row], s1 = ysc[row + 8];
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) {
+            const int col = 8 * (warp * NPW + n) + 2 * q;
+            *reinterpret_cast<float2 *>(Yo + row * D + col) = make_float2(acc[m][n][0] * s0, acc[m][n][1] * s0);
+            *reinterpret_cast<float2 *>(Yo + (row + 8) * D + col) = make_float2(acc[m][n][2] * s1, acc[m][n][3] * s1);
+        }
+    }
+}
+
+// The same product for an fp32 input given as fp16 high (ka) and low (kl) parts of
+// the rows times a power of two, against W 2^12 in high / low fragments: three MMAs
+// per step (high x low, low x high, high x high), ~22 significant bits.  Used for the
+// QJL projection p = S r of the residuals; Y[row] is written scaled by ysc[row].
+template <int D, int TM>
+__device__ __forceinline__ void mma_rows3(const uint4 *__restrict__ frag, const __half *ka, const __half *kl,
+                                          const float *ysc, float *Yo)
+{
+    constexpr int KS = D / 16, NPW = D / 64, MTS = TM / 16, KA = D + 8;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = lane >> 2, q = lane & 3;
+    float acc[MTS][NPW][4];
+#pragma unroll
+    for (int m = 0; m < MTS; ++m)
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) acc[m][n][0] = acc[m][n][1] = acc[m][n][2] = acc[m][n][3] = 0.f;
+    const uint32_t kab = static_cast<uint32_t>(__cvta_generic_to_shared(ka));
+    const uint32_t klb = static_cast<uint32_t>(__cvta_generic_to_shared(kl));
+#pragma unroll 2
+    for (int s = 0; s < KS; ++s) {
+        uint4 bf[NPW];
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) bf[n] = __ldg(frag + ((warp * NPW + n) * KS + s) * 32 + lane);
+#pragma unroll
+        for (int m = 0; m < MTS; ++m) {
+            uint32_t a0, a1, a2, a3, l0, l1, l2, l3;
+            const uint32_t off = 2u * ((16 * m + (lane & 15)) * KA + 16 * s + 8 * (lane >> 4));
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(kab + off));
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(l0), "=r"(l1), "=r"(l2), "=r"(l3) : "r"(klb + off));
+#pragma unroll
+            for (int n = 0; n < NPW; ++n) {
+                mma16816_f16(acc[m][n], a0, a1, a2, a3, bf[n].z, bf[n].w);  // small products first
+                mma16816_f16(acc[m][n], l0, l1, l2, l3, bf[n].x, bf[n].y);
                 mma16816_f16(acc[m][n], a0, a1, a2, a3, bf[n].x, bf[n].y);
             }
         }
@@ -636,13 +654,50 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     __syncthreads();
     // ---- QJL: p = S r, gamma, sign guard ---------------------------------------
     if (C.qjl) {
-        matvec_rows<D, TM>(C.ST, yb, kf);
+        // the residuals as fp16 high + low parts times a power of two per row (high in
+        // ka, low over yb once every row is in registers), then p = S r on mma.sync
+        constexpr int E = D / 32, RPW = TM / kWarps, KA = D + 8;
+        float rv[RPW][E];
+#pragma unroll
+        for (int k = 0; k < RPW; ++k) {
+            const int row = warp + kWarps * k;
+            float ss = 0.f, mx = 0.f;
+#pragma unroll
+            for (int m = 0; m < E; ++m) {
+                rv[k][m] = yb[row * D + lane + 32 * m];
+                ss = fmaf(rv[k][m], rv[k][m], ss);
+                mx = fmaxf(mx, fabsf(rv[k][m]));
+            }
+            ss = warp_sum(ss);
+            mx = warp_max(mx);
+            if (lane == 0) {
+                s_rn[row] = sqrtf(ss);
+                // max |r| 2^(15 - ex) in [2^14, 2^15); back by 2^(ex - 15 - 12)
+                const bool ok = mx >= 0x1p-60f && mx <= 0x1p60f;
+                const int ex = ok ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 126 : 0;
+                s_scale[row] = ok ? __uint_as_float(static_cast<uint32_t>(127 + 15 - ex) << 23) : 0.f;
+                s_ysc[row] = ok ? __uint_as_float(static_cast<uint32_t>(127 + ex - 27) << 23) : 0.f;
+            }
+        }
+        __syncthreads();  // every residual is in registers; row scales published
+        __half *klo = reinterpret_cast<__half *>(yb);
+#pragma unroll
+        for (int k = 0; k < RPW; ++k) {
+            const int row = warp + kWarps * k;
+            const float sc = s_scale[row];
+#pragma unroll
+            for (int m = 0; m < E; ++m) {
+                const float x = rv[k][m] * sc;
+                const __half h = __float2half_rn(x);
+                ka[row * KA + lane + 32 * m] = h;
+                klo[row * KA + lane + 32 * m] = __float2half_rn(x - __half2float(h));
+            }
+        }
+        __syncthreads();
+        mma_rows3<D, TM>(C.s_frag, ka, klo, s_ysc, kf);
         __syncthreads();
         for (int row = warp; row < TM; row += kWarps) {
-            float ss = 0.f;
-            for (int j = lane; j < D; j += 32) ss = fmaf(yb[row * D + j], yb[row * D + j], ss);
-            ss = warp_sum(ss);
-            const float rn = sqrtf(ss);
+            const float rn = s_rn[row];
             bool near = false;
             for (int j = lane; j < D; j += 32) near |= fabsf(kf[row * D + j]) < kSignGuard * rn;
             near = __any_sync(0xffffffffu, near);
