@@ -626,7 +626,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const Codec C, 
             // row (8 tokens of one coordinate) per k; the 8 lanes of a store phase (j7 = 0..7)
             // write the 8 rows of one core matrix ----
             {
-                const ValueItem vi{raw_s, pok_s, page_bytes, pos0, L, pshift, P, gshift, pt & 7, (pt >> 3) & 7, pt >> 6};
+                // the four 8-lane groups of a warp take the four coordinate blocks of the same
+                // tokens: their code and scale loads fall in different banks
+                const ValueItem vi{raw_s, pok_s, page_bytes, pos0, L, pshift, P, gshift, pt & 7, pt >> 5, (pt >> 3) & 3};
                 if (vb == 2) decode_values<2>(C, PG, vi, vlut, vt);
                 else if (vb == 3) decode_values<3>(C, PG, vi, vlut, vt);
                 else decode_values<4>(C, PG, vi, vlut, vt);
