@@ -540,3 +540,52 @@ def test_size_edges():
         native.tq_decode_attention(codec.handle, q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(),
                                    sl.data_ptr(), 1, w.num_q_heads, w.num_kv_heads, w.page_size, 1,
                                    b.num_blocks, b.sm_scale, 1025, ws.data_ptr(), ws.numel(), out.data_ptr(), 0)
+
+
+# --------------------------------------------------------------------------- #
+# Query rotation on the tensor cores (many query rows)                         #
+# --------------------------------------------------------------------------- #
+
+@pytest.mark.parametrize("d,kb,vb,G", [(128, 3, 2, 8), (128, 4, 4, 4), (256, 2, 3, 4), (256, 4, 2, 8)])
+def test_many_query_rows_use_the_tensor_core_rotation(d, kb, vb, G):
+    """A call with at least 2,048 query rows rotates the queries with mma.sync (Pi 2^10
+    and M = S Pi as fp16 high/low fragments) instead of the fp32 kernel; decode through
+    it (with and without QJL, both head dims, one split and several) still matches the
+    oracle element by element, and the rotation equals the fp32 path's to 2^-16 of its
+    largest element (both are ~2^-22-accurate products; a wrong matrix errs by O(1))."""
+    Hkv = 4
+    B = 2048 // (Hkv * G) + 3
+    w = W.Workload("many_rows", d, kb, vb, 32, 16, num_kv_heads=Hkv, num_q_heads=Hkv * G, batch=B,
+                   seq_len_range=(20, 90), seed=d + kb + G)
+    b = W.generate(w, device="cpu")
+    b = W.Batch(**{f: (getattr(b, f).to(DEV) if isinstance(getattr(b, f), torch.Tensor) else getattr(b, f))
+                   for f in b.__dataclass_fields__})
+    codec = Codec(d, kb, vb, 32, w.codec_seed())
+    ora = O.Oracle(d, kb, vb, 32, w.codec_seed())
+    kc, vc = _compress(codec, w, b)
+    kc_np, vc_np = kc.cpu().numpy(), vc.cpu().numpy()
+    ref = _decode_oracle(ora, w, b, kc_np, vc_np)
+    for splits in (1, 3):
+        check_decode(_decode_gpu(codec, w, b, kc, vc, splits=splits), ref)
+    assert codec.get_status() == 0
+    # the rotated queries themselves: fp32 workspace rows after a call with many rows
+    # against a call with few (the fp32 kernel), sequence by sequence
+    rows = B * w.num_q_heads
+    ws = codec.workspace(B, w.num_q_heads, 1, device=DEV)
+    codec.decode_attention(b.q, kc, vc, b.block_table, b.seq_lens, Hkv, 16, b.num_blocks, b.sm_scale, splits=1,
+                           workspace=ws)
+    torch.cuda.synchronize()
+    wsf = ws.view(torch.float32)
+    al = lambda x: (x + 63) // 64 * 64  # 256-byte pieces, in floats
+    qrot_many = wsf[al(rows * d): al(rows * d) + rows * d].clone()
+    ws1 = codec.workspace(1, w.num_q_heads, 1, device=DEV)
+    qrot_few = torch.empty_like(qrot_many)
+    for s in range(B):
+        codec.decode_attention(b.q[s:s + 1].contiguous(), kc, vc, b.block_table[s:s + 1].contiguous(),
+                               b.seq_lens[s:s + 1].contiguous(), Hkv, 16, b.num_blocks, b.sm_scale, splits=1,
+                               workspace=ws1)
+        r1 = w.num_q_heads
+        qrot_few[s * r1 * d:(s + 1) * r1 * d] = ws1.view(torch.float32)[al(r1 * d): al(r1 * d) + r1 * d]
+    torch.cuda.synchronize()
+    scale = qrot_few.abs().max()
+    assert float((qrot_many - qrot_few).abs().max()) <= float(scale) * 2.0 ** -16
