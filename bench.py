@@ -469,6 +469,18 @@ def per_config(dev, peak, reps, only=None):
                         "decode_us": round(t_d * 1e6, 1), "decode_splits": splits,
                         "decode_kv_tokens_per_s": round(sum(lens) * w.num_kv_heads / t_d, 1),
                         "decode_query_tokens_per_s": round(w.batch / t_d, 1)})
+        if name == "paged_decode":
+            # dequantisation of the whole cache back to bf16 (tq_dequant_kv): every record
+            # read once, K and V written in bf16
+            ko = torch.empty_like(b.k)
+            vo = torch.empty_like(b.v)
+            t_q = timed(lambda: codec.dequant_kv(kc, vc, w.page_size, b.num_blocks, w.num_kv_heads, b.slot_mapping,
+                                                 k_out=ko, v_out=vo, stream=stream))
+            qb = T * w.num_kv_heads * (sum(record_bytes(w.head_dim, w.k_bits, w.v_bits, w.group)) + 4 * w.head_dim) + T * 8
+            ent.update({"dequant_gbs": round(qb / t_q / 1e9, 1), "dequant_frac": round(qb / t_q / 1e9 / peak, 4),
+                        "dequant_us": round(t_q * 1e6, 1),
+                        "dequant_mtoken_heads_per_s": round(T * w.num_kv_heads / t_q / 1e6, 1)})
+            del ko, vo
         if codec.get_status(stream) != 0:
             raise RuntimeError(f"device status bits set in the {name} workload")
         out[name] = ent

@@ -177,18 +177,20 @@ tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t s
                 put(1, i, j, ht.S[static_cast<size_t>(i) * d + j] * 4096.0);
             }
     }
-    // Pi 2^10, M 2^10 (M = S Pi) and S 2^12 as fp16 high / low parts in the fragment
+    // Pi 2^10, M 2^10 (M = S Pi), S 2^12, Pi^T 2^10 and S^T 2^12 as fp16 high / low parts in the fragment
     // order of mma.sync m16n8k16's B operand (B[k][n] = W[n][k]): for n-tile nt, k-step
     // ks and lane (r, q) the pairs (k0, k0 + 1) and (k0 + 8, k0 + 9) of row n = 8 nt + r,
     // k0 = 16 ks + 2 q
     const size_t frag_one = static_cast<size_t>(d / 8) * (d / 16) * 32 * 4;
-    const size_t frag_words = 3 * frag_one;
+    const size_t frag_words = 5 * frag_one;
     std::vector<uint32_t> frag(frag_words);
-    for (int mat = 0; mat < 3; ++mat) {
-        const double *W = mat == 0 ? ht.Pi.data() : (mat == 1 ? Md.data() : ht.S.data());
-        const double scale = mat == 2 ? 4096.0 : 1024.0;
+    for (int mat = 0; mat < 5; ++mat) {
+        // W[n][k]: Pi, M, S, then the transposes Pi^T and S^T (W[n][k] = Pi[k][n], S[k][n])
+        const double *W = mat == 0 ? ht.Pi.data() : (mat == 1 ? Md.data() : (mat == 3 ? ht.Pi.data() : ht.S.data()));
+        const bool tr = mat >= 3;
+        const double scale = (mat == 2 || mat == 4) ? 4096.0 : 1024.0;
         auto hl = [&](int n, int kk, uint16_t *hi, uint16_t *lo) {
-            const double x = W[static_cast<size_t>(n) * d + kk] * scale;
+            const double x = W[tr ? static_cast<size_t>(kk) * d + n : static_cast<size_t>(n) * d + kk] * scale;
             const __half h = __float2half_rn(static_cast<float>(x));
             *hi = __half_as_ushort(h);
             *lo = __half_as_ushort(__float2half_rn(static_cast<float>(x - static_cast<double>(__half2float(h)))));
@@ -269,6 +271,8 @@ tq_status tq_init_ex(int head_dim, int k_bits, int v_bits, int group, uint64_t s
     k.pi_frag = reinterpret_cast<const uint4 *>(frag_dev);
     k.m_frag = reinterpret_cast<const uint4 *>(frag_dev) + frag_one / 4;
     k.s_frag = reinterpret_cast<const uint4 *>(frag_dev) + 2 * (frag_one / 4);
+    k.pit_frag = reinterpret_cast<const uint4 *>(frag_dev) + 3 * (frag_one / 4);
+    k.st_frag = reinterpret_cast<const uint4 *>(frag_dev) + 4 * (frag_one / 4);
     k.rotation = rotation;
     k.status = status;
     k.wait_limit = tq::kDefaultWaitLimit;

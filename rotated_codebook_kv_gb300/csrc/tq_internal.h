@@ -38,6 +38,8 @@ struct Codec {
     const uint4 *pi_frag;  // Pi 2^10 as fp16 high / low mma.sync B fragments: [d/8 n-tiles][d/16 k-steps][32 lanes]
     const uint4 *m_frag;   // M 2^10 (M = S Pi) in the same fragment image
     const uint4 *s_frag;   // S 2^12 in the same fragment image
+    const uint4 *pit_frag; // Pi^T 2^10 in the same fragment image (y = Pi^T x)
+    const uint4 *st_frag;  // S^T 2^12 in the same fragment image
     int rotation;          // 0: dense Haar, 1: randomized Hadamard
     int vmse;              // values coded by the rotation and a Lloyd-Max codebook (TQ_VALUES_MSE)
     float vcentroids[16];  // value codebook (vmse), N(0,1) units, ascending

@@ -589,3 +589,52 @@ def test_many_query_rows_use_the_tensor_core_rotation(d, kb, vb, G):
     torch.cuda.synchronize()
     scale = qrot_few.abs().max()
     assert float((qrot_many - qrot_few).abs().max()) <= float(scale) * 2.0 ** -16
+
+
+@pytest.mark.parametrize("d,kb,vb,g,values", [(128, 3, 2, 32, "group"), (128, 4, 4, 64, "group"),
+                                              (256, 2, 3, 32, "group"), (128, 2, 3, 32, "mse"),
+                                              (256, 4, 2, 64, "mse")])
+def test_dequant_many_slots_on_the_tensor_cores(d, kb, vb, g, values):
+    """tq_dequant_kv over thousands of (slot, kv head) rows runs on mma.sync (Pi^T and
+    S^T as fp16 high/low fragment images); every reconstructed element is within one
+    bf16 ulp of the oracle's double-precision dequantisation, or 2^-20 of its row's
+    norm for elements near zero (the products carry ~22 bits: measured worst 1.4e-7 of
+    the norm), skipped slots (-1) are left untouched, and a second call with a few
+    slots (the CUDA-core kernel) agrees to the same bound."""
+    Hkv = 2
+    w = W.Workload("dq_many", d, kb, vb, g, 16, num_kv_heads=Hkv, num_q_heads=Hkv, batch=8,
+                   seq_len_range=(250, 450), seed=3 * d + kb + vb)
+    b = W.generate(w, device="cpu")
+    b = W.Batch(**{f: (getattr(b, f).to(DEV) if isinstance(getattr(b, f), torch.Tensor) else getattr(b, f))
+                   for f in b.__dataclass_fields__})
+    codec = Codec(d, kb, vb, g, w.codec_seed(), values=values)
+    ora = O.Oracle(d, kb, vb, g, w.codec_seed(), values=values)
+    kc, vc = codec.alloc_cache(b.num_blocks, Hkv, 16, fill=0xA5)
+    codec.compress_kv(b.k, b.v, b.slot_mapping, kc, vc, 16, b.num_blocks)
+    slots = b.slot_mapping.clone()
+    slots[5] = -1
+    assert slots.numel() * Hkv >= 2048
+    ko = torch.full((slots.numel(), Hkv, d), 0x7FC1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    vo = torch.full_like(ko, 0)
+    vo.view(torch.int16).fill_(0x7FC1)
+    codec.dequant_kv(kc, vc, 16, b.num_blocks, Hkv, slots, k_out=ko, v_out=vo)
+    torch.cuda.synchronize()
+    assert codec.get_status() == 0
+    rk, rv = ora.dequant_slots(kc.cpu().numpy(), vc.cpu().numpy(), 16, Hkv, slots.cpu().numpy())
+    gk, gv = O.bf16_to_double(W.as_u16(ko)), O.bf16_to_double(W.as_u16(vo))
+    keep = np.ones(slots.numel(), dtype=bool)
+    keep[5] = False
+    def bound(ref):
+        ax = np.abs(ref)
+        ulp = 2.0 ** (np.floor(np.log2(np.where(ax > 0, ax, 1.0))) - 7)
+        return ulp + 2.0 ** -20 * np.linalg.norm(ref, axis=-1, keepdims=True)
+    for gg, rr_ in ((gk, rk), (gv, rv)):
+        assert np.all(np.abs(gg[keep] - rr_[keep]) <= bound(rr_[keep]))
+    assert np.all(W.as_u16(ko)[5] == 0x7FC1) and np.all(W.as_u16(vo)[5] == 0x7FC1)
+    few = slots[:40].contiguous()
+    kf, vf = codec.dequant_kv(kc, vc, 16, b.num_blocks, Hkv, few)
+    torch.cuda.synchronize()
+    m = np.ones(40, dtype=bool)
+    m[5] = False
+    for a_, r_ in ((kf, rk[:40]), (vf, rv[:40])):
+        assert np.all(np.abs(O.bf16_to_double(W.as_u16(a_))[m] - r_[m]) <= bound(r_[m]))
