@@ -36,8 +36,9 @@ template <int D>
 struct CompressSmem {
     static constexpr int TM = kRowsPerBlock;
     static constexpr int kCodeStride = D + 4;
-    static constexpr size_t kKf = sizeof(float) * TM * D;      // keys, later S r
-    static constexpr size_t kYb = sizeof(float) * TM * D;      // Pi k, later r
+    static constexpr int kRS = D + 8;                          // fp32 row stride (8 rows of an MMA fragment: 8 bank groups)
+    static constexpr size_t kKf = sizeof(float) * TM * kRS;    // keys, later S r
+    static constexpr size_t kYb = sizeof(float) * TM * kRS;    // Pi k, later r
     static constexpr size_t kCodes = ((TM * kCodeStride + 15) / 16) * 16;
     static constexpr size_t kScratch = sizeof(double) * kWarps * D;
     static constexpr size_t kKa = sizeof(__half) * TM * (D + 8);  // fp16 keys for the tensor-core rotation
@@ -154,7 +155,7 @@ __device__ __forceinline__ void stage_fp16_row(const float *kf, __half *ka, int 
     const int ex = ok ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 126 : 0;
     const float sc = ok ? __uint_as_float(static_cast<uint32_t>(127 + 15 - ex) << 23) : 0.f;
     for (int j = 2 * lane; j < D; j += 64) {
-        const float2 x = *reinterpret_cast<const float2 *>(kf + row * D + j);
+        const float2 x = *reinterpret_cast<const float2 *>(kf + row * (D + 8) + j);
         *reinterpret_cast<__half2 *>(ka + row * (D + 8) + j) = __floats2half2_rn(x.x * sc, x.y * sc);
     }
     if (lane == 0) ysc[row] = ok ? __uint_as_float(static_cast<uint32_t>(127 + ex - 25) << 23) : 0.f;
@@ -215,8 +216,9 @@ __device__ __forceinline__ void mma_rows(const uint4 *__restrict__ pi_frag, cons
 #pragma unroll
         for (int n = 0; n < NPW; ++n) {
             const int col = 8 * (warp * NPW + n) + 2 * q;
-            *reinterpret_cast<float2 *>(Yo + row * D + col) = make_float2(acc[m][n][0] * s0, acc[m][n][1] * s0);
-            *reinterpret_cast<float2 *>(Yo + (row + 8) * D + col) = make_float2(acc[m][n][2] * s1, acc[m][n][3] * s1);
+            *reinterpret_cast<float2 *>(Yo + row * (D + 8) + col) = make_float2(acc[m][n][0] * s0, acc[m][n][1] * s0);
+            *reinterpret_cast<float2 *>(Yo + (row + 8) * (D + 8) + col) =
+                make_float2(acc[m][n][2] * s1, acc[m][n][3] * s1);
         }
     }
 }
@@ -267,8 +269,9 @@ __device__ __forceinline__ void mma_rows3(const uint4 *__restrict__ frag, const 
 #pragma unroll
         for (int n = 0; n < NPW; ++n) {
             const int col = 8 * (warp * NPW + n) + 2 * q;
-            *reinterpret_cast<float2 *>(Yo + row * D + col) = make_float2(acc[m][n][0] * s0, acc[m][n][1] * s0);
-            *reinterpret_cast<float2 *>(Yo + (row + 8) * D + col) = make_float2(acc[m][n][2] * s1, acc[m][n][3] * s1);
+            *reinterpret_cast<float2 *>(Yo + row * (D + 8) + col) = make_float2(acc[m][n][0] * s0, acc[m][n][1] * s0);
+            *reinterpret_cast<float2 *>(Yo + (row + 8) * (D + 8) + col) =
+                make_float2(acc[m][n][2] * s1, acc[m][n][3] * s1);
         }
     }
 }
@@ -292,7 +295,7 @@ __device__ __forceinline__ void fwht_rows(const float *__restrict__ hsign, const
         float x[E];
 #pragma unroll
         for (int m = 0; m < E; m += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(X + row * D + E * lane + m);
+            const float4 v = *reinterpret_cast<const float4 *>(X + row * (D + 8) + E * lane + m);
             x[m] = v.x * sg[m];
             x[m + 1] = v.y * sg[m + 1];
             x[m + 2] = v.z * sg[m + 2];
@@ -318,7 +321,7 @@ __device__ __forceinline__ void fwht_rows(const float *__restrict__ hsign, const
         }
 #pragma unroll
         for (int m = 0; m < E; m += 4)
-            *reinterpret_cast<float4 *>(Y + row * D + E * lane + m) =
+            *reinterpret_cast<float4 *>(Y + row * (D + 8) + E * lane + m) =
                 make_float4(x[m] * inv, x[m + 1] * inv, x[m + 2] * inv, x[m + 3] * inv);
     }
 }
@@ -526,6 +529,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     using SM = CompressSmem<D>;
     constexpr int TM = SM::TM;
     constexpr int CS = SM::kCodeStride;
+    constexpr int RS = SM::kRS;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float *kf = reinterpret_cast<float *>(smem_raw);
     float *yb = reinterpret_cast<float *>(smem_raw + SM::kKf);
@@ -590,15 +594,15 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
                                 bf16_to_float(u.y >> 16));
         float4 hi = make_float4(bf16_to_float(u.z & 0xffffu), bf16_to_float(u.z >> 16), bf16_to_float(u.w & 0xffffu),
                                 bf16_to_float(u.w >> 16));
-        *reinterpret_cast<float4 *>(kf + row * D + c8 * 8) = lo;
-        *reinterpret_cast<float4 *>(kf + row * D + c8 * 8 + 4) = hi;
+        *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8) = lo;
+        *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8 + 4) = hi;
     }
     __syncthreads();
     // ---- norms; rows with an extreme range take the exact path -------------
     for (int row = warp; row < TM; row += kWarps) {
         float ss = 0.f, mx = 0.f;
         for (int j = lane; j < D; j += 32) {
-            const float x = kf[row * D + j];
+            const float x = kf[row * RS + j];
             ss = fmaf(x, x, ss);
             mx = fmaxf(mx, fabsf(x));
         }
@@ -632,7 +636,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     for (int e = tid; e < TM * D; e += kThreads) {
         const int row = e / D, i = e - row * D;
         const int fl = s_flag[row];
-        const float z = yb[e] * s_scale[row];
+        const float z = yb[row * RS + i] * s_scale[row];
         bool near;
         int code;
         if (!binbad) {
@@ -648,7 +652,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         // flagged 3: the exact pass re-decides just the marked codes
         const bool mark = (fl == 0 || fl == 3) && near;
         codes[row * CS + i] = static_cast<uint8_t>(code | (mark ? 0x80 : 0));
-        yb[e] = (fl == 2) ? 0.f : z - s_cent[code];
+        yb[row * RS + i] = (fl == 2) ? 0.f : z - s_cent[code];
         if (mark) s_flag[row] = 3;
     }
     __syncthreads();
@@ -664,7 +668,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             float ss = 0.f, mx = 0.f;
 #pragma unroll
             for (int m = 0; m < E; ++m) {
-                rv[k][m] = yb[row * D + lane + 32 * m];
+                rv[k][m] = yb[row * RS + lane + 32 * m];
                 ss = fmaf(rv[k][m], rv[k][m], ss);
                 mx = fmaxf(mx, fabsf(rv[k][m]));
             }
@@ -699,7 +703,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         for (int row = warp; row < TM; row += kWarps) {
             const float rn = s_rn[row];
             bool near = false;
-            for (int j = lane; j < D; j += 32) near |= fabsf(kf[row * D + j]) < kSignGuard * rn;
+            for (int j = lane; j < D; j += 32) near |= fabsf(kf[row * RS + j]) < kSignGuard * rn;
             near = __any_sync(0xffffffffu, near);
             if (lane == 0) {
                 s_rn[row] = rn;
@@ -723,7 +727,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
                                                         codes + row * CS, C.thresholds, (1 << C.k_bits) - 1);
             if (!(changed && C.qjl)) continue;
         }
-        precise_key_row<D>(C, kin + t * ks + static_cast<int64_t>(h) * D, codes + row * CS, kf + row * D,
+        precise_key_row<D>(C, kin + t * ks + static_cast<int64_t>(h) * D, codes + row * CS, kf + row * RS,
                            scratch + warp * D, &s_n16[row], &s_g16[row], C.thresholds, C.centroids, C.k_bits,
                            C.qjl != 0);
     }
@@ -743,7 +747,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         if (C.qjl) {
 #pragma unroll
             for (int w = 0; w < D / 32; ++w) {
-                uint32_t bits = __ballot_sync(0xffffffffu, kf[row * D + 32 * w + lane] >= 0.f);
+                uint32_t bits = __ballot_sync(0xffffffffu, kf[row * RS + 32 * w + lane] >= 0.f);
                 if (zero) bits = 0u;
                 if (lane == w)
                     *reinterpret_cast<uint32_t *>(krec + G.k_sign_off + static_cast<int64_t>(off) * C.k_sign_bytes +
@@ -853,10 +857,10 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
                 const int h = static_cast<int>(r - t * Hkv);
                 u = __ldg(reinterpret_cast<const uint4 *>(vin + t * vs + static_cast<int64_t>(h) * D) + c8);
             }
-            *reinterpret_cast<float4 *>(kf + row * D + c8 * 8) =
+            *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8) =
                 make_float4(bf16_to_float(u.x & 0xffffu), bf16_to_float(u.x >> 16), bf16_to_float(u.y & 0xffffu),
                             bf16_to_float(u.y >> 16));
-            *reinterpret_cast<float4 *>(kf + row * D + c8 * 8 + 4) =
+            *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8 + 4) =
                 make_float4(bf16_to_float(u.z & 0xffffu), bf16_to_float(u.z >> 16), bf16_to_float(u.w & 0xffffu),
                             bf16_to_float(u.w >> 16));
         }
@@ -864,7 +868,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         for (int row = warp; row < TM; row += kWarps) {
             float ss = 0.f, mx = 0.f;
             for (int j = lane; j < D; j += 32) {
-                const float x = kf[row * D + j];
+                const float x = kf[row * RS + j];
                 ss = fmaf(x, x, ss);
                 mx = fmaxf(mx, fabsf(x));
             }
@@ -892,7 +896,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         for (int e = tid; e < TM * D; e += kThreads) {
             const int row = e / D, i = e - row * D;
             const int fl = s_flag[row];
-            const float z = yb[e] * s_scale[row];
+            const float z = yb[row * RS + i] * s_scale[row];
             bool near;
             int code;
             if (!binbad) {
@@ -919,7 +923,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
                                        C.vthresholds, (1 << C.v_bits) - 1);
                 continue;
             }
-            precise_key_row<D>(C, vin + t * vs + static_cast<int64_t>(h) * D, codes + row * CS, kf + row * D,
+            precise_key_row<D>(C, vin + t * vs + static_cast<int64_t>(h) * D, codes + row * CS, kf + row * RS,
                                scratch + warp * D, &s_n16[row], &s_g16[row], C.vthresholds, C.vcentroids, C.v_bits,
                                false);
         }
