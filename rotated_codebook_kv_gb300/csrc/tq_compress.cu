@@ -276,6 +276,115 @@ __device__ __forceinline__ void mma_rows3(const uint4 *__restrict__ frag, const 
     }
 }
 
+// Codes by a table of 64 bins on u = z / 8 + 1/2 (z in [-4, 4]; outside it the end
+// bins, which hold no threshold), each bin widened by 1/64 on both sides so that a
+// threshold within the guard band of any z of the bin is the bin's own.  Entry
+// [bin][copy] = {that threshold or +inf, 2^23 + number of thresholds below the
+// widened bin}, in kBinCopies copies (lane l reads copy l % kBinCopies).  A bin that
+// would hold two thresholds makes the build report failure (the codes then take the
+// binary search); the Lloyd-Max thresholds are >= 0.25 apart, wider than a bin.
+constexpr int kBinCopies = 8;
+constexpr float kBinScale = 8064.f;  // 63 bins * 128: round(u * 8064) / 128 is the bin
+
+__device__ __forceinline__ bool build_code_bins(float2 *bins, const float *thr, int nthr)
+{
+    bool bad = false;
+    for (int e = threadIdx.x; e < 64 * kBinCopies; e += blockDim.x) {
+        const float b = static_cast<float>(e / kBinCopies);
+        const float lo = 8.f * (128.f * b - 0.5f) / kBinScale - 4.f - 1.f / 64.f;
+        const float hi = 8.f * (128.f * b + 127.5f) / kBinScale - 4.f + 1.f / 64.f;
+        int below = 0, idx = -1, hits = 0;
+        for (int t = 0; t < nthr; ++t) {
+            const float th = thr[t];
+            if (th < lo) ++below;
+            else if (th <= hi) { idx = t; ++hits; }
+        }
+        bins[e] = make_float2(idx >= 0 ? thr[idx] : INFINITY, __uint_as_float(0x4B000000u + below));
+        bad |= hits > 1;
+    }
+    return bad;
+}
+
+// code = number of thresholds <= z; near: a threshold lies within kCodeGuard of z
+__device__ __forceinline__ int bin_code(float z, const unsigned char *binb, bool &near)
+{
+    const float u = __saturatef(fmaf(z, 0.125f, 0.5f));
+    const uint32_t a = (__float_as_uint(fmaf(u, kBinScale, kRoundMagic)) & 0x1F80u) >> 1;  // bin * 64 bytes
+    const float2 e = *reinterpret_cast<const float2 *>(binb + a);
+    const float dz = z - e.x;
+    near = fabsf(dz) < kCodeGuard;
+    return static_cast<int>(__float_as_uint(e.y) - 0x4B000000u) + (dz >= 0.f ? 1 : 0);
+}
+
+// The dense rotation with the codes decided in the epilogue, for keys without QJL
+// (no residual is needed): z = (Pi k)_j sqrt(d) / n from the accumulators (rounded
+// as the stored rotation would be: y = acc ysc, then z = y scale), the code from the
+// bin table (binary search if the table could not be built), codes inside the
+// guard band marked (bit 7) and their row flagged 3, zero keys (flag 2) coded 0.
+template <int D, int TM>
+__device__ __forceinline__ void mma_rows_codes(const uint4 *__restrict__ pi_frag, const __half *ka, const float *ysc,
+                                               const float *zsc, int *flag, const unsigned char *binb, bool binbad,
+                                               const float *thr, int kb, uint8_t *codes, int cs)
+{
+    constexpr int KS = D / 16, NPW = D / 64, MTS = TM / 16, KA = D + 8;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = lane >> 2, q = lane & 3;
+    float acc[MTS][NPW][4];
+#pragma unroll
+    for (int m = 0; m < MTS; ++m)
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) acc[m][n][0] = acc[m][n][1] = acc[m][n][2] = acc[m][n][3] = 0.f;
+    const uint32_t kab = static_cast<uint32_t>(__cvta_generic_to_shared(ka));
+#pragma unroll 2
+    for (int s = 0; s < KS; ++s) {
+        uint4 bf[NPW];
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) bf[n] = __ldg(pi_frag + ((warp * NPW + n) * KS + s) * 32 + lane);
+#pragma unroll
+        for (int m = 0; m < MTS; ++m) {
+            uint32_t a0, a1, a2, a3;
+            const uint32_t addr = kab + 2u * ((16 * m + (lane & 15)) * KA + 16 * s + 8 * (lane >> 4));
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(addr));
+#pragma unroll
+            for (int n = 0; n < NPW; ++n) {
+                mma16816_f16(acc[m][n], a0, a1, a2, a3, bf[n].z, bf[n].w);  // low parts first
+                mma16816_f16(acc[m][n], a0, a1, a2, a3, bf[n].x, bf[n].y);
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MTS; ++m)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int row = 16 * m + r + 8 * h2;
+            const float ys = ysc[row], zs = zsc[row];
+            const int fl = flag[row];
+            bool marked = false;
+#pragma unroll
+            for (int n = 0; n < NPW; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = 8 * (warp * NPW + n) + 2 * q + e;
+                    const float z = (acc[m][n][2 * h2 + e] * ys) * zs;
+                    bool near;
+                    int code;
+                    if (!binbad) {
+                        code = bin_code(z, binb, near);
+                    } else {
+                        code = 0;
+                        for (int step = 1 << (kb - 1); step > 0; step >>= 1)
+                            if (thr[code + step] <= z) code += step;
+                        near = fminf(z - thr[code], thr[code + 1] - z) < kCodeGuard;
+                    }
+                    const bool mark = (fl == 0 || fl == 3) && near;
+                    marked |= mark;
+                    codes[row * cs + col] = static_cast<uint8_t>((fl == 2 ? 0 : code) | (mark ? 0x80 : 0));
+                }
+            if (marked) flag[row] = 3;
+        }
+}
+
 // Hadamard rotation of TM rows (turbo-attn, "How it works", step 1):
 // Y[row] = H (s * X[row]) / sqrt(D) with H the Sylvester Hadamard matrix, by the
 // fast Walsh-Hadamard butterfly.  One warp per row; lane l holds the E = D / 32
@@ -480,46 +589,6 @@ __device__ __noinline__ bool refine_marked_codes(const float *__restrict__ Pi, c
     return changed;
 }
 
-// Codes by a table of 64 bins on u = z / 8 + 1/2 (z in [-4, 4]; outside it the end
-// bins, which hold no threshold), each bin widened by 1/64 on both sides so that a
-// threshold within the guard band of any z of the bin is the bin's own.  Entry
-// [bin][copy] = {that threshold or +inf, 2^23 + number of thresholds below the
-// widened bin}, in kBinCopies copies (lane l reads copy l % kBinCopies).  A bin that
-// would hold two thresholds makes the build report failure (the codes then take the
-// binary search); the Lloyd-Max thresholds are >= 0.25 apart, wider than a bin.
-constexpr int kBinCopies = 8;
-constexpr float kBinScale = 8064.f;  // 63 bins * 128: round(u * 8064) / 128 is the bin
-
-__device__ __forceinline__ bool build_code_bins(float2 *bins, const float *thr, int nthr)
-{
-    bool bad = false;
-    for (int e = threadIdx.x; e < 64 * kBinCopies; e += blockDim.x) {
-        const float b = static_cast<float>(e / kBinCopies);
-        const float lo = 8.f * (128.f * b - 0.5f) / kBinScale - 4.f - 1.f / 64.f;
-        const float hi = 8.f * (128.f * b + 127.5f) / kBinScale - 4.f + 1.f / 64.f;
-        int below = 0, idx = -1, hits = 0;
-        for (int t = 0; t < nthr; ++t) {
-            const float th = thr[t];
-            if (th < lo) ++below;
-            else if (th <= hi) { idx = t; ++hits; }
-        }
-        bins[e] = make_float2(idx >= 0 ? thr[idx] : INFINITY, __uint_as_float(0x4B000000u + below));
-        bad |= hits > 1;
-    }
-    return bad;
-}
-
-// code = number of thresholds <= z; near: a threshold lies within kCodeGuard of z
-__device__ __forceinline__ int bin_code(float z, const unsigned char *binb, bool &near)
-{
-    const float u = __saturatef(fmaf(z, 0.125f, 0.5f));
-    const uint32_t a = (__float_as_uint(fmaf(u, kBinScale, kRoundMagic)) & 0x1F80u) >> 1;  // bin * 64 bytes
-    const float2 e = *reinterpret_cast<const float2 *>(binb + a);
-    const float dz = z - e.x;
-    near = fabsf(dz) < kCodeGuard;
-    return static_cast<int>(__float_as_uint(e.y) - 0x4B000000u) + (dz >= 0.f ? 1 : 0);
-}
-
 template <int D, bool HAD, bool VMSE>
 __global__ void __launch_bounds__(kThreads, 2)
 compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
@@ -580,31 +649,49 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     // the key codebook's bin table; the barrier also publishes the rows' tokens
     const unsigned char *binb = reinterpret_cast<const unsigned char *>(s_bins) + 8 * (lane % kBinCopies);
     bool binbad = __syncthreads_or(build_code_bins(s_bins, C.thresholds, nthr));
-    // ---- load key rows (bf16 -> fp32, exact) ---------------------------------
-    for (int e = tid; e < TM * (D / 8); e += kThreads) {
-        const int row = e / (D / 8), c8 = e - row * (D / 8);
-        const int64_t r = r0 + row;
-        uint4 u = make_uint4(0, 0, 0, 0);
-        if (r < rows) {
-            const int64_t t = s_tok[row];
-            const int h = static_cast<int>(r - t * Hkv);
-            u = __ldg(reinterpret_cast<const uint4 *>(kin + t * ks + static_cast<int64_t>(h) * D) + c8);
+    if constexpr (HAD) {
+        // ---- load key rows (bf16 -> fp32, exact) ---------------------------------
+        for (int e = tid; e < TM * (D / 8); e += kThreads) {
+            const int row = e / (D / 8), c8 = e - row * (D / 8);
+            const int64_t r = r0 + row;
+            uint4 u = make_uint4(0, 0, 0, 0);
+            if (r < rows) {
+                const int64_t t = s_tok[row];
+                const int h = static_cast<int>(r - t * Hkv);
+                u = __ldg(reinterpret_cast<const uint4 *>(kin + t * ks + static_cast<int64_t>(h) * D) + c8);
+            }
+            float4 lo = make_float4(bf16_to_float(u.x & 0xffffu), bf16_to_float(u.x >> 16), bf16_to_float(u.y & 0xffffu),
+                                    bf16_to_float(u.y >> 16));
+            float4 hi = make_float4(bf16_to_float(u.z & 0xffffu), bf16_to_float(u.z >> 16), bf16_to_float(u.w & 0xffffu),
+                                    bf16_to_float(u.w >> 16));
+            *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8) = lo;
+            *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8 + 4) = hi;
         }
-        float4 lo = make_float4(bf16_to_float(u.x & 0xffffu), bf16_to_float(u.x >> 16), bf16_to_float(u.y & 0xffffu),
-                                bf16_to_float(u.y >> 16));
-        float4 hi = make_float4(bf16_to_float(u.z & 0xffffu), bf16_to_float(u.z >> 16), bf16_to_float(u.w & 0xffffu),
-                                bf16_to_float(u.w >> 16));
-        *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8) = lo;
-        *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8 + 4) = hi;
+        __syncthreads();
     }
-    __syncthreads();
-    // ---- norms; rows with an extreme range take the exact path -------------
+    // ---- norms; rows with an extreme range take the exact path; dense rotation:
+    // the keys go straight from bf16 into the fp16 operand (exact after the row scale) ----
     for (int row = warp; row < TM; row += kWarps) {
+        constexpr int E = D / 32;
+        float x[E];
+        if constexpr (HAD) {
+#pragma unroll
+            for (int m = 0; m < E; ++m) x[m] = kf[row * RS + lane + 32 * m];
+        } else {
+            const int64_t r = r0 + row;
+            const uint16_t *src = nullptr;
+            if (r < rows) {
+                const int64_t t = s_tok[row];
+                src = kin + t * ks + (r - t * Hkv) * D;
+            }
+#pragma unroll
+            for (int m = 0; m < E; ++m) x[m] = src ? bf16_to_float(src[lane + 32 * m]) : 0.f;
+        }
         float ss = 0.f, mx = 0.f;
-        for (int j = lane; j < D; j += 32) {
-            const float x = kf[row * RS + j];
-            ss = fmaf(x, x, ss);
-            mx = fmaxf(mx, fabsf(x));
+#pragma unroll
+        for (int m = 0; m < E; ++m) {
+            ss = fmaf(x[m], x[m], ss);
+            mx = fmaxf(mx, fabsf(x[m]));
         }
         ss = warp_sum(ss);
         mx = warp_max(mx);
@@ -618,14 +705,27 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             s_n16[row] = float_to_bf16_bits(n);
             s_g16[row] = 0;
         }
-        if constexpr (!HAD) stage_fp16_row<D>(kf, ka, row, mx, s_ysc);
+        if constexpr (!HAD) {
+            // mx = f 2^ex with f in [0.5, 1); the row times 2^(15 - ex) is exact in fp16
+            const bool ok = mx >= 0x1p-30f && mx <= 0x1p30f;
+            const int ex = ok ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 126 : 0;
+            const float sc = ok ? __uint_as_float(static_cast<uint32_t>(127 + 15 - ex) << 23) : 0.f;
+#pragma unroll
+            for (int m = 0; m < E; ++m) ka[row * (D + 8) + lane + 32 * m] = __float2half_rn(x[m] * sc);
+            if (lane == 0) s_ysc[row] = ok ? __uint_as_float(static_cast<uint32_t>(127 + ex - 25) << 23) : 0.f;
+        }
     }
-    // ---- rotation: yb = Pi k (unnormalised) -----------------------------------
+    // ---- rotation: yb = Pi k (unnormalised); without QJL the codes come straight
+    // from the accumulators ---------------------------------------------------
+    const bool fused = !HAD && !C.qjl;
     if constexpr (HAD) {
         fwht_rows<D, TM>(C.hsign, kf, yb);
     } else {
         __syncthreads();  // ka and s_ysc of every row are staged
-        mma_rows<D, TM>(C.pi_frag, ka, s_ysc, yb);
+        if (fused)
+            mma_rows_codes<D, TM>(C.pi_frag, ka, s_ysc, s_scale, s_flag, binb, binbad, s_thr, C.k_bits, codes, CS);
+        else
+            mma_rows<D, TM>(C.pi_frag, ka, s_ysc, yb);
     }
     __syncthreads();
     // ---- codes, guard band, residual -----------------------------------------
@@ -633,7 +733,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     // (s_thr[c + 1] is threshold c); the distance to the nearest threshold is to
     // one of the two that bracket z
     const int kb = C.k_bits;
-    for (int e = tid; e < TM * D; e += kThreads) {
+    for (int e = fused ? TM * D : tid; e < TM * D; e += kThreads) {
         const int row = e / D, i = e - row * D;
         const int fl = s_flag[row];
         const float z = yb[row * RS + i] * s_scale[row];
