@@ -49,6 +49,12 @@ constexpr int kStreamWarps = 8;
 constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23: adding it rounds to an integer
 constexpr uint32_t kRoundBits = 0x4B400000u;
 
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
+{
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+
 template <int E>
 __device__ __forceinline__ void unpack_bf16(const uint32_t (&w)[E / 2], float (&x)[E])
 {
@@ -99,32 +105,43 @@ __device__ __forceinline__ uint32_t quantize_values_lane(const float (&x)[E], in
     if (sv != 0.f) asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sv));
     const bool exact_all = zv != mn || (sv != 0.f && sv < 6.103515625e-05f);
     codes = 0u;
+    if (!exact_all) {
+        // every element's guess first, then one branch for the rare near-ties, so that
+        // the elements' chains are not split by a branch each
+        uint32_t qq[E], tb[E], tie = 0u;
+#pragma unroll
+        for (int m = 0; m < E; ++m) {
+            const float dx = x[m] - zv;
+            qq[m] = __float_as_uint(fmaf(dx, inv, kRoundMagic)) - kRoundBits;
+            tb[m] = __float_as_uint(fmaf(dx, inv, 192.5f + 4.f / 65536.f));
+            tie |= ((tb[m] & 0xFFF8u) == 0u) ? (1u << m) : 0u;
+        }
+        if (tie) {
+#pragma unroll
+            for (int m = 0; m < E; ++m)
+                if ((tie >> m) & 1u) {
+                    const uint32_t n = (tb[m] >> 16) & 0x1Fu;
+                    const float b = fmaf(static_cast<float>(n), sv, -0.5f * sv);
+                    float a, ea;
+                    two_sum(x[m], -zv, a, ea);
+                    qq[m] = (__fadd_rn(__fsub_rn(a, b), ea) >= 0.f) ? n : n - 1u;
+                }
+        }
+#pragma unroll
+        for (int m = 0; m < E; ++m) codes |= qq[m] << (VB * m);
+        return static_cast<uint32_t>(__half_as_ushort(s16)) | (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
+    }
 #pragma unroll
     for (int m = 0; m < E; ++m) {
-        uint32_t q;
-        if (!exact_all) {
-            const float dx = x[m] - zv;
-            q = __float_as_uint(fmaf(dx, inv, kRoundMagic)) - kRoundBits;
-            const uint32_t tb = __float_as_uint(fmaf(dx, inv, 192.5f + 4.f / 65536.f));
-            if ((tb & 0xFFF8u) == 0u) {
-                const uint32_t n = (tb >> 16) & 0x1Fu;
-                const float b = fmaf(static_cast<float>(n), sv, -0.5f * sv);
-                float a, ea;
-                two_sum(x[m], -zv, a, ea);
-                q = (__fadd_rn(__fsub_rn(a, b), ea) >= 0.f) ? n : n - 1u;
-            }
-        } else {
-            int qi = 0;
-            if (sv != 0.f) {
-                float a, ea;
-                two_sum(x[m], -zv, a, ea);
-                qi = static_cast<int>(fminf(fmaxf(floorf(fmaf(x[m] - zv, inv, 0.5f)), 0.f), static_cast<float>(L)));
-                while (qi < L && __fadd_rn(__fsub_rn(a, (qi + 0.5f) * sv), ea) >= 0.f) ++qi;
-                while (qi > 0 && !(__fadd_rn(__fsub_rn(a, (qi - 0.5f) * sv), ea) >= 0.f)) --qi;
-            }
-            q = static_cast<uint32_t>(qi);
+        int qi = 0;
+        if (sv != 0.f) {
+            float a, ea;
+            two_sum(x[m], -zv, a, ea);
+            qi = static_cast<int>(fminf(fmaxf(floorf(fmaf(x[m] - zv, inv, 0.5f)), 0.f), static_cast<float>(L)));
+            while (qi < L && __fadd_rn(__fsub_rn(a, (qi + 0.5f) * sv), ea) >= 0.f) ++qi;
+            while (qi > 0 && !(__fadd_rn(__fsub_rn(a, (qi - 0.5f) * sv), ea) >= 0.f)) --qi;
         }
-        codes |= q << (VB * m);
+        codes |= static_cast<uint32_t>(qi) << (VB * m);
     }
     return static_cast<uint32_t>(__half_as_ushort(s16)) | (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
 }
@@ -138,6 +155,49 @@ __device__ __forceinline__ void store_code_bytes(uint8_t *p, uint32_t w, int nby
         p[0] = static_cast<uint8_t>(w);
         p[1] = static_cast<uint8_t>(w >> 8);
         p[2] = static_cast<uint8_t>(w >> 16);
+    }
+}
+
+// Word w of the LSB-first bitstream of b-bit codes held one per byte (bit 7 clear):
+// 4- and 2-bit codes fill whole bytes, so their words come from aligned 32-bit loads
+// and shifts; 3-bit codes take the generic bit loop.  `codes` is 4-byte aligned.
+__device__ __forceinline__ uint32_t code_word(const uint8_t *codes, int w, int b)
+{
+    if (b == 4) {
+        const uint32_t lo = *reinterpret_cast<const uint32_t *>(codes + 8 * w);
+        const uint32_t hi = *reinterpret_cast<const uint32_t *>(codes + 8 * w + 4);
+        // bytes 0 and 2 of x | x >> 4 hold codes (0, 1) and (2, 3) as nibble pairs
+        return __byte_perm(lo | (lo >> 4), hi | (hi >> 4), 0x6420);
+    }
+    if (b == 2) {
+        uint32_t v = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t x = *reinterpret_cast<const uint32_t *>(codes + 16 * w + 4 * i);
+            const uint32_t t = x | (x >> 6);  // bits 0-3: codes 0, 1; bits 16-19: codes 2, 3
+            v |= ((t & 0xFu) | ((t >> 12) & 0xF0u)) << (8 * i);
+        }
+        return v;
+    }
+    return pack_word(codes, w, b);
+}
+
+// The b-bit code words of a CTA's TM rows (codes one per byte, row stride cs) stored
+// at each row's slot of its page, all threads of the CTA over rows x words; rows
+// without a slot are skipped and zero rows (flag 2) store zeros.
+template <int D, int TM>
+__device__ __forceinline__ void store_code_words(const uint8_t *codes, int cs, int b, const int64_t *dst,
+                                                 const int *off, const int *flag, uint8_t *pool, int64_t page_bytes,
+                                                 int code_bytes)
+{
+    const int nw = D * b / 32;
+    for (int e = threadIdx.x; e < TM * nw; e += blockDim.x) {
+        const int row = e / nw, w = e - row * nw;
+        const int64_t d = dst[row];
+        if (d < 0) continue;
+        const uint32_t word = flag[row] == 2 ? 0u : code_word(codes + row * cs, w, b);
+        *reinterpret_cast<uint32_t *>(pool + d * page_bytes + static_cast<int64_t>(off[row]) * code_bytes + 4 * w) =
+            word;
     }
 }
 
@@ -316,43 +376,23 @@ __device__ __forceinline__ int bin_code(float z, const unsigned char *binb, bool
     return static_cast<int>(__float_as_uint(e.y) - 0x4B000000u) + (dz >= 0.f ? 1 : 0);
 }
 
-// The dense rotation with the codes decided in the epilogue, for keys without QJL
-// (no residual is needed): z = (Pi k)_j sqrt(d) / n from the accumulators (rounded
-// as the stored rotation would be: y = acc ysc, then z = y scale), the code from the
-// bin table (binary search if the table could not be built), codes inside the
+// The epilogue of the dense rotation without QJL: z = (Pi k)_j sqrt(d) / n from the
+// accumulators (rounded as the stored rotation would be: y = acc ysc, then z = y
+// scale), the code from the bin table (BINS) or by binary search, codes inside the
 // guard band marked (bit 7) and their row flagged 3, zero keys (flag 2) coded 0.
-template <int D, int TM>
-__device__ __forceinline__ void mma_rows_codes(const uint4 *__restrict__ pi_frag, const __half *ka, const float *ysc,
-                                               const float *zsc, int *flag, const unsigned char *binb, bool binbad,
-                                               const float *thr, int kb, uint8_t *codes, int cs)
+// All of a lane's 32 codes are decided before any is stored, so that the table
+// lookups are not ordered behind the stores; each pair of adjacent columns is one
+// 16-bit store.
+template <bool BINS, int D, int TM>
+__device__ __forceinline__ void codes_from_acc(const float (&acc)[TM / 16][D / 64][4], const float *ysc,
+                                               const float *zsc, int *flag, const unsigned char *__restrict__ binb,
+                                               const float *__restrict__ thr, int kb, uint8_t *codes, int cs)
 {
-    constexpr int KS = D / 16, NPW = D / 64, MTS = TM / 16, KA = D + 8;
+    constexpr int NPW = D / 64, MTS = TM / 16;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = lane >> 2, q = lane & 3;
-    float acc[MTS][NPW][4];
-#pragma unroll
-    for (int m = 0; m < MTS; ++m)
-#pragma unroll
-        for (int n = 0; n < NPW; ++n) acc[m][n][0] = acc[m][n][1] = acc[m][n][2] = acc[m][n][3] = 0.f;
-    const uint32_t kab = static_cast<uint32_t>(__cvta_generic_to_shared(ka));
-#pragma unroll 2
-    for (int s = 0; s < KS; ++s) {
-        uint4 bf[NPW];
-#pragma unroll
-        for (int n = 0; n < NPW; ++n) bf[n] = __ldg(pi_frag + ((warp * NPW + n) * KS + s) * 32 + lane);
-#pragma unroll
-        for (int m = 0; m < MTS; ++m) {
-            uint32_t a0, a1, a2, a3;
-            const uint32_t addr = kab + 2u * ((16 * m + (lane & 15)) * KA + 16 * s + 8 * (lane >> 4));
-            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(addr));
-#pragma unroll
-            for (int n = 0; n < NPW; ++n) {
-                mma16816_f16(acc[m][n], a0, a1, a2, a3, bf[n].z, bf[n].w);  // low parts first
-                mma16816_f16(acc[m][n], a0, a1, a2, a3, bf[n].x, bf[n].y);
-            }
-        }
-    }
+    uint32_t pair[MTS][2][NPW];
+    bool marked[MTS][2];
 #pragma unroll
     for (int m = 0; m < MTS; ++m)
 #pragma unroll
@@ -360,16 +400,16 @@ __device__ __forceinline__ void mma_rows_codes(const uint4 *__restrict__ pi_frag
             const int row = 16 * m + r + 8 * h2;
             const float ys = ysc[row], zs = zsc[row];
             const int fl = flag[row];
-            bool marked = false;
+            marked[m][h2] = false;
 #pragma unroll
-            for (int n = 0; n < NPW; ++n)
+            for (int n = 0; n < NPW; ++n) {
+                uint32_t pr = 0u;
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int col = 8 * (warp * NPW + n) + 2 * q + e;
                     const float z = (acc[m][n][2 * h2 + e] * ys) * zs;
                     bool near;
                     int code;
-                    if (!binbad) {
+                    if constexpr (BINS) {
                         code = bin_code(z, binb, near);
                     } else {
                         code = 0;
@@ -378,11 +418,73 @@ __device__ __forceinline__ void mma_rows_codes(const uint4 *__restrict__ pi_frag
                         near = fminf(z - thr[code], thr[code + 1] - z) < kCodeGuard;
                     }
                     const bool mark = (fl == 0 || fl == 3) && near;
-                    marked |= mark;
-                    codes[row * cs + col] = static_cast<uint8_t>((fl == 2 ? 0 : code) | (mark ? 0x80 : 0));
+                    marked[m][h2] |= mark;
+                    pr |= static_cast<uint32_t>((fl == 2 ? 0 : code) | (mark ? 0x80 : 0)) << (8 * e);
                 }
-            if (marked) flag[row] = 3;
+                pair[m][h2][n] = pr;
+            }
         }
+#pragma unroll
+    for (int m = 0; m < MTS; ++m)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int row = 16 * m + r + 8 * h2;
+#pragma unroll
+            for (int n = 0; n < NPW; ++n)
+                *reinterpret_cast<uint16_t *>(codes + row * cs + 8 * (warp * NPW + n) + 2 * q) =
+                    static_cast<uint16_t>(pair[m][h2][n]);
+            if (marked[m][h2]) flag[row] = 3;
+        }
+}
+
+// The dense rotation with the codes decided in the epilogue (codes_from_acc), for
+// keys without QJL: no residual is needed, so Pi k never goes to shared memory.
+template <int D, int TM>
+__device__ __forceinline__ void mma_rows_codes(const uint4 *__restrict__ pi_frag, const __half *ka, const float *ysc,
+                                               const float *zsc, int *flag, const unsigned char *binb, bool binbad,
+                                               const float *thr, int kb, uint8_t *codes, int cs)
+{
+    constexpr int KS = D / 16, NPW = D / 64, MTS = TM / 16, KA = D + 8;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float acc[MTS][NPW][4];
+#pragma unroll
+    for (int m = 0; m < MTS; ++m)
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) acc[m][n][0] = acc[m][n][1] = acc[m][n][2] = acc[m][n][3] = 0.f;
+    const uint32_t kab = static_cast<uint32_t>(__cvta_generic_to_shared(ka));
+    // B fragments one k-step ahead; all low-part MMAs of a step before the high parts,
+    // so that the two products into one accumulator are MTS * NPW issues apart
+    uint4 bf[NPW];
+#pragma unroll
+    for (int n = 0; n < NPW; ++n) bf[n] = __ldg(pi_frag + ((warp * NPW + n) * KS) * 32 + lane);
+#pragma unroll 2
+    for (int s = 0; s < KS; ++s) {
+        uint4 bn[NPW];
+        const int sn = s + 1 < KS ? s + 1 : s;
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) bn[n] = __ldg(pi_frag + ((warp * NPW + n) * KS + sn) * 32 + lane);
+        uint32_t a[MTS][4];
+#pragma unroll
+        for (int m = 0; m < MTS; ++m) {
+            const uint32_t addr = kab + 2u * ((16 * m + (lane & 15)) * KA + 16 * s + 8 * (lane >> 4));
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(a[m][0]), "=r"(a[m][1]), "=r"(a[m][2]), "=r"(a[m][3]) : "r"(addr));
+        }
+#pragma unroll
+        for (int m = 0; m < MTS; ++m)
+#pragma unroll
+            for (int n = 0; n < NPW; ++n)  // low parts first
+                mma16816_f16(acc[m][n], a[m][0], a[m][1], a[m][2], a[m][3], bf[n].z, bf[n].w);
+#pragma unroll
+        for (int m = 0; m < MTS; ++m)
+#pragma unroll
+            for (int n = 0; n < NPW; ++n)
+                mma16816_f16(acc[m][n], a[m][0], a[m][1], a[m][2], a[m][3], bf[n].x, bf[n].y);
+#pragma unroll
+        for (int n = 0; n < NPW; ++n) bf[n] = bn[n];
+    }
+    if (!binbad) codes_from_acc<true, D, TM>(acc, ysc, zsc, flag, binb, thr, kb, codes, cs);
+    else codes_from_acc<false, D, TM>(acc, ysc, zsc, flag, binb, thr, kb, codes, cs);
 }
 
 // Hadamard rotation of TM rows (turbo-attn, "How it works", step 1):
@@ -589,6 +691,35 @@ __device__ __noinline__ bool refine_marked_codes(const float *__restrict__ Pi, c
     return changed;
 }
 
+// The group-quantised value rows warp + kWarps k (k < TM / kWarps) of a CTA, read
+// from the bf16 stage in shared memory (row stride D), one row at a time per warp
+// (four rows in flight per warp ran 30% slower); lane l holds elements 8 l .. 8 l + 7.
+template <int D, int TM, int VB>
+__device__ __forceinline__ void quantize_value_rows(const unsigned char *vstage, const int64_t *s_dst, const int *s_off,
+                                                    uint8_t *vc, const PageGeom &G, const Codec &C)
+{
+    constexpr int E = D / 32;
+    static_assert(E == 8, "group-quantised values in this kernel: head dim 256");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lpg = C.group / E;  // lanes per group
+#pragma unroll 1
+    for (int row = warp; row < TM; row += kWarps) {
+        const int64_t dst = s_dst[row];
+        if (dst < 0) continue;
+        const uint4 u = *reinterpret_cast<const uint4 *>(vstage + (row * D + lane * E) * 2);
+        const uint32_t w[E / 2] = {u.x, u.y, u.z, u.w};
+        float x[E];
+        unpack_bf16<E>(w, x);
+        uint32_t vw;
+        const uint32_t meta = quantize_values_lane<E, VB>(x, lpg, vw);
+        uint8_t *vrec = vc + dst * G.v_page;
+        const int64_t off = s_off[row];
+        store_code_bytes(vrec + off * C.v_code_bytes + VB * lane, vw, VB);
+        if ((lane & (lpg - 1)) == 0)
+            *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + off * C.v_meta_bytes + 4 * (lane / lpg)) = meta;
+    }
+}
+
 template <int D, bool HAD, bool VMSE>
 __global__ void __launch_bounds__(kThreads, 2)
 compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
@@ -619,33 +750,61 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * TM;
+    // row r0 + i is token t0 + (h0 + i) / Hkv, head (h0 + i) % Hkv: one 64-bit division
+    const int64_t t0 = r0 / Hkv;
+    const int h0 = static_cast<int>(r0 - t0 * Hkv);
     const float sqrtd = sqrtf(static_cast<float>(D));
     const int nthr = (1 << C.k_bits) - 1;
     if (tid < 18) s_thr[tid] = tid == 0 ? -INFINITY : (tid <= nthr ? C.thresholds[tid - 1] : INFINITY);
     if (tid < 16) s_cent[tid] = C.centroids[tid];
 
-    if (tid < TM) {
-        const int64_t r = r0 + tid;
-        int64_t dst = -1;
-        int off = 0;
-        if (r < rows) {
-            const int64_t t = r / Hkv;
-            s_tok[tid] = t;
-            const int h = static_cast<int>(r - t * Hkv);
-            const int64_t s = slots[t];
-            if (s >= 0) {
-                if (s < num_blocks * G.P) {
-                    const int64_t blk = s / G.P;
-                    off = static_cast<int>(s - blk * G.P);
-                    dst = blk * Hkv + h;
+    // the rows' slots are requested now and turned into page and offset just before
+    // the rotation, so that their latency overlaps the key loads and the bin table
+    int64_t slot = -1;  // rows past the end keep -1
+    if (tid < TM && r0 + tid < rows) {
+        const int64_t t = t0 + (h0 + tid) / Hkv;
+        s_tok[tid] = t;
+        slot = slots[t];
+    }
+    // Each warp's key rows (dense rotation: the lane's E contiguous elements) are
+    // loaded now, and without QJL the value rows are copied into yb's upper half (free
+    // until the pack loop), so that their latency overlaps the slot loads and the bin
+    // table.  With QJL the values are copied once the residuals are in registers.
+    constexpr int E = D / 32, RPW = TM / kWarps;
+    uint32_t kraw[RPW][E / 2];
+    if constexpr (!HAD) {
+#pragma unroll
+        for (int k = 0; k < RPW; ++k) {
+            const int row = warp + kWarps * k;
+#pragma unroll
+            for (int i = 0; i < E / 2; ++i) kraw[k][i] = 0u;
+            if (r0 + row < rows) {
+                const int q = (h0 + row) / Hkv;
+                const uint16_t *src = kin + (t0 + q) * ks + static_cast<int64_t>(h0 + row - q * Hkv) * D + lane * E;
+                if constexpr (E == 8) {
+                    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src));
+                    kraw[k][0] = u.x; kraw[k][1] = u.y; kraw[k][2] = u.z; kraw[k][3] = u.w;
                 } else {
-                    atomicOr(C.status, TQ_DEVERR_SLOT_RANGE);
+                    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(src));
+                    kraw[k][0] = u.x; kraw[k][1] = u.y;
                 }
             }
         }
-        s_dst[tid] = dst;
-        s_off[tid] = off;
     }
+    unsigned char *vstage = reinterpret_cast<unsigned char *>(yb) + SM::kKa;  // TM rows of D bf16 values
+    auto stage_values = [&]() {
+        for (int e = tid; e < TM * (D / 8); e += kThreads) {
+            const int row = e / (D / 8), c8 = e - row * (D / 8);
+            if (r0 + row < rows) {
+                const int q = (h0 + row) / Hkv;
+                cp_async16(vstage + (row * D + c8 * 8) * 2,
+                           vin + (t0 + q) * vs + static_cast<int64_t>(h0 + row - q * Hkv) * D + c8 * 8);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    const bool fused = !HAD && !C.qjl;
+    if (!VMSE && fused) stage_values();
     // the key codebook's bin table; the barrier also publishes the rows' tokens
     const unsigned char *binb = reinterpret_cast<const unsigned char *>(s_bins) + 8 * (lane % kBinCopies);
     bool binbad = __syncthreads_or(build_code_bins(s_bins, C.thresholds, nthr));
@@ -671,21 +830,15 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     }
     // ---- norms; rows with an extreme range take the exact path; dense rotation:
     // the keys go straight from bf16 into the fp16 operand (exact after the row scale) ----
-    for (int row = warp; row < TM; row += kWarps) {
-        constexpr int E = D / 32;
-        float x[E];
+#pragma unroll
+    for (int k = 0; k < RPW; ++k) {
+        const int row = warp + kWarps * k;
+        float x[E];  // HAD: elements lane + 32 m; dense: elements E lane + m
         if constexpr (HAD) {
 #pragma unroll
             for (int m = 0; m < E; ++m) x[m] = kf[row * RS + lane + 32 * m];
         } else {
-            const int64_t r = r0 + row;
-            const uint16_t *src = nullptr;
-            if (r < rows) {
-                const int64_t t = s_tok[row];
-                src = kin + t * ks + (r - t * Hkv) * D;
-            }
-#pragma unroll
-            for (int m = 0; m < E; ++m) x[m] = src ? bf16_to_float(src[lane + 32 * m]) : 0.f;
+            unpack_bf16<E>(kraw[k], x);
         }
         float ss = 0.f, mx = 0.f;
 #pragma unroll
@@ -710,14 +863,36 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             const bool ok = mx >= 0x1p-30f && mx <= 0x1p30f;
             const int ex = ok ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 126 : 0;
             const float sc = ok ? __uint_as_float(static_cast<uint32_t>(127 + 15 - ex) << 23) : 0.f;
+            uint32_t h2[E / 2];
 #pragma unroll
-            for (int m = 0; m < E; ++m) ka[row * (D + 8) + lane + 32 * m] = __float2half_rn(x[m] * sc);
+            for (int i = 0; i < E / 2; ++i) {
+                const __half2 h = __floats2half2_rn(x[2 * i] * sc, x[2 * i + 1] * sc);
+                h2[i] = *reinterpret_cast<const uint32_t *>(&h);
+            }
+            if constexpr (E == 8)
+                *reinterpret_cast<uint4 *>(ka + row * (D + 8) + lane * E) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+            else
+                *reinterpret_cast<uint2 *>(ka + row * (D + 8) + lane * E) = make_uint2(h2[0], h2[1]);
             if (lane == 0) s_ysc[row] = ok ? __uint_as_float(static_cast<uint32_t>(127 + ex - 25) << 23) : 0.f;
         }
     }
+    if (tid < TM) {
+        int64_t dst = -1;
+        int off = 0;
+        if (slot >= 0) {
+            if (slot < num_blocks * G.P) {
+                const int64_t blk = slot / G.P;
+                off = static_cast<int>(slot - blk * G.P);
+                dst = blk * Hkv + (h0 + tid) % Hkv;
+            } else {
+                atomicOr(C.status, TQ_DEVERR_SLOT_RANGE);
+            }
+        }
+        s_dst[tid] = dst;  // published by the barrier after the rotation
+        s_off[tid] = off;
+    }
     // ---- rotation: yb = Pi k (unnormalised); without QJL the codes come straight
     // from the accumulators ---------------------------------------------------
-    const bool fused = !HAD && !C.qjl;
     if constexpr (HAD) {
         fwht_rows<D, TM>(C.hsign, kf, yb);
     } else {
@@ -756,11 +931,12 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         if (mark) s_flag[row] = 3;
     }
     __syncthreads();
+    if (!VMSE && !fused && !C.qjl) stage_values();  // yb's residuals are not read without QJL
     // ---- QJL: p = S r, gamma, sign guard ---------------------------------------
     if (C.qjl) {
         // the residuals as fp16 high + low parts times a power of two per row (high in
         // ka, low over yb once every row is in registers), then p = S r on mma.sync
-        constexpr int E = D / 32, RPW = TM / kWarps, KA = D + 8;
+        constexpr int KA = D + 8;
         float rv[RPW][E];
 #pragma unroll
         for (int k = 0; k < RPW; ++k) {
@@ -784,6 +960,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             }
         }
         __syncthreads();  // every residual is in registers; row scales published
+        if (!VMSE) stage_values();  // the low parts below fill yb's lower half only
         __half *klo = reinterpret_cast<__half *>(yb);
 #pragma unroll
         for (int k = 0; k < RPW; ++k) {
@@ -819,9 +996,8 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     for (int row = warp; row < TM; row += kWarps) {
         int fl = s_flag[row];
         if ((fl != 1 && fl != 3) || s_dst[row] < 0) continue;
-        const int64_t r = r0 + row;
-        const int64_t t = r / Hkv;
-        const int h = static_cast<int>(r - t * Hkv);
+        const int64_t t = s_tok[row];  // a row with a slot has a token
+        const int h = static_cast<int>(r0 + row - t * Hkv);
         if (fl == 3) {
             const bool changed = refine_marked_codes<D>(C.Pi, kin + t * ks + static_cast<int64_t>(h) * D,
                                                         codes + row * CS, C.thresholds, (1 << C.k_bits) - 1);
@@ -831,19 +1007,17 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
                            scratch + warp * D, &s_n16[row], &s_g16[row], C.thresholds, C.centroids, C.k_bits,
                            C.qjl != 0);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    // ---- pack and store: one warp per row ------------------------------------
+    // ---- pack and store: code words by the whole CTA, then per row its sign
+    // bits, gamma and norm, then (group-quantised values) the value rows ---------
+    store_code_words<D, TM>(codes, CS, C.k_bits, s_dst, s_off, s_flag, kc, G.k_page, C.k_code_bytes);
     for (int row = warp; row < TM; row += kWarps) {
         const int64_t dst = s_dst[row];
         if (dst < 0) continue;
         const int off = s_off[row];
         const bool zero = (s_flag[row] == 2);
         uint8_t *krec = kc + dst * G.k_page;
-        const int nw = D * C.k_bits / 32;
-        if (lane < nw) {
-            const uint32_t w = zero ? 0u : pack_word(codes + row * CS, lane, C.k_bits);
-            *reinterpret_cast<uint32_t *>(krec + static_cast<int64_t>(off) * C.k_code_bytes + 4 * lane) = w;
-        }
         if (C.qjl) {
 #pragma unroll
             for (int w = 0; w < D / 32; ++w) {
@@ -856,90 +1030,11 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * off) = zero ? 0 : s_g16[row];
         }
         if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * off) = zero ? 0 : s_n16[row];
-        if constexpr (VMSE) continue;  // values take the codebook pass below
-
-        // ---- value row -------------------------------------------------------
-        constexpr int E = D / 32;
-        const int64_t r = r0 + row;
-        const int64_t t = r / Hkv;
-        const int h = static_cast<int>(r - t * Hkv);
-        const uint16_t *vsrc = vin + t * vs + static_cast<int64_t>(h) * D + lane * E;
-        float x[E];
-        if constexpr (E == 4) {
-            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(vsrc));
-            x[0] = bf16_to_float(u.x & 0xffffu); x[1] = bf16_to_float(u.x >> 16);
-            x[2] = bf16_to_float(u.y & 0xffffu); x[3] = bf16_to_float(u.y >> 16);
-        } else {
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(vsrc));
-            x[0] = bf16_to_float(u.x & 0xffffu); x[1] = bf16_to_float(u.x >> 16);
-            x[2] = bf16_to_float(u.y & 0xffffu); x[3] = bf16_to_float(u.y >> 16);
-            x[4] = bf16_to_float(u.z & 0xffffu); x[5] = bf16_to_float(u.z >> 16);
-            x[6] = bf16_to_float(u.w & 0xffffu); x[7] = bf16_to_float(u.w >> 16);
-        }
-        const int lpg = C.group / E;  // lanes per group
-        if constexpr (E == 8) {
-            // the lane's 8 codes are VB whole bytes: one fused multiply-add per element with
-            // an exact decision near ties (as in the streaming kernel)
-            uint32_t vw = 0u, meta = 0u;
-            const int vb = C.v_bits;
-            if (vb == 2) meta = quantize_values_lane<8, 2>(x, lpg, vw);
-            else if (vb == 3) meta = quantize_values_lane<8, 3>(x, lpg, vw);
-            else meta = quantize_values_lane<8, 4>(x, lpg, vw);
-            uint8_t *vrec = vc + dst * G.v_page;
-            store_code_bytes(vrec + static_cast<int64_t>(off) * C.v_code_bytes + vb * lane, vw, vb);
-            if ((lane & (lpg - 1)) == 0)
-                *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + static_cast<int64_t>(off) * C.v_meta_bytes +
-                                              4 * (lane / lpg)) = meta;
-            continue;
-        }
-        float mn = x[0], mxv = x[0];
-#pragma unroll
-        for (int m = 1; m < E; ++m) { mn = fminf(mn, x[m]); mxv = fmaxf(mxv, x[m]); }
-        for (int o = lpg >> 1; o > 0; o >>= 1) {
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-            mxv = fmaxf(mxv, __shfl_xor_sync(0xffffffffu, mxv, o));
-        }
-        const int L = (1 << C.v_bits) - 1;
-        float dh, de;
-        two_sum(mxv, -mn, dh, de);
-        // (max - min) / L with L in {3, 7, 15} is either exact in fp32 or a
-        // non-terminating binary fraction, so rounding it to fp32 first never
-        // lands on an fp16 rounding midpoint: one rounding to fp16 results.
-        const __half s16 = (de == 0.f) ? __float2half_rn(__fdiv_rn(dh, static_cast<float>(L)))
-                                       : __double2half((static_cast<double>(mxv) - static_cast<double>(mn)) / L);
-        const __half z16 = __float2half_rn(mn);
-        const float sv = __half2float(s16), zv = __half2float(z16);
-        uint8_t *vcodes = codes + row * CS;  // key codes of this row are already packed
-        __syncwarp();
-#pragma unroll
-        for (int m = 0; m < E; ++m) {
-            int q = 0;
-            if (sv != 0.f) {
-                // x - z exactly as a + ea; the code counts midpoints (j + 1/2) s <= x - z.
-                float a, ea;
-                two_sum(x[m], -zv, a, ea);
-                const float qf = floorf(__fdiv_rn(a, sv) + 0.5f);
-                q = static_cast<int>(fminf(fmaxf(qf, 0.f), static_cast<float>(L)));  // NaN -> 0
-                // exact fix-up of the guess against the midpoints
-                while (q < L && __fadd_rn(__fsub_rn(a, (q + 0.5f) * sv), ea) >= 0.f) ++q;
-                while (q > 0 && !(__fadd_rn(__fsub_rn(a, (q - 0.5f) * sv), ea) >= 0.f)) --q;
-            }
-            vcodes[lane * E + m] = static_cast<uint8_t>(q);
-        }
-        __syncwarp();
-        uint8_t *vrec = vc + dst * G.v_page;
-        const int nvw = D * C.v_bits / 32;
-        if (lane < nvw)
-            *reinterpret_cast<uint32_t *>(vrec + static_cast<int64_t>(off) * C.v_code_bytes + 4 * lane) =
-                pack_word(vcodes, lane, C.v_bits);
-        if ((lane % lpg) == 0) {
-            const int gi = lane / lpg;
-            const uint32_t meta = static_cast<uint32_t>(__half_as_ushort(s16)) |
-                                  (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
-            *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + static_cast<int64_t>(off) * C.v_meta_bytes + 4 * gi) =
-                meta;
-        }
-        __syncwarp();
+    }
+    if constexpr (!VMSE) {
+        if (C.v_bits == 2) quantize_value_rows<D, TM, 2>(vstage, s_dst, s_off, vc, G, C);
+        else if (C.v_bits == 3) quantize_value_rows<D, TM, 3>(vstage, s_dst, s_off, vc, G, C);
+        else quantize_value_rows<D, TM, 4>(vstage, s_dst, s_off, vc, G, C);
     }
     if constexpr (VMSE) {
         // ==== values coded like keys without QJL (brightcoding blog, "What is
@@ -1015,9 +1110,8 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         for (int row = warp; row < TM; row += kWarps) {
             const int fl = s_flag[row];
             if ((fl != 1 && fl != 3) || s_dst[row] < 0) continue;
-            const int64_t r = r0 + row;
-            const int64_t t = r / Hkv;
-            const int h = static_cast<int>(r - t * Hkv);
+            const int64_t t = s_tok[row];
+            const int h = static_cast<int>(r0 + row - t * Hkv);
             if (fl == 3) {  // no QJL on values: the re-decided codes are final
                 refine_marked_codes<D>(C.Pi, vin + t * vs + static_cast<int64_t>(h) * D, codes + row * CS,
                                        C.vthresholds, (1 << C.v_bits) - 1);
@@ -1028,17 +1122,13 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
                                false);
         }
         __syncthreads();
-        for (int row = warp; row < TM; row += kWarps) {
+        store_code_words<D, TM>(codes, CS, C.v_bits, s_dst, s_off, s_flag, vc, G.v_page, C.v_code_bytes);
+        for (int row = tid; row < TM; row += kThreads) {
             const int64_t dst = s_dst[row];
             if (dst < 0) continue;
             const int off = s_off[row];
-            const bool zero = (s_flag[row] == 2);
-            uint8_t *vrec = vc + dst * G.v_page;
-            const int nw = D * C.v_bits / 32;
-            if (lane < nw)
-                *reinterpret_cast<uint32_t *>(vrec + static_cast<int64_t>(off) * C.v_code_bytes + 4 * lane) =
-                    zero ? 0u : pack_word(codes + row * CS, lane, C.v_bits);
-            if (lane == 0) *reinterpret_cast<uint16_t *>(vrec + G.v_meta_off + 2 * off) = zero ? 0 : s_n16[row];
+            *reinterpret_cast<uint16_t *>(vc + dst * G.v_page + G.v_meta_off + 2 * off) =
+                s_flag[row] == 2 ? 0 : s_n16[row];
         }
     }
 }
