@@ -158,47 +158,77 @@ __device__ __forceinline__ void store_code_bytes(uint8_t *p, uint32_t w, int nby
     }
 }
 
-// Word w of the LSB-first bitstream of b-bit codes held one per byte (bit 7 clear):
-// 4- and 2-bit codes fill whole bytes, so their words come from aligned 32-bit loads
-// and shifts; 3-bit codes take the generic bit loop.  `codes` is 4-byte aligned.
-__device__ __forceinline__ uint32_t code_word(const uint8_t *codes, int w, int b)
+// The B words of the LSB-first bitstream of 32 B-bit codes held one per byte (bit 7
+// clear) at c (4-byte aligned): 4 codes per 32-bit load, then shifts.
+template <int B>
+__device__ __forceinline__ void pack32_codes(const uint8_t *c, uint32_t (&w)[B])
 {
-    if (b == 4) {
-        const uint32_t lo = *reinterpret_cast<const uint32_t *>(codes + 8 * w);
-        const uint32_t hi = *reinterpret_cast<const uint32_t *>(codes + 8 * w + 4);
-        // bytes 0 and 2 of x | x >> 4 hold codes (0, 1) and (2, 3) as nibble pairs
-        return __byte_perm(lo | (lo >> 4), hi | (hi >> 4), 0x6420);
-    }
-    if (b == 2) {
-        uint32_t v = 0u;
+    uint32_t x[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t x = *reinterpret_cast<const uint32_t *>(codes + 16 * w + 4 * i);
-            const uint32_t t = x | (x >> 6);  // bits 0-3: codes 0, 1; bits 16-19: codes 2, 3
-            v |= ((t & 0xFu) | ((t >> 12) & 0xF0u)) << (8 * i);
+    for (int i = 0; i < 8; ++i) x[i] = *reinterpret_cast<const uint32_t *>(c + 4 * i);
+    if constexpr (B == 4) {
+        // bytes 0 and 2 of x | x >> 4 hold codes (0, 1) and (2, 3) as nibble pairs
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = __byte_perm(x[2 * j] | (x[2 * j] >> 4), x[2 * j + 1] | (x[2 * j + 1] >> 4), 0x6420);
+    } else if constexpr (B == 2) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            uint32_t v = 0u;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t t = x[4 * j + i] | (x[4 * j + i] >> 6);  // bits 0-3: codes 0, 1; 16-19: codes 2, 3
+                v |= ((t & 0xFu) | ((t >> 12) & 0xF0u)) << (8 * i);
+            }
+            w[j] = v;
         }
-        return v;
+    } else {
+        static_assert(B == 3, "code widths 2, 3 and 4");
+        // four codes -> one 12-bit chunk; chunk k sits at bit 12 k of the 96-bit stream
+        uint32_t t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            t[i] = (x[i] & 7u) | ((x[i] >> 5) & 0x38u) | ((x[i] >> 10) & 0x1C0u) | ((x[i] >> 15) & 0xE00u);
+        const uint64_t lo = static_cast<uint64_t>(t[0]) | (static_cast<uint64_t>(t[1]) << 12) |
+                            (static_cast<uint64_t>(t[2]) << 24) | (static_cast<uint64_t>(t[3]) << 36) |
+                            (static_cast<uint64_t>(t[4]) << 48) | (static_cast<uint64_t>(t[5]) << 60);
+        w[0] = static_cast<uint32_t>(lo);
+        w[1] = static_cast<uint32_t>(lo >> 32);
+        w[2] = (t[5] >> 4) | (t[6] << 8) | (t[7] << 20);
     }
-    return pack_word(codes, w, b);
 }
 
-// The b-bit code words of a CTA's TM rows (codes one per byte, row stride cs) stored
-// at each row's slot of its page, all threads of the CTA over rows x words; rows
-// without a slot are skipped and zero rows (flag 2) store zeros.
+// The B-bit code words of a CTA's TM rows (codes one per byte, row stride cs) stored
+// at each row's slot of its page, all threads of the CTA over rows x groups of 32
+// codes (B words each); rows without a slot are skipped and zero rows (flag 2) store
+// zeros.
+template <int D, int TM, int B>
+__device__ __forceinline__ void store_code_words_b(const uint8_t *codes, int cs, const int64_t *dst, const int *off,
+                                                   const int *flag, uint8_t *pool, int64_t page_bytes, int code_bytes)
+{
+    constexpr int NG = D / 32;
+    for (int e = threadIdx.x; e < TM * NG; e += blockDim.x) {
+        const int row = e / NG, g = e % NG;
+        const int64_t d = dst[row];
+        if (d < 0) continue;
+        uint32_t w[B];
+        pack32_codes<B>(codes + row * cs + 32 * g, w);
+        const bool zero = flag[row] == 2;
+        uint32_t *out = reinterpret_cast<uint32_t *>(pool + d * page_bytes + static_cast<int64_t>(off[row]) * code_bytes) +
+                        B * g;
+#pragma unroll
+        for (int j = 0; j < B; ++j) out[j] = zero ? 0u : w[j];
+    }
+}
+
 template <int D, int TM>
 __device__ __forceinline__ void store_code_words(const uint8_t *codes, int cs, int b, const int64_t *dst,
                                                  const int *off, const int *flag, uint8_t *pool, int64_t page_bytes,
                                                  int code_bytes)
 {
-    const int nw = D * b / 32;
-    for (int e = threadIdx.x; e < TM * nw; e += blockDim.x) {
-        const int row = e / nw, w = e - row * nw;
-        const int64_t d = dst[row];
-        if (d < 0) continue;
-        const uint32_t word = flag[row] == 2 ? 0u : code_word(codes + row * cs, w, b);
-        *reinterpret_cast<uint32_t *>(pool + d * page_bytes + static_cast<int64_t>(off[row]) * code_bytes + 4 * w) =
-            word;
-    }
+    if (b == 2) store_code_words_b<D, TM, 2>(codes, cs, dst, off, flag, pool, page_bytes, code_bytes);
+    else if (b == 3) store_code_words_b<D, TM, 3>(codes, cs, dst, off, flag, pool, page_bytes, code_bytes);
+    else store_code_words_b<D, TM, 4>(codes, cs, dst, off, flag, pool, page_bytes, code_bytes);
 }
 
 // One row of fp32 keys (exact bf16 values) staged as fp16 after the power-of-two
@@ -691,6 +721,62 @@ __device__ __noinline__ bool refine_marked_codes(const float *__restrict__ Pi, c
     return changed;
 }
 
+// Codes of TM rotated rows (yb, row stride rs; z = yb scale[row]) by the whole CTA:
+// the code from the bin table (BINS) or by binary search over thr (thr[c + 1] is
+// threshold c; the distance to the nearest threshold is to one of the two that
+// bracket z); a code inside the guard band of a threshold is marked (bit 7) and its
+// row flagged 3 (the exact pass re-decides just the marked codes); zero rows (flag
+// 2) get code 0.  With RESID the residual z - centroid (0 for zero rows) replaces
+// yb.  Each thread takes four elements at a time, all loaded before any store.
+template <bool BINS, bool RESID, int D, int TM>
+__device__ __forceinline__ void codes_and_residuals(float *yb, int rs, const float *scale, int *flag,
+                                                    const unsigned char *__restrict__ binb,
+                                                    const float *__restrict__ thr, const float *__restrict__ cent,
+                                                    int kb, uint8_t *codes, int cs)
+{
+    constexpr int PER = TM * D / kThreads;
+    static_assert(PER % 4 == 0, "four elements per thread at a time");
+#pragma unroll 1
+    for (int k0 = 0; k0 < PER; k0 += 4) {
+        int row[4], col[4], fl[4], code[4];
+        float z[4];
+        bool near[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = threadIdx.x + kThreads * (k0 + j);
+            row[j] = e / D;
+            col[j] = e - row[j] * D;
+            fl[j] = flag[row[j]];
+            z[j] = yb[row[j] * rs + col[j]] * scale[row[j]];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if constexpr (BINS) {
+                code[j] = bin_code(z[j], binb, near[j]);
+            } else {
+                int c = 0;
+                for (int step = 1 << (kb - 1); step > 0; step >>= 1)
+                    if (thr[c + step] <= z[j]) c += step;
+                near[j] = fminf(z[j] - thr[c], thr[c + 1] - z[j]) < kCodeGuard;
+                code[j] = c;
+            }
+            if (fl[j] == 2) code[j] = 0;
+        }
+        float r[4];
+        if constexpr (RESID) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) r[j] = (fl[j] == 2) ? 0.f : z[j] - cent[code[j]];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool mark = (fl[j] == 0 || fl[j] == 3) && near[j];
+            codes[row[j] * cs + col[j]] = static_cast<uint8_t>(code[j] | (mark ? 0x80 : 0));
+            if constexpr (RESID) yb[row[j] * rs + col[j]] = r[j];
+            if (mark) flag[row[j]] = 3;
+        }
+    }
+}
+
 // The group-quantised value rows warp + kWarps k (k < TM / kWarps) of a CTA, read
 // from the bf16 stage in shared memory (row stride D), one row at a time per warp
 // (four rows in flight per warp ran 30% slower); lane l holds elements 8 l .. 8 l + 7.
@@ -903,35 +989,23 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             mma_rows<D, TM>(C.pi_frag, ka, s_ysc, yb);
     }
     __syncthreads();
-    // ---- codes, guard band, residual -----------------------------------------
-    // code = #{t : threshold_t <= z} by a binary search over the sorted thresholds
-    // (s_thr[c + 1] is threshold c); the distance to the nearest threshold is to
-    // one of the two that bracket z
-    const int kb = C.k_bits;
-    for (int e = fused ? TM * D : tid; e < TM * D; e += kThreads) {
-        const int row = e / D, i = e - row * D;
-        const int fl = s_flag[row];
-        const float z = yb[row * RS + i] * s_scale[row];
-        bool near;
-        int code;
-        if (!binbad) {
-            code = bin_code(z, binb, near);
+    // ---- codes, guard band, residual (the residual only for QJL) ---------------
+    if (!fused) {
+        if (C.qjl) {
+            if (!binbad)
+                codes_and_residuals<true, true, D, TM>(yb, RS, s_scale, s_flag, binb, s_thr, s_cent, C.k_bits, codes, CS);
+            else
+                codes_and_residuals<false, true, D, TM>(yb, RS, s_scale, s_flag, binb, s_thr, s_cent, C.k_bits, codes, CS);
         } else {
-            code = 0;
-            for (int step = 1 << (kb - 1); step > 0; step >>= 1)
-                if (s_thr[code + step] <= z) code += step;
-            near = fminf(z - s_thr[code], s_thr[code + 1] - z) < kCodeGuard;
+            if (!binbad)
+                codes_and_residuals<true, false, D, TM>(yb, RS, s_scale, s_flag, binb, s_thr, s_cent, C.k_bits, codes, CS);
+            else
+                codes_and_residuals<false, false, D, TM>(yb, RS, s_scale, s_flag, binb, s_thr, s_cent, C.k_bits, codes,
+                                                         CS);
         }
-        if (fl == 2) code = 0;
-        // a code inside the guard band of a threshold is marked (0x80) and its row
-        // flagged 3: the exact pass re-decides just the marked codes
-        const bool mark = (fl == 0 || fl == 3) && near;
-        codes[row * CS + i] = static_cast<uint8_t>(code | (mark ? 0x80 : 0));
-        yb[row * RS + i] = (fl == 2) ? 0.f : z - s_cent[code];
-        if (mark) s_flag[row] = 3;
     }
     __syncthreads();
-    if (!VMSE && !fused && !C.qjl) stage_values();  // yb's residuals are not read without QJL
+    if (!VMSE && !fused && !C.qjl) stage_values();  // yb holds no residuals without QJL
     // ---- QJL: p = S r, gamma, sign guard ---------------------------------------
     if (C.qjl) {
         // the residuals as fp16 high + low parts times a power of two per row (high in
@@ -1087,25 +1161,10 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             mma_rows<D, TM>(C.pi_frag, ka, s_ysc, yb);
         }
         __syncthreads();
-        const int vb = C.v_bits;
-        for (int e = tid; e < TM * D; e += kThreads) {
-            const int row = e / D, i = e - row * D;
-            const int fl = s_flag[row];
-            const float z = yb[row * RS + i] * s_scale[row];
-            bool near;
-            int code;
-            if (!binbad) {
-                code = bin_code(z, binb, near);
-            } else {
-                code = 0;
-                for (int step = 1 << (vb - 1); step > 0; step >>= 1)
-                    if (s_thr[code + step] <= z) code += step;
-                near = fminf(z - s_thr[code], s_thr[code + 1] - z) < kCodeGuard;
-            }
-            const bool mark = (fl == 0 || fl == 3) && near;
-            codes[row * CS + i] = static_cast<uint8_t>((fl == 2 ? 0 : code) | (mark ? 0x80 : 0));
-            if (mark) s_flag[row] = 3;
-        }
+        if (!binbad)
+            codes_and_residuals<true, false, D, TM>(yb, RS, s_scale, s_flag, binb, s_thr, s_cent, C.v_bits, codes, CS);
+        else
+            codes_and_residuals<false, false, D, TM>(yb, RS, s_scale, s_flag, binb, s_thr, s_cent, C.v_bits, codes, CS);
         __syncthreads();
         for (int row = warp; row < TM; row += kWarps) {
             const int fl = s_flag[row];
