@@ -254,28 +254,26 @@ __device__ __forceinline__ void decode_keys(const KeyItem &ki, uint32_t lut, uin
         }
         off[k] = umma::core_offset(t, 8 * c, D);
     }
+    // every table lookup before any store (the shared-memory accesses are volatile, so
+    // a store would hold back the next item's lookups); the codes of an invalid page
+    // are masked into the table like any others and their entries replaced by zeros
+    uint2 e[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) e[k][m] = lds64(lut + ((w[k] >> (2 * KB * m)) & PM) * (8 * CP));
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = hv;
-        if (tv[k]) {
-            const uint2 e0 = lds64(lut + (w[k] & PM) * (8 * CP)), e1 = lds64(lut + ((w[k] >> (2 * KB)) & PM) * (8 * CP));
-            const uint2 e2 = lds64(lut + ((w[k] >> (4 * KB)) & PM) * (8 * CP));
-            const uint2 e3 = lds64(lut + ((w[k] >> (6 * KB)) & PM) * (8 * CP));
-            hv = make_uint4(e0.x, e1.x, e2.x, e3.x);
-            lv = make_uint4(e0.y, e1.y, e2.y, e3.y);
-        }
+        const uint4 hv = tv[k] ? make_uint4(e[k][0].x, e[k][1].x, e[k][2].x, e[k][3].x) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 lv = tv[k] ? make_uint4(e[k][0].y, e[k][1].y, e[k][2].y, e[k][3].y) : make_uint4(0u, 0u, 0u, 0u);
         sts128(kh + off[k], hv);
         sts128(kl + off[k], lv);
         if constexpr (QJL) {
-            uint4 sv = make_uint4(0u, 0u, 0u, 0u);
-            if (tv[k]) {
-                // fp16 2^8 g (exact: a bf16 times 2^8, g >= 0), sign bit set where the bit is 0
-                const uint32_t g2 = half2_bits(__float2half2_rn(bf16_to_float(g[k]) * kKScale));
-                const uint32_t nb = ~sb[k];
-                auto sg = [&](int m) { return g2 | (((nb >> (2 * m)) & 1u) << 15) | (((nb >> (2 * m + 1)) & 1u) << 31); };
-                sv = make_uint4(sg(0), sg(1), sg(2), sg(3));
-            }
-            sts128(ksg + off[k], sv);
+            // fp16 2^8 g (exact: a bf16 times 2^8, g >= 0), sign bit set where the bit is 0
+            const uint32_t g2 = tv[k] ? half2_bits(__float2half2_rn(bf16_to_float(g[k]) * kKScale)) : 0u;
+            const uint32_t nb = tv[k] ? ~sb[k] : 0u;
+            auto sg = [&](int m) { return g2 | (((nb >> (2 * m)) & 1u) << 15) | (((nb >> (2 * m + 1)) & 1u) << 31); };
+            sts128(ksg + off[k], make_uint4(sg(0), sg(1), sg(2), sg(3)));
         }
     }
 }
