@@ -766,11 +766,12 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 }
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                int ex = 0;
-                if (mx > 0.f) frexpf(mx, &ex);  // mx in [2^(ex-1), 2^ex)
+                // mx in [2^(ex-1), 2^ex) from its exponent field (a subnormal or zero mx
+                // gives ex = -126: tiny either way)
+                const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 126;
                 // |k'| < 2^15; keys too small for a finite fp32 scale are redone exactly
                 const bool tiny = (15 - ex) > 126;
-                const float sc = ldexpf(1.f, tiny ? 126 : 15 - ex);
+                const float sc = __uint_as_float(static_cast<uint32_t>(127 + (tiny ? 126 : 15 - ex)) << 23);
                 float ss = 0.f;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -803,7 +804,11 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                         if (tiny) ri.flag = 4;
                         const float nsc = sqrtf(ss);  // ||k|| 2^(15-ex)
                         ri.zscale = sqrtd / (nsc * 1024.f);
-                        ri.n16g16 = float_to_bf16_bits(ldexpf(nsc, ex - 15));
+                        // ||k|| = nsc / sc: one exact multiply by 2^(ex - 15), or 2^-126 for a
+                        // tiny key (whose row is redone exactly anyway)
+                        const float nk = tiny ? ldexpf(nsc, -126)
+                                              : nsc * __uint_as_float(static_cast<uint32_t>(112 + ex) << 23);
+                        ri.n16g16 = float_to_bf16_bits(nk);
                     }
                     rinfo[rl] = ri;
                 }
