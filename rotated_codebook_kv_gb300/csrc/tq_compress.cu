@@ -42,7 +42,10 @@ struct CompressSmem {
     static constexpr size_t kCodes = ((TM * kCodeStride + 15) / 16) * 16;
     static constexpr size_t kScratch = sizeof(double) * kWarps * D;
     static constexpr size_t kKa = sizeof(__half) * TM * (D + 8);  // fp16 keys for the tensor-core rotation
-    static constexpr size_t kBytes = kKf + kYb + kCodes + kScratch + kKa;
+    // MSE values at d = 128 (the only use of this kernel there): the bf16 value rows,
+    // copied at the start so that the value pass does not wait for them
+    static constexpr size_t kVs = D == 128 ? sizeof(uint16_t) * TM * D : 0;
+    static constexpr size_t kBytes = kKf + kYb + kCodes + kScratch + kKa + kVs;
 };
 
 constexpr int kStreamWarps = 8;
@@ -878,6 +881,8 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         }
     }
     unsigned char *vstage = reinterpret_cast<unsigned char *>(yb) + SM::kKa;  // TM rows of D bf16 values
+    unsigned char *vpre = smem_raw + SM::kKf + SM::kYb + SM::kCodes + SM::kScratch + SM::kKa;
+    if constexpr (VMSE && SM::kVs > 0) vstage = vpre;
     auto stage_values = [&]() {
         for (int e = tid; e < TM * (D / 8); e += kThreads) {
             const int row = e / (D / 8), c8 = e - row * (D / 8);
@@ -890,7 +895,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
     const bool fused = !HAD && !C.qjl;
-    if (!VMSE && fused) stage_values();
+    if ((!VMSE && fused) || (VMSE && SM::kVs > 0)) stage_values();
     // the key codebook's bin table; the barrier also publishes the rows' tokens
     const unsigned char *binb = reinterpret_cast<const unsigned char *>(s_bins) + 8 * (lane % kBinCopies);
     bool binbad = __syncthreads_or(build_code_bins(s_bins, C.thresholds, nthr));
@@ -1122,9 +1127,13 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             const int64_t r = r0 + row;
             uint4 u = make_uint4(0, 0, 0, 0);
             if (r < rows) {
-                const int64_t t = s_tok[row];
-                const int h = static_cast<int>(r - t * Hkv);
-                u = __ldg(reinterpret_cast<const uint4 *>(vin + t * vs + static_cast<int64_t>(h) * D) + c8);
+                if constexpr (SM::kVs > 0) {
+                    u = *reinterpret_cast<const uint4 *>(vpre + (row * D + c8 * 8) * 2);  // copied at the start
+                } else {
+                    const int64_t t = s_tok[row];
+                    const int h = static_cast<int>(r - t * Hkv);
+                    u = __ldg(reinterpret_cast<const uint4 *>(vin + t * vs + static_cast<int64_t>(h) * D) + c8);
+                }
             }
             *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8) =
                 make_float4(bf16_to_float(u.x & 0xffffu), bf16_to_float(u.x >> 16), bf16_to_float(u.y & 0xffffu),
