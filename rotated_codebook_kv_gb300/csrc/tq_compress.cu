@@ -42,10 +42,7 @@ struct CompressSmem {
     static constexpr size_t kCodes = ((TM * kCodeStride + 15) / 16) * 16;
     static constexpr size_t kScratch = sizeof(double) * kWarps * D;
     static constexpr size_t kKa = sizeof(__half) * TM * (D + 8);  // fp16 keys for the tensor-core rotation
-    // MSE values at d = 128 (the only use of this kernel there): the bf16 value rows,
-    // copied at the start so that the value pass does not wait for them
-    static constexpr size_t kVs = D == 128 ? sizeof(uint16_t) * TM * D : 0;
-    static constexpr size_t kBytes = kKf + kYb + kCodes + kScratch + kKa + kVs;
+    static constexpr size_t kBytes = kKf + kYb + kCodes + kScratch + kKa;
 };
 
 constexpr int kStreamWarps = 8;
@@ -881,8 +878,6 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         }
     }
     unsigned char *vstage = reinterpret_cast<unsigned char *>(yb) + SM::kKa;  // TM rows of D bf16 values
-    unsigned char *vpre = smem_raw + SM::kKf + SM::kYb + SM::kCodes + SM::kScratch + SM::kKa;
-    if constexpr (VMSE && SM::kVs > 0) vstage = vpre;
     auto stage_values = [&]() {
         for (int e = tid; e < TM * (D / 8); e += kThreads) {
             const int row = e / (D / 8), c8 = e - row * (D / 8);
@@ -895,7 +890,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
     const bool fused = !HAD && !C.qjl;
-    if ((!VMSE && fused) || (VMSE && SM::kVs > 0)) stage_values();
+    if (!VMSE && fused) stage_values();
     // the key codebook's bin table; the barrier also publishes the rows' tokens
     const unsigned char *binb = reinterpret_cast<const unsigned char *>(s_bins) + 8 * (lane % kBinCopies);
     bool binbad = __syncthreads_or(build_code_bins(s_bins, C.thresholds, nthr));
@@ -1127,13 +1122,9 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             const int64_t r = r0 + row;
             uint4 u = make_uint4(0, 0, 0, 0);
             if (r < rows) {
-                if constexpr (SM::kVs > 0) {
-                    u = *reinterpret_cast<const uint4 *>(vpre + (row * D + c8 * 8) * 2);  // copied at the start
-                } else {
-                    const int64_t t = s_tok[row];
-                    const int h = static_cast<int>(r - t * Hkv);
-                    u = __ldg(reinterpret_cast<const uint4 *>(vin + t * vs + static_cast<int64_t>(h) * D) + c8);
-                }
+                const int64_t t = s_tok[row];
+                const int h = static_cast<int>(r - t * Hkv);
+                u = __ldg(reinterpret_cast<const uint4 *>(vin + t * vs + static_cast<int64_t>(h) * D) + c8);
             }
             *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8) =
                 make_float4(bf16_to_float(u.x & 0xffffu), bf16_to_float(u.x >> 16), bf16_to_float(u.y & 0xffffu),
@@ -1443,11 +1434,29 @@ cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *
                             int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
                             int64_t num_blocks, cudaStream_t st)
 {
-    if (c.vmse) {  // values coded like keys: the two-pass SIMT kernel at either head dim
+    if (c.vmse && c.d == 128) {
+        // values coded like keys: an MSE value record is a key record without QJL (codes,
+        // then a bf16 norm per token), so the tensor-core kernel runs twice, on the keys
+        // and on the values through a codec whose key fields hold the value codebook
+        cudaError_t e = launch_compress_tc_keys(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, c.num_sms, st);
+        if (e != cudaSuccess) return e;
+        Codec cv = c;
+        cv.k_bits = c.v_bits;
+        cv.qjl = 0;
+        cv.k_code_bytes = c.v_code_bytes;
+        cv.k_sign_bytes = 0;
+        for (int i = 0; i < 16; ++i) {
+            cv.centroids[i] = c.vcentroids[i];
+            cv.thresholds[i] = c.vthresholds[i];
+        }
+        PageGeom gv = pg;
+        gv.k_page = pg.v_page;
+        gv.k_sign_off = gv.k_norm_off = pg.v_meta_off;
+        gv.k_gamma_off = pg.v_meta_off + 2LL * pg.P;  // not written without QJL
+        return launch_compress_tc_keys(cv, gv, v, T, Hkv, vs, slots, vc, num_blocks, c.num_sms, st);
+    }
+    if (c.vmse) {  // values coded like keys at head dim 256: the two-pass SIMT kernel
         const bool had = c.rotation == 1;
-        if (c.d == 128)
-            return had ? launch_compress_d<128, true, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st)
-                       : launch_compress_d<128, false, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
         return had ? launch_compress_d<256, true, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st)
                    : launch_compress_d<256, false, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
     }

@@ -684,7 +684,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
             // three row-info buffers: the epilogue may still finish tile it-2 while tile it is converted
             RowInfo *rinfo = rinfo_all + buf * TM;
             // keys and values of this CTA's next tile start streaming into L2 now
-            if (ptid < 2 && tile + static_cast<int>(gridDim.x) < num_tiles) {
+            if (ptid < (VB > 0 ? 2 : 1) && tile + static_cast<int>(gridDim.x) < num_tiles) {
                 const int64_t n0 = r0 + static_cast<int64_t>(gridDim.x) * TM;
                 const int64_t n1 = min(n0 + TM, rows);
                 const uint16_t *base = ptid == 0 ? kin : vin;
@@ -715,7 +715,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                     const uint4 *ksrc = reinterpret_cast<const uint4 *>(kin + t * ks + static_cast<int64_t>(h) * D);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) kr[p][j] = ld_pinned(ksrc + sub + 4 * j);
-                    if (p == 0) {
+                    if (VB > 0 && p == 0) {
                         const uint4 *vsrc = reinterpret_cast<const uint4 *>(vin + t * vs + static_cast<int64_t>(h) * D);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) va[j] = ld_pinned(vsrc + 4 * sub + j);
@@ -838,6 +838,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
                 }
             }
             // ---- values of this tile: pass p + 1 is loaded while pass p is quantised ----
+            if constexpr (VB > 0) {
             const int lpg = C.group >> 5;  // lanes per group: 1, 2 or 4
 #pragma unroll 1
             for (int p = 0; p < kPasses; ++p) {
@@ -875,6 +876,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
 #pragma unroll
                 for (int j = 0; j < 4; ++j) va[j] = vb[j];
             }
+            }  // VB > 0
         }
     } else {
         // =========================== epilogue ==================================
@@ -1105,6 +1107,17 @@ cudaError_t launch_tc_kb(const Codec &c, const PageGeom &pg, const uint16_t *k, 
 }  // namespace
 
 size_t compress_tc_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_compress_tc_keys(const Codec &c, const PageGeom &pg, const uint16_t *k, int64_t T, int Hkv,
+                                    int64_t ks, const int64_t *slots, uint8_t *kc, int64_t num_blocks, int num_sms,
+                                    cudaStream_t st)
+{
+    switch (c.k_bits) {
+    case 2: return launch_tc<2, 0>(c, pg, k, nullptr, T, Hkv, ks, 0, slots, kc, nullptr, num_blocks, num_sms, st);
+    case 3: return launch_tc<3, 0>(c, pg, k, nullptr, T, Hkv, ks, 0, slots, kc, nullptr, num_blocks, num_sms, st);
+    default: return launch_tc<4, 0>(c, pg, k, nullptr, T, Hkv, ks, 0, slots, kc, nullptr, num_blocks, num_sms, st);
+    }
+}
 
 cudaError_t launch_compress_tc(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
                                int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
