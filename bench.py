@@ -304,7 +304,9 @@ def run_gpu(args, rank, world, local_rank):
     c_gbs = c_bytes / c_time / 1e9
     d_gbs = d_bytes / d_time / 1e9
     traffic = committed_traffic("compress_kernel")
-    launches = args.steps * len(layers) * 4
+    # per layer: tq_compress_kv is one launch, two at head dim 128 without QJL (the
+    # keys-only tensor-core pass, then the value kernel); tq_decode_attention is three
+    launches = args.steps * sum((2 if (L.w.head_dim == 128 and L.w.k_bits == 4) else 1) + 3 for L in layers)
 
     # ---- end to end: host buffers, copies inside the timed region ------------
     # The next layer's inputs are copied on two copy streams while this layer is
@@ -384,7 +386,7 @@ def run_gpu(args, rank, world, local_rank):
         "decode_kv_tokens_per_s": round(world * sum(sum(L.seq_lens) * L.w.num_kv_heads for L in layers) / d_time, 1),
         "decode_query_tokens_per_s": round(world * w.batch * w.layers / d_time, 1),
         "roofline": {
-            "bound": "hbm", "kernel": "compress_tc_kernel (tq_compress_kv)",
+            "bound": "hbm", "kernel": "compress_tc_kernel (tq_compress_kv; 4-bit layers: its keys-only form + compress_values_tc_kernel)",
             "achieved": round(c_gbs, 1), "peak": peak, "peak_kind": f"of {peak_kind}",
             "unit": "GB/s", "frac": round(c_gbs / peak, 4),
             "traffic": None if traffic is None else traffic.get("bytes_per_launch"),

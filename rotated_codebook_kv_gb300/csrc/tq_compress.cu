@@ -1460,6 +1460,14 @@ cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *
         return had ? launch_compress_d<256, true, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st)
                    : launch_compress_d<256, false, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
     }
+    if (c.d == 128 && !c.qjl) {
+        // without QJL the keys-only tensor-core pass and a streaming value kernel beat the
+        // fused kernel, whose producers spend a third of its time on values; with QJL its
+        // epilogue sets the pace and the fused kernel stays ahead
+        cudaError_t e = launch_compress_tc_keys(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, c.num_sms, st);
+        if (e != cudaSuccess) return e;
+        return launch_compress_values_tc(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, c.num_sms, st);
+    }
     if (c.d == 128) return launch_compress_tc(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, c.num_sms, st);
     if (c.rotation == 1 && !c.qjl) {
         switch (c.v_bits) {

@@ -1077,6 +1077,85 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     if (warp == 0) umma::tmem_dealloc(tmem, 512);
 }
 
+// Group-quantised values alone (the keys taking the keys-only pass): the fused
+// kernel's value layout, four lanes per row, lane sub holding channels
+// [32 sub, 32 sub + 32), eight rows per warp; row octets strided over a one-wave grid
+// with the next octet's values and slots in flight while the current one is
+// quantised.  The loop bounds are the same for the whole warp, so the group
+// reductions' shuffles always run with every lane.
+template <int VB>
+__global__ void __launch_bounds__(256, 2)
+compress_values_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ vin, int64_t rows, int Hkv,
+                          int64_t vs, const int64_t *__restrict__ slots, uint8_t *__restrict__ vc, int64_t num_blocks)
+{
+    const int lane = threadIdx.x & 31, sub = lane & 3, rq = lane >> 2;
+    const int lpg = C.group >> 5;  // lanes per group: 1, 2 or 4
+    const int hshift = (Hkv & (Hkv - 1)) == 0 ? __ffs(Hkv) - 1 : -1;
+    const int pshift = __ffs(G.P) - 1;
+    const int64_t cache_slots = num_blocks * G.P;
+    const int64_t stride = 8 * static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    auto fetch = [&](int64_t r, uint4 (&w)[4], int64_t &sl) {
+        sl = -1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows) {
+            const int64_t t = hshift >= 0 ? (r >> hshift) : r / Hkv;
+            const uint4 *src = reinterpret_cast<const uint4 *>(vin + t * vs + (r - t * Hkv) * D);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w[j] = ld_pinned(src + 4 * sub + j);
+            sl = ld_pinned_s64(slots + t);
+        }
+    };
+    int64_t base = 8 * (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5));
+    uint4 wn[4];
+    int64_t sn;
+    fetch(base + rq, wn, sn);
+    for (; base < rows; base += stride) {
+        const int64_t r = base + rq;
+        uint4 w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = wn[j];
+        const int64_t slot = sn;
+        fetch(base + stride + rq, wn, sn);
+        uint32_t cw[VB], meta;
+        quantize_values32<VB>(w, lpg, cw, meta);
+        if (r >= rows || slot < 0) continue;
+        if (slot >= cache_slots) {
+            if (sub == 0) atomicOr(C.status, TQ_DEVERR_SLOT_RANGE);
+            continue;
+        }
+        const int64_t t = hshift >= 0 ? (r >> hshift) : r / Hkv;
+        const int64_t dst = (slot >> pshift) * Hkv + (r - t * Hkv);
+        const int64_t off = slot & (G.P - 1);
+        uint8_t *vrec = vc + dst * G.v_page;
+        uint8_t *vcode = vrec + off * (D * VB / 8);
+        if constexpr (VB == 2) {
+            reinterpret_cast<uint2 *>(vcode)[sub] = make_uint2(cw[0], cw[1]);
+        } else if constexpr (VB == 4) {
+            reinterpret_cast<uint4 *>(vcode)[sub] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        } else {
+            uint32_t *vw = reinterpret_cast<uint32_t *>(vcode) + VB * sub;
+#pragma unroll
+            for (int k = 0; k < VB; ++k) vw[k] = cw[k];
+        }
+        if ((sub & (lpg - 1)) == 0)
+            *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + off * C.v_meta_bytes + 4 * (sub / lpg)) = meta;
+    }
+}
+
+template <int VB>
+cudaError_t launch_values_tc(const Codec &c, const PageGeom &pg, const uint16_t *v, int64_t T, int Hkv, int64_t vs,
+                             const int64_t *slots, uint8_t *vc, int64_t num_blocks, int num_sms, cudaStream_t st)
+{
+    const int64_t rows = T * Hkv;
+    int64_t blocks = (rows + 63) / 64;  // 8 warps x 8 rows
+    const int64_t cap = static_cast<int64_t>(num_sms) * 2;  // one wave: two resident CTAs per SM
+    if (blocks > cap) blocks = cap;
+    compress_values_tc_kernel<VB><<<static_cast<unsigned>(blocks), 256, 0, st>>>(c, pg, v, rows, Hkv, vs, slots, vc,
+                                                                               num_blocks);
+    return cudaGetLastError();
+}
+
 template <int KB, int VB>
 cudaError_t launch_tc(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T, int Hkv,
                       int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc, int64_t num_blocks,
@@ -1107,6 +1186,17 @@ cudaError_t launch_tc_kb(const Codec &c, const PageGeom &pg, const uint16_t *k, 
 }  // namespace
 
 size_t compress_tc_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_compress_values_tc(const Codec &c, const PageGeom &pg, const uint16_t *v, int64_t T, int Hkv,
+                                      int64_t vs, const int64_t *slots, uint8_t *vc, int64_t num_blocks, int num_sms,
+                                      cudaStream_t st)
+{
+    switch (c.v_bits) {
+    case 2: return launch_values_tc<2>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
+    case 3: return launch_values_tc<3>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
+    default: return launch_values_tc<4>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
+    }
+}
 
 cudaError_t launch_compress_tc_keys(const Codec &c, const PageGeom &pg, const uint16_t *k, int64_t T, int Hkv,
                                     int64_t ks, const int64_t *slots, uint8_t *kc, int64_t num_blocks, int num_sms,
