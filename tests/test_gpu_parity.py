@@ -291,10 +291,16 @@ def test_strided_token_rows(name):
     assert torch.equal(kc, kc_ref) and torch.equal(vc, vc_ref)
 
 
-def test_bad_ids_set_status_and_write_nothing_out_of_bounds():
-    w = SMALL["paged_decode_small"]
+# compress paths: the fused tensor-core kernel (QJL keys), its keys-only form with
+# the value kernel (4-bit keys), and its keys-only form twice (MSE-coded values)
+COMPRESS_PATHS = [("paged_decode_small", "group"), ("mixed_k4v4_small", "group"), ("paged_decode_small", "mse")]
+
+
+@pytest.mark.parametrize("name,values", COMPRESS_PATHS)
+def test_bad_ids_set_status_and_write_nothing_out_of_bounds(name, values):
+    w = SMALL[name]
     b = W.generate(w, device=DEV)
-    codec, _ = _codec_pair(w)
+    codec = Codec(w.head_dim, w.k_bits, w.v_bits, w.group, w.codec_seed(), values=values)
     kpb, vpb = codec.cache_layout(w.page_size)
     guard = 4096
     kbig = torch.full((guard * 2 + b.num_blocks * w.num_kv_heads * kpb,), 0x5A, dtype=torch.uint8, device=DEV)
@@ -421,6 +427,30 @@ def test_wait_timeouts_report_and_recover():
     assert codec.get_status() & native.TQ_DEVERR_TIMEOUT
     codec.set_wait_limit(native.TQ_DEFAULT_WAIT_LIMIT)
     assert np.array_equal(_decode_gpu(codec, w, b, kc, vc), ref)
+    kc3, vc3 = _compress(codec, w, b)
+    assert codec.get_status() == 0
+    assert torch.equal(kc3, kc) and torch.equal(vc3, vc)
+
+
+@pytest.mark.parametrize("name,values", COMPRESS_PATHS[1:])
+def test_compress_wait_timeouts_on_the_keys_only_paths(name, values):
+    """The keys-only form of the tensor-core kernel (4-bit keys with the value
+    kernel; MSE-coded values, run twice) under a wait limit of 0: its epilogue's
+    first hand-off wait cannot have completed (the producers must load the tile
+    first), so it reports TQ_DEVERR_TIMEOUT and winds down; with the default limit
+    restored the same call writes the same bytes as before."""
+    from rotated_codebook_kv_gb300 import native
+    w = SMALL[name]
+    b = W.generate(w, device=DEV)
+    codec = Codec(w.head_dim, w.k_bits, w.v_bits, w.group, w.codec_seed(), values=values)
+    kc, vc = _compress(codec, w, b)
+    assert codec.get_status() == 0
+    codec.set_wait_limit(0)
+    kc2, vc2 = codec.alloc_cache(b.num_blocks, w.num_kv_heads, w.page_size, fill=0xA5)
+    codec.compress_kv(b.k, b.v, b.slot_mapping, kc2, vc2, w.page_size, b.num_blocks)
+    torch.cuda.synchronize()
+    assert codec.get_status() & native.TQ_DEVERR_TIMEOUT
+    codec.set_wait_limit(native.TQ_DEFAULT_WAIT_LIMIT)
     kc3, vc3 = _compress(codec, w, b)
     assert codec.get_status() == 0
     assert torch.equal(kc3, kc) and torch.equal(vc3, vc)
