@@ -890,7 +890,9 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
     const bool fused = !HAD && !C.qjl;
-    if (!VMSE && fused) stage_values();
+    // without a value input (values taken by their own kernel) there is no value work
+    const bool vals = !VMSE && vin != nullptr;
+    if (vals && fused) stage_values();
     // the key codebook's bin table; the barrier also publishes the rows' tokens
     const unsigned char *binb = reinterpret_cast<const unsigned char *>(s_bins) + 8 * (lane % kBinCopies);
     bool binbad = __syncthreads_or(build_code_bins(s_bins, C.thresholds, nthr));
@@ -1005,7 +1007,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         }
     }
     __syncthreads();
-    if (!VMSE && !fused && !C.qjl) stage_values();  // yb holds no residuals without QJL
+    if (vals && !fused && !C.qjl) stage_values();  // yb holds no residuals without QJL
     // ---- QJL: p = S r, gamma, sign guard ---------------------------------------
     if (C.qjl) {
         // the residuals as fp16 high + low parts times a power of two per row (high in
@@ -1034,7 +1036,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             }
         }
         __syncthreads();  // every residual is in registers; row scales published
-        if (!VMSE) stage_values();  // the low parts below fill yb's lower half only
+        if (vals) stage_values();  // the low parts below fill yb's lower half only
         __half *klo = reinterpret_cast<__half *>(yb);
 #pragma unroll
         for (int k = 0; k < RPW; ++k) {
@@ -1106,9 +1108,14 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * off) = zero ? 0 : s_n16[row];
     }
     if constexpr (!VMSE) {
-        if (C.v_bits == 2) quantize_value_rows<D, TM, 2>(vstage, s_dst, s_off, vc, G, C);
-        else if (C.v_bits == 3) quantize_value_rows<D, TM, 3>(vstage, s_dst, s_off, vc, G, C);
-        else quantize_value_rows<D, TM, 4>(vstage, s_dst, s_off, vc, G, C);
+        if (!vals) {
+        } else if (C.v_bits == 2) {
+            quantize_value_rows<D, TM, 2>(vstage, s_dst, s_off, vc, G, C);
+        } else if (C.v_bits == 3) {
+            quantize_value_rows<D, TM, 3>(vstage, s_dst, s_off, vc, G, C);
+        } else {
+            quantize_value_rows<D, TM, 4>(vstage, s_dst, s_off, vc, G, C);
+        }
     }
     if constexpr (VMSE) {
         // ==== values coded like keys without QJL (brightcoding blog, "What is
@@ -1476,9 +1483,13 @@ cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *
         default: return launch_stream<256, 4>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
         }
     }
-    if (c.rotation == 1)
-        return launch_compress_d<256, true, false>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
-    return launch_compress_d<256, false, false>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+    // the general kernel on the keys alone, then the value kernel: its value pass is
+    // ~40% of a CTA's time at 16 warps per SM, the value kernel streams them faster
+    cudaError_t e = c.rotation == 1
+                        ? launch_compress_d<256, true, false>(c, pg, k, nullptr, T, Hkv, ks, 0, slots, kc, vc, num_blocks, st)
+                        : launch_compress_d<256, false, false>(c, pg, k, nullptr, T, Hkv, ks, 0, slots, kc, vc, num_blocks, st);
+    if (e != cudaSuccess) return e;
+    return launch_compress_values_tc(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, c.num_sms, st);
 }
 
 }  // namespace tq

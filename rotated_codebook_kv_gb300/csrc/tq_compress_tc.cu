@@ -1077,36 +1077,37 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
     if (warp == 0) umma::tmem_dealloc(tmem, 512);
 }
 
-// Group-quantised values alone (the keys taking the keys-only pass): the fused
-// kernel's value layout, four lanes per row, lane sub holding channels
-// [32 sub, 32 sub + 32), eight rows per warp; row octets strided over a one-wave grid
-// with the next octet's values and slots in flight while the current one is
+// Group-quantised values alone (the keys taking a keys-only pass): the fused
+// kernel's value layout, DD / 32 lanes per row, lane sub of a row holding channels
+// [32 sub, 32 sub + 32), 1024 / DD rows per warp; row groups strided over a one-wave
+// grid with the next group's values and slots in flight while the current one is
 // quantised.  The loop bounds are the same for the whole warp, so the group
-// reductions' shuffles always run with every lane.
-template <int VB>
+// reductions' shuffles (within a row's lanes) always run with every lane.
+template <int DD, int VB>
 __global__ void __launch_bounds__(256, 2)
 compress_values_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ vin, int64_t rows, int Hkv,
                           int64_t vs, const int64_t *__restrict__ slots, uint8_t *__restrict__ vc, int64_t num_blocks)
 {
-    const int lane = threadIdx.x & 31, sub = lane & 3, rq = lane >> 2;
+    constexpr int LPR = DD / 32, RPW = 32 / LPR;  // lanes per row, rows per warp
+    const int lane = threadIdx.x & 31, sub = lane % LPR, rq = lane / LPR;
     const int lpg = C.group >> 5;  // lanes per group: 1, 2 or 4
     const int hshift = (Hkv & (Hkv - 1)) == 0 ? __ffs(Hkv) - 1 : -1;
     const int pshift = __ffs(G.P) - 1;
     const int64_t cache_slots = num_blocks * G.P;
-    const int64_t stride = 8 * static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int64_t stride = RPW * static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     auto fetch = [&](int64_t r, uint4 (&w)[4], int64_t &sl) {
         sl = -1;
 #pragma unroll
         for (int j = 0; j < 4; ++j) w[j] = make_uint4(0u, 0u, 0u, 0u);
         if (r < rows) {
             const int64_t t = hshift >= 0 ? (r >> hshift) : r / Hkv;
-            const uint4 *src = reinterpret_cast<const uint4 *>(vin + t * vs + (r - t * Hkv) * D);
+            const uint4 *src = reinterpret_cast<const uint4 *>(vin + t * vs + (r - t * Hkv) * DD);
 #pragma unroll
             for (int j = 0; j < 4; ++j) w[j] = ld_pinned(src + 4 * sub + j);
             sl = ld_pinned_s64(slots + t);
         }
     };
-    int64_t base = 8 * (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5));
+    int64_t base = RPW * (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5));
     uint4 wn[4];
     int64_t sn;
     fetch(base + rq, wn, sn);
@@ -1128,7 +1129,7 @@ compress_values_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__res
         const int64_t dst = (slot >> pshift) * Hkv + (r - t * Hkv);
         const int64_t off = slot & (G.P - 1);
         uint8_t *vrec = vc + dst * G.v_page;
-        uint8_t *vcode = vrec + off * (D * VB / 8);
+        uint8_t *vcode = vrec + off * (DD * VB / 8);
         if constexpr (VB == 2) {
             reinterpret_cast<uint2 *>(vcode)[sub] = make_uint2(cw[0], cw[1]);
         } else if constexpr (VB == 4) {
@@ -1143,16 +1144,17 @@ compress_values_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__res
     }
 }
 
-template <int VB>
+template <int DD, int VB>
 cudaError_t launch_values_tc(const Codec &c, const PageGeom &pg, const uint16_t *v, int64_t T, int Hkv, int64_t vs,
                              const int64_t *slots, uint8_t *vc, int64_t num_blocks, int num_sms, cudaStream_t st)
 {
     const int64_t rows = T * Hkv;
-    int64_t blocks = (rows + 63) / 64;  // 8 warps x 8 rows
+    constexpr int64_t kRowsPerCta = 8 * (1024 / DD);  // 8 warps
+    int64_t blocks = (rows + kRowsPerCta - 1) / kRowsPerCta;
     const int64_t cap = static_cast<int64_t>(num_sms) * 2;  // one wave: two resident CTAs per SM
     if (blocks > cap) blocks = cap;
-    compress_values_tc_kernel<VB><<<static_cast<unsigned>(blocks), 256, 0, st>>>(c, pg, v, rows, Hkv, vs, slots, vc,
-                                                                               num_blocks);
+    compress_values_tc_kernel<DD, VB><<<static_cast<unsigned>(blocks), 256, 0, st>>>(c, pg, v, rows, Hkv, vs, slots,
+                                                                                   vc, num_blocks);
     return cudaGetLastError();
 }
 
@@ -1191,10 +1193,17 @@ cudaError_t launch_compress_values_tc(const Codec &c, const PageGeom &pg, const 
                                       int64_t vs, const int64_t *slots, uint8_t *vc, int64_t num_blocks, int num_sms,
                                       cudaStream_t st)
 {
+    if (c.d == 256) {
+        switch (c.v_bits) {
+        case 2: return launch_values_tc<256, 2>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
+        case 3: return launch_values_tc<256, 3>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
+        default: return launch_values_tc<256, 4>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
+        }
+    }
     switch (c.v_bits) {
-    case 2: return launch_values_tc<2>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
-    case 3: return launch_values_tc<3>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
-    default: return launch_values_tc<4>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
+    case 2: return launch_values_tc<128, 2>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
+    case 3: return launch_values_tc<128, 3>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
+    default: return launch_values_tc<128, 4>(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, num_sms, st);
     }
 }
 

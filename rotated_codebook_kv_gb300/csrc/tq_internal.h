@@ -107,7 +107,7 @@ cudaError_t launch_compress_tc(const Codec &c, const PageGeom &pg, const uint16_
 cudaError_t launch_compress_tc_keys(const Codec &c, const PageGeom &pg, const uint16_t *k, int64_t T, int Hkv,
                                     int64_t ks, const int64_t *slots, uint8_t *kc, int64_t num_blocks, int num_sms,
                                     cudaStream_t st);
-// Group-quantised value records alone at head dim 128 (the keys taking the keys-only pass).
+// Group-quantised value records alone, head dim 128 or 256 (the keys taking a keys-only pass).
 cudaError_t launch_compress_values_tc(const Codec &c, const PageGeom &pg, const uint16_t *v, int64_t T, int Hkv,
                                       int64_t vs, const int64_t *slots, uint8_t *vc, int64_t num_blocks, int num_sms,
                                       cudaStream_t st);
