@@ -9,8 +9,13 @@
 // Values (0xsero/turboquant, "Value Compression"): per group of `group`
 //   channels, scale = fp16((max - min) / (2^b - 1)), zero = fp16(min), and
 //   code = #{m < 2^b - 1 : x - zero >= (m + 1/2) scale} (round half up).
-// K and V of the same tokens are compressed in one launch (brightcoding blog,
-// "Key Features": compress_kv fuses key and value compression).
+// One call compresses K and V of the same tokens (brightcoding blog, "Key
+// Features": compress_kv takes both).  Its launches (launch_compress, at the end):
+// head dim 128 with QJL keys the fused tensor-core kernel (tq_compress_tc.cu);
+// without QJL that kernel's keys-only form and the value kernel; head dim 256 the
+// Hadamard streaming kernel below (4-bit keys, values fused) or the general kernel
+// below on the keys alone and the value kernel; with MSE-coded values the keys-only
+// pass twice, on the keys and on the values coded like keys.
 //
 // Numerics.  The fast path rotates and projects in fp32.  A code whose fp32 z
 // lies within kCodeGuard of a threshold, or a sign whose |p| lies within
@@ -806,7 +811,7 @@ __device__ __forceinline__ void quantize_value_rows(const unsigned char *vstage,
     }
 }
 
-template <int D, bool HAD, bool VMSE>
+template <int D, bool HAD>
 __global__ void __launch_bounds__(kThreads, 2)
 compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
                 int64_t rows, int Hkv, int64_t ks, int64_t vs, const int64_t *__restrict__ slots,
@@ -891,7 +896,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     };
     const bool fused = !HAD && !C.qjl;
     // without a value input (values taken by their own kernel) there is no value work
-    const bool vals = !VMSE && vin != nullptr;
+    const bool vals = vin != nullptr;
     if (vals && fused) stage_values();
     // the key codebook's bin table; the barrier also publishes the rows' tokens
     const unsigned char *binb = reinterpret_cast<const unsigned char *>(s_bins) + 8 * (lane % kBinCopies);
@@ -1107,95 +1112,13 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         }
         if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * off) = zero ? 0 : s_n16[row];
     }
-    if constexpr (!VMSE) {
-        if (!vals) {
-        } else if (C.v_bits == 2) {
-            quantize_value_rows<D, TM, 2>(vstage, s_dst, s_off, vc, G, C);
-        } else if (C.v_bits == 3) {
-            quantize_value_rows<D, TM, 3>(vstage, s_dst, s_off, vc, G, C);
-        } else {
-            quantize_value_rows<D, TM, 4>(vstage, s_dst, s_off, vc, G, C);
-        }
-    }
-    if constexpr (VMSE) {
-        // ==== values coded like keys without QJL (brightcoding blog, "What is
-        // TurboQuant-GPU?" / "Example 4"): norm, rotation, Lloyd-Max codes ====
-        __syncthreads();  // the key pass is done with kf, yb and codes
-        if (tid < 18) s_thr[tid] = tid == 0 ? -INFINITY : (tid <= (1 << C.v_bits) - 1 ? C.vthresholds[tid - 1] : INFINITY);
-        if (tid < 16) s_cent[tid] = C.vcentroids[tid];
-        binbad = __syncthreads_or(build_code_bins(s_bins, C.vthresholds, (1 << C.v_bits) - 1));
-        for (int e = tid; e < TM * (D / 8); e += kThreads) {
-            const int row = e / (D / 8), c8 = e - row * (D / 8);
-            const int64_t r = r0 + row;
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (r < rows) {
-                const int64_t t = s_tok[row];
-                const int h = static_cast<int>(r - t * Hkv);
-                u = __ldg(reinterpret_cast<const uint4 *>(vin + t * vs + static_cast<int64_t>(h) * D) + c8);
-            }
-            *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8) =
-                make_float4(bf16_to_float(u.x & 0xffffu), bf16_to_float(u.x >> 16), bf16_to_float(u.y & 0xffffu),
-                            bf16_to_float(u.y >> 16));
-            *reinterpret_cast<float4 *>(kf + row * RS + c8 * 8 + 4) =
-                make_float4(bf16_to_float(u.z & 0xffffu), bf16_to_float(u.z >> 16), bf16_to_float(u.w & 0xffffu),
-                            bf16_to_float(u.w >> 16));
-        }
-        __syncthreads();
-        for (int row = warp; row < TM; row += kWarps) {
-            float ss = 0.f, mx = 0.f;
-            for (int j = lane; j < D; j += 32) {
-                const float x = kf[row * RS + j];
-                ss = fmaf(x, x, ss);
-                mx = fmaxf(mx, fabsf(x));
-            }
-            ss = warp_sum(ss);
-            mx = warp_max(mx);
-            if (lane == 0) {
-                int flag = 0;
-                if (mx == 0.f) flag = 2;
-                else if (!(mx >= 0x1p-30f && mx <= 0x1p30f)) flag = 1;
-                const float n = sqrtf(ss);
-                s_scale[row] = (flag == 0) ? sqrtd / n : 0.f;
-                s_flag[row] = flag;
-                s_n16[row] = flag == 2 ? 0 : float_to_bf16_bits(n);
-            }
-            if constexpr (!HAD) stage_fp16_row<D>(kf, ka, row, mx, s_ysc);
-        }
-        if constexpr (HAD) {
-            fwht_rows<D, TM>(C.hsign, kf, yb);
-        } else {
-            __syncthreads();
-            mma_rows<D, TM>(C.pi_frag, ka, s_ysc, yb);
-        }
-        __syncthreads();
-        if (!binbad)
-            codes_and_residuals<true, false, D, TM>(yb, RS, s_scale, s_flag, binb, s_thr, s_cent, C.v_bits, codes, CS);
-        else
-            codes_and_residuals<false, false, D, TM>(yb, RS, s_scale, s_flag, binb, s_thr, s_cent, C.v_bits, codes, CS);
-        __syncthreads();
-        for (int row = warp; row < TM; row += kWarps) {
-            const int fl = s_flag[row];
-            if ((fl != 1 && fl != 3) || s_dst[row] < 0) continue;
-            const int64_t t = s_tok[row];
-            const int h = static_cast<int>(r0 + row - t * Hkv);
-            if (fl == 3) {  // no QJL on values: the re-decided codes are final
-                refine_marked_codes<D>(C.Pi, vin + t * vs + static_cast<int64_t>(h) * D, codes + row * CS,
-                                       C.vthresholds, (1 << C.v_bits) - 1);
-                continue;
-            }
-            precise_key_row<D>(C, vin + t * vs + static_cast<int64_t>(h) * D, codes + row * CS, kf + row * RS,
-                               scratch + warp * D, &s_n16[row], &s_g16[row], C.vthresholds, C.vcentroids, C.v_bits,
-                               false);
-        }
-        __syncthreads();
-        store_code_words<D, TM>(codes, CS, C.v_bits, s_dst, s_off, s_flag, vc, G.v_page, C.v_code_bytes);
-        for (int row = tid; row < TM; row += kThreads) {
-            const int64_t dst = s_dst[row];
-            if (dst < 0) continue;
-            const int off = s_off[row];
-            *reinterpret_cast<uint16_t *>(vc + dst * G.v_page + G.v_meta_off + 2 * off) =
-                s_flag[row] == 2 ? 0 : s_n16[row];
-        }
+    if (!vals) {
+    } else if (C.v_bits == 2) {
+        quantize_value_rows<D, TM, 2>(vstage, s_dst, s_off, vc, G, C);
+    } else if (C.v_bits == 3) {
+        quantize_value_rows<D, TM, 3>(vstage, s_dst, s_off, vc, G, C);
+    } else {
+        quantize_value_rows<D, TM, 4>(vstage, s_dst, s_off, vc, G, C);
     }
 }
 
@@ -1420,52 +1343,67 @@ cudaError_t launch_stream(const Codec &c, const PageGeom &pg, const uint16_t *k,
     return cudaGetLastError();
 }
 
-template <int D, bool HAD, bool VMSE>
+template <int D, bool HAD>
 cudaError_t launch_compress_d(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
                               int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
                               int64_t num_blocks, cudaStream_t st)
 {
     const size_t smem = CompressSmem<D>::kBytes;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(compress_kernel<D, HAD, VMSE>), smem);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(compress_kernel<D, HAD>), smem);
     if (e != cudaSuccess) return e;
     const int64_t rows = T * Hkv;
     const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-    compress_kernel<D, HAD, VMSE><<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(c, pg, k, v, rows, Hkv, ks, vs, slots,
-                                                                             kc, vc, num_blocks);
+    compress_kernel<D, HAD><<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(c, pg, k, v, rows, Hkv, ks, vs, slots, kc,
+                                                                       vc, num_blocks);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+// The codec and page geometry that code MSE values as key records: an MSE value
+// record is exactly a key record without QJL (codes, then a bf16 norm per token).
+static void values_as_keys(const Codec &c, const PageGeom &pg, Codec &cv, PageGeom &gv)
+{
+    cv = c;
+    cv.k_bits = c.v_bits;
+    cv.qjl = 0;
+    cv.k_code_bytes = c.v_code_bytes;
+    cv.k_sign_bytes = 0;
+    for (int i = 0; i < 16; ++i) {
+        cv.centroids[i] = c.vcentroids[i];
+        cv.thresholds[i] = c.vthresholds[i];
+    }
+    gv = pg;
+    gv.k_page = pg.v_page;
+    gv.k_sign_off = gv.k_norm_off = pg.v_meta_off;
+    gv.k_gamma_off = pg.v_meta_off + 2LL * pg.P;  // not written without QJL
+}
+
+// Key records alone at head dim 256: the general kernel without a value input.
+static cudaError_t launch_keys_256(const Codec &c, const PageGeom &pg, const uint16_t *k, int64_t T, int Hkv,
+                                   int64_t ks, const int64_t *slots, uint8_t *kc, int64_t num_blocks, cudaStream_t st)
+{
+    return c.rotation == 1
+               ? launch_compress_d<256, true>(c, pg, k, nullptr, T, Hkv, ks, 0, slots, kc, nullptr, num_blocks, st)
+               : launch_compress_d<256, false>(c, pg, k, nullptr, T, Hkv, ks, 0, slots, kc, nullptr, num_blocks, st);
+}
+
 cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
                             int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
                             int64_t num_blocks, cudaStream_t st)
 {
-    if (c.vmse && c.d == 128) {
-        // values coded like keys: an MSE value record is a key record without QJL (codes,
-        // then a bf16 norm per token), so the tensor-core kernel runs twice, on the keys
-        // and on the values through a codec whose key fields hold the value codebook
-        cudaError_t e = launch_compress_tc_keys(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, c.num_sms, st);
+    if (c.vmse) {
+        // values coded like keys: the keys-only pass on the keys, then on the values
+        // through the value codebook in the key fields (tensor-core kernel at 128,
+        // general kernel at 256)
+        Codec cv;
+        PageGeom gv;
+        values_as_keys(c, pg, cv, gv);
+        cudaError_t e = c.d == 128 ? launch_compress_tc_keys(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, c.num_sms, st)
+                                   : launch_keys_256(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, st);
         if (e != cudaSuccess) return e;
-        Codec cv = c;
-        cv.k_bits = c.v_bits;
-        cv.qjl = 0;
-        cv.k_code_bytes = c.v_code_bytes;
-        cv.k_sign_bytes = 0;
-        for (int i = 0; i < 16; ++i) {
-            cv.centroids[i] = c.vcentroids[i];
-            cv.thresholds[i] = c.vthresholds[i];
-        }
-        PageGeom gv = pg;
-        gv.k_page = pg.v_page;
-        gv.k_sign_off = gv.k_norm_off = pg.v_meta_off;
-        gv.k_gamma_off = pg.v_meta_off + 2LL * pg.P;  // not written without QJL
-        return launch_compress_tc_keys(cv, gv, v, T, Hkv, vs, slots, vc, num_blocks, c.num_sms, st);
-    }
-    if (c.vmse) {  // values coded like keys at head dim 256: the two-pass SIMT kernel
-        const bool had = c.rotation == 1;
-        return had ? launch_compress_d<256, true, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st)
-                   : launch_compress_d<256, false, true>(c, pg, k, v, T, Hkv, ks, vs, slots, kc, vc, num_blocks, st);
+        return c.d == 128 ? launch_compress_tc_keys(cv, gv, v, T, Hkv, vs, slots, vc, num_blocks, c.num_sms, st)
+                          : launch_keys_256(cv, gv, v, T, Hkv, vs, slots, vc, num_blocks, st);
     }
     if (c.d == 128 && !c.qjl) {
         // without QJL the keys-only tensor-core pass and a streaming value kernel beat the
@@ -1485,9 +1423,7 @@ cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *
     }
     // the general kernel on the keys alone, then the value kernel: its value pass is
     // ~40% of a CTA's time at 16 warps per SM, the value kernel streams them faster
-    cudaError_t e = c.rotation == 1
-                        ? launch_compress_d<256, true, false>(c, pg, k, nullptr, T, Hkv, ks, 0, slots, kc, vc, num_blocks, st)
-                        : launch_compress_d<256, false, false>(c, pg, k, nullptr, T, Hkv, ks, 0, slots, kc, vc, num_blocks, st);
+    cudaError_t e = launch_keys_256(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, st);
     if (e != cudaSuccess) return e;
     return launch_compress_values_tc(c, pg, v, T, Hkv, vs, slots, vc, num_blocks, c.num_sms, st);
 }
