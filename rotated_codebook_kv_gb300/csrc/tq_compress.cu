@@ -54,12 +54,6 @@ constexpr int kStreamWarps = 8;
 constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23: adding it rounds to an integer
 constexpr uint32_t kRoundBits = 0x4B400000u;
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
-{
-    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
-
 template <int E>
 __device__ __forceinline__ void unpack_bf16(const uint32_t (&w)[E / 2], float (&x)[E])
 {
@@ -782,40 +776,10 @@ __device__ __forceinline__ void codes_and_residuals(float *yb, int rs, const flo
     }
 }
 
-// The group-quantised value rows warp + kWarps k (k < TM / kWarps) of a CTA, read
-// from the bf16 stage in shared memory (row stride D), one row at a time per warp
-// (four rows in flight per warp ran 30% slower); lane l holds elements 8 l .. 8 l + 7.
-template <int D, int TM, int VB>
-__device__ __forceinline__ void quantize_value_rows(const unsigned char *vstage, const int64_t *s_dst, const int *s_off,
-                                                    uint8_t *vc, const PageGeom &G, const Codec &C)
-{
-    constexpr int E = D / 32;
-    static_assert(E == 8, "group-quantised values in this kernel: head dim 256");
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int lpg = C.group / E;  // lanes per group
-#pragma unroll 1
-    for (int row = warp; row < TM; row += kWarps) {
-        const int64_t dst = s_dst[row];
-        if (dst < 0) continue;
-        const uint4 u = *reinterpret_cast<const uint4 *>(vstage + (row * D + lane * E) * 2);
-        const uint32_t w[E / 2] = {u.x, u.y, u.z, u.w};
-        float x[E];
-        unpack_bf16<E>(w, x);
-        uint32_t vw;
-        const uint32_t meta = quantize_values_lane<E, VB>(x, lpg, vw);
-        uint8_t *vrec = vc + dst * G.v_page;
-        const int64_t off = s_off[row];
-        store_code_bytes(vrec + off * C.v_code_bytes + VB * lane, vw, VB);
-        if ((lane & (lpg - 1)) == 0)
-            *reinterpret_cast<uint32_t *>(vrec + G.v_meta_off + off * C.v_meta_bytes + 4 * (lane / lpg)) = meta;
-    }
-}
-
 template <int D, bool HAD>
 __global__ void __launch_bounds__(kThreads, 2)
-compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin,
-                int64_t rows, int Hkv, int64_t ks, int64_t vs, const int64_t *__restrict__ slots,
-                uint8_t *__restrict__ kc, uint8_t *__restrict__ vc, int64_t num_blocks)
+compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, int64_t rows, int Hkv, int64_t ks,
+                const int64_t *__restrict__ slots, uint8_t *__restrict__ kc, int64_t num_blocks)
 {
     using SM = CompressSmem<D>;
     constexpr int TM = SM::TM;
@@ -858,9 +822,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         slot = slots[t];
     }
     // Each warp's key rows (dense rotation: the lane's E contiguous elements) are
-    // loaded now, and without QJL the value rows are copied into yb's upper half (free
-    // until the pack loop), so that their latency overlaps the slot loads and the bin
-    // table.  With QJL the values are copied once the residuals are in registers.
+    // loaded now, so that their latency overlaps the slot loads and the bin table.
     constexpr int E = D / 32, RPW = TM / kWarps;
     uint32_t kraw[RPW][E / 2];
     if constexpr (!HAD) {
@@ -882,22 +844,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             }
         }
     }
-    unsigned char *vstage = reinterpret_cast<unsigned char *>(yb) + SM::kKa;  // TM rows of D bf16 values
-    auto stage_values = [&]() {
-        for (int e = tid; e < TM * (D / 8); e += kThreads) {
-            const int row = e / (D / 8), c8 = e - row * (D / 8);
-            if (r0 + row < rows) {
-                const int q = (h0 + row) / Hkv;
-                cp_async16(vstage + (row * D + c8 * 8) * 2,
-                           vin + (t0 + q) * vs + static_cast<int64_t>(h0 + row - q * Hkv) * D + c8 * 8);
-            }
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
     const bool fused = !HAD && !C.qjl;
-    // without a value input (values taken by their own kernel) there is no value work
-    const bool vals = vin != nullptr;
-    if (vals && fused) stage_values();
     // the key codebook's bin table; the barrier also publishes the rows' tokens
     const unsigned char *binb = reinterpret_cast<const unsigned char *>(s_bins) + 8 * (lane % kBinCopies);
     bool binbad = __syncthreads_or(build_code_bins(s_bins, C.thresholds, nthr));
@@ -1012,7 +959,6 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         }
     }
     __syncthreads();
-    if (vals && !fused && !C.qjl) stage_values();  // yb holds no residuals without QJL
     // ---- QJL: p = S r, gamma, sign guard ---------------------------------------
     if (C.qjl) {
         // the residuals as fp16 high + low parts times a power of two per row (high in
@@ -1041,7 +987,6 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             }
         }
         __syncthreads();  // every residual is in registers; row scales published
-        if (vals) stage_values();  // the low parts below fill yb's lower half only
         __half *klo = reinterpret_cast<__half *>(yb);
 #pragma unroll
         for (int k = 0; k < RPW; ++k) {
@@ -1088,10 +1033,9 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
                            scratch + warp * D, &s_n16[row], &s_g16[row], C.thresholds, C.centroids, C.k_bits,
                            C.qjl != 0);
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     // ---- pack and store: code words by the whole CTA, then per row its sign
-    // bits, gamma and norm, then (group-quantised values) the value rows ---------
+    // bits, gamma and norm ------------------------------------------------------
     store_code_words<D, TM>(codes, CS, C.k_bits, s_dst, s_off, s_flag, kc, G.k_page, C.k_code_bytes);
     for (int row = warp; row < TM; row += kWarps) {
         const int64_t dst = s_dst[row];
@@ -1111,14 +1055,6 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_gamma_off + 2 * off) = zero ? 0 : s_g16[row];
         }
         if (lane == 0) *reinterpret_cast<uint16_t *>(krec + G.k_norm_off + 2 * off) = zero ? 0 : s_n16[row];
-    }
-    if (!vals) {
-    } else if (C.v_bits == 2) {
-        quantize_value_rows<D, TM, 2>(vstage, s_dst, s_off, vc, G, C);
-    } else if (C.v_bits == 3) {
-        quantize_value_rows<D, TM, 3>(vstage, s_dst, s_off, vc, G, C);
-    } else {
-        quantize_value_rows<D, TM, 4>(vstage, s_dst, s_off, vc, G, C);
     }
 }
 
@@ -1344,17 +1280,16 @@ cudaError_t launch_stream(const Codec &c, const PageGeom &pg, const uint16_t *k,
 }
 
 template <int D, bool HAD>
-cudaError_t launch_compress_d(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
-                              int Hkv, int64_t ks, int64_t vs, const int64_t *slots, uint8_t *kc, uint8_t *vc,
-                              int64_t num_blocks, cudaStream_t st)
+cudaError_t launch_compress_d(const Codec &c, const PageGeom &pg, const uint16_t *k, int64_t T, int Hkv, int64_t ks,
+                              const int64_t *slots, uint8_t *kc, int64_t num_blocks, cudaStream_t st)
 {
     const size_t smem = CompressSmem<D>::kBytes;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(compress_kernel<D, HAD>), smem);
     if (e != cudaSuccess) return e;
     const int64_t rows = T * Hkv;
     const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-    compress_kernel<D, HAD><<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(c, pg, k, v, rows, Hkv, ks, vs, slots, kc,
-                                                                       vc, num_blocks);
+    compress_kernel<D, HAD><<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(c, pg, k, rows, Hkv, ks, slots, kc,
+                                                                                   num_blocks);
     return cudaGetLastError();
 }
 
@@ -1383,9 +1318,8 @@ static void values_as_keys(const Codec &c, const PageGeom &pg, Codec &cv, PageGe
 static cudaError_t launch_keys_256(const Codec &c, const PageGeom &pg, const uint16_t *k, int64_t T, int Hkv,
                                    int64_t ks, const int64_t *slots, uint8_t *kc, int64_t num_blocks, cudaStream_t st)
 {
-    return c.rotation == 1
-               ? launch_compress_d<256, true>(c, pg, k, nullptr, T, Hkv, ks, 0, slots, kc, nullptr, num_blocks, st)
-               : launch_compress_d<256, false>(c, pg, k, nullptr, T, Hkv, ks, 0, slots, kc, nullptr, num_blocks, st);
+    return c.rotation == 1 ? launch_compress_d<256, true>(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, st)
+                           : launch_compress_d<256, false>(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, st);
 }
 
 cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
