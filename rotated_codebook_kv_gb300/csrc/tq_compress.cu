@@ -37,13 +37,15 @@ constexpr int kRowsPerBlock = 32;
 constexpr float kCodeGuard = 1e-5f;  // z units
 constexpr float kSignGuard = 2e-5f;  // |p| / ||r||
 
-template <int D>
+// FUSED: dense rotation without QJL, codes decided in the rotation's epilogue; the
+// fp32 row buffers kf and yb are never touched then and take no space.
+template <int D, bool FUSED>
 struct CompressSmem {
     static constexpr int TM = kRowsPerBlock;
     static constexpr int kCodeStride = D + 4;
     static constexpr int kRS = D + 8;                          // fp32 row stride (8 rows of an MMA fragment: 8 bank groups)
-    static constexpr size_t kKf = sizeof(float) * TM * kRS;    // keys, later S r
-    static constexpr size_t kYb = sizeof(float) * TM * kRS;    // Pi k, later r
+    static constexpr size_t kKf = FUSED ? 0 : sizeof(float) * TM * kRS;  // keys, later S r
+    static constexpr size_t kYb = FUSED ? 0 : sizeof(float) * TM * kRS;  // Pi k, later r
     static constexpr size_t kCodes = ((TM * kCodeStride + 15) / 16) * 16;
     static constexpr size_t kScratch = sizeof(double) * kWarps * D;
     static constexpr size_t kKa = sizeof(__half) * TM * (D + 8);  // fp16 keys for the tensor-core rotation
@@ -776,12 +778,13 @@ __device__ __forceinline__ void codes_and_residuals(float *yb, int rs, const flo
     }
 }
 
-template <int D, bool HAD>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int D, bool HAD, bool FUSED>
+__global__ void __launch_bounds__(kThreads, FUSED ? 3 : 2)
 compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, int64_t rows, int Hkv, int64_t ks,
                 const int64_t *__restrict__ slots, uint8_t *__restrict__ kc, int64_t num_blocks)
 {
-    using SM = CompressSmem<D>;
+    static_assert(!(HAD && FUSED), "the fused epilogue follows the dense rotation");
+    using SM = CompressSmem<D, FUSED>;
     constexpr int TM = SM::TM;
     constexpr int CS = SM::kCodeStride;
     constexpr int RS = SM::kRS;
@@ -844,7 +847,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
             }
         }
     }
-    const bool fused = !HAD && !C.qjl;
+    constexpr bool fused = FUSED;  // launched exactly when !HAD && !C.qjl
     // the key codebook's bin table; the barrier also publishes the rows' tokens
     const unsigned char *binb = reinterpret_cast<const unsigned char *>(s_bins) + 8 * (lane % kBinCopies);
     bool binbad = __syncthreads_or(build_code_bins(s_bins, C.thresholds, nthr));
@@ -937,14 +940,14 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         fwht_rows<D, TM>(C.hsign, kf, yb);
     } else {
         __syncthreads();  // ka and s_ysc of every row are staged
-        if (fused)
+        if constexpr (fused)
             mma_rows_codes<D, TM>(C.pi_frag, ka, s_ysc, s_scale, s_flag, binb, binbad, s_thr, C.k_bits, codes, CS);
         else
             mma_rows<D, TM>(C.pi_frag, ka, s_ysc, yb);
     }
     __syncthreads();
     // ---- codes, guard band, residual (the residual only for QJL) ---------------
-    if (!fused) {
+    if constexpr (!fused) {
         if (C.qjl) {
             if (!binbad)
                 codes_and_residuals<true, true, D, TM>(yb, RS, s_scale, s_flag, binb, s_thr, s_cent, C.k_bits, codes, CS);
@@ -960,7 +963,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
     }
     __syncthreads();
     // ---- QJL: p = S r, gamma, sign guard ---------------------------------------
-    if (C.qjl) {
+    if (!fused && C.qjl) {
         // the residuals as fp16 high + low parts times a power of two per row (high in
         // ka, low over yb once every row is in registers), then p = S r on mma.sync
         constexpr int KA = D + 8;
@@ -1043,7 +1046,7 @@ compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ ki
         const int off = s_off[row];
         const bool zero = (s_flag[row] == 2);
         uint8_t *krec = kc + dst * G.k_page;
-        if (C.qjl) {
+        if (!fused && C.qjl) {
 #pragma unroll
             for (int w = 0; w < D / 32; ++w) {
                 uint32_t bits = __ballot_sync(0xffffffffu, kf[row * RS + 32 * w + lane] >= 0.f);
@@ -1279,17 +1282,17 @@ cudaError_t launch_stream(const Codec &c, const PageGeom &pg, const uint16_t *k,
     return cudaGetLastError();
 }
 
-template <int D, bool HAD>
+template <int D, bool HAD, bool FUSED>
 cudaError_t launch_compress_d(const Codec &c, const PageGeom &pg, const uint16_t *k, int64_t T, int Hkv, int64_t ks,
                               const int64_t *slots, uint8_t *kc, int64_t num_blocks, cudaStream_t st)
 {
-    const size_t smem = CompressSmem<D>::kBytes;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(compress_kernel<D, HAD>), smem);
+    const size_t smem = CompressSmem<D, FUSED>::kBytes;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(compress_kernel<D, HAD, FUSED>), smem);
     if (e != cudaSuccess) return e;
     const int64_t rows = T * Hkv;
     const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-    compress_kernel<D, HAD><<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(c, pg, k, rows, Hkv, ks, slots, kc,
-                                                                                   num_blocks);
+    compress_kernel<D, HAD, FUSED><<<static_cast<unsigned>(blocks), kThreads, smem, st>>>(c, pg, k, rows, Hkv, ks, slots,
+                                                                                          kc, num_blocks);
     return cudaGetLastError();
 }
 
@@ -1318,8 +1321,9 @@ static void values_as_keys(const Codec &c, const PageGeom &pg, Codec &cv, PageGe
 static cudaError_t launch_keys_256(const Codec &c, const PageGeom &pg, const uint16_t *k, int64_t T, int Hkv,
                                    int64_t ks, const int64_t *slots, uint8_t *kc, int64_t num_blocks, cudaStream_t st)
 {
-    return c.rotation == 1 ? launch_compress_d<256, true>(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, st)
-                           : launch_compress_d<256, false>(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, st);
+    if (c.rotation == 1) return launch_compress_d<256, true, false>(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, st);
+    return c.qjl ? launch_compress_d<256, false, false>(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, st)
+                 : launch_compress_d<256, false, true>(c, pg, k, T, Hkv, ks, slots, kc, num_blocks, st);
 }
 
 cudaError_t launch_compress(const Codec &c, const PageGeom &pg, const uint16_t *k, const uint16_t *v, int64_t T,
