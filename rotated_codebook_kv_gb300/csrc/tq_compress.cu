@@ -779,7 +779,7 @@ __device__ __forceinline__ void codes_and_residuals(float *yb, int rs, const flo
 }
 
 template <int D, bool HAD, bool FUSED>
-__global__ void __launch_bounds__(kThreads, FUSED ? 3 : 2)
+__global__ void __launch_bounds__(kThreads, FUSED ? 4 : 2)
 compress_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ kin, int64_t rows, int Hkv, int64_t ks,
                 const int64_t *__restrict__ slots, uint8_t *__restrict__ kc, int64_t num_blocks)
 {
