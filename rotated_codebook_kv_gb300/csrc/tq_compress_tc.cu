@@ -1084,7 +1084,7 @@ compress_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__
 // quantised.  The loop bounds are the same for the whole warp, so the group
 // reductions' shuffles (within a row's lanes) always run with every lane.
 template <int DD, int VB>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, 4)
 compress_values_tc_kernel(const Codec C, const PageGeom G, const uint16_t *__restrict__ vin, int64_t rows, int Hkv,
                           int64_t vs, const int64_t *__restrict__ slots, uint8_t *__restrict__ vc, int64_t num_blocks)
 {
@@ -1151,7 +1151,7 @@ cudaError_t launch_values_tc(const Codec &c, const PageGeom &pg, const uint16_t 
     const int64_t rows = T * Hkv;
     constexpr int64_t kRowsPerCta = 8 * (1024 / DD);  // 8 warps
     int64_t blocks = (rows + kRowsPerCta - 1) / kRowsPerCta;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 2;  // one wave: two resident CTAs per SM
+    const int64_t cap = static_cast<int64_t>(num_sms) * 4;  // one wave: four resident CTAs per SM
     if (blocks > cap) blocks = cap;
     compress_values_tc_kernel<DD, VB><<<static_cast<unsigned>(blocks), 256, 0, st>>>(c, pg, v, rows, Hkv, vs, slots,
                                                                                    vc, num_blocks);
