@@ -141,7 +141,10 @@ tq_status tq_cache_layout(tq_handle h, int page_size, size_t *k_page_bytes, size
  * k_cache, v_cache: device pools sized num_blocks * num_kv_heads * page bytes
  *       (tq_cache_layout), 16-byte aligned.  Only the bytes of written slots
  *       change.  Two tokens mapped to one slot race (caller error).
- * One kernel launch on `stream`; T == 0 launches nothing.
+ * One or two kernel launches on `stream` (one with QJL keys at head_dim 128 and
+ * with the Hadamard rotation and 4-bit keys at 256; otherwise the keys and the
+ * values are coded by separate kernels, MSE-coded values by a second keys-only
+ * pass); T == 0 launches nothing.
  */
 tq_status tq_compress_kv(tq_handle h, const uint16_t *k, const uint16_t *v, int64_t T, int num_kv_heads,
                          int64_t k_stride_tok, int64_t v_stride_tok, const int64_t *slot_mapping,
