@@ -232,26 +232,6 @@ __device__ __forceinline__ void store_code_words(const uint8_t *codes, int cs, i
     else store_code_words_b<D, TM, 4>(codes, cs, dst, off, flag, pool, page_bytes, code_bytes);
 }
 
-// One row of fp32 keys (exact bf16 values) staged as fp16 after the power-of-two
-// scale 2^(15 - e), max |k| in [2^(e-1), 2^e): every bf16 value within 2^29 of the
-// row's maximum is exact in fp16 and smaller ones change Pi k by less than 2^-29 of
-// it.  ysc[row] = 2^(e - 25) undoes the scale and Pi's 2^10.  By one warp; rows
-// without a finite scale (zero or extreme, taken exactly) stage zeros.
-template <int D>
-__device__ __forceinline__ void stage_fp16_row(const float *kf, __half *ka, int row, float mx, float *ysc)
-{
-    const int lane = threadIdx.x & 31;
-    // mx = f 2^ex with f in [0.5, 1): ex from the exponent field (mx is normal here)
-    const bool ok = mx >= 0x1p-30f && mx <= 0x1p30f;
-    const int ex = ok ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 126 : 0;
-    const float sc = ok ? __uint_as_float(static_cast<uint32_t>(127 + 15 - ex) << 23) : 0.f;
-    for (int j = 2 * lane; j < D; j += 64) {
-        const float2 x = *reinterpret_cast<const float2 *>(kf + row * (D + 8) + j);
-        *reinterpret_cast<__half2 *>(ka + row * (D + 8) + j) = __floats2half2_rn(x.x * sc, x.y * sc);
-    }
-    if (lane == 0) ysc[row] = ok ? __uint_as_float(static_cast<uint32_t>(127 + ex - 25) << 23) : 0.f;
-}
-
 // Dense rotation of TM rows on the tensor cores (mma.sync m16n8k16, fp16 in,
 // fp32 accumulate): Y = K' (Pi 2^10)^T with K' the keys scaled by a power of two
 // per row so that they are exact in fp16 (staged in ka, row stride D + 8 halves so

@@ -94,31 +94,4 @@ __device__ __forceinline__ int64_t ld_pinned_s64(const int64_t *p)
     return v;
 }
 
-// Word w of the LSB-first bitstream of b-bit codes (one code per byte in `codes`).
-__device__ __forceinline__ uint32_t pack_word(const uint8_t *codes, int w, int b)
-{
-    const int bit0 = 32 * w;
-    int c = bit0 / b;
-    const int sh = bit0 - c * b;
-    uint64_t acc = static_cast<uint64_t>(codes[c]) >> sh;
-    int nb = b - sh;
-    ++c;
-    while (nb < 32) {
-        acc |= static_cast<uint64_t>(codes[c]) << nb;
-        nb += b;
-        ++c;
-    }
-    return static_cast<uint32_t>(acc);
-}
-
-// b-bit code j of an LSB-first bitstream held as 32-bit words.
-__device__ __forceinline__ uint32_t code_from_words(const uint32_t *w, int j, int b)
-{
-    const int o = j * b;
-    const int wi = o >> 5, sh = o & 31;
-    const uint32_t lo = w[wi];
-    const uint32_t hi = (sh + b > 32) ? w[wi + 1] : 0u;
-    return __funnelshift_r(lo, hi, sh) & ((1u << b) - 1u);
-}
-
 }  // namespace tq
