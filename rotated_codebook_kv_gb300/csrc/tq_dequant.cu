@@ -98,9 +98,9 @@ __device__ __forceinline__ void dq_mma(float (&c)[4], uint32_t a0, uint32_t a1, 
 }
 
 // acc = A (TM x D, fp16 in shared memory, row stride D + 8) times W^T from a fragment
-// image, for warp w's output columns [D/8 w, D/8 (w + 1)); with `lo`, A's low parts
-// (same layout) add the two cross products: a_h w_l + a_l w_h + a_h w_h.
-template <int D>
+// image, for warp w's output columns [D/8 w, D/8 (w + 1)); with LO, A's low parts
+// (al, same layout) add the two cross products: a_h w_l + a_l w_h + a_h w_h.
+template <int D, bool LO>
 __device__ __forceinline__ void dq_product(const uint4 *__restrict__ frag, const __half *ah, const __half *al,
                                            float (&acc)[kDqRows / 16][D / 64][4])
 {
@@ -111,7 +111,7 @@ __device__ __forceinline__ void dq_product(const uint4 *__restrict__ frag, const
 #pragma unroll
         for (int n = 0; n < NPW; ++n) acc[m][n][0] = acc[m][n][1] = acc[m][n][2] = acc[m][n][3] = 0.f;
     const uint32_t hb = static_cast<uint32_t>(__cvta_generic_to_shared(ah));
-    const uint32_t lb = al ? static_cast<uint32_t>(__cvta_generic_to_shared(al)) : 0u;
+    const uint32_t lb = LO ? static_cast<uint32_t>(__cvta_generic_to_shared(al)) : 0u;
 #pragma unroll 2
     for (int s = 0; s < KS; ++s) {
         uint4 bf[NPW];
@@ -123,7 +123,7 @@ __device__ __forceinline__ void dq_product(const uint4 *__restrict__ frag, const
             uint32_t a0, a1, a2, a3;
             asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                          : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(hb + off));
-            if (al) {
+            if constexpr (LO) {
                 uint32_t l0, l1, l2, l3;
                 asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                              : "=r"(l0), "=r"(l1), "=r"(l2), "=r"(l3) : "r"(lb + off));
@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(256) dequant_mma_kernel(const Codec C, const P
                                                           uint16_t *__restrict__ kout, uint16_t *__restrict__ vout)
 {
     using SM = DqSmem<D>;
-    constexpr int KA = SM::KA, E = D / 32, NPW = D / 64;
+    constexpr int KA = SM::KA, E = D / 32, NPW = D / 64, RPW = kDqRows / 8;  // RPW rows per warp
+    constexpr int OS = D / 2 + 4;  // bf16-pair row stride of the output tile (rows in different banks)
     extern __shared__ __align__(16) unsigned char smem[];
     float *u = reinterpret_cast<float *>(smem);
     __half *ah = reinterpret_cast<__half *>(smem + SM::kU);
@@ -165,9 +166,15 @@ __global__ void __launch_bounds__(256) dequant_mma_kernel(const Codec C, const P
     __shared__ int64_t s_rec[kDqRows];  // record (block * Hkv + head), -1: row skipped
     __shared__ int s_off[kDqRows];
     __shared__ float s_n[kDqRows], s_g[kDqRows], s_sc[kDqRows];
+    __shared__ float s_cent[2][16];  // key and value centroids / sqrt(d)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rr = lane >> 2, qq = lane & 3;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kDqRows;  // row = slot index * Hkv + head
+    const float rsd = rsqrtf(static_cast<float>(D));
+    if (tid < 16) {
+        s_cent[0][tid] = C.centroids[tid] * rsd;
+        s_cent[1][tid] = C.vcentroids[tid] * rsd;
+    }
     if (tid < kDqRows) {
         const int64_t r = r0 + tid;
         int64_t rec = -1;
@@ -190,45 +197,83 @@ __global__ void __launch_bounds__(256) dequant_mma_kernel(const Codec C, const P
         s_off[tid] = off;
     }
     __syncthreads();
-    const float rsd = rsqrtf(static_cast<float>(D));
 
-    // u = c[code] / sqrt(d) from a record's codes (packed LSB first), sigma into ah with QJL
-    auto stage = [&](bool values) {
+    // The E codes of lane l (coordinates E l .. E l + E - 1, E b <= 32 bits) of warp
+    // row k from two aligned words of the record's packed codes; every row's words
+    // are loaded before any is decoded.  The word after a row's codes lies inside
+    // its page (signs, norms or value metadata follow the codes).
+    auto load_codes = [&](bool values, uint32_t (&cw)[RPW], uint32_t (&aux)[RPW], float (&nrm)[RPW],
+                          float (&gam)[RPW]) {
         const int bits = values ? C.v_bits : C.k_bits;
         const int cbytes = values ? C.v_code_bytes : C.k_code_bytes;
-        const bool qjl = !values && C.qjl;
-        for (int row = warp; row < kDqRows; row += 8) {
-            const int64_t rec = s_rec[row];
-            const int off = s_off[row];
-            const uint8_t *pr = rec >= 0 ? (values ? vc + rec * G.v_page : kc + rec * G.k_page) : nullptr;
+        const int bit0 = E * lane * bits;
 #pragma unroll
-            for (int m = 0; m < E; ++m) {
-                const int j = lane + 32 * m;
-                float x = 0.f;
-                __half sg = __float2half_rn(0.f);
-                if (pr) {
-                    const uint8_t *cb = pr + static_cast<int64_t>(off) * cbytes;
-                    const int bit = j * bits;
-                    const uint32_t w = cb[bit >> 3] | (static_cast<uint32_t>(cb[min((bit >> 3) + 1, cbytes - 1)]) << 8);
-                    const uint32_t code = (w >> (bit & 7)) & ((1u << bits) - 1u);
-                    x = (values ? C.vcentroids[code] : C.centroids[code]) * rsd;
-                    if (qjl) {
-                        const uint8_t *sb = pr + G.k_sign_off + static_cast<int64_t>(off) * C.k_sign_bytes;
-                        sg = __float2half_rn(((sb[j >> 3] >> (j & 7)) & 1u) ? 1.f : -1.f);
+        for (int k = 0; k < RPW; ++k) {
+            const int row = warp + 8 * k;
+            const int64_t rec = s_rec[row];
+            uint32_t w0 = 0u, w1 = 0u;
+            aux[k] = 0u;
+            nrm[k] = gam[k] = 0.f;
+            if (rec >= 0) {
+                const int off = s_off[row];
+                const uint8_t *pr = values ? vc + rec * G.v_page : kc + rec * G.k_page;
+                const uint32_t *wp = reinterpret_cast<const uint32_t *>(pr + static_cast<int64_t>(off) * cbytes);
+                w0 = __ldg(wp + (bit0 >> 5));
+                w1 = __ldg(wp + (bit0 >> 5) + 1);
+                if (values && !C.vmse) {  // the lane's group: its (scale, zero) pair
+                    aux[k] = __ldg(reinterpret_cast<const uint32_t *>(pr + G.v_meta_off +
+                                                                     static_cast<int64_t>(off) * C.v_meta_bytes) +
+                                   (E * lane) / C.group);
+                } else {
+                    nrm[k] = bf16_to_float(__ldg(reinterpret_cast<const uint16_t *>(
+                        pr + (values ? G.v_meta_off : G.k_norm_off) + 2 * off)));
+                    if (!values && C.qjl) {
+                        aux[k] = __ldg(pr + G.k_sign_off + static_cast<int64_t>(off) * C.k_sign_bytes + (E * lane >> 3));
+                        gam[k] = bf16_to_float(__ldg(reinterpret_cast<const uint16_t *>(pr + G.k_gamma_off + 2 * off)));
                     }
                 }
-                u[row * D + j] = x;
-                if (qjl) ah[row * KA + j] = sg;
+            }
+            cw[k] = __funnelshift_r(w0, w1, bit0 & 31);
+        }
+    };
+
+    // u = c[code] / sqrt(d) (0 for skipped rows), with QJL the signs into ah
+    auto stage = [&](bool values) {
+        uint32_t cw[RPW], aux[RPW];
+        float nrm[RPW], gam[RPW];
+        load_codes(values, cw, aux, nrm, gam);
+        const int bits = values ? C.v_bits : C.k_bits;
+        const uint32_t mask = (1u << bits) - 1u;
+        const bool qjl = !values && C.qjl;
+        const float *cent = s_cent[values ? 1 : 0];
+#pragma unroll
+        for (int k = 0; k < RPW; ++k) {
+            const int row = warp + 8 * k;
+            const bool live = s_rec[row] >= 0;
+            float x[E];
+#pragma unroll
+            for (int m = 0; m < E; ++m) x[m] = live ? cent[(cw[k] >> (bits * m)) & mask] : 0.f;
+#pragma unroll
+            for (int m = 0; m < E; m += 4)
+                *reinterpret_cast<float4 *>(u + row * D + E * lane + m) = make_float4(x[m], x[m + 1], x[m + 2], x[m + 3]);
+            if (qjl) {
+                const uint32_t sb = aux[k] >> ((E * lane) & 7);
+                uint32_t h2[E / 2];
+#pragma unroll
+                for (int m = 0; m < E; m += 2) {
+                    // +-1 in fp16 (0x3C00 / 0xBC00) where the row is live, else 0
+                    const uint32_t lo = live ? (((sb >> m) & 1u) ? 0x3C00u : 0xBC00u) : 0u;
+                    const uint32_t hi = live ? (((sb >> (m + 1)) & 1u) ? 0x3C00u : 0xBC00u) : 0u;
+                    h2[m / 2] = lo | (hi << 16);
+                }
+                if constexpr (E == 4)
+                    *reinterpret_cast<uint2 *>(ah + row * KA + E * lane) = make_uint2(h2[0], h2[1]);
+                else
+                    *reinterpret_cast<uint4 *>(ah + row * KA + E * lane) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
             }
             if (lane == 0) {
-                float n = 0.f, g = 0.f;
-                if (pr) {
-                    n = bf16_to_float(*reinterpret_cast<const uint16_t *>(
-                        pr + (values ? G.v_meta_off : G.k_norm_off) + 2 * off));
-                    if (qjl) g = bf16_to_float(*reinterpret_cast<const uint16_t *>(pr + G.k_gamma_off + 2 * off));
-                }
-                s_n[row] = n;
-                s_g[row] = g;
+                s_n[row] = nrm[k];
+                s_g[row] = gam[k];
             }
         }
         __syncthreads();
@@ -258,25 +303,32 @@ __global__ void __launch_bounds__(256) dequant_mma_kernel(const Codec C, const P
         }
         __syncthreads();
     };
-    // out[row] = n Pi^T u in bf16, pairs of coordinates per lane
+    // out[row] = n Pi^T u in bf16: the tile is assembled in shared memory (over u,
+    // already split into ah / al) and written as whole 16-byte pieces of rows
     auto rotate_out = [&](uint16_t *out) {
         float acc[kDqRows / 16][NPW][4];
-        dq_product<D>(C.pit_frag, ah, al, acc);
+        dq_product<D, true>(C.pit_frag, ah, al, acc);
+        uint32_t *ob = reinterpret_cast<uint32_t *>(u);
 #pragma unroll
         for (int m = 0; m < kDqRows / 16; ++m)
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 const int row = 16 * m + rr + 8 * h2;
-                if (s_rec[row] < 0) continue;
                 const float f = s_sc[row] * s_n[row];
 #pragma unroll
                 for (int n = 0; n < NPW; ++n) {
                     const int col = 8 * (warp * NPW + n) + 2 * qq;
-                    const uint32_t pk = float_to_bf16_bits(acc[m][n][2 * h2] * f) |
-                                        (static_cast<uint32_t>(float_to_bf16_bits(acc[m][n][2 * h2 + 1] * f)) << 16);
-                    *reinterpret_cast<uint32_t *>(out + (r0 + row) * D + col) = pk;
+                    ob[row * OS + col / 2] = float_to_bf16_bits(acc[m][n][2 * h2] * f) |
+                                             (static_cast<uint32_t>(float_to_bf16_bits(acc[m][n][2 * h2 + 1] * f)) << 16);
                 }
             }
+        __syncthreads();
+        for (int e = tid; e < kDqRows * (D / 8); e += 256) {
+            const int row = e / (D / 8), c8 = e - row * (D / 8);
+            if (s_rec[row] < 0) continue;
+            *reinterpret_cast<uint4 *>(out + (r0 + row) * D + 8 * c8) =
+                *reinterpret_cast<const uint4 *>(ob + row * OS + 4 * c8);
+        }
         __syncthreads();
     };
 
@@ -284,7 +336,7 @@ __global__ void __launch_bounds__(256) dequant_mma_kernel(const Codec C, const P
     stage(false);
     if (C.qjl) {  // u += sqrt(pi/2) / d gamma S^T sigma
         float acc[kDqRows / 16][NPW][4];
-        dq_product<D>(C.st_frag, ah, nullptr, acc);
+        dq_product<D, false>(C.st_frag, ah, nullptr, acc);
 #pragma unroll
         for (int m = 0; m < kDqRows / 16; ++m)
 #pragma unroll
@@ -310,25 +362,28 @@ __global__ void __launch_bounds__(256) dequant_mma_kernel(const Codec C, const P
         rotate_out(vout);
         return;
     }
-    for (int row = warp; row < kDqRows; row += 8) {
-        const int64_t rec = s_rec[row];
-        if (rec < 0) continue;
-        const int off = s_off[row];
-        const uint8_t *vr = vc + rec * G.v_page;
-        const uint8_t *vb = vr + static_cast<int64_t>(off) * C.v_code_bytes;
+    // code * scale + zero per group: the lane's E values of one group, written as
+    // one 8- or 16-byte piece
+    uint32_t cw[RPW], meta[RPW];
+    float nrm[RPW], gam[RPW];
+    load_codes(true, cw, meta, nrm, gam);
+    const uint32_t vmask = (1u << C.v_bits) - 1u;
 #pragma unroll
-        for (int m = 0; m < E; ++m) {
-            const int j = lane + 32 * m;
-            const int vbit = j * C.v_bits;
-            const uint32_t vw =
-                vb[vbit >> 3] | (static_cast<uint32_t>(vb[min((vbit >> 3) + 1, C.v_code_bytes - 1)]) << 8);
-            const uint32_t vcode = (vw >> (vbit & 7)) & ((1u << C.v_bits) - 1u);
-            const __half2 sz = *reinterpret_cast<const __half2 *>(vr + G.v_meta_off +
-                                                                 static_cast<int64_t>(off) * C.v_meta_bytes +
-                                                                 4 * (j / C.group));
-            const float2 f = __half22float2(sz);
-            vout[(r0 + row) * D + j] = float_to_bf16_bits(fmaf(static_cast<float>(vcode), f.x, f.y));
+    for (int k = 0; k < RPW; ++k) {
+        const int row = warp + 8 * k;
+        if (s_rec[row] < 0) continue;
+        const float2 sz = __half22float2(*reinterpret_cast<const __half2 *>(&meta[k]));
+        uint32_t o[E / 2];
+#pragma unroll
+        for (int m = 0; m < E; m += 2) {
+            const float a = fmaf(static_cast<float>((cw[k] >> (C.v_bits * m)) & vmask), sz.x, sz.y);
+            const float b = fmaf(static_cast<float>((cw[k] >> (C.v_bits * (m + 1))) & vmask), sz.x, sz.y);
+            o[m / 2] = float_to_bf16_bits(a) | (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
         }
+        if constexpr (E == 4)
+            *reinterpret_cast<uint2 *>(vout + (r0 + row) * D + E * lane) = make_uint2(o[0], o[1]);
+        else
+            *reinterpret_cast<uint4 *>(vout + (r0 + row) * D + E * lane) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
