@@ -267,7 +267,7 @@ def test_decode_round_remainders(P):
         check_decode(_decode_gpu(codec, w, b, kc, vc, splits=s), ref)
 
 
-@pytest.mark.parametrize("name", ["mixed_k3v2_small", "mixed_k4v4_small"])
+@pytest.mark.parametrize("name", ["mixed_k3v2_small", "mixed_k4v4_small", "wide_head_small"])
 def test_strided_token_rows(name):
     """K and V whose token stride exceeds heads x head_dim (views into wider
     buffers, as in fused QKV projections) give the same records as contiguous ones."""
