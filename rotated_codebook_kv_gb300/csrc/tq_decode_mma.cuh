@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
     const int rot0 = (8 * quad + 29) & 31, rot1 = (8 * quad + 1) & 31;
     const uint32_t lut_lane = 8u * (lane & (SM::kLutCopies - 1));  // 3- and 4-bit codes: this lane's table copy
     const uint32_t slut_off = static_cast<uint32_t>(SM::kLut);
+    const int mt_mask = (C.group >> 4) - 1;     // m-tiles per value group - 1
     // value codes of coordinates 16 mt + 2 row (+1): byte (2-bit) or nibble pair (4-bit) of the row
     const uint32_t vsel = (VB == 2) ? (static_cast<uint32_t>(row >> 1) | (static_cast<uint32_t>(4 + (row >> 1)) << 8))
                                     : (static_cast<uint32_t>(row & 3) | (static_cast<uint32_t>(4 + (row & 3)) << 8));
@@ -567,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 2) decode_mma_kernel(
             const uint32_t vlut_lane = vlut_off + 4u * (lane & 7);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                if constexpr (!VM) {  // the m-tile's value group (reloaded per m-tile: no branch in the loop)
+                if (!VM && (mt & mt_mask) == 0) {  // a new value group: scale the B operands
                     const int g4 = 4 * ((16 * mt) >> gshift);
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
